@@ -1,0 +1,265 @@
+/*
+ * nvfp4moe.h -- C ABI of the NVFP4 W4A4 + RAC MoE hot path for sm_103a (GB300).
+ *
+ * "QUADS" is the paper "QUADS: Stabilizing NVFP4 Reinforcement Learning for
+ * MoE via QUantization-error Alignment across Dual Sides".  Each entry point
+ * cites the passage that defines what it computes.
+ *
+ * Conventions (all entry points):
+ *  - Every function returns an nvfp4_status.  Argument errors are detected on
+ *    the host before anything is launched; nothing is launched when a call
+ *    returns an error.  Errors found on the device (a non-finite amax, a
+ *    bounded wait that ran out) are written to the optional `dev_status`
+ *    word (device int32, first error wins, 0 = OK) which the caller reads
+ *    whenever it likes.  No exception crosses the ABI.
+ *  - The caller owns all memory.  Pointers marked "device" are CUDA device
+ *    pointers; the library allocates nothing and frees nothing.
+ *  - Every call is asynchronous and stream-ordered on `stream` (a
+ *    cudaStream_t passed as void*; NULL = legacy default stream) and never
+ *    synchronizes.  Outputs are valid once the stream reaches them.
+ *  - BF16 is passed as `void*` holding IEEE bfloat16 bit patterns.
+ *  - Device pointers must be 16-byte aligned (NVFP4_ERR_ALIGNMENT otherwise).
+ *  - There is no CPU path: without an sm_103 device every call returns
+ *    NVFP4_ERR_ARCH.
+ *
+ * NVFP4 tensor format produced by nvfp4_quantize (QUADS §2.2 "FP4."):
+ *  - codes  [rows, K/2] uint8: E2M1 codes, two per byte, element 2i in the
+ *           low nibble, element 2i+1 in the high nibble.
+ *  - scales swizzled E4M3 block scales, one per 16 consecutive elements along
+ *           K, grouped in 512-byte tiles of 128 rows x 4 blocks: tile
+ *           (m/128, kb/4) starts at byte ((m/128)*(K/64) + kb/4)*512 (with
+ *           K/64 rounded up) and holds row m, block kb at byte
+ *           (m%32)*16 + ((m%128)/32)*4 + kb%4.  Size:
+ *           ceil(rows/128)*128 * ceil(K/64)*4 bytes; unused bytes are 0.
+ *           This is the layout the block-scaled tensor-core MMA reads.
+ *  - gs     FP32 per-tensor scale, gs = amax/2688 (amax = max|x| over the
+ *           tensor; 2688 = 6*448), gs = 1 for an all-zero tensor.
+ *  - value  of element (m, j) = e2m1(code) * e4m3(scale) * gs.
+ */
+#ifndef NVFP4MOE_H
+#define NVFP4MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1, /* a null pointer, a negative size, a bad enum  */
+    NVFP4_ERR_UNSUPPORTED = 2, /* a shape outside the kernels' rules           */
+    NVFP4_ERR_ALIGNMENT = 3,   /* a pointer or stride not 16-byte aligned      */
+    NVFP4_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed         */
+    NVFP4_ERR_TIMEOUT = 5,     /* a bounded device wait ran out (dev_status)   */
+    NVFP4_ERR_NONFINITE = 6,   /* a tensor amax was Inf/NaN (dev_status)       */
+    NVFP4_ERR_ARCH = 7         /* no sm_103 device current                     */
+} nvfp4_status;
+
+/* Output element type of the GEMMs. */
+enum { NVFP4_OUT_F32 = 0, NVFP4_OUT_BF16 = 1 };
+/* Epilogue of the W4A4 + RAC GEMM. */
+enum { NVFP4_EPI_NONE = 0, NVFP4_EPI_SWIGLU = 1 };
+
+/* Name of a status code ("NVFP4_OK", ...); never NULL. */
+const char *nvfp4_status_str(int status);
+
+/* Checks that the current CUDA device is an sm_103 part and loads the driver
+ * entry point used to build TMA descriptors.  Called implicitly by every
+ * entry point; returns NVFP4_ERR_ARCH on any other device. */
+int nvfp4_init(void);
+
+/* Text of the last CUDA error seen by the library in this thread ("" if none). */
+const char *nvfp4_last_error(void);
+
+/* ------------------------------------------------------------------------ */
+/* Quantization (QUADS §2.2 "FP4."; §3.1 Eq. 9; §3.3 Eq. 20-21)              */
+/* ------------------------------------------------------------------------ */
+
+/* Per-tensor amax = max |x| for `ntensors` BF16 matrices of M x K (row
+ * stride ldx elements) laid out `tensor_stride` elements apart.
+ *   x          device, BF16
+ *   amax_out   device float[ntensors]; overwritten (it is cleared first).
+ * NaN/Inf inputs propagate to amax_out as a non-finite value.
+ * Errors: INVALID_ARG (null, negative sizes, ldx < K), ALIGNMENT (x not 16-byte
+ * aligned or ldx % 8 != 0), UNSUPPORTED (K % 8 != 0). */
+int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensors,
+               int64_t tensor_stride, float *amax_out, void *stream);
+
+/* NVFP4 quantize of a BF16 activation matrix x [M, K] (row stride ldx) with
+ * the RAC residual of QUADS §3.3 Eq. 20-21 on a fixed channel set S.
+ *   amax        device float: the tensor's amax (from nvfp4_amax, or any
+ *               caller value); gs = amax/2688 (1 if amax == 0).
+ *   gs_out      device float or NULL: receives gs.
+ *   S, k        device int32[k], strictly increasing channel indices < K,
+ *               0 <= k <= K, k % 8 == 0 (k = 0: no residual; S may be NULL).
+ *   dst_row     device int32[M*fanout] or NULL.  NULL: row m is written to
+ *               output row m (fanout must be 1).  Otherwise row m is written
+ *               to every output row dst_row[m*fanout + f], f < fanout (the MoE
+ *               dispatch: each token's codes go to its routed rows).
+ *   rows_out    number of output rows (>= M when dst_row is NULL).
+ *   codes       device uint8 [rows_out, K/2]
+ *   scales      device uint8, swizzled layout for rows_out rows (see top)
+ *   resid       device BF16 [rows_out, k]: r = bf16(x - dequant(q(x))) on S,
+ *               i.e. minus the quantization error Delta X_q of Eq. 20.
+ * Per element: block scale sb = e4m3_rn_sat(amax16 / (6*gs)); den = sb*gs;
+ * code = e2m1_rn_sat(x * (1/den)) with 1/den correctly rounded (a zero den
+ * gives a signed zero code); dequant = (code*sb)*gs in binary32.
+ * Output rows not named by dst_row are left untouched (see
+ * nvfp4_moe_clear_padding).  dev_status gets NONFINITE if amax is not finite.
+ * Errors: INVALID_ARG, ALIGNMENT (pointers; ldx % 8), UNSUPPORTED (K % 32,
+ * k % 8, fanout < 1). */
+int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float *amax,
+                   float *gs_out, const int32_t *S, int32_t k, const int32_t *dst_row,
+                   int32_t fanout, int64_t rows_out, uint8_t *codes, uint8_t *scales,
+                   void *resid, int32_t *dev_status, void *stream);
+
+/* Trainer-side weight fake-quantization QDQ_W of QUADS §3.2 Eq. 12:
+ * w_hat = bf16((code*sb)*gs) for `ntensors` BF16 weights of rows x cols,
+ * each with its own gs (one per tensor), the same block layout and rounding
+ * as nvfp4_quantize, so that the learner sees exactly the weights rollout
+ * dequantizes (Eq. 15-16).
+ *   w, w_hat    device BF16 [ntensors, rows, cols] (may not alias)
+ *   gs_out      device float[ntensors] or NULL
+ *   amax_ws     device float[ntensors], caller-provided scratch (the amax).
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (cols % 32). */
+int nvfp4_fake_quant(const void *w, int32_t ntensors, int64_t rows, int64_t cols, void *w_hat,
+                     float *gs_out, float *amax_ws, int32_t *dev_status, void *stream);
+
+/* Rollout weight preparation, once per weight update (QUADS §3.2 Eq. 15: the
+ * rollout loads the trainer's weights): per expert e of w [E, N, K] BF16,
+ * NVFP4-quantize with the expert's own gs and gather the dequantized,
+ * unscaled weight on the RAC channels:
+ *   w_codes     device uint8 [E, N, K/2]
+ *   w_scales    device uint8 [E][swizzled N x K] (E * N * K/16 bytes)
+ *   gs_w        device float[E]
+ *   w_sel       device BF16 [E, N, k]: w_sel[e,n,s] = code*sb of W[e,n,S[s]]
+ *               (exact in BF16; the GEMM multiplies by gs_w[e])
+ *   amax_ws     device float[E] scratch.
+ *   interleave  1: store rows in gate/up tile order for the fused SwiGLU
+ *               epilogue: packed row 128t+i is source row 64t+i (i < 64, a
+ *               gate row) or N/2 + 64t + i-64 (i >= 64, an up row).  Needs
+ *               N % 128 == 0.  0: rows in source order.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, k % 8). */
+int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_t K, const int32_t *S,
+                          int32_t k, int32_t interleave, uint8_t *w_codes, uint8_t *w_scales,
+                          float *gs_w, void *w_sel, float *amax_ws, int32_t *dev_status,
+                          void *stream);
+
+/* Channel calibration, QUADS §3.3 Eq. 23-24 on a calibration batch x [M, K]
+ * (BF16): score_j = ||Q_A(X)[:,j] - X[:,j]||_2 (summed in binary64, rows in
+ * order), S = the k channels of largest score (ties to the lower index),
+ * written in increasing order.  The build fixes S per projection site from
+ * a calibration batch rather than online per forward pass.
+ *   amax        device float: the batch's amax (nvfp4_amax)
+ *   S_out       device int32[k]
+ *   score_ws    device double[K] scratch; holds the squared scores after.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 16, K > 16384, k > K). */
+int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, const float *amax, int32_t k,
+                              int32_t *S_out, double *score_ws, void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Grouped GEMMs (QUADS §3.3 Eq. 21; §3.2 Eq. 12)                            */
+/* ------------------------------------------------------------------------ */
+
+/* W4A4 + RAC grouped GEMM on the FP4 tensor cores (tcgen05 block-scaled MMA
+ * with E4M3 block scales, FP32 accumulation in tensor memory) plus the rank-k
+ * BF16 correction of Residual Activation Compensation, QUADS §3.3 Eq. 21:
+ *   y[r, n] = gs_a*gs_w[e] * sum_K (ca*sa)(cw*sw)  +  gs_w[e] * sum_{s<k} r[r,s]*w_sel[e,n,s]
+ * for every routed row r in expert e's segment [offsets[e], offsets[e+1]).
+ *   a_codes/a_scales  device, the routed activations from nvfp4_quantize,
+ *                     rows_cap rows; a_resid device BF16 [rows_cap, k]
+ *   gs_a              device float (nvfp4_quantize's gs_out)
+ *   w_codes/w_scales/gs_w/w_sel  from nvfp4_prepare_weights (E experts, N x K)
+ *   offsets           device int32[E+1], non-decreasing multiples of 128,
+ *                     offsets[0] = 0, offsets[E] <= rows_cap
+ *   epilogue          NVFP4_EPI_NONE: y [rows_cap, N] (ldy >= N).
+ *                     NVFP4_EPI_SWIGLU: the weights were prepared with
+ *                     interleave = 1; y = bf16(silu(gate) * up) [rows_cap, N/2]
+ *                     (ldy >= N/2, out_dtype must be BF16).
+ *   out_dtype         NVFP4_OUT_F32 or NVFP4_OUT_BF16 (= bf16_rn of the F32 value)
+ *   amax_out          device float or NULL: receives max|y| of the stored
+ *                     values (the next quantize's amax); the call clears it
+ *                     on `stream` before the kernel runs.
+ * Rows of a segment beyond the expert's real token count must hold zero
+ * codes/scales/residual (nvfp4_moe_clear_padding); their outputs are zero.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 256, N % 128, k % 16,
+ * k > 256, E > 1024); dev_status gets TIMEOUT if a pipeline wait runs out. */
+int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
+                                const void *a_resid, const float *gs_a, const uint8_t *w_codes,
+                                const uint8_t *w_scales, const float *gs_w, const void *w_sel,
+                                int32_t k, const int32_t *offsets, int32_t E, int64_t rows_cap,
+                                int64_t N, int64_t K, int32_t epilogue, int32_t out_dtype,
+                                void *y, int64_t ldy, float *amax_out, int32_t *dev_status,
+                                void *stream);
+
+/* BF16 grouped GEMM of the asymmetric-QAT forward, QUADS §3.2 Eq. 12:
+ * y[r, n] = sum_K x[r, K] * w_hat[e, n, K] (tcgen05 BF16 MMA, FP32 accumulate)
+ * for routed rows r of expert e.
+ *   x        device BF16 [rows_cap, K] (routed rows, see nvfp4_moe_scatter_rows)
+ *   w_hat    device BF16 [E, N, K] (nvfp4_fake_quant output, rows in source
+ *            order: for SwiGLU, gate rows [0, N/2) then up rows [N/2, N))
+ *   offsets  as for nvfp4_w4a4_rac_grouped_gemm
+ *   epilogue NVFP4_EPI_NONE: y [rows_cap, N]; NVFP4_EPI_SWIGLU: y =
+ *            bf16(silu(gate) * up) [rows_cap, N/2] (out_dtype must be BF16).
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, E > 1024). */
+int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const int32_t *offsets, int32_t E,
+                            int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype,
+                            int32_t epilogue, void *y, int64_t ldy, int32_t *dev_status,
+                            void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* MoE routing, dispatch and combine (not described by QUADS; the plainest    */
+/* top-k softmax MoE)                                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Top-k softmax router.  For each token t: p = softmax(logits[t]) in FP32;
+ * ids[t] = the topk experts of largest logit (ties to the lower expert
+ * index, in decreasing order), weights[t] = their p (no renormalization).
+ * Routed rows are ordered by (expert, token); each expert segment starts at
+ * a multiple of 128:
+ *   counts   device int32[E]      tokens routed to each expert
+ *   offsets  device int32[E+1]    padded segment starts (offsets[E] = total)
+ *   dst_row  device int32[T*topk] routed row of (t, slot)
+ * All outputs are overwritten.  Needs topk <= 32 and topk <= E <= 1024. */
+int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32_t topk, int32_t *ids,
+                     float *weights, int32_t *counts, int32_t *offsets, int32_t *dst_row,
+                     void *stream);
+
+/* Zero the padding rows [offsets[e]+counts[e], offsets[e+1]) of a routed
+ * NVFP4 activation (codes [rows_cap, K/2], swizzled scales, resid [rows_cap,
+ * k] BF16 or NULL when k = 0), so that padded rows contribute zeros. */
+int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *offsets, int32_t E,
+                            int64_t rows_cap, int64_t K, int32_t k, uint8_t *codes,
+                            uint8_t *scales, void *resid, void *stream);
+
+/* Copy BF16 token rows x [T, K] to their routed rows y [rows_cap, K]
+ * (y[dst_row[t*topk+s]] = x[t]) and zero the padding rows (the QAT path's
+ * dispatch).  counts/offsets/dst_row from nvfp4_route_topk. */
+int nvfp4_moe_scatter_rows(const void *x, int32_t T, int64_t K, int32_t topk,
+                           const int32_t *dst_row, const int32_t *counts, const int32_t *offsets,
+                           int32_t E, int64_t rows_cap, void *y, void *stream);
+
+/* Weighted combine: out[t, :] = sum_{s<topk} weights[t,s] * y[dst_row[t,s], :]
+ * in FP32, slots in order.  y is F32 or BF16 (y_dtype) with row stride ldy.
+ *   out  device float [T, H] (overwritten). */
+int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t *dst_row,
+                      const float *weights, int32_t T, int32_t topk, int64_t H, float *out,
+                      void *stream);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Runs one CTA that waits, with the library's bounded-wait routine and a
+ * limit of `limit_us` microseconds (1 .. 10^7), on a pipeline barrier that
+ * nothing ever signals; when the limit runs out it writes NVFP4_ERR_TIMEOUT
+ * to dev_status and returns normally.  Exercises the timeout path without a
+ * real fault.  The GEMM pipelines use the same routine with a 2 s limit. */
+int nvfp4_selftest_wait_timeout(int32_t limit_us, int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4MOE_H */

@@ -1,0 +1,201 @@
+"""Python binding of libnvfp4moe, the NVFP4 W4A4 + RAC MoE hot path for GB300.
+
+Argument marshalling only: each function here has the name of a C entry point
+of ``include/nvfp4moe.h``, takes torch tensors, passes their device pointers,
+sizes and the current CUDA stream to that entry point, and raises
+``NVFP4Error`` when it returns a non-zero status.  Every step of the path runs
+in the library's CUDA kernels; there is no CPU path, and importing the
+functions without the built library fails loudly.
+
+"QUADS" is the paper "QUADS: Stabilizing NVFP4 Reinforcement Learning for MoE
+via QUantization-error Alignment across Dual Sides"; the header cites, per
+entry point, the section or equation it implements.
+"""
+import ctypes
+import os
+
+import torch
+
+from .build import LIB, build_library
+
+NVFP4_OUT_F32, NVFP4_OUT_BF16 = 0, 1
+NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU = 0, 1
+STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED",
+          3: "NVFP4_ERR_ALIGNMENT", 4: "NVFP4_ERR_CUDA", 5: "NVFP4_ERR_TIMEOUT",
+          6: "NVFP4_ERR_NONFINITE", 7: "NVFP4_ERR_ARCH"}
+
+# entry point -> argument types (p = pointer, q = int64, i = int32)
+_SIGS = {
+    "nvfp4_init": "",
+    "nvfp4_amax": "pqqqiqpp",
+    "nvfp4_quantize": "pqqqpppipiqppppp",
+    "nvfp4_fake_quant": "piqqppppp",
+    "nvfp4_prepare_weights": "piqqpiippppppp",
+    "nvfp4_rac_select_channels": "pqqpippp",
+    "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
+    "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
+    "nvfp4_route_topk": "piiipppppp",
+    "nvfp4_moe_clear_padding": "ppiqqipppp",
+    "nvfp4_moe_scatter_rows": "piqipppiqpp",
+    "nvfp4_moe_combine": "piqppiiqpp",
+    "nvfp4_selftest_wait_timeout": "ipp",
+}
+_CT = {"p": ctypes.c_void_p, "q": ctypes.c_int64, "i": ctypes.c_int32}
+
+
+class NVFP4Error(RuntimeError):
+    def __init__(self, fn, status, detail=""):
+        self.status = status
+        super().__init__("%s -> %s%s" % (fn, STATUS.get(status, status), (": " + detail) if detail else ""))
+
+
+_lib = None
+
+
+def library_path():
+    return LIB
+
+
+def load(build: bool = False):
+    """Load libnvfp4moe.so (compiling it first if `build`); raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build:
+        build_library()
+    if not os.path.exists(LIB):
+        raise RuntimeError("libnvfp4moe.so is not built (%s); run __graft_entry__.build() "
+                           "or python -m nvfp4_precision_moe_gb300.build" % LIB)
+    L = ctypes.CDLL(LIB)
+    for name, sig in _SIGS.items():
+        fn = getattr(L, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [_CT[c] for c in sig]
+    L.nvfp4_status_str.restype = ctypes.c_char_p
+    L.nvfp4_status_str.argtypes = [ctypes.c_int]
+    L.nvfp4_last_error.restype = ctypes.c_char_p
+    L.nvfp4_last_error.argtypes = []
+    _lib = L
+    return L
+
+
+def _p(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    assert t.is_cuda, "device tensor expected"
+    return t.data_ptr()
+
+
+def _s(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _call(name, *args):
+    L = load()
+    st = getattr(L, name)(*args)
+    if st != 0:
+        raise NVFP4Error(name, st, L.nvfp4_last_error().decode())
+
+
+def nvfp4_init():
+    _call("nvfp4_init")
+
+
+def nvfp4_amax(x, amax_out, ntensors=1, stream=None):
+    """A1: amax_out[t] = max|x[t]| for x [ntensors*M, K] (or [ntensors, M, K]) BF16."""
+    K = x.shape[-1]
+    M = x.numel() // (K * ntensors)
+    _call("nvfp4_amax", _p(x), M, K, K, ntensors, M * K, _p(amax_out), _s(stream))
+
+
+def nvfp4_quantize(x, amax, codes, scales, resid=None, S=None, gs_out=None, dst_row=None,
+                   fanout=1, rows_out=None, dev_status=None, stream=None):
+    """A1-A5, A9: NVFP4 codes, swizzled scales and the RAC residual of x [M, K]."""
+    M, K = x.shape
+    k = 0 if S is None else S.numel()
+    if rows_out is None:
+        rows_out = codes.shape[0]
+    _call("nvfp4_quantize", _p(x), M, K, x.stride(0), _p(amax), _p(gs_out), _p(S), k,
+          _p(dst_row), fanout, rows_out, _p(codes), _p(scales), _p(resid), _p(dev_status),
+          _s(stream))
+
+
+def nvfp4_fake_quant(w, w_hat, amax_ws, gs_out=None, dev_status=None, stream=None):
+    """A16: QDQ_W of each w[t] (w: [ntensors, rows, cols] BF16)."""
+    nt, rows, cols = w.shape
+    _call("nvfp4_fake_quant", _p(w), nt, rows, cols, _p(w_hat), _p(gs_out), _p(amax_ws),
+          _p(dev_status), _s(stream))
+
+
+def nvfp4_prepare_weights(w, w_codes, w_scales, gs_w, amax_ws, S=None, w_sel=None, interleave=0,
+                          dev_status=None, stream=None):
+    """A7: rollout weight pack of w [E, N, K] BF16."""
+    E, N, K = w.shape
+    k = 0 if S is None else S.numel()
+    _call("nvfp4_prepare_weights", _p(w), E, N, K, _p(S), k, interleave, _p(w_codes),
+          _p(w_scales), _p(gs_w), _p(w_sel), _p(amax_ws), _p(dev_status), _s(stream))
+
+
+def nvfp4_rac_select_channels(x, amax, k, S_out, score_ws, stream=None):
+    """A6: channel calibration (Eq. 23-24) on a calibration batch x [M, K]."""
+    M, K = x.shape
+    _call("nvfp4_rac_select_channels", _p(x), M, K, _p(amax), k, _p(S_out), _p(score_ws),
+          _s(stream))
+
+
+def nvfp4_w4a4_rac_grouped_gemm(a_codes, a_scales, a_resid, gs_a, w_codes, w_scales, gs_w, w_sel,
+                                k, offsets, E, N, K, y, epilogue=NVFP4_EPI_NONE,
+                                out_dtype=NVFP4_OUT_F32, amax_out=None, dev_status=None,
+                                stream=None):
+    """A10-A13: y = gs_a*gs_w*(A.W^T) + gs_w*(r.W_sel^T) per expert segment."""
+    rows_cap = a_codes.shape[0]
+    _call("nvfp4_w4a4_rac_grouped_gemm", _p(a_codes), _p(a_scales), _p(a_resid), _p(gs_a),
+          _p(w_codes), _p(w_scales), _p(gs_w), _p(w_sel), k, _p(offsets), E, rows_cap, N, K,
+          epilogue, out_dtype, _p(y), y.stride(0), _p(amax_out), _p(dev_status), _s(stream))
+
+
+def nvfp4_bf16_grouped_gemm(x, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F32,
+                            epilogue=NVFP4_EPI_NONE, dev_status=None, stream=None):
+    """A17: y = x . w_hat[e]^T per expert segment (BF16 in, FP32 accumulate)."""
+    rows_cap = x.shape[0]
+    _call("nvfp4_bf16_grouped_gemm", _p(x), _p(w_hat), _p(offsets), E, rows_cap, N, K, out_dtype,
+          epilogue, _p(y), y.stride(0), _p(dev_status), _s(stream))
+
+
+def nvfp4_route_topk(logits, topk, ids, weights, counts, offsets, dst_row, stream=None):
+    """A8: top-k softmax routing and the padded routed-row layout."""
+    T, E = logits.shape
+    _call("nvfp4_route_topk", _p(logits), T, E, topk, _p(ids), _p(weights), _p(counts),
+          _p(offsets), _p(dst_row), _s(stream))
+
+
+def nvfp4_moe_clear_padding(counts, offsets, E, K, k, codes, scales, resid=None, stream=None):
+    """Zero the padding rows of a routed NVFP4 activation."""
+    _call("nvfp4_moe_clear_padding", _p(counts), _p(offsets), E, codes.shape[0], K, k, _p(codes),
+          _p(scales), _p(resid), _s(stream))
+
+
+def nvfp4_moe_scatter_rows(x, topk, dst_row, counts, offsets, E, y, stream=None):
+    """BF16 dispatch of token rows to routed rows (QAT path)."""
+    T, K = x.shape
+    _call("nvfp4_moe_scatter_rows", _p(x), T, K, topk, _p(dst_row), _p(counts), _p(offsets), E,
+          y.shape[0], _p(y), _s(stream))
+
+
+def nvfp4_moe_combine(y, dst_row, weights, topk, out, stream=None):
+    """A15: out[t] = sum_s weights[t,s] * y[dst_row[t,s]] (FP32)."""
+    y_dtype = NVFP4_OUT_BF16 if y.dtype == torch.bfloat16 else NVFP4_OUT_F32
+    T, H = out.shape
+    _call("nvfp4_moe_combine", _p(y), y_dtype, y.stride(0), _p(dst_row), _p(weights), T, topk, H,
+          _p(out), _s(stream))
+
+
+def nvfp4_selftest_wait_timeout(limit_us, dev_status, stream=None):
+    """Bounded-wait self test: dev_status becomes NVFP4_ERR_TIMEOUT."""
+    _call("nvfp4_selftest_wait_timeout", limit_us, _p(dev_status), _s(stream))
+
+
+from .layer import RolloutMoE, QatMoE, scale_bytes, rows_capacity  # noqa: E402

@@ -1,0 +1,512 @@
+// gemm.cu -- grouped GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// Two instantiations of one warp-specialised, persistent pipeline:
+//  * FP4=true : the W4A4 + RAC GEMM of QUADS §3.3 Eq. 21.  The main product
+//    runs as block-scaled E2M1 x E2M1 MMAs (kind::mxf4nvf4, one UE4M3 scale
+//    per 16 K-elements, scale_vec::4X) into an FP32 accumulator in tensor
+//    memory; the rank-k residual correction r_sel . W_sel^T runs as BF16 MMAs
+//    (kind::f16) into a second accumulator; the epilogue combines
+//    gs_a*gs_w*D_main + gs_w*D_res (and optionally SwiGLU).
+//  * FP4=false: the BF16 GEMM of the asymmetric-QAT forward, QUADS §3.2 Eq. 12.
+//
+// Tiles are 128 rows x 128 columns of the output; the K loop moves 128-byte
+// wide K-slices (256 FP4 or 64 BF16 elements) through a ring of shared-memory
+// stages fed by TMA (128-byte swizzle).  Warp roles per CTA (192 threads):
+//   warp 0  TMA producer (one lane)     warp 1  TMEM owner + MMA issuer (one lane)
+//   warps 2-5 epilogue: tcgen05.ld of their 32-lane quarter, scale, store.
+// Expert segments are contiguous 128-row groups of the routed rows, so the
+// tile list is (row tile, column tile) over all routed rows; each tile's
+// expert comes from a binary search of the segment offsets.
+#include "common.cuh"
+
+namespace nvfp4 {
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kTileBytes = 16384;  // 128 rows x 128 bytes
+constexpr int kSFBytes = 2048;     // 4 MMA-K chunks x 512 bytes (128 rows x 4 scales)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccMain = 0, kAccRes = 128, kSFCol0 = 256;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
+constexpr int kMaxExperts = 1024;
+
+// Instruction descriptors (M = 128, N = 128, both operands K-major).
+//  kind::mxf4nvf4: A, B = E2M1 (1) at bits 7-9 / 10-12, N>>3 at 17, scale
+//  format UE4M3 (0) at bit 23, M>>4 at 24, scale-factor ids 0.
+constexpr uint32_t kIdescNVF4 = (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) | ((kBM >> 4) << 24);
+//  kind::f16: D = F32 (1) at bits 4-5, A, B = BF16 (1).
+constexpr uint32_t kIdescBF16 = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) | ((kBM >> 4) << 24);
+
+template <bool FP4>
+struct Cfg {
+    static constexpr int kStages = FP4 ? 5 : 6;
+    static constexpr int kStageBytes = 2 * kTileBytes + (FP4 ? 2 * kSFBytes : 0);
+    static constexpr int kBarOffset = kStages * kStageBytes;
+    // barriers (2*stages + 3) x 8 bytes, tmem slot, abort flag, offsets
+    static constexpr int kOffOffset = kBarOffset + (2 * kStages + 3) * 8 + 16;
+    static constexpr int kSmemBytes = 1024 + kOffOffset + (kMaxExperts + 1) * 4;
+};
+
+struct GemmParams {
+    const uint8_t *a_scales;
+    const uint8_t *w_scales;
+    const float *gs_a;
+    const float *gs_w;
+    const int32_t *offsets;
+    int32_t rows_cap;
+    int32_t E, k;
+    int64_t N, K;
+    int32_t epilogue, out_dtype;
+    void *y;
+    int64_t ldy;
+    float *amax_out;
+    int32_t *dev_status;
+};
+
+__device__ __forceinline__ int expert_of(const int32_t *off, int E, int32_t m0) {
+    int lo = 0, hi = E - 1;  // first e with off[e+1] > m0
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (off[mid + 1] <= m0) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
+           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
+}
+
+template <bool FP4>
+__global__ void __launch_bounds__(192, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmWs,
+                        GemmParams p) {
+    using C = Cfg<FP4>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *acc_full = empty + C::kStages;
+    uint64_t *acc_empty = acc_full + 1;
+    uint64_t *drain = acc_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::kOffOffset);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = p.offsets[i];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        if (FP4 && p.k > 0) {
+            prefetch_tmap(&tmR);
+            prefetch_tmap(&tmWs);
+        }
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    // rows beyond the caller's buffers are never touched, whatever offsets hold
+    const int32_t total_rows = min(s_off[E], p.rows_cap) & ~(kBM - 1);
+    const int num_nt = (int)(p.N / kBN);
+    const int num_tiles = (total_rows / kBM) * num_nt;
+    const int nkt = FP4 ? (int)(p.K / 256) : (int)(p.K / 64);
+    const int nrt = FP4 ? (p.k + 63) / 64 : 0;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued_phase[C::kStages];
+            bool issued[C::kStages];
+            for (int s = 0; s < C::kStages; ++s) issued[s] = false;
+            bool ok = true;
+            const int64_t kgroups = p.K / 64;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int mt = tile / num_nt, nt = tile - mt * num_nt;
+                const int32_t m0 = mt * kBM;
+                const int e = expert_of(s_off, E, m0);
+                const int32_t brow = (int32_t)(e * p.N + nt * kBN);
+                const bool swiglu_rows = !FP4 && p.epilogue == NVFP4_EPI_SWIGLU;
+                const int32_t brow_lo = swiglu_rows ? (int32_t)(e * p.N + nt * 64) : brow;
+                const int32_t brow_hi = swiglu_rows ? (int32_t)(e * p.N + p.N / 2 + nt * 64) : brow + 64;
+                for (int it = 0; it < nkt + nrt; ++it) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *sa = smem + stage * C::kStageBytes;
+                    uint8_t *sb = sa + kTileBytes;
+                    if (it < nkt) {
+                        if (FP4) {
+                            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * kSFBytes);
+                            tma_load_2d(sa, &tmA, it * 128, m0, &full[stage]);
+                            tma_load_2d(sb, &tmB, it * 128, brow, &full[stage]);
+                            const uint8_t *sfa = p.a_scales + ((int64_t)mt * kgroups + it * 4) * 512;
+                            const uint8_t *sfb = p.w_scales + (int64_t)e * p.N * (p.K / 16) +
+                                                 ((int64_t)nt * kgroups + it * 4) * 512;
+                            bulk_load(sb + kTileBytes, sfa, kSFBytes, &full[stage]);
+                            bulk_load(sb + kTileBytes + kSFBytes, sfb, kSFBytes, &full[stage]);
+                        } else {
+                            // two 64-row boxes: rows [n0, n0+128), or for SwiGLU the gate
+                            // rows [64nt, 64nt+64) and the up rows N/2 + [64nt, 64nt+64)
+                            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                            tma_load_2d(sa, &tmA, it * 64, m0, &full[stage]);
+                            tma_load_2d(sb, &tmB, it * 64, brow_lo, &full[stage]);
+                            tma_load_2d(sb + kTileBytes / 2, &tmB, it * 64, brow_hi, &full[stage]);
+                        }
+                    } else {  // RAC slice: residual rows and the selected weight columns
+                        const int r = it - nkt;
+                        mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                        tma_load_2d(sa, &tmR, r * 64, m0, &full[stage]);
+                        tma_load_2d(sb, &tmWs, r * 64, brow, &full[stage]);
+                    }
+                    issued[stage] = true;
+                    issued_phase[stage] = phase;
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                report(p.dev_status, NVFP4_ERR_TIMEOUT);
+                *abort_flag = 1;
+                // let every copy already issued land before the CTA can exit
+                for (int s = 0; s < C::kStages; ++s)
+                    if (issued[s]) (void)mbar_wait_bounded(&full[s], issued_phase[s], kWaitLimitNs);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            int local = 0;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+                if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int it = 0; it < nkt + nrt; ++it) {
+                    if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+                    const uint32_t b_addr = a_addr + kTileBytes;
+                    if (it < nkt) {
+                        if (FP4) {
+                            const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * 32u;
+                            const uint32_t sfa_s = b_addr + kTileBytes, sfb_s = sfa_s + kSFBytes;
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) {
+                                tc_cp_sf(sf + 4 * c, desc_sf(sfa_s + 512 * c));
+                                tc_cp_sf(sf + 16 + 4 * c, desc_sf(sfb_s + 512 * c));
+                            }
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                tc_mma_nvf4(tmem + kAccMain, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
+                                            kIdescNVF4, sf + 4 * c, sf + 16 + 4 * c, (it | c) != 0);
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                tc_mma_bf16(tmem + kAccMain, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
+                                            kIdescBF16, (it | c) != 0);
+                        }
+                    } else {
+                        const int r = it - nkt;
+                        const int nm = min(4, (p.k - r * 64) / 16);
+                        for (int c = 0; c < nm; ++c)
+                            tc_mma_bf16(tmem + kAccRes, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
+                                        kIdescBF16, (r | c) != 0);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(acc_full);
+            }
+            if (!ok) {
+                report(p.dev_status, NVFP4_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // no MMA may still run when TMEM is released: `drain` completes
+            // once every tcgen05 op this thread issued has finished
+            tc_commit(drain);
+            (void)mbar_wait_bounded(drain, 0, kWaitLimitNs);
+        }
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+        const int row_in_tile = q * 32 + lane;
+        const float gsa = FP4 ? *p.gs_a : 1.0f;
+        float amax_local = 0.0f;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            // every lane waits; the warp goes on only if all lanes saw the phase
+            // complete, so the .sync.aligned TMEM loads below stay converged
+            const bool got = mbar_wait_bounded(acc_full, (uint32_t)local & 1u, kWaitLimitNs, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) {
+                    report(p.dev_status, NVFP4_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
+            }
+            tc_fence_after();
+            const int mt = tile / num_nt, nt = tile - mt * num_nt;
+            const int64_t row = (int64_t)mt * kBM + row_in_tile;
+            float gsw = 1.0f, gmul = 1.0f;
+            if (FP4) {
+                gsw = p.gs_w[expert_of(s_off, E, mt * kBM)];
+                gmul = __fmul_rn(gsa, gsw);
+            }
+            const bool has_res = FP4 && p.k > 0;
+            if (p.epilogue == NVFP4_EPI_SWIGLU) {
+                uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 64;
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t g[16], u[16], gr[16], ur[16];
+                    tmem_ld16(tmem + lane_base + kAccMain + 16 * j, g);
+                    tmem_ld16(tmem + lane_base + kAccMain + 64 + 16 * j, u);
+                    if (has_res) {
+                        tmem_ld16(tmem + lane_base + kAccRes + 16 * j, gr);
+                        tmem_ld16(tmem + lane_base + kAccRes + 64 + 16 * j, ur);
+                    }
+                    tmem_ld_wait();
+                    uint32_t o[8];
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        float hv[2];
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            float gv = __fmul_rn(gmul, __uint_as_float(g[i + t]));
+                            float uv = __fmul_rn(gmul, __uint_as_float(u[i + t]));
+                            if (has_res) {
+                                gv = __fadd_rn(gv, __fmul_rn(gsw, __uint_as_float(gr[i + t])));
+                                uv = __fadd_rn(uv, __fmul_rn(gsw, __uint_as_float(ur[i + t])));
+                            }
+                            float silu = gv / (1.0f + expf(-gv));
+                            hv[t] = __fmul_rn(silu, uv);
+                        }
+                        o[i / 2] = pack_bf16x2(hv[0], hv[1]);
+                        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] << 16)));
+                        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] & 0xffff0000u)));
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + 16 * j);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            } else {
+#pragma unroll 1
+                for (int j = 0; j < kBN / 16; ++j) {
+                    uint32_t d[16], dr[16];
+                    tmem_ld16(tmem + lane_base + kAccMain + 16 * j, d);
+                    if (has_res) tmem_ld16(tmem + lane_base + kAccRes + 16 * j, dr);
+                    tmem_ld_wait();
+                    float v[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x = __uint_as_float(d[i]);
+                        if (FP4) {
+                            x = __fmul_rn(gmul, x);
+                            if (has_res) x = __fadd_rn(x, __fmul_rn(gsw, __uint_as_float(dr[i])));
+                        }
+                        v[i] = x;
+                    }
+                    const int64_t col = (int64_t)nt * kBN + 16 * j;
+                    if (p.out_dtype == NVFP4_OUT_F32) {
+                        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + row * p.ldy + col);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
+                    } else {
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] << 16)));
+                            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] & 0xffff0000u)));
+                        }
+                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + col);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+        if (p.amax_out) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, o));
+            if (lane == 0) atomicMax(reinterpret_cast<unsigned int *>(p.amax_out), __float_as_uint(amax_local));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool FP4>
+static int set_smem_attr() {
+    static bool done[2] = {false, false};
+    if (!done[FP4]) {
+        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<FP4>::kSmemBytes);
+        if (e != cudaSuccess) {
+            set_last_error("cudaFuncSetAttribute(grouped_gemm_kernel)", e);
+            return NVFP4_ERR_CUDA;
+        }
+        done[FP4] = true;
+    }
+    return NVFP4_OK;
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const void *a_resid,
+                                           const float *gs_a, const uint8_t *w_codes, const uint8_t *w_scales,
+                                           const float *gs_w, const void *w_sel, int32_t k, const int32_t *offsets,
+                                           int32_t E, int64_t rows_cap, int64_t N, int64_t K, int32_t epilogue,
+                                           int32_t out_dtype, void *y, int64_t ldy, float *amax_out,
+                                           int32_t *dev_status, void *stream) {
+    if (!a_codes || !a_scales || !gs_a || !w_codes || !w_scales || !gs_w || !offsets || !y || E < 1 ||
+        rows_cap < 0 || N < 0 || K < 0 || k < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (k > 0 && (!a_resid || !w_sel)) return NVFP4_ERR_INVALID_ARG;
+    if (epilogue != NVFP4_EPI_NONE && epilogue != NVFP4_EPI_SWIGLU) return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (epilogue == NVFP4_EPI_SWIGLU && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    const int64_t ncols = epilogue == NVFP4_EPI_SWIGLU ? N / 2 : N;
+    if (ldy < ncols) return NVFP4_ERR_INVALID_ARG;
+    if (K % 256 || N % 128 || k % 16 || k > 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) ||
+        (int64_t)E * N > (1ll << 31))
+        return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) || !aligned16(w_scales) || !aligned16(y) ||
+        (a_resid && !aligned16(a_resid)) || (w_sel && !aligned16(w_sel)) || ldy % 8)
+        return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    if (amax_out) {
+        cudaError_t e = cudaMemsetAsync(amax_out, 0, sizeof(float), (cudaStream_t)stream);
+        if (e != cudaSuccess) {
+            set_last_error("cudaMemsetAsync(amax_out)", e);
+            return NVFP4_ERR_CUDA;
+        }
+    }
+    if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
+    int s = set_smem_attr<true>();
+    if (s != NVFP4_OK) return s;
+
+    CUtensorMap tA, tB, tR, tW;
+    s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a_codes, K / 2, rows_cap, K / 2, 128, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == NVFP4_OK)
+        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)w_codes, K / 2, (uint64_t)E * N, K / 2, 128, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == NVFP4_OK && k > 0) {
+        s = encode_tmap_2d(&tR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a_resid, k, rows_cap, 2 * k, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+        if (s == NVFP4_OK)
+            s = encode_tmap_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_sel, k, (uint64_t)E * N, 2 * k, 64, 128,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+        tR = tA;
+        tW = tB;
+    }
+    if (s != NVFP4_OK) return s;
+
+    GemmParams p{};
+    p.a_scales = a_scales;
+    p.w_scales = w_scales;
+    p.gs_a = gs_a;
+    p.gs_w = gs_w;
+    p.offsets = offsets;
+    p.rows_cap = (int32_t)rows_cap;
+    p.E = E;
+    p.k = k;
+    p.N = N;
+    p.K = K;
+    p.epilogue = epilogue;
+    p.out_dtype = out_dtype;
+    p.y = y;
+    p.ldy = ldy;
+    p.amax_out = amax_out;
+    p.dev_status = dev_status;
+    const int64_t max_tiles = (rows_cap / 128) * (N / 128);
+    const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
+    grouped_gemm_kernel<true><<<grid, 192, Cfg<true>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tR, tW, p);
+    return launch_status("grouped_gemm_kernel<fp4>");
+}
+
+extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const int32_t *offsets, int32_t E,
+                                       int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, int32_t epilogue,
+                                       void *y, int64_t ldy, int32_t *dev_status, void *stream) {
+    if (!x || !w_hat || !offsets || !y || E < 1 || rows_cap < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (epilogue != NVFP4_EPI_NONE && epilogue != NVFP4_EPI_SWIGLU) return NVFP4_ERR_INVALID_ARG;
+    if (epilogue == NVFP4_EPI_SWIGLU && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (ldy < (epilogue == NVFP4_EPI_SWIGLU ? N / 2 : N)) return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 || N % 128 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) || (int64_t)E * N > (1ll << 31))
+        return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(w_hat) || !aligned16(y) || ldy % 8) return NVFP4_ERR_ALIGNMENT;
+    if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    int s = set_smem_attr<false>();
+    if (s != NVFP4_OK) return s;
+    CUtensorMap tA, tB;
+    s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)x, K, rows_cap, 2 * K, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == NVFP4_OK)
+        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_hat, K, (uint64_t)E * N, 2 * K, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != NVFP4_OK) return s;
+    GemmParams p{};
+    p.epilogue = epilogue;
+    p.offsets = offsets;
+    p.rows_cap = (int32_t)rows_cap;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.out_dtype = out_dtype;
+    p.y = y;
+    p.ldy = ldy;
+    p.dev_status = dev_status;
+    const int64_t max_tiles = (rows_cap / 128) * (N / 128);
+    const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
+    grouped_gemm_kernel<false><<<grid, 192, Cfg<false>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tA, tB, p);
+    return launch_status("grouped_gemm_kernel<bf16>");
+}

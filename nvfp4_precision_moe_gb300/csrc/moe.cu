@@ -1,0 +1,192 @@
+// moe.cu -- MoE routing (top-k softmax), routed-row layout and combine.
+//
+// The paper's MoE layers (QUADS §4.1, MoE 25B-A2.8B) do not spell out the
+// router; this is the plainest top-k softmax router: FP32 softmax over the
+// experts, the k largest logits (ties to the lower expert index), their
+// probabilities as combine weights without renormalization.  Routed rows are
+// grouped by expert, tokens in order inside an expert, and every expert
+// segment starts at a multiple of 128 rows (one GEMM M-tile).
+#include "common.cuh"
+
+namespace nvfp4 {
+
+// one warp per token
+__global__ void topk_kernel(const float *logits, int32_t T, int32_t E, int32_t topk, int32_t *ids,
+                            float *weights) {
+    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float *l = logits + t * E;
+    float mx = -INFINITY;
+    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float sum = 0.0f;
+    for (int e = lane; e < E; e += 32) sum += expf(l[e] - mx);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    // bitmask of experts already taken, E <= 1024 -> 32 words, word w owned by lane w
+    uint32_t taken = 0u;
+    for (int s = 0; s < topk; ++s) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+        for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count for the shuffle
+            const int e = e0 + lane;
+            const uint32_t word = __shfl_sync(0xffffffffu, taken, e0 >> 5);
+            if (e < E && !((word >> lane) & 1u)) {
+                float v = l[e];
+                if (v > bv || (v == bv && e < be)) {
+                    bv = v;
+                    be = e;
+                }
+            }
+        }
+        // lanes with no candidate in this pass still take part in the shuffles
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (lane == (be >> 5)) taken |= 1u << (be & 31);
+        if (lane == 0) {
+            ids[t * topk + s] = be;
+            weights[t * topk + s] = expf(bv - mx) / sum;
+        }
+    }
+}
+
+// block per expert: number of routed tokens
+__global__ void count_kernel(const int32_t *ids, int64_t n, int32_t *counts) {
+    const int e = blockIdx.x;
+    int c = 0;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) c += (ids[i] == e);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+    __shared__ int red[32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int s = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+        counts[e] = s;
+    }
+}
+
+// block per expert: padded segment start, then ranks of its tokens in order
+__global__ void __launch_bounds__(1024) dst_row_kernel(const int32_t *ids, int32_t T, int32_t E, int32_t topk,
+                                                       const int32_t *counts, int32_t *offsets, int32_t *dst_row) {
+    const int e = blockIdx.x;
+    __shared__ int32_t s_base;
+    __shared__ int32_t warp_sums[32];
+    if (threadIdx.x == 0) {
+        int64_t off = 0;
+        for (int i = 0; i < e; ++i) off += (counts[i] + 127) / 128 * 128;
+        s_base = (int32_t)off;
+        offsets[e] = (int32_t)off;
+        if (e == E - 1) offsets[E] = (int32_t)(off + (counts[e] + 127) / 128 * 128);
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int64_t t0 = 0; t0 < T; t0 += blockDim.x) {
+        const int64_t t = t0 + threadIdx.x;
+        int slot = -1;
+        if (t < T)
+            for (int s = 0; s < topk; ++s)
+                if (ids[t * topk + s] == e) slot = s;
+        const int flag = slot >= 0;
+        const unsigned bal = __ballot_sync(0xffffffffu, flag);
+        if (lane == 0) warp_sums[wid] = __popc(bal);
+        __syncthreads();
+        int pre = __popc(bal & ((1u << lane) - 1u));
+        for (int w = 0; w < wid; ++w) pre += warp_sums[w];
+        if (flag) dst_row[t * topk + slot] = s_base + pre;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int tot = 0;
+            for (int w = 0; w < nw; ++w) tot += warp_sums[w];
+            s_base += tot;
+        }
+        __syncthreads();
+    }
+}
+
+// out[t, c:c+8] = sum_s w[t,s] * y[row(t,s), c:c+8] in FP32, slots in order
+template <bool BF16>
+__global__ void combine_kernel(const void *y, int64_t ldy, const int32_t *dst_row, const float *weights,
+                               int32_t T, int32_t topk, int64_t H, float *out) {
+    const int64_t per_row = H >> 3;
+    const int64_t total = (int64_t)T * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_row, c = (i - t * per_row) * 8;
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int s = 0; s < topk; ++s) {
+            const int64_t row = dst_row[t * topk + s];
+            const float w = weights[t * topk + s];
+            float v[8];
+            if (BF16) {
+                uint4 q = __ldg(reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(y) + row * ldy + c));
+                uint32_t ww[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    v[2 * j] = __uint_as_float(ww[j] << 16);
+                    v[2 * j + 1] = __uint_as_float(ww[j] & 0xffff0000u);
+                }
+            } else {
+                const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(y) + row * ldy + c);
+                float4 a = __ldg(p), b = __ldg(p + 1);
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(w, v[j]));
+        }
+        float4 *o = reinterpret_cast<float4 *>(out + t * H + c);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32_t topk, int32_t *ids, float *weights,
+                                int32_t *counts, int32_t *offsets, int32_t *dst_row, void *stream) {
+    if (!logits || !ids || !weights || !counts || !offsets || !dst_row || T < 0 || E < 1 || topk < 1)
+        return NVFP4_ERR_INVALID_ARG;
+    if (topk > 32 || topk > E || E > 1024) return NVFP4_ERR_UNSUPPORTED;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T > 0) {
+        topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, st>>>(logits, T, E, topk, ids, weights);
+        int s = launch_status("topk_kernel");
+        if (s != NVFP4_OK) return s;
+    }
+    count_kernel<<<E, 512, 0, st>>>(ids, (int64_t)T * topk, counts);
+    int s = launch_status("count_kernel");
+    if (s != NVFP4_OK) return s;
+    dst_row_kernel<<<E, 1024, 0, st>>>(ids, T, E, topk, counts, offsets, dst_row);
+    return launch_status("dst_row_kernel");
+}
+
+extern "C" int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t *dst_row,
+                                 const float *weights, int32_t T, int32_t topk, int64_t H, float *out, void *stream) {
+    if (!y || !dst_row || !weights || !out || T < 0 || topk < 1 || H < 0 || ldy < H) return NVFP4_ERR_INVALID_ARG;
+    if (y_dtype != NVFP4_OUT_F32 && y_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (H % 8 || ldy % 8) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(y) || !aligned16(out)) return NVFP4_ERR_ALIGNMENT;
+    if (T == 0 || H == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    int64_t total = (int64_t)T * (H / 8);
+    int64_t blocks = (total + 255) / 256, cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (y_dtype == NVFP4_OUT_BF16)
+        combine_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(y, ldy, dst_row, weights, T, topk, H, out);
+    else
+        combine_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(y, ldy, dst_row, weights, T, topk, H, out);
+    return launch_status("combine_kernel");
+}

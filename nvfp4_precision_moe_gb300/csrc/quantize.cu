@@ -1,0 +1,564 @@
+// quantize.cu -- NVFP4 quantization kernels (HBM-bound).
+//
+// QUADS §2.2 "FP4.": E2M1 elements, one E4M3 scale per 16 consecutive
+// elements, an FP32 per-tensor scale; §3.1 Eq. 9 / §3.3 Eq. 20-21: the
+// activation quantizer Q_A and the RAC residual on a channel set S; §3.2
+// Eq. 12: the weight fake-quantizer QDQ_W, which must round exactly like the
+// rollout quantizer (both use quant_block below).
+//
+// Work split: one warp per (row, segment of 32 blocks); each lane owns one
+// 16-element block (32 bytes of BF16 in, 8 bytes of codes out), so a warp
+// reads 1 KB contiguous and writes 256 B of codes contiguous.  Four lanes
+// pack their block scales into one 32-bit store of the swizzled layout.
+#include "common.cuh"
+
+namespace nvfp4 {
+
+constexpr int kMaxBlocksPerRow = 1024;  // K <= 16384
+
+enum QuantMode { kModeAct = 0, kModeWeight = 1, kModeFake = 2 };
+
+struct QuantArgs {
+    const uint16_t *x;
+    int64_t M, K, ldx, x_tstride;  // elements
+    const float *amax;             // [ntensors]
+    float *gs_out;                 // [ntensors] or null
+    const int32_t *S;
+    int32_t k;
+    const int32_t *dst_row;
+    int32_t fanout;
+    int64_t rows_out;
+    uint8_t *codes;
+    int64_t codes_tstride;  // bytes
+    uint8_t *scales;
+    int64_t scales_tstride;  // bytes
+    uint16_t *resid;         // act mode: [rows_out, k]
+    uint16_t *wsel;          // weight mode: [rows, k] per tensor
+    int64_t wsel_tstride;
+    uint16_t *w_hat;  // fake mode: [M, K] per tensor
+    int64_t what_tstride;
+    int32_t interleave;
+    int32_t *dev_status;
+};
+
+// Byte offset of (row m, block kb) in the swizzled scale layout, for a
+// tensor whose rows hold K/16 blocks.
+__device__ __forceinline__ int64_t swz_offset(int64_t m, int64_t kb, int64_t kgroups) {
+    return ((m >> 7) * kgroups + (kb >> 2)) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (kb & 3);
+}
+
+// One 16-element block: scale code, E2M1 codes, the block's dequant factor.
+struct BlockQ {
+    uint32_t sb;      // E4M3 code
+    float sbf;        // its value
+    uint32_t c[16];   // E2M1 codes
+};
+
+__device__ __forceinline__ void quant_block(const float (&v)[16], float gs, float p6, BlockQ &q) {
+    float amax_b = 0.0f;
+#pragma unroll
+    for (int t = 0; t < 16; ++t) amax_b = fmaxf(amax_b, fabsf(v[t]));
+    // block scale: E4M3 of amax_b / (6*gs), RNE with saturation
+    float s = __fdiv_rn(amax_b, p6);
+    q.sb = e4m3_from_f32(s);
+    q.sbf = e4m3_to_f32(q.sb);
+    float den = __fmul_rn(q.sbf, gs);
+    if (den != 0.0f) {
+        float inv = __frcp_rn(den);  // correctly rounded reciprocal
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+            uint32_t pr = e2m1x2_from_f32(__fmul_rn(v[t], inv), __fmul_rn(v[t + 1], inv));
+            q.c[t] = pr & 15u;
+            q.c[t + 1] = pr >> 4;
+        }
+    } else {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) q.c[t] = (__float_as_uint(v[t]) >> 31) << 3;  // signed zero
+    }
+}
+
+__device__ __forceinline__ void load_block(const uint16_t *src, float (&v)[16]) {
+    const uint4 *p = reinterpret_cast<const uint4 *>(src);
+    uint4 a = __ldg(p), b = __ldg(p + 1);
+    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
+    __shared__ uint32_t s_mask[kMaxBlocksPerRow];
+    __shared__ int32_t s_base[kMaxBlocksPerRow];
+    const int tensor = blockIdx.y;
+    const int64_t nb = a.K >> 4;
+    const int64_t kgroups = (nb + 3) >> 2;
+    const bool has_sel = (MODE != kModeFake) && a.k > 0;
+
+    if (has_sel) {  // which elements of each block belong to S, and S's index of the first
+        for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) s_mask[b] = 0u;
+        __syncthreads();
+        for (int s = threadIdx.x; s < a.k; s += blockDim.x) {
+            int j = a.S[s];
+            atomicOr(&s_mask[j >> 4], 1u << (j & 15));
+            if (s == 0 || (a.S[s - 1] >> 4) != (j >> 4)) s_base[j >> 4] = s;
+        }
+        __syncthreads();
+    }
+
+    const float amax_t = a.amax[tensor];
+    const float gs = tensor_scale(amax_t);
+    const float p6 = __fmul_rn(gs, 6.0f);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (a.gs_out) a.gs_out[tensor] = gs;
+        if (!isfinite(amax_t)) report(a.dev_status, NVFP4_ERR_NONFINITE);
+    }
+
+    const int lane = threadIdx.x & 31;
+    const int64_t segs = (nb + 31) >> 5;
+    const int64_t nwarps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const uint16_t *xt = a.x + (int64_t)tensor * a.x_tstride;
+
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < a.M * segs;
+         w += nwarps_total) {
+        const int64_t m = w / segs;  // output row (packed row in weight mode)
+        const int64_t b = (w - m * segs) * 32 + lane;
+        const bool valid = b < nb;
+        int64_t src_row = m;
+        if (MODE == kModeWeight && a.interleave) {
+            int64_t t = m >> 7, i = m & 127;
+            src_row = (i < 64) ? (t * 64 + i) : (a.M / 2 + t * 64 + (i - 64));
+        }
+        float v[16];
+        BlockQ q;
+        if (valid) {
+            load_block(xt + src_row * a.ldx + b * 16, v);
+            quant_block(v, gs, p6, q);
+        } else {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) v[t] = 0.0f;
+            q.sb = 0u;
+            q.sbf = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) q.c[t] = 0u;
+        }
+
+        if (MODE == kModeFake) {
+            if (valid) {
+                uint32_t o[8];
+#pragma unroll
+                for (int t = 0; t < 16; t += 2) {
+                    float d0 = __fmul_rn(__fmul_rn(e2m1_to_f32(q.c[t]), q.sbf), gs);
+                    float d1 = __fmul_rn(__fmul_rn(e2m1_to_f32(q.c[t + 1]), q.sbf), gs);
+                    o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
+                               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
+                }
+                uint4 *dst = reinterpret_cast<uint4 *>(a.w_hat + (int64_t)tensor * a.what_tstride +
+                                                       m * a.K + b * 16);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            continue;
+        }
+
+        // packed codes: element 2i in the low nibble
+        uint2 packed;
+        packed.x = q.c[0] | (q.c[1] << 4) | (q.c[2] << 8) | (q.c[3] << 12) | (q.c[4] << 16) |
+                   (q.c[5] << 20) | (q.c[6] << 24) | (q.c[7] << 28);
+        packed.y = q.c[8] | (q.c[9] << 4) | (q.c[10] << 8) | (q.c[11] << 12) | (q.c[12] << 16) |
+                   (q.c[13] << 20) | (q.c[14] << 24) | (q.c[15] << 28);
+        // four consecutive blocks' scales -> one 32-bit word (lane%4 == 0 stores)
+        uint32_t sw = q.sb;
+        uint32_t s1 = __shfl_down_sync(0xffffffffu, sw, 1);
+        uint32_t s2 = __shfl_down_sync(0xffffffffu, sw, 2);
+        uint32_t s3 = __shfl_down_sync(0xffffffffu, sw, 3);
+        sw = sw | (s1 << 8) | (s2 << 16) | (s3 << 24);
+        const bool group_lead = ((lane & 3) == 0) && (b < ((nb + 3) & ~3LL));
+
+        uint32_t mask = 0u;
+        int32_t base = 0;
+        if (has_sel && valid) {
+            mask = s_mask[b];
+            base = s_base[b];
+        }
+
+        if (MODE == kModeWeight) {
+            uint8_t *codes = a.codes + (int64_t)tensor * a.codes_tstride;
+            uint8_t *scales = a.scales + (int64_t)tensor * a.scales_tstride;
+            if (valid) *reinterpret_cast<uint2 *>(codes + m * (a.K >> 1) + b * 8) = packed;
+            if (group_lead) *reinterpret_cast<uint32_t *>(scales + swz_offset(m, b, kgroups)) = sw;
+            if (mask) {
+                uint16_t *wsel = a.wsel + (int64_t)tensor * a.wsel_tstride + m * a.k;
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    if (mask & (1u << t)) {
+                        const int s = base + __popc(mask & ((1u << t) - 1u));
+                        const float cs = __fmul_rn(e2m1_to_f32(q.c[t]), q.sbf);  // exact
+                        wsel[s] = __bfloat16_as_ushort(__float2bfloat16_rn(cs));
+                    }
+            }
+            continue;
+        }
+
+        // activation mode: codes and scales to every routed row of this row
+        for (int f = 0; f < a.fanout; ++f) {
+            const int64_t dm = a.dst_row ? (int64_t)a.dst_row[m * a.fanout + f] : m;
+            if (dm < 0 || dm >= a.rows_out) continue;  // a map entry outside the output is skipped
+            if (valid) *reinterpret_cast<uint2 *>(a.codes + dm * (a.K >> 1) + b * 8) = packed;
+            if (group_lead) *reinterpret_cast<uint32_t *>(a.scales + swz_offset(dm, b, kgroups)) = sw;
+        }
+        if (mask) {  // residual r = bf16(x - (code*sb)*gs) on the selected channels
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+                if (mask & (1u << t)) {
+                    const int s = base + __popc(mask & ((1u << t) - 1u));
+                    const float xq = __fmul_rn(__fmul_rn(e2m1_to_f32(q.c[t]), q.sbf), gs);
+                    const uint16_t r = __bfloat16_as_ushort(__float2bfloat16_rn(__fsub_rn(v[t], xq)));
+                    for (int f = 0; f < a.fanout; ++f) {
+                        const int64_t dm = a.dst_row ? (int64_t)a.dst_row[m * a.fanout + f] : m;
+                        if (dm >= 0 && dm < a.rows_out) a.resid[dm * a.k + s] = r;
+                    }
+                }
+        }
+    }
+}
+
+// max |x| per tensor: bit patterns of |bf16| compare like the values (NaN
+// sorts above Inf, so it propagates).
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                                                   int64_t tstride, float *out) {
+    const uint16_t *xt = x + (int64_t)blockIdx.y * tstride;
+    uint32_t mx = 0u;
+    const int64_t vec_per_row = K >> 3;
+    const int64_t total = M * vec_per_row;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (ldx == K) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(xt);
+        for (; i + 3 * stride < total; i += 4 * stride) {
+            uint4 v0 = __ldg(p + i), v1 = __ldg(p + i + stride), v2 = __ldg(p + i + 2 * stride),
+                  v3 = __ldg(p + i + 3 * stride);
+            uint32_t w[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
+                              v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+            for (int j = 0; j < 16; ++j) mx = __vmaxu2(mx, w[j] & 0x7fff7fffu);
+        }
+        for (; i < total; i += stride) {
+            uint4 v = __ldg(p + i);
+            mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
+            mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
+            mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
+            mx = __vmaxu2(mx, v.w & 0x7fff7fffu);
+        }
+    } else {
+        for (; i < total; i += stride) {
+            int64_t r = i / vec_per_row, c = i - r * vec_per_row;
+            uint4 v = __ldg(reinterpret_cast<const uint4 *>(xt + r * ldx) + c);
+            mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
+            mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
+            mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
+            mx = __vmaxu2(mx, v.w & 0x7fff7fffu);
+        }
+    }
+    uint32_t m16 = max(mx & 0xffffu, mx >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, o));
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m16;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t r = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = max(r, red[w]);
+        atomicMax(reinterpret_cast<unsigned int *>(out + blockIdx.y), r << 16);
+    }
+}
+
+// zero the padding rows of each expert segment of a routed NVFP4 activation
+__global__ void clear_padding_kernel(const int32_t *counts, const int32_t *offsets, int64_t rows_cap, int64_t K,
+                                     int32_t k, uint8_t *codes, uint8_t *scales, uint16_t *resid) {
+    const int e = blockIdx.y;
+    const int64_t r0 = (int64_t)offsets[e] + counts[e], r1 = offsets[e + 1];
+    const int64_t row = r0 + blockIdx.x;
+    if (row >= r1 || row >= rows_cap || row < 0) return;
+    const int64_t nb = K >> 4, kgroups = (nb + 3) >> 2;
+    uint32_t *c = reinterpret_cast<uint32_t *>(codes + row * (K >> 1));
+    for (int64_t i = threadIdx.x; i < (K >> 3); i += blockDim.x) c[i] = 0u;
+    for (int64_t g = threadIdx.x; g < kgroups; g += blockDim.x)
+        *reinterpret_cast<uint32_t *>(scales + swz_offset(row, g * 4, kgroups)) = 0u;
+    if (resid)
+        for (int64_t i = threadIdx.x; i < k; i += blockDim.x) resid[row * k + i] = 0;
+}
+
+// BF16 rows to routed order (QAT dispatch); padding rows zeroed
+__global__ void scatter_rows_kernel(const uint16_t *x, int32_t T, int64_t K, int32_t topk, const int32_t *dst_row,
+                                    int64_t rows_cap, uint16_t *y) {
+    const int64_t t = blockIdx.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + t * K);
+    for (int64_t i = threadIdx.x; i < (K >> 3); i += blockDim.x) {
+        uint4 v = __ldg(src + i);
+        for (int s = 0; s < topk; ++s) {
+            const int64_t r = dst_row[t * topk + s];
+            if (r >= 0 && r < rows_cap) reinterpret_cast<uint4 *>(y + r * K)[i] = v;
+        }
+    }
+}
+
+__global__ void zero_pad_rows_kernel(const int32_t *counts, const int32_t *offsets, int64_t rows_cap, int64_t K,
+                                     uint16_t *y) {
+    const int e = blockIdx.y;
+    const int64_t row = (int64_t)offsets[e] + counts[e] + blockIdx.x;
+    if (row >= offsets[e + 1] || row >= rows_cap || row < 0) return;
+    uint4 *d = reinterpret_cast<uint4 *>(y + row * K);
+    for (int64_t i = threadIdx.x; i < (K >> 3); i += blockDim.x) d[i] = make_uint4(0, 0, 0, 0);
+}
+
+// Eq. 23 squared scores: one thread per channel, rows in order, binary64.
+__global__ void channel_score_kernel(const uint16_t *x, int64_t M, int64_t K, const float *amax, double *ssq) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // K % 16 == 0, grid covers K
+    const bool valid = j < K;
+    const float gs = tensor_scale(amax[0]);
+    const float p6 = __fmul_rn(gs, 6.0f);
+    const double gsd = (double)gs;
+    double acc = 0.0;
+    for (int64_t i = 0; i < M; ++i) {
+        float v = valid ? __uint_as_float((uint32_t)x[i * K + j] << 16) : 0.0f;
+        float am = fabsf(v);
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+        float sbf = e4m3_to_f32(e4m3_from_f32(__fdiv_rn(am, p6)));
+        float den = __fmul_rn(sbf, gs);
+        uint32_t c;
+        if (den != 0.0f) {
+            float qv = __fmul_rn(v, __frcp_rn(den));
+            c = e2m1x2_from_f32(qv, qv) & 15u;
+        } else {
+            c = (__float_as_uint(v) >> 31) << 3;
+        }
+        double xq = __dmul_rn((double)__fmul_rn(e2m1_to_f32(c), sbf), gsd);  // exact
+        double d = __dsub_rn(xq, (double)v);
+        acc = __dadd_rn(acc, __dmul_rn(d, d));
+    }
+    if (valid) ssq[j] = acc;
+}
+
+// Eq. 24: keep the k largest (ties to the lower index), write them in order.
+// Non-negative doubles order like their bit patterns.
+__global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, int64_t K, int32_t k, int32_t *S) {
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t carry;
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const long long *bits = reinterpret_cast<const long long *>(ssq);
+    for (int64_t j0 = 0; j0 < K; j0 += blockDim.x) {
+        int64_t j = j0 + threadIdx.x;
+        int flag = 0;
+        if (j < K) {
+            long long sj = bits[j];
+            int64_t rank = 0;
+            for (int64_t i = 0; i < K && rank < k; ++i) {
+                long long si = bits[i];
+                rank += (si > sj) || (si == sj && i < j);
+            }
+            flag = rank < k;
+        }
+        // block-wide exclusive scan of flags, in channel order
+        unsigned ballot = __ballot_sync(0xffffffffu, flag);
+        int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+        int pre = __popc(ballot & ((1u << lane) - 1u));
+        if (lane == 0) warp_sums[wid] = __popc(ballot);
+        __syncthreads();
+        int wpre = 0;
+        for (int w = 0; w < wid; ++w) wpre += warp_sums[w];
+        if (flag) S[carry + wpre + pre] = (int32_t)j;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int tot = 0;
+            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += warp_sums[w];
+            carry += tot;
+        }
+        __syncthreads();
+    }
+}
+
+static int quant_grid(int64_t rows, int64_t nb) {
+    int64_t warps = rows * ((nb + 31) / 32);
+    int64_t blocks = (warps + 7) / 8;
+    int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+static int amax_launch(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t nt, int64_t tstride, float *out,
+                       cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)nt, st);
+    if (e != cudaSuccess) {
+        set_last_error("cudaMemsetAsync(amax)", e);
+        return NVFP4_ERR_CUDA;
+    }
+    if (M == 0 || K == 0) return NVFP4_OK;
+    int64_t vecs = M * (K / 8);
+    int64_t blocks = (vecs + 255) / 256;
+    int64_t cap = (int64_t)sm_count() * 8 / (nt > 8 ? 8 : (nt < 1 ? 1 : nt));
+    if (cap < 1) cap = 1;
+    if (blocks > cap) blocks = cap;
+    amax_kernel<<<dim3((unsigned)blocks, (unsigned)nt), 256, 0, st>>>((const uint16_t *)x, M, K, ldx, tstride, out);
+    return launch_status("amax_kernel");
+}
+
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensors, int64_t tensor_stride,
+                          float *amax_out, void *stream) {
+    if (!x || !amax_out || M < 0 || K < 0 || ldx < K || ntensors < 1 || tensor_stride < 0) return NVFP4_ERR_INVALID_ARG;
+    if (ntensors > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (K % 8) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || ldx % 8 || tensor_stride % 8) return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    return amax_launch(x, M, K, ldx, ntensors, tensor_stride, amax_out, (cudaStream_t)stream);
+}
+
+extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float *amax, float *gs_out,
+                              const int32_t *S, int32_t k, const int32_t *dst_row, int32_t fanout, int64_t rows_out,
+                              uint8_t *codes, uint8_t *scales, void *resid, int32_t *dev_status, void *stream) {
+    if (!x || !amax || !codes || !scales || M < 0 || K < 0 || ldx < K || k < 0 || k > K || fanout < 1)
+        return NVFP4_ERR_INVALID_ARG;
+    if (k > 0 && (!S || !resid)) return NVFP4_ERR_INVALID_ARG;
+    if (!dst_row && (fanout != 1 || rows_out < M)) return NVFP4_ERR_INVALID_ARG;
+    if (K % 32 || k % 8 || K / 16 > kMaxBlocksPerRow) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || ldx % 8 || !aligned16(codes) || !aligned16(scales) || (resid && !aligned16(resid)))
+        return NVFP4_ERR_ALIGNMENT;
+    if (M == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    QuantArgs a{};
+    a.x = (const uint16_t *)x;
+    a.M = M;
+    a.K = K;
+    a.ldx = ldx;
+    a.amax = amax;
+    a.gs_out = gs_out;
+    a.S = S;
+    a.k = k;
+    a.dst_row = dst_row;
+    a.fanout = fanout;
+    a.rows_out = rows_out;
+    a.codes = codes;
+    a.scales = scales;
+    a.resid = (uint16_t *)resid;
+    a.dev_status = dev_status;
+    quantize_kernel<kModeAct><<<quant_grid(M, K / 16), 256, 0, (cudaStream_t)stream>>>(a);
+    return launch_status("quantize_kernel");
+}
+
+extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat, float *gs_out,
+                                float *amax_ws, int32_t *dev_status, void *stream) {
+    if (!w || !w_hat || !amax_ws || nt < 1 || rows < 0 || cols < 0) return NVFP4_ERR_INVALID_ARG;
+    if (cols % 32 || cols / 16 > kMaxBlocksPerRow || nt > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(w_hat)) return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    int s = amax_launch(w, rows, cols, cols, nt, rows * cols, amax_ws, st);
+    if (s != NVFP4_OK || rows == 0) return s;
+    QuantArgs a{};
+    a.x = (const uint16_t *)w;
+    a.M = rows;
+    a.K = cols;
+    a.ldx = cols;
+    a.x_tstride = rows * cols;
+    a.amax = amax_ws;
+    a.gs_out = gs_out;
+    a.fanout = 1;
+    a.w_hat = (uint16_t *)w_hat;
+    a.what_tstride = rows * cols;
+    a.dev_status = dev_status;
+    int g = quant_grid(rows, cols / 16) / (nt > 8 ? 8 : nt);
+    quantize_kernel<kModeFake><<<dim3(g < 1 ? 1 : g, nt), 256, 0, st>>>(a);
+    return launch_status("quantize_kernel<fake>");
+}
+
+extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_t K, const int32_t *S, int32_t k,
+                                     int32_t interleave, uint8_t *w_codes, uint8_t *w_scales, float *gs_w,
+                                     void *w_sel, float *amax_ws, int32_t *dev_status, void *stream) {
+    if (!w || !w_codes || !w_scales || !gs_w || !amax_ws || E < 1 || N < 0 || K < 0 || k < 0 || k > K)
+        return NVFP4_ERR_INVALID_ARG;
+    if (k > 0 && (!S || !w_sel)) return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 || N % 128 || k % 8 || K / 16 > kMaxBlocksPerRow || E > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(w_codes) || !aligned16(w_scales) || (w_sel && !aligned16(w_sel)))
+        return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    int s = amax_launch(w, N, K, K, E, N * K, amax_ws, st);
+    if (s != NVFP4_OK || N == 0) return s;
+    QuantArgs a{};
+    a.x = (const uint16_t *)w;
+    a.M = N;
+    a.K = K;
+    a.ldx = K;
+    a.x_tstride = N * K;
+    a.amax = amax_ws;
+    a.gs_out = gs_w;
+    a.S = S;
+    a.k = k;
+    a.fanout = 1;
+    a.codes = w_codes;
+    a.codes_tstride = N * K / 2;
+    a.scales = w_scales;
+    a.scales_tstride = N * K / 16;
+    a.wsel = (uint16_t *)w_sel;
+    a.wsel_tstride = N * (int64_t)k;
+    a.interleave = interleave;
+    a.dev_status = dev_status;
+    int g = quant_grid(N, K / 16) / (E > 8 ? 8 : E);
+    quantize_kernel<kModeWeight><<<dim3(g < 1 ? 1 : g, E), 256, 0, st>>>(a);
+    return launch_status("quantize_kernel<weight>");
+}
+
+extern "C" int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,
+                                       int64_t K, int32_t k, uint8_t *codes, uint8_t *scales, void *resid,
+                                       void *stream) {
+    if (!counts || !offsets || !codes || !scales || E < 1 || K < 0 || k < 0 || rows_cap < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (k > 0 && !resid) return NVFP4_ERR_INVALID_ARG;
+    if (K % 32 || E > 65535) return NVFP4_ERR_UNSUPPORTED;
+    NVFP4_CHECK_INIT();
+    clear_padding_kernel<<<dim3(127, E), 128, 0, (cudaStream_t)stream>>>(counts, offsets, rows_cap, K, k, codes,
+                                                                         scales, (uint16_t *)resid);
+    return launch_status("clear_padding_kernel");
+}
+
+extern "C" int nvfp4_moe_scatter_rows(const void *x, int32_t T, int64_t K, int32_t topk, const int32_t *dst_row,
+                                      const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,
+                                      void *y, void *stream) {
+    if (!x || !dst_row || !counts || !offsets || !y || T < 0 || K < 0 || topk < 1 || E < 1 || rows_cap < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 8 || E > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(y)) return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    if (T > 0) {
+        scatter_rows_kernel<<<T, 256, 0, st>>>((const uint16_t *)x, T, K, topk, dst_row, rows_cap, (uint16_t *)y);
+        int s = launch_status("scatter_rows_kernel");
+        if (s != NVFP4_OK) return s;
+    }
+    zero_pad_rows_kernel<<<dim3(127, E), 256, 0, st>>>(counts, offsets, rows_cap, K, (uint16_t *)y);
+    return launch_status("zero_pad_rows_kernel");
+}
+
+extern "C" int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, const float *amax, int32_t k,
+                                         int32_t *S_out, double *score_ws, void *stream) {
+    if (!x || !amax || !score_ws || M < 0 || K < 0 || k < 0) return NVFP4_ERR_INVALID_ARG;
+    if (k > 0 && !S_out) return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 || K > 16384 || k > K) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(score_ws)) return NVFP4_ERR_ALIGNMENT;
+    if (K == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    channel_score_kernel<<<(unsigned)((K + 255) / 256), 256, 0, st>>>((const uint16_t *)x, M, K, amax, score_ws);
+    int s = launch_status("channel_score_kernel");
+    if (s != NVFP4_OK || k == 0) return s;
+    select_topk_kernel<<<1, 1024, 0, st>>>(score_ws, K, k, S_out);
+    return launch_status("select_topk_kernel");
+}

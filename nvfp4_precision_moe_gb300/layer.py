@@ -1,0 +1,178 @@
+"""MoE layers built from the C-ABI calls: the rollout W4A4 + RAC forward and
+the trainer's asymmetric-QAT forward.
+
+These classes only allocate device buffers (torch) and call the library's
+entry points in order; all arithmetic runs in the CUDA kernels.
+
+Rollout forward (QUADS §3.3, Eq. 20-21, on both projections of an expert):
+  route (top-k softmax) -> amax(x) -> quantize x with its RAC residual,
+  scattered to the routed rows -> clear padding rows -> W4A4+RAC gate_up GEMM
+  with fused SwiGLU (and fused amax of h) -> quantize h with its residual ->
+  W4A4+RAC down GEMM -> weighted combine.
+Trainer forward (QUADS §3.2, Eq. 12): fake-quantize the expert weights, route,
+dispatch BF16 rows, BF16 gate_up GEMM with fused SwiGLU, BF16 down GEMM,
+combine.
+"""
+import torch
+
+from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16, NVFP4_OUT_F32,
+               nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
+               nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
+               nvfp4_route_topk, nvfp4_w4a4_rac_grouped_gemm)
+
+
+def scale_bytes(rows, K):
+    """Bytes of the swizzled block-scale layout of a rows x K NVFP4 tensor."""
+    return ((rows + 127) // 128) * 128 * ((K // 16 + 3) // 4) * 4
+
+
+def rows_capacity(T, topk, E):
+    """Upper bound of the padded routed-row count (segments start at multiples of 128)."""
+    return ((T * topk + E * 127 + 127) // 128) * 128
+
+
+class _Routing:
+    def __init__(self, T, E, topk, dev):
+        self.ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+        self.weights = torch.empty((T, topk), dtype=torch.float32, device=dev)
+        self.counts = torch.empty(E, dtype=torch.int32, device=dev)
+        self.offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        self.dst_row = torch.empty((T, topk), dtype=torch.int32, device=dev)
+
+
+class _Nvfp4Act:
+    """A routed NVFP4 activation: codes, swizzled scales, residual, gs."""
+
+    def __init__(self, rows, K, k, dev):
+        self.codes = torch.zeros((rows, K // 2), dtype=torch.uint8, device=dev)
+        self.scales = torch.zeros(scale_bytes(rows, K), dtype=torch.uint8, device=dev)
+        self.resid = torch.zeros((rows, max(k, 1)), dtype=torch.bfloat16, device=dev)[:, :k]
+        self.gs = torch.zeros(1, dtype=torch.float32, device=dev)
+        self.amax = torch.zeros(1, dtype=torch.float32, device=dev)
+
+
+class _Nvfp4Weights:
+    """Rollout weight pack of E experts (nvfp4_prepare_weights)."""
+
+    def __init__(self, w, S, interleave):
+        E, N, K = w.shape
+        dev = w.device
+        k = 0 if S is None else S.numel()
+        self.E, self.N, self.K, self.k = E, N, K, k
+        self.codes = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(E * N * K // 16, dtype=torch.uint8, device=dev)
+        self.gs = torch.empty(E, dtype=torch.float32, device=dev)
+        self.sel = torch.empty((E, N, max(k, 1)), dtype=torch.bfloat16, device=dev)[:, :, :k].contiguous() \
+            if k else None
+        self.amax_ws = torch.empty(E, dtype=torch.float32, device=dev)
+        self.S = S
+        nvfp4_prepare_weights(w, self.codes, self.scales, self.gs, self.amax_ws, S=S, w_sel=self.sel,
+                              interleave=interleave)
+
+
+class RolloutMoE:
+    """W4A4 + RAC MoE layer (rollout side).
+
+    w13: [E, 2I, H] BF16 (gate rows then up rows); w_down: [E, H, I] BF16;
+    S13 / S_down: int32 RAC channel sets of the two projections (sorted, on
+    the device; may be None for plain W4A4); max_tokens: buffer capacity.
+    """
+
+    def __init__(self, w13, w_down, S13, S_down, topk, max_tokens, out_dtype=torch.float32):
+        self.E, N13, self.H = w13.shape
+        self.I = N13 // 2
+        self.topk = topk
+        dev = w13.device
+        self.dev = dev
+        self.w13 = _Nvfp4Weights(w13, S13, interleave=1)
+        self.wd = _Nvfp4Weights(w_down, S_down, interleave=0)
+        self.k13 = self.w13.k
+        self.kd = self.wd.k
+        self.S13, self.Sd = S13, S_down
+        self.max_tokens = max_tokens
+        self.rows_cap = rows_capacity(max_tokens, topk, self.E)
+        self.route = _Routing(max_tokens, self.E, topk, dev)
+        self.xa = _Nvfp4Act(self.rows_cap, self.H, self.k13, dev)
+        self.h = torch.zeros((self.rows_cap, self.I), dtype=torch.bfloat16, device=dev)
+        self.ha = _Nvfp4Act(self.rows_cap, self.I, self.kd, dev)
+        self.y = torch.zeros((self.rows_cap, self.H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((max_tokens, self.H), dtype=torch.float32, device=dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def forward(self, x, logits, stream=None):
+        """x [T, H] BF16, logits [T, E] FP32 -> out [T, H] FP32 (a view of a reused buffer)."""
+        T = x.shape[0]
+        assert T <= self.max_tokens and logits.shape == (T, self.E)
+        r = self.route
+        ids, w, dst = r.ids[:T], r.weights[:T], r.dst_row[:T]
+        nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=stream)
+        xa, ha = self.xa, self.ha
+        nvfp4_amax(x, xa.amax, stream=stream)
+        nvfp4_quantize(x, xa.amax, xa.codes, xa.scales, resid=xa.resid if self.k13 else None,
+                       S=self.S13 if self.k13 else None, gs_out=xa.gs, dst_row=dst,
+                       fanout=self.topk, rows_out=self.rows_cap, dev_status=self.dev_status,
+                       stream=stream)
+        nvfp4_moe_clear_padding(r.counts, r.offsets, self.E, self.H, self.k13, xa.codes, xa.scales,
+                                xa.resid if self.k13 else None, stream=stream)
+        W = self.w13
+        nvfp4_w4a4_rac_grouped_gemm(xa.codes, xa.scales, xa.resid if W.k else None, xa.gs, W.codes,
+                                    W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.h,
+                                    epilogue=NVFP4_EPI_SWIGLU, out_dtype=NVFP4_OUT_BF16,
+                                    amax_out=ha.amax, dev_status=self.dev_status, stream=stream)
+        nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
+                       S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
+                       stream=stream)
+        W = self.wd
+        nvfp4_w4a4_rac_grouped_gemm(ha.codes, ha.scales, ha.resid if W.k else None, ha.gs, W.codes,
+                                    W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.y,
+                                    epilogue=NVFP4_EPI_NONE, out_dtype=NVFP4_OUT_BF16,
+                                    dev_status=self.dev_status, stream=stream)
+        out = self.out[:T]
+        nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
+        return out
+
+
+class QatMoE:
+    """Trainer-side asymmetric-QAT MoE forward (weights fake-quantized, BF16 activations)."""
+
+    def __init__(self, w13, w_down, topk, max_tokens):
+        self.E, N13, self.H = w13.shape
+        self.I = N13 // 2
+        self.topk = topk
+        dev = w13.device
+        self.w13, self.wd = w13, w_down
+        self.w13_hat = torch.empty_like(w13)
+        self.wd_hat = torch.empty_like(w_down)
+        self.gs13 = torch.empty(self.E, dtype=torch.float32, device=dev)
+        self.gsd = torch.empty(self.E, dtype=torch.float32, device=dev)
+        self.amax_ws = torch.empty(self.E, dtype=torch.float32, device=dev)
+        self.max_tokens = max_tokens
+        self.rows_cap = rows_capacity(max_tokens, topk, self.E)
+        self.route = _Routing(max_tokens, self.E, topk, dev)
+        self.xr = torch.zeros((self.rows_cap, self.H), dtype=torch.bfloat16, device=dev)
+        self.h = torch.zeros((self.rows_cap, self.I), dtype=torch.bfloat16, device=dev)
+        self.y = torch.zeros((self.rows_cap, self.H), dtype=torch.bfloat16, device=dev)
+        self.out = torch.empty((max_tokens, self.H), dtype=torch.float32, device=dev)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def fake_quant(self, stream=None):
+        nvfp4_fake_quant(self.w13, self.w13_hat, self.amax_ws, gs_out=self.gs13,
+                         dev_status=self.dev_status, stream=stream)
+        nvfp4_fake_quant(self.wd, self.wd_hat, self.amax_ws, gs_out=self.gsd,
+                         dev_status=self.dev_status, stream=stream)
+
+    def forward(self, x, logits, stream=None):
+        T = x.shape[0]
+        r = self.route
+        ids, w, dst = r.ids[:T], r.weights[:T], r.dst_row[:T]
+        self.fake_quant(stream=stream)
+        nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=stream)
+        nvfp4_moe_scatter_rows(x, self.topk, dst, r.counts, r.offsets, self.E, self.xr, stream=stream)
+        nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.h,
+                                out_dtype=NVFP4_OUT_BF16, epilogue=NVFP4_EPI_SWIGLU,
+                                dev_status=self.dev_status, stream=stream)
+        nvfp4_bf16_grouped_gemm(self.h, self.wd_hat, r.offsets, self.E, self.H, self.I, self.y,
+                                out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
+        out = self.out[:T]
+        nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
+        return out

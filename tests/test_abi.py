@@ -1,0 +1,114 @@
+"""The C-ABI library builds, loads and exports every symbol its header
+declares; the Python binding passes arguments with the header's types; host
+argument checks reject bad calls before anything reaches a GPU.  CPU only."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4moe.h")
+
+import nvfp4_precision_moe_gb300 as nv  # noqa: E402
+from nvfp4_precision_moe_gb300.build import build_library  # noqa: E402
+
+OK, INVALID, UNSUP, ALIGN, ARCH = 0, 1, 2, 3, 7
+
+
+def _decls():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(int|const char \*)\s*(nvfp4_\w+)\s*\(([^)]*)\)\s*;", txt):
+        args = [a.strip() for a in m.group(3).split(",") if a.strip() and a.strip() != "void"]
+        sig = ""
+        for a in args:
+            if "*" in a:
+                sig += "p"
+            elif a.startswith("int64_t"):
+                sig += "q"
+            elif a.startswith("int32_t") or a.startswith("int "):
+                sig += "i"
+            else:
+                raise AssertionError("unknown argument type: " + a)
+        out[m.group(2)] = (m.group(1), sig)
+    return out
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return nv.load()
+
+
+def test_header_declares_the_boundary():
+    d = _decls()
+    for name in ["nvfp4_quantize", "nvfp4_amax", "nvfp4_fake_quant", "nvfp4_prepare_weights",
+                 "nvfp4_w4a4_rac_grouped_gemm", "nvfp4_bf16_grouped_gemm", "nvfp4_route_topk",
+                 "nvfp4_moe_combine", "nvfp4_rac_select_channels", "nvfp4_status_str"]:
+        assert name in d
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _decls():
+        assert hasattr(lib, name), name
+
+
+def test_binding_signatures_match_header(lib):
+    d = _decls()
+    for name, (ret, sig) in d.items():
+        if ret != "int":
+            continue
+        assert nv._SIGS.get(name) == sig, (name, nv._SIGS.get(name), sig)
+
+
+def test_status_strings(lib):
+    for code, name in nv.STATUS.items():
+        assert lib.nvfp4_status_str(code).decode() == name
+
+
+# a fake, 16-byte aligned "device" address: the host checks never dereference it
+P = 0x10000
+PM = 0x10008  # misaligned
+
+
+def test_host_checks_without_gpu(lib):
+    q = lib.nvfp4_quantize
+    # x, M, K, ldx, amax, gs, S, k, dst, fanout, rows_out, codes, scales, resid, status, stream
+    assert q(None, 4, 64, 64, P, None, None, 0, None, 1, 4, P, P, None, None, None) == INVALID
+    assert q(P, 4, 48, 48, P, None, None, 0, None, 1, 4, P, P, None, None, None) == UNSUP  # K % 32
+    assert q(PM, 4, 64, 64, P, None, None, 0, None, 1, 4, P, P, None, None, None) == ALIGN
+    assert q(P, 4, 64, 64, P, None, P, 8, None, 1, 4, P, P, None, None, None) == INVALID  # k>0, no resid
+    assert q(P, 4, 64, 64, P, None, None, 0, None, 2, 4, P, P, None, None, None) == INVALID  # fanout w/o map
+    g = lib.nvfp4_w4a4_rac_grouped_gemm
+    args = [P, P, None, P, P, P, P, None, 0, P, 1, 128, 128, 256, 0, 0, P, 128, None, None, None]
+    bad_k = list(args)
+    bad_k[13] = 192  # K % 256
+    assert g(*bad_k) == UNSUP
+    bad_n = list(args)
+    bad_n[12] = 96  # N % 128
+    assert g(*bad_n) == UNSUP
+    swiglu_f32 = list(args)
+    swiglu_f32[14] = 1  # SwiGLU needs BF16 output
+    assert g(*swiglu_f32) == INVALID
+    mis = list(args)
+    mis[16] = PM
+    assert g(*mis) == ALIGN
+    # a valid call reaches the device check: there is no CPU path
+    import torch
+    if not torch.cuda.is_available():
+        assert g(*args) == ARCH
+        assert lib.nvfp4_init() == ARCH
+    r = lib.nvfp4_route_topk
+    assert r(P, 16, 8, 9, P, P, P, P, P, None) == UNSUP  # topk > E
+    c = lib.nvfp4_moe_combine
+    assert c(P, 3, 64, P, P, 4, 2, 64, P, None) == INVALID  # bad dtype
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    import importlib
+    monkeypatch.setattr(nv, "_lib", None)
+    monkeypatch.setattr(nv, "LIB", str(tmp_path / "absent.so"))
+    with pytest.raises(RuntimeError):
+        nv.load()
