@@ -1,0 +1,335 @@
+"""Benchmark of the NVFP4 W4A4 + RAC MoE hot path on GB300.
+
+One step = one rollout MoE layer forward of the prefill workload (16384 tokens,
+hidden 4096, 128 experts top-8 with Zipf(1.1) routing, intermediate 1536,
+SwiGLU, RAC k = 128 on both projections): route -> amax -> quantize x with its
+residual, dispatched to routed rows -> clear padding -> W4A4+RAC gate_up GEMM
+with fused SwiGLU and amax -> quantize h -> W4A4+RAC down GEMM -> combine.
+The metric is the GEMM work of the step (FP4 + RAC BF16 FLOPs) per second.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  With --impl reference the CPU oracle is
+timed on a bounded sample of the same workload on this host's cores.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "W4A4+RAC MoE GEMM TFLOPS (% FP4 peak); quantize GB/s (% HBM)"
+WORKLOAD = 5
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core ratio, nominal
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def setup_distributed(n):
+    rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def build_workload(dev):
+    import torch
+
+    import nvfp4_precision_moe_gb300 as nv
+    import synth
+
+    c = synth.CONFIGS[WORKLOAD]
+    E, H, I, T, topk, k = c["E"], c["H"], c["I"], c["T"], c["topk"], c["k"]
+    x = synth.activations(WORKLOAD).to(dev)
+    logits = synth.router_logits(WORKLOAD).to(dev)
+    w13 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev)
+    wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
+    for e in range(E):
+        w13[e].copy_(synth.expert_weight(WORKLOAD, e, "w13"))
+        wd[e].copy_(synth.expert_weight(WORKLOAD, e, "down"))
+    # channel calibration (offline, Eq. 23-24) on an independent calibration batch
+    xc = synth.activations(WORKLOAD, batch=1).to(dev)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    nv.nvfp4_amax(xc, amax)
+    S13 = torch.empty(k, dtype=torch.int32, device=dev)
+    nv.nvfp4_rac_select_channels(xc, amax, k, S13, torch.empty(H, dtype=torch.float64, device=dev))
+    # the down projection's channels: calibrate on the calibration batch's h
+    g = torch.Generator().manual_seed(5)
+    Sd0 = torch.sort(torch.randperm(I, generator=g)[:k]).values.to(torch.int32).to(dev)
+    cal = nv.RolloutMoE(w13, wd, S13, Sd0, topk, T)
+    cal.forward(xc, synth.router_logits(WORKLOAD).roll(1, 0).to(dev))
+    hmax = torch.zeros(1, dtype=torch.float32, device=dev)
+    nv.nvfp4_amax(cal.h, hmax)
+    Sd = torch.empty(k, dtype=torch.int32, device=dev)
+    nv.nvfp4_rac_select_channels(cal.h, hmax, k, Sd, torch.empty(I, dtype=torch.float64, device=dev))
+    del cal, xc
+    layer = nv.RolloutMoE(w13, wd, S13, Sd, topk, T)  # weight prep (A7), once per weight update
+    torch.cuda.synchronize()
+    return c, layer, x, logits
+
+
+def run_ours(args):
+    import torch
+
+    rank, world, local = setup_distributed(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import nvfp4_precision_moe_gb300 as nv
+    import synth
+
+    nv.load(build=True)
+    c, layer, x, logits = build_workload(dev)
+    T, H, E, I, k = c["T"], c["H"], c["E"], c["I"], c["k"]
+    f4, fb = synth.flops_moe(WORKLOAD)
+    f4_13 = 2 * T * c["topk"] * 2 * I * H
+    fb_13 = 2 * T * c["topk"] * 2 * I * k
+    stream = torch.cuda.current_stream()
+
+    # per-stage events of one step (all launches are on `stream`)
+    nstage = 8
+
+    def step(ev=None):
+        layer.forward(x, logits, mark=(lambda i: ev[i].record(stream)) if ev is not None else None)
+
+    launches_per_step = layer.LAUNCHES
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0, nv.STATUS.get(int(layer.dev_status.item()))
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.15)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+        dist.barrier()
+    ms_step = ms / args.steps
+    names = ["route", "amax_x", "quantize_x", "gemm_gate_up", "quantize_h", "gemm_down", "combine"]
+    stage = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)])
+             for j, n in enumerate(names)}
+    gemm13_ms = statistics.mean([evs[i][3].elapsed_time(evs[i][4]) for i in range(args.steps)])
+
+    # ---- end to end through host buffers: inputs H2D from pinned memory, result D2H
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    oh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    for _ in range(max(1, args.warmup // 2)):
+        x.copy_(xh, non_blocking=True)
+        logits.copy_(lh, non_blocking=True)
+        step()
+        oh.copy_(layer.out[:T], non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(xh, non_blocking=True)
+        logits.copy_(lh, non_blocking=True)
+        step()
+        oh.copy_(layer.out[:T], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    assert int(layer.dev_status.item()) == 0
+
+    pk = peaks()
+    fp4_peak = pk["bf16"] * NOMINAL_FP4_OVER_BF16
+    value = world * (f4 + fb) / (ms_step * 1e-3) / 1e12
+    gemm13_tflops = f4_13 / (gemm13_ms * 1e-3) / 1e12
+    R = T * c["topk"]
+    q_bytes = 2 * T * H + R * (H // 2 + H // 16 + 2 * k)  # read x, write routed codes/scales/residual
+    q_gbs = q_bytes / (stage["quantize_x"] * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1 (fp32 accum) + bf16 RAC", "data": "synthetic",
+        "config": {"workload": "moe_prefill T=16384 H=4096 E=128 top8 zipf1.1 I=1536 k=128",
+                   "T": T, "H": H, "E": E, "topk": c["topk"], "I": I, "k": k, "parallelism": "replicas",
+                   "l2": "no flush: every step streams ~3 GB, far more than the 129 MB L2"},
+        "fp4_peak_frac_step": round(world * f4 / (ms_step * 1e-3) / 1e12 / fp4_peak, 4),
+        "quantize_x": {"gbs": round(q_gbs, 1), "hbm_frac": round(q_gbs / pk["hbm"], 4), "bytes": q_bytes},
+        "stages_ms": {n: round(v, 4) for n, v in stage.items()},
+        "roofline": {"kernel": "grouped_gemm_kernel<fp4> (gate_up, SwiGLU)", "bound": "tensor",
+                     "achieved": round(gemm13_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                     "frac": round(gemm13_tflops / fp4_peak, 4), "traffic": None,
+                     "peak_src": "%s bf16 burst x nominal fp4/bf16 ratio 6" % pk["src"]},
+        "e2e": {"value": round(world * (f4 + fb) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(x.numel() * 2 + logits.numel() * 4),
+                "d2h_bytes_per_step": int(T * H * 4)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+_ORACLE_WEIGHTS = {}
+
+
+def cpu_baseline(seconds=12.0, rows=None):
+    """The oracle as it stands (plain C, one thread) on a bounded sample of the
+    workload: the routed rows of one expert through both W4A4+RAC projections
+    (quantize of the expert's weights included).  Returns TFLOP/s of GEMM work."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    c = synth.CONFIGS[WORKLOAD]
+    H, I, k = c["H"], c["I"], c["k"]
+    t_start = time.perf_counter()
+    n = rows or 64
+    x = synth.u16(synth.activations(WORKLOAD, rows=n))
+    S13 = np.arange(0, H, H // k, dtype=np.int32)
+    Sd = np.arange(0, I, I // k, dtype=np.int32)
+    if "w" not in _ORACLE_WEIGHTS:  # the weight pack is per weight update: not timed
+        cw, sw, _, gw = oracle.quantize(synth.u16(synth.expert_weight(WORKLOAD, 0, "w13")))
+        cd, sd, _, gd = oracle.quantize(synth.u16(synth.expert_weight(WORKLOAD, 0, "down")))
+        _ORACLE_WEIGHTS["w"] = (oracle.dequantize_exact(cw, sw, gw), oracle.dequantize_exact(cd, sd, gd))
+    wq13, wqd = _ORACLE_WEIGHTS["w"]
+    t0 = time.perf_counter()
+    ca, sa, ra, ga = oracle.quantize(x, S=S13)
+    y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, ga), wq13, ra, S13)
+    h = oracle.bf16_round(oracle.swiglu(y, I).astype(np.float32))
+    ch, sh, rh, gh = oracle.quantize(h, S=Sd)
+    oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gh), wqd, rh, Sd)
+    dt = time.perf_counter() - t0
+    fl = 2 * n * (2 * I) * (H + k) + 2 * n * H * (I + k)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": "%d routed rows of one expert: quantize x, W4A4+RAC gate_up, SwiGLU, quantize h, "
+                      "W4A4+RAC down; plain C oracle, 1 thread (%.1f s timed)" % (n, dt),
+            "seconds": round(time.perf_counter() - t_start, 2)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle.build import build_oracle
+
+    build_oracle()
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(rows=32)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(rows=32))
+    wall = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+           "data": "synthetic",
+           "config": {"workload": "moe_prefill T=16384 H=4096 E=128 top8 zipf1.1 I=1536 k=128",
+                      "sample": "32 routed rows of one expert per step (the CPU oracle)"},
+           "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                            "sample": vals[0]["sample"]},
+           "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -99,36 +99,52 @@ class RolloutMoE:
         self.out = torch.empty((max_tokens, self.H), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def forward(self, x, logits, stream=None):
-        """x [T, H] BF16, logits [T, E] FP32 -> out [T, H] FP32 (a view of a reused buffer)."""
+    # number of library kernels one forward launches
+    LAUNCHES = 10
+
+    def forward(self, x, logits, stream=None, mark=None):
+        """x [T, H] BF16, logits [T, E] FP32 -> out [T, H] FP32 (a view of a reused buffer).
+
+        `mark(i)`, if given, is called before stage i = 0..6 (route, amax,
+        quantize x, gate_up GEMM, quantize h, down GEMM, combine) and with
+        i = 7 at the end, e.g. to record CUDA events."""
+        mark = mark or (lambda i: None)
         T = x.shape[0]
         assert T <= self.max_tokens and logits.shape == (T, self.E)
         r = self.route
         ids, w, dst = r.ids[:T], r.weights[:T], r.dst_row[:T]
+        mark(0)
         nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=stream)
         xa, ha = self.xa, self.ha
+        mark(1)
         nvfp4_amax(x, xa.amax, stream=stream)
+        mark(2)
         nvfp4_quantize(x, xa.amax, xa.codes, xa.scales, resid=xa.resid if self.k13 else None,
                        S=self.S13 if self.k13 else None, gs_out=xa.gs, dst_row=dst,
                        fanout=self.topk, rows_out=self.rows_cap, dev_status=self.dev_status,
                        stream=stream)
         nvfp4_moe_clear_padding(r.counts, r.offsets, self.E, self.H, self.k13, xa.codes, xa.scales,
                                 xa.resid if self.k13 else None, stream=stream)
+        mark(3)
         W = self.w13
         nvfp4_w4a4_rac_grouped_gemm(xa.codes, xa.scales, xa.resid if W.k else None, xa.gs, W.codes,
                                     W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.h,
                                     epilogue=NVFP4_EPI_SWIGLU, out_dtype=NVFP4_OUT_BF16,
                                     amax_out=ha.amax, dev_status=self.dev_status, stream=stream)
+        mark(4)
         nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
                        S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
                        stream=stream)
+        mark(5)
         W = self.wd
         nvfp4_w4a4_rac_grouped_gemm(ha.codes, ha.scales, ha.resid if W.k else None, ha.gs, W.codes,
                                     W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.y,
                                     epilogue=NVFP4_EPI_NONE, out_dtype=NVFP4_OUT_BF16,
                                     dev_status=self.dev_status, stream=stream)
+        mark(6)
         out = self.out[:T]
         nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
+        mark(7)
         return out
 
 

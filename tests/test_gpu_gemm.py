@@ -264,8 +264,8 @@ def test_swiglu_epilogue_and_fused_amax():
         n = counts[e]
         y = oracle.rac_gemm(xq[pos:pos + n], wq, r[pos:pos + n], S)
         ref = oracle.swiglu(y, I)
-        # BF16 output: half an ulp (2^-9 relative) plus the GEMM tolerance
-        assert G.rel_err(got[offsets[e]:offsets[e] + n], ref) <= 2.0 ** -9 + TOL
+        # BF16 output: the unit roundoff 2^-8 of BF16 plus the GEMM tolerance
+        assert G.rel_err(got[offsets[e]:offsets[e] + n], ref) <= 2.0 ** -8 + TOL
         assert (got[offsets[e] + n:offsets[e + 1]] == 0).all()
         pos += n
     assert hmax.item() == np.abs(got).max()
@@ -303,6 +303,6 @@ def test_bf16_grouped_gemm_parity(swiglu):
         ref = oracle.bf16_gemm(xu[offsets[e]:offsets[e] + n], wu[e])
         if swiglu:
             ref = oracle.swiglu(ref, N // 2)
-            assert G.rel_err(got[offsets[e]:offsets[e] + n], ref) <= 2.0 ** -9 + TOL
+            assert G.rel_err(got[offsets[e]:offsets[e] + n], ref) <= 2.0 ** -8 + TOL
         else:
             assert G.rel_err(got[offsets[e]:offsets[e] + n], ref) <= TOL

@@ -127,7 +127,7 @@ def test_rollout_layer_end_to_end_reduced():
     h_gpu = layer.h[:R].float().cpu().numpy()
     live = np.zeros(R, bool)
     live[dst.reshape(-1)] = True
-    assert G.rel_err(h_gpu[live], h_ref[live]) <= 2.0 ** -9 + TOL
+    assert G.rel_err(h_gpu[live], h_ref[live]) <= 2.0 ** -8 + TOL
     assert (h_gpu[~live] == 0).all()
     # continue the oracle chain from its own BF16 h
     hu = oracle.bf16_round(h_ref.astype(np.float32))

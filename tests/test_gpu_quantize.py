@@ -149,9 +149,10 @@ def test_block_scale_ties_and_subnormals():
 def test_zero_tensor_and_signed_zeros():
     x = np.zeros((4, 64), np.uint16)
     x[1, :] = 0x8000  # -0
-    got = _gpu_quantize(x, S=np.array([0, 5, 63], np.int32))
+    S = np.array([0, 5, 9, 20, 33, 40, 50, 63], np.int32)
+    got = _gpu_quantize(x, S=S)
     assert got["gs"] == 1.0 and got["amax"] == 0.0
-    codes, _, _, _ = oracle.quantize(x, S=np.array([0, 5, 63], np.int32))
+    codes, _, _, _ = oracle.quantize(x, S=S)
     assert np.array_equal(got["codes"], codes)
     assert not got["scales"].any() and not got["resid"].any()
     assert (got["codes"][1] == 0x88).all()
@@ -160,7 +161,7 @@ def test_zero_tensor_and_signed_zeros():
 def test_scatter_to_routed_rows():
     rng = np.random.default_rng(9)
     x = synth.u16(synth.activations(1))[:40]
-    S = np.array([3, 100, 200, 511], np.int32)
+    S = np.array([3, 100, 101, 200, 300, 301, 400, 511], np.int32)
     fan = 3
     rows_out = 256
     dst = rng.permutation(rows_out)[: 40 * fan].reshape(40, fan)
@@ -169,7 +170,7 @@ def test_scatter_to_routed_rows():
     # scatter the oracle's rows the same way in the test (plain indexing)
     oc = np.zeros((rows_out, 256), np.uint8)
     osc = np.zeros((rows_out, 32), np.uint8)
-    ores = np.zeros((rows_out, 4), np.uint16)
+    ores = np.zeros((rows_out, 8), np.uint16)
     for t in range(40):
         for f in range(fan):
             oc[dst[t, f]] = codes[t]
@@ -187,7 +188,7 @@ def test_nonfinite_amax_is_reported():
 
 
 def test_fake_quant_parity():
-    ws = [synth.dense_weight(1), synth.dense_weight(1) * 7, synth.activations(1)[:, :512]]
+    ws = [synth.dense_weight(1), synth.dense_weight(1) * 7, torch.cat([synth.activations(1)] * 8)]
     w = torch.stack([t.contiguous() for t in ws])
     wd = w.to(G.DEV)
     w_hat = torch.empty_like(wd)
