@@ -315,6 +315,81 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def run_profile_case(args):
+    """A single kernel on a reduced case sized for ncu (inputs above L2, a few
+    hundred MB in all): `gemm13` (gate_up W4A4+RAC GEMM with SwiGLU, 32
+    experts x 512 rows, N=3072, K=4096, k=128), `gemm_down` (N=4096, K=1536),
+    `quantize_x` (16384 x 4096 scatter-quantize, top-8), `bf16_gemm`
+    (QAT gate_up, BF16, same shape as gemm13).  Runs `--steps` launches."""
+    import torch
+
+    import nvfp4_precision_moe_gb300 as nv
+
+    nv.load(build=True)
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    E, per = 32, 512
+    rows = E * per
+    offsets = torch.arange(0, rows + 1, per, dtype=torch.int32, device=dev)
+    case = args.profile_case
+    if case in ("gemm13", "gemm_down"):
+        N, K = (3072, 4096) if case == "gemm13" else (4096, 1536)
+        k = 128
+        a = torch.randint(0, 256, (rows, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        a_s = torch.randint(0x28, 0x40, (rows * K // 16,), dtype=torch.uint8, device=dev, generator=g)
+        r = (torch.randn((rows, k), device=dev, generator=g) * 0.1).to(torch.bfloat16)
+        w = torch.randint(0, 256, (E, N, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        w_s = torch.randint(0x28, 0x40, (E * N * K // 16,), dtype=torch.uint8, device=dev, generator=g)
+        sel = torch.randn((E, N, k), device=dev, generator=g).to(torch.bfloat16)
+        gs_a = torch.full((1,), 0.01, device=dev)
+        gs_w = torch.full((E,), 0.001, device=dev)
+        swi = case == "gemm13"
+        y = torch.empty((rows, N // 2 if swi else N), dtype=torch.bfloat16, device=dev)
+        amax = torch.zeros(1, device=dev)
+        fn = lambda: nv.nvfp4_w4a4_rac_grouped_gemm(
+            a, a_s, r, gs_a, w, w_s, gs_w, sel, k, offsets, E, N, K, y,
+            epilogue=nv.NVFP4_EPI_SWIGLU if swi else nv.NVFP4_EPI_NONE, out_dtype=nv.NVFP4_OUT_BF16,
+            amax_out=amax if swi else None)
+        flops = 2 * rows * N * K
+    elif case == "bf16_gemm":
+        N, K = 3072, 4096
+        x = torch.randn((rows, K), device=dev, generator=g).to(torch.bfloat16)
+        w = (torch.randn((E, N, K), device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        y = torch.empty((rows, N // 2), dtype=torch.bfloat16, device=dev)
+        fn = lambda: nv.nvfp4_bf16_grouped_gemm(x, w, offsets, E, N, K, y, out_dtype=nv.NVFP4_OUT_BF16,
+                                                epilogue=nv.NVFP4_EPI_SWIGLU)
+        flops = 2 * rows * N * K
+    elif case == "quantize_x":
+        T, H, topk, k = 16384, 4096, 8, 128
+        x = torch.randn((T, H), device=dev, generator=g).to(torch.bfloat16)
+        cap = T * topk
+        dst = torch.randperm(cap, device=dev, generator=g).to(torch.int32).view(T, topk)
+        codes = torch.empty((cap, H // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty(nv.scale_bytes(cap, H), dtype=torch.uint8, device=dev)
+        resid = torch.empty((cap, k), dtype=torch.bfloat16, device=dev)
+        S = torch.arange(0, H, H // k, dtype=torch.int32, device=dev)
+        amax = torch.zeros(1, device=dev)
+        nv.nvfp4_amax(x, amax)
+        fn = lambda: nv.nvfp4_quantize(x, amax, codes, scales, resid=resid, S=S, dst_row=dst, fanout=topk,
+                                       rows_out=cap)
+        flops = 0
+    else:
+        raise SystemExit("unknown --profile-case " + case)
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(args.steps):
+        fn()
+    t1.record()
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    print(json.dumps({"profile_case": case, "ms": round(ms, 4),
+                      "tflops": round(flops / ms / 1e9, 1) if flops else None}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -322,10 +397,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-case", default=None,
+                    help="run one kernel on a reduced case for ncu: gemm13, gemm_down, quantize_x, bf16_gemm")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
