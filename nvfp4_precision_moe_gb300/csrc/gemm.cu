@@ -11,9 +11,16 @@
 //
 // Tiles are 128 rows x 128 columns of the output; the K loop moves 128-byte
 // wide K-slices (256 FP4 or 64 BF16 elements) through a ring of shared-memory
-// stages fed by TMA (128-byte swizzle).  Warp roles per CTA (192 threads):
-//   warp 0  TMA producer (one lane)     warp 1  TMEM owner + MMA issuer (one lane)
-//   warps 2-5 epilogue: tcgen05.ld of their 32-lane quarter, scale, store.
+// stages fed by TMA (128-byte swizzle).  Warp roles per CTA (320 threads):
+//   warp 0     TMA producer (one lane)
+//   warp 1     TMEM owner + MMA issuer (one lane)
+//   warps 2-9  epilogue: warp w reads TMEM lane quarter w%4 and column half
+//              (w-2)/4 of the tile, scales, applies SwiGLU, stores.
+// Tensor memory (512 columns): the main accumulator is double-buffered
+// (columns 0-127 and 128-255), so the epilogue of one tile overlaps the MMAs
+// of the next; the RAC accumulator (256-383) is single-buffered and its MMAs
+// are issued last in each tile, after the previous tile's epilogue has read
+// it; columns 384-511 hold the block scales of the 4 pipeline stages.
 // Expert segments are contiguous 128-row groups of the routed rows, so the
 // tile list is (row tile, column tile) over all routed rows; each tile's
 // expert comes from a binary search of the segment offsets.
@@ -25,9 +32,11 @@ constexpr int kBM = 128, kBN = 128;
 constexpr int kTileBytes = 16384;  // 128 rows x 128 bytes
 constexpr int kSFBytes = 2048;     // 4 MMA-K chunks x 512 bytes (128 rows x 4 scales)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccMain = 0, kAccRes = 128, kSFCol0 = 256;
+constexpr uint32_t kAccMain0 = 0, kAccRes = 256, kSFCol0 = 384;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxExperts = 1024;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 // Instruction descriptors (M = 128, N = 128, both operands K-major).
 //  kind::mxf4nvf4: A, B = E2M1 (1) at bits 7-9 / 10-12, N>>3 at 17, scale
@@ -38,12 +47,14 @@ constexpr uint32_t kIdescBF16 = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3)
 
 template <bool FP4>
 struct Cfg {
-    static constexpr int kStages = FP4 ? 5 : 6;
+    static constexpr int kStages = FP4 ? 4 : 6;
     static constexpr int kStageBytes = 2 * kTileBytes + (FP4 ? 2 * kSFBytes : 0);
     static constexpr int kBarOffset = kStages * kStageBytes;
-    // barriers (2*stages + 3) x 8 bytes, tmem slot, abort flag, offsets
-    static constexpr int kOffOffset = kBarOffset + (2 * kStages + 3) * 8 + 16;
-    static constexpr int kSmemBytes = 1024 + kOffOffset + (kMaxExperts + 1) * 4;
+    // barriers: full/empty per stage, acc_full[2], acc_empty[2], res_empty, drain
+    static constexpr int kNumBars = 2 * kStages + 6;
+    static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
+    static constexpr int kGswOffset = kOffOffset + (kMaxExperts + 1) * 4;
+    static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
 };
 
 struct GemmParams {
@@ -77,8 +88,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
            ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
 }
 
+// silu(g) * u with the fast exponential and division (a few ulp; the BF16
+// rounding of the result dominates).
+__device__ __forceinline__ float swiglu1(float g, float u) {
+    const float e = __expf(-g);
+    return __fmul_rn(__fdividef(g, 1.0f + e), u);
+}
+
 template <bool FP4>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmWs,
                         GemmParams p) {
@@ -87,23 +105,30 @@ __global__ void __launch_bounds__(192, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
     uint64_t *empty = full + C::kStages;
-    uint64_t *acc_full = empty + C::kStages;
-    uint64_t *acc_empty = acc_full + 1;
-    uint64_t *drain = acc_empty + 1;
+    uint64_t *acc_full = empty + C::kStages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;       // [2]
+    uint64_t *res_empty = acc_empty + 2;
+    uint64_t *drain = res_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::kOffOffset);
+    float *s_gsw = reinterpret_cast<float *>(smem + C::kGswOffset);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
     for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = p.offsets[i];
+    if (FP4)
+        for (int i = threadIdx.x; i < E; i += blockDim.x) s_gsw[i] = p.gs_w[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_full[b], 1);
+            mbar_init(&acc_empty[b], kEpiWarps);
+        }
+        mbar_init(res_empty, kEpiWarps);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -202,12 +227,24 @@ __global__ void __launch_bounds__(192, 1)
             bool ok = true;
             int local = 0;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-                if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
+                const uint32_t buf = (uint32_t)local & 1u;
+                const uint32_t acc = tmem + kAccMain0 + buf * kBN;
+                // the epilogue must have drained this buffer (used two tiles ago)
+                if (!mbar_wait_bounded(&acc_empty[buf], (((uint32_t)local >> 1) & 1u) ^ 1u, kWaitLimitNs,
+                                       abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int it = 0; it < nkt + nrt; ++it) {
+                    if (it == nkt) {
+                        // the single RAC accumulator: the previous tile's epilogue has read it
+                        if (!mbar_wait_bounded(res_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
                     if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
                         ok = false;
                         break;
@@ -226,12 +263,12 @@ __global__ void __launch_bounds__(192, 1)
                             }
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                tc_mma_nvf4(tmem + kAccMain, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
+                                tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
                                             kIdescNVF4, sf + 4 * c, sf + 16 + 4 * c, (it | c) != 0);
                         } else {
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                tc_mma_bf16(tmem + kAccMain, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
+                                tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
                                             kIdescBF16, (it | c) != 0);
                         }
                     } else {
@@ -248,7 +285,7 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
                 if (!ok) break;
-                tc_commit(acc_full);
+                tc_commit(&acc_full[buf]);
             }
             if (!ok) {
                 report(p.dev_status, NVFP4_ERR_TIMEOUT);
@@ -261,16 +298,20 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int ew = warp - 2;             // 0..7
+        const int q = warp & 3;              // TMEM lane quarter this warp may access
+        const int half = ew >> 2;            // which half of the tile's columns
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int row_in_tile = q * 32 + lane;
         const float gsa = FP4 ? *p.gs_a : 1.0f;
+        const bool has_res = FP4 && p.k > 0;
         float amax_local = 0.0f;
         int local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            const uint32_t buf = (uint32_t)local & 1u;
             // every lane waits; the warp goes on only if all lanes saw the phase
             // complete, so the .sync.aligned TMEM loads below stay converged
-            const bool got = mbar_wait_bounded(acc_full, (uint32_t)local & 1u, kWaitLimitNs, abort_flag);
+            const bool got = mbar_wait_bounded(&acc_full[buf], ((uint32_t)local >> 1) & 1u, kWaitLimitNs, abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) {
                     report(p.dev_status, NVFP4_ERR_TIMEOUT);
@@ -279,24 +320,27 @@ __global__ void __launch_bounds__(192, 1)
                 break;
             }
             tc_fence_after();
+            const uint32_t acc = tmem + lane_base + kAccMain0 + buf * kBN;
+            const uint32_t res = tmem + lane_base + kAccRes;
             const int mt = tile / num_nt, nt = tile - mt * num_nt;
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
             float gsw = 1.0f, gmul = 1.0f;
             if (FP4) {
-                gsw = p.gs_w[expert_of(s_off, E, mt * kBM)];
+                gsw = s_gsw[expert_of(s_off, E, mt * kBM)];
                 gmul = __fmul_rn(gsa, gsw);
             }
-            const bool has_res = FP4 && p.k > 0;
             if (p.epilogue == NVFP4_EPI_SWIGLU) {
-                uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 64;
+                // columns 0-63 gate, 64-127 up; this warp: output columns [32*half, 32*half+32)
+                uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 64 + 32 * half;
 #pragma unroll 1
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < 2; ++j) {
+                    const int c0 = 32 * half + 16 * j;
                     uint32_t g[16], u[16], gr[16], ur[16];
-                    tmem_ld16(tmem + lane_base + kAccMain + 16 * j, g);
-                    tmem_ld16(tmem + lane_base + kAccMain + 64 + 16 * j, u);
+                    tmem_ld16(acc + c0, g);
+                    tmem_ld16(acc + 64 + c0, u);
                     if (has_res) {
-                        tmem_ld16(tmem + lane_base + kAccRes + 16 * j, gr);
-                        tmem_ld16(tmem + lane_base + kAccRes + 64 + 16 * j, ur);
+                        tmem_ld16(res + c0, gr);
+                        tmem_ld16(res + 64 + c0, ur);
                     }
                     tmem_ld_wait();
                     uint32_t o[8];
@@ -311,8 +355,7 @@ __global__ void __launch_bounds__(192, 1)
                                 gv = __fadd_rn(gv, __fmul_rn(gsw, __uint_as_float(gr[i + t])));
                                 uv = __fadd_rn(uv, __fmul_rn(gsw, __uint_as_float(ur[i + t])));
                             }
-                            float silu = gv / (1.0f + expf(-gv));
-                            hv[t] = __fmul_rn(silu, uv);
+                            hv[t] = swiglu1(gv, uv);
                         }
                         o[i / 2] = pack_bf16x2(hv[0], hv[1]);
                         amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] << 16)));
@@ -324,10 +367,11 @@ __global__ void __launch_bounds__(192, 1)
                 }
             } else {
 #pragma unroll 1
-                for (int j = 0; j < kBN / 16; ++j) {
+                for (int j = 0; j < 4; ++j) {
+                    const int c0 = 64 * half + 16 * j;
                     uint32_t d[16], dr[16];
-                    tmem_ld16(tmem + lane_base + kAccMain + 16 * j, d);
-                    if (has_res) tmem_ld16(tmem + lane_base + kAccRes + 16 * j, dr);
+                    tmem_ld16(acc + c0, d);
+                    if (has_res) tmem_ld16(res + c0, dr);
                     tmem_ld_wait();
                     float v[16];
 #pragma unroll
@@ -339,7 +383,7 @@ __global__ void __launch_bounds__(192, 1)
                         }
                         v[i] = x;
                     }
-                    const int64_t col = (int64_t)nt * kBN + 16 * j;
+                    const int64_t col = (int64_t)nt * kBN + c0;
                     if (p.out_dtype == NVFP4_OUT_F32) {
                         float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + row * p.ldy + col);
 #pragma unroll
@@ -360,9 +404,13 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
+            // all TMEM reads of this tile are complete (tcgen05.wait::ld above)
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (lane == 0) {
+                if (has_res) mbar_arrive(res_empty);
+                mbar_arrive(&acc_empty[buf]);
+            }
         }
         if (p.amax_out) {
 #pragma unroll
@@ -468,7 +516,7 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
     p.dev_status = dev_status;
     const int64_t max_tiles = (rows_cap / 128) * (N / 128);
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
-    grouped_gemm_kernel<true><<<grid, 192, Cfg<true>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tR, tW, p);
+    grouped_gemm_kernel<true><<<grid, kThreads, Cfg<true>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tR, tW, p);
     return launch_status("grouped_gemm_kernel<fp4>");
 }
 
@@ -507,6 +555,6 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     p.dev_status = dev_status;
     const int64_t max_tiles = (rows_cap / 128) * (N / 128);
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
-    grouped_gemm_kernel<false><<<grid, 192, Cfg<false>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tA, tB, p);
+    grouped_gemm_kernel<false><<<grid, kThreads, Cfg<false>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tA, tB, p);
     return launch_status("grouped_gemm_kernel<bf16>");
 }

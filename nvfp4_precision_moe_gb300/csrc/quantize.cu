@@ -47,40 +47,65 @@ __device__ __forceinline__ int64_t swz_offset(int64_t m, int64_t kb, int64_t kgr
     return ((m >> 7) * kgroups + (kb >> 2)) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (kb & 3);
 }
 
-// One 16-element block: scale code, E2M1 codes, the block's dequant factor.
+// E2M1 code -> value, from a packed table of 2*|value| (0,1,2,3,4,6,8,12).
+__device__ __forceinline__ float e2m1_val(uint32_t c) {
+    const float mag = 0.5f * (float)((0xC8643210u >> (4u * (c & 7u))) & 15u);
+    return (c & 8u) ? -mag : mag;
+}
+
+// One 16-element block: the E4M3 scale code, its value, and the 16 E2M1 codes
+// packed two per byte (element 2i in the low nibble) into two words.
 struct BlockQ {
-    uint32_t sb;      // E4M3 code
-    float sbf;        // its value
-    uint32_t c[16];   // E2M1 codes
+    uint32_t sb;
+    float sbf;
+    uint32_t w0, w1;
+    __device__ __forceinline__ uint32_t code(int t) const { return ((t < 8 ? w0 : w1) >> (4 * (t & 7))) & 15u; }
 };
+
+// four pairs of binary32 values -> four E2M1 byte pairs in one word
+__device__ __forceinline__ uint32_t e2m1x8(const float *q) {
+    uint32_t w;
+    asm("{ .reg .b8 b0, b1, b2, b3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        "mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(w)
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+    return w;
+}
 
 __device__ __forceinline__ void quant_block(const float (&v)[16], float gs, float p6, BlockQ &q) {
     float amax_b = 0.0f;
 #pragma unroll
     for (int t = 0; t < 16; ++t) amax_b = fmaxf(amax_b, fabsf(v[t]));
     // block scale: E4M3 of amax_b / (6*gs), RNE with saturation
-    float s = __fdiv_rn(amax_b, p6);
+    const float s = __fdiv_rn(amax_b, p6);
     q.sb = e4m3_from_f32(s);
     q.sbf = e4m3_to_f32(q.sb);
-    float den = __fmul_rn(q.sbf, gs);
+    const float den = __fmul_rn(q.sbf, gs);
     if (den != 0.0f) {
-        float inv = __frcp_rn(den);  // correctly rounded reciprocal
+        const float inv = __frcp_rn(den);  // correctly rounded reciprocal
+        float qv[16];
 #pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-            uint32_t pr = e2m1x2_from_f32(__fmul_rn(v[t], inv), __fmul_rn(v[t + 1], inv));
-            q.c[t] = pr & 15u;
-            q.c[t + 1] = pr >> 4;
+        for (int t = 0; t < 16; ++t) qv[t] = __fmul_rn(v[t], inv);
+        q.w0 = e2m1x8(qv);
+        q.w1 = e2m1x8(qv + 8);
+    } else {  // a zero block scale: signed zeros
+        uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            w0 |= ((__float_as_uint(v[t]) >> 31) << 3) << (4 * t);
+            w1 |= ((__float_as_uint(v[t + 8]) >> 31) << 3) << (4 * t);
         }
-    } else {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) q.c[t] = (__float_as_uint(v[t]) >> 31) << 3;  // signed zero
+        q.w0 = w0;
+        q.w1 = w1;
     }
 }
 
-__device__ __forceinline__ void load_block(const uint16_t *src, float (&v)[16]) {
-    const uint4 *p = reinterpret_cast<const uint4 *>(src);
-    uint4 a = __ldg(p), b = __ldg(p + 1);
-    uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+__device__ __forceinline__ void unpack_block(const uint4 &a, const uint4 &b, float (&v)[16]) {
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         v[2 * i] = __uint_as_float(w[i] << 16);
@@ -88,17 +113,27 @@ __device__ __forceinline__ void load_block(const uint16_t *src, float (&v)[16]) 
     }
 }
 
+constexpr int kQThreads = 256;
+constexpr int kQWarps = kQThreads / 32;
+constexpr int kMaxStagedK = 1024;  // residual row staged in shared memory up to this k
+
+// One warp per output row (grid-stride), looping over the row in segments of
+// 32 blocks (512 elements, one block per lane).  The RAC residual of the row
+// is gathered in shared memory and written once per destination row as
+// 16-byte chunks.
 template <int MODE>
-__global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
     __shared__ uint32_t s_mask[kMaxBlocksPerRow];
     __shared__ int32_t s_base[kMaxBlocksPerRow];
+    __shared__ __align__(16) uint16_t s_res[kQWarps][kMaxStagedK];
     const int tensor = blockIdx.y;
-    const int64_t nb = a.K >> 4;
+    const int nb = (int)(a.K >> 4);
     const int64_t kgroups = (nb + 3) >> 2;
     const bool has_sel = (MODE != kModeFake) && a.k > 0;
+    const bool staged = a.k <= kMaxStagedK;
 
     if (has_sel) {  // which elements of each block belong to S, and S's index of the first
-        for (int64_t b = threadIdx.x; b < nb; b += blockDim.x) s_mask[b] = 0u;
+        for (int b = threadIdx.x; b < nb; b += blockDim.x) s_mask[b] = 0u;
         __syncthreads();
         for (int s = threadIdx.x; s < a.k; s += blockDim.x) {
             int j = a.S[s];
@@ -116,111 +151,137 @@ __global__ void __launch_bounds__(256) quantize_kernel(QuantArgs a) {
         if (!isfinite(amax_t)) report(a.dev_status, NVFP4_ERR_NONFINITE);
     }
 
-    const int lane = threadIdx.x & 31;
-    const int64_t segs = (nb + 31) >> 5;
-    const int64_t nwarps_total = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int segs = (nb + 31) >> 5;
+    const int64_t nwarps_total = (int64_t)gridDim.x * kQWarps;
     const uint16_t *xt = a.x + (int64_t)tensor * a.x_tstride;
+    uint16_t *stage = s_res[wid];
+    const int fanout = (MODE == kModeAct) ? a.fanout : 1;
 
-    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < a.M * segs;
-         w += nwarps_total) {
-        const int64_t m = w / segs;  // output row (packed row in weight mode)
-        const int64_t b = (w - m * segs) * 32 + lane;
-        const bool valid = b < nb;
+    for (int64_t m = (int64_t)blockIdx.x * kQWarps + wid; m < a.M; m += nwarps_total) {
         int64_t src_row = m;
         if (MODE == kModeWeight && a.interleave) {
-            int64_t t = m >> 7, i = m & 127;
+            const int64_t t = m >> 7, i = m & 127;
             src_row = (i < 64) ? (t * 64 + i) : (a.M / 2 + t * 64 + (i - 64));
         }
-        float v[16];
-        BlockQ q;
-        if (valid) {
-            load_block(xt + src_row * a.ldx + b * 16, v);
-            quant_block(v, gs, p6, q);
+        // destination rows of this source row: lane f holds the f-th
+        int64_t my_dst = -1;
+        if (MODE == kModeAct) {
+            if (lane < fanout) my_dst = a.dst_row ? (int64_t)a.dst_row[m * fanout + lane] : m;
+            if (my_dst >= a.rows_out) my_dst = -1;  // a map entry outside the output is skipped
         } else {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) v[t] = 0.0f;
-            q.sb = 0u;
-            q.sbf = 0.0f;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) q.c[t] = 0u;
+            my_dst = m;
         }
+        const uint16_t *xrow = xt + src_row * a.ldx;
 
-        if (MODE == kModeFake) {
-            if (valid) {
-                uint32_t o[8];
-#pragma unroll
-                for (int t = 0; t < 16; t += 2) {
-                    float d0 = __fmul_rn(__fmul_rn(e2m1_to_f32(q.c[t]), q.sbf), gs);
-                    float d1 = __fmul_rn(__fmul_rn(e2m1_to_f32(q.c[t + 1]), q.sbf), gs);
-                    o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
-                               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(a.w_hat + (int64_t)tensor * a.what_tstride +
-                                                       m * a.K + b * 16);
-                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        // software pipeline: the next segment's 32 bytes are in flight while
+        // this one is quantized
+        uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
+        if (lane < nb) {
+            const uint4 *p0 = reinterpret_cast<const uint4 *>(xrow + lane * 16);
+            ra = __ldg(p0);
+            rb = __ldg(p0 + 1);
+        }
+        for (int seg = 0; seg < segs; ++seg) {
+            const int b = seg * 32 + lane;
+            const bool valid = b < nb;
+            const uint4 ca = ra, cb = rb;
+            if (seg + 1 < segs && b + 32 < nb) {
+                const uint4 *pn = reinterpret_cast<const uint4 *>(xrow + (b + 32) * 16);
+                ra = __ldg(pn);
+                rb = __ldg(pn + 1);
             }
-            continue;
-        }
+            float v[16];
+            BlockQ q;
+            if (valid) {
+                unpack_block(ca, cb, v);
+                quant_block(v, gs, p6, q);
+            } else {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v[t] = 0.0f;
+                q.sb = 0u;
+                q.sbf = 0.0f;
+                q.w0 = q.w1 = 0u;
+            }
 
-        // packed codes: element 2i in the low nibble
-        uint2 packed;
-        packed.x = q.c[0] | (q.c[1] << 4) | (q.c[2] << 8) | (q.c[3] << 12) | (q.c[4] << 16) |
-                   (q.c[5] << 20) | (q.c[6] << 24) | (q.c[7] << 28);
-        packed.y = q.c[8] | (q.c[9] << 4) | (q.c[10] << 8) | (q.c[11] << 12) | (q.c[12] << 16) |
-                   (q.c[13] << 20) | (q.c[14] << 24) | (q.c[15] << 28);
-        // four consecutive blocks' scales -> one 32-bit word (lane%4 == 0 stores)
-        uint32_t sw = q.sb;
-        uint32_t s1 = __shfl_down_sync(0xffffffffu, sw, 1);
-        uint32_t s2 = __shfl_down_sync(0xffffffffu, sw, 2);
-        uint32_t s3 = __shfl_down_sync(0xffffffffu, sw, 3);
-        sw = sw | (s1 << 8) | (s2 << 16) | (s3 << 24);
-        const bool group_lead = ((lane & 3) == 0) && (b < ((nb + 3) & ~3LL));
+            if (MODE == kModeFake) {
+                if (valid) {
+                    uint32_t o[8];
+#pragma unroll
+                    for (int t = 0; t < 16; t += 2) {
+                        const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
+                        const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
+                        o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
+                                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(a.w_hat + (int64_t)tensor * a.what_tstride + m * a.K + b * 16);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+                continue;
+            }
 
-        uint32_t mask = 0u;
-        int32_t base = 0;
-        if (has_sel && valid) {
-            mask = s_mask[b];
-            base = s_base[b];
-        }
+            // four consecutive blocks' scales -> one 32-bit word (lane%4 == 0 stores)
+            uint32_t sw = q.sb;
+            const uint32_t s1 = __shfl_down_sync(0xffffffffu, sw, 1);
+            const uint32_t s2 = __shfl_down_sync(0xffffffffu, sw, 2);
+            const uint32_t s3 = __shfl_down_sync(0xffffffffu, sw, 3);
+            sw = sw | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            const bool group_lead = ((lane & 3) == 0) && (b < ((nb + 3) & ~3));
 
-        if (MODE == kModeWeight) {
+            // residual (activation) or unscaled dequantized weight on S
+            if (has_sel && valid) {
+                const uint32_t mask = s_mask[b];
+                if (mask) {
+                    const int base = s_base[b];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        if (mask & (1u << t)) {
+                            const int si = base + __popc(mask & ((1u << t) - 1u));
+                            const float cs = __fmul_rn(e2m1_val(q.code(t)), q.sbf);  // exact
+                            uint16_t val;
+                            if (MODE == kModeWeight) {
+                                val = __bfloat16_as_ushort(__float2bfloat16_rn(cs));
+                            } else {
+                                const float xq = __fmul_rn(cs, gs);
+                                val = __bfloat16_as_ushort(__float2bfloat16_rn(__fsub_rn(v[t], xq)));
+                            }
+                            if (staged) {
+                                stage[si] = val;
+                            } else if (MODE == kModeWeight) {
+                                a.wsel[(int64_t)tensor * a.wsel_tstride + m * a.k + si] = val;
+                            } else {
+                                for (int f = 0; f < fanout; ++f) {  // divergent here: read the map directly
+                                    const int64_t dm = a.dst_row ? (int64_t)a.dst_row[m * fanout + f] : m;
+                                    if (dm >= 0 && dm < a.rows_out) a.resid[dm * a.k + si] = val;
+                                }
+                            }
+                        }
+                }
+            }
+
             uint8_t *codes = a.codes + (int64_t)tensor * a.codes_tstride;
             uint8_t *scales = a.scales + (int64_t)tensor * a.scales_tstride;
-            if (valid) *reinterpret_cast<uint2 *>(codes + m * (a.K >> 1) + b * 8) = packed;
-            if (group_lead) *reinterpret_cast<uint32_t *>(scales + swz_offset(m, b, kgroups)) = sw;
-            if (mask) {
-                uint16_t *wsel = a.wsel + (int64_t)tensor * a.wsel_tstride + m * a.k;
-#pragma unroll
-                for (int t = 0; t < 16; ++t)
-                    if (mask & (1u << t)) {
-                        const int s = base + __popc(mask & ((1u << t) - 1u));
-                        const float cs = __fmul_rn(e2m1_to_f32(q.c[t]), q.sbf);  // exact
-                        wsel[s] = __bfloat16_as_ushort(__float2bfloat16_rn(cs));
-                    }
+            for (int f = 0; f < fanout; ++f) {
+                const int64_t dm = __shfl_sync(0xffffffffu, my_dst, f);
+                if (dm < 0) continue;
+                if (valid) *reinterpret_cast<uint2 *>(codes + dm * (a.K >> 1) + b * 8) = make_uint2(q.w0, q.w1);
+                if (group_lead) *reinterpret_cast<uint32_t *>(scales + swz_offset(dm, b, kgroups)) = sw;
             }
-            continue;
         }
 
-        // activation mode: codes and scales to every routed row of this row
-        for (int f = 0; f < a.fanout; ++f) {
-            const int64_t dm = a.dst_row ? (int64_t)a.dst_row[m * a.fanout + f] : m;
-            if (dm < 0 || dm >= a.rows_out) continue;  // a map entry outside the output is skipped
-            if (valid) *reinterpret_cast<uint2 *>(a.codes + dm * (a.K >> 1) + b * 8) = packed;
-            if (group_lead) *reinterpret_cast<uint32_t *>(a.scales + swz_offset(dm, b, kgroups)) = sw;
-        }
-        if (mask) {  // residual r = bf16(x - (code*sb)*gs) on the selected channels
-#pragma unroll
-            for (int t = 0; t < 16; ++t)
-                if (mask & (1u << t)) {
-                    const int s = base + __popc(mask & ((1u << t) - 1u));
-                    const float xq = __fmul_rn(__fmul_rn(e2m1_to_f32(q.c[t]), q.sbf), gs);
-                    const uint16_t r = __bfloat16_as_ushort(__float2bfloat16_rn(__fsub_rn(v[t], xq)));
-                    for (int f = 0; f < a.fanout; ++f) {
-                        const int64_t dm = a.dst_row ? (int64_t)a.dst_row[m * a.fanout + f] : m;
-                        if (dm >= 0 && dm < a.rows_out) a.resid[dm * a.k + s] = r;
-                    }
-                }
+        if (has_sel && staged) {  // the row's k residual values -> every destination row
+            __syncwarp();
+            const int chunks = a.k >> 3;  // 16-byte chunks (k % 8 == 0)
+            const uint4 *src = reinterpret_cast<const uint4 *>(stage);
+            for (int f = 0; f < fanout; ++f) {
+                const int64_t dm = __shfl_sync(0xffffffffu, my_dst, f);
+                if (dm < 0) continue;
+                uint16_t *row = (MODE == kModeWeight) ? a.wsel + (int64_t)tensor * a.wsel_tstride + dm * a.k
+                                                      : a.resid + dm * a.k;
+                for (int c = lane; c < chunks; c += 32) reinterpret_cast<uint4 *>(row)[c] = src[c];
+            }
+            __syncwarp();
         }
     }
 }
@@ -382,9 +443,8 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, in
     }
 }
 
-static int quant_grid(int64_t rows, int64_t nb) {
-    int64_t warps = rows * ((nb + 31) / 32);
-    int64_t blocks = (warps + 7) / 8;
+static int quant_grid(int64_t rows) {
+    int64_t blocks = (rows + kQWarps - 1) / kQWarps;
     int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     return (int)(blocks < 1 ? 1 : blocks);
@@ -449,7 +509,7 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
     a.scales = scales;
     a.resid = (uint16_t *)resid;
     a.dev_status = dev_status;
-    quantize_kernel<kModeAct><<<quant_grid(M, K / 16), 256, 0, (cudaStream_t)stream>>>(a);
+    quantize_kernel<kModeAct><<<quant_grid(M), kQThreads, 0, (cudaStream_t)stream>>>(a);
     return launch_status("quantize_kernel");
 }
 
@@ -474,8 +534,8 @@ extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t
     a.w_hat = (uint16_t *)w_hat;
     a.what_tstride = rows * cols;
     a.dev_status = dev_status;
-    int g = quant_grid(rows, cols / 16) / (nt > 8 ? 8 : nt);
-    quantize_kernel<kModeFake><<<dim3(g < 1 ? 1 : g, nt), 256, 0, st>>>(a);
+    int g = quant_grid(rows) / (nt > 8 ? 8 : nt);
+    quantize_kernel<kModeFake><<<dim3(g < 1 ? 1 : g, nt), kQThreads, 0, st>>>(a);
     return launch_status("quantize_kernel<fake>");
 }
 
@@ -511,8 +571,8 @@ extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_
     a.wsel_tstride = N * (int64_t)k;
     a.interleave = interleave;
     a.dev_status = dev_status;
-    int g = quant_grid(N, K / 16) / (E > 8 ? 8 : E);
-    quantize_kernel<kModeWeight><<<dim3(g < 1 ? 1 : g, E), 256, 0, st>>>(a);
+    int g = quant_grid(N) / (E > 8 ? 8 : E);
+    quantize_kernel<kModeWeight><<<dim3(g < 1 ? 1 : g, E), kQThreads, 0, st>>>(a);
     return launch_status("quantize_kernel<weight>");
 }
 
