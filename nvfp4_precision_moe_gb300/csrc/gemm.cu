@@ -11,11 +11,17 @@
 //
 // Tiles are 128 rows x 128 columns of the output; the K loop moves 128-byte
 // wide K-slices (256 FP4 or 64 BF16 elements) through a ring of shared-memory
-// stages fed by TMA (128-byte swizzle).  Warp roles per CTA (320 threads):
-//   warp 0     TMA producer (one lane)
-//   warp 1     TMEM owner + MMA issuer (one lane)
-//   warps 2-9  epilogue: warp w reads TMEM lane quarter w%4 and column half
-//              (w-2)/4 of the tile, scales, applies SwiGLU, stores.
+// stages fed by TMA (128-byte swizzle).  Warp roles per CTA (448 threads):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM owner + MMA issuer (one lane)
+//   warps 2-5   scale warps (FP4): once a stage has landed, each writes the
+//               stage's block scales into its 32-lane quarter of tensor
+//               memory with tcgen05.st, replicated as the block-scaled MMA
+//               reads them.  (Copying them with tcgen05.cp instead occupies
+//               the tensor pipe between MMAs and costs about two thirds of
+//               the MMA rate.)
+//   warps 6-13  epilogue: warp w reads TMEM lane quarter w%4 and column half
+//               (w-6)/4 of the tile, scales, applies SwiGLU, stores.
 // Tensor memory (512 columns): the main accumulator is double-buffered
 // (columns 0-127 and 128-255), so the epilogue of one tile overlaps the MMAs
 // of the next; the RAC accumulator (256-383) is single-buffered and its MMAs
@@ -36,7 +42,9 @@ constexpr uint32_t kAccMain0 = 0, kAccRes = 256, kSFCol0 = 384;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxExperts = 1024;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kSFWarps = 4;
+constexpr int kEpiWarp0 = 2 + kSFWarps;
+constexpr int kThreads = 64 + 32 * kSFWarps + 32 * kEpiWarps;
 
 // Instruction descriptors (M = 128, N = 128, both operands K-major).
 //  kind::mxf4nvf4: A, B = E2M1 (1) at bits 7-9 / 10-12, N>>3 at 17, scale
@@ -50,8 +58,8 @@ struct Cfg {
     static constexpr int kStages = FP4 ? 4 : 6;
     static constexpr int kStageBytes = 2 * kTileBytes + (FP4 ? 2 * kSFBytes : 0);
     static constexpr int kBarOffset = kStages * kStageBytes;
-    // barriers: full/empty per stage, acc_full[2], acc_empty[2], res_empty, drain
-    static constexpr int kNumBars = 2 * kStages + 6;
+    // barriers: full/empty/sf_ready per stage, acc_full[2], acc_empty[2], res_empty, drain
+    static constexpr int kNumBars = 3 * kStages + 6;
     static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
     static constexpr int kGswOffset = kOffOffset + (kMaxExperts + 1) * 4;
     static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
@@ -105,7 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
     uint64_t *empty = full + C::kStages;
-    uint64_t *acc_full = empty + C::kStages;  // [2]
+    uint64_t *sf_ready = empty + C::kStages;  // [kStages]
+    uint64_t *acc_full = sf_ready + C::kStages;  // [2]
     uint64_t *acc_empty = acc_full + 2;       // [2]
     uint64_t *res_empty = acc_empty + 2;
     uint64_t *drain = res_empty + 1;
@@ -123,6 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], kSFWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_full[b], 1);
@@ -255,12 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (it < nkt) {
                         if (FP4) {
                             const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * 32u;
-                            const uint32_t sfa_s = b_addr + kTileBytes, sfb_s = sfa_s + kSFBytes;
-#pragma unroll
-                            for (int c = 0; c < 4; ++c) {
-                                tc_cp_sf(sf + 4 * c, desc_sf(sfa_s + 512 * c));
-                                tc_cp_sf(sf + 16 + 4 * c, desc_sf(sfb_s + 512 * c));
+                            // the scale warps have written this stage's scales
+                            if (!mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
+                                ok = false;
+                                break;
                             }
+                            tc_fence_after();
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
                                 tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
@@ -296,9 +306,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_commit(drain);
             (void)mbar_wait_bounded(drain, 0, kWaitLimitNs);
         }
+    } else if (warp < kEpiWarp0) {
+        // ---------------------------------------------------- scale warps
+        // Slice by slice in the producer's order: wait for the stage, then
+        // write its 8 scale chunks (SFA then SFB, 512 bytes each: 32 rows of
+        // 16 bytes) into this warp's lane quarter: lane i, column 4c + j gets
+        // word j of row i of chunk c.  Every quarter holds the same copy.
+        if (FP4) {
+            const uint32_t q = (uint32_t)(warp & 3);
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+                bool ok = true;
+                for (int it = 0; it < nkt + nrt; ++it) {
+                    const bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    if (it < nkt) {
+                        const uint8_t *sfs = smem + stage * C::kStageBytes + 2 * kTileBytes;
+                        uint32_t r[32];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 w = *reinterpret_cast<const uint4 *>(sfs + 512 * c + 16 * lane);
+                            r[4 * c] = w.x;
+                            r[4 * c + 1] = w.y;
+                            r[4 * c + 2] = w.z;
+                            r[4 * c + 3] = w.w;
+                        }
+                        tmem_st32(tmem + ((q * 32u) << 16) + kSFCol0 + (uint32_t)stage * 32u, r);
+                        tmem_st_wait();
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sf_ready[stage]);
+                    if (++stage == C::kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) {
+                    if (lane == 0) {
+                        report(p.dev_status, NVFP4_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
+            }
+        }
     } else {
         // ---------------------------------------------------- epilogue
-        const int ew = warp - 2;             // 0..7
+        const int ew = warp - kEpiWarp0;     // 0..7
         const int q = warp & 3;              // TMEM lane quarter this warp may access
         const int half = ew >> 2;            // which half of the tile's columns
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
