@@ -126,6 +126,28 @@ int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float
 int nvfp4_fake_quant(const void *w, int32_t ntensors, int64_t rows, int64_t cols, void *w_hat,
                      float *gs_out, float *amax_ws, int32_t *dev_status, void *stream);
 
+/* nvfp4_fake_quant for callers that cannot allocate device memory.  The paper
+ * has no counterpart; this is a convenience of the library.  A framework that
+ * owns all device memory through its own pool, or a latency-critical loop
+ * that must not call cudaMalloc/cudaFree (which can stall the whole device),
+ * cannot provide the amax scratch that nvfp4_fake_quant asks for.  This
+ * variant takes the same arguments minus `amax_ws` and computes the same
+ * w_hat and gs_out (bit for bit), using a fixed array of 4096 floats that the
+ * library declares in device memory (16 KB held on every GPU that loads the
+ * library, until the process exits).  Nothing is allocated by the call.
+ *   - ntensors must be <= 4096: larger calls return NVFP4_ERR_UNSUPPORTED
+ *     (nvfp4_last_error() says why) and launch nothing.
+ *   - The first call on a device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call
+ *     before any stream capture begins.
+ *   - Every call shares the one array: the slots a call uses are cleared on
+ *     `stream` before use, and keep that call's amax values afterwards.  Calls
+ *     whose work can overlap on the GPU (different streams without ordering
+ *     between them, or several host threads) race on the array and must be
+ *     serialized by the caller. */
+int nvfp4_fake_quant_noalloc(const void *w, int32_t ntensors, int64_t rows, int64_t cols,
+                             void *w_hat, float *gs_out, int32_t *dev_status, void *stream);
+
 /* Rollout weight preparation, once per weight update (QUADS §3.2 Eq. 15: the
  * rollout loads the trainer's weights): per expert e of w [E, N, K] BF16,
  * NVFP4-quantize with the expert's own gs and gather the dequantized,

@@ -30,6 +30,7 @@ _SIGS = {
     "nvfp4_amax": "pqqqiqpp",
     "nvfp4_quantize": "pqqqpppipiqppppp",
     "nvfp4_fake_quant": "piqqppppp",
+    "nvfp4_fake_quant_noalloc": "piqqpppp",
     "nvfp4_prepare_weights": "piqqpiippppppp",
     "nvfp4_rac_select_channels": "pqqpippp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
@@ -128,6 +129,13 @@ def nvfp4_fake_quant(w, w_hat, amax_ws, gs_out=None, dev_status=None, stream=Non
     nt, rows, cols = w.shape
     _call("nvfp4_fake_quant", _p(w), nt, rows, cols, _p(w_hat), _p(gs_out), _p(amax_ws),
           _p(dev_status), _s(stream))
+
+
+def nvfp4_fake_quant_noalloc(w, w_hat, gs_out=None, dev_status=None, stream=None):
+    """A16 without caller scratch: the library's own fixed array (<= 4096 tensors)."""
+    nt, rows, cols = w.shape
+    _call("nvfp4_fake_quant_noalloc", _p(w), nt, rows, cols, _p(w_hat), _p(gs_out), _p(dev_status),
+          _s(stream))
 
 
 def nvfp4_prepare_weights(w, w_codes, w_scales, gs_w, amax_ws, S=None, w_sel=None, interleave=0,

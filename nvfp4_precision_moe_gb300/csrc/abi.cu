@@ -13,6 +13,8 @@ void set_last_error(const char *what, cudaError_t e) {
     snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, cudaGetErrorString(e));
 }
 
+void set_last_error_text(const char *text) { snprintf(g_last_error, sizeof(g_last_error), "%s", text); }
+
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static int g_dev_ok[64];   // 0 unknown, 1 ok, 2 not sm_103
 static int g_dev_sms[64];

@@ -18,6 +18,8 @@ namespace nvfp4 {
 
 // Records the CUDA error text for nvfp4_last_error().
 void set_last_error(const char *what, cudaError_t e);
+// Records a plain message for nvfp4_last_error().
+void set_last_error_text(const char *text);
 // nvfp4_init() plus "is the current device an sm_103 part" (cached per device).
 int ensure_init();
 // Number of SMs of the current device (cached).

@@ -10,6 +10,8 @@
 // 16-element block (32 bytes of BF16 in, 8 bytes of codes out), so a warp
 // reads 1 KB contiguous and writes 256 B of codes contiguous.  Four lanes
 // pack their block scales into one 32-bit store of the swizzled layout.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace nvfp4 {
@@ -621,4 +623,61 @@ extern "C" int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, co
     if (s != NVFP4_OK || k == 0) return s;
     select_topk_kernel<<<1, 1024, 0, st>>>(score_ws, K, k, S_out);
     return launch_status("select_topk_kernel");
+}
+
+// ---------------------------------------------------------------------------
+// Fake-quant without any allocation by the caller.
+//
+// Some callers cannot hand the library a scratch buffer: a host framework
+// that owns all device memory through its own pool (a raw cudaMalloc would
+// bypass its accounting and can fail once the pool has reserved the GPU), or a
+// latency-critical loop that must not call cudaMalloc/cudaFree (cudaFree waits
+// for the whole device).  nvfp4_fake_quant needs ntensors floats of scratch
+// for the per-tensor amax; this variant keeps them in a fixed array in device
+// memory that the library itself declares, so nothing is allocated at call time.
+namespace nvfp4 {
+constexpr int kNoAllocMaxTensors = 4096;  // 16 KB per GPU that loads the library
+static __device__ __align__(256) float g_noalloc_amax[kNoAllocMaxTensors];
+static float *g_noalloc_addr[64];  // device address of the array, per device
+static std::mutex g_noalloc_mu;
+
+// The array's name in host code is not a device address: look the address up
+// once per device, with that device current, and pass it to the kernels.
+static int noalloc_scratch(float **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        set_last_error("cudaGetDevice", e);
+        return NVFP4_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_amax);
+        if (e != cudaSuccess || !p) {
+            set_last_error("cudaGetSymbolAddress(no-alloc scratch)", e);
+            return NVFP4_ERR_CUDA;
+        }
+        g_noalloc_addr[dev] = static_cast<float *>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return NVFP4_OK;
+}
+}  // namespace nvfp4
+
+extern "C" int nvfp4_fake_quant_noalloc(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat,
+                                        float *gs_out, int32_t *dev_status, void *stream) {
+    if (!w || !w_hat || nt < 1 || rows < 0 || cols < 0) return NVFP4_ERR_INVALID_ARG;
+    if (nt > kNoAllocMaxTensors) {
+        set_last_error_text("nvfp4_fake_quant_noalloc: more than 4096 tensors in one call");
+        return NVFP4_ERR_UNSUPPORTED;
+    }
+    if (cols % 32 || cols / 16 > kMaxBlocksPerRow) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(w_hat)) return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    float *scratch = nullptr;
+    const int s = noalloc_scratch(&scratch);
+    if (s != NVFP4_OK) return s;
+    // the amax slots are cleared on `stream` before use (inside nvfp4_fake_quant)
+    return nvfp4_fake_quant(w, nt, rows, cols, w_hat, gs_out, scratch, dev_status, stream);
 }
