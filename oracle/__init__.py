@@ -52,8 +52,8 @@ def lib():
             "orc_dequantize_f32": (None, [_u8p, _u8p, _i64, _i64, ctypes.c_float, _f32p]),
             "orc_swizzle_scales": (None, [_u8p, _i64, _i64, _u8p]),
             "orc_fake_quant": (None, [_u16p, _i64, _i64, _u16p, ctypes.POINTER(ctypes.c_float)]),
-            "orc_rac_gemm": (None, [_f64p, ctypes.c_void_p, ctypes.c_void_p, _i32, _f64p,
-                                    _i64, _i64, _i64, _f64p]),
+            "orc_rac_gemm": (None, [_f64p, ctypes.c_void_p, ctypes.c_void_p, _i32, ctypes.c_double,
+                                    _f64p, _i64, _i64, _i64, _f64p]),
             "orc_bf16_gemm": (None, [_u16p, _u16p, _i64, _i64, _i64, _f64p]),
             "orc_channel_scores": (None, [_u16p, _i64, _i64, ctypes.c_float, _f64p]),
             "orc_select_channels": (None, [_f64p, _i64, _i32, _i32p]),
@@ -128,7 +128,8 @@ def amax(x):
 
 
 def tensor_scale(a):
-    """Per-tensor FP32 scale gs = amax / 2688 (1 for an all-zero tensor)."""
+    """Per-tensor FP32 scale: the smallest power of two >= fl(amax / 2688)
+    (1 for an all-zero tensor)."""
     return float(np.float32(lib().orc_tensor_scale(float(a))))
 
 
@@ -136,7 +137,8 @@ def quantize(x, gs=None, S=None):
     """NVFP4 quantize of a BF16 matrix [M,K] (QUADS §2.2, Eq. 9 / Eq. 20).
 
     Returns (codes [M,K/2] u8, scales [M,K/16] u8 canonical, resid [M,k] u16
-    bf16 bits, gs float).  gs defaults to the tensor scale of x's amax.
+    bf16 bits of the residual in units of gs, gs float).  gs defaults to the
+    tensor scale of x's amax.
     """
     x = _c(x, np.uint16)
     M, K = x.shape
@@ -201,11 +203,12 @@ def fake_quant(w):
 
 # ----------------------------------------------------------------- GEMMs --
 
-def rac_gemm(xq, wq, resid=None, S=None):
+def rac_gemm(xq, wq, resid=None, S=None, gs_a=1.0):
     """W4A4 + RAC product (QUADS §3.3 Eq. 21), binary64.
 
     xq [M,K], wq [N,K]: exact dequantized operands (float64);
-    resid [M,k] bf16 bits on channels S.  Returns float64 [M,N].
+    resid [M,k] bf16 bits on channels S, in units of gs_a (as quantize()
+    returns it).  Returns float64 [M,N].
     """
     xq = _c(xq, np.float64)
     wq = _c(wq, np.float64)
@@ -215,7 +218,7 @@ def rac_gemm(xq, wq, resid=None, S=None):
     Sa = _c(S, np.int32) if k else None
     ra = _c(resid, np.uint16) if k else None
     y = np.empty((M, N), np.float64)
-    lib().orc_rac_gemm(xq, _ptr(ra), _ptr(Sa), k, wq, M, N, K, y)
+    lib().orc_rac_gemm(xq, _ptr(ra), _ptr(Sa), k, float(gs_a), wq, M, N, K, y)
     return y
 
 

@@ -152,13 +152,22 @@ float orc_amax(const uint16_t *x, int64_t M, int64_t K, int64_t ldx)
     return m;
 }
 
-/* The optional FP32 per-tensor scale of §2.2.  Reading: gs = amax / (6*448),
- * so the largest block of the tensor gets a block scale of 448 (the E4M3
- * maximum) before rounding; an all-zero tensor gets gs = 1. */
+/* The optional FP32 per-tensor scale of §2.2.  Reading: the smallest power of
+ * two not below fl(amax / (6*448)), so every block scale target
+ * amax16 / (6*gs) is at most 448 (the E4M3 maximum) and the largest block's
+ * lies in (224, 448]; an all-zero tensor gets gs = 1.  A power of two keeps
+ * (code*sb)*gs exact and lets the RAC residual be carried exactly in units
+ * of gs (see orc_quantize). */
 float orc_tensor_scale(float amax)
 {
+    float q;
+    int e;
+    double f;
     if (amax == 0.0f) return 1.0f;
-    return amax / 2688.0f;
+    q = amax / 2688.0f;
+    f = frexp((double)q, &e); /* q = f * 2^e, f in [0.5, 1) */
+    if (f == 0.5) return q;   /* already a power of two */
+    return (float)ldexp(1.0, e);
 }
 
 /* The E4M3 block scale of one 16-element block.  Reading: the block scale is
@@ -197,10 +206,13 @@ static float element_dequant(int code, float sbf, float gs)
  * consecutive elements share an E4M3 block scale").
  *   codes  [M, K/2]  two E2M1 codes per byte, element 2i in the low nibble
  *   scales [M, K/16] E4M3 block-scale codes, row-major (canonical layout)
- *   resid  [M, k]    for the channels S[0..k) (strictly increasing):
- *                    r = bf16(x - dequant(q(x))), the negative of the
- *                    activation quantization error Delta X_q of Eq. 9 / Eq. 20,
- *                    which Residual Activation Compensation (Eq. 21) adds back.
+ *   resid  [M, k]    for the channels S[0..k) (strictly increasing): the
+ *                    residual r = bf16(x - dequant(q(x))) -- the negative of
+ *                    the activation quantization error Delta X_q of Eq. 9 /
+ *                    Eq. 20, which Residual Activation Compensation (Eq. 21)
+ *                    adds back -- stored in units of gs: bf16(r * (1/gs)).
+ *                    With gs a power of two this is r / gs exactly (unless it
+ *                    falls below the BF16 normal range).
  * gs is the per-tensor scale (orc_tensor_scale of the tensor's amax).
  */
 void orc_quantize(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, float gs,
@@ -236,7 +248,8 @@ void orc_quantize(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, float gs
             int64_t j = S[s];
             float xv = orc_bf16_value(x[i * ldx + j]);
             float d = xv - xq_row[j];
-            resid[i * (int64_t)k + s] = orc_bf16_round(d);
+            float r = orc_bf16_value(orc_bf16_round(d));
+            resid[i * (int64_t)k + s] = orc_bf16_round(r * (1.0f / gs));
         }
     }
     free(xq_row);
@@ -314,13 +327,14 @@ void orc_fake_quant(const uint16_t *w, int64_t M, int64_t K, uint16_t *w_hat, fl
 
 /*
  * W4A4 + RAC product for one expert, accumulated in binary64:
- *   y[i,n] = sum_K xq[i,K] * wq[n,K]  +  sum_{s<k} r[i,s] * wq[n, S[s]]
+ *   y[i,n] = sum_K xq[i,K] * wq[n,K]  +  sum_{s<k} (gs_a * r[i,s]) * wq[n, S[s]]
  * xq, wq: exact dequantized operands [M,K], [N,K] (orc_dequantize_exact);
- * r: the BF16 residual [M,k] on channels S.  The first sum is the native
+ * r: the BF16 residual [M,k] on channels S in units of the activation's
+ * per-tensor scale gs_a (orc_quantize's resid).  The first sum is the native
  * W4A4 GEMM; the second is the rank-k correction on the selected channels
  * (Eq. 21, with the residual kept in BF16 and the weight dequantized NVFP4).
  */
-void orc_rac_gemm(const double *xq, const uint16_t *r, const int32_t *S, int32_t k,
+void orc_rac_gemm(const double *xq, const uint16_t *r, const int32_t *S, int32_t k, double gs_a,
                   const double *wq, int64_t M, int64_t N, int64_t K, double *y)
 {
     for (int64_t i = 0; i < M; i++)
@@ -328,7 +342,7 @@ void orc_rac_gemm(const double *xq, const uint16_t *r, const int32_t *S, int32_t
             double acc = 0.0;
             for (int64_t j = 0; j < K; j++) acc += xq[i * K + j] * wq[n * K + j];
             for (int32_t s = 0; s < k; s++)
-                acc += (double)orc_bf16_value(r[i * (int64_t)k + s]) * wq[n * K + S[s]];
+                acc += gs_a * (double)orc_bf16_value(r[i * (int64_t)k + s]) * wq[n * K + S[s]];
             y[i * N + n] = acc;
         }
 }

@@ -31,8 +31,8 @@ def test_rac_gemm_matches_numpy_matmul():
     cw, sw, _, gw = oracle.quantize(w)
     xq = oracle.dequantize_exact(ca, sa, ga)
     wq = oracle.dequantize_exact(cw, sw, gw)
-    y = oracle.rac_gemm(xq, wq, r, S)
-    ref = xq @ wq.T + oracle.bf16_to_f32(r).astype(np.float64) @ wq[:, S].T
+    y = oracle.rac_gemm(xq, wq, r, S, ga)
+    ref = xq @ wq.T + (ga * oracle.bf16_to_f32(r).astype(np.float64)) @ wq[:, S].T
     assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
 
 
@@ -60,11 +60,11 @@ def test_all_channels_reproduces_w4a16():
     cw, sw, _, gw = oracle.quantize(w)
     xq = oracle.dequantize_exact(ca, sa, ga)
     wq = oracle.dequantize_exact(cw, sw, gw)
-    y = oracle.rac_gemm(xq, wq, r, S)
+    y = oracle.rac_gemm(xq, wq, r, S, ga)
     xf = oracle.bf16_to_f32(x).astype(np.float64)
     w4a16 = xf @ wq.T
     # error of the compensated activation, element by element
-    err = np.abs(xq + oracle.bf16_to_f32(r) - xf)
+    err = np.abs(xq + ga * oracle.bf16_to_f32(r) - xf)
     bound = err @ np.abs(wq).T
     assert np.all(np.abs(y - w4a16) <= bound * (1 + 1e-9) + 1e-12)
     # the bound is much smaller than the uncompensated W4A4 error
@@ -84,9 +84,9 @@ def test_all_channels_exact_case():
     ca, sa, r, _ = oracle.quantize(x, gs=gs, S=S)
     xq32 = oracle.dequantize_f32(ca, sa, gs).astype(np.float64)
     xf = oracle.bf16_to_f32(x).astype(np.float64)
-    assert np.array_equal(oracle.bf16_to_f32(r).astype(np.float64), xf - xq32)
+    assert np.array_equal(gs * oracle.bf16_to_f32(r).astype(np.float64), xf - xq32)
     wq = rng.integers(-6, 7, (8, K)).astype(np.float64)
-    y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, gs), wq, r, S)
+    y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, gs), wq, r, S, gs)
     assert np.array_equal(y, xf @ wq.T)
 
 

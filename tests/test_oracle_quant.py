@@ -145,18 +145,33 @@ def test_zero_tensor():
     assert not codes.any() and not scales.any() and not resid.any()
 
 
+def test_tensor_scale_is_a_power_of_two_bounding_every_block_scale():
+    rng = np.random.default_rng(16)
+    for a in list(np.exp(rng.uniform(-40, 40, 2000)).astype(np.float32)) + [2688.0, 168.0, 1.0, 5376.0001]:
+        gs = oracle.tensor_scale(float(a))
+        m, e = np.frexp(gs)
+        assert m == 0.5  # a power of two
+        q = np.float32(a) / np.float32(2688.0)
+        # the smallest power of two not below fl(amax / 2688)
+        assert gs >= q and gs / 2 < q
+    assert oracle.tensor_scale(0.0) == 1.0
+
+
 def test_residual_definition_and_eq22():
     x = synth.u16(synth.activations(1))
     S = np.array(sorted(np.random.default_rng(6).choice(512, 16, replace=False)), np.int32)
     codes, scales, resid, gs = oracle.quantize(x, S=S)
     xq = oracle.dequantize_f32(codes, scales, gs)
     xf = oracle.bf16_to_f32(x)
-    # r = bf16(x - xq) on the channels S (Eq. 20 with the sign of -Delta X_q)
-    want = torch.from_numpy((xf[:, S] - xq[:, S]).astype(np.float32)).to(torch.bfloat16)
+    # r = bf16(x - xq) on the channels S (Eq. 20 with the sign of -Delta X_q),
+    # stored in units of gs: gs is a power of two, so this is exact here
+    r = torch.from_numpy((xf[:, S] - xq[:, S]).astype(np.float32)).to(torch.bfloat16).float().numpy()
+    want = torch.from_numpy((r / np.float32(gs)).astype(np.float32)).to(torch.bfloat16)
     assert np.array_equal(resid, want.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(oracle.bf16_to_f32(resid).astype(np.float64) * gs, r.astype(np.float64))
     # Eq. 22: compensating S strictly lowers the distance to X
     xt = xq.astype(np.float64).copy()
-    xt[:, S] += oracle.bf16_to_f32(resid)
+    xt[:, S] += gs * oracle.bf16_to_f32(resid)
     e_plain = np.linalg.norm(xq.astype(np.float64) - xf)
     e_rac = np.linalg.norm(xt - xf)
     assert e_rac < e_plain
@@ -170,6 +185,9 @@ def test_fake_quant_equals_dequant_of_quant():
     assert gs == gs2
     deq = oracle.dequantize_f32(codes, scales, gs)
     assert np.array_equal(w_hat, oracle.bf16_round(deq))
+    # with a power-of-two gs nothing rounds: W_hat is exactly code * sb * gs,
+    # the value the rollout GEMM multiplies (Eq. 16: zero weight mismatch)
+    assert np.array_equal(oracle.bf16_to_f32(w_hat).astype(np.float64), oracle.dequantize_exact(codes, scales, gs))
 
 
 def test_swizzle_is_a_bijection_with_zero_padding():
