@@ -276,10 +276,10 @@ def cpu_baseline(seconds=12.0, rows=None):
     wq13, wqd = _ORACLE_WEIGHTS["w"]
     t0 = time.perf_counter()
     ca, sa, ra, ga = oracle.quantize(x, S=S13)
-    y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, ga), wq13, ra, S13)
+    y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, ga), wq13, ra, S13, ga)
     h = oracle.bf16_round(oracle.swiglu(y, I).astype(np.float32))
     ch, sh, rh, gh = oracle.quantize(h, S=Sd)
-    oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gh), wqd, rh, Sd)
+    oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gh), wqd, rh, Sd, gh)
     dt = time.perf_counter() - t0
     fl = 2 * n * (2 * I) * (H + k) + 2 * n * H * (I + k)
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",

@@ -32,8 +32,10 @@
  *           (m%32)*16 + ((m%128)/32)*4 + kb%4.  Size:
  *           ceil(rows/128)*128 * ceil(K/64)*4 bytes; unused bytes are 0.
  *           This is the layout the block-scaled tensor-core MMA reads.
- *  - gs     FP32 per-tensor scale, gs = amax/2688 (amax = max|x| over the
- *           tensor; 2688 = 6*448), gs = 1 for an all-zero tensor.
+ *  - gs     FP32 per-tensor scale: the smallest power of two not below
+ *           fl(amax/2688) (amax = max|x| over the tensor; 2688 = 6*448), so
+ *           every block-scale target amax16/(6*gs) is at most 448; gs = 1 for
+ *           an all-zero tensor.
  *  - value  of element (m, j) = e2m1(code) * e4m3(scale) * gs.
  */
 #ifndef NVFP4MOE_H
@@ -89,7 +91,7 @@ int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensor
 /* NVFP4 quantize of a BF16 activation matrix x [M, K] (row stride ldx) with
  * the RAC residual of QUADS §3.3 Eq. 20-21 on a fixed channel set S.
  *   amax        device float: the tensor's amax (from nvfp4_amax, or any
- *               caller value); gs = amax/2688 (1 if amax == 0).
+ *               caller value); gs = its power-of-two tensor scale (see top).
  *   gs_out      device float or NULL: receives gs.
  *   S, k        device int32[k], strictly increasing channel indices < K,
  *               0 <= k <= K, k % 8 == 0 (k = 0: no residual; S may be NULL).
@@ -100,8 +102,11 @@ int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensor
  *   rows_out    number of output rows (>= M when dst_row is NULL).
  *   codes       device uint8 [rows_out, K/2]
  *   scales      device uint8, swizzled layout for rows_out rows (see top)
- *   resid       device BF16 [rows_out, k]: r = bf16(x - dequant(q(x))) on S,
- *               i.e. minus the quantization error Delta X_q of Eq. 20.
+ *   resid       device BF16 [rows_out, k]: the residual r = bf16(x -
+ *               dequant(q(x))) on S -- minus the quantization error Delta X_q
+ *               of Eq. 20 -- in units of gs: bf16(r * (1/gs)), which is r/gs
+ *               exactly (gs is a power of two) unless it falls below the BF16
+ *               normal range.  The GEMM multiplies it by gs again.
  * Per element: block scale sb = e4m3_rn_sat(amax16 / (6*gs)); den = sb*gs;
  * code = e2m1_rn_sat(x * (1/den)) with 1/den correctly rounded (a zero den
  * gives a signed zero code); dequant = (code*sb)*gs in binary32.
@@ -159,10 +164,11 @@ int nvfp4_fake_quant_noalloc(const void *w, int32_t ntensors, int64_t rows, int6
  *               (exact in BF16; the GEMM multiplies by gs_w[e])
  *   amax_ws     device float[E] scratch.
  *   interleave  1: store rows in gate/up tile order for the fused SwiGLU
- *               epilogue: packed row 128t+i is source row 64t+i (i < 64, a
- *               gate row) or N/2 + 64t + i-64 (i >= 64, an up row).  Needs
- *               N % 128 == 0.  0: rows in source order.
- * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, k % 8). */
+ *               epilogue: packed row 256t+i is source row 128t+i (i < 128, a
+ *               gate row) or N/2 + 128t + i-128 (i >= 128, an up row).  Needs
+ *               N % 256 == 0.  0: rows in source order.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128 (N % 256 when
+ * interleaving), k % 8). */
 int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_t K, const int32_t *S,
                           int32_t k, int32_t interleave, uint8_t *w_codes, uint8_t *w_scales,
                           float *gs_w, void *w_sel, float *amax_ws, int32_t *dev_status,
@@ -187,8 +193,11 @@ int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, const float *
 /* W4A4 + RAC grouped GEMM on the FP4 tensor cores (tcgen05 block-scaled MMA
  * with E4M3 block scales, FP32 accumulation in tensor memory) plus the rank-k
  * BF16 correction of Residual Activation Compensation, QUADS §3.3 Eq. 21:
- *   y[r, n] = gs_a*gs_w[e] * sum_K (ca*sa)(cw*sw)  +  gs_w[e] * sum_{s<k} r[r,s]*w_sel[e,n,s]
- * for every routed row r in expert e's segment [offsets[e], offsets[e+1]).
+ *   y[r, n] = gs_a*gs_w[e] * ( sum_K (ca*sa)(cw*sw) + sum_{s<k} rg[r,s]*w_sel[e,n,s] )
+ * for every routed row r in expert e's segment [offsets[e], offsets[e+1]),
+ * where rg = r/gs_a is the residual as nvfp4_quantize stores it: both sums
+ * accumulate in one FP32 tensor-memory accumulator, the correction as BF16
+ * MMAs over the k selected channels.
  *   a_codes/a_scales  device, the routed activations from nvfp4_quantize,
  *                     rows_cap rows; a_resid device BF16 [rows_cap, k]
  *   gs_a              device float (nvfp4_quantize's gs_out)
@@ -199,13 +208,14 @@ int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, const float *
  *                     NVFP4_EPI_SWIGLU: the weights were prepared with
  *                     interleave = 1; y = bf16(silu(gate) * up) [rows_cap, N/2]
  *                     (ldy >= N/2, out_dtype must be BF16).
+ * Output tiles are 128 rows x 256 columns.
  *   out_dtype         NVFP4_OUT_F32 or NVFP4_OUT_BF16 (= bf16_rn of the F32 value)
  *   amax_out          device float or NULL: receives max|y| of the stored
  *                     values (the next quantize's amax); the call clears it
  *                     on `stream` before the kernel runs.
  * Rows of a segment beyond the expert's real token count must hold zero
  * codes/scales/residual (nvfp4_moe_clear_padding); their outputs are zero.
- * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 256, N % 128, k % 16,
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 256, N % 256, k % 16,
  * k > 256, E > 1024); dev_status gets TIMEOUT if a pipeline wait runs out. */
 int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
                                 const void *a_resid, const float *gs_a, const uint8_t *w_codes,
@@ -224,7 +234,7 @@ int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
  *   offsets  as for nvfp4_w4a4_rac_grouped_gemm
  *   epilogue NVFP4_EPI_NONE: y [rows_cap, N]; NVFP4_EPI_SWIGLU: y =
  *            bf16(silu(gate) * up) [rows_cap, N/2] (out_dtype must be BF16).
- * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, E > 1024). */
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 256, E > 1024). */
 int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const int32_t *offsets, int32_t E,
                             int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype,
                             int32_t epilogue, void *y, int64_t ldy, int32_t *dev_status,

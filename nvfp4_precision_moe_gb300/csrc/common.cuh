@@ -61,9 +61,15 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t h16) {
     return __uint_as_float(h16 << 16);
 }
 
-// Per-tensor scale gs = amax / (6*448), 1 for an all-zero tensor.
+// Per-tensor scale: the smallest power of two not below fl(amax / (6*448)),
+// 1 for an all-zero tensor.  (For amax in the contract the quotient is a
+// normal binary32 number, so rounding it up to a power of two is a matter of
+// its exponent and mantissa bits.)
 __device__ __forceinline__ float tensor_scale(float amax) {
-    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 2688.0f);
+    if (amax == 0.0f) return 1.0f;
+    const uint32_t q = __float_as_uint(__fdiv_rn(amax, 2688.0f));
+    const uint32_t e = q & 0x7f800000u;
+    return (q & 0x007fffffu) ? __uint_as_float(e + 0x00800000u) : __uint_as_float(e);
 }
 
 // E4M3 (RNE, saturating to 448) of a non-negative binary32 value.
@@ -270,6 +276,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes <- registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 

@@ -3,15 +3,17 @@
 // Two instantiations of one warp-specialised, persistent pipeline:
 //  * FP4=true : the W4A4 + RAC GEMM of QUADS §3.3 Eq. 21.  The main product
 //    runs as block-scaled E2M1 x E2M1 MMAs (kind::mxf4nvf4, one UE4M3 scale
-//    per 16 K-elements, scale_vec::4X) into an FP32 accumulator in tensor
-//    memory; the rank-k residual correction r_sel . W_sel^T runs as BF16 MMAs
-//    (kind::f16) into a second accumulator; the epilogue combines
-//    gs_a*gs_w*D_main + gs_w*D_res (and optionally SwiGLU).
+//    per 16 K-elements, scale_vec::4X); the rank-k residual correction
+//    rg . W_sel^T runs as BF16 MMAs (kind::f16) into the same FP32
+//    accumulator -- the residual arrives in units of the activation's
+//    power-of-two tensor scale, so both sums share the units (ca*sa)(cw*sw)
+//    -- and the epilogue multiplies by gs_a*gs_w (optionally with SwiGLU).
 //  * FP4=false: the BF16 GEMM of the asymmetric-QAT forward, QUADS §3.2 Eq. 12.
 //
-// Tiles are 128 rows x 128 columns of the output; the K loop moves 128-byte
-// wide K-slices (256 FP4 or 64 BF16 elements) through a ring of shared-memory
-// stages fed by TMA (128-byte swizzle).  Warp roles per CTA (448 threads):
+// Output tiles are 128 rows x 256 columns; the K loop moves 128-byte wide
+// K-slices (256 FP4 or 64 BF16 elements) through 4 shared-memory stages fed
+// by TMA (128-byte swizzle).  Per FP4 stage: A 16 KB, B 32 KB, scales 6 KB.
+// Warp roles per CTA (448 threads):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner + MMA issuer (one lane)
 //   warps 2-5   scale warps (FP4): once a stage has landed, each writes the
@@ -22,11 +24,11 @@
 //               the MMA rate.)
 //   warps 6-13  epilogue: warp w reads TMEM lane quarter w%4 and column half
 //               (w-6)/4 of the tile, scales, applies SwiGLU, stores.
-// Tensor memory (512 columns): the main accumulator is double-buffered
-// (columns 0-127 and 128-255), so the epilogue of one tile overlaps the MMAs
-// of the next; the RAC accumulator (256-383) is single-buffered and its MMAs
-// are issued last in each tile, after the previous tile's epilogue has read
-// it; columns 384-511 hold the block scales of the 4 pipeline stages.
+// Tensor memory (512 columns): accumulator in columns 0-255; the scales of
+// the 4 stages in 48-column slots from column 256 (A: 16, B: 32).  The
+// accumulator is single-buffered: the epilogue reads it in two halves and
+// releases it after the second read, so the next tile's MMAs wait only for
+// the first half's stores.
 // Expert segments are contiguous 128-row groups of the routed rows, so the
 // tile list is (row tile, column tile) over all routed rows; each tile's
 // expert comes from a binary search of the segment offsets.
@@ -34,19 +36,22 @@
 
 namespace nvfp4 {
 
-constexpr int kBM = 128, kBN = 128;
-constexpr int kTileBytes = 16384;  // 128 rows x 128 bytes
-constexpr int kSFBytes = 2048;     // 4 MMA-K chunks x 512 bytes (128 rows x 4 scales)
+constexpr int kBM = 128, kBN = 256;
+constexpr int kATileBytes = 16384;  // 128 rows x 128 bytes
+constexpr int kBTileBytes = 32768;  // 256 rows x 128 bytes
+constexpr int kSFABytes = 2048;     // 4 MMA-K chunks x 512 bytes (128 rows x 4 scales)
+constexpr int kSFBBytes = 4096;     // two 128-row groups of the B tile
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccMain0 = 0, kAccRes = 256, kSFCol0 = 384;
+constexpr uint32_t kAcc = 0, kSFCol0 = 256, kSFSlotCols = 48;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxExperts = 1024;
 constexpr int kEpiWarps = 8;
 constexpr int kSFWarps = 4;
 constexpr int kEpiWarp0 = 2 + kSFWarps;
 constexpr int kThreads = 64 + 32 * kSFWarps + 32 * kEpiWarps;
+constexpr int kStages = 4;
 
-// Instruction descriptors (M = 128, N = 128, both operands K-major).
+// Instruction descriptors (M = 128, N = 256, both operands K-major).
 //  kind::mxf4nvf4: A, B = E2M1 (1) at bits 7-9 / 10-12, N>>3 at 17, scale
 //  format UE4M3 (0) at bit 23, M>>4 at 24, scale-factor ids 0.
 constexpr uint32_t kIdescNVF4 = (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) | ((kBM >> 4) << 24);
@@ -55,15 +60,15 @@ constexpr uint32_t kIdescBF16 = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3)
 
 template <bool FP4>
 struct Cfg {
-    static constexpr int kStages = FP4 ? 4 : 6;
-    static constexpr int kStageBytes = 2 * kTileBytes + (FP4 ? 2 * kSFBytes : 0);
+    static constexpr int kStageBytes = kATileBytes + kBTileBytes + (FP4 ? kSFABytes + kSFBBytes : 0);
     static constexpr int kBarOffset = kStages * kStageBytes;
-    // barriers: full/empty/sf_ready per stage, acc_full[2], acc_empty[2], res_empty, drain
-    static constexpr int kNumBars = 3 * kStages + 6;
+    // barriers: full/empty/sf_ready per stage, acc_full, acc_empty, drain
+    static constexpr int kNumBars = 3 * kStages + 3;
     static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
     static constexpr int kGswOffset = kOffOffset + (kMaxExperts + 1) * 4;
     static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
 };
+static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory budget");
 
 struct GemmParams {
     const uint8_t *a_scales;
@@ -103,6 +108,51 @@ __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fdividef(g, 1.0f + e), u);
 }
 
+// 16 columns of this warp's TMEM rows -> 16 BF16 stores (32 bytes), or 16
+// FP32 stores (64 bytes); tracks max|stored value|.
+__device__ __forceinline__ void store16(const GemmParams &p, int64_t row, int64_t col, float gmul,
+                                        const uint32_t (&d)[16], float &amax_local) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(gmul, __uint_as_float(d[i]));
+    if (p.out_dtype == NVFP4_OUT_F32) {
+        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + row * p.ldy + col);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
+    } else {
+        uint32_t o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] << 16)));
+            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] & 0xffff0000u)));
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + col);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// 16 SwiGLU outputs from 16 gate and 16 up columns -> 32 bytes of BF16.
+__device__ __forceinline__ void swiglu16(uint16_t *dst16, float gmul, const uint32_t (&g)[16],
+                                         const uint32_t (&u)[16], float &amax_local) {
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        const float h0 = swiglu1(__fmul_rn(gmul, __uint_as_float(g[i])), __fmul_rn(gmul, __uint_as_float(u[i])));
+        const float h1 =
+            swiglu1(__fmul_rn(gmul, __uint_as_float(g[i + 1])), __fmul_rn(gmul, __uint_as_float(u[i + 1])));
+        o[i / 2] = pack_bf16x2(h0, h1);
+        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] << 16)));
+        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] & 0xffff0000u)));
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(dst16);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
 template <bool FP4>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -112,12 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
-    uint64_t *empty = full + C::kStages;
-    uint64_t *sf_ready = empty + C::kStages;  // [kStages]
-    uint64_t *acc_full = sf_ready + C::kStages;  // [2]
-    uint64_t *acc_empty = acc_full + 2;       // [2]
-    uint64_t *res_empty = acc_empty + 2;
-    uint64_t *drain = res_empty + 1;
+    uint64_t *empty = full + kStages;
+    uint64_t *sf_ready = empty + kStages;
+    uint64_t *acc_full = sf_ready + kStages;
+    uint64_t *acc_empty = acc_full + 1;
+    uint64_t *drain = acc_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::kOffOffset);
@@ -129,16 +178,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (FP4)
         for (int i = threadIdx.x; i < E; i += blockDim.x) s_gsw[i] = p.gs_w[i];
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], kSFWarps);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], kEpiWarps);
-        }
-        mbar_init(res_empty, kEpiWarps);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kEpiWarps);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -169,53 +215,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------ TMA producer
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_phase[C::kStages];
-            bool issued[C::kStages];
-            for (int s = 0; s < C::kStages; ++s) issued[s] = false;
+            uint32_t issued_phase[kStages];
+            bool issued[kStages];
+            for (int s = 0; s < kStages; ++s) issued[s] = false;
             bool ok = true;
             const int64_t kgroups = p.K / 64;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int mt = tile / num_nt, nt = tile - mt * num_nt;
                 const int32_t m0 = mt * kBM;
                 const int e = expert_of(s_off, E, m0);
-                const int32_t brow = (int32_t)(e * p.N + nt * kBN);
+                const int32_t brow = (int32_t)(e * p.N + (int64_t)nt * kBN);
+                // BF16 SwiGLU: B rows are the gate rows [128nt, +128) and the up rows N/2 + [128nt, +128)
                 const bool swiglu_rows = !FP4 && p.epilogue == NVFP4_EPI_SWIGLU;
-                const int32_t brow_lo = swiglu_rows ? (int32_t)(e * p.N + nt * 64) : brow;
-                const int32_t brow_hi = swiglu_rows ? (int32_t)(e * p.N + p.N / 2 + nt * 64) : brow + 64;
+                const int32_t brow_lo = swiglu_rows ? (int32_t)(e * p.N + nt * 128) : brow;
+                const int32_t brow_hi = swiglu_rows ? (int32_t)(e * p.N + p.N / 2 + nt * 128) : brow + 128;
                 for (int it = 0; it < nkt + nrt; ++it) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
                         ok = false;
                         break;
                     }
                     uint8_t *sa = smem + stage * C::kStageBytes;
-                    uint8_t *sb = sa + kTileBytes;
+                    uint8_t *sb = sa + kATileBytes;
                     if (it < nkt) {
                         if (FP4) {
-                            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes + 2 * kSFBytes);
+                            mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes + kSFABytes + kSFBBytes);
                             tma_load_2d(sa, &tmA, it * 128, m0, &full[stage]);
                             tma_load_2d(sb, &tmB, it * 128, brow, &full[stage]);
-                            const uint8_t *sfa = p.a_scales + ((int64_t)mt * kgroups + it * 4) * 512;
-                            const uint8_t *sfb = p.w_scales + (int64_t)e * p.N * (p.K / 16) +
-                                                 ((int64_t)nt * kgroups + it * 4) * 512;
-                            bulk_load(sb + kTileBytes, sfa, kSFBytes, &full[stage]);
-                            bulk_load(sb + kTileBytes + kSFBytes, sfb, kSFBytes, &full[stage]);
+                            uint8_t *ssf = sb + kBTileBytes;
+                            const uint8_t *wsc = p.w_scales + (int64_t)e * p.N * (p.K / 16);
+                            bulk_load(ssf, p.a_scales + ((int64_t)mt * kgroups + it * 4) * 512, kSFABytes, &full[stage]);
+                            bulk_load(ssf + kSFABytes, wsc + ((int64_t)(2 * nt) * kgroups + it * 4) * 512, kSFBBytes / 2,
+                                      &full[stage]);
+                            bulk_load(ssf + kSFABytes + kSFBBytes / 2, wsc + ((int64_t)(2 * nt + 1) * kgroups + it * 4) * 512,
+                                      kSFBBytes / 2, &full[stage]);
                         } else {
-                            // two 64-row boxes: rows [n0, n0+128), or for SwiGLU the gate
-                            // rows [64nt, 64nt+64) and the up rows N/2 + [64nt, 64nt+64)
-                            mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                            mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
                             tma_load_2d(sa, &tmA, it * 64, m0, &full[stage]);
                             tma_load_2d(sb, &tmB, it * 64, brow_lo, &full[stage]);
-                            tma_load_2d(sb + kTileBytes / 2, &tmB, it * 64, brow_hi, &full[stage]);
+                            tma_load_2d(sb + kBTileBytes / 2, &tmB, it * 64, brow_hi, &full[stage]);
                         }
                     } else {  // RAC slice: residual rows and the selected weight columns
                         const int r = it - nkt;
-                        mbar_arrive_expect_tx(&full[stage], 2 * kTileBytes);
+                        mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
                         tma_load_2d(sa, &tmR, r * 64, m0, &full[stage]);
                         tma_load_2d(sb, &tmWs, r * 64, brow, &full[stage]);
                     }
                     issued[stage] = true;
                     issued_phase[stage] = phase;
-                    if (++stage == C::kStages) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -225,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 report(p.dev_status, NVFP4_ERR_TIMEOUT);
                 *abort_flag = 1;
                 // let every copy already issued land before the CTA can exit
-                for (int s = 0; s < C::kStages; ++s)
+                for (int s = 0; s < kStages; ++s)
                     if (issued[s]) (void)mbar_wait_bounded(&full[s], issued_phase[s], kWaitLimitNs);
             }
         }
@@ -236,35 +283,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             int local = 0;
+            const uint32_t acc = tmem + kAcc;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-                const uint32_t buf = (uint32_t)local & 1u;
-                const uint32_t acc = tmem + kAccMain0 + buf * kBN;
-                // the epilogue must have drained this buffer (used two tiles ago)
-                if (!mbar_wait_bounded(&acc_empty[buf], (((uint32_t)local >> 1) & 1u) ^ 1u, kWaitLimitNs,
-                                       abort_flag)) {
+                // the epilogue has read the previous tile out of the accumulator
+                if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int it = 0; it < nkt + nrt; ++it) {
-                    if (it == nkt) {
-                        // the single RAC accumulator: the previous tile's epilogue has read it
-                        if (!mbar_wait_bounded(res_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
                     if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
-                    const uint32_t b_addr = a_addr + kTileBytes;
+                    const uint32_t b_addr = a_addr + kATileBytes;
                     if (it < nkt) {
                         if (FP4) {
-                            const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * 32u;
+                            const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * kSFSlotCols;
                             // the scale warps have written this stage's scales
                             if (!mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
                                 ok = false;
@@ -273,29 +310,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tc_fence_after();
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                            kIdescNVF4, sf + 4 * c, sf + 16 + 4 * c, (it | c) != 0);
+                                tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescNVF4,
+                                            sf + 4 * c, sf + 16 + 8 * c, (it | c) != 0);
                         } else {
 #pragma unroll
                             for (int c = 0; c < 4; ++c)
-                                tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                            kIdescBF16, (it | c) != 0);
+                                tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescBF16,
+                                            (it | c) != 0);
                         }
                     } else {
+                        // RAC: accumulate rg . W_sel^T into the same accumulator
                         const int r = it - nkt;
                         const int nm = min(4, (p.k - r * 64) / 16);
                         for (int c = 0; c < nm; ++c)
-                            tc_mma_bf16(tmem + kAccRes, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                        kIdescBF16, (r | c) != 0);
+                            tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescBF16, 1u);
                     }
                     tc_commit(&empty[stage]);
-                    if (++stage == C::kStages) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                tc_commit(&acc_full[buf]);
+                tc_commit(acc_full);
             }
             if (!ok) {
                 report(p.dev_status, NVFP4_ERR_TIMEOUT);
@@ -309,9 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------- scale warps
         // Slice by slice in the producer's order: wait for the stage, then
-        // write its 8 scale chunks (SFA then SFB, 512 bytes each: 32 rows of
-        // 16 bytes) into this warp's lane quarter: lane i, column 4c + j gets
-        // word j of row i of chunk c.  Every quarter holds the same copy.
+        // write its 12 scale chunks (512 bytes each: 32 rows of 16 bytes) into
+        // this warp's lane quarter.  Slot columns: A chunk c -> 4c..4c+3;
+        // B chunk c -> 16+8c..16+8c+7 (its first and second 128 rows).  Lane
+        // i, column base+j gets word j of row i of the chunk; every quarter
+        // holds the same copy.
         if (FP4) {
             const uint32_t q = (uint32_t)(warp & 3);
             int stage = 0;
@@ -325,23 +364,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     if (it < nkt) {
-                        const uint8_t *sfs = smem + stage * C::kStageBytes + 2 * kTileBytes;
-                        uint32_t r[32];
+                        const uint8_t *sfs = smem + stage * C::kStageBytes + kATileBytes + kBTileBytes;
+                        uint32_t r0[32], r1[16];
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
+                        for (int c = 0; c < 4; ++c) {  // A: columns 4c..4c+3
                             const uint4 w = *reinterpret_cast<const uint4 *>(sfs + 512 * c + 16 * lane);
-                            r[4 * c] = w.x;
-                            r[4 * c + 1] = w.y;
-                            r[4 * c + 2] = w.z;
-                            r[4 * c + 3] = w.w;
+                            r0[4 * c] = w.x;
+                            r0[4 * c + 1] = w.y;
+                            r0[4 * c + 2] = w.z;
+                            r0[4 * c + 3] = w.w;
                         }
-                        tmem_st32(tmem + ((q * 32u) << 16) + kSFCol0 + (uint32_t)stage * 32u, r);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {  // B: columns 16+8c (rows 0-127), 20+8c (rows 128-255)
+                            const uint4 lo = *reinterpret_cast<const uint4 *>(sfs + kSFABytes + 512 * c + 16 * lane);
+                            const uint4 hi =
+                                *reinterpret_cast<const uint4 *>(sfs + kSFABytes + kSFBBytes / 2 + 512 * c + 16 * lane);
+                            const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const int col = 16 + 8 * c + j;  // 16..47
+                                if (col < 32) r0[col] = v[j];
+                                else r1[col - 32] = v[j];
+                            }
+                        }
+                        const uint32_t base = tmem + ((q * 32u) << 16) + kSFCol0 + (uint32_t)stage * kSFSlotCols;
+                        tmem_st32(base, r0);
+                        tmem_st16(base + 32, r1);
                         tmem_st_wait();
                     }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sf_ready[stage]);
-                    if (++stage == C::kStages) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -357,20 +411,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------- epilogue
-        const int ew = warp - kEpiWarp0;     // 0..7
-        const int q = warp & 3;              // TMEM lane quarter this warp may access
-        const int half = ew >> 2;            // which half of the tile's columns
+        const int ew = warp - kEpiWarp0;  // 0..7
+        const int q = warp & 3;           // TMEM lane quarter this warp may access
+        const int half = ew >> 2;         // which half of the tile's columns
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int row_in_tile = q * 32 + lane;
         const float gsa = FP4 ? *p.gs_a : 1.0f;
-        const bool has_res = FP4 && p.k > 0;
+        const bool swiglu = p.epilogue == NVFP4_EPI_SWIGLU;
         float amax_local = 0.0f;
         int local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-            const uint32_t buf = (uint32_t)local & 1u;
             // every lane waits; the warp goes on only if all lanes saw the phase
             // complete, so the .sync.aligned TMEM loads below stay converged
-            const bool got = mbar_wait_bounded(&acc_full[buf], ((uint32_t)local >> 1) & 1u, kWaitLimitNs, abort_flag);
+            const bool got = mbar_wait_bounded(acc_full, (uint32_t)local & 1u, kWaitLimitNs, abort_flag);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) {
                     report(p.dev_status, NVFP4_ERR_TIMEOUT);
@@ -379,96 +432,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t acc = tmem + lane_base + kAccMain0 + buf * kBN;
-            const uint32_t res = tmem + lane_base + kAccRes;
+            const uint32_t acc = tmem + lane_base + kAcc;
             const int mt = tile / num_nt, nt = tile - mt * num_nt;
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
-            float gsw = 1.0f, gmul = 1.0f;
-            if (FP4) {
-                gsw = s_gsw[expert_of(s_off, E, mt * kBM)];
-                gmul = __fmul_rn(gsa, gsw);
-            }
-            if (p.epilogue == NVFP4_EPI_SWIGLU) {
-                // columns 0-63 gate, 64-127 up; this warp: output columns [32*half, 32*half+32)
-                uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 64 + 32 * half;
+            const float gmul = FP4 ? __fmul_rn(gsa, s_gsw[expert_of(s_off, E, mt * kBM)]) : 1.0f;
+            // two halves of this warp's work: the first is stored before the
+            // second is read, then the accumulator is released
+            uint32_t x0[16], x1[16], x2[16], x3[16];
 #pragma unroll 1
-                for (int j = 0; j < 2; ++j) {
-                    const int c0 = 32 * half + 16 * j;
-                    uint32_t g[16], u[16], gr[16], ur[16];
-                    tmem_ld16(acc + c0, g);
-                    tmem_ld16(acc + 64 + c0, u);
-                    if (has_res) {
-                        tmem_ld16(res + c0, gr);
-                        tmem_ld16(res + 64 + c0, ur);
-                    }
+            for (int part = 0; part < 2; ++part) {
+                if (swiglu) {
+                    // output columns 64*half + 32*part + [0, 32): gate = D[c], up = D[128 + c]
+                    const int c0 = 64 * half + 32 * part;
+                    tmem_ld16(acc + c0, x0);
+                    tmem_ld16(acc + 128 + c0, x1);
+                    tmem_ld16(acc + c0 + 16, x2);
+                    tmem_ld16(acc + 128 + c0 + 16, x3);
                     tmem_ld_wait();
-                    uint32_t o[8];
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        float hv[2];
-#pragma unroll
-                        for (int t = 0; t < 2; ++t) {
-                            float gv = __fmul_rn(gmul, __uint_as_float(g[i + t]));
-                            float uv = __fmul_rn(gmul, __uint_as_float(u[i + t]));
-                            if (has_res) {
-                                gv = __fadd_rn(gv, __fmul_rn(gsw, __uint_as_float(gr[i + t])));
-                                uv = __fadd_rn(uv, __fmul_rn(gsw, __uint_as_float(ur[i + t])));
-                            }
-                            hv[t] = swiglu1(gv, uv);
-                        }
-                        o[i / 2] = pack_bf16x2(hv[0], hv[1]);
-                        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] << 16)));
-                        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] & 0xffff0000u)));
+                    if (part == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(yrow + 16 * j);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                }
-            } else {
-#pragma unroll 1
-                for (int j = 0; j < 4; ++j) {
-                    const int c0 = 64 * half + 16 * j;
-                    uint32_t d[16], dr[16];
-                    tmem_ld16(acc + c0, d);
-                    if (has_res) tmem_ld16(res + c0, dr);
+                    uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 128 + c0;
+                    swiglu16(yrow, gmul, x0, x1, amax_local);
+                    swiglu16(yrow + 16, gmul, x2, x3, amax_local);
+                } else {
+                    const int c0 = 128 * half + 64 * part;
+                    tmem_ld16(acc + c0, x0);
+                    tmem_ld16(acc + c0 + 16, x1);
+                    tmem_ld16(acc + c0 + 32, x2);
+                    tmem_ld16(acc + c0 + 48, x3);
                     tmem_ld_wait();
-                    float v[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x = __uint_as_float(d[i]);
-                        if (FP4) {
-                            x = __fmul_rn(gmul, x);
-                            if (has_res) x = __fadd_rn(x, __fmul_rn(gsw, __uint_as_float(dr[i])));
-                        }
-                        v[i] = x;
+                    if (part == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty);
                     }
                     const int64_t col = (int64_t)nt * kBN + c0;
-                    if (p.out_dtype == NVFP4_OUT_F32) {
-                        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + row * p.ldy + col);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
-                    } else {
-                        uint32_t o[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] << 16)));
-                            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] & 0xffff0000u)));
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + col);
-                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
+                    store16(p, row, col, gmul, x0, amax_local);
+                    store16(p, row, col + 16, gmul, x1, amax_local);
+                    store16(p, row, col + 32, gmul, x2, amax_local);
+                    store16(p, row, col + 48, gmul, x3, amax_local);
                 }
-            }
-            // all TMEM reads of this tile are complete (tcgen05.wait::ld above)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (has_res) mbar_arrive(res_empty);
-                mbar_arrive(&acc_empty[buf]);
             }
         }
         if (p.amax_out) {
@@ -520,7 +526,7 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
     if (epilogue == NVFP4_EPI_SWIGLU && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
     const int64_t ncols = epilogue == NVFP4_EPI_SWIGLU ? N / 2 : N;
     if (ldy < ncols) return NVFP4_ERR_INVALID_ARG;
-    if (K % 256 || N % 128 || k % 16 || k > 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) ||
+    if (K % 256 || N % 256 || k % 16 || k > 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) ||
         (int64_t)E * N > (1ll << 31))
         return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) || !aligned16(w_scales) || !aligned16(y) ||
@@ -542,13 +548,13 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
     s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a_codes, K / 2, rows_cap, K / 2, 128, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == NVFP4_OK)
-        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)w_codes, K / 2, (uint64_t)E * N, K / 2, 128, 128,
+        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)w_codes, K / 2, (uint64_t)E * N, K / 2, 128, 256,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == NVFP4_OK && k > 0) {
         s = encode_tmap_2d(&tR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a_resid, k, rows_cap, 2 * k, 64, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B);
         if (s == NVFP4_OK)
-            s = encode_tmap_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_sel, k, (uint64_t)E * N, 2 * k, 64, 128,
+            s = encode_tmap_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_sel, k, (uint64_t)E * N, 2 * k, 64, 256,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     } else {
         tR = tA;
@@ -573,7 +579,7 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
     p.ldy = ldy;
     p.amax_out = amax_out;
     p.dev_status = dev_status;
-    const int64_t max_tiles = (rows_cap / 128) * (N / 128);
+    const int64_t max_tiles = (rows_cap / kBM) * (N / kBN);
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     grouped_gemm_kernel<true><<<grid, kThreads, Cfg<true>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tR, tW, p);
     return launch_status("grouped_gemm_kernel<fp4>");
@@ -587,7 +593,7 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     if (epilogue != NVFP4_EPI_NONE && epilogue != NVFP4_EPI_SWIGLU) return NVFP4_ERR_INVALID_ARG;
     if (epilogue == NVFP4_EPI_SWIGLU && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
     if (ldy < (epilogue == NVFP4_EPI_SWIGLU ? N / 2 : N)) return NVFP4_ERR_INVALID_ARG;
-    if (K % 64 || N % 128 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) || (int64_t)E * N > (1ll << 31))
+    if (K % 64 || N % 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) || (int64_t)E * N > (1ll << 31))
         return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(w_hat) || !aligned16(y) || ldy % 8) return NVFP4_ERR_ALIGNMENT;
     if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
@@ -598,7 +604,7 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)x, K, rows_cap, 2 * K, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == NVFP4_OK)
-        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_hat, K, (uint64_t)E * N, 2 * K, 64, 64,
+        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_hat, K, (uint64_t)E * N, 2 * K, 64, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != NVFP4_OK) return s;
     GemmParams p{};
@@ -612,7 +618,7 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     p.y = y;
     p.ldy = ldy;
     p.dev_status = dev_status;
-    const int64_t max_tiles = (rows_cap / 128) * (N / 128);
+    const int64_t max_tiles = (rows_cap / kBM) * (N / kBN);
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
     grouped_gemm_kernel<false><<<grid, kThreads, Cfg<false>::kSmemBytes, (cudaStream_t)stream>>>(tA, tB, tA, tB, p);
     return launch_status("grouped_gemm_kernel<bf16>");

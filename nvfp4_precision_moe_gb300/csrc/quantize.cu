@@ -148,6 +148,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
     const float amax_t = a.amax[tensor];
     const float gs = tensor_scale(amax_t);
     const float p6 = __fmul_rn(gs, 6.0f);
+    const float inv_gs = __frcp_rn(gs);  // exact: gs is a power of two
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         if (a.gs_out) a.gs_out[tensor] = gs;
         if (!isfinite(amax_t)) report(a.dev_status, NVFP4_ERR_NONFINITE);
@@ -162,9 +163,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
 
     for (int64_t m = (int64_t)blockIdx.x * kQWarps + wid; m < a.M; m += nwarps_total) {
         int64_t src_row = m;
-        if (MODE == kModeWeight && a.interleave) {
-            const int64_t t = m >> 7, i = m & 127;
-            src_row = (i < 64) ? (t * 64 + i) : (a.M / 2 + t * 64 + (i - 64));
+        if (MODE == kModeWeight && a.interleave) {  // 256-row tiles: 128 gate rows, then 128 up rows
+            const int64_t t = m >> 8, i = m & 255;
+            src_row = (i < 128) ? (t * 128 + i) : (a.M / 2 + t * 128 + (i - 128));
         }
         // destination rows of this source row: lane f holds the f-th
         int64_t my_dst = -1;
@@ -245,8 +246,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
                             if (MODE == kModeWeight) {
                                 val = __bfloat16_as_ushort(__float2bfloat16_rn(cs));
                             } else {
+                                // r = bf16(x - (code*sb)*gs), stored in units of gs
                                 const float xq = __fmul_rn(cs, gs);
-                                val = __bfloat16_as_ushort(__float2bfloat16_rn(__fsub_rn(v[t], xq)));
+                                const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v[t], xq)));
+                                val = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
                             }
                             if (staged) {
                                 stage[si] = val;
@@ -547,7 +550,8 @@ extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_
     if (!w || !w_codes || !w_scales || !gs_w || !amax_ws || E < 1 || N < 0 || K < 0 || k < 0 || k > K)
         return NVFP4_ERR_INVALID_ARG;
     if (k > 0 && (!S || !w_sel)) return NVFP4_ERR_INVALID_ARG;
-    if (K % 64 || N % 128 || k % 8 || K / 16 > kMaxBlocksPerRow || E > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (K % 64 || N % 128 || (interleave && N % 256) || k % 8 || K / 16 > kMaxBlocksPerRow || E > 65535)
+        return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(w) || !aligned16(w_codes) || !aligned16(w_scales) || (w_sel && !aligned16(w_sel)))
         return NVFP4_ERR_ALIGNMENT;
     NVFP4_CHECK_INIT();

@@ -82,12 +82,12 @@ def test_host_checks_without_gpu(lib):
     assert q(P, 4, 64, 64, P, None, P, 8, None, 1, 4, P, P, None, None, None) == INVALID  # k>0, no resid
     assert q(P, 4, 64, 64, P, None, None, 0, None, 2, 4, P, P, None, None, None) == INVALID  # fanout w/o map
     g = lib.nvfp4_w4a4_rac_grouped_gemm
-    args = [P, P, None, P, P, P, P, None, 0, P, 1, 128, 128, 256, 0, 0, P, 128, None, None, None]
+    args = [P, P, None, P, P, P, P, None, 0, P, 1, 128, 256, 256, 0, 0, P, 256, None, None, None]
     bad_k = list(args)
     bad_k[13] = 192  # K % 256
     assert g(*bad_k) == UNSUP
     bad_n = list(args)
-    bad_n[12] = 96  # N % 128
+    bad_n[12] = 128  # N % 256
     assert g(*bad_n) == UNSUP
     swiglu_f32 = list(args)
     swiglu_f32[14] = 1  # SwiGLU needs BF16 output

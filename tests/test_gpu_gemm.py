@@ -119,7 +119,7 @@ def _oracle_dense(x_u16, w_u16, S):
     cw, sw, _, gw = oracle.quantize(w_u16)
     xq = oracle.dequantize_exact(ca, sa, ga)
     wq = oracle.dequantize_exact(cw, sw, gw)
-    return oracle.rac_gemm(xq, wq, r, S), xq, wq
+    return oracle.rac_gemm(xq, wq, r, S, ga), xq, wq
 
 
 def _cfg_S(cfg, k):
@@ -209,7 +209,7 @@ def test_grouped_ragged_segments():
         wq = oracle.dequantize_exact(cw, sw, g)
         n = counts[e]
         if n:
-            ref = oracle.rac_gemm(xq[pos:pos + n], wq, r[pos:pos + n], S)
+            ref = oracle.rac_gemm(xq[pos:pos + n], wq, r[pos:pos + n], S, ga)
             assert G.rel_err(got[offsets[e]:offsets[e] + n], ref) <= TOL, e
         # padding rows of a segment are exactly zero
         assert (got[offsets[e] + n:offsets[e + 1]] == 0).all()
@@ -262,7 +262,7 @@ def test_swiglu_epilogue_and_fused_amax():
         cw, sw, _, g = oracle.quantize(synth.u16(w13[e]))
         wq = oracle.dequantize_exact(cw, sw, g)
         n = counts[e]
-        y = oracle.rac_gemm(xq[pos:pos + n], wq, r[pos:pos + n], S)
+        y = oracle.rac_gemm(xq[pos:pos + n], wq, r[pos:pos + n], S, ga)
         ref = oracle.swiglu(y, I)
         # BF16 output: the unit roundoff 2^-8 of BF16 plus the GEMM tolerance
         assert G.rel_err(got[offsets[e]:offsets[e] + n], ref) <= 2.0 ** -8 + TOL

@@ -120,7 +120,7 @@ def test_rollout_layer_end_to_end_reduced():
         if toks.size == 0:
             continue
         cw, sw, _, g = oracle.quantize(synth.u16(w13[e]))
-        y = oracle.rac_gemm(xq[toks], oracle.dequantize_exact(cw, sw, g), ra[toks], S13)
+        y = oracle.rac_gemm(xq[toks], oracle.dequantize_exact(cw, sw, g), ra[toks], S13, ga)
         rows = dst[toks, np.argmax(ids[toks] == e, 1)]
         h_ref[rows] = oracle.swiglu(y, I)
     # stage check: the GPU's h on every routed row
@@ -139,7 +139,7 @@ def test_rollout_layer_end_to_end_reduced():
         if r1 == r0:
             continue
         cw, sw, _, g = oracle.quantize(synth.u16(wd[e]))
-        y_ref[r0:r1] = oracle.rac_gemm(hq[r0:r1], oracle.dequantize_exact(cw, sw, g), rh[r0:r1], Sd)
+        y_ref[r0:r1] = oracle.rac_gemm(hq[r0:r1], oracle.dequantize_exact(cw, sw, g), rh[r0:r1], Sd, gh)
     y_ref_b = oracle.bf16_to_f32(oracle.bf16_round(y_ref.astype(np.float32))).astype(np.float64)
     out_ref = oracle.combine(y_ref_b, dst.astype(np.int32), rw)
     err = G.rel_err(out, out_ref)
