@@ -242,9 +242,9 @@ def test_prepare_weights_parity(interleave):
     torch.cuda.synchronize()
     G.status_ok(st)
     if interleave:
-        t = np.arange(N) // 128
-        i = np.arange(N) % 128
-        perm = np.where(i < 64, t * 64 + i, N // 2 + t * 64 + (i - 64))
+        t = np.arange(N) // 256
+        i = np.arange(N) % 256
+        perm = np.where(i < 128, t * 128 + i, N // 2 + t * 128 + (i - 128))
     else:
         perm = np.arange(N)
     gsel = G.u16(sel)
