@@ -319,7 +319,8 @@ def run_profile_case(args):
     """A single kernel on a reduced case sized for ncu (inputs above L2, a few
     hundred MB in all): `gemm13` (gate_up W4A4+RAC GEMM with SwiGLU, 32
     experts x 512 rows, N=3072, K=4096, k=128), `gemm_down` (N=4096, K=1536),
-    `quantize_x` (16384 x 4096 scatter-quantize, top-8), `bf16_gemm`
+    `quantize_x` (16384 x 4096 scatter-quantize, top-8), `quantize_h`
+    (147456 x 1536, k=128), `combine` (16384 tokens x 8 x 4096), `bf16_gemm`
     (QAT gate_up, BF16, same shape as gemm13).  Runs `--steps` launches."""
     import torch
 
@@ -373,6 +374,27 @@ def run_profile_case(args):
         nv.nvfp4_amax(x, amax)
         fn = lambda: nv.nvfp4_quantize(x, amax, codes, scales, resid=resid, S=S, dst_row=dst, fanout=topk,
                                        rows_out=cap)
+        flops = 0
+    elif case == "quantize_h":
+        rows, I, k = 147456, 1536, 128
+        x = (torch.randn((rows, I), device=dev, generator=g) * 0.1).to(torch.bfloat16)
+        codes = torch.empty((rows, I // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty(nv.scale_bytes(rows, I), dtype=torch.uint8, device=dev)
+        resid = torch.empty((rows, k), dtype=torch.bfloat16, device=dev)
+        spread = os.environ.get("NVFP4_PROFILE_S", "spread") == "spread"
+        S = (torch.arange(0, I, I // k) if spread else torch.arange(k)).to(torch.int32).to(dev)
+        amax = torch.zeros(1, device=dev)
+        nv.nvfp4_amax(x, amax)
+        fn = lambda: nv.nvfp4_quantize(x, amax, codes, scales, resid=resid, S=S)
+        flops = 0
+    elif case == "combine":
+        T, topk, H = 16384, 8, 4096
+        rows = T * topk
+        y = (torch.randn((rows, H), device=dev, generator=g)).to(torch.bfloat16)
+        dst = torch.randperm(rows, device=dev, generator=g).to(torch.int32).view(T, topk)
+        w = torch.rand((T, topk), device=dev, generator=g)
+        out = torch.empty((T, H), dtype=torch.float32, device=dev)
+        fn = lambda: nv.nvfp4_moe_combine(y, dst, w, topk, out)
         flops = 0
     else:
         raise SystemExit("unknown --profile-case " + case)

@@ -161,12 +161,27 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
     uint16_t *stage = s_res[wid];
     const int fanout = (MODE == kModeAct) ? a.fanout : 1;
 
-    for (int64_t m = (int64_t)blockIdx.x * kQWarps + wid; m < a.M; m += nwarps_total) {
-        int64_t src_row = m;
+    // source row of output row m (weights may be stored in gate/up tile order)
+    auto source_row = [&](int64_t m) -> int64_t {
         if (MODE == kModeWeight && a.interleave) {  // 256-row tiles: 128 gate rows, then 128 up rows
             const int64_t t = m >> 8, i = m & 255;
-            src_row = (i < 128) ? (t * 128 + i) : (a.M / 2 + t * 128 + (i - 128));
+            return (i < 128) ? (t * 128 + i) : (a.M / 2 + t * 128 + (i - 128));
         }
+        return m;
+    };
+    // software pipeline across segments and rows: the next segment's 32
+    // bytes per lane are in flight while this one is quantized
+    uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
+    {
+        const int64_t m0 = (int64_t)blockIdx.x * kQWarps + wid;
+        if (m0 < a.M && lane < nb) {
+            const uint4 *p0 = reinterpret_cast<const uint4 *>(xt + source_row(m0) * a.ldx + lane * 16);
+            ra = __ldg(p0);
+            rb = __ldg(p0 + 1);
+        }
+    }
+    for (int64_t m = (int64_t)blockIdx.x * kQWarps + wid; m < a.M; m += nwarps_total) {
+        const int64_t src_row = source_row(m);
         // destination rows of this source row: lane f holds the f-th
         int64_t my_dst = -1;
         if (MODE == kModeAct) {
@@ -176,21 +191,20 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
             my_dst = m;
         }
         const uint16_t *xrow = xt + src_row * a.ldx;
+        const uint16_t *xnext = (m + nwarps_total < a.M) ? xt + source_row(m + nwarps_total) * a.ldx : nullptr;
 
-        // software pipeline: the next segment's 32 bytes are in flight while
-        // this one is quantized
-        uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
-        if (lane < nb) {
-            const uint4 *p0 = reinterpret_cast<const uint4 *>(xrow + lane * 16);
-            ra = __ldg(p0);
-            rb = __ldg(p0 + 1);
-        }
         for (int seg = 0; seg < segs; ++seg) {
             const int b = seg * 32 + lane;
             const bool valid = b < nb;
             const uint4 ca = ra, cb = rb;
-            if (seg + 1 < segs && b + 32 < nb) {
-                const uint4 *pn = reinterpret_cast<const uint4 *>(xrow + (b + 32) * 16);
+            if (seg + 1 < segs) {
+                if (b + 32 < nb) {
+                    const uint4 *pn = reinterpret_cast<const uint4 *>(xrow + (b + 32) * 16);
+                    ra = __ldg(pn);
+                    rb = __ldg(pn + 1);
+                }
+            } else if (xnext && lane < nb) {  // first segment of this warp's next row
+                const uint4 *pn = reinterpret_cast<const uint4 *>(xnext + lane * 16);
                 ra = __ldg(pn);
                 rb = __ldg(pn + 1);
             }
