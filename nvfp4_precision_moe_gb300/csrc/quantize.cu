@@ -55,6 +55,18 @@ __device__ __forceinline__ float e2m1_val(uint32_t c) {
     return (c & 8u) ? -mag : mag;
 }
 
+// v[t] for a run-time t, by a tree of selects (keeps v in registers)
+__device__ __forceinline__ float sel16(const float (&v)[16], int t) {
+    float a[8], b[4], c[2];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = (t & 1) ? v[2 * i + 1] : v[2 * i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) b[i] = (t & 2) ? a[2 * i + 1] : a[2 * i];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) c[i] = (t & 4) ? b[2 * i + 1] : b[2 * i];
+    return (t & 8) ? c[1] : c[0];
+}
+
 // One 16-element block: the E4M3 scale code, its value, and the 16 E2M1 codes
 // packed two per byte (element 2i in the low nibble) into two words.
 struct BlockQ {
@@ -78,17 +90,42 @@ __device__ __forceinline__ uint32_t e2m1x8(const float *q) {
     return w;
 }
 
-__device__ __forceinline__ void quant_block(const float (&v)[16], float gs, float p6, BlockQ &q) {
+// Per-block tables, filled once per CTA (gs is a power of two, so scaling by
+// it commutes with rounding in the normal range):
+//   div6[m] = fl((1 + m/128) / 6): fl(a / (6 gs)) = div6[mant7(a)] * 2^exp(a) / gs
+//            for a BF16 block amax a (7 mantissa bits);
+//   rcp[c]  = fl(1 / e4m3(c)):      fl(1 / (sb * gs)) = rcp[sb] / gs.
+struct QTables {
+    float div6[128];
+    float rcp[128];
+};
+
+__device__ __forceinline__ void fill_tables(QTables &t) {
+    for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+        t.div6[i] = __fdiv_rn(1.0f + (float)i * (1.0f / 128.0f), 6.0f);
+        t.rcp[i] = __frcp_rn(e4m3_to_f32((uint32_t)i));
+    }
+}
+
+// 2^n for |n| within the normal exponent range
+__device__ __forceinline__ float pow2f(int n) { return __uint_as_float((uint32_t)(n + 127) << 23); }
+
+__device__ __forceinline__ void quant_block(const float (&v)[16], float gs, float p6, float inv_gs,
+                                            const QTables &tb, BlockQ &q) {
     float amax_b = 0.0f;
 #pragma unroll
     for (int t = 0; t < 16; ++t) amax_b = fmaxf(amax_b, fabsf(v[t]));
-    // block scale: E4M3 of amax_b / (6*gs), RNE with saturation
-    const float s = __fdiv_rn(amax_b, p6);
+    // block scale: E4M3 of fl(amax_b / (6*gs)), RNE with saturation
+    const uint32_t ab = __float_as_uint(amax_b);
+    const int ex = (int)(ab >> 23);  // biased exponent of the block amax
+    float s;
+    if (ex >= 8) s = __fmul_rn(__fmul_rn(tb.div6[(ab >> 16) & 127u], pow2f(ex - 127)), inv_gs);
+    else s = __fdiv_rn(amax_b, p6);  // tiny or zero block amax: the plain division
     q.sb = e4m3_from_f32(s);
     q.sbf = e4m3_to_f32(q.sb);
     const float den = __fmul_rn(q.sbf, gs);
     if (den != 0.0f) {
-        const float inv = __frcp_rn(den);  // correctly rounded reciprocal
+        const float inv = __fmul_rn(tb.rcp[q.sb], inv_gs);  // = the correctly rounded 1/den
         float qv[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) qv[t] = __fmul_rn(v[t], inv);
@@ -128,7 +165,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
     __shared__ uint32_t s_mask[kMaxBlocksPerRow];
     __shared__ int32_t s_base[kMaxBlocksPerRow];
     __shared__ __align__(16) uint16_t s_res[kQWarps][kMaxStagedK];
+    __shared__ QTables s_tab;
     const int tensor = blockIdx.y;
+    fill_tables(s_tab);
     const int nb = (int)(a.K >> 4);
     const int64_t kgroups = (nb + 3) >> 2;
     const bool has_sel = (MODE != kModeFake) && a.k > 0;
@@ -136,7 +175,9 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
 
     if (has_sel) {  // which elements of each block belong to S, and S's index of the first
         for (int b = threadIdx.x; b < nb; b += blockDim.x) s_mask[b] = 0u;
-        __syncthreads();
+    }
+    __syncthreads();  // tables (and the cleared masks) are ready
+    if (has_sel) {
         for (int s = threadIdx.x; s < a.k; s += blockDim.x) {
             int j = a.S[s];
             atomicOr(&s_mask[j >> 4], 1u << (j & 15));
@@ -212,7 +253,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
             BlockQ q;
             if (valid) {
                 unpack_block(ca, cb, v);
-                quant_block(v, gs, p6, q);
+                quant_block(v, gs, p6, inv_gs, s_tab, q);
             } else {
 #pragma unroll
                 for (int t = 0; t < 16; ++t) v[t] = 0.0f;
@@ -251,10 +292,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
                 const uint32_t mask = s_mask[b];
                 if (mask) {
                     const int base = s_base[b];
-#pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        if (mask & (1u << t)) {
-                            const int si = base + __popc(mask & ((1u << t) - 1u));
+                    for (uint32_t mm = mask; mm; mm &= mm - 1u) {
+                        const int t = __ffs(mm) - 1;
+                        const int si = base + __popc(mask & ((1u << t) - 1u));
+                        {
                             const float cs = __fmul_rn(e2m1_val(q.code(t)), q.sbf);  // exact
                             uint16_t val;
                             if (MODE == kModeWeight) {
@@ -262,7 +303,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
                             } else {
                                 // r = bf16(x - (code*sb)*gs), stored in units of gs
                                 const float xq = __fmul_rn(cs, gs);
-                                const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v[t], xq)));
+                                const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(sel16(v, t), xq)));
                                 val = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
                             }
                             if (staged) {
@@ -276,6 +317,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
                                 }
                             }
                         }
+                    }
                 }
             }
 
