@@ -319,6 +319,8 @@ def run_profile_case(args):
     """A single kernel on a reduced case sized for ncu (inputs above L2, a few
     hundred MB in all): `gemm13` (gate_up W4A4+RAC GEMM with SwiGLU, 32
     experts x 512 rows, N=3072, K=4096, k=128), `gemm_down` (N=4096, K=1536),
+    `gemm13_moe` / `gemm_down_moe` (the same GEMMs at the prefill layer's own
+    launch shape: 128 experts, segments of the Zipf routing, about 2 GB),
     `quantize_x` (16384 x 4096 scatter-quantize, top-8), `quantize_h`
     (147456 x 1536, k=128), `combine` (16384 tokens x 8 x 4096), `bf16_gemm`
     (QAT gate_up, BF16, same shape as gemm13).  Runs `--steps` launches."""
@@ -334,6 +336,21 @@ def run_profile_case(args):
     rows = E * per
     offsets = torch.arange(0, rows + 1, per, dtype=torch.int32, device=dev)
     case = args.profile_case
+    if case in ("gemm13_moe", "gemm_down_moe"):
+        # the prefill layer's own launch shape: 128 experts, the Zipf routing's padded segments
+        import synth
+
+        c = synth.CONFIGS[WORKLOAD]
+        T, E, topk = c["T"], c["E"], c["topk"]
+        rows = nv.rows_capacity(T, topk, E)
+        logits = synth.router_logits(WORKLOAD).to(dev)
+        ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+        rw = torch.empty((T, topk), dtype=torch.float32, device=dev)
+        counts = torch.empty(E, dtype=torch.int32, device=dev)
+        offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+        dst = torch.empty((T, topk), dtype=torch.int32, device=dev)
+        nv.nvfp4_route_topk(logits, topk, ids, rw, counts, offsets, dst)
+        case = case.replace("_moe", "")
     if case in ("gemm13", "gemm_down"):
         N, K = (3072, 4096) if case == "gemm13" else (4096, 1536)
         k = 128
@@ -352,7 +369,7 @@ def run_profile_case(args):
             a, a_s, r, gs_a, w, w_s, gs_w, sel, k, offsets, E, N, K, y,
             epilogue=nv.NVFP4_EPI_SWIGLU if swi else nv.NVFP4_EPI_NONE, out_dtype=nv.NVFP4_OUT_BF16,
             amax_out=amax if swi else None)
-        flops = 2 * rows * N * K
+        flops = 2 * int(offsets[-1].item()) * N * K
     elif case == "bf16_gemm":
         N, K = 3072, 4096
         x = torch.randn((rows, K), device=dev, generator=g).to(torch.bfloat16)

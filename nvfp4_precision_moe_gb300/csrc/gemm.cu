@@ -13,17 +13,21 @@
 // Output tiles are 128 rows x 256 columns; the K loop moves 128-byte wide
 // K-slices (256 FP4 or 64 BF16 elements) through 4 shared-memory stages fed
 // by TMA (128-byte swizzle).  Per FP4 stage: A 16 KB, B 32 KB, scales 6 KB.
-// Warp roles per CTA (448 threads):
+// Warp roles per CTA (512 threads, four warpgroups):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner + MMA issuer (one lane)
-//   warps 2-5   scale warps (FP4): once a stage has landed, each writes the
+//   warps 2-3   idle
+//   warps 4-7   scale warps (FP4): once a stage has landed, each writes the
 //               stage's block scales into its 32-lane quarter of tensor
 //               memory with tcgen05.st, replicated as the block-scaled MMA
 //               reads them.  (Copying them with tcgen05.cp instead occupies
 //               the tensor pipe between MMAs and costs about two thirds of
 //               the MMA rate.)
-//   warps 6-13  epilogue: warp w reads TMEM lane quarter w%4 and column half
-//               (w-6)/4 of the tile, scales, applies SwiGLU, stores.
+//   warps 8-15  epilogue: warp w reads TMEM lane quarter w%4 and column half
+//               (w-8)/4 of the tile -- all 128 of a thread's columns at once,
+//               in registers given up by the other warpgroups (setmaxnreg) --
+//               releases the accumulator, then scales, applies SwiGLU and
+//               stores while the next tile's MMAs run.
 // Tensor memory (512 columns): accumulator in columns 0-255; the scales of
 // the 4 stages in 48-column slots from column 256 (A: 16, B: 32).  The
 // accumulator is single-buffered: the epilogue reads it in two halves and
@@ -47,8 +51,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxExperts = 1024;
 constexpr int kEpiWarps = 8;
 constexpr int kSFWarps = 4;
-constexpr int kEpiWarp0 = 2 + kSFWarps;
-constexpr int kThreads = 64 + 32 * kSFWarps + 32 * kEpiWarps;
+constexpr int kSFWarp0 = 4;   // warpgroup 1
+constexpr int kEpiWarp0 = 8;  // warpgroups 2 and 3
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+// Register split (per thread) after launch at 65536 / 512 = 128: the producer
+// and MMA warpgroup and the scale warpgroup give registers to the epilogue,
+// which holds a thread's 128 accumulator columns at once.
+constexpr uint32_t kRegsCtl = 64, kRegsSF = 72, kRegsEpi = 184;
+static_assert(128 * kRegsCtl + 128 * kRegsSF + 256 * kRegsEpi <= 65536, "register split above the launch budget");
 constexpr int kStages = 4;
 
 // Instruction descriptors (M = 128, N = 256, both operands K-major).
@@ -62,8 +72,8 @@ template <bool FP4>
 struct Cfg {
     static constexpr int kStageBytes = kATileBytes + kBTileBytes + (FP4 ? kSFABytes + kSFBBytes : 0);
     static constexpr int kBarOffset = kStages * kStageBytes;
-    // barriers: full/empty/sf_ready per stage, acc_full, acc_empty, drain
-    static constexpr int kNumBars = 3 * kStages + 3;
+    // barriers: full/empty/sf_full/sf_ready per stage, acc_full, acc_empty, drain
+    static constexpr int kNumBars = 4 * kStages + 3;
     static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
     static constexpr int kGswOffset = kOffOffset + (kMaxExperts + 1) * 4;
     static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
@@ -82,6 +92,7 @@ struct GemmParams {
     int32_t epilogue, out_dtype;
     void *y;
     int64_t ldy;
+    int32_t vec32;  // y and its row pitch are 32-byte aligned: whole-sector stores
     float *amax_out;
     int32_t *dev_status;
 };
@@ -108,17 +119,34 @@ __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fdividef(g, 1.0f + e), u);
 }
 
+// 8 words to a 32-byte output segment: one whole-sector store when the
+// output allows it (stores are a large share of the kernel's L2 requests),
+// else two 16-byte stores.
+__device__ __forceinline__ void store32B(void *dst, bool vec32, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
+    if (vec32) {
+        st_global_v8(dst, a0, a1, a2, a3, a4, a5, a6, a7);
+    } else {
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        d[0] = make_uint4(a0, a1, a2, a3);
+        d[1] = make_uint4(a4, a5, a6, a7);
+    }
+}
+
 // 16 columns of this warp's TMEM rows -> 16 BF16 stores (32 bytes), or 16
 // FP32 stores (64 bytes); tracks max|stored value|.
 __device__ __forceinline__ void store16(const GemmParams &p, int64_t row, int64_t col, float gmul,
-                                        const uint32_t (&d)[16], float &amax_local) {
+                                        const uint32_t *d, float &amax_local) {
     float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(gmul, __uint_as_float(d[i]));
     if (p.out_dtype == NVFP4_OUT_F32) {
-        float4 *dst = reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + row * p.ldy + col);
+        float *dst = reinterpret_cast<float *>(p.y) + row * p.ldy + col;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        for (int i = 0; i < 2; ++i)
+            store32B(dst + 8 * i, p.vec32, __float_as_uint(v[8 * i]), __float_as_uint(v[8 * i + 1]),
+                     __float_as_uint(v[8 * i + 2]), __float_as_uint(v[8 * i + 3]), __float_as_uint(v[8 * i + 4]),
+                     __float_as_uint(v[8 * i + 5]), __float_as_uint(v[8 * i + 6]), __float_as_uint(v[8 * i + 7]));
 #pragma unroll
         for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
     } else {
@@ -129,15 +157,14 @@ __device__ __forceinline__ void store16(const GemmParams &p, int64_t row, int64_
             amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] << 16)));
             amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] & 0xffff0000u)));
         }
-        uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + col);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        store32B(reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + col, p.vec32, o[0], o[1], o[2], o[3], o[4], o[5],
+                 o[6], o[7]);
     }
 }
 
 // 16 SwiGLU outputs from 16 gate and 16 up columns -> 32 bytes of BF16.
-__device__ __forceinline__ void swiglu16(uint16_t *dst16, float gmul, const uint32_t (&g)[16],
-                                         const uint32_t (&u)[16], float &amax_local) {
+__device__ __forceinline__ void swiglu16(uint16_t *dst16, bool vec32, float gmul, const uint32_t *g,
+                                         const uint32_t *u, float &amax_local) {
     uint32_t o[8];
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
@@ -148,9 +175,7 @@ __device__ __forceinline__ void swiglu16(uint16_t *dst16, float gmul, const uint
         amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] << 16)));
         amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] & 0xffff0000u)));
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(dst16);
-    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    store32B(dst16, vec32, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
 }
 
 template <bool FP4>
@@ -163,7 +188,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
     uint64_t *empty = full + kStages;
-    uint64_t *sf_ready = empty + kStages;
+    uint64_t *sf_full = empty + kStages;
+    uint64_t *sf_ready = sf_full + kStages;
     uint64_t *acc_full = sf_ready + kStages;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *drain = acc_empty + 1;
@@ -181,6 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_full[s], 1);
             mbar_init(&sf_ready[s], kSFWarps);
         }
         mbar_init(acc_full, 1);
@@ -210,143 +237,156 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkt = FP4 ? (int)(p.K / 256) : (int)(p.K / 64);
     const int nrt = FP4 ? (p.k + 63) / 64 : 0;
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t issued_phase[kStages];
-            bool issued[kStages];
-            for (int s = 0; s < kStages; ++s) issued[s] = false;
-            bool ok = true;
-            const int64_t kgroups = p.K / 64;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int mt = tile / num_nt, nt = tile - mt * num_nt;
-                const int32_t m0 = mt * kBM;
-                const int e = expert_of(s_off, E, m0);
-                const int32_t brow = (int32_t)(e * p.N + (int64_t)nt * kBN);
-                // BF16 SwiGLU: B rows are the gate rows [128nt, +128) and the up rows N/2 + [128nt, +128)
-                const bool swiglu_rows = !FP4 && p.epilogue == NVFP4_EPI_SWIGLU;
-                const int32_t brow_lo = swiglu_rows ? (int32_t)(e * p.N + nt * 128) : brow;
-                const int32_t brow_hi = swiglu_rows ? (int32_t)(e * p.N + p.N / 2 + nt * 128) : brow + 128;
-                for (int it = 0; it < nkt + nrt; ++it) {
-                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *sa = smem + stage * C::kStageBytes;
-                    uint8_t *sb = sa + kATileBytes;
-                    if (it < nkt) {
-                        if (FP4) {
-                            mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes + kSFABytes + kSFBBytes);
-                            tma_load_2d(sa, &tmA, it * 128, m0, &full[stage]);
-                            tma_load_2d(sb, &tmB, it * 128, brow, &full[stage]);
-                            uint8_t *ssf = sb + kBTileBytes;
-                            const uint8_t *wsc = p.w_scales + (int64_t)e * p.N * (p.K / 16);
-                            bulk_load(ssf, p.a_scales + ((int64_t)mt * kgroups + it * 4) * 512, kSFABytes, &full[stage]);
-                            bulk_load(ssf + kSFABytes, wsc + ((int64_t)(2 * nt) * kgroups + it * 4) * 512, kSFBBytes / 2,
-                                      &full[stage]);
-                            bulk_load(ssf + kSFABytes + kSFBBytes / 2, wsc + ((int64_t)(2 * nt + 1) * kgroups + it * 4) * 512,
-                                      kSFBBytes / 2, &full[stage]);
-                        } else {
-                            mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
-                            tma_load_2d(sa, &tmA, it * 64, m0, &full[stage]);
-                            tma_load_2d(sb, &tmB, it * 64, brow_lo, &full[stage]);
-                            tma_load_2d(sb + kBTileBytes / 2, &tmB, it * 64, brow_hi, &full[stage]);
+    // one setmaxnreg per warpgroup, at the head of its role's code
+    if (warp < kSFWarp0) {
+        regs_dec<kRegsCtl>();
+        if (warp == 0) {
+            if (lane == 0) {
+                // ------------------------------------------------ TMA producer
+                int stage = 0;
+                uint32_t phase = 0;
+                uint32_t issued_phase[kStages];
+                bool issued[kStages];
+                for (int s = 0; s < kStages; ++s) issued[s] = false;
+                bool ok = true;
+                const int64_t kgroups = p.K / 64;
+                for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                    const int mt = tile / num_nt, nt = tile - mt * num_nt;
+                    const int32_t m0 = mt * kBM;
+                    const int e = expert_of(s_off, E, m0);
+                    const int32_t brow = (int32_t)(e * p.N + (int64_t)nt * kBN);
+                    // BF16 SwiGLU: B rows are the gate rows [128nt, +128) and the up rows N/2 + [128nt, +128)
+                    const bool swiglu_rows = !FP4 && p.epilogue == NVFP4_EPI_SWIGLU;
+                    const int32_t brow_lo = swiglu_rows ? (int32_t)(e * p.N + nt * 128) : brow;
+                    const int32_t brow_hi = swiglu_rows ? (int32_t)(e * p.N + p.N / 2 + nt * 128) : brow + 128;
+                    for (int it = 0; it < nkt + nrt; ++it) {
+                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                            ok = false;
+                            break;
                         }
-                    } else {  // RAC slice: residual rows and the selected weight columns
-                        const int r = it - nkt;
-                        mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
-                        tma_load_2d(sa, &tmR, r * 64, m0, &full[stage]);
-                        tma_load_2d(sb, &tmWs, r * 64, brow, &full[stage]);
-                    }
-                    issued[stage] = true;
-                    issued_phase[stage] = phase;
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
+                        uint8_t *sa = smem + stage * C::kStageBytes;
+                        uint8_t *sb = sa + kATileBytes;
+                        if (it < nkt) {
+                            if (FP4) {
+                                // the scales first, on their own barrier: the scale warps
+                                // move them to tensor memory while A and B are in flight
+                                uint8_t *ssf = sb + kBTileBytes;
+                                const uint8_t *wsc = p.w_scales + (int64_t)e * p.N * (p.K / 16);
+                                mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
+                                bulk_load(ssf, p.a_scales + ((int64_t)mt * kgroups + it * 4) * 512, kSFABytes, &sf_full[stage]);
+                                bulk_load(ssf + kSFABytes, wsc + ((int64_t)(2 * nt) * kgroups + it * 4) * 512, kSFBBytes / 2,
+                                          &sf_full[stage]);
+                                bulk_load(ssf + kSFABytes + kSFBBytes / 2, wsc + ((int64_t)(2 * nt + 1) * kgroups + it * 4) * 512,
+                                          kSFBBytes / 2, &sf_full[stage]);
+                                mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
+                                tma_load_2d(sa, &tmA, it * 128, m0, &full[stage]);
+                                tma_load_2d(sb, &tmB, it * 128, brow, &full[stage]);
+                            } else {
+                                mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
+                                tma_load_2d(sa, &tmA, it * 64, m0, &full[stage]);
+                                tma_load_2d(sb, &tmB, it * 64, brow_lo, &full[stage]);
+                                tma_load_2d(sb + kBTileBytes / 2, &tmB, it * 64, brow_hi, &full[stage]);
+                            }
+                        } else {  // RAC slice: residual rows and the selected weight columns
+                            const int r = it - nkt;
+                            if (FP4) mbar_arrive(&sf_full[stage]);  // no scales: the scale warps only pass
+                            mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
+                            tma_load_2d(sa, &tmR, r * 64, m0, &full[stage]);
+                            tma_load_2d(sb, &tmWs, r * 64, brow, &full[stage]);
+                        }
+                        issued[stage] = true;
+                        issued_phase[stage] = phase;
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
                 }
-            }
-            if (!ok) {
-                report(p.dev_status, NVFP4_ERR_TIMEOUT);
-                *abort_flag = 1;
-                // let every copy already issued land before the CTA can exit
-                for (int s = 0; s < kStages; ++s)
-                    if (issued[s]) (void)mbar_wait_bounded(&full[s], issued_phase[s], kWaitLimitNs);
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            int local = 0;
-            const uint32_t acc = tmem + kAcc;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-                // the epilogue has read the previous tile out of the accumulator
-                if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
-                    ok = false;
-                    break;
+                if (!ok) {
+                    report(p.dev_status, NVFP4_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    // let every copy already issued land before the CTA can exit
+                    for (int s = 0; s < kStages; ++s)
+                        if (issued[s]) {
+                            (void)mbar_wait_bounded(&full[s], issued_phase[s], kWaitLimitNs);
+                            if (FP4) (void)mbar_wait_bounded(&sf_full[s], issued_phase[s], kWaitLimitNs);
+                        }
                 }
-                tc_fence_after();
-                for (int it = 0; it < nkt + nrt; ++it) {
-                    if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
+            }
+        } else if (warp == 1) {
+            if (lane == 0) {
+                // ------------------------------------------------ MMA issuer
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                int local = 0;
+                const uint32_t acc = tmem + kAcc;
+                for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+                    // the epilogue has read the previous tile out of the accumulator
+                    if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
-                    const uint32_t b_addr = a_addr + kATileBytes;
-                    if (it < nkt) {
-                        if (FP4) {
-                            const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * kSFSlotCols;
-                            // the scale warps have written this stage's scales
-                            if (!mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescNVF4,
-                                            sf + 4 * c, sf + 16 + 8 * c, (it | c) != 0);
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescBF16,
-                                            (it | c) != 0);
+                    for (int it = 0; it < nkt + nrt; ++it) {
+                        if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
+                            ok = false;
+                            break;
                         }
-                    } else {
-                        // RAC: accumulate rg . W_sel^T into the same accumulator
-                        const int r = it - nkt;
-                        const int nm = min(4, (p.k - r * 64) / 16);
-                        for (int c = 0; c < nm; ++c)
-                            tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescBF16, 1u);
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+                        const uint32_t b_addr = a_addr + kATileBytes;
+                        if (it < nkt) {
+                            if (FP4) {
+                                const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * kSFSlotCols;
+                                // the scale warps have written this stage's scales
+                                if (!mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after();
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescNVF4,
+                                                sf + 4 * c, sf + 16 + 8 * c, (it | c) != 0);
+                            } else {
+#pragma unroll
+                                for (int c = 0; c < 4; ++c)
+                                    tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescBF16,
+                                                (it | c) != 0);
+                            }
+                        } else {
+                            // RAC: accumulate rg . W_sel^T into the same accumulator
+                            const int r = it - nkt;
+                            const int nm = min(4, (p.k - r * 64) / 16);
+                            for (int c = 0; c < nm; ++c)
+                                tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescBF16, 1u);
+                        }
+                        tc_commit(&empty[stage]);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
                     }
-                    tc_commit(&empty[stage]);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    if (!ok) break;
+                    tc_commit(acc_full);
                 }
-                if (!ok) break;
-                tc_commit(acc_full);
+                if (!ok) {
+                    report(p.dev_status, NVFP4_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                // no MMA may still run when TMEM is released: `drain` completes
+                // once every tcgen05 op this thread issued has finished
+                tc_commit(drain);
+                (void)mbar_wait_bounded(drain, 0, kWaitLimitNs);
             }
-            if (!ok) {
-                report(p.dev_status, NVFP4_ERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-            // no MMA may still run when TMEM is released: `drain` completes
-            // once every tcgen05 op this thread issued has finished
-            tc_commit(drain);
-            (void)mbar_wait_bounded(drain, 0, kWaitLimitNs);
-        }
+        }  // warps 2 and 3: idle
     } else if (warp < kEpiWarp0) {
+        regs_dec<kRegsSF>();
         // ---------------------------------------------------- scale warps
-        // Slice by slice in the producer's order: wait for the stage, then
-        // write its 12 scale chunks (512 bytes each: 32 rows of 16 bytes) into
+        // Slice by slice in the producer's order: wait for the stage's scales
+        // (their own barrier, so this overlaps the A/B copies), then write its
+        // 12 scale chunks (512 bytes each: 32 rows of 16 bytes) into
         // this warp's lane quarter.  Slot columns: A chunk c -> 4c..4c+3;
         // B chunk c -> 16+8c..16+8c+7 (its first and second 128 rows).  Lane
         // i, column base+j gets word j of row i of the chunk; every quarter
@@ -358,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
                 bool ok = true;
                 for (int it = 0; it < nkt + nrt; ++it) {
-                    const bool got = mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag);
+                    const bool got = mbar_wait_bounded(&sf_full[stage], phase, kWaitLimitNs, abort_flag);
                     if (!__all_sync(0xffffffffu, got)) {
                         ok = false;
                         break;
@@ -410,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
+        regs_inc<kRegsEpi>();
         // ---------------------------------------------------- epilogue
         const int ew = warp - kEpiWarp0;  // 0..7
         const int q = warp & 3;           // TMEM lane quarter this warp may access
@@ -433,48 +474,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const uint32_t acc = tmem + lane_base + kAcc;
+            // read this thread's 128 accumulator columns (two 64-column loads),
+            // release the accumulator, then scale and store while the next
+            // tile's MMAs run
+            uint32_t v[128];
+            if (swiglu) {
+                // output columns 64*half + [0, 64): gate = D[c], up = D[128 + c]
+                tmem_ld64(acc + 64 * half, v);
+                tmem_ld64(acc + 128 + 64 * half, v + 64);
+            } else {
+                tmem_ld64(acc + 128 * half, v);
+                tmem_ld64(acc + 128 * half + 64, v + 64);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
             const int mt = tile / num_nt, nt = tile - mt * num_nt;
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
             const float gmul = FP4 ? __fmul_rn(gsa, s_gsw[expert_of(s_off, E, mt * kBM)]) : 1.0f;
-            // two halves of this warp's work: the first is stored before the
-            // second is read, then the accumulator is released
-            uint32_t x0[16], x1[16], x2[16], x3[16];
-#pragma unroll 1
-            for (int part = 0; part < 2; ++part) {
-                if (swiglu) {
-                    // output columns 64*half + 32*part + [0, 32): gate = D[c], up = D[128 + c]
-                    const int c0 = 64 * half + 32 * part;
-                    tmem_ld16(acc + c0, x0);
-                    tmem_ld16(acc + 128 + c0, x1);
-                    tmem_ld16(acc + c0 + 16, x2);
-                    tmem_ld16(acc + 128 + c0 + 16, x3);
-                    tmem_ld_wait();
-                    if (part == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
-                    }
-                    uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 128 + c0;
-                    swiglu16(yrow, gmul, x0, x1, amax_local);
-                    swiglu16(yrow + 16, gmul, x2, x3, amax_local);
-                } else {
-                    const int c0 = 128 * half + 64 * part;
-                    tmem_ld16(acc + c0, x0);
-                    tmem_ld16(acc + c0 + 16, x1);
-                    tmem_ld16(acc + c0 + 32, x2);
-                    tmem_ld16(acc + c0 + 48, x3);
-                    tmem_ld_wait();
-                    if (part == 1) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(acc_empty);
-                    }
-                    const int64_t col = (int64_t)nt * kBN + c0;
-                    store16(p, row, col, gmul, x0, amax_local);
-                    store16(p, row, col + 16, gmul, x1, amax_local);
-                    store16(p, row, col + 32, gmul, x2, amax_local);
-                    store16(p, row, col + 48, gmul, x3, amax_local);
-                }
+            if (swiglu) {
+                uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 128 + 64 * half;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) swiglu16(yrow + 16 * j, p.vec32, gmul, v + 16 * j, v + 64 + 16 * j, amax_local);
+            } else {
+                const int64_t col = (int64_t)nt * kBN + 128 * half;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) store16(p, row, col + 16 * j, gmul, v + 16 * j, amax_local);
             }
         }
         if (p.amax_out) {
@@ -577,6 +603,8 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
     p.out_dtype = out_dtype;
     p.y = y;
     p.ldy = ldy;
+    p.vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) &&
+              (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
     p.amax_out = amax_out;
     p.dev_status = dev_status;
     const int64_t max_tiles = (rows_cap / kBM) * (N / kBN);
@@ -617,6 +645,8 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     p.out_dtype = out_dtype;
     p.y = y;
     p.ldy = ldy;
+    p.vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) &&
+              (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
     p.dev_status = dev_status;
     const int64_t max_tiles = (rows_cap / kBM) * (N / kBN);
     const int grid = (int)(max_tiles < sm_count() ? max_tiles : sm_count());
