@@ -436,33 +436,48 @@ __global__ void zero_pad_rows_kernel(const int32_t *counts, const int32_t *offse
     for (int64_t i = threadIdx.x; i < (K >> 3); i += blockDim.x) d[i] = make_uint4(0, 0, 0, 0);
 }
 
-// Eq. 23 squared scores: one thread per channel, rows in order, binary64.
-__global__ void channel_score_kernel(const uint16_t *x, int64_t M, int64_t K, const float *amax, double *ssq) {
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // K % 16 == 0, grid covers K
+// Eq. 23 squared scores in binary64, each channel's sum taken in row order.
+// A block owns 32 channels (one per lane); its 32 warps compute the squared
+// quantization errors of 32 rows at a time into shared memory, then warp 0
+// adds them to the channels' sums row by row, so every sum is the sequential
+// one while the element work runs on all warps.
+constexpr int kScoreWarps = 32;
+__global__ void __launch_bounds__(32 * kScoreWarps) channel_score_kernel(const uint16_t *x, int64_t M, int64_t K,
+                                                                         const float *amax, double *ssq) {
+    __shared__ double sq[kScoreWarps][33];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t j = (int64_t)blockIdx.x * 32 + lane;  // K % 16 == 0: a 16-lane block is all valid or all not
     const bool valid = j < K;
     const float gs = tensor_scale(amax[0]);
     const float p6 = __fmul_rn(gs, 6.0f);
     const double gsd = (double)gs;
     double acc = 0.0;
-    for (int64_t i = 0; i < M; ++i) {
-        float v = valid ? __uint_as_float((uint32_t)x[i * K + j] << 16) : 0.0f;
+    for (int64_t i0 = 0; i0 < M; i0 += kScoreWarps) {
+        const int64_t i = i0 + w;
+        float v = (valid && i < M) ? __uint_as_float((uint32_t)x[i * K + j] << 16) : 0.0f;
         float am = fabsf(v);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-        float sbf = e4m3_to_f32(e4m3_from_f32(__fdiv_rn(am, p6)));
-        float den = __fmul_rn(sbf, gs);
+        const float sbf = e4m3_to_f32(e4m3_from_f32(__fdiv_rn(am, p6)));
+        const float den = __fmul_rn(sbf, gs);
         uint32_t c;
         if (den != 0.0f) {
-            float qv = __fmul_rn(v, __frcp_rn(den));
+            const float qv = __fmul_rn(v, __frcp_rn(den));
             c = e2m1x2_from_f32(qv, qv) & 15u;
         } else {
             c = (__float_as_uint(v) >> 31) << 3;
         }
-        double xq = __dmul_rn((double)__fmul_rn(e2m1_to_f32(c), sbf), gsd);  // exact
-        double d = __dsub_rn(xq, (double)v);
-        acc = __dadd_rn(acc, __dmul_rn(d, d));
+        const double xq = __dmul_rn((double)__fmul_rn(e2m1_to_f32(c), sbf), gsd);  // exact
+        const double d = __dsub_rn(xq, (double)v);
+        sq[w][lane] = __dmul_rn(d, d);
+        __syncthreads();
+        if (w == 0) {
+            const int n = (M - i0 < kScoreWarps) ? (int)(M - i0) : kScoreWarps;
+            for (int r = 0; r < n; ++r) acc = __dadd_rn(acc, sq[r][lane]);
+        }
+        __syncthreads();
     }
-    if (valid) ssq[j] = acc;
+    if (w == 0 && valid) ssq[j] = acc;
 }
 
 // Eq. 24: keep the k largest (ties to the lower index), write them in order.
@@ -678,7 +693,8 @@ extern "C" int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, co
     if (K == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
     cudaStream_t st = (cudaStream_t)stream;
-    channel_score_kernel<<<(unsigned)((K + 255) / 256), 256, 0, st>>>((const uint16_t *)x, M, K, amax, score_ws);
+    channel_score_kernel<<<(unsigned)((K + 31) / 32), 32 * kScoreWarps, 0, st>>>((const uint16_t *)x, M, K, amax,
+                                                                                 score_ws);
     int s = launch_status("channel_score_kernel");
     if (s != NVFP4_OK || k == 0) return s;
     select_topk_kernel<<<1, 1024, 0, st>>>(score_ws, K, k, S_out);
