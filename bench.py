@@ -31,7 +31,8 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core ratio, nominal
 
 # DRAM bytes (read + write) of one gate_up GEMM launch at this workload's launch shape, from
 # one ncu capture (profiles/grouped_gemm_kernel_moe_prefill.md), valid only for the kernel
-# sources it was taken on: reported as null once they change.
+# sources it was taken on (common.cuh, gemm_common.cuh, gemm_single.cu): reported as null
+# once they change.
 GATE_UP_TRAFFIC = {"bytes": 1362224000 + 414388480,
                    "sources_sha256": "e29bfbf6e9332e980a7e65ad97376795903e2749dfeeb9af30a1e2be4919e040"}
 
@@ -40,7 +41,7 @@ def gate_up_traffic():
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("common.cuh", "gemm.cu"):
+    for f in ("common.cuh", "gemm_common.cuh", "gemm_single.cu"):
         with open(os.path.join(ROOT, "nvfp4_precision_moe_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return GATE_UP_TRAFFIC["bytes"] if h.hexdigest() == GATE_UP_TRAFFIC["sources_sha256"] else None
@@ -249,7 +250,7 @@ def run_ours(args):
         "fp4_peak_frac_step": round(world * f4 / (ms_step * 1e-3) / 1e12 / fp4_peak, 4),
         "quantize_x": {"gbs": round(q_gbs, 1), "hbm_frac": round(q_gbs / pk["hbm"], 4), "bytes": q_bytes},
         "stages_ms": {n: round(v, 4) for n, v in stage.items()},
-        "roofline": {"kernel": "grouped_gemm_kernel<fp4> (gate_up, SwiGLU)", "bound": "tensor",
+        "roofline": {"kernel": "single_gemm_kernel<fp4> (gate_up, SwiGLU)", "bound": "tensor",
                      "achieved": round(gemm13_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm13_tflops / fp4_peak, 4), "traffic": gate_up_traffic(),
                      "peak_src": "%s bf16 burst x nominal fp4/bf16 ratio 6" % pk["src"]},

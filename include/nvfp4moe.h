@@ -62,6 +62,7 @@ typedef enum {
 enum { NVFP4_OUT_F32 = 0, NVFP4_OUT_BF16 = 1 };
 /* Epilogue of the W4A4 + RAC GEMM. */
 enum { NVFP4_EPI_NONE = 0, NVFP4_EPI_SWIGLU = 1 };
+enum { NVFP4_PIPELINE_AUTO = 0, NVFP4_PIPELINE_SINGLE = 1, NVFP4_PIPELINE_PAIR = 2 };
 
 /* Name of a status code ("NVFP4_OK", ...); never NULL. */
 const char *nvfp4_status_str(int status);
@@ -208,7 +209,8 @@ int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, const float *
  *                     NVFP4_EPI_SWIGLU: the weights were prepared with
  *                     interleave = 1; y = bf16(silu(gate) * up) [rows_cap, N/2]
  *                     (ldy >= N/2, out_dtype must be BF16).
- * Output tiles are 128 rows x 256 columns.
+ * Tiles: 128 x 256 outputs per CTA (single-CTA pipeline, the default for this
+ * kind) or 256 x 256 per CTA pair (pair pipeline); see nvfp4_gemm_pipeline.
  *   out_dtype         NVFP4_OUT_F32 or NVFP4_OUT_BF16 (= bf16_rn of the F32 value)
  *   amax_out          device float or NULL: receives max|y| of the stored
  *                     values (the next quantize's amax); the call clears it
@@ -239,6 +241,18 @@ int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const int32_t *off
                             int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype,
                             int32_t epilogue, void *y, int64_t ldy, int32_t *dev_status,
                             void *stream);
+
+/* Pipeline of the two grouped GEMMs above (no counterpart in the paper: an
+ * implementation choice).  Both pipelines compute the same results:
+ *   NVFP4_PIPELINE_SINGLE  one CTA per 128 x 256 output tile (tcgen05 cta_group::1)
+ *   NVFP4_PIPELINE_PAIR    a cluster of two CTAs per 256 x 256 tile
+ *                          (tcgen05 cta_group::2: each SM holds half of B)
+ *   NVFP4_PIPELINE_AUTO    (initial) the one measured faster per kind on GB300:
+ *                          single for W4A4 + RAC, pair for BF16.
+ * Process-wide; takes effect for calls made after it returns.
+ *   previous  host int32 or NULL: receives the setting it replaces.
+ * Errors: INVALID_ARG (unknown value). */
+int nvfp4_gemm_pipeline(int32_t which, int32_t *previous);
 
 /* ------------------------------------------------------------------------ */
 /* MoE routing, dispatch and combine (not described by QUADS; the plainest    */

@@ -20,6 +20,7 @@ from .build import LIB, build_library
 
 NVFP4_OUT_F32, NVFP4_OUT_BF16 = 0, 1
 NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU = 0, 1
+NVFP4_PIPELINE_AUTO, NVFP4_PIPELINE_SINGLE, NVFP4_PIPELINE_PAIR = 0, 1, 2
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED",
           3: "NVFP4_ERR_ALIGNMENT", 4: "NVFP4_ERR_CUDA", 5: "NVFP4_ERR_TIMEOUT",
           6: "NVFP4_ERR_NONFINITE", 7: "NVFP4_ERR_ARCH"}
@@ -35,6 +36,7 @@ _SIGS = {
     "nvfp4_rac_select_channels": "pqqpippp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
     "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
+    "nvfp4_gemm_pipeline": "ip",
     "nvfp4_route_topk": "piiipppppp",
     "nvfp4_moe_clear_padding": "ppiqqipppp",
     "nvfp4_moe_scatter_rows": "piqipppiqpp",
@@ -171,6 +173,14 @@ def nvfp4_bf16_grouped_gemm(x, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F
     rows_cap = x.shape[0]
     _call("nvfp4_bf16_grouped_gemm", _p(x), _p(w_hat), _p(offsets), E, rows_cap, N, K, out_dtype,
           epilogue, _p(y), y.stride(0), _p(dev_status), _s(stream))
+
+
+def nvfp4_gemm_pipeline(which):
+    """Selects the grouped-GEMM pipeline (NVFP4_PIPELINE_AUTO / _SINGLE / _PAIR)
+    for later calls, process-wide; returns the previous setting."""
+    prev = ctypes.c_int32(0)
+    _call("nvfp4_gemm_pipeline", which, ctypes.byref(prev))
+    return prev.value
 
 
 def nvfp4_route_topk(logits, topk, ids, weights, counts, offsets, dst_row, stream=None):

@@ -1,661 +1,33 @@
-// gemm.cu -- grouped GEMMs on the 5th-generation tensor cores (tcgen05, sm_103a).
-//
-// Two instantiations of one warp-specialised, persistent pipeline:
-//  * FP4=true : the W4A4 + RAC GEMM of QUADS §3.3 Eq. 21.  The main product
-//    runs as block-scaled E2M1 x E2M1 MMAs (kind::mxf4nvf4, one UE4M3 scale
-//    per 16 K-elements, scale_vec::4X); the rank-k residual correction
-//    rg . W_sel^T runs as BF16 MMAs (kind::f16) into the same FP32
-//    accumulator -- the residual arrives in units of the activation's
-//    power-of-two tensor scale, so both sums share the units (ca*sa)(cw*sw)
-//    -- and the epilogue multiplies by gs_a*gs_w (optionally with SwiGLU).
-//  * FP4=false: the BF16 GEMM of the asymmetric-QAT forward, QUADS §3.2 Eq. 12.
-//
-// Output tiles are 128 rows x 256 columns; the K loop moves 128-byte wide
-// K-slices (256 FP4 or 64 BF16 elements) through 4 shared-memory stages fed
-// by TMA (128-byte swizzle).  Per FP4 stage: A 16 KB, B 32 KB, scales 6 KB.
-// Warp roles per CTA (512 threads, four warpgroups):
-//   warp 0      TMA producer (one lane)
-//   warp 1      TMEM owner + MMA issuer (one lane)
-//   warps 2-3   idle
-//   warps 4-7   scale warps (FP4): once a stage has landed, each writes the
-//               stage's block scales into its 32-lane quarter of tensor
-//               memory with tcgen05.st, replicated as the block-scaled MMA
-//               reads them.  (Copying them with tcgen05.cp instead occupies
-//               the tensor pipe between MMAs and costs about two thirds of
-//               the MMA rate.)
-//   warps 8-15  epilogue: warp w reads TMEM lane quarter w%4 and column half
-//               (w-8)/4 of the tile -- all 128 of a thread's columns at once,
-//               in registers given up by the other warpgroups (setmaxnreg) --
-//               releases the accumulator, then scales, applies SwiGLU and
-//               stores while the next tile's MMAs run.
-// Tensor memory (512 columns): accumulator in columns 0-255; the scales of
-// the 4 stages in 48-column slots from column 256 (A: 16, B: 32).  The
-// accumulator is single-buffered: the epilogue reads it in two halves and
-// releases it after the second read, so the next tile's MMAs wait only for
-// the first half's stores.
-// Expert segments are contiguous 128-row groups of the routed rows, so the
-// tile list is (row tile, column tile) over all routed rows; each tile's
-// expert comes from a binary search of the segment offsets.
-#include "common.cuh"
+// gemm.cu -- the grouped-GEMM entry points: argument checks, tensor maps, and
+// the choice between the two tcgen05 pipelines (gemm_single.cu: one CTA per
+// 128x256 tile; gemm_pair.cu: a CTA pair per 256x256 tile).  By default each
+// kind runs on the pipeline measured faster for it on GB300 -- FP4 (W4A4 +
+// RAC) on the single-CTA pipeline, BF16 on the pair pipeline;
+// nvfp4_gemm_pipeline() overrides the choice process-wide.
+#include <atomic>
 
-namespace nvfp4 {
-
-constexpr int kBM = 128;             // rows per CTA; a CTA pair covers 256
-constexpr int kBN = 256;             // output columns per tile
-constexpr int kATileBytes = 16384;   // 128 rows x 128 bytes
-constexpr int kBHalfBytes = 16384;   // this CTA's 128 of the tile's 256 B rows
-constexpr int kSFABytes = 2048;      // 4 MMA-K chunks x 512 bytes (128 rows x 4 scales)
-constexpr int kSFBBytes = 4096;      // all 256 B rows: each SM reads the whole set from its own TMEM
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAcc = 0, kSFCol0 = 256, kSFSlotCols = 48;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
-constexpr uint64_t kSettleNs = 200000ull;         // after an abort: 200 us for copies in flight
-constexpr int kMaxExperts = 1024;
-constexpr int kEpiWarps = 8;
-constexpr int kSFWarps = 4;
-constexpr int kSFWarp0 = 4;   // warpgroup 1
-constexpr int kEpiWarp0 = 8;  // warpgroups 2 and 3
-constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
-// Register split (per thread) after launch at 65536 / 512 = 128: the producer
-// and MMA warpgroup and the scale warpgroup give registers to the epilogue,
-// which holds a thread's 128 accumulator columns at once.
-constexpr uint32_t kRegsCtl = 96, kRegsSF = 64, kRegsEpi = 176;
-static_assert(128 * kRegsCtl + 128 * kRegsSF + 256 * kRegsEpi <= 65536, "register split above the launch budget");
-
-// Instruction descriptors of the 2-SM MMA (M = 256, N = 256, both operands K-major).
-//  kind::mxf4nvf4: A, B = E2M1 (1) at bits 7-9 / 10-12, N>>3 at 17, scale
-//  format UE4M3 (0) at bit 23, M>>4 at 24, scale-factor ids 0.
-constexpr uint32_t kIdescNVF4 = (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) | (((2 * kBM) >> 4) << 24);
-//  kind::f16: D = F32 (1) at bits 4-5, A, B = BF16 (1).
-constexpr uint32_t kIdescBF16 = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) | (((2 * kBM) >> 4) << 24);
-
-template <bool FP4>
-struct Cfg {
-    // FP4 stage: A 16 KB + B half 16 KB + scales 6 KB; BF16 stage: A + B half
-    static constexpr int kStages = FP4 ? 5 : 6;
-    static constexpr int kStageBytes = kATileBytes + kBHalfBytes + (FP4 ? kSFABytes + kSFBBytes : 0);
-    static constexpr int kBarOffset = kStages * kStageBytes;
-    // barriers: full/empty/sf_full/sf_ready per stage, acc_full, acc_empty, drain
-    static constexpr int kNumBars = 4 * kStages + 3;
-    static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
-    static constexpr int kPairOffset = kOffOffset + (kMaxExperts + 1) * 4;
-    static constexpr int kGswOffset = kPairOffset + (kMaxExperts + 1) * 4;
-    static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
-};
-static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<false>::kSmemBytes <= 232448, "shared memory budget");
-static_assert(kSFCol0 + Cfg<true>::kStages * kSFSlotCols <= kTmemCols, "tensor memory budget");
-static_assert(Cfg<true>::kStageBytes % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0, "stage alignment");
-
-struct GemmParams {
-    const uint8_t *a_scales;
-    const uint8_t *w_scales;
-    const float *gs_a;
-    const float *gs_w;
-    const int32_t *offsets;
-    int32_t rows_cap;
-    int32_t E, k;
-    int64_t N, K;
-    int32_t epilogue, out_dtype;
-    void *y;
-    int64_t ldy;
-    int32_t vec32;  // y and its row pitch are 32-byte aligned: whole-sector stores
-    float *amax_out;
-    int32_t *dev_status;
-};
-
-// Work item (pair of 128-row tiles of one expert, column tile).  Each expert's
-// 128-row tiles are paired in order; an odd last tile is paired with a phantom
-// (rows past the segment) that the peer computes but never stores.
-struct PairTile {
-    int e, nt;
-    int32_t m0;       // this CTA's first row
-    int32_t lead_m0;  // the leader's first row (always a real tile)
-    bool live;        // this CTA's rows belong to the expert
-};
-
-__device__ __forceinline__ PairTile decode_item(const int32_t *off, const int32_t *pairs, int E, int num_nt, int item,
-                                                uint32_t rank) {
-    PairTile t;
-    const int q = item / num_nt;
-    t.nt = item - q * num_nt;
-    int lo = 0, hi = E - 1;  // the expert e with pairs[e] <= q < pairs[e+1]
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pairs[mid] <= q) lo = mid;
-        else hi = mid - 1;
-    }
-    t.e = lo;
-    t.lead_m0 = off[lo] + 2 * kBM * (q - pairs[lo]);
-    t.m0 = t.lead_m0 + kBM * (int32_t)rank;
-    t.live = t.m0 < off[lo + 1];
-    return t;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a)) |
-           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(b)) << 16);
-}
-
-// silu(g) * u with the fast exponential and division (a few ulp; the BF16
-// rounding of the result dominates).
-__device__ __forceinline__ float swiglu1(float g, float u) {
-    const float e = __expf(-g);
-    return __fmul_rn(__fdividef(g, 1.0f + e), u);
-}
-
-// 8 words to a 32-byte output segment: one whole-sector store when the
-// output allows it (stores are a large share of the kernel's L2 requests),
-// else two 16-byte stores.
-__device__ __forceinline__ void store32B(void *dst, bool vec32, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t a4, uint32_t a5, uint32_t a6, uint32_t a7) {
-    if (vec32) {
-        st_global_v8(dst, a0, a1, a2, a3, a4, a5, a6, a7);
-    } else {
-        uint4 *d = reinterpret_cast<uint4 *>(dst);
-        d[0] = make_uint4(a0, a1, a2, a3);
-        d[1] = make_uint4(a4, a5, a6, a7);
-    }
-}
-
-// 16 columns of this warp's TMEM rows -> 16 BF16 stores (32 bytes), or 16
-// FP32 stores (64 bytes); tracks max|stored value|.
-__device__ __forceinline__ void store16(const GemmParams &p, int64_t row, int64_t col, float gmul,
-                                        const uint32_t *d, float &amax_local) {
-    float v[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __fmul_rn(gmul, __uint_as_float(d[i]));
-    if (p.out_dtype == NVFP4_OUT_F32) {
-        float *dst = reinterpret_cast<float *>(p.y) + row * p.ldy + col;
-#pragma unroll
-        for (int i = 0; i < 2; ++i)
-            store32B(dst + 8 * i, p.vec32, __float_as_uint(v[8 * i]), __float_as_uint(v[8 * i + 1]),
-                     __float_as_uint(v[8 * i + 2]), __float_as_uint(v[8 * i + 3]), __float_as_uint(v[8 * i + 4]),
-                     __float_as_uint(v[8 * i + 5]), __float_as_uint(v[8 * i + 6]), __float_as_uint(v[8 * i + 7]));
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax_local = fmaxf(amax_local, fabsf(v[i]));
-    } else {
-        uint32_t o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] << 16)));
-            amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i] & 0xffff0000u)));
-        }
-        store32B(reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + col, p.vec32, o[0], o[1], o[2], o[3], o[4], o[5],
-                 o[6], o[7]);
-    }
-}
-
-// 16 SwiGLU outputs from 16 gate and 16 up columns -> 32 bytes of BF16.
-__device__ __forceinline__ void swiglu16(uint16_t *dst16, bool vec32, float gmul, const uint32_t *g,
-                                         const uint32_t *u, float &amax_local) {
-    uint32_t o[8];
-#pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-        const float h0 = swiglu1(__fmul_rn(gmul, __uint_as_float(g[i])), __fmul_rn(gmul, __uint_as_float(u[i])));
-        const float h1 =
-            swiglu1(__fmul_rn(gmul, __uint_as_float(g[i + 1])), __fmul_rn(gmul, __uint_as_float(u[i + 1])));
-        o[i / 2] = pack_bf16x2(h0, h1);
-        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] << 16)));
-        amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] & 0xffff0000u)));
-    }
-    store32B(dst16, vec32, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
-}
-
-template <bool FP4>
-__global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmWs,
-                        GemmParams p) {
-    using C = Cfg<FP4>;
-    constexpr int kStages = C::kStages;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
-    uint64_t *empty = full + kStages;
-    uint64_t *sf_full = empty + kStages;
-    uint64_t *sf_ready = sf_full + kStages;
-    uint64_t *acc_full = sf_ready + kStages;
-    uint64_t *acc_empty = acc_full + 1;
-    uint64_t *drain = acc_empty + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::kOffOffset);
-    int32_t *s_pairs = reinterpret_cast<int32_t *>(smem + C::kPairOffset);
-    float *s_gsw = reinterpret_cast<float *>(smem + C::kGswOffset);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-    const int E = p.E;
-    // rows beyond the caller's buffers are never touched, whatever offsets hold
-    const int32_t row_limit = p.rows_cap & ~(kBM - 1);
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = min(max(p.offsets[i], 0), row_limit);
-    if (FP4)
-        for (int i = threadIdx.x; i < E; i += blockDim.x) s_gsw[i] = p.gs_w[i];
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);                  // leader: its producer + both CTAs' operand bytes
-            mbar_init(&empty[s], 1);                 // the leader's MMA commit, sent to both CTAs
-            mbar_init(&sf_full[s], 1);               // this CTA's scale bytes
-            mbar_init(&sf_ready[s], 2 * kSFWarps);   // leader: the scale warps of both CTAs
-        }
-        mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 2 * kEpiWarps);  // leader: the epilogue warps of both CTAs
-        mbar_init(drain, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-        if (FP4 && p.k > 0) {
-            prefetch_tmap(&tmR);
-            prefetch_tmap(&tmWs);
-        }
-    }
-    if (warp == 1) tmem_alloc_pair(tmem_slot, kTmemCols);
-    __syncthreads();  // s_off is complete
-    if (warp == 2) {
-        // pairs[e] = sum over e' < e of ceil(tiles(e') / 2): a warp-wide exclusive scan
-        const int per = (E + 31) >> 5;
-        auto npairs = [&](int e) {
-            const int32_t t = (s_off[e + 1] - s_off[e]) / kBM;
-            return t > 0 ? (t + 1) >> 1 : 0;
-        };
-        int sum = 0;
-        for (int i = 0; i < per; ++i) {
-            const int e = lane * per + i;
-            if (e < E) sum += npairs(e);
-        }
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - sum;
-        for (int i = 0; i < per; ++i) {
-            const int e = lane * per + i;
-            if (e < E) {
-                s_pairs[e] = run;
-                run += npairs(e);
-            }
-        }
-        if (lane == 31) s_pairs[E] = incl;
-    }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();  // both CTAs' barriers and tensor memory exist before either signals the other
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-
-    const int num_nt = (int)(p.N / kBN);
-    const int num_items = s_pairs[E] * num_nt;
-    const int item0 = (int)(blockIdx.x >> 1), item_step = (int)(gridDim.x >> 1);
-    const int nkt = FP4 ? (int)(p.K / 256) : (int)(p.K / 64);
-    const int nrt = FP4 ? (p.k + 63) / 64 : 0;
-
-    // one setmaxnreg per warpgroup, at the head of its role's code
-    if (warp < kSFWarp0) {
-        regs_dec<kRegsCtl>();
-        if (warp == 0) {
-            if (lane == 0) {
-                // ------------------------------------------------ TMA producer (both CTAs)
-                // A rows and this CTA's half of the B rows land in this CTA's
-                // shared memory; their bytes complete on the leader's full barrier.
-                int stage = 0;
-                uint32_t phase = 0;
-                uint32_t issued_phase[kStages];
-                bool issued[kStages];
-                for (int s = 0; s < kStages; ++s) issued[s] = false;
-                bool ok = true;
-                const int64_t kgroups = p.K / 64;
-                const uint32_t full_lead = cluster_addr(full, 0);
-                for (int item = item0; ok && item < num_items; item += item_step) {
-                    const PairTile t = decode_item(s_off, s_pairs, E, num_nt, item, rank);
-                    const int64_t sfa_tile = (t.live ? t.m0 : t.lead_m0) / kBM;  // scales of a real tile
-                    const int e = t.e, nt = t.nt;
-                    const int32_t brow = (int32_t)(e * p.N + (int64_t)nt * kBN);
-                    // this CTA's B rows: [n0 + 128 rank, +128); for the BF16 SwiGLU the gate
-                    // rows [128nt, +128) (leader) or the up rows N/2 + [128nt, +128) (peer)
-                    const bool swiglu_rows = !FP4 && p.epilogue == NVFP4_EPI_SWIGLU;
-                    const int32_t brow_mine =
-                        swiglu_rows ? (int32_t)(e * p.N + (int64_t)rank * (p.N / 2) + nt * 128) : brow + kBM * (int32_t)rank;
-                    for (int it = 0; it < nkt + nrt; ++it) {
-                        if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        uint8_t *sa = smem + stage * C::kStageBytes;
-                        uint8_t *sb = sa + kATileBytes;
-                        if (FP4) {
-                            if (it < nkt) {
-                                // the scales first, on this CTA's own barrier: the scale
-                                // warps move them to tensor memory while A and B are in flight
-                                uint8_t *ssf = sb + kBHalfBytes;
-                                const uint8_t *wsc = p.w_scales + (int64_t)e * p.N * (p.K / 16);
-                                mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
-                                bulk_load(ssf, p.a_scales + (sfa_tile * kgroups + it * 4) * 512, kSFABytes, &sf_full[stage]);
-                                bulk_load(ssf + kSFABytes, wsc + ((int64_t)(2 * nt) * kgroups + it * 4) * 512, kSFBBytes / 2,
-                                          &sf_full[stage]);
-                                bulk_load(ssf + kSFABytes + kSFBBytes / 2,
-                                          wsc + ((int64_t)(2 * nt + 1) * kgroups + it * 4) * 512, kSFBBytes / 2,
-                                          &sf_full[stage]);
-                            } else {
-                                mbar_arrive(&sf_full[stage]);  // no scales: the scale warps only pass
-                            }
-                        }
-                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kATileBytes + kBHalfBytes));
-                        const uint32_t fb = full_lead + 8u * (uint32_t)stage;
-                        if (it < nkt) {
-                            const int32_t x = FP4 ? it * 128 : it * 64;
-                            tma_load_2d_pair(sa, &tmA, x, t.m0, fb);
-                            tma_load_2d_pair(sb, &tmB, x, brow_mine, fb);
-                        } else {  // RAC slice: residual rows and the selected weight columns
-                            const int r = it - nkt;
-                            tma_load_2d_pair(sa, &tmR, r * 64, t.m0, fb);
-                            tma_load_2d_pair(sb, &tmWs, r * 64, brow_mine, fb);
-                        }
-                        issued[stage] = true;
-                        issued_phase[stage] = phase;
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                }
-                if (!ok) {
-                    report(p.dev_status, NVFP4_ERR_TIMEOUT);
-                    *abort_flag = 1;
-                    // Every copy already issued must land before the CTAs can exit.  This
-                    // CTA's scale copies complete on its own barrier; the operand copies of
-                    // both CTAs complete on the leader's, which the peer cannot watch and
-                    // the leader may not have armed yet.  So wait for what can be watched,
-                    // then hold the CTA for a settle window far longer than a copy takes;
-                    // the cluster barrier at the end keeps the other CTA alive as long.
-                    for (int s = 0; s < kStages; ++s)
-                        if (issued[s]) {
-                            if (leader) (void)mbar_wait_bounded(&full[s], issued_phase[s], kWaitLimitNs);
-                            if (FP4) (void)mbar_wait_bounded(&sf_full[s], issued_phase[s], kWaitLimitNs);
-                        }
-                    const uint64_t t0 = global_ns();
-                    while (global_ns() - t0 < kSettleNs) {
-                    }
-                }
-            }
-        } else if (warp == 1) {
-            if (lane == 0 && leader) {
-                // ------------------------------------------------ MMA issuer (leader)
-                int stage = 0;
-                uint32_t phase = 0;
-                bool ok = true;
-                int local = 0;
-                const uint32_t acc = tmem + kAcc;
-                for (int item = item0; ok && item < num_items; item += item_step, ++local) {
-                    // both epilogues have read the previous tile out of the accumulators
-                    if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    for (int it = 0; it < nkt + nrt; ++it) {
-                        if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        // the scale warps of both CTAs are done with this stage (they
-                        // pass RAC slices too): every phase of sf_ready is consumed here,
-                        // in order, so no arrival of a later use can land in this one
-                        if (FP4 && !mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
-                        const uint32_t b_addr = a_addr + kATileBytes;
-                        if (it < nkt) {
-                            if (FP4) {
-                                const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * kSFSlotCols;
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    tc_mma_nvf4_pair(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                                     kIdescNVF4, sf + 4 * c, sf + 16 + 8 * c, (it | c) != 0);
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < 4; ++c)
-                                    tc_mma_bf16_pair(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                                     kIdescBF16, (it | c) != 0);
-                            }
-                        } else {
-                            // RAC: accumulate rg . W_sel^T into the same accumulator
-                            const int r = it - nkt;
-                            const int nm = min(4, (p.k - r * 64) / 16);
-                            for (int c = 0; c < nm; ++c)
-                                tc_mma_bf16_pair(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                                 kIdescBF16, 1u);
-                        }
-                        tc_commit_pair_mc(&empty[stage]);  // frees the stage in both CTAs
-                        if (++stage == kStages) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                    }
-                    if (!ok) break;
-                    tc_commit_pair_mc(acc_full);
-                }
-                if (!ok) {
-                    report(p.dev_status, NVFP4_ERR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                // no MMA may still run when tensor memory is released: `drain`
-                // completes once every tcgen05 op this thread issued has finished
-                tc_commit_pair(drain);
-                (void)mbar_wait_bounded(drain, 0, kWaitLimitNs);
-            }
-        }  // warps 2 and 3: idle
-    } else if (warp < kEpiWarp0) {
-        regs_dec<kRegsSF>();
-        // ---------------------------------------------------- scale warps (both CTAs)
-        // Slice by slice in the producer's order: wait for the stage's scales
-        // (their own barrier, so this overlaps the A/B copies), then write its
-        // 12 scale chunks (512 bytes each: 32 rows of 16 bytes) into this
-        // warp's lane quarter.  Slot columns: A chunk c -> 4c..4c+3; B chunk c
-        // -> 16+8c..16+8c+7 (B rows 0-127, then 128-255).  Lane i, column
-        // base+j gets word j of row i of the chunk; every quarter holds the
-        // same copy.  Then one arrival per warp on the leader's sf_ready.
-        if (FP4) {
-            const uint32_t q = (uint32_t)(warp & 3);
-            const uint32_t ready_lead = cluster_addr(sf_ready, 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int item = item0; item < num_items; item += item_step) {
-                bool ok = true;
-                for (int it = 0; it < nkt + nrt; ++it) {
-                    const bool got = mbar_wait_bounded(&sf_full[stage], phase, kWaitLimitNs, abort_flag);
-                    if (!__all_sync(0xffffffffu, got)) {
-                        ok = false;
-                        break;
-                    }
-                    if (it < nkt) {
-                        const uint8_t *sfs = smem + stage * C::kStageBytes + kATileBytes + kBHalfBytes;
-                        uint32_t r0[32], r1[16];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // A: columns 4c..4c+3
-                            const uint4 w = *reinterpret_cast<const uint4 *>(sfs + 512 * c + 16 * lane);
-                            r0[4 * c] = w.x;
-                            r0[4 * c + 1] = w.y;
-                            r0[4 * c + 2] = w.z;
-                            r0[4 * c + 3] = w.w;
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // B: columns 16+8c (rows 0-127), 20+8c (rows 128-255)
-                            const uint4 lo = *reinterpret_cast<const uint4 *>(sfs + kSFABytes + 512 * c + 16 * lane);
-                            const uint4 hi =
-                                *reinterpret_cast<const uint4 *>(sfs + kSFABytes + kSFBBytes / 2 + 512 * c + 16 * lane);
-                            const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int col = 16 + 8 * c + j;  // 16..47
-                                if (col < 32) r0[col] = v[j];
-                                else r1[col - 32] = v[j];
-                            }
-                        }
-                        const uint32_t base = tmem + ((q * 32u) << 16) + kSFCol0 + (uint32_t)stage * kSFSlotCols;
-                        tmem_st32(base, r0);
-                        tmem_st16(base + 32, r1);
-                        tmem_st_wait();
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(ready_lead + 8u * (uint32_t)stage);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) {
-                    if (lane == 0) {
-                        report(p.dev_status, NVFP4_ERR_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-            }
-        }
-    } else {
-        regs_inc<kRegsEpi>();
-        // ---------------------------------------------------- epilogue (both CTAs)
-        const int ew = warp - kEpiWarp0;  // 0..7
-        const int q = warp & 3;           // TMEM lane quarter this warp may access
-        const int half = ew >> 2;         // which half of the tile's columns
-        const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-        const int row_in_tile = q * 32 + lane;
-        const float gsa = FP4 ? *p.gs_a : 1.0f;
-        const bool swiglu = p.epilogue == NVFP4_EPI_SWIGLU;
-        const uint32_t empty_lead = cluster_addr(acc_empty, 0);
-        float amax_local = 0.0f;
-        int local = 0;
-        for (int item = item0; item < num_items; item += item_step, ++local) {
-            // every lane waits; the warp goes on only if all lanes saw the phase
-            // complete, so the .sync.aligned TMEM loads below stay converged
-            const bool got = mbar_wait_bounded(acc_full, (uint32_t)local & 1u, kWaitLimitNs, abort_flag);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (lane == 0) {
-                    report(p.dev_status, NVFP4_ERR_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                break;
-            }
-            tc_fence_after();
-            const uint32_t acc = tmem + lane_base + kAcc;
-            // read this thread's 128 accumulator columns (two 64-column loads),
-            // release the accumulator, then scale and store while the next
-            // tile's MMAs run
-            uint32_t v[128];
-            if (swiglu) {
-                // output columns 64*half + [0, 64): gate = D[c], up = D[128 + c]
-                tmem_ld64(acc + 64 * half, v);
-                tmem_ld64(acc + 128 + 64 * half, v + 64);
-            } else {
-                tmem_ld64(acc + 128 * half, v);
-                tmem_ld64(acc + 128 * half + 64, v + 64);
-            }
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(empty_lead);
-            const PairTile t = decode_item(s_off, s_pairs, E, num_nt, item, rank);
-            if (!t.live) continue;  // the phantom half of an odd tile count: nothing to store
-            const int64_t row = (int64_t)t.m0 + row_in_tile;
-            const float gmul = FP4 ? __fmul_rn(gsa, s_gsw[t.e]) : 1.0f;
-            if (swiglu) {
-                uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)t.nt * 128 + 64 * half;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) swiglu16(yrow + 16 * j, p.vec32, gmul, v + 16 * j, v + 64 + 16 * j, amax_local);
-            } else {
-                const int64_t col = (int64_t)t.nt * kBN + 128 * half;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) store16(p, row, col + 16 * j, gmul, v + 16 * j, amax_local);
-            }
-        }
-        if (p.amax_out) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, o));
-            if (lane == 0) atomicMax(reinterpret_cast<unsigned int *>(p.amax_out), __float_as_uint(amax_local));
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    // the leader's last MMAs (which write the peer's tensor memory) and every
-    // signal between the CTAs are done before either CTA frees or exits
-    cluster_sync();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc_pair(tmem, kTmemCols);
-    }
-}
-
-template <bool FP4>
-static int set_smem_attr() {
-    static bool done[2] = {false, false};
-    if (!done[FP4]) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<FP4>::kSmemBytes);
-        if (e != cudaSuccess) {
-            set_last_error("cudaFuncSetAttribute(grouped_gemm_kernel)", e);
-            return NVFP4_ERR_CUDA;
-        }
-        done[FP4] = true;
-    }
-    return NVFP4_OK;
-}
-
-// Persistent launch in clusters of two CTAs (one 2-SM MMA pipeline each): as
-// many pairs as the work needs and as fit on the GPU at once.
-template <bool FP4>
-static int launch_gemm(int64_t rows_cap, int32_t E, int64_t N, const CUtensorMap &tA, const CUtensorMap &tB,
-                       const CUtensorMap &tR, const CUtensorMap &tW, const GemmParams &p, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<FP4>::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    static int max_pairs[2] = {0, 0};
-    if (max_pairs[FP4] == 0) {
-        int n = 0;
-        cfg.gridDim = dim3(2 * (unsigned)(sm_count() / 2), 1, 1);
-        const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<FP4>, &cfg);
-        if (e != cudaSuccess || n < 1) {
-            set_last_error("cudaOccupancyMaxActiveClusters(grouped_gemm_kernel)", e);
-            return NVFP4_ERR_CUDA;
-        }
-        max_pairs[FP4] = n;
-    }
-    // at most ceil(tiles_e / 2) tile pairs per expert
-    const int64_t items = ((rows_cap / kBM + E) / 2) * (N / kBN);
-    int64_t pairs = max_pairs[FP4];
-    if (items < pairs) pairs = items;
-    if (pairs < 1) pairs = 1;
-    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<FP4>, tA, tB, tR, tW, p);
-    if (e != cudaSuccess) {
-        set_last_error("cudaLaunchKernelEx(grouped_gemm_kernel)", e);
-        return NVFP4_ERR_CUDA;
-    }
-    return launch_status(FP4 ? "grouped_gemm_kernel<fp4>" : "grouped_gemm_kernel<bf16>");
-}
-
-}  // namespace nvfp4
+#include "gemm_common.cuh"
 
 using namespace nvfp4;
+
+namespace {
+std::atomic<int> g_pipeline{NVFP4_PIPELINE_AUTO};
+
+bool use_pair(bool fp4) {
+    const int which = g_pipeline.load(std::memory_order_relaxed);
+    if (which == NVFP4_PIPELINE_SINGLE) return false;
+    if (which == NVFP4_PIPELINE_PAIR) return true;
+    return !fp4;
+}
+}  // namespace
+
+extern "C" int nvfp4_gemm_pipeline(int32_t which, int32_t *previous) {
+    if (which != NVFP4_PIPELINE_AUTO && which != NVFP4_PIPELINE_SINGLE && which != NVFP4_PIPELINE_PAIR)
+        return NVFP4_ERR_INVALID_ARG;
+    const int prev = g_pipeline.exchange(which);
+    if (previous) *previous = prev;
+    return NVFP4_OK;
+}
 
 extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t *a_scales, const void *a_resid,
                                            const float *gs_a, const uint8_t *w_codes, const uint8_t *w_scales,
@@ -687,21 +59,21 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
         }
     }
     if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
-    int s = set_smem_attr<true>();
-    if (s != NVFP4_OK) return s;
+    const bool pair = use_pair(true);
+    const uint32_t brows = pair ? 128 : 256;  // B rows per copy: this CTA's half, or the whole tile
 
     CUtensorMap tA, tB, tR, tW;
-    s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a_codes, K / 2, rows_cap, K / 2, 128, 128,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
-    if (s == NVFP4_OK)
-        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)w_codes, K / 2, (uint64_t)E * N, K / 2, 128, 128,
+    int s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a_codes, K / 2, rows_cap, K / 2, 128, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == NVFP4_OK)
+        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)w_codes, K / 2, (uint64_t)E * N, K / 2, 128,
+                           brows, CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == NVFP4_OK && k > 0) {
         s = encode_tmap_2d(&tR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a_resid, k, rows_cap, 2 * k, 64, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B);
         if (s == NVFP4_OK)
-            s = encode_tmap_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_sel, k, (uint64_t)E * N, 2 * k, 64, 128,
-                               CU_TENSOR_MAP_SWIZZLE_128B);
+            s = encode_tmap_2d(&tW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_sel, k, (uint64_t)E * N, 2 * k, 64,
+                               brows, CU_TENSOR_MAP_SWIZZLE_128B);
     } else {
         tR = tA;
         tW = tB;
@@ -727,7 +99,8 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
               (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
     p.amax_out = amax_out;
     p.dev_status = dev_status;
-    return launch_gemm<true>(rows_cap, E, N, tA, tB, tR, tW, p, (cudaStream_t)stream);
+    return pair ? launch_pair_gemm<true>(tA, tB, tR, tW, p, rows_cap, N, (cudaStream_t)stream)
+                : launch_single_gemm<true>(tA, tB, tR, tW, p, rows_cap, N, (cudaStream_t)stream);
 }
 
 extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const int32_t *offsets, int32_t E,
@@ -743,10 +116,8 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     if (!aligned16(x) || !aligned16(w_hat) || !aligned16(y) || ldy % 8) return NVFP4_ERR_ALIGNMENT;
     if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
-    int s = set_smem_attr<false>();
-    if (s != NVFP4_OK) return s;
     CUtensorMap tA, tB;
-    s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)x, K, rows_cap, 2 * K, 64, 128,
+    int s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)x, K, rows_cap, 2 * K, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == NVFP4_OK)
         s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_hat, K, (uint64_t)E * N, 2 * K, 64, 128,
@@ -765,5 +136,6 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     p.vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) &&
               (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
     p.dev_status = dev_status;
-    return launch_gemm<false>(rows_cap, E, N, tA, tB, tA, tB, p, (cudaStream_t)stream);
+    return use_pair(false) ? launch_pair_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream)
+                           : launch_single_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream);
 }

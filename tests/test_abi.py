@@ -106,6 +106,14 @@ def test_host_checks_without_gpu(lib):
     assert c(P, 3, 64, P, P, 4, 2, 64, P, None) == INVALID  # bad dtype
 
 
+def test_gemm_pipeline_selector(lib):
+    prev = ctypes.c_int32(-1)
+    assert lib.nvfp4_gemm_pipeline(7, None) == INVALID
+    assert lib.nvfp4_gemm_pipeline(nv.NVFP4_PIPELINE_PAIR, ctypes.byref(prev)) == OK
+    assert prev.value == nv.NVFP4_PIPELINE_AUTO
+    assert nv.nvfp4_gemm_pipeline(nv.NVFP4_PIPELINE_AUTO) == nv.NVFP4_PIPELINE_PAIR
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     import importlib
     monkeypatch.setattr(nv, "_lib", None)

@@ -10,6 +10,8 @@
 * Grouping: ragged expert segments (1, 127, 128, 129 rows, an empty expert).
 * SwiGLU epilogue and the fused amax of its output.
 * BF16 GEMM of the asymmetric-QAT forward (QUADS §3.2 Eq. 12).
+Every test runs on both tcgen05 pipelines (one CTA per 128x256 tile; a CTA
+pair per 256x256 tile), which must give the same results.
 """
 import numpy as np
 import pytest
@@ -31,6 +33,14 @@ def _lib():
     import nvfp4_precision_moe_gb300 as m
     m.load(build=True)
     nv = m
+
+
+@pytest.fixture(autouse=True, params=["single", "pair"])
+def pipeline(request, _lib):
+    which = {"single": nv.NVFP4_PIPELINE_SINGLE, "pair": nv.NVFP4_PIPELINE_PAIR}[request.param]
+    prev = nv.nvfp4_gemm_pipeline(which)
+    yield request.param
+    nv.nvfp4_gemm_pipeline(prev)
 
 
 def _lut2():
