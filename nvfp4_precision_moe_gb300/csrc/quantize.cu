@@ -157,34 +157,27 @@ constexpr int kQWarps = kQThreads / 32;
 constexpr int kMaxStagedK = 1024;  // residual row staged in shared memory up to this k
 
 // One warp per output row (grid-stride), looping over the row in segments of
-// 32 blocks (512 elements, one block per lane).  The RAC residual of the row
-// is gathered in shared memory and written once per destination row as
+// 32 blocks (512 elements, one block per lane).  Each row's destination rows
+// are resolved once: their code-row offsets and the row part of their
+// swizzled scale offsets sit in shared memory, so a block's stores to every
+// destination cost an add each.  The RAC residual is computed after the row's
+// blocks, one selected channel per lane, from the row's block scales kept in
+// shared memory; it is staged there and written once per destination row as
 // 16-byte chunks.
 template <int MODE>
-__global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
-    __shared__ uint32_t s_mask[kMaxBlocksPerRow];
-    __shared__ int32_t s_base[kMaxBlocksPerRow];
+__global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
     __shared__ __align__(16) uint16_t s_res[kQWarps][kMaxStagedK];
+    __shared__ uint8_t s_sb[kQWarps][kMaxBlocksPerRow];
+    __shared__ int64_t s_cbase[kQWarps][32];  // destination f: byte offset of its code row (-1: skipped)
+    __shared__ int64_t s_sbase[kQWarps][32];  // destination f: row part of its swizzled scale offsets
     __shared__ QTables s_tab;
     const int tensor = blockIdx.y;
     fill_tables(s_tab);
+    __syncthreads();  // tables are ready
     const int nb = (int)(a.K >> 4);
     const int64_t kgroups = (nb + 3) >> 2;
     const bool has_sel = (MODE != kModeFake) && a.k > 0;
     const bool staged = a.k <= kMaxStagedK;
-
-    if (has_sel) {  // which elements of each block belong to S, and S's index of the first
-        for (int b = threadIdx.x; b < nb; b += blockDim.x) s_mask[b] = 0u;
-    }
-    __syncthreads();  // tables (and the cleared masks) are ready
-    if (has_sel) {
-        for (int s = threadIdx.x; s < a.k; s += blockDim.x) {
-            int j = a.S[s];
-            atomicOr(&s_mask[j >> 4], 1u << (j & 15));
-            if (s == 0 || (a.S[s - 1] >> 4) != (j >> 4)) s_base[j >> 4] = s;
-        }
-        __syncthreads();
-    }
 
     const float amax_t = a.amax[tensor];
     const float gs = tensor_scale(amax_t);
@@ -200,7 +193,10 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
     const int64_t nwarps_total = (int64_t)gridDim.x * kQWarps;
     const uint16_t *xt = a.x + (int64_t)tensor * a.x_tstride;
     uint16_t *stage = s_res[wid];
+    uint8_t *row_sb = s_sb[wid];
     const int fanout = (MODE == kModeAct) ? a.fanout : 1;
+    uint8_t *codes = a.codes + (int64_t)tensor * a.codes_tstride;
+    uint8_t *scales = a.scales + (int64_t)tensor * a.scales_tstride;
 
     // source row of output row m (weights may be stored in gate/up tile order)
     auto source_row = [&](int64_t m) -> int64_t {
@@ -223,13 +219,17 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
     }
     for (int64_t m = (int64_t)blockIdx.x * kQWarps + wid; m < a.M; m += nwarps_total) {
         const int64_t src_row = source_row(m);
-        // destination rows of this source row: lane f holds the f-th
-        int64_t my_dst = -1;
-        if (MODE == kModeAct) {
-            if (lane < fanout) my_dst = a.dst_row ? (int64_t)a.dst_row[m * fanout + lane] : m;
-            if (my_dst >= a.rows_out) my_dst = -1;  // a map entry outside the output is skipped
-        } else {
-            my_dst = m;
+        if (MODE != kModeFake) {
+            // destination rows of this source row: lane f resolves the f-th
+            __syncwarp();  // the previous row's readers of s_cbase / s_sbase are done
+            if (lane < fanout) {
+                int64_t dm = m;
+                if (MODE == kModeAct && a.dst_row) dm = (int64_t)a.dst_row[m * fanout + lane];
+                const bool ok = dm >= 0 && dm < ((MODE == kModeAct) ? a.rows_out : a.M);  // others are skipped
+                s_cbase[wid][lane] = ok ? dm * (a.K >> 1) : -1;
+                s_sbase[wid][lane] = ok ? ((dm >> 7) * kgroups * 512 + (dm & 31) * 16 + ((dm & 127) >> 5) * 4) : 0;
+            }
+            __syncwarp();
         }
         const uint16_t *xrow = xt + src_row * a.ldx;
         const uint16_t *xnext = (m + nwarps_total < a.M) ? xt + source_row(m + nwarps_total) * a.ldx : nullptr;
@@ -255,8 +255,6 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
                 unpack_block(ca, cb, v);
                 quant_block(v, gs, p6, inv_gs, s_tab, q);
             } else {
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] = 0.0f;
                 q.sb = 0u;
                 q.sbf = 0.0f;
                 q.w0 = q.w1 = 0u;
@@ -279,6 +277,7 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
                 continue;
             }
 
+            if (has_sel && valid) row_sb[b] = (uint8_t)q.sb;
             // four consecutive blocks' scales -> one 32-bit word (lane%4 == 0 stores)
             uint32_t sw = q.sb;
             const uint32_t s1 = __shfl_down_sync(0xffffffffu, sw, 1);
@@ -286,63 +285,62 @@ __global__ void __launch_bounds__(kQThreads) quantize_kernel(QuantArgs a) {
             const uint32_t s3 = __shfl_down_sync(0xffffffffu, sw, 3);
             sw = sw | (s1 << 8) | (s2 << 16) | (s3 << 24);
             const bool group_lead = ((lane & 3) == 0) && (b < ((nb + 3) & ~3));
-
-            // residual (activation) or unscaled dequantized weight on S
-            if (has_sel && valid) {
-                const uint32_t mask = s_mask[b];
-                if (mask) {
-                    const int base = s_base[b];
-                    for (uint32_t mm = mask; mm; mm &= mm - 1u) {
-                        const int t = __ffs(mm) - 1;
-                        const int si = base + __popc(mask & ((1u << t) - 1u));
-                        {
-                            const float cs = __fmul_rn(e2m1_val(q.code(t)), q.sbf);  // exact
-                            uint16_t val;
-                            if (MODE == kModeWeight) {
-                                val = __bfloat16_as_ushort(__float2bfloat16_rn(cs));
-                            } else {
-                                // r = bf16(x - (code*sb)*gs), stored in units of gs
-                                const float xq = __fmul_rn(cs, gs);
-                                const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(sel16(v, t), xq)));
-                                val = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
-                            }
-                            if (staged) {
-                                stage[si] = val;
-                            } else if (MODE == kModeWeight) {
-                                a.wsel[(int64_t)tensor * a.wsel_tstride + m * a.k + si] = val;
-                            } else {
-                                for (int f = 0; f < fanout; ++f) {  // divergent here: read the map directly
-                                    const int64_t dm = a.dst_row ? (int64_t)a.dst_row[m * fanout + f] : m;
-                                    if (dm >= 0 && dm < a.rows_out) a.resid[dm * a.k + si] = val;
-                                }
-                            }
-                        }
-                    }
-                }
-            }
-
-            uint8_t *codes = a.codes + (int64_t)tensor * a.codes_tstride;
-            uint8_t *scales = a.scales + (int64_t)tensor * a.scales_tstride;
+            const int64_t boff = (int64_t)(b >> 2) * 512 + (b & 3);  // block part of the scale offset
             for (int f = 0; f < fanout; ++f) {
-                const int64_t dm = __shfl_sync(0xffffffffu, my_dst, f);
-                if (dm < 0) continue;
-                if (valid) *reinterpret_cast<uint2 *>(codes + dm * (a.K >> 1) + b * 8) = make_uint2(q.w0, q.w1);
-                if (group_lead) *reinterpret_cast<uint32_t *>(scales + swz_offset(dm, b, kgroups)) = sw;
+                const int64_t cbase = s_cbase[wid][f];
+                if (cbase < 0) continue;
+                if (valid) *reinterpret_cast<uint2 *>(codes + cbase + b * 8) = make_uint2(q.w0, q.w1);
+                if (group_lead) *reinterpret_cast<uint32_t *>(scales + s_sbase[wid][f] + boff) = sw;
             }
         }
 
-        if (has_sel && staged) {  // the row's k residual values -> every destination row
-            __syncwarp();
-            const int chunks = a.k >> 3;  // 16-byte chunks (k % 8 == 0)
-            const uint4 *src = reinterpret_cast<const uint4 *>(stage);
-            for (int f = 0; f < fanout; ++f) {
-                const int64_t dm = __shfl_sync(0xffffffffu, my_dst, f);
-                if (dm < 0) continue;
-                uint16_t *row = (MODE == kModeWeight) ? a.wsel + (int64_t)tensor * a.wsel_tstride + dm * a.k
-                                                      : a.resid + dm * a.k;
-                for (int c = lane; c < chunks; c += 32) reinterpret_cast<uint4 *>(row)[c] = src[c];
+        if (has_sel) {
+            // residual (activation) or unscaled dequantized weight on S, one
+            // selected channel per lane: the element's code is recomputed from
+            // its block scale exactly as its block quantized it
+            __syncwarp();  // row_sb is complete
+            for (int si = lane; si < a.k; si += 32) {
+                const int j = __ldg(a.S + si);
+                const float v = __uint_as_float((uint32_t)__ldg(xrow + j) << 16);
+                const uint32_t sb = row_sb[j >> 4];
+                const float sbf = e4m3_to_f32(sb);
+                uint32_t c;
+                if (__fmul_rn(sbf, gs) != 0.0f) c = e2m1x2_from_f32(__fmul_rn(v, __fmul_rn(s_tab.rcp[sb], inv_gs)), 0.0f) & 15u;
+                else c = (__float_as_uint(v) >> 31) << 3;
+                const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
+                uint16_t val;
+                if (MODE == kModeWeight) {
+                    val = __bfloat16_as_ushort(__float2bfloat16_rn(cs));
+                } else {
+                    // r = bf16(x - (code*sb)*gs), stored in units of gs
+                    const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
+                    val = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
+                }
+                if (staged) {
+                    stage[si] = val;
+                } else {
+                    for (int f = 0; f < fanout; ++f) {
+                        const int64_t cbase = s_cbase[wid][f];
+                        if (cbase < 0) continue;
+                        const int64_t dm = cbase / (a.K >> 1);
+                        if (MODE == kModeWeight) a.wsel[(int64_t)tensor * a.wsel_tstride + dm * a.k + si] = val;
+                        else a.resid[dm * a.k + si] = val;
+                    }
+                }
             }
-            __syncwarp();
+            if (staged) {  // the row's k values -> every destination row
+                __syncwarp();
+                const int chunks = a.k >> 3;  // 16-byte chunks (k % 8 == 0)
+                const uint4 *src = reinterpret_cast<const uint4 *>(stage);
+                for (int f = 0; f < fanout; ++f) {
+                    const int64_t cbase = s_cbase[wid][f];
+                    if (cbase < 0) continue;
+                    const int64_t dm = cbase / (a.K >> 1);
+                    uint16_t *row = (MODE == kModeWeight) ? a.wsel + (int64_t)tensor * a.wsel_tstride + dm * a.k
+                                                          : a.resid + dm * a.k;
+                    for (int c = lane; c < chunks; c += 32) reinterpret_cast<uint4 *>(row)[c] = src[c];
+                }
+            }
         }
     }
 }
