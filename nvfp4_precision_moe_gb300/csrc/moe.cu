@@ -149,6 +149,44 @@ __global__ void combine_kernel(const void *y, int64_t ldy, const int32_t *dst_ro
     }
 }
 
+// BF16 routed rows, topk <= kCombineMaxK: every slot's 16 bytes are loaded
+// before the slots are summed (in slot order, as above), so a thread keeps
+// topk loads in flight instead of one.
+constexpr int kCombineMaxK = 8;
+__global__ void combine_bf16_kernel(const uint16_t *y, int64_t ldy, const int32_t *dst_row, const float *weights,
+                                    int32_t T, int32_t topk, int64_t H, float *out) {
+    const int64_t per_row = H >> 3;
+    const int64_t total = (int64_t)T * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = i / per_row, c = (i - t * per_row) * 8;
+        uint4 q[kCombineMaxK];
+        float w[kCombineMaxK];
+#pragma unroll
+        for (int s = 0; s < kCombineMaxK; ++s) {
+            if (s < topk) {
+                const int64_t row = __ldg(dst_row + t * topk + s);
+                w[s] = __ldg(weights + t * topk + s);
+                q[s] = __ldg(reinterpret_cast<const uint4 *>(y + row * ldy + c));
+            }
+        }
+        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+        for (int s = 0; s < kCombineMaxK; ++s) {
+            if (s < topk) {
+                const uint32_t ww[4] = {q[s].x, q[s].y, q[s].z, q[s].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    acc[2 * j] = __fadd_rn(acc[2 * j], __fmul_rn(w[s], __uint_as_float(ww[j] << 16)));
+                    acc[2 * j + 1] = __fadd_rn(acc[2 * j + 1], __fmul_rn(w[s], __uint_as_float(ww[j] & 0xffff0000u)));
+                }
+            }
+        }
+        float4 *o = reinterpret_cast<float4 *>(out + t * H + c);
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
@@ -184,7 +222,10 @@ extern "C" int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, co
     int64_t blocks = (total + 255) / 256, cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
     cudaStream_t st = (cudaStream_t)stream;
-    if (y_dtype == NVFP4_OUT_BF16)
+    if (y_dtype == NVFP4_OUT_BF16 && topk <= kCombineMaxK)
+        combine_bf16_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint16_t *)y, ldy, dst_row, weights, T, topk, H,
+                                                              out);
+    else if (y_dtype == NVFP4_OUT_BF16)
         combine_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(y, ldy, dst_row, weights, T, topk, H, out);
     else
         combine_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(y, ldy, dst_row, weights, T, topk, H, out);
