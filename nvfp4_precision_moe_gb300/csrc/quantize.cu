@@ -155,6 +155,24 @@ __device__ __forceinline__ void unpack_block(const uint4 &a, const uint4 &b, flo
 constexpr int kQThreads = 256;
 constexpr int kQWarps = kQThreads / 32;
 constexpr int kMaxStagedK = 1024;  // residual row staged in shared memory up to this k
+constexpr int kResidBatch = 4;     // selected channels per lane whose inputs are fetched together
+
+// The RAC value of one selected element x (BF16 bits) of a block with scale
+// code sb: its E2M1 code is recomputed exactly as the block's quantization
+// computed it; activations give the residual bf16(x - (code*sb)*gs) in units
+// of gs, weights the unscaled dequantized value bf16(code*sb).
+template <int MODE>
+__device__ __forceinline__ uint16_t resid_value(uint16_t xb, uint32_t sb, float gs, float inv_gs, const QTables &tb) {
+    const float v = __uint_as_float((uint32_t)xb << 16);
+    const float sbf = e4m3_to_f32(sb);
+    uint32_t c;
+    if (__fmul_rn(sbf, gs) != 0.0f) c = e2m1x2_from_f32(__fmul_rn(v, __fmul_rn(tb.rcp[sb], inv_gs)), 0.0f) & 15u;
+    else c = (__float_as_uint(v) >> 31) << 3;
+    const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
+    if (MODE == kModeWeight) return __bfloat16_as_ushort(__float2bfloat16_rn(cs));
+    const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
+}
 
 // One warp per output row (grid-stride), looping over the row in segments of
 // 32 blocks (512 elements, one block per lane).  Each row's destination rows
@@ -170,14 +188,17 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
     __shared__ uint8_t s_sb[kQWarps][kMaxBlocksPerRow];
     __shared__ int64_t s_cbase[kQWarps][32];  // destination f: byte offset of its code row (-1: skipped)
     __shared__ int64_t s_sbase[kQWarps][32];  // destination f: row part of its swizzled scale offsets
+    __shared__ int32_t s_S[kMaxStagedK];
     __shared__ QTables s_tab;
     const int tensor = blockIdx.y;
     fill_tables(s_tab);
-    __syncthreads();  // tables are ready
     const int nb = (int)(a.K >> 4);
     const int64_t kgroups = (nb + 3) >> 2;
     const bool has_sel = (MODE != kModeFake) && a.k > 0;
     const bool staged = a.k <= kMaxStagedK;
+    if (has_sel && staged)
+        for (int i = threadIdx.x; i < a.k; i += blockDim.x) s_S[i] = a.S[i];
+    __syncthreads();  // tables (and S) are ready
 
     const float amax_t = a.amax[tensor];
     const float gs = tensor_scale(amax_t);
@@ -299,26 +320,28 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
             // selected channel per lane: the element's code is recomputed from
             // its block scale exactly as its block quantized it
             __syncwarp();  // row_sb is complete
-            for (int si = lane; si < a.k; si += 32) {
-                const int j = __ldg(a.S + si);
-                const float v = __uint_as_float((uint32_t)__ldg(xrow + j) << 16);
-                const uint32_t sb = row_sb[j >> 4];
-                const float sbf = e4m3_to_f32(sb);
-                uint32_t c;
-                if (__fmul_rn(sbf, gs) != 0.0f) c = e2m1x2_from_f32(__fmul_rn(v, __fmul_rn(s_tab.rcp[sb], inv_gs)), 0.0f) & 15u;
-                else c = (__float_as_uint(v) >> 31) << 3;
-                const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
-                uint16_t val;
-                if (MODE == kModeWeight) {
-                    val = __bfloat16_as_ushort(__float2bfloat16_rn(cs));
-                } else {
-                    // r = bf16(x - (code*sb)*gs), stored in units of gs
-                    const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
-                    val = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
+            if (staged) {
+                // four selected channels per lane at a time: their inputs are
+                // fetched together, then each value is computed
+                for (int si0 = lane; si0 < a.k; si0 += 32 * kResidBatch) {
+                    int jj[kResidBatch];
+                    uint16_t xb[kResidBatch];
+#pragma unroll
+                    for (int u = 0; u < kResidBatch; ++u) {
+                        const int si = si0 + 32 * u;
+                        jj[u] = si < a.k ? s_S[si] : 0;
+                        xb[u] = si < a.k ? __ldg(xrow + jj[u]) : (uint16_t)0;
+                    }
+#pragma unroll
+                    for (int u = 0; u < kResidBatch; ++u) {
+                        const int si = si0 + 32 * u;
+                        if (si < a.k) stage[si] = resid_value<MODE>(xb[u], row_sb[jj[u] >> 4], gs, inv_gs, s_tab);
+                    }
                 }
-                if (staged) {
-                    stage[si] = val;
-                } else {
+            } else {  // k beyond the stage: values go straight to every destination row
+                for (int si = lane; si < a.k; si += 32) {
+                    const int j = __ldg(a.S + si);
+                    const uint16_t val = resid_value<MODE>(__ldg(xrow + j), row_sb[j >> 4], gs, inv_gs, s_tab);
                     for (int f = 0; f < fanout; ++f) {
                         const int64_t cbase = s_cbase[wid][f];
                         if (cbase < 0) continue;
