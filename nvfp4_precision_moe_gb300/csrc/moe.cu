@@ -10,106 +10,139 @@
 
 namespace nvfp4 {
 
-// one warp per token
-__global__ void topk_kernel(const float *logits, int32_t T, int32_t E, int32_t topk, int32_t *ids,
-                            float *weights) {
-    const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+// one warp per token; each block counts the experts its tokens chose
+// in shared memory and adds its counts into `counts` (zeroed on the stream
+// before the launch)
+__global__ void __launch_bounds__(256) topk_kernel(const float *logits, int32_t T, int32_t E, int32_t topk,
+                                                   int32_t *ids, float *weights, int32_t *counts) {
+    __shared__ int32_t s_hist[1024];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_hist[e] = 0;
+    __syncthreads();
     const int lane = threadIdx.x & 31;
-    if (t >= T) return;
-    const float *l = logits + t * E;
-    float mx = -INFINITY;
-    for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+        const float *l = logits + t * E;
+        float mx = -INFINITY;
+        for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    float sum = 0.0f;
-    for (int e = lane; e < E; e += 32) sum += expf(l[e] - mx);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float sum = 0.0f;
+        for (int e = lane; e < E; e += 32) sum += expf(l[e] - mx);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    // bitmask of experts already taken, E <= 1024 -> 32 words, word w owned by lane w
-    uint32_t taken = 0u;
-    for (int s = 0; s < topk; ++s) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
-        for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count for the shuffle
-            const int e = e0 + lane;
-            const uint32_t word = __shfl_sync(0xffffffffu, taken, e0 >> 5);
-            if (e < E && !((word >> lane) & 1u)) {
-                float v = l[e];
-                if (v > bv || (v == bv && e < be)) {
-                    bv = v;
-                    be = e;
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        // bitmask of experts already taken, E <= 1024 -> 32 words, word w owned by lane w
+        uint32_t taken = 0u;
+        for (int s = 0; s < topk; ++s) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+            for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count for the shuffle
+                const int e = e0 + lane;
+                const uint32_t word = __shfl_sync(0xffffffffu, taken, e0 >> 5);
+                if (e < E && !((word >> lane) & 1u)) {
+                    float v = l[e];
+                    if (v > bv || (v == bv && e < be)) {
+                        bv = v;
+                        be = e;
+                    }
                 }
             }
-        }
-        // lanes with no candidate in this pass still take part in the shuffles
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
+            // lanes with no candidate in this pass still take part in the shuffles
+            for (int o = 16; o > 0; o >>= 1) {
+                float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ov > bv || (ov == bv && oe < be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if (lane == (be >> 5)) taken |= 1u << (be & 31);
+            if (lane == 0) {
+                ids[t * topk + s] = be;
+                weights[t * topk + s] = expf(bv - mx) / sum;
+                atomicAdd(&s_hist[be], 1);
             }
         }
-        if (lane == (be >> 5)) taken |= 1u << (be & 31);
-        if (lane == 0) {
-            ids[t * topk + s] = be;
-            weights[t * topk + s] = expf(bv - mx) / sum;
-        }
     }
-}
-
-// block per expert: number of routed tokens
-__global__ void count_kernel(const int32_t *ids, int64_t n, int32_t *counts) {
-    const int e = blockIdx.x;
-    int c = 0;
-    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) c += (ids[i] == e);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-    __shared__ int red[32];
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = c;
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int s = 0;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-        counts[e] = s;
-    }
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
 }
 
-// block per expert: padded segment start, then ranks of its tokens in order
+// block per expert: the padded segment start (from all experts' counts),
+// then the ranks of its tokens in token order.  Thread i owns a contiguous
+// run of tokens: it counts its matches, a block-wide scan gives its first
+// rank, and a second pass over the same run writes the rows.
 __global__ void __launch_bounds__(1024) dst_row_kernel(const int32_t *ids, int32_t T, int32_t E, int32_t topk,
                                                        const int32_t *counts, int32_t *offsets, int32_t *dst_row) {
     const int e = blockIdx.x;
+    __shared__ int32_t s_part[32];
     __shared__ int32_t s_base;
-    __shared__ int32_t warp_sums[32];
-    if (threadIdx.x == 0) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if (wid == 0) {  // segment start: sum of the padded counts of experts < e
         int64_t off = 0;
-        for (int i = 0; i < e; ++i) off += (counts[i] + 127) / 128 * 128;
-        s_base = (int32_t)off;
-        offsets[e] = (int32_t)off;
-        if (e == E - 1) offsets[E] = (int32_t)(off + (counts[e] + 127) / 128 * 128);
+        for (int i = lane; i < e; i += 32) off += (counts[i] + 127) / 128 * 128;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) off += __shfl_xor_sync(0xffffffffu, off, o);
+        if (lane == 0) {
+            s_base = (int32_t)off;
+            offsets[e] = (int32_t)off;
+            if (e == E - 1) offsets[E] = (int32_t)(off + (counts[e] + 127) / 128 * 128);
+        }
+    }
+    const int64_t per = (T + (int64_t)blockDim.x - 1) / blockDim.x;
+    const int64_t t0 = (int64_t)threadIdx.x * per;
+    const int64_t t1 = min((int64_t)T, t0 + per);
+    // the run's ids are contiguous: read them 16 bytes at a time when rows are whole int4s
+    const bool vec = (topk & 3) == 0 && (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
+    int c = 0;
+    if (vec) {
+        const int4 *p = reinterpret_cast<const int4 *>(ids + t0 * topk);
+        const int64_t n4 = (t1 - t0) * topk / 4;
+        for (int64_t i = 0; i < n4; ++i) {
+            const int4 q = __ldg(p + i);
+            c += (q.x == e) + (q.y == e) + (q.z == e) + (q.w == e);
+        }
+    } else {
+        for (int64_t t = t0; t < t1; ++t)
+            for (int s = 0; s < topk; ++s) c += ids[t * topk + s] == e;
+    }
+    // block-wide exclusive scan of c (thread order = token order)
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_part[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int v = lane < nw ? s_part[lane] : 0;
+        int w = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        if (lane < nw) s_part[lane] = w - v;  // exclusive prefix of the warps
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    for (int64_t t0 = 0; t0 < T; t0 += blockDim.x) {
-        const int64_t t = t0 + threadIdx.x;
-        int slot = -1;
-        if (t < T)
-            for (int s = 0; s < topk; ++s)
-                if (ids[t * topk + s] == e) slot = s;
-        const int flag = slot >= 0;
-        const unsigned bal = __ballot_sync(0xffffffffu, flag);
-        if (lane == 0) warp_sums[wid] = __popc(bal);
-        __syncthreads();
-        int pre = __popc(bal & ((1u << lane) - 1u));
-        for (int w = 0; w < wid; ++w) pre += warp_sums[w];
-        if (flag) dst_row[t * topk + slot] = s_base + pre;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int tot = 0;
-            for (int w = 0; w < nw; ++w) tot += warp_sums[w];
-            s_base += tot;
+    int r = s_base + s_part[wid] + incl - c;
+    if (c == 0) return;  // nothing of this expert in the run
+    if (vec) {
+        const int4 *p = reinterpret_cast<const int4 *>(ids + t0 * topk);
+        const int64_t n4 = (t1 - t0) * topk / 4;
+        for (int64_t i = 0; i < n4; ++i) {
+            const int4 q = __ldg(p + i);
+            int32_t *d = dst_row + t0 * topk + 4 * i;
+            if (q.x == e) d[0] = r++;
+            if (q.y == e) d[1] = r++;
+            if (q.z == e) d[2] = r++;
+            if (q.w == e) d[3] = r++;
         }
-        __syncthreads();
+    } else {
+        for (int64_t t = t0; t < t1; ++t)
+            for (int s = 0; s < topk; ++s)
+                if (ids[t * topk + s] == e) dst_row[t * topk + s] = r++;
     }
 }
 
@@ -198,14 +231,17 @@ extern "C" int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32
     if (topk > 32 || topk > E || E > 1024) return NVFP4_ERR_UNSUPPORTED;
     NVFP4_CHECK_INIT();
     cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t ce = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)E, st);
+    if (ce != cudaSuccess) {
+        set_last_error("cudaMemsetAsync(counts)", ce);
+        return NVFP4_ERR_CUDA;
+    }
     if (T > 0) {
-        topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, st>>>(logits, T, E, topk, ids, weights);
+        // a warp per token: the selection passes are latency-bound, so every token gets its own warp
+        topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, st>>>(logits, T, E, topk, ids, weights, counts);
         int s = launch_status("topk_kernel");
         if (s != NVFP4_OK) return s;
     }
-    count_kernel<<<E, 512, 0, st>>>(ids, (int64_t)T * topk, counts);
-    int s = launch_status("count_kernel");
-    if (s != NVFP4_OK) return s;
     dst_row_kernel<<<E, 1024, 0, st>>>(ids, T, E, topk, counts, offsets, dst_row);
     return launch_status("dst_row_kernel");
 }
