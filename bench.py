@@ -30,11 +30,11 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core ratio, nominal
 
 
 # DRAM bytes (read + write) of one gate_up GEMM launch at this workload's launch shape, from
-# one ncu capture (profiles/grouped_gemm_kernel_moe_prefill.md), valid only for the kernel
+# one ncu capture (profiles/single_gemm_kernel_moe_prefill.md), valid only for the kernel
 # sources it was taken on (common.cuh, gemm_common.cuh, gemm_single.cu): reported as null
 # once they change.
-GATE_UP_TRAFFIC = {"bytes": 1362224000 + 414388480,
-                   "sources_sha256": "e29bfbf6e9332e980a7e65ad97376795903e2749dfeeb9af30a1e2be4919e040"}
+GATE_UP_TRAFFIC = {"bytes": 1362264000 + 414798336,
+                   "sources_sha256": "158884eaf1d16ca296e7c3092996026b424756b5321f97cfc15b98cb397cecac"}
 
 
 def gate_up_traffic():
