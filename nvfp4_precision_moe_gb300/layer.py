@@ -102,8 +102,10 @@ class RolloutMoE:
     # number of library kernels one forward launches
     LAUNCHES = 9  # routing 2, amax, quantize x, clear padding, gate_up GEMM, quantize h, down GEMM, combine
 
-    def forward(self, x, logits, stream=None, mark=None):
-        """x [T, H] BF16, logits [T, E] FP32 -> out [T, H] FP32 (a view of a reused buffer).
+    def forward(self, x, logits, stream=None, mark=None, out=None):
+        """x [T, H] BF16, logits [T, E] FP32 -> out [T, H] FP32: `out` if given
+        (e.g. to alternate output buffers while an earlier result is being
+        copied out), else a view of a reused buffer.
 
         `mark(i)`, if given, is called before stage i = 0..6 (route, amax,
         quantize x, gate_up GEMM, quantize h, down GEMM, combine) and with
@@ -142,7 +144,9 @@ class RolloutMoE:
                                     epilogue=NVFP4_EPI_NONE, out_dtype=NVFP4_OUT_BF16,
                                     dev_status=self.dev_status, stream=stream)
         mark(6)
-        out = self.out[:T]
+        if out is None:
+            out = self.out[:T]
+        assert out.shape == (T, self.H) and out.dtype == torch.float32
         nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
         mark(7)
         return out
