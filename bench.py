@@ -296,11 +296,59 @@ def run_ours(args):
         "clocks": clk,
     }
     if rank == 0:
+        out["qat"] = qat_measure(dev, max(3, min(args.steps, 10)))
         out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(out), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def qat_measure(dev, steps):
+    """The trainer side at the QAT workload (128 experts, W13 3072x4096 and down
+    4096x1536 fake-quantized every step, 4096 tokens top-8 through the BF16
+    grouped GEMMs): per-stage CUDA events over `steps` forwards.  Weights are
+    random BF16 drawn on the device (values do not change the work)."""
+    import torch
+
+    import nvfp4_precision_moe_gb300 as nv
+    import synth
+
+    c = synth.CONFIGS[4]
+    E, H, I, T, topk = c["E"], c["H"], c["I"], c["T"], c["topk"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(44)
+    w13 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev)
+    wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
+    for e in range(E):
+        w13[e].copy_(torch.randn((2 * I, H), device=dev, generator=g) * 0.02)
+        wd[e].copy_(torch.randn((H, I), device=dev, generator=g) * 0.02)
+    x = synth.activations(4).to(dev)
+    logits = synth.router_logits(4).to(dev)
+    layer = nv.QatMoE(w13, wd, topk, T)
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        layer.forward(x, logits)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
+    for i in range(steps):
+        layer.forward(x, logits, mark=lambda j, i=i: ev[i][j].record(stream))
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    st = lambda a, b: statistics.median([ev[i][a].elapsed_time(ev[i][b]) for i in range(steps)])
+    fq_ms, g13_ms, gd_ms, fwd_ms = st(0, 1), st(3, 4), st(4, 5), st(0, 6)
+    n_w = E * (2 * I * H + H * I)
+    fq_bytes = 4 * n_w  # read and write every BF16 weight once
+    R = T * topk
+    fl13, fld = 2 * R * 2 * I * H, 2 * R * H * I
+    pk = peaks()
+    return {"workload": "qat E=128 W13 3072x4096 down 4096x1536 fake-quantized per step, T=4096 top8",
+            "fake_quant": {"ms": round(fq_ms, 4), "gbs": round(fq_bytes / (fq_ms * 1e-3) / 1e9, 1),
+                           "hbm_frac": round(fq_bytes / (fq_ms * 1e-3) / 1e9 / pk["hbm"], 4), "bytes": fq_bytes},
+            "bf16_gemm": {"gate_up_ms": round(g13_ms, 4), "down_ms": round(gd_ms, 4),
+                          "tflops": round((fl13 + fld) / ((g13_ms + gd_ms) * 1e-3) / 1e12, 1),
+                          "bf16_frac": round((fl13 + fld) / ((g13_ms + gd_ms) * 1e-3) / 1e12 / pk["bf16"], 4)},
+            "forward_ms": round(fwd_ms, 4)}
 
 
 _ORACLE_WEIGHTS = {}

@@ -181,18 +181,31 @@ class QatMoE:
         nvfp4_fake_quant(self.wd, self.wd_hat, self.amax_ws, gs_out=self.gsd,
                          dev_status=self.dev_status, stream=stream)
 
-    def forward(self, x, logits, stream=None):
+    def forward(self, x, logits, stream=None, mark=None):
+        """x [T, H] BF16, logits [T, E] FP32 -> out [T, H] FP32 (a view of a reused buffer).
+
+        `mark(i)`, if given, is called before stage i = 0..5 (fake-quant,
+        route, scatter, gate_up GEMM, down GEMM, combine) and with i = 6 at
+        the end, e.g. to record CUDA events."""
+        mark = mark or (lambda i: None)
         T = x.shape[0]
         r = self.route
         ids, w, dst = r.ids[:T], r.weights[:T], r.dst_row[:T]
+        mark(0)
         self.fake_quant(stream=stream)
+        mark(1)
         nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=stream)
+        mark(2)
         nvfp4_moe_scatter_rows(x, self.topk, dst, r.counts, r.offsets, self.E, self.xr, stream=stream)
+        mark(3)
         nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.h,
                                 out_dtype=NVFP4_OUT_BF16, epilogue=NVFP4_EPI_SWIGLU,
                                 dev_status=self.dev_status, stream=stream)
+        mark(4)
         nvfp4_bf16_grouped_gemm(self.h, self.wd_hat, r.offsets, self.E, self.H, self.I, self.y,
                                 out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
+        mark(5)
         out = self.out[:T]
         nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
+        mark(6)
         return out
