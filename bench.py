@@ -109,13 +109,33 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def setup_distributed(n):
+def setup_distributed(n, backend="nccl"):
     rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
     return rank, world, local
+
+
+def job_time(ms, world, device=None):
+    """The job's timed-region length: the slowest rank's, every rank returning it
+    (replicas run the same step independently; the reduction and the barriers are
+    the only collectives)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
+def job_value(units_per_rank, world, ms_job):
+    """Whole-job throughput: the units all ranks processed over the job's time."""
+    return world * units_per_rank / (ms_job * 1e-3)
 
 
 def build_workload(dev):
@@ -199,12 +219,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-        dist.barrier()
+    ms = job_time(ms, world, dev)
     ms_step = ms / args.steps
     names = ["route", "amax_x", "quantize_x", "gemm_gate_up", "quantize_h", "gemm_down", "combine"]
     stage = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)])
@@ -263,13 +278,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     e0, e1 = e2e_run(args.steps)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_ms = job_time(e0.elapsed_time(e1), world, dev) / args.steps
     assert int(layer.dev_status.item()) == 0
     assert torch.equal(oh[(args.steps - 1) % 2], layer.forward(x, logits).cpu())
 
     pk = peaks()
     fp4_peak = pk["bf16"] * NOMINAL_FP4_OVER_BF16
-    value = world * (f4 + fb) / (ms_step * 1e-3) / 1e12
+    value = job_value(f4 + fb, world, ms_step) / 1e12
     gemm13_tflops = f4_13 / (gemm13_ms * 1e-3) / 1e12
     R = T * c["topk"]
     q_bytes = 2 * T * H + R * (H // 2 + H // 16 + 2 * k)  # read x, write routed codes/scales/residual
