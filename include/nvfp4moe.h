@@ -25,13 +25,14 @@
  * NVFP4 tensor format produced by nvfp4_quantize (QUADS §2.2 "FP4."):
  *  - codes  [rows, K/2] uint8: E2M1 codes, two per byte, element 2i in the
  *           low nibble, element 2i+1 in the high nibble.
- *  - scales swizzled E4M3 block scales, one per 16 consecutive elements along
- *           K, grouped in 512-byte tiles of 128 rows x 4 blocks: tile
- *           (m/128, kb/4) starts at byte ((m/128)*(K/64) + kb/4)*512 (with
- *           K/64 rounded up) and holds row m, block kb at byte
- *           (m%32)*16 + ((m%128)/32)*4 + kb%4.  Size:
- *           ceil(rows/128)*128 * ceil(K/64)*4 bytes; unused bytes are 0.
- *           This is the layout the block-scaled tensor-core MMA reads.
+ *  - scales tiled E4M3 block scales, one per 16 consecutive elements along
+ *           K, grouped in 2048-byte tiles of 128 rows x 16 blocks (one GEMM
+ *           K-slice of 256 elements): tile (m/128, kb/16) starts at byte
+ *           ((m/128)*(K/256) + kb/16)*2048 (with K/256 rounded up) and holds
+ *           row m, block kb at byte (m%128)*16 + kb%16.  Size:
+ *           ceil(rows/128)*128 * ceil(K/256)*16 bytes; unused bytes are 0.
+ *           The GEMM copies a tile per K-slice and interleaves it into tensor
+ *           memory as the block-scaled MMA reads it.
  *  - gs     FP32 per-tensor scale: the smallest power of two not below
  *           fl(amax/2688) (amax = max|x| over the tensor; 2688 = 6*448), so
  *           every block-scale target amax16/(6*gs) is at most 448; gs = 1 for

@@ -36,7 +36,7 @@ constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 // Register split (per thread) after launch at 65536 / 512 = 128: the producer
 // and MMA warpgroup and the scale warpgroup give registers to the epilogue,
 // which holds a thread's 128 accumulator columns at once.
-constexpr uint32_t kRegsCtl = 96, kRegsSF = 64, kRegsEpi = 176;
+constexpr uint32_t kRegsCtl = 88, kRegsSF = 72, kRegsEpi = 176;
 static_assert(128 * kRegsCtl + 128 * kRegsSF + 256 * kRegsEpi <= 65536, "register split above the launch budget");
 
 struct GemmParams {
@@ -125,6 +125,39 @@ __device__ __forceinline__ void swiglu16(uint16_t *dst16, bool vec32, float gmul
         amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] & 0xffff0000u)));
     }
     store32B(dst16, vec32, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+}
+
+// One stage's block scales, from shared memory to this warp's 32-lane quarter
+// of the stage's tensor-memory slot (every quarter holds the same copy, as the
+// block-scaled MMA reads it).  Shared memory holds the A tile [128 rows][16 B]
+// and then the B tile's rows 0-127 and 128-255, each [128][16 B]; MMA-K chunk
+// c of a row is its bytes 4c..4c+3.  Slot columns: A chunk c -> 4c..4c+3
+// (column 4c+j holds row 32j+lane); B chunk c -> 16+8c+j, rows 32j+lane for
+// j < 4 and 128+32(j-4)+lane for j >= 4.  The caller waits for the stores.
+__device__ __forceinline__ void sf_stage_to_tmem(const uint8_t *sfs, uint32_t base, int lane) {
+    {
+        uint32_t r[16];  // A: column 4c + j
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 a = *reinterpret_cast<const uint4 *>(sfs + 16 * (lane + 32 * j));
+            r[j] = a.x;
+            r[4 + j] = a.y;
+            r[8 + j] = a.z;
+            r[12 + j] = a.w;
+        }
+        tmem_st16(base, r);
+    }
+    uint32_t rb[32];  // B: column 16 + 8c + j -> index 8c + j
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(sfs + kSFABytes + (j < 4 ? 0 : kSFBBytes / 2) +
+                                                         16 * (lane + 32 * (j & 3)));
+        rb[j] = w.x;
+        rb[8 + j] = w.y;
+        rb[16 + j] = w.z;
+        rb[24 + j] = w.w;
+    }
+    tmem_st32(base + 16, rb);
 }
 
 // Launchers of the two pipelines (FP4: W4A4 + RAC; !FP4: BF16).  Tensor maps:

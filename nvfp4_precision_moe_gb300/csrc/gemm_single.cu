@@ -265,12 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_dec<kRegsSF>();
         // ---------------------------------------------------- scale warps
         // Slice by slice in the producer's order: wait for the stage's scales
-        // (their own barrier, so this overlaps the A/B copies), then write its
-        // 12 scale chunks (512 bytes each: 32 rows of 16 bytes) into
-        // this warp's lane quarter.  Slot columns: A chunk c -> 4c..4c+3;
-        // B chunk c -> 16+8c..16+8c+7 (its first and second 128 rows).  Lane
-        // i, column base+j gets word j of row i of the chunk; every quarter
-        // holds the same copy.
+        // (their own barrier, so this overlaps the A/B copies), then write them
+        // into this warp's lane quarter of the stage's tensor-memory slot
+        // (sf_stage_to_tmem: the tiled 128-row x 16-byte shared-memory layout
+        // interleaved as the block-scaled MMA reads it).
         if (FP4) {
             const uint32_t q = (uint32_t)(warp & 3);
             int stage = 0;
@@ -285,31 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (it < nkt) {
                         const uint8_t *sfs = smem + stage * C::kStageBytes + kATileBytes + kBTileBytes;
-                        uint32_t r0[32], r1[16];
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // A: columns 4c..4c+3
-                            const uint4 w = *reinterpret_cast<const uint4 *>(sfs + 512 * c + 16 * lane);
-                            r0[4 * c] = w.x;
-                            r0[4 * c + 1] = w.y;
-                            r0[4 * c + 2] = w.z;
-                            r0[4 * c + 3] = w.w;
-                        }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) {  // B: columns 16+8c (rows 0-127), 20+8c (rows 128-255)
-                            const uint4 lo = *reinterpret_cast<const uint4 *>(sfs + kSFABytes + 512 * c + 16 * lane);
-                            const uint4 hi =
-                                *reinterpret_cast<const uint4 *>(sfs + kSFABytes + kSFBBytes / 2 + 512 * c + 16 * lane);
-                            const uint32_t v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const int col = 16 + 8 * c + j;  // 16..47
-                                if (col < 32) r0[col] = v[j];
-                                else r1[col - 32] = v[j];
-                            }
-                        }
                         const uint32_t base = tmem + ((q * 32u) << 16) + kSFCol0 + (uint32_t)stage * kSFSlotCols;
-                        tmem_st32(base, r0);
-                        tmem_st16(base + 32, r1);
+                        sf_stage_to_tmem(sfs, base, lane);
                         tmem_st_wait();
                     }
                     tc_fence_before();

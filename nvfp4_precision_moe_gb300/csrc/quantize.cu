@@ -45,8 +45,11 @@ struct QuantArgs {
 
 // Byte offset of (row m, block kb) in the swizzled scale layout, for a
 // tensor whose rows hold K/16 blocks.
-__device__ __forceinline__ int64_t swz_offset(int64_t m, int64_t kb, int64_t kgroups) {
-    return ((m >> 7) * kgroups + (kb >> 2)) * 512 + (m & 31) * 16 + ((m & 127) >> 5) * 4 + (kb & 3);
+// Tiles of 128 rows x 16 blocks (2048 bytes, one GEMM K-slice of a row tile):
+// tile (m/128, kb/16) at ((m/128)*kslices + kb/16)*2048, row m and block kb
+// inside it at (m%128)*16 + kb%16.
+__device__ __forceinline__ int64_t swz_offset(int64_t m, int64_t kb, int64_t kslices) {
+    return ((m >> 7) * kslices + (kb >> 4)) * 2048 + (m & 127) * 16 + (kb & 15);
 }
 
 // E2M1 code -> value, from a packed table of 2*|value| (0,1,2,3,4,6,8,12).
@@ -193,7 +196,7 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
     const int tensor = blockIdx.y;
     fill_tables(s_tab);
     const int nb = (int)(a.K >> 4);
-    const int64_t kgroups = (nb + 3) >> 2;
+    const int64_t kslices = (nb + 15) >> 4;
     const bool has_sel = (MODE != kModeFake) && a.k > 0;
     const bool staged = a.k <= kMaxStagedK;
     if (has_sel && staged)
@@ -248,7 +251,7 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
                 if (MODE == kModeAct && a.dst_row) dm = (int64_t)a.dst_row[m * fanout + lane];
                 const bool ok = dm >= 0 && dm < ((MODE == kModeAct) ? a.rows_out : a.M);  // others are skipped
                 s_cbase[wid][lane] = ok ? dm * (a.K >> 1) : -1;
-                s_sbase[wid][lane] = ok ? ((dm >> 7) * kgroups * 512 + (dm & 31) * 16 + ((dm & 127) >> 5) * 4) : 0;
+                s_sbase[wid][lane] = ok ? ((dm >> 7) * kslices * 2048 + (dm & 127) * 16) : 0;
             }
             __syncwarp();
         }
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
             const uint32_t s3 = __shfl_down_sync(0xffffffffu, sw, 3);
             sw = sw | (s1 << 8) | (s2 << 16) | (s3 << 24);
             const bool group_lead = ((lane & 3) == 0) && (b < ((nb + 3) & ~3));
-            const int64_t boff = (int64_t)(b >> 2) * 512 + (b & 3);  // block part of the scale offset
+            const int64_t boff = (int64_t)(b >> 4) * 2048 + (b & 15);  // block part of the scale offset
             for (int f = 0; f < fanout; ++f) {
                 const int64_t cbase = s_cbase[wid][f];
                 if (cbase < 0) continue;
@@ -425,11 +428,11 @@ __global__ void clear_padding_kernel(const int32_t *counts, const int32_t *offse
     const int64_t r0 = (int64_t)offsets[e] + counts[e], r1 = offsets[e + 1];
     const int64_t row = r0 + blockIdx.x;
     if (row >= r1 || row >= rows_cap || row < 0) return;
-    const int64_t nb = K >> 4, kgroups = (nb + 3) >> 2;
+    const int64_t nb = K >> 4, kslices = (nb + 15) >> 4;
     uint32_t *c = reinterpret_cast<uint32_t *>(codes + row * (K >> 1));
     for (int64_t i = threadIdx.x; i < (K >> 3); i += blockDim.x) c[i] = 0u;
-    for (int64_t g = threadIdx.x; g < kgroups; g += blockDim.x)
-        *reinterpret_cast<uint32_t *>(scales + swz_offset(row, g * 4, kgroups)) = 0u;
+    for (int64_t g = threadIdx.x; g < kslices * 4; g += blockDim.x)  // 4-byte words of the row's 16-byte runs
+        *reinterpret_cast<uint32_t *>(scales + swz_offset(row, g * 4, kslices)) = 0u;
     if (resid)
         for (int64_t i = threadIdx.x; i < k; i += blockDim.x) resid[row * k + i] = 0;
 }

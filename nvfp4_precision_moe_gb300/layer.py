@@ -22,8 +22,8 @@ from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16, NVFP4_OUT_F32,
 
 
 def scale_bytes(rows, K):
-    """Bytes of the swizzled block-scale layout of a rows x K NVFP4 tensor."""
-    return ((rows + 127) // 128) * 128 * ((K // 16 + 3) // 4) * 4
+    """Bytes of the tiled block-scale layout of a rows x K NVFP4 tensor."""
+    return ((rows + 127) // 128) * 128 * ((K // 16 + 15) // 16) * 16
 
 
 def rows_capacity(T, topk, E):

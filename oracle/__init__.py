@@ -178,12 +178,12 @@ def dequantize_f32(codes, scales, gs):
 
 
 def swizzled_scale_bytes(M, K):
-    """Size of the tensor-core scale layout: ceil(M/128)*128 * ceil(K/64)*4."""
-    return ((M + 127) // 128) * 128 * ((K // 16 + 3) // 4) * 4
+    """Size of the tiled scale layout: ceil(M/128)*128 * ceil(K/256)*16."""
+    return ((M + 127) // 128) * 128 * ((K // 16 + 15) // 16) * 16
 
 
 def swizzle_scales(scales, K):
-    """Canonical [M,K/16] scales -> the 128x4 tile layout (1-D u8)."""
+    """Canonical [M,K/16] scales -> the tiled layout of 128 rows x 16 blocks (1-D u8)."""
     scales = _c(scales, np.uint8)
     M = scales.shape[0]
     out = np.empty(swizzled_scale_bytes(M, K), np.uint8)

@@ -285,19 +285,20 @@ void orc_dequantize_f32(const uint8_t *codes, const uint8_t *scales, int64_t M, 
         }
 }
 
-/* Scale layout consumed by the block-scaled tensor-core MMA: the canonical
- * [M, K/16] scales regrouped into 512-byte tiles of 128 rows x 4 blocks.
- * Tile (m/128, kb/4) sits at ((m/128) * ceil(K/64) + kb/4) * 512; inside it
- * row m and block kb go to (m%32)*16 + ((m%128)/32)*4 + kb%4.  Rows beyond M
- * and blocks beyond K/16 are zero.  (Layout choice of this build; the paper
- * only says the quantizer's layout must match the GEMM's, §3.2.) */
+/* Scale layout shared by the quantizer and the block-scaled GEMM: the
+ * canonical [M, K/16] scales regrouped into 2048-byte tiles of 128 rows x 16
+ * blocks (one GEMM K-slice of 256 elements).  Tile (m/128, kb/16) sits at
+ * ((m/128) * ceil(K/256) + kb/16) * 2048; inside it row m and block kb go to
+ * (m%128)*16 + kb%16.  Rows beyond M and blocks beyond K/16 are zero.
+ * (Layout choice of this build; the paper only says the quantizer's layout
+ * must match the GEMM's, §3.2.) */
 void orc_swizzle_scales(const uint8_t *scales, int64_t M, int64_t K, uint8_t *out)
 {
-    int64_t nb = K / 16, mt = (M + 127) / 128, kt = (nb + 3) / 4;
-    memset(out, 0, (size_t)(mt * 128 * kt * 4));
+    int64_t nb = K / 16, mt = (M + 127) / 128, kt = (nb + 15) / 16;
+    memset(out, 0, (size_t)(mt * 128 * kt * 16));
     for (int64_t m = 0; m < M; m++)
         for (int64_t kb = 0; kb < nb; kb++) {
-            int64_t off = ((m / 128) * kt + kb / 4) * 512 + (m % 32) * 16 + ((m % 128) / 32) * 4 + kb % 4;
+            int64_t off = ((m / 128) * kt + kb / 16) * 2048 + (m % 128) * 16 + kb % 16;
             out[off] = scales[m * nb + kb];
         }
 }

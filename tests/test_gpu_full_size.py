@@ -4,7 +4,7 @@ Zipf routing, intermediate 1536, k = 128 on both projections) through
 RolloutMoE.forward, checked stage by stage on sampled rows.  Each stage's GPU
 output is compared with the oracle applied to the previous stage's GPU output:
 
-* quantize x: gs exact; codes, block scales (read back through the swizzled
+* quantize x: gs exact; codes, block scales (read back through the tiled
   layout of the header) and residual bit-exact for sampled tokens at all 8 of
   their routed rows; padding rows of the routed codes are zero.
 * gate_up W4A4 + RAC GEMM + SwiGLU (QUADS §3.3 Eq. 21): sampled rows of the
@@ -28,14 +28,14 @@ TOL_BF16 = 2.0 ** -8 + 1e-3
 
 
 def _scale_rows(sw, rows, K):
-    """Canonical [len(rows), K/16] block scales of `rows` from the swizzled
-    layout: row m, block kb at ((m/128)*ceil(K/64) + kb/4)*512 +
-    (m%32)*16 + ((m%128)/32)*4 + kb%4."""
-    kg = (K // 16 + 3) // 4
+    """Canonical [len(rows), K/16] block scales of `rows` from the tiled layout
+    of the header: row m, block kb at ((m/128)*ceil(K/256) + kb/16)*2048 +
+    (m%128)*16 + kb%16."""
+    kt = (K // 16 + 15) // 16
     kb = np.arange(K // 16)
     out = np.empty((len(rows), K // 16), np.uint8)
     for i, m in enumerate(rows):
-        idx = ((m // 128) * kg + kb // 4) * 512 + (m % 32) * 16 + ((m % 128) // 32) * 4 + kb % 4
+        idx = ((m // 128) * kt + kb // 16) * 2048 + (m % 128) * 16 + kb % 16
         out[i] = sw[idx]
     return out
 

@@ -191,15 +191,16 @@ def test_fake_quant_equals_dequant_of_quant():
 
 
 def test_swizzle_is_a_bijection_with_zero_padding():
-    M, K = 200, 320  # ragged in both dimensions: 2 row tiles, 5 block groups
+    M, K = 200, 320  # ragged in both dimensions: 2 row tiles, 2 slices of 16 blocks (the second 4/16 full)
     rng = np.random.default_rng(8)
     sc = rng.integers(1, 255, (M, K // 16), dtype=np.uint8)
     out = oracle.swizzle_scales(sc, K)
-    assert out.size == 256 * 20
+    assert out.size == 256 * 32
     assert np.count_nonzero(out) == sc.size
     assert sorted(out[out != 0].tolist()) == sorted(sc.reshape(-1).tolist())
-    # tile 0, rows 0..127, block group 0 is the first 512 bytes: row m, block kb
-    # at (m%32)*16 + (m//32)*4 + kb
-    assert out[0] == sc[0, 0] and out[16 * 5 + 4 * 2 + 3] == sc[69, 3]
-    # tile (row tile 1, block group 1) starts at (1*5 + 1) * 512
-    assert out[6 * 512] == sc[128, 4]
+    # tile (row tile 0, slice 0) is the first 2048 bytes: row m, block kb at m*16 + kb
+    assert out[0] == sc[0, 0] and out[69 * 16 + 3] == sc[69, 3]
+    # tile (row tile 0, slice 1) starts at 2048: block 16 + j of row m at 2048 + m*16 + j
+    assert out[2048 + 5 * 16 + 2] == sc[5, 18] and out[2048 + 5 * 16 + 4] == 0
+    # tile (row tile 1, slice 1) starts at (1*2 + 1) * 2048
+    assert out[3 * 2048 + 3] == sc[128, 19]
