@@ -33,8 +33,8 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core ratio, nominal
 # one ncu capture (profiles/single_gemm_kernel_moe_prefill.md), valid only for the kernel
 # sources it was taken on (common.cuh, gemm_common.cuh, gemm_single.cu): reported as null
 # once they change.
-GATE_UP_TRAFFIC = {"bytes": 1362264000 + 414798336,
-                   "sources_sha256": "158884eaf1d16ca296e7c3092996026b424756b5321f97cfc15b98cb397cecac"}
+GATE_UP_TRAFFIC = {"bytes": 1362329000 + 414975744,
+                   "sources_sha256": "8b11a365931434943c26ea652d17e01eb4d5150f5b93204837c7e917e49d9a38"}
 
 
 def gate_up_traffic():
@@ -171,7 +171,7 @@ def build_workload(dev):
     del cal, xc
     layer = nv.RolloutMoE(w13, wd, S13, Sd, topk, T)  # weight prep (A7), once per weight update
     torch.cuda.synchronize()
-    return c, layer, x, logits
+    return c, layer, x, logits, (w13, wd)
 
 
 def run_ours(args):
@@ -184,7 +184,7 @@ def run_ours(args):
     import synth
 
     nv.load(build=True)
-    c, layer, x, logits = build_workload(dev)
+    c, layer, x, logits, w_bf16 = build_workload(dev)
     T, H, E, I, k = c["T"], c["H"], c["E"], c["I"], c["k"]
     f4, fb = synth.flops_moe(WORKLOAD)
     f4_13 = 2 * T * c["topk"] * 2 * I * H
@@ -312,6 +312,7 @@ def run_ours(args):
     }
     if rank == 0:
         out["qat"] = qat_measure(dev, max(3, min(args.steps, 10)))
+        out["mismatch"] = mismatch_measure(layer, x, logits, *w_bf16)
         out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -366,13 +367,44 @@ def qat_measure(dev, steps):
             "forward_ms": round(fwd_ms, 4)}
 
 
+def mismatch_measure(layer, x, logits, w13, wd):
+    """Layer-wise forward mismatch of QUADS §3.1 Eq. 11 (Fig. 4b) on the
+    benchmark's own batch and weights: ||Y_rollout - Y_trainer|| / ||Y_trainer||
+    for the W4A4 rollout against the BF16 trainer (no QAT), the W4A4 rollout
+    against the W4A16 QAT trainer, and the W4A4 + RAC rollout (`layer`) against
+    the QAT trainer; norms by nvfp4_mismatch_norm in binary64."""
+    import torch
+
+    import nvfp4_precision_moe_gb300 as nv
+
+    T = x.shape[0]
+    outs = {"w4a4_rac": layer.forward(x, logits).clone()}
+    for name, mk in [("w4a4", lambda: nv.RolloutMoE(w13, wd, None, None, layer.topk, T)),
+                     ("w16a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=False)),
+                     ("w4a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=True))]:
+        lay = mk()
+        outs[name] = lay.forward(x, logits).clone()
+        torch.cuda.synchronize()
+        assert int(lay.dev_status.item()) == 0
+        del lay
+    acc = torch.zeros(2, dtype=torch.float64, device=x.device)
+    res = {}
+    for key, (a, b) in {"no_qat": ("w4a4", "w16a16"), "qat": ("w4a4", "w4a16"),
+                        "qat_rac": ("w4a4_rac", "w4a16")}.items():
+        d, n = nv.nvfp4_mismatch_norm(outs[a], outs[b], acc)
+        res[key] = round(d / n, 5)
+    res["what"] = "||Y_infer - Y_train|| / ||Y_train||: W4A4 vs BF16, W4A4 vs W4A16 QAT, W4A4+RAC vs W4A16 QAT"
+    return res
+
+
 _ORACLE_WEIGHTS = {}
 
 
-def cpu_baseline(seconds=12.0, rows=None):
+def cpu_baseline(seconds=10.0, rows=None):
     """The oracle as it stands (plain C, one thread) on a bounded sample of the
-    workload: the routed rows of one expert through both W4A4+RAC projections
-    (quantize of the expert's weights included).  Returns TFLOP/s of GEMM work."""
+    workload: batches of routed rows of one expert through both W4A4+RAC
+    projections, repeated until `seconds` of oracle time have run (one batch
+    when 0).  Returns TFLOP/s of GEMM work."""
     import numpy as np
 
     import oracle
@@ -390,17 +422,20 @@ def cpu_baseline(seconds=12.0, rows=None):
         cd, sd, _, gd = oracle.quantize(synth.u16(synth.expert_weight(WORKLOAD, 0, "down")))
         _ORACLE_WEIGHTS["w"] = (oracle.dequantize_exact(cw, sw, gw), oracle.dequantize_exact(cd, sd, gd))
     wq13, wqd = _ORACLE_WEIGHTS["w"]
-    t0 = time.perf_counter()
-    ca, sa, ra, ga = oracle.quantize(x, S=S13)
-    y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, ga), wq13, ra, S13, ga)
-    h = oracle.bf16_round(oracle.swiglu(y, I).astype(np.float32))
-    ch, sh, rh, gh = oracle.quantize(h, S=Sd)
-    oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gh), wqd, rh, Sd, gh)
-    dt = time.perf_counter() - t0
-    fl = 2 * n * (2 * I) * (H + k) + 2 * n * H * (I + k)
+    dt, batches = 0.0, 0
+    while batches == 0 or dt < seconds:
+        t0 = time.perf_counter()
+        ca, sa, ra, ga = oracle.quantize(x, S=S13)
+        y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, ga), wq13, ra, S13, ga)
+        h = oracle.bf16_round(oracle.swiglu(y, I).astype(np.float32))
+        ch, sh, rh, gh = oracle.quantize(h, S=Sd)
+        oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gh), wqd, rh, Sd, gh)
+        dt += time.perf_counter() - t0
+        batches += 1
+    fl = batches * (2 * n * (2 * I) * (H + k) + 2 * n * H * (I + k))
     return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": "%d routed rows of one expert: quantize x, W4A4+RAC gate_up, SwiGLU, quantize h, "
-                      "W4A4+RAC down; plain C oracle, 1 thread (%.1f s timed)" % (n, dt),
+            "sample": "%d x %d routed rows of one expert: quantize x, W4A4+RAC gate_up, SwiGLU, quantize h, "
+                      "W4A4+RAC down; plain C oracle, 1 thread (%.1f s timed)" % (batches, n, dt),
             "seconds": round(time.perf_counter() - t_start, 2)}
 
 
@@ -413,10 +448,10 @@ def run_reference(args):
     build_oracle()
     vals = []
     for _ in range(args.warmup):
-        cpu_baseline(rows=32)
+        cpu_baseline(seconds=0, rows=32)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(rows=32))
+        vals.append(cpu_baseline(seconds=0, rows=32))
     wall = time.perf_counter() - t0
     v = statistics.median(x["value"] for x in vals)
     out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
@@ -551,7 +586,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-case", default=None,
                     help="run one kernel on a reduced case for ncu: gemm13, gemm_down, quantize_x, bf16_gemm")
     args = ap.parse_args()

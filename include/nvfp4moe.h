@@ -305,6 +305,21 @@ int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t
  * real fault.  The GEMM pipelines use the same routine with a 2 s limit. */
 int nvfp4_selftest_wait_timeout(int32_t limit_us, int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Layer-wise forward mismatch of QUADS §3.1 Eq. 11, dY = ||Y_infer - Y_train||_2
+ * (Frobenius norm over the layer output), with the reference's own norm for
+ * scale: acc[0] = sum (y_infer - y_train)^2 and acc[1] = sum y_train^2 over
+ * the n elements, in binary64 (per-block partial sums added atomically, so the
+ * last bits depend on the order the blocks finish).  The call clears acc on
+ * `stream` first; dY = sqrt(acc[0]).
+ *   y_infer, y_train  device float[n]
+ *   acc               device double[2]
+ * Errors: INVALID_ARG, ALIGNMENT (16-byte pointers). */
+int nvfp4_mismatch_norm(const float *y_infer, const float *y_train, int64_t n, double *acc, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -42,6 +42,7 @@ _SIGS = {
     "nvfp4_moe_scatter_rows": "piqipppiqpp",
     "nvfp4_moe_combine": "piqppiiqpp",
     "nvfp4_selftest_wait_timeout": "ipp",
+    "nvfp4_mismatch_norm": "ppqpp",
 }
 _CT = {"p": ctypes.c_void_p, "q": ctypes.c_int64, "i": ctypes.c_int32}
 
@@ -214,6 +215,15 @@ def nvfp4_moe_combine(y, dst_row, weights, topk, out, stream=None):
 def nvfp4_selftest_wait_timeout(limit_us, dev_status, stream=None):
     """Bounded-wait self test: dev_status becomes NVFP4_ERR_TIMEOUT."""
     _call("nvfp4_selftest_wait_timeout", limit_us, _p(dev_status), _s(stream))
+
+
+def nvfp4_mismatch_norm(y_infer, y_train, acc, stream=None):
+    """QUADS §3.1 Eq. 11: (||y_infer - y_train||_2, ||y_train||_2) of two FP32
+    layer outputs; `acc` is a device float64[2] work buffer."""
+    assert y_infer.shape == y_train.shape
+    _call("nvfp4_mismatch_norm", _p(y_infer), _p(y_train), y_train.numel(), _p(acc), _s(stream))
+    a = acc.cpu().tolist()
+    return a[0] ** 0.5, a[1] ** 0.5
 
 
 from .layer import RolloutMoE, QatMoE, scale_bytes, rows_capacity  # noqa: E402

@@ -220,9 +220,47 @@ __global__ void combine_bf16_kernel(const uint16_t *y, int64_t ldy, const int32_
     }
 }
 
+// QUADS §3.1 Eq. 11: sum (a - b)^2 and sum b^2, each thread in binary64 over
+// its grid-stride share (FP32 products of FP32 values are exact in binary64),
+// then a warp reduction and one atomic add per warp.
+__global__ void mismatch_kernel(const float *a, const float *b, int64_t n, double *acc) {
+    double d2 = 0.0, b2 = 0.0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const double x = (double)a[i], y = (double)b[i];
+        d2 = __dadd_rn(d2, __dmul_rn(__dsub_rn(x, y), __dsub_rn(x, y)));
+        b2 = __dadd_rn(b2, __dmul_rn(y, y));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+        b2 += __shfl_xor_sync(0xffffffffu, b2, o);
+    }
+    if ((threadIdx.x & 31) == 0) {
+        atomicAdd(&acc[0], d2);
+        atomicAdd(&acc[1], b2);
+    }
+}
+
 }  // namespace nvfp4
 
 using namespace nvfp4;
+
+extern "C" int nvfp4_mismatch_norm(const float *y_infer, const float *y_train, int64_t n, double *acc, void *stream) {
+    if (!y_infer || !y_train || !acc || n < 0) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(y_infer) || !aligned16(y_train) || !aligned16(acc)) return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = cudaMemsetAsync(acc, 0, 2 * sizeof(double), st);
+    if (e != cudaSuccess) {
+        set_last_error("cudaMemsetAsync(acc)", e);
+        return NVFP4_ERR_CUDA;
+    }
+    if (n == 0) return NVFP4_OK;
+    int64_t blocks = (n + 255) / 256, cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    mismatch_kernel<<<(unsigned)blocks, 256, 0, st>>>(y_infer, y_train, n, acc);
+    return launch_status("mismatch_kernel");
+}
 
 extern "C" int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32_t topk, int32_t *ids, float *weights,
                                 int32_t *counts, int32_t *offsets, int32_t *dst_row, void *stream) {

@@ -153,16 +153,19 @@ class RolloutMoE:
 
 
 class QatMoE:
-    """Trainer-side asymmetric-QAT MoE forward (weights fake-quantized, BF16 activations)."""
+    """Trainer-side asymmetric-QAT MoE forward (weights fake-quantized, BF16
+    activations: W4A16).  fake=False gives the plain BF16 trainer (W16A16),
+    the reference of the mismatch diagnostic."""
 
-    def __init__(self, w13, w_down, topk, max_tokens):
+    def __init__(self, w13, w_down, topk, max_tokens, fake=True):
         self.E, N13, self.H = w13.shape
         self.I = N13 // 2
         self.topk = topk
         dev = w13.device
         self.w13, self.wd = w13, w_down
-        self.w13_hat = torch.empty_like(w13)
-        self.wd_hat = torch.empty_like(w_down)
+        self.fake = fake
+        self.w13_hat = torch.empty_like(w13) if fake else w13
+        self.wd_hat = torch.empty_like(w_down) if fake else w_down
         self.gs13 = torch.empty(self.E, dtype=torch.float32, device=dev)
         self.gsd = torch.empty(self.E, dtype=torch.float32, device=dev)
         self.amax_ws = torch.empty(self.E, dtype=torch.float32, device=dev)
@@ -176,6 +179,8 @@ class QatMoE:
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def fake_quant(self, stream=None):
+        if not self.fake:
+            return
         nvfp4_fake_quant(self.w13, self.w13_hat, self.amax_ws, gs_out=self.gs13,
                          dev_status=self.dev_status, stream=stream)
         nvfp4_fake_quant(self.wd, self.wd_hat, self.amax_ws, gs_out=self.gsd,

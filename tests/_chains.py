@@ -1,0 +1,91 @@
+"""Oracle chains of one MoE layer forward, for the mismatch tests (QUADS §3.1
+Eq. 11, §3.2 Eq. 12, §3.3 Eq. 21): the trainer (BF16 activations; weights BF16
+or fake-quantized) and the rollout (W4A4, optionally with the RAC residual).
+Rounding points follow the library's layers: BF16 routed inputs, binary64
+GEMM sums, BF16 h and y, binary64 combine."""
+import numpy as np
+
+import oracle
+import synth
+
+
+def route(logits, E, topk):
+    ids, rw = oracle.route_topk(logits, topk)
+    counts, offs, dst = oracle.route_layout(ids, E)
+    return ids, rw, counts, offs, dst
+
+
+def _combine(y_rows, dst, rw):
+    yb = oracle.bf16_to_f32(oracle.bf16_round(y_rows.astype(np.float32))).astype(np.float64)
+    return oracle.combine(yb, dst.astype(np.int32), rw)
+
+
+def trainer(x_u16, logits, w13, wd, topk, fake):
+    """W16A16 (fake=False) or W4A16 (fake=True) trainer forward -> out [T, H] binary64."""
+    E, N13, H = w13.shape
+    I = N13 // 2
+    ids, rw, counts, offs, dst = route(logits, E, topk)
+    R = int(offs[-1])
+    xf = oracle.bf16_to_f32(x_u16).astype(np.float64)
+    h = np.zeros((R, I))
+    yd = np.zeros((R, H))
+    wq13, wqd = [], []
+    for e in range(E):
+        a, b = synth.u16(w13[e]), synth.u16(wd[e])
+        if fake:
+            a, _ = oracle.fake_quant(a)
+            b, _ = oracle.fake_quant(b)
+        wq13.append(oracle.bf16_to_f32(a).astype(np.float64))
+        wqd.append(oracle.bf16_to_f32(b).astype(np.float64))
+    for e in range(E):
+        toks = np.nonzero((ids == e).any(1))[0]
+        if toks.size:
+            rows = dst[toks, np.argmax(ids[toks] == e, 1)]
+            h[rows] = oracle.swiglu(xf[toks] @ wq13[e].T, I)
+    hb = oracle.bf16_to_f32(oracle.bf16_round(h.astype(np.float32))).astype(np.float64)
+    for e in range(E):
+        r0, r1 = offs[e], offs[e] + counts[e]
+        if r1 > r0:
+            yd[r0:r1] = hb[r0:r1] @ wqd[e].T
+    return _combine(yd, dst, rw)
+
+
+def rollout(x_u16, logits, w13, wd, topk, S13=None, Sd=None):
+    """W4A4 rollout forward, with the RAC residual on S13 / Sd when given -> out [T, H]."""
+    E, N13, H = w13.shape
+    I = N13 // 2
+    ids, rw, counts, offs, dst = route(logits, E, topk)
+    R = int(offs[-1])
+    ca, sa, ra, ga = oracle.quantize(x_u16, S=S13)
+    xq = oracle.dequantize_exact(ca, sa, ga)
+    h = np.zeros((R, I))
+    for e in range(E):
+        toks = np.nonzero((ids == e).any(1))[0]
+        if toks.size:
+            cw, sw, _, gw = oracle.quantize(synth.u16(w13[e]))
+            y = oracle.rac_gemm(xq[toks], oracle.dequantize_exact(cw, sw, gw), ra[toks] if S13 is not None else None,
+                                S13, ga)
+            rows = dst[toks, np.argmax(ids[toks] == e, 1)]
+            h[rows] = oracle.swiglu(y, I)
+    hu = oracle.bf16_round(h.astype(np.float32))
+    ch, sh, rh, gh = oracle.quantize(hu, S=Sd)
+    hq = oracle.dequantize_exact(ch, sh, gh)
+    yd = np.zeros((R, H))
+    for e in range(E):
+        r0, r1 = offs[e], offs[e] + counts[e]
+        if r1 > r0:
+            cw, sw, _, gw = oracle.quantize(synth.u16(wd[e]))
+            yd[r0:r1] = oracle.rac_gemm(hq[r0:r1], oracle.dequantize_exact(cw, sw, gw),
+                                        rh[r0:r1] if Sd is not None else None, Sd, gh)
+    return _combine(yd, dst, rw)
+
+
+def inputs(cfg, T):
+    c = synth.CONFIGS[cfg]
+    x = synth.activations(cfg)[:T].contiguous()
+    logits = synth.router_logits(cfg)[:T].contiguous()
+    import torch
+
+    w13 = torch.stack([synth.expert_weight(cfg, e, "w13") for e in range(c["E"])])
+    wd = torch.stack([synth.expert_weight(cfg, e, "down") for e in range(c["E"])])
+    return c, x, logits, w13, wd

@@ -47,7 +47,7 @@ def layer_run():
 
     nv.load(build=True)
     dev = torch.device(G.DEV)
-    c, layer, x, logits = bench.build_workload(dev)
+    c, layer, x, logits, _ = bench.build_workload(dev)
     out = layer.forward(x, logits)
     torch.cuda.synchronize()
     G.status_ok(layer.dev_status)

@@ -1,0 +1,42 @@
+"""Pin of the oracle's layer-mismatch chains (QUADS §3.1 Eq. 11, Fig. 4b): on a
+small MoE layer whose activations carry outlier channels, the forward mismatch
+dY = ||Y_infer - Y_train|| against a W4A4 rollout must shrink when the trainer
+fake-quantizes its weights (W4A16 QAT removes the weight term of Eq. 11, §3.2)
+and shrink again when the rollout adds the RAC residual on the selected
+channels (Eq. 20-22 remove part of the activation term).  A sign error in the
+correction, a dropped fake-quant or a transposed operand breaks the order."""
+import numpy as np
+import torch
+
+import oracle
+from tests import _chains
+
+
+def small_moe(seed=0, T=64, E=4, H=256, I=256, n_out=4):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((T, H), generator=g, dtype=torch.float64)
+    out_ch = torch.randperm(H, generator=g)[:n_out]
+    x[:, out_ch] *= 40
+    logits = torch.randn((T, E), generator=g)
+    w13 = (torch.randn((E, 2 * I, H), generator=g) * 0.02).to(torch.bfloat16)
+    wd = (torch.randn((E, H, I), generator=g) * 0.02).to(torch.bfloat16)
+    return x.to(torch.bfloat16), logits, w13, wd
+
+
+def test_mismatch_order_no_qat_qat_rac():
+    x, logits, w13, wd = small_moe()
+    xu = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+    S13 = oracle.select_channels(oracle.channel_scores_sq(xu), 32)
+    Sd = np.arange(0, 256, 16, dtype=np.int32)
+    l = logits.numpy()
+    y16 = _chains.trainer(xu, l, w13, wd, 2, fake=False)
+    y416 = _chains.trainer(xu, l, w13, wd, 2, fake=True)
+    y44 = _chains.rollout(xu, l, w13, wd, 2)
+    y44r = _chains.rollout(xu, l, w13, wd, 2, S13, Sd)
+    d_noqat = np.linalg.norm(y44 - y16)
+    d_qat = np.linalg.norm(y44 - y416)
+    d_rac = np.linalg.norm(y44r - y416)
+    assert d_noqat > d_qat > d_rac > 0
+    # the weight term alone: with both sides on the same fake-quantized weights
+    # and BF16 activations the mismatch is the rounding of h and y only
+    assert np.linalg.norm(y416 - _chains.trainer(xu, l, w13, wd, 2, fake=True)) == 0.0
