@@ -369,31 +369,45 @@ def qat_measure(dev, steps):
 
 def mismatch_measure(layer, x, logits, w13, wd):
     """Layer-wise forward mismatch of QUADS §3.1 Eq. 11 (Fig. 4b) on the
-    benchmark's own batch and weights: ||Y_rollout - Y_trainer|| / ||Y_trainer||
-    for the W4A4 rollout against the BF16 trainer (no QAT), the W4A4 rollout
-    against the W4A16 QAT trainer, and the W4A4 + RAC rollout (`layer`) against
-    the QAT trainer; norms by nvfp4_mismatch_norm in binary64."""
+    benchmark's own batch and weights, ||Y_rollout - Y_trainer|| / ||Y_trainer||
+    (norms by nvfp4_mismatch_norm in binary64), for the W4A4 rollout against
+    the BF16 trainer (no QAT), against the W4A16 QAT trainer, the W4A4 + RAC
+    rollout (`layer`) against the QAT trainer, and the W4A4 rollout against
+    the symmetric W4A4 QAT trainer (§4.3.1 Fig. 7).  `eta` repeats them with
+    the rollout's input drifted by ~2^-10 relative (Eq. 8), next to the
+    drift's own effect on the BF16 layer."""
     import torch
 
     import nvfp4_precision_moe_gb300 as nv
+    import synth
 
     T = x.shape[0]
-    outs = {"w4a4_rac": layer.forward(x, logits).clone()}
-    for name, mk in [("w4a4", lambda: nv.RolloutMoE(w13, wd, None, None, layer.topk, T)),
-                     ("w16a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=False)),
-                     ("w4a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=True))]:
+    xe = synth.engine_drift(x.cpu(), 2.0 ** -10, 1).to(x.device)
+    outs = {"w4a4_rac": layer.forward(x, logits).clone(), "w4a4_rac@eta": layer.forward(xe, logits).clone()}
+    for name, mk, drift in [("w4a4", lambda: nv.RolloutMoE(w13, wd, None, None, layer.topk, T), True),
+                            ("w16a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=False), True),
+                            ("w4a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=True), False),
+                            ("w4a4_sym", lambda: nv.QatMoE(w13, wd, layer.topk, T, sym=True), False)]:
         lay = mk()
         outs[name] = lay.forward(x, logits).clone()
+        if drift:
+            outs[name + "@eta"] = lay.forward(xe, logits).clone()
         torch.cuda.synchronize()
         assert int(lay.dev_status.item()) == 0
         del lay
     acc = torch.zeros(2, dtype=torch.float64, device=x.device)
-    res = {}
-    for key, (a, b) in {"no_qat": ("w4a4", "w16a16"), "qat": ("w4a4", "w4a16"),
-                        "qat_rac": ("w4a4_rac", "w4a16")}.items():
+
+    def rel(a, b):
         d, n = nv.nvfp4_mismatch_norm(outs[a], outs[b], acc)
-        res[key] = round(d / n, 5)
-    res["what"] = "||Y_infer - Y_train|| / ||Y_train||: W4A4 vs BF16, W4A4 vs W4A16 QAT, W4A4+RAC vs W4A16 QAT"
+        return round(d / n, 6)
+
+    res = {"no_qat": rel("w4a4", "w16a16"), "qat": rel("w4a4", "w4a16"), "qat_rac": rel("w4a4_rac", "w4a16"),
+           "sym_qat": rel("w4a4", "w4a4_sym"),
+           "eta": {"rel": 2.0 ** -10, "bf16": rel("w16a16@eta", "w16a16"), "no_qat": rel("w4a4@eta", "w16a16"),
+                   "qat": rel("w4a4@eta", "w4a16"), "qat_rac": rel("w4a4_rac@eta", "w4a16"),
+                   "sym_qat": rel("w4a4@eta", "w4a4_sym")}}
+    res["what"] = ("||Y_infer - Y_train|| / ||Y_train||: W4A4 vs BF16, W4A4 vs W4A16 QAT, W4A4+RAC vs W4A16 "
+                   "QAT, W4A4 vs symmetric W4A4 QAT; eta: the rollout's input drifted (bf16: the drift alone)")
     return res
 
 

@@ -155,15 +155,19 @@ class RolloutMoE:
 class QatMoE:
     """Trainer-side asymmetric-QAT MoE forward (weights fake-quantized, BF16
     activations: W4A16).  fake=False gives the plain BF16 trainer (W16A16),
-    the reference of the mismatch diagnostic."""
+    the reference of the mismatch diagnostic; sym=True (with fake=True) the
+    symmetric W4A4 QAT ablation of QUADS §4.3.1 Fig. 7, which fake-quantizes
+    the activations x and h as well (one tensor scale each, the rollout's
+    NVFP4 recipe)."""
 
-    def __init__(self, w13, w_down, topk, max_tokens, fake=True):
+    def __init__(self, w13, w_down, topk, max_tokens, fake=True, sym=False):
+        assert fake or not sym
         self.E, N13, self.H = w13.shape
         self.I = N13 // 2
         self.topk = topk
         dev = w13.device
         self.w13, self.wd = w13, w_down
-        self.fake = fake
+        self.fake, self.sym = fake, sym
         self.w13_hat = torch.empty_like(w13) if fake else w13
         self.wd_hat = torch.empty_like(w_down) if fake else w_down
         self.gs13 = torch.empty(self.E, dtype=torch.float32, device=dev)
@@ -177,6 +181,11 @@ class QatMoE:
         self.y = torch.zeros((self.rows_cap, self.H), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((max_tokens, self.H), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if sym:
+            self.x_hat = torch.empty((max_tokens, self.H), dtype=torch.bfloat16, device=dev)
+            self.h_hat = torch.zeros((self.rows_cap, self.I), dtype=torch.bfloat16, device=dev)
+            self.act_amax = torch.empty(2, dtype=torch.float32, device=dev)
+            self.act_gs = torch.empty(2, dtype=torch.float32, device=dev)
 
     def fake_quant(self, stream=None):
         if not self.fake:
@@ -201,13 +210,29 @@ class QatMoE:
         mark(1)
         nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=stream)
         mark(2)
+        if self.sym:  # QDQ_A of x over the batch's T tokens (the rollout's amax)
+            nvfp4_fake_quant(x.view(1, T, self.H), self.x_hat[:T].view(1, T, self.H), self.act_amax[0:1],
+                             gs_out=self.act_gs[0:1], dev_status=self.dev_status, stream=stream)
+            x = self.x_hat[:T]
         nvfp4_moe_scatter_rows(x, self.topk, dst, r.counts, r.offsets, self.E, self.xr, stream=stream)
         mark(3)
+        cap = rows_capacity(T, self.topk, self.E)
+        if self.sym:
+            # rows [offsets[E], cap) are not written by the GEMM: zero them all
+            # first so that the amax of QDQ_A(h) sees the routed rows only
+            with torch.cuda.stream(stream or torch.cuda.current_stream()):
+                self.h[:cap].zero_()
         nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.h,
                                 out_dtype=NVFP4_OUT_BF16, epilogue=NVFP4_EPI_SWIGLU,
                                 dev_status=self.dev_status, stream=stream)
+        h = self.h
+        if self.sym:
+            nvfp4_fake_quant(self.h[:cap].view(1, cap, self.I), self.h_hat[:cap].view(1, cap, self.I),
+                             self.act_amax[1:2], gs_out=self.act_gs[1:2], dev_status=self.dev_status,
+                             stream=stream)
+            h = self.h_hat
         mark(4)
-        nvfp4_bf16_grouped_gemm(self.h, self.wd_hat, r.offsets, self.E, self.H, self.I, self.y,
+        nvfp4_bf16_grouped_gemm(h, self.wd_hat, r.offsets, self.E, self.H, self.I, self.y,
                                 out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
         mark(5)
         out = self.out[:T]

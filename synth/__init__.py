@@ -115,6 +115,17 @@ def router_logits(cfg_id):
     return (gumbel + logp[None, :]).to(torch.float32)
 
 
+def engine_drift(x, rel, seed):
+    """Synthetic engine drift eta (QUADS §3.1 Eq. 8): the inference engine's
+    copy of a BF16 activation x, bf16(x * (1 + rel * z)) with z ~ N(0, 1)
+    seeded per element -- a relative perturbation of about rel, standing in
+    for the different reduction orders of two engines."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(7919 * 100003 + seed)
+    z = torch.randn(x.shape, generator=g, dtype=torch.float64)
+    return (x.double() * (1.0 + rel * z)).to(torch.bfloat16)
+
+
 def u16(t):
     """BF16 torch tensor -> numpy uint16 bit patterns (for the oracle)."""
     return t.contiguous().view(torch.int16).numpy().view("uint16")

@@ -1,6 +1,7 @@
 """Oracle chains of one MoE layer forward, for the mismatch tests (QUADS §3.1
-Eq. 11, §3.2 Eq. 12, §3.3 Eq. 21): the trainer (BF16 activations; weights BF16
-or fake-quantized) and the rollout (W4A4, optionally with the RAC residual).
+Eq. 11, §3.2 Eq. 12, §3.3 Eq. 21, §4.3.1 Fig. 7): the trainer (weights BF16 or
+fake-quantized; activations BF16, or fake-quantized too for the symmetric W4A4
+QAT ablation) and the rollout (W4A4, optionally with the RAC residual).
 Rounding points follow the library's layers: BF16 routed inputs, binary64
 GEMM sums, BF16 h and y, binary64 combine."""
 import numpy as np
@@ -20,12 +21,16 @@ def _combine(y_rows, dst, rw):
     return oracle.combine(yb, dst.astype(np.int32), rw)
 
 
-def trainer(x_u16, logits, w13, wd, topk, fake):
-    """W16A16 (fake=False) or W4A16 (fake=True) trainer forward -> out [T, H] binary64."""
+def trainer(x_u16, logits, w13, wd, topk, fake, sym=False):
+    """W16A16 (fake=False), W4A16 (fake=True) or, with sym=True, symmetric W4A4
+    QAT (x and h fake-quantized as well, one tensor scale each) trainer forward
+    -> out [T, H] binary64."""
     E, N13, H = w13.shape
     I = N13 // 2
     ids, rw, counts, offs, dst = route(logits, E, topk)
     R = int(offs[-1])
+    if sym:
+        x_u16, _ = oracle.fake_quant(x_u16)
     xf = oracle.bf16_to_f32(x_u16).astype(np.float64)
     h = np.zeros((R, I))
     yd = np.zeros((R, H))
@@ -42,7 +47,10 @@ def trainer(x_u16, logits, w13, wd, topk, fake):
         if toks.size:
             rows = dst[toks, np.argmax(ids[toks] == e, 1)]
             h[rows] = oracle.swiglu(xf[toks] @ wq13[e].T, I)
-    hb = oracle.bf16_to_f32(oracle.bf16_round(h.astype(np.float32))).astype(np.float64)
+    hu = oracle.bf16_round(h.astype(np.float32))
+    if sym:
+        hu, _ = oracle.fake_quant(hu)
+    hb = oracle.bf16_to_f32(hu).astype(np.float64)
     for e in range(E):
         r0, r1 = offs[e], offs[e] + counts[e]
         if r1 > r0:

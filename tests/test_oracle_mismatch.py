@@ -9,6 +9,7 @@ import numpy as np
 import torch
 
 import oracle
+import synth
 from tests import _chains
 
 
@@ -37,6 +38,28 @@ def test_mismatch_order_no_qat_qat_rac():
     d_qat = np.linalg.norm(y44 - y416)
     d_rac = np.linalg.norm(y44r - y416)
     assert d_noqat > d_qat > d_rac > 0
-    # the weight term alone: with both sides on the same fake-quantized weights
-    # and BF16 activations the mismatch is the rounding of h and y only
-    assert np.linalg.norm(y416 - _chains.trainer(xu, l, w13, wd, 2, fake=True)) == 0.0
+
+
+def test_symmetric_qat_aligns_only_without_engine_drift():
+    """Symmetric W4A4 QAT (QUADS §4.3.1 Fig. 7): the learner fake-quantizes x
+    and h with the rollout's own NVFP4 recipe (§3.2 Eq. 15-16 for the shared
+    QDQ path), so with identical inputs (eta = 0, Eq. 8) its forward IS the
+    W4A4 rollout forward -- every quantized operand is exact in BF16 and both
+    chains sum in binary64.  With a drift eta of ~2^-10 relative on the
+    rollout's input, the two sides quantize different activations (Table 1)
+    and the E2M1 decision boundaries amplify it: the symmetric mismatch is
+    many times the drift's own effect on the BF16 layer."""
+    x, logits, w13, wd = small_moe()
+    xu, l = synth.u16(x), logits.numpy()
+    y_sym = _chains.trainer(xu, l, w13, wd, 2, fake=True, sym=True)
+    y44 = _chains.rollout(xu, l, w13, wd, 2)
+    assert np.array_equal(y_sym, y44)
+    # a dropped activation fake-quant is not aligned
+    y416 = _chains.trainer(xu, l, w13, wd, 2, fake=True)
+    assert np.linalg.norm(y416 - y44) > 0.05 * np.linalg.norm(y44)
+    xe = synth.u16(synth.engine_drift(x, 2.0 ** -10, 1))
+    assert (xe != xu).any()
+    d_eta = np.linalg.norm(_chains.trainer(xe, l, w13, wd, 2, fake=False)
+                           - _chains.trainer(xu, l, w13, wd, 2, fake=False))
+    d_sym = np.linalg.norm(_chains.rollout(xe, l, w13, wd, 2) - y_sym)
+    assert d_sym > 5 * d_eta > 0
