@@ -387,7 +387,9 @@ def mismatch_measure(layer, x, logits, w13, wd):
     for name, mk, drift in [("w4a4", lambda: nv.RolloutMoE(w13, wd, None, None, layer.topk, T), True),
                             ("w16a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=False), True),
                             ("w4a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=True), False),
-                            ("w4a4_sym", lambda: nv.QatMoE(w13, wd, layer.topk, T, sym=True), False)]:
+                            ("w4a4_sym", lambda: nv.QatMoE(w13, wd, layer.topk, T, sym=True), False),
+                            ("w4a4_rac_fp4", lambda: nv.RolloutMoE(w13, wd, layer.S13, layer.Sd, layer.topk, T,
+                                                                   resid_fp4=True), False)]:
         lay = mk()
         outs[name] = lay.forward(x, logits).clone()
         if drift:
@@ -402,12 +404,14 @@ def mismatch_measure(layer, x, logits, w13, wd):
         return round(d / n, 6)
 
     res = {"no_qat": rel("w4a4", "w16a16"), "qat": rel("w4a4", "w4a16"), "qat_rac": rel("w4a4_rac", "w4a16"),
+           "qat_rac_fp4": rel("w4a4_rac_fp4", "w4a16"),
            "sym_qat": rel("w4a4", "w4a4_sym"),
            "eta": {"rel": 2.0 ** -10, "bf16": rel("w16a16@eta", "w16a16"), "no_qat": rel("w4a4@eta", "w16a16"),
                    "qat": rel("w4a4@eta", "w4a16"), "qat_rac": rel("w4a4_rac@eta", "w4a16"),
                    "sym_qat": rel("w4a4@eta", "w4a4_sym")}}
     res["what"] = ("||Y_infer - Y_train|| / ||Y_train||: W4A4 vs BF16, W4A4 vs W4A16 QAT, W4A4+RAC vs W4A16 "
-                   "QAT, W4A4 vs symmetric W4A4 QAT; eta: the rollout's input drifted (bf16: the drift alone)")
+                   "QAT (BF16 residual; FP4 residual of the literal Eq. 21), W4A4 vs symmetric W4A4 QAT; eta: "
+                   "the rollout's input drifted (bf16: the drift alone)")
     return res
 
 

@@ -188,6 +188,25 @@ int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_t K, const 
 int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, const float *amax, int32_t k,
                               int32_t *S_out, double *score_ws, void *stream);
 
+/* The literal second-pass form of RAC, QUADS §3.3 Eq. 21: the residual on S
+ * is itself NVFP4-quantized, X~ = Q_A(X) + M_S * Q_A(r) with r = -Delta X_q.
+ * Reading: Q_A acts on the gathered [rows, k] residual -- 16-element blocks
+ * along the gathered channel axis -- with a tensor scale of its own, from
+ * amax |r| over the routed rows.  Replaces, in place, the BF16 residual that
+ * nvfp4_quantize stored (in units of gs_a) by Q_A(r) in the same units; every
+ * such value is exact in BF16, so nvfp4_w4a4_rac_grouped_gemm applies the
+ * second-pass correction unchanged.
+ *   resid     device BF16 [rows_cap, k] (row pitch k), nvfp4_quantize's resid
+ *   offsets   device int32[E+1] from nvfp4_route_topk: rows [0, offsets[E])
+ *             are processed (their padding rows hold zeros); NULL: all rows
+ *   amax_ws   device float scratch: receives max |resid| of those rows
+ *   gs_out    device float or NULL: the residual's tensor scale (units of gs_a)
+ * Rows past offsets[E] are neither read nor written.  dev_status gets
+ * NONFINITE (and resid is left as it was) if the amax is not finite.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (k % 16). */
+int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t k, const int32_t *offsets, int32_t E,
+                               float *amax_ws, float *gs_out, int32_t *dev_status, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Grouped GEMMs (QUADS §3.3 Eq. 21; §3.2 Eq. 12)                            */
 /* ------------------------------------------------------------------------ */

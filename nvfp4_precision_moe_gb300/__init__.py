@@ -34,6 +34,7 @@ _SIGS = {
     "nvfp4_fake_quant_noalloc": "piqqpppp",
     "nvfp4_prepare_weights": "piqqpiippppppp",
     "nvfp4_rac_select_channels": "pqqpippp",
+    "nvfp4_rac_requant_residual": "pqipipppp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
     "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
     "nvfp4_gemm_pipeline": "ip",
@@ -139,6 +140,14 @@ def nvfp4_fake_quant_noalloc(w, w_hat, gs_out=None, dev_status=None, stream=None
     nt, rows, cols = w.shape
     _call("nvfp4_fake_quant_noalloc", _p(w), nt, rows, cols, _p(w_hat), _p(gs_out), _p(dev_status),
           _s(stream))
+
+
+def nvfp4_rac_requant_residual(resid, amax_ws, offsets=None, E=0, gs_out=None, dev_status=None, stream=None):
+    """Literal Eq. 21 residual: resid [rows_cap, k] BF16 replaced in place by
+    its own NVFP4 quantize-dequantize (rows [0, offsets[E]) when offsets is given)."""
+    rows_cap, k = resid.shape
+    _call("nvfp4_rac_requant_residual", _p(resid), rows_cap, k, _p(offsets), E, _p(amax_ws), _p(gs_out),
+          _p(dev_status), _s(stream))
 
 
 def nvfp4_prepare_weights(w, w_codes, w_scales, gs_w, amax_ws, S=None, w_sel=None, interleave=0,

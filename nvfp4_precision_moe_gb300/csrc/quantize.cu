@@ -543,6 +543,79 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, in
     }
 }
 
+// ---- literal second-pass RAC residual (QUADS §3.3 Eq. 21): the BF16 residual
+// that quantize_kernel stored for the routed rows [0, offsets[E]) is itself
+// NVFP4-quantized -- 16-element blocks along the gathered channel axis, a
+// tensor scale of its own -- and replaced in place by its dequantized value
+// (exact in BF16: a grid value times an E4M3 scale has at most 6 significant
+// bits, and the tensor scale is a power of two).  Rows past offsets[E] are
+// left alone, so stale rows of an earlier, larger batch cannot reach the amax.
+__device__ __forceinline__ int64_t resid_rows(int64_t rows_cap, const int32_t *offsets, int32_t E) {
+    if (!offsets) return rows_cap;
+    const int64_t r = offsets[E];
+    return r < 0 ? 0 : (r > rows_cap ? rows_cap : r);
+}
+
+__global__ void __launch_bounds__(256) resid_amax_kernel(const uint16_t *resid, int64_t rows_cap, int32_t k,
+                                                        const int32_t *offsets, int32_t E, float *out) {
+    const int64_t total = resid_rows(rows_cap, offsets, E) * (k >> 3);  // 8 BF16 per 16-byte load
+    const uint4 *p = reinterpret_cast<const uint4 *>(resid);
+    uint32_t mx = 0u;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 v = __ldg(p + i);
+        mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
+        mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
+        mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
+        mx = __vmaxu2(mx, v.w & 0x7fff7fffu);
+    }
+    uint32_t m16 = max(mx & 0xffffu, mx >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, o));
+    __shared__ uint32_t red[8];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m16;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t r = 0;
+        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = max(r, red[w]);
+        atomicMax(reinterpret_cast<unsigned int *>(out), r << 16);
+    }
+}
+
+__global__ void __launch_bounds__(256) resid_qdq_kernel(uint16_t *resid, int64_t rows_cap, int32_t k,
+                                                       const int32_t *offsets, int32_t E, const float *amax,
+                                                       float *gs_out, int32_t *dev_status) {
+    __shared__ QTables tb;
+    fill_tables(tb);
+    __syncthreads();
+    const float am = *amax;
+    if (!isfinite(am)) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report(dev_status, NVFP4_ERR_NONFINITE);
+        return;
+    }
+    const float gs = tensor_scale(am);
+    const float p6 = __fmul_rn(gs, 6.0f);
+    const float inv_gs = __frcp_rn(gs);  // exact: gs is a power of two
+    if (gs_out && blockIdx.x == 0 && threadIdx.x == 0) *gs_out = gs;
+    const int64_t nblk = resid_rows(rows_cap, offsets, E) * (k >> 4);
+    uint4 *p = reinterpret_cast<uint4 *>(resid);
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += (int64_t)gridDim.x * blockDim.x) {
+        float v[16];
+        unpack_block(p[2 * b], p[2 * b + 1], v);
+        BlockQ q;
+        quant_block(v, gs, p6, inv_gs, tb, q);
+        uint32_t o[8];
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+            const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
+            const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
+            o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
+        }
+        p[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
+        p[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
 static int quant_grid(int64_t rows) {
     int64_t blocks = (rows + kQWarps - 1) / kQWarps;
     int64_t cap = (int64_t)sm_count() * 8;
@@ -675,6 +748,33 @@ extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_
     int g = quant_grid(N) / (E > 8 ? 8 : E);
     quantize_kernel<kModeWeight><<<dim3(g < 1 ? 1 : g, E), kQThreads, 0, st>>>(a);
     return launch_status("quantize_kernel<weight>");
+}
+
+extern "C" int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t k, const int32_t *offsets, int32_t E,
+                                          float *amax_ws, float *gs_out, int32_t *dev_status, void *stream) {
+    if (!resid || !amax_ws || rows_cap < 0 || k < 0 || (offsets && E < 1)) return NVFP4_ERR_INVALID_ARG;
+    if (k % 16) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(resid)) return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(float), st);
+    if (e != cudaSuccess) {
+        set_last_error("cudaMemsetAsync(residual amax)", e);
+        return NVFP4_ERR_CUDA;
+    }
+    if (rows_cap == 0 || k == 0) return NVFP4_OK;
+    // sized for all rows_cap rows; the kernels stop at offsets[E]
+    int64_t blocks = (rows_cap * (k / 8) + 255) / 256;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    resid_amax_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint16_t *)resid, rows_cap, k, offsets, E, amax_ws);
+    int s = launch_status("resid_amax_kernel");
+    if (s != NVFP4_OK) return s;
+    blocks = (rows_cap * (k / 16) + 255) / 256;
+    if (blocks > cap) blocks = cap;
+    resid_qdq_kernel<<<(unsigned)blocks, 256, 0, st>>>((uint16_t *)resid, rows_cap, k, offsets, E, amax_ws, gs_out,
+                                                      dev_status);
+    return launch_status("resid_qdq_kernel");
 }
 
 extern "C" int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,

@@ -18,7 +18,7 @@ import torch
 from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16, NVFP4_OUT_F32,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
-               nvfp4_route_topk, nvfp4_w4a4_rac_grouped_gemm)
+               nvfp4_rac_requant_residual, nvfp4_route_topk, nvfp4_w4a4_rac_grouped_gemm)
 
 
 def scale_bytes(rows, K):
@@ -76,9 +76,11 @@ class RolloutMoE:
     w13: [E, 2I, H] BF16 (gate rows then up rows); w_down: [E, H, I] BF16;
     S13 / S_down: int32 RAC channel sets of the two projections (sorted, on
     the device; may be None for plain W4A4); max_tokens: buffer capacity.
+    resid_fp4: the literal second-pass form of QUADS §3.3 Eq. 21, the residual
+    itself NVFP4-quantized (nvfp4_rac_requant_residual) before the GEMMs.
     """
 
-    def __init__(self, w13, w_down, S13, S_down, topk, max_tokens, out_dtype=torch.float32):
+    def __init__(self, w13, w_down, S13, S_down, topk, max_tokens, out_dtype=torch.float32, resid_fp4=False):
         self.E, N13, self.H = w13.shape
         self.I = N13 // 2
         self.topk = topk
@@ -98,9 +100,15 @@ class RolloutMoE:
         self.y = torch.zeros((self.rows_cap, self.H), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((max_tokens, self.H), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.resid_fp4 = resid_fp4
+        self.resid_amax = torch.zeros(2, dtype=torch.float32, device=dev)
+        self.resid_gs = torch.zeros(2, dtype=torch.float32, device=dev)
+        # number of library kernels one forward launches: routing 2, amax, quantize x,
+        # clear padding, gate_up GEMM, quantize h, down GEMM, combine (+2 per
+        # second-pass residual)
+        self.LAUNCHES = 9 + (2 * (self.k13 > 0) + 2 * (self.kd > 0) if resid_fp4 else 0)
 
-    # number of library kernels one forward launches
-    LAUNCHES = 9  # routing 2, amax, quantize x, clear padding, gate_up GEMM, quantize h, down GEMM, combine
+    LAUNCHES = 9
 
     def forward(self, x, logits, stream=None, mark=None, out=None):
         """x [T, H] BF16, logits [T, E] FP32 -> out [T, H] FP32: `out` if given
@@ -127,6 +135,9 @@ class RolloutMoE:
                        stream=stream)
         nvfp4_moe_clear_padding(r.counts, r.offsets, self.E, self.H, self.k13, xa.codes, xa.scales,
                                 xa.resid if self.k13 else None, stream=stream)
+        if self.resid_fp4 and self.k13:
+            nvfp4_rac_requant_residual(xa.resid, self.resid_amax[0:1], r.offsets, self.E, gs_out=self.resid_gs[0:1],
+                                       dev_status=self.dev_status, stream=stream)
         mark(3)
         W = self.w13
         nvfp4_w4a4_rac_grouped_gemm(xa.codes, xa.scales, xa.resid if W.k else None, xa.gs, W.codes,
@@ -137,6 +148,9 @@ class RolloutMoE:
         nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
                        S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
                        stream=stream)
+        if self.resid_fp4 and self.kd:
+            nvfp4_rac_requant_residual(ha.resid, self.resid_amax[1:2], r.offsets, self.E, gs_out=self.resid_gs[1:2],
+                                       dev_status=self.dev_status, stream=stream)
         mark(5)
         W = self.wd
         nvfp4_w4a4_rac_grouped_gemm(ha.codes, ha.scales, ha.resid if W.k else None, ha.gs, W.codes,

@@ -191,6 +191,23 @@ def swizzle_scales(scales, K):
     return out
 
 
+def requant_residual(resid, gs_a):
+    """The literal second-pass form of QUADS §3.3 Eq. 21: the residual on the
+    selected channels is itself NVFP4-quantized, Q_A(r) with r = resid*gs_a
+    (resid as quantize() returns it, in units of gs_a).  Reading: Q_A acts on
+    the gathered [M, k] residual -- 16-element blocks along the gathered
+    channel axis -- with a tensor scale of its own (from amax |r| over all M
+    rows).  Returns Q_A(r)/gs_a as BF16 bits [M, k] (exact: FP4-grid values
+    need at most 6 significant bits) and the residual's tensor scale."""
+    resid = _c(resid, np.uint16)
+    r = bf16_round((bf16_to_f32(resid).astype(np.float64) * gs_a).astype(np.float32))
+    codes, scales, _, gs_r = quantize(r)
+    q = dequantize_exact(codes, scales, gs_r) / gs_a
+    out = bf16_round(q.astype(np.float32))
+    assert np.array_equal(bf16_to_f32(out).astype(np.float64), q), "Q_A(r)/gs_a not exact in BF16"
+    return out, gs_r
+
+
 def fake_quant(w):
     """QDQ_W of QUADS §3.2 Eq. 12: returns (w_hat bf16 bits [M,K], gs)."""
     w = _c(w, np.uint16)

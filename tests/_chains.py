@@ -58,13 +58,16 @@ def trainer(x_u16, logits, w13, wd, topk, fake, sym=False):
     return _combine(yd, dst, rw)
 
 
-def rollout(x_u16, logits, w13, wd, topk, S13=None, Sd=None):
-    """W4A4 rollout forward, with the RAC residual on S13 / Sd when given -> out [T, H]."""
+def rollout(x_u16, logits, w13, wd, topk, S13=None, Sd=None, fp4_resid=False):
+    """W4A4 rollout forward, with the RAC residual on S13 / Sd when given (BF16,
+    or with fp4_resid the literal Eq. 21 second NVFP4 pass) -> out [T, H]."""
     E, N13, H = w13.shape
     I = N13 // 2
     ids, rw, counts, offs, dst = route(logits, E, topk)
     R = int(offs[-1])
     ca, sa, ra, ga = oracle.quantize(x_u16, S=S13)
+    if fp4_resid and S13 is not None:
+        ra, _ = oracle.requant_residual(ra, ga)
     xq = oracle.dequantize_exact(ca, sa, ga)
     h = np.zeros((R, I))
     for e in range(E):
@@ -77,6 +80,8 @@ def rollout(x_u16, logits, w13, wd, topk, S13=None, Sd=None):
             h[rows] = oracle.swiglu(y, I)
     hu = oracle.bf16_round(h.astype(np.float32))
     ch, sh, rh, gh = oracle.quantize(hu, S=Sd)
+    if fp4_resid and Sd is not None:
+        rh, _ = oracle.requant_residual(rh, gh)
     hq = oracle.dequantize_exact(ch, sh, gh)
     yd = np.zeros((R, H))
     for e in range(E):
