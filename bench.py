@@ -384,14 +384,27 @@ def mismatch_measure(layer, x, logits, w13, wd):
     T = x.shape[0]
     xe = synth.engine_drift(x.cpu(), 2.0 ** -10, 1).to(x.device)
     outs = {"w4a4_rac": layer.forward(x, logits).clone(), "w4a4_rac@eta": layer.forward(xe, logits).clone()}
+    step_ms = {}
     for name, mk, drift in [("w4a4", lambda: nv.RolloutMoE(w13, wd, None, None, layer.topk, T), True),
                             ("w16a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=False), True),
                             ("w4a16", lambda: nv.QatMoE(w13, wd, layer.topk, T, fake=True), False),
                             ("w4a4_sym", lambda: nv.QatMoE(w13, wd, layer.topk, T, sym=True), False),
                             ("w4a4_rac_fp4", lambda: nv.RolloutMoE(w13, wd, layer.S13, layer.Sd, layer.topk, T,
-                                                                   resid_fp4=True), False)]:
+                                                                   resid_fp4=True), False),
+                            ("w4a4_rac_online", lambda: nv.RolloutMoE(w13, wd, layer.S13, layer.Sd, layer.topk, T,
+                                                                      online=True), False)]:
         lay = mk()
         outs[name] = lay.forward(x, logits).clone()
+        if name in ("w4a4_rac_fp4", "w4a4_rac_online"):  # the variant's step time, inputs resident
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            for _ in range(3):
+                lay.forward(x, logits)
+            ev[0].record()
+            for _ in range(10):
+                lay.forward(x, logits)
+            ev[1].record()
+            torch.cuda.synchronize()
+            step_ms[name] = round(ev[0].elapsed_time(ev[1]) / 10, 4)
         if drift:
             outs[name + "@eta"] = lay.forward(xe, logits).clone()
         torch.cuda.synchronize()
@@ -404,13 +417,16 @@ def mismatch_measure(layer, x, logits, w13, wd):
         return round(d / n, 6)
 
     res = {"no_qat": rel("w4a4", "w16a16"), "qat": rel("w4a4", "w4a16"), "qat_rac": rel("w4a4_rac", "w4a16"),
-           "qat_rac_fp4": rel("w4a4_rac_fp4", "w4a16"),
+           "qat_rac_fp4": rel("w4a4_rac_fp4", "w4a16"), "qat_rac_online": rel("w4a4_rac_online", "w4a16"),
+           "variant_ms_per_step": {"rac_fp4_residual": step_ms["w4a4_rac_fp4"],
+                                   "rac_online_selection": step_ms["w4a4_rac_online"]},
            "sym_qat": rel("w4a4", "w4a4_sym"),
            "eta": {"rel": 2.0 ** -10, "bf16": rel("w16a16@eta", "w16a16"), "no_qat": rel("w4a4@eta", "w16a16"),
                    "qat": rel("w4a4@eta", "w4a16"), "qat_rac": rel("w4a4_rac@eta", "w4a16"),
                    "sym_qat": rel("w4a4@eta", "w4a4_sym")}}
     res["what"] = ("||Y_infer - Y_train|| / ||Y_train||: W4A4 vs BF16, W4A4 vs W4A16 QAT, W4A4+RAC vs W4A16 "
-                   "QAT (BF16 residual; FP4 residual of the literal Eq. 21), W4A4 vs symmetric W4A4 QAT; eta: "
+                   "QAT (BF16 residual; FP4 residual of the literal Eq. 21; channels chosen online per forward, Eq. 23-24), "
+                   "W4A4 vs symmetric W4A4 QAT; eta: "
                    "the rollout's input drifted (bf16: the drift alone)")
     return res
 

@@ -207,6 +207,35 @@ int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, const float *
 int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t k, const int32_t *offsets, int32_t E,
                                float *amax_ws, float *gs_out, int32_t *dev_status, void *stream);
 
+/* Online channel selection, QUADS §3.3 Eq. 23-24 applied to the batch at hand
+ * on every forward pass (the paper's own mode; nvfp4_rac_select_channels is
+ * the calibration form).  Same score and rule -- score_j^2 = sum over rows of
+ * (Q_A(X)[i,j] - X[i,j])^2, S = the k largest, ties to the lower index, in
+ * increasing order -- over the rows [0, offsets[E]) of a routed activation
+ * (all rows_cap rows when offsets is NULL).  The sums are taken in a fixed
+ * order built for speed (compensated binary32 per lane, binary64 across
+ * lanes and row chunks): deterministic, within a few binary32 ulp of the
+ * exact sums, so channels whose scores tie that closely may be chosen either
+ * way.
+ *   x          device BF16 [rows_cap, K]
+ *   amax       device float: the activation's amax (nvfp4_amax, or a GEMM's amax_out)
+ *   S_out      device int32[k]
+ *   score_ws   device double[257 * K]: squared scores in [0, K), then scratch.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 16, K > 16384, k > K). */
+int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K, const int32_t *offsets, int32_t E,
+                                     const float *amax, int32_t k, int32_t *S_out, double *score_ws, void *stream);
+
+/* The selected weight columns of a rollout weight pack, for a new channel set:
+ * w_sel[e, n, s] = bf16(code * sb) of element (n, S[s]) of expert e -- what
+ * nvfp4_prepare_weights writes for S -- read from its packed codes and tiled
+ * scales (rows in the pack's own order, interleaved or not).
+ *   w_codes, w_scales   from nvfp4_prepare_weights (E experts, N x K)
+ *   S                   device int32[k], entries in [0, K) (others are clamped)
+ *   w_sel               device BF16 [E, N, k]
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, k % 8). */
+int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N, int64_t K,
+                                  const int32_t *S, int32_t k, void *w_sel, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Grouped GEMMs (QUADS §3.3 Eq. 21; §3.2 Eq. 12)                            */
 /* ------------------------------------------------------------------------ */

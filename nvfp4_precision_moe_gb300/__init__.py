@@ -35,6 +35,8 @@ _SIGS = {
     "nvfp4_prepare_weights": "piqqpiippppppp",
     "nvfp4_rac_select_channels": "pqqpippp",
     "nvfp4_rac_requant_residual": "pqipipppp",
+    "nvfp4_rac_select_channels_online": "pqqpipippp",
+    "nvfp4_gather_selected_weights": "ppiqqpipp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
     "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
     "nvfp4_gemm_pipeline": "ip",
@@ -148,6 +150,20 @@ def nvfp4_rac_requant_residual(resid, amax_ws, offsets=None, E=0, gs_out=None, d
     rows_cap, k = resid.shape
     _call("nvfp4_rac_requant_residual", _p(resid), rows_cap, k, _p(offsets), E, _p(amax_ws), _p(gs_out),
           _p(dev_status), _s(stream))
+
+
+def nvfp4_rac_select_channels_online(x, amax, k, S_out, score_ws, offsets=None, E=0, stream=None):
+    """Eq. 23-24 on the batch at hand (rows [0, offsets[E]) of x when offsets is
+    given); score_ws: device float64[257 * K]."""
+    rows_cap, K = x.shape
+    _call("nvfp4_rac_select_channels_online", _p(x), rows_cap, K, _p(offsets), E, _p(amax), k, _p(S_out),
+          _p(score_ws), _s(stream))
+
+
+def nvfp4_gather_selected_weights(w_codes, w_scales, E, N, K, S, w_sel, stream=None):
+    """w_sel [E, N, k] of a weight pack for the channel set S."""
+    _call("nvfp4_gather_selected_weights", _p(w_codes), _p(w_scales), E, N, K, _p(S), S.numel(), _p(w_sel),
+          _s(stream))
 
 
 def nvfp4_prepare_weights(w, w_codes, w_scales, gs_w, amax_ws, S=None, w_sel=None, interleave=0,

@@ -505,39 +505,94 @@ __global__ void __launch_bounds__(32 * kScoreWarps) channel_score_kernel(const u
 }
 
 // Eq. 24: keep the k largest (ties to the lower index), write them in order.
-// Non-negative doubles order like their bit patterns.
+// Non-negative doubles order like their bit patterns.  Radix selection: the
+// k-th largest key T is found 8 bits at a time with shared-memory histograms
+// of the keys that share the bits found so far; then every channel with a key
+// above T, and the first (k - #above) channels with key T in channel order,
+// are written in channel order.
 __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, int64_t K, int32_t k, int32_t *S) {
-    __shared__ int32_t warp_sums[32];
-    __shared__ int32_t carry;
-    if (threadIdx.x == 0) carry = 0;
-    __syncthreads();
-    const long long *bits = reinterpret_cast<const long long *>(ssq);
-    for (int64_t j0 = 0; j0 < K; j0 += blockDim.x) {
-        int64_t j = j0 + threadIdx.x;
-        int flag = 0;
-        if (j < K) {
-            long long sj = bits[j];
-            int64_t rank = 0;
-            for (int64_t i = 0; i < K && rank < k; ++i) {
-                long long si = bits[i];
-                rank += (si > sj) || (si == sj && i < j);
-            }
-            flag = rank < k;
-        }
-        // block-wide exclusive scan of flags, in channel order
-        unsigned ballot = __ballot_sync(0xffffffffu, flag);
-        int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-        int pre = __popc(ballot & ((1u << lane) - 1u));
-        if (lane == 0) warp_sums[wid] = __popc(ballot);
+    __shared__ uint32_t hist[256];
+    __shared__ int32_t warp_a[32], warp_b[32];
+    __shared__ unsigned long long s_prefix;
+    __shared__ int32_t s_need, carry_eq, carry_out;
+    const unsigned long long *key = reinterpret_cast<const unsigned long long *>(ssq);
+    if (threadIdx.x == 0) {
+        s_prefix = 0ull;
+        s_need = k;  // rank of T among the keys that share the prefix, counted from the top
+        carry_eq = 0;
+        carry_out = 0;
+    }
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
+    for (int shift = 56; shift >= 0; shift -= 8) {
+        for (int b = threadIdx.x; b < 256; b += blockDim.x) hist[b] = 0u;
         __syncthreads();
-        int wpre = 0;
-        for (int w = 0; w < wid; ++w) wpre += warp_sums[w];
-        if (flag) S[carry + wpre + pre] = (int32_t)j;
+        const unsigned long long hi = shift == 56 ? 0ull : (~0ull << (shift + 8));
+        const unsigned long long prefix = s_prefix;
+        // warp-aggregated counts: the keys of a warp that fall in one bucket add once
+        for (int64_t j0 = 0; j0 < K; j0 += blockDim.x) {
+            const int64_t j = j0 + threadIdx.x;
+            const unsigned long long v = j < K ? key[j] : 0ull;
+            const bool act = j < K && (v & hi) == prefix;
+            const uint32_t bucket = act ? (uint32_t)((v >> shift) & 255u) : 256u + (uint32_t)lane;
+            const unsigned peers = __match_any_sync(0xffffffffu, bucket);
+            if (act && lane == __ffs(peers) - 1) atomicAdd(&hist[bucket], (uint32_t)__popc(peers));
+        }
+        __syncthreads();
+        if (wid == 0) {
+            // lane l holds buckets 255-8l down to 248-8l; find the bucket of rank s_need from the top
+            uint32_t h[8], tot = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                h[i] = hist[255 - 8 * lane - i];
+                tot += h[i];
+            }
+            uint32_t incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const int32_t need = s_need;
+            const unsigned hit = __ballot_sync(0xffffffffu, (int32_t)incl >= need);
+            if (lane == __ffs(hit) - 1) {
+                int32_t cum = (int32_t)(incl - tot);
+                for (int i = 0; i < 8; ++i) {
+                    if (cum + (int32_t)h[i] >= need) {
+                        s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - i) << shift);
+                        s_need = need - cum;
+                        break;
+                    }
+                    cum += (int32_t)h[i];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    const unsigned long long T = s_prefix;
+    const int32_t need_eq = s_need;  // keys equal to T to keep, lowest channels first
+    for (int64_t j0 = 0; j0 < K; j0 += blockDim.x) {
+        const int64_t j = j0 + threadIdx.x;
+        const unsigned long long v = j < K ? key[j] : 0ull;
+        const int eq = j < K && v == T;
+        // rank of this channel among the equal keys, in channel order
+        const unsigned be = __ballot_sync(0xffffffffu, eq);
+        if (lane == 0) warp_a[wid] = __popc(be);
+        __syncthreads();
+        int pre_eq = carry_eq + __popc(be & ((1u << lane) - 1u));
+        for (int w = 0; w < wid; ++w) pre_eq += warp_a[w];
+        const int flag = j < K && (v > T || (eq && pre_eq < need_eq));
+        const unsigned bf = __ballot_sync(0xffffffffu, flag);
+        if (lane == 0) warp_b[wid] = __popc(bf);
+        __syncthreads();
+        int pos = carry_out + __popc(bf & ((1u << lane) - 1u));
+        for (int w = 0; w < wid; ++w) pos += warp_b[w];
+        if (flag) S[pos] = (int32_t)j;
         __syncthreads();
         if (threadIdx.x == 0) {
-            int tot = 0;
-            for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += warp_sums[w];
-            carry += tot;
+            for (int w = 0; w < nw; ++w) {
+                carry_eq += warp_a[w];
+                carry_out += warp_b[w];
+            }
         }
         __syncthreads();
     }
@@ -613,6 +668,150 @@ __global__ void __launch_bounds__(256) resid_qdq_kernel(uint16_t *resid, int64_t
         }
         p[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
         p[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
+// ---- online per-forward channel selection (QUADS §3.3 Eq. 23-24 on the
+// batch at hand).  Scores of the rows [0, offsets[E]) (all rows_cap rows when
+// offsets is null): a (row chunk, 512-column segment) per block, one 16-element
+// block per lane as the quantizer sees it, 8 warps striding over the chunk's
+// rows.  The squared error of an element, (code*sb*gs - x)^2, is exact in
+// binary32 (both terms have few significant bits and lie within a factor of a
+// block scale of each other); a lane keeps compensated binary32 sums of its 16
+// channels, the warps' sums are added in binary64 in warp order, and the
+// chunks' in chunk order -- deterministic, within a few ulp of binary32 of the
+// exact sums.
+constexpr int kOnlineChunks = 256;  // at most; about 512 rows of the buffer per chunk
+static_assert(kOnlineChunks % 16 == 0, "the finishing sum loads 16 chunks at a time");
+static int64_t online_chunks(int64_t rows_cap) {
+    int64_t c = (rows_cap / 512 + 15) / 16 * 16;
+    return c < 16 ? 16 : (c > kOnlineChunks ? kOnlineChunks : c);
+}
+
+__global__ void __launch_bounds__(256) online_score_kernel(const uint16_t *x, int64_t rows_cap, int64_t K,
+                                                          const int32_t *offsets, int32_t E, const float *amax,
+                                                          double *part) {
+    const int64_t nchunks = gridDim.x;
+    __shared__ QTables tb;
+    __shared__ double red[8][512];
+    fill_tables(tb);
+    __syncthreads();
+    const float gs = tensor_scale(*amax);
+    const float p6 = __fmul_rn(gs, 6.0f);
+    const float inv_gs = __frcp_rn(gs);
+    const int64_t rows = resid_rows(rows_cap, offsets, E);
+    const int c = blockIdx.x, lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t r0 = rows * c / nchunks, r1 = rows * (c + 1) / nchunks;
+    const int64_t col = (int64_t)blockIdx.y * 512 + 16 * lane;  // this lane's block
+    const bool valid = col < K;
+    float sum[16], comp[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) sum[t] = comp[t] = 0.0f;
+    if (valid) {
+        // four rows' loads in flight per warp (rows r, r+8, r+16, r+24), added in row order
+        for (int64_t rb = r0 + w; rb < r1; rb += 32) {
+            uint4 raw[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t r = rb + 8 * u;
+                if (r < r1) {
+                    const uint4 *p = reinterpret_cast<const uint4 *>(x + r * K + col);
+                    raw[u][0] = __ldg(p);
+                    raw[u][1] = __ldg(p + 1);
+                } else {
+                    raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);  // adds exact zeros
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float v[16];
+                unpack_block(raw[u][0], raw[u][1], v);
+                BlockQ q;
+                quant_block(v, gs, p6, inv_gs, tb, q);
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    const float d = __fsub_rn(__fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs), v[t]);
+                    const float y = __fsub_rn(__fmul_rn(d, d), comp[t]);
+                    const float s2 = __fadd_rn(sum[t], y);
+                    comp[t] = __fsub_rn(__fsub_rn(s2, sum[t]), y);
+                    sum[t] = s2;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) red[w][16 * lane + t] = (double)sum[t] - (double)comp[t];
+    __syncthreads();
+    for (int i = threadIdx.x; i < 512; i += blockDim.x) {
+        const int64_t j = (int64_t)blockIdx.y * 512 + i;
+        if (j >= K) continue;
+        double acc = 0.0;
+        for (int ww = 0; ww < 8; ++ww) acc = __dadd_rn(acc, red[ww][i]);
+        part[(int64_t)c * K + j] = acc;
+    }
+}
+
+__global__ void online_score_finish_kernel(const double *part, int64_t K, int nchunks, double *ssq) {
+    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (j >= K) return;
+    double acc = 0.0;
+    for (int c0 = 0; c0 < nchunks; c0 += 16) {  // nchunks % 16 == 0  // 16 loads in flight, added in chunk order
+        double v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) v[u] = __ldg(part + (int64_t)(c0 + u) * K + j);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) acc = __dadd_rn(acc, v[u]);
+    }
+    ssq[j] = acc;
+}
+
+// W_sel[e, n, s] = bf16(code * sb) of packed weight element (n, S[s]) of
+// expert e -- the unscaled dequantized value nvfp4_prepare_weights stores for
+// the channels S -- gathered for a new S.  One warp per weight row: the row's
+// packed codes and its block scales are read once, coalesced, into shared
+// memory; the lanes then emit the row's k outputs two at a time.
+constexpr int kGatherWarps = 8;
+
+__host__ __device__ constexpr int64_t gather_row_bytes(int64_t K) { return K / 2 + (((K / 16) + 15) / 16) * 16; }
+__host__ __device__ constexpr int64_t gather_s_bytes(int32_t k) { return (((int64_t)k * 4) + 15) / 16 * 16; }
+
+__global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_kernel(const uint8_t *codes, const uint8_t *scales,
+                                                                      int64_t E, int64_t N, int64_t K,
+                                                                      const int32_t *S, int32_t k, uint16_t *wsel) {
+    extern __shared__ __align__(16) uint8_t gsm[];
+    int32_t *sS = reinterpret_cast<int32_t *>(gsm);
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint8_t *rowc = gsm + gather_s_bytes(k) + w * gather_row_bytes(K);  // codes, then scales
+    uint8_t *rows_ = rowc + K / 2;
+    for (int i = threadIdx.x; i < k; i += blockDim.x) sS[i] = min(max(S[i], 0), (int32_t)(K - 1));  // S within [0, K)
+    __syncthreads();
+    const int64_t nb = K >> 4, kslices = (nb + 15) >> 4;
+    for (int64_t row = (int64_t)blockIdx.x * kGatherWarps + w; row < E * N; row += (int64_t)gridDim.x * kGatherWarps) {
+        const int64_t e = row / N, n = row - e * N;
+        const uint4 *src = reinterpret_cast<const uint4 *>(codes + row * (K >> 1));
+        for (int64_t i = lane; i < (K >> 5); i += 32) reinterpret_cast<uint4 *>(rowc)[i] = __ldg(src + i);
+        // the row's block scales: a 16-byte run per 256-element K-slice of the tiled layout
+        const uint8_t *sten = scales + e * N * nb;  // an expert's scales
+        for (int64_t t = lane; t < kslices; t += 32) {
+            const uint8_t *run = sten + ((n >> 7) * kslices + t) * 2048 + (n & 127) * 16;
+            const int64_t cnt = nb - 16 * t < 16 ? nb - 16 * t : 16;
+            if (cnt == 16) *reinterpret_cast<uint4 *>(rows_ + 16 * t) = __ldg(reinterpret_cast<const uint4 *>(run));
+            else
+                for (int64_t b = 0; b < cnt; ++b) rows_[16 * t + b] = run[b];
+        }
+        __syncwarp();
+        uint32_t *dst = reinterpret_cast<uint32_t *>(wsel + row * k);
+        for (int s2 = 2 * lane; s2 < k; s2 += 64) {
+            uint32_t h[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int j = sS[s2 + u];
+                const uint32_t c = (rowc[j >> 1] >> (4 * (j & 1))) & 15u;
+                h[u] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(e2m1_val(c), e4m3_to_f32(rows_[j >> 4]))));
+            }
+            dst[s2 >> 1] = h[0] | (h[1] << 16);
+        }
+        __syncwarp();
     }
 }
 
@@ -775,6 +974,55 @@ extern "C" int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t
     resid_qdq_kernel<<<(unsigned)blocks, 256, 0, st>>>((uint16_t *)resid, rows_cap, k, offsets, E, amax_ws, gs_out,
                                                       dev_status);
     return launch_status("resid_qdq_kernel");
+}
+
+extern "C" int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K, const int32_t *offsets,
+                                                int32_t E, const float *amax, int32_t k, int32_t *S_out,
+                                                double *score_ws, void *stream) {
+    if (!x || !amax || !score_ws || rows_cap < 0 || K < 0 || k < 0 || (offsets && E < 1))
+        return NVFP4_ERR_INVALID_ARG;
+    if (k > 0 && !S_out) return NVFP4_ERR_INVALID_ARG;
+    if (K % 16 || K > 16384 || k > K) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(score_ws)) return NVFP4_ERR_ALIGNMENT;
+    if (K == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    double *part = score_ws + K;  // [kOnlineChunks][K]
+    const int nchunks = (int)online_chunks(rows_cap);
+    online_score_kernel<<<dim3((unsigned)nchunks, (unsigned)((K + 511) / 512)), 256, 0, st>>>(
+        (const uint16_t *)x, rows_cap, K, offsets, E, amax, part);
+    int s = launch_status("online_score_kernel");
+    if (s != NVFP4_OK) return s;
+    online_score_finish_kernel<<<(unsigned)((K + 63) / 64), 64, 0, st>>>(part, K, nchunks, score_ws);
+    s = launch_status("online_score_finish_kernel");
+    if (s != NVFP4_OK || k == 0) return s;
+    select_topk_kernel<<<1, 1024, 0, st>>>(score_ws, K, k, S_out);
+    return launch_status("select_topk_kernel");
+}
+
+extern "C" int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N,
+                                             int64_t K, const int32_t *S, int32_t k, void *w_sel, void *stream) {
+    if (!w_codes || !w_scales || !S || !w_sel || E < 1 || N < 0 || K < 0 || k < 1 || k > K)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 || N % 128 || k % 8 || K / 16 > kMaxBlocksPerRow) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(w_sel) || !aligned16(w_codes) || !aligned16(w_scales)) return NVFP4_ERR_ALIGNMENT;
+    if (N == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    const int64_t smem = gather_s_bytes(k) + kGatherWarps * gather_row_bytes(K);
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(gather_wsel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) {
+            set_last_error("cudaFuncSetAttribute(gather_wsel_kernel)", e);
+            return NVFP4_ERR_CUDA;
+        }
+    }
+    int64_t blocks = ((int64_t)E * N + kGatherWarps - 1) / kGatherWarps;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    gather_wsel_kernel<<<(unsigned)blocks, 32 * kGatherWarps, (size_t)smem, (cudaStream_t)stream>>>(
+        w_codes, w_scales, E, N, K, S, k, (uint16_t *)w_sel);
+    return launch_status("gather_wsel_kernel");
 }
 
 extern "C" int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,

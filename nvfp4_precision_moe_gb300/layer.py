@@ -18,7 +18,8 @@ import torch
 from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16, NVFP4_OUT_F32,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
-               nvfp4_rac_requant_residual, nvfp4_route_topk, nvfp4_w4a4_rac_grouped_gemm)
+               nvfp4_gather_selected_weights, nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online,
+               nvfp4_route_topk, nvfp4_w4a4_rac_grouped_gemm)
 
 
 def scale_bytes(rows, K):
@@ -78,9 +79,16 @@ class RolloutMoE:
     the device; may be None for plain W4A4); max_tokens: buffer capacity.
     resid_fp4: the literal second-pass form of QUADS §3.3 Eq. 21, the residual
     itself NVFP4-quantized (nvfp4_rac_requant_residual) before the GEMMs.
+    online: choose S13 / S_down on every forward from the batch at hand (Eq.
+    23-24, the paper's own mode): the given sets only fix k and the first
+    weight pack; the layer keeps its own copies, readable after a forward.
     """
 
-    def __init__(self, w13, w_down, S13, S_down, topk, max_tokens, out_dtype=torch.float32, resid_fp4=False):
+    def __init__(self, w13, w_down, S13, S_down, topk, max_tokens, out_dtype=torch.float32, resid_fp4=False,
+                 online=False):
+        if online:
+            S13 = S13.clone() if S13 is not None else None
+            S_down = S_down.clone() if S_down is not None else None
         self.E, N13, self.H = w13.shape
         self.I = N13 // 2
         self.topk = topk
@@ -106,7 +114,11 @@ class RolloutMoE:
         # number of library kernels one forward launches: routing 2, amax, quantize x,
         # clear padding, gate_up GEMM, quantize h, down GEMM, combine (+2 per
         # second-pass residual)
-        self.LAUNCHES = 9 + (2 * (self.k13 > 0) + 2 * (self.kd > 0) if resid_fp4 else 0)
+        self.online = online
+        if online:
+            self.score_ws = torch.empty(257 * max(self.H, self.I), dtype=torch.float64, device=dev)
+        self.LAUNCHES = 9 + (2 * (self.k13 > 0) + 2 * (self.kd > 0) if resid_fp4 else 0) + \
+            (4 * (self.k13 > 0) + 4 * (self.kd > 0) if online else 0)
 
     LAUNCHES = 9
 
@@ -128,6 +140,10 @@ class RolloutMoE:
         xa, ha = self.xa, self.ha
         mark(1)
         nvfp4_amax(x, xa.amax, stream=stream)
+        if self.online and self.k13:  # Eq. 23-24 on this batch, and the weight columns it picks
+            nvfp4_rac_select_channels_online(x, xa.amax, self.k13, self.S13, self.score_ws, stream=stream)
+            W = self.w13
+            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.S13, W.sel, stream=stream)
         mark(2)
         nvfp4_quantize(x, xa.amax, xa.codes, xa.scales, resid=xa.resid if self.k13 else None,
                        S=self.S13 if self.k13 else None, gs_out=xa.gs, dst_row=dst,
@@ -145,6 +161,11 @@ class RolloutMoE:
                                     epilogue=NVFP4_EPI_SWIGLU, out_dtype=NVFP4_OUT_BF16,
                                     amax_out=ha.amax, dev_status=self.dev_status, stream=stream)
         mark(4)
+        if self.online and self.kd:  # the routed rows of h only: rows past offsets[E] may be stale
+            nvfp4_rac_select_channels_online(self.h, ha.amax, self.kd, self.Sd, self.score_ws, offsets=r.offsets,
+                                             E=self.E, stream=stream)
+            W = self.wd
+            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.Sd, W.sel, stream=stream)
         nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
                        S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
                        stream=stream)

@@ -102,3 +102,50 @@ def inputs(cfg, T):
     w13 = torch.stack([synth.expert_weight(cfg, e, "w13") for e in range(c["E"])])
     wd = torch.stack([synth.expert_weight(cfg, e, "down") for e in range(c["E"])])
     return c, x, logits, w13, wd
+
+
+def valid_topk(S, scores, k, rel=1e-6):
+    """S is a top-k of `scores` (ties within `rel` either way), sorted, distinct."""
+    S = np.asarray(S)
+    if len(S) != k or np.any(np.diff(S) <= 0):
+        return False
+    t = np.sort(scores)[::-1][k - 1]
+    sel = np.zeros(len(scores), bool)
+    sel[S] = True
+    return bool(np.all(scores[sel] >= t * (1 - rel)) and np.all(scores[~sel] <= t * (1 + rel)))
+
+
+def rollout_online(x_u16, logits, w13, wd, topk, k13, kd, S13=None, Sd=None):
+    """W4A4 + RAC rollout forward with Eq. 23-24 applied to this batch: S13 from
+    the scores of x, Sd from the scores of the routed rows of h (padding rows
+    included: they are zero).  S13 / Sd, when given (e.g. the library's own
+    choice), replace the oracle's choice downstream; the oracle's scores are
+    returned either way -> (out, S13, Sd, scores13, scoresd)."""
+    E, N13, H = w13.shape
+    I = N13 // 2
+    sc13 = oracle.channel_scores_sq(x_u16)
+    S13 = oracle.select_channels(sc13, k13) if S13 is None else np.asarray(S13, np.int32)
+    ids, rw, counts, offs, dst = route(logits, E, topk)
+    R = int(offs[-1])
+    ca, sa, ra, ga = oracle.quantize(x_u16, S=S13)
+    xq = oracle.dequantize_exact(ca, sa, ga)
+    h = np.zeros((R, I))
+    for e in range(E):
+        toks = np.nonzero((ids == e).any(1))[0]
+        if toks.size:
+            cw, sw, _, gw = oracle.quantize(synth.u16(w13[e]))
+            y = oracle.rac_gemm(xq[toks], oracle.dequantize_exact(cw, sw, gw), ra[toks], S13, ga)
+            rows = dst[toks, np.argmax(ids[toks] == e, 1)]
+            h[rows] = oracle.swiglu(y, I)
+    hu = oracle.bf16_round(h.astype(np.float32))
+    scd = oracle.channel_scores_sq(hu)
+    Sd = oracle.select_channels(scd, kd) if Sd is None else np.asarray(Sd, np.int32)
+    ch, sh, rh, gh = oracle.quantize(hu, S=Sd)
+    hq = oracle.dequantize_exact(ch, sh, gh)
+    yd = np.zeros((R, H))
+    for e in range(E):
+        r0, r1 = offs[e], offs[e] + counts[e]
+        if r1 > r0:
+            cw, sw, _, gw = oracle.quantize(synth.u16(wd[e]))
+            yd[r0:r1] = oracle.rac_gemm(hq[r0:r1], oracle.dequantize_exact(cw, sw, gw), rh[r0:r1], Sd, gh)
+    return _combine(yd, dst, rw), S13, Sd, sc13, scd

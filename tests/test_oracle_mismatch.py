@@ -63,3 +63,17 @@ def test_symmetric_qat_aligns_only_without_engine_drift():
                            - _chains.trainer(xu, l, w13, wd, 2, fake=False))
     d_sym = np.linalg.norm(_chains.rollout(xe, l, w13, wd, 2) - y_sym)
     assert d_sym > 5 * d_eta > 0
+
+
+def test_online_selection_chain():
+    """The oracle's online chain (Eq. 23-24 on this batch, for x and for h)
+    picks the outlier channels of x and lowers the mismatch below plain W4A4."""
+    x, logits, w13, wd = small_moe()
+    xu, l = synth.u16(x), logits.numpy()
+    out, S13, Sd, sc13, scd = _chains.rollout_online(xu, l, w13, wd, 2, 32, 16)
+    assert _chains.valid_topk(S13, sc13, 32, rel=0) and _chains.valid_topk(Sd, scd, 16, rel=0)
+    # the 4 scaled outlier channels of small_moe carry the largest errors
+    big = np.argsort(np.abs(oracle.bf16_to_f32(xu)).max(0))[::-1][:4]
+    assert set(big.tolist()) <= set(S13.tolist())
+    y_qat = _chains.trainer(xu, l, w13, wd, 2, fake=True)
+    assert np.linalg.norm(out - y_qat) < np.linalg.norm(_chains.rollout(xu, l, w13, wd, 2) - y_qat)
