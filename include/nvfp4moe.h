@@ -343,6 +343,63 @@ int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t
                       void *stream);
 
 /* ------------------------------------------------------------------------ */
+/* Trainer backward (QUADS §3.2 Eq. 13: straight-through estimator)           */
+/* ------------------------------------------------------------------------ */
+/* The asymmetric-QAT learner treats the weight fake-quantizer as the identity
+ * in the backward pass: dW = dW_hat and dX = W_hat^T dY (Eq. 13).  For one MoE
+ * layer out = combine(swiglu(scatter(x) W13_hat^T) Wd_hat^T) the backward is
+ * combine backward -> dY routed; dh = dY Wd_hat; dWd = dY^T h; SwiGLU backward
+ * -> d(gate|up); dx_routed = d(gate|up) W13_hat; dW13 = d(gate|up)^T x_routed;
+ * dx = the sum of each token's routed rows (nvfp4_moe_combine with unit
+ * weights).  The input-gradient products run on nvfp4_bf16_grouped_gemm with
+ * transposed weights (nvfp4_transpose_bf16), the weight gradients on
+ * nvfp4_bf16_grouped_gemm_wgrad. */
+
+/* y[b] = x[b]^T for `batch` row-major BF16 matrices of rows x cols (y[b] is
+ * cols x rows).  x and y may not overlap.  Errors: INVALID_ARG, UNSUPPORTED
+ * (batch > 65535). */
+int nvfp4_transpose_bf16(const void *x, int32_t batch, int64_t rows, int64_t cols, void *y, void *stream);
+
+/* h = bf16(silu(g) * u) from saved BF16 pre-activations gu = [g | u]
+ * (rows x 2I, the gate columns first), silu(g) = g / (1 + exp(-g)) in
+ * binary32.  h: device BF16 [rows, I].  Errors: INVALID_ARG. */
+int nvfp4_swiglu(const void *gu, int64_t rows, int64_t I, void *h, void *stream);
+
+/* SwiGLU backward: from gu = [g | u] and dh (rows x I, BF16),
+ * d(gate) = bf16(dh * u * s (1 + g (1 - s))) and d(up) = bf16(dh * g * s),
+ * s = 1 / (1 + exp(-g)), in binary32, written as dgu = [dg | du] (rows x 2I).
+ * Errors: INVALID_ARG. */
+int nvfp4_swiglu_backward(const void *gu, const void *dh, int64_t rows, int64_t I, void *dgu, void *stream);
+
+/* Backward of nvfp4_moe_combine: dy[dst_row[t,s]] = bf16(weights[t,s] *
+ * dout[t]) for every token t and slot s (rows outside [0, rows_cap) are
+ * skipped), the padding rows [offsets[e] + counts[e], offsets[e+1]) of dy set
+ * to zero, and, when dweights is not NULL, the combine weights' gradient
+ * dweights[t,s] = sum_h y[dst_row[t,s], h] * dout[t, h] (binary32).
+ *   dout      device float [T, H];  y  device BF16 [rows_cap, H] (the forward's rows)
+ *   dy        device BF16 [rows_cap, H];  dweights  device float [T, topk] or NULL
+ * Errors: INVALID_ARG, UNSUPPORTED (E > 65535). */
+int nvfp4_moe_combine_backward(const float *dout, const void *y, const int32_t *dst_row, const float *weights,
+                               int32_t T, int32_t topk, int64_t H, const int32_t *counts, const int32_t *offsets,
+                               int32_t E, int64_t rows_cap, void *dy, float *dweights, void *stream);
+
+/* Grouped weight gradient: dw[e] = a_t[:, seg e] . b_t[:, seg e]^T for every
+ * expert e, seg e = the routed rows [offsets[e], offsets[e+1]) (tcgen05 BF16
+ * MMA, FP32 accumulation over the expert's rows; an expert without rows gets
+ * zeros).  The operands are the transposed routed tensors, so the reduction
+ * axis is contiguous:
+ *   a_t      device BF16 [M, R] (e.g. dY^T of a projection's output)
+ *   b_t      device BF16 [N, R] (e.g. its input, transposed)
+ *   offsets  device int32[E+1] as for nvfp4_bf16_grouped_gemm, offsets[E] <= R
+ *   dw       device [E, M, N], F32 or BF16 (out_dtype)
+ * Runs on the single-CTA pipeline whatever nvfp4_gemm_pipeline selects.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (M % 128, N % 256, R % 128,
+ * E > 1024); dev_status gets TIMEOUT if a pipeline wait runs out. */
+int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_t *offsets, int32_t E, int64_t R,
+                                  int64_t M, int64_t N, int32_t out_dtype, void *dw, int32_t *dev_status,
+                                  void *stream);
+
+/* ------------------------------------------------------------------------ */
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------ */
 

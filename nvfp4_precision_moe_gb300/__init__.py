@@ -37,6 +37,11 @@ _SIGS = {
     "nvfp4_rac_requant_residual": "pqipipppp",
     "nvfp4_rac_select_channels_online": "pqqpipippp",
     "nvfp4_gather_selected_weights": "ppiqqpipp",
+    "nvfp4_transpose_bf16": "piqqpp",
+    "nvfp4_swiglu": "pqqpp",
+    "nvfp4_swiglu_backward": "ppqqpp",
+    "nvfp4_moe_combine_backward": "ppppiiqppiqppp",
+    "nvfp4_bf16_grouped_gemm_wgrad": "pppiqqqippp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
     "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
     "nvfp4_gemm_pipeline": "ip",
@@ -199,6 +204,39 @@ def nvfp4_bf16_grouped_gemm(x, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F
     rows_cap = x.shape[0]
     _call("nvfp4_bf16_grouped_gemm", _p(x), _p(w_hat), _p(offsets), E, rows_cap, N, K, out_dtype,
           epilogue, _p(y), y.stride(0), _p(dev_status), _s(stream))
+
+
+def nvfp4_transpose_bf16(x, y, stream=None):
+    """y[b] = x[b]^T for BF16 x [batch, rows, cols] (or [rows, cols])."""
+    b, r, c = (1, *x.shape) if x.dim() == 2 else x.shape
+    _call("nvfp4_transpose_bf16", _p(x), b, r, c, _p(y), _s(stream))
+
+
+def nvfp4_swiglu(gu, h, stream=None):
+    """h = bf16(silu(g) * u), gu = [g | u] BF16 [rows, 2I]."""
+    rows, n2 = gu.shape
+    _call("nvfp4_swiglu", _p(gu), rows, n2 // 2, _p(h), _s(stream))
+
+
+def nvfp4_swiglu_backward(gu, dh, dgu, stream=None):
+    """dgu = [dg | du] from gu = [g | u] and dh."""
+    rows, n2 = gu.shape
+    _call("nvfp4_swiglu_backward", _p(gu), _p(dh), rows, n2 // 2, _p(dgu), _s(stream))
+
+
+def nvfp4_moe_combine_backward(dout, y, dst_row, weights, counts, offsets, E, dy, dweights=None, stream=None):
+    """Routed gradient dy (BF16 [rows_cap, H]) and the combine weights' gradient."""
+    T, topk = dst_row.shape
+    _call("nvfp4_moe_combine_backward", _p(dout), _p(y), _p(dst_row), _p(weights), T, topk, dout.shape[1],
+          _p(counts), _p(offsets), E, dy.shape[0], _p(dy), _p(dweights), _s(stream))
+
+
+def nvfp4_bf16_grouped_gemm_wgrad(a_t, b_t, offsets, E, dw, out_dtype=NVFP4_OUT_F32, dev_status=None, stream=None):
+    """dw[e] = a_t[:, seg e] . b_t[:, seg e]^T; a_t [M, R], b_t [N, R] BF16, dw [E, M, N]."""
+    M, R = a_t.shape
+    N = b_t.shape[0]
+    _call("nvfp4_bf16_grouped_gemm_wgrad", _p(a_t), _p(b_t), _p(offsets), E, R, M, N, out_dtype, _p(dw),
+          _p(dev_status), _s(stream))
 
 
 def nvfp4_gemm_pipeline(which):

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libnvfp4moe.so")
-SOURCES = ["abi.cu", "quantize.cu", "moe.cu", "gemm.cu", "gemm_single.cu", "gemm_pair.cu"]
+SOURCES = ["abi.cu", "quantize.cu", "moe.cu", "gemm.cu", "gemm_single.cu", "gemm_pair.cu", "train.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE]
 

@@ -139,3 +139,47 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     return use_pair(false) ? launch_pair_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream)
                            : launch_single_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream);
 }
+
+extern "C" int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_t *offsets, int32_t E,
+                                             int64_t R, int64_t M, int64_t N, int32_t out_dtype, void *dw,
+                                             int32_t *dev_status, void *stream) {
+    if (!a_t || !b_t || !offsets || !dw || E < 1 || R < 0 || M < 0 || N < 0) return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (M % 128 || N % 256 || R % 128 || E > kMaxExperts || R > (1ll << 31) || (int64_t)E * M > (1ll << 31))
+        return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(a_t) || !aligned16(b_t) || !aligned16(dw)) return NVFP4_ERR_ALIGNMENT;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    if (R == 0) {  // no routed rows at all: every gradient is zero
+        const cudaError_t e = cudaMemsetAsync(dw, 0, (size_t)E * M * N * (out_dtype == NVFP4_OUT_F32 ? 4 : 2),
+                                              (cudaStream_t)stream);
+        if (e != cudaSuccess) {
+            set_last_error("cudaMemsetAsync(dw)", e);
+            return NVFP4_ERR_CUDA;
+        }
+        return NVFP4_OK;
+    }
+    CUtensorMap tA, tB;
+    int s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a_t, R, M, 2 * R, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == NVFP4_OK)
+        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)b_t, R, N, 2 * R, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != NVFP4_OK) return s;
+    GemmParams p{};
+    p.wgrad = 1;
+    p.M = M;
+    p.offsets = offsets;
+    p.rows_cap = (int32_t)R;
+    p.E = E;
+    p.N = N;
+    p.K = R;
+    p.epilogue = NVFP4_EPI_NONE;
+    p.out_dtype = out_dtype;
+    p.y = dw;
+    p.ldy = N;
+    p.vec32 = (reinterpret_cast<uintptr_t>(dw) % 32 == 0) && (N * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
+    p.dev_status = dev_status;
+    // the weight-gradient mode exists on the single-CTA pipeline only
+    return launch_single_gemm<false>(tA, tB, tA, tB, p, (int64_t)E * M, N, (cudaStream_t)stream);
+}

@@ -54,6 +54,10 @@ struct GemmParams {
     int32_t vec32;  // y and its row pitch are 32-byte aligned: whole-sector stores
     float *amax_out;
     int32_t *dev_status;
+    // weight-gradient mode (BF16, single-CTA pipeline): y[e] (M x N) = A[:, seg e] . B[:, seg e]^T,
+    // A [M, rows_cap] and B [N, rows_cap] K-major, seg e = [offsets[e], offsets[e+1])
+    int32_t wgrad;
+    int64_t M;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

@@ -47,6 +47,27 @@ struct Cfg {
 };
 static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory budget");
 
+// A tile of the weight-gradient mode: expert e, output tile (mt, nt), and the
+// expert's routed rows [k0, k0 + 64 nk) as the reduction range.
+struct WTile {
+    int e, mt, nt;
+    int32_t k0;
+    int nk;
+};
+
+__device__ __forceinline__ WTile wgrad_tile(const int32_t *off, int num_mt, int num_nt, int32_t rows_cap, int tile) {
+    WTile w;
+    const int per = num_mt * num_nt;
+    w.e = tile / per;
+    const int rem = tile - w.e * per;
+    w.mt = rem / num_nt;
+    w.nt = rem - w.mt * num_nt;
+    const int32_t lo = min(max(off[w.e], 0), rows_cap), hi = min(max(off[w.e + 1], 0), rows_cap);
+    w.k0 = lo;
+    w.nk = hi > lo ? (hi - lo) / 64 : 0;
+    return w;
+}
+
 __device__ __forceinline__ int expert_of(const int32_t *off, int E, int32_t m0) {
     int lo = 0, hi = E - 1;  // first e with off[e+1] > m0
     while (lo < hi) {
@@ -112,7 +133,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows beyond the caller's buffers are never touched, whatever offsets hold
     const int32_t total_rows = min(s_off[E], p.rows_cap) & ~(kBM - 1);
     const int num_nt = (int)(p.N / kBN);
-    const int num_tiles = (total_rows / kBM) * num_nt;
+    // weight-gradient mode (BF16): tiles (expert, M tile, N tile), each reducing over its expert's rows
+    const bool wgrad = !FP4 && p.wgrad;
+    const int num_mt_w = wgrad ? (int)(p.M / kBM) : 0;
+    const int num_tiles = wgrad ? E * num_mt_w * num_nt : (total_rows / kBM) * num_nt;
     const int nkt = FP4 ? (int)(p.K / 256) : (int)(p.K / 64);
     const int nrt = FP4 ? (p.k + 63) / 64 : 0;
 
@@ -130,6 +154,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 const int64_t kgroups = p.K / 64;
                 for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                    if (wgrad) {
+                        // A rows [128 mt, +128) and B rows [256 nt, +256) over the expert's routed rows
+                        const WTile w = wgrad_tile(s_off, num_mt_w, num_nt, p.rows_cap, tile);
+                        for (int it = 0; it < w.nk; ++it) {
+                            if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            uint8_t *sa = smem + stage * C::kStageBytes;
+                            uint8_t *sb = sa + kATileBytes;
+                            const int32_t x = w.k0 + it * 64;
+                            mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
+                            tma_load_2d(sa, &tmA, x, w.mt * kBM, &full[stage]);
+                            tma_load_2d(sb, &tmB, x, w.nt * kBN, &full[stage]);
+                            tma_load_2d(sb + kBTileBytes / 2, &tmB, x, w.nt * kBN + 128, &full[stage]);
+                            issued[stage] = true;
+                            issued_phase[stage] = phase;
+                            if (++stage == kStages) {
+                                stage = 0;
+                                phase ^= 1u;
+                            }
+                        }
+                        continue;
+                    }
                     const int mt = tile / num_nt, nt = tile - mt * num_nt;
                     const int32_t m0 = mt * kBM;
                     const int e = expert_of(s_off, E, m0);
@@ -207,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    for (int it = 0; it < nkt + nrt; ++it) {
+                    const int nslices = wgrad ? wgrad_tile(s_off, num_mt_w, num_nt, p.rows_cap, tile).nk : nkt + nrt;
+                    for (int it = 0; it < nslices; ++it) {
                         if (!mbar_wait_bounded(&full[stage], phase, kWaitLimitNs, abort_flag)) {
                             ok = false;
                             break;
@@ -222,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
                         const uint32_t b_addr = a_addr + kATileBytes;
-                        if (it < nkt) {
+                        if (wgrad || it < nkt) {
                             if (FP4) {
                                 const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * kSFSlotCols;
 #pragma unroll
@@ -345,6 +394,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
+            if (wgrad) {
+                const WTile w = wgrad_tile(s_off, num_mt_w, num_nt, p.rows_cap, tile);
+                if (w.nk == 0) {  // an expert without routed rows: its gradient is zero
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) v[i] = 0u;
+                }
+                const int64_t row = (int64_t)w.e * p.M + (int64_t)w.mt * kBM + row_in_tile;
+                const int64_t col = (int64_t)w.nt * kBN + 128 * half;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) store16(p, row, col + 16 * j, 1.0f, v + 16 * j, amax_local);
+                continue;
+            }
             const int mt = tile / num_nt, nt = tile - mt * num_nt;
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
             const float gmul = FP4 ? __fmul_rn(gsa, s_gsw[expert_of(s_off, E, mt * kBM)]) : 1.0f;

@@ -1,0 +1,172 @@
+// train.cu -- the element-wise and data-movement kernels of the trainer-side
+// backward of the asymmetric-QAT MoE layer (QUADS §3.2 Eq. 13: the
+// straight-through estimator, dW = dW_hat and dX = W_hat^T dY; the GEMMs
+// themselves are the grouped GEMMs of gemm.cu): BF16 batched transposes, the
+// SwiGLU forward on saved pre-activations and its backward, and the backward
+// of the weighted top-k combine.  All HBM-bound.
+#include "common.cuh"
+
+namespace nvfp4 {
+namespace {
+
+// y[b][c][r] = x[b][r][c] for a batch of rows x cols BF16 matrices: 32 x 32
+// tiles through shared memory, so that both the reads (along c) and the writes
+// (along r) are coalesced.
+__global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *x, int64_t rows, int64_t cols, uint16_t *y) {
+    __shared__ uint16_t t[32][34];
+    const int64_t off = (int64_t)blockIdx.z * rows * cols;
+    const uint16_t *xb = x + off;
+    uint16_t *yb = y + off;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    for (int64_t r0 = (int64_t)blockIdx.y * 32; r0 < rows; r0 += (int64_t)gridDim.y * 32) {
+        const int64_t c0 = (int64_t)blockIdx.x * 32;
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+            const int64_t r = r0 + ty + i, c = c0 + tx;
+            t[ty + i][tx] = (r < rows && c < cols) ? xb[r * cols + c] : (uint16_t)0;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 32; i += 8) {
+            const int64_t c = c0 + ty + i, r = r0 + tx;
+            if (c < cols && r < rows) yb[c * rows + r] = t[tx][ty + i];
+        }
+        __syncthreads();
+    }
+}
+
+__device__ __forceinline__ float bf(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+__device__ __forceinline__ uint16_t to_bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
+
+// logistic function with the accurate exponential
+__device__ __forceinline__ float sigmoid(float g) { return __frcp_rn(__fadd_rn(1.0f, expf(-g))); }
+
+// h = bf16(silu(g) * u) from saved BF16 pre-activations gu = [g | u] (rows x 2I)
+__global__ void __launch_bounds__(256) swiglu_kernel(const uint16_t *gu, int64_t rows, int64_t I, uint16_t *h) {
+    const int64_t total = rows * I;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / I, c = i - r * I;
+        const float g = bf(gu[r * 2 * I + c]), u = bf(gu[r * 2 * I + I + c]);
+        h[i] = to_bf(__fmul_rn(__fmul_rn(g, sigmoid(g)), u));
+    }
+}
+
+// dg = dh * u * silu'(g), du = dh * silu(g); silu'(g) = s (1 + g (1 - s)), s = sigmoid(g)
+__global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint16_t *gu, const uint16_t *dh, int64_t rows,
+                                                              int64_t I, uint16_t *dgu) {
+    const int64_t total = rows * I;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / I, c = i - r * I;
+        const float g = bf(gu[r * 2 * I + c]), u = bf(gu[r * 2 * I + I + c]), d = bf(dh[i]);
+        const float s = sigmoid(g);
+        const float ds = __fmul_rn(s, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s))));
+        dgu[r * 2 * I + c] = to_bf(__fmul_rn(__fmul_rn(d, u), ds));
+        dgu[r * 2 * I + I + c] = to_bf(__fmul_rn(d, __fmul_rn(g, s)));
+    }
+}
+
+// Backward of out[t] = sum_s w[t,s] y[dst[t,s]]: the routed gradient
+// dy[dst[t,s]] = bf16(w[t,s] dout[t]) and, when asked, the weights' gradient
+// dw[t,s] = <y[dst[t,s]], dout[t]> (binary32 lane sums, one block per token).
+__global__ void __launch_bounds__(256) combine_backward_kernel(const float *dout, const uint16_t *y,
+                                                               const int32_t *dst, const float *w, int32_t topk,
+                                                               int64_t H, int64_t rows_cap, uint16_t *dy, float *dw) {
+    __shared__ float red[8];
+    const int64_t t = blockIdx.x;
+    const float *g = dout + t * H;
+    for (int s = 0; s < topk; ++s) {
+        const int64_t r = dst[t * topk + s];
+        const bool ok = r >= 0 && r < rows_cap;
+        const float ws = w[t * topk + s];
+        float acc = 0.0f;
+        for (int64_t h = threadIdx.x; h < H; h += blockDim.x) {
+            const float gv = g[h];
+            if (ok) {
+                dy[r * H + h] = to_bf(__fmul_rn(ws, gv));
+                acc = __fmaf_rn(bf(y[r * H + h]), gv, acc);
+            }
+        }
+        if (dw) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                float sum = 0.0f;
+                for (int i = 0; i < (int)(blockDim.x >> 5); ++i) sum += red[i];
+                dw[t * topk + s] = sum;
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// zero the padding rows [offsets[e] + counts[e], offsets[e+1]) of a routed BF16 tensor
+__global__ void zero_padding_bf16_kernel(const int32_t *counts, const int32_t *offsets, int64_t rows_cap, int64_t H,
+                                         uint16_t *y) {
+    const int e = blockIdx.y;
+    const int64_t row = (int64_t)offsets[e] + counts[e] + blockIdx.x;
+    if (row >= offsets[e + 1] || row >= rows_cap || row < 0) return;
+    for (int64_t h = threadIdx.x; h < H; h += blockDim.x) y[row * H + h] = 0;
+}
+
+int grid_for(int64_t work, int64_t per_block) {
+    int64_t b = (work + per_block - 1) / per_block;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (b > cap) b = cap;
+    return (int)(b < 1 ? 1 : b);
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" int nvfp4_transpose_bf16(const void *x, int32_t batch, int64_t rows, int64_t cols, void *y, void *stream) {
+    if (!x || !y || batch < 1 || rows < 0 || cols < 0) return NVFP4_ERR_INVALID_ARG;
+    if (batch > 65535 || (cols + 31) / 32 > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED;
+    if (rows == 0 || cols == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    const int64_t gy = (rows + 31) / 32;
+    transpose_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)(gy < 65535 ? gy : 65535), (unsigned)batch), 256,
+                       0, (cudaStream_t)stream>>>((const uint16_t *)x, rows, cols, (uint16_t *)y);
+    return launch_status("transpose_kernel");
+}
+
+extern "C" int nvfp4_swiglu(const void *gu, int64_t rows, int64_t I, void *h, void *stream) {
+    if (!gu || !h || rows < 0 || I < 0) return NVFP4_ERR_INVALID_ARG;
+    if (rows == 0 || I == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    swiglu_kernel<<<grid_for(rows * I, 256), 256, 0, (cudaStream_t)stream>>>((const uint16_t *)gu, rows, I,
+                                                                            (uint16_t *)h);
+    return launch_status("swiglu_kernel");
+}
+
+extern "C" int nvfp4_swiglu_backward(const void *gu, const void *dh, int64_t rows, int64_t I, void *dgu,
+                                     void *stream) {
+    if (!gu || !dh || !dgu || rows < 0 || I < 0) return NVFP4_ERR_INVALID_ARG;
+    if (rows == 0 || I == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    swiglu_backward_kernel<<<grid_for(rows * I, 256), 256, 0, (cudaStream_t)stream>>>(
+        (const uint16_t *)gu, (const uint16_t *)dh, rows, I, (uint16_t *)dgu);
+    return launch_status("swiglu_backward_kernel");
+}
+
+extern "C" int nvfp4_moe_combine_backward(const float *dout, const void *y, const int32_t *dst_row,
+                                          const float *weights, int32_t T, int32_t topk, int64_t H,
+                                          const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,
+                                          void *dy, float *dweights, void *stream) {
+    if (!dout || !y || !dst_row || !weights || !counts || !offsets || !dy || T < 0 || topk < 1 || H < 0 || E < 1 ||
+        rows_cap < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (E > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (H == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    zero_padding_bf16_kernel<<<dim3(127, E), 256, 0, st>>>(counts, offsets, rows_cap, H, (uint16_t *)dy);
+    int s = launch_status("zero_padding_bf16_kernel");
+    if (s != NVFP4_OK || T == 0) return s;
+    combine_backward_kernel<<<(unsigned)T, 256, 0, st>>>(dout, (const uint16_t *)y, dst_row, weights, topk, H,
+                                                         rows_cap, (uint16_t *)dy, dweights);
+    return launch_status("combine_backward_kernel");
+}

@@ -18,8 +18,9 @@ import torch
 from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16, NVFP4_OUT_F32,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
-               nvfp4_gather_selected_weights, nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online,
-               nvfp4_route_topk, nvfp4_w4a4_rac_grouped_gemm)
+               nvfp4_bf16_grouped_gemm_wgrad, nvfp4_gather_selected_weights, nvfp4_moe_combine_backward,
+               nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online, nvfp4_route_topk, nvfp4_swiglu,
+               nvfp4_swiglu_backward, nvfp4_transpose_bf16, nvfp4_w4a4_rac_grouped_gemm)
 
 
 def scale_bytes(rows, K):
@@ -193,10 +194,13 @@ class QatMoE:
     the reference of the mismatch diagnostic; sym=True (with fake=True) the
     symmetric W4A4 QAT ablation of QUADS §4.3.1 Fig. 7, which fake-quantizes
     the activations x and h as well (one tensor scale each, the rollout's
-    NVFP4 recipe)."""
+    NVFP4 recipe).  train=True keeps the gate/up pre-activations (the gate_up
+    GEMM stores them in BF16 and a separate SwiGLU pass makes h) so that
+    backward() can run (QUADS §3.2 Eq. 13)."""
 
-    def __init__(self, w13, w_down, topk, max_tokens, fake=True, sym=False):
+    def __init__(self, w13, w_down, topk, max_tokens, fake=True, sym=False, train=False):
         assert fake or not sym
+        assert not (train and sym)
         self.E, N13, self.H = w13.shape
         self.I = N13 // 2
         self.topk = topk
@@ -216,6 +220,25 @@ class QatMoE:
         self.y = torch.zeros((self.rows_cap, self.H), dtype=torch.bfloat16, device=dev)
         self.out = torch.empty((max_tokens, self.H), dtype=torch.float32, device=dev)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.train = train
+        if train:
+            R, H, I, E = self.rows_cap, self.H, self.I, self.E
+            bf = dict(dtype=torch.bfloat16, device=dev)
+            self.gu = torch.zeros((R, 2 * I), **bf)
+            self.dy = torch.zeros((R, H), **bf)
+            self.dh = torch.zeros((R, I), **bf)
+            self.dgu = torch.zeros((R, 2 * I), **bf)
+            self.dxr = torch.zeros((R, H), **bf)
+            self.t_big = torch.zeros(max(H, 2 * I) * R, **bf)   # a transposed routed tensor
+            self.t_small = torch.zeros(max(H, 2 * I) * R, **bf)  # the other operand of a weight gradient
+            self.w13_t = torch.empty((E, H, 2 * I), **bf)
+            self.wd_t = torch.empty((E, I, H), **bf)
+            self.ones = torch.ones((max_tokens, topk), dtype=torch.float32, device=dev)
+            self.dw13 = torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev)
+            self.dwd = torch.empty((E, H, I), dtype=torch.float32, device=dev)
+            self.dweights = torch.empty((max_tokens, topk), dtype=torch.float32, device=dev)
+            self.dx = torch.empty((max_tokens, H), dtype=torch.float32, device=dev)
+            self._T = 0
         if sym:
             self.x_hat = torch.empty((max_tokens, self.H), dtype=torch.bfloat16, device=dev)
             self.h_hat = torch.zeros((self.rows_cap, self.I), dtype=torch.bfloat16, device=dev)
@@ -257,9 +280,14 @@ class QatMoE:
             # first so that the amax of QDQ_A(h) sees the routed rows only
             with torch.cuda.stream(stream or torch.cuda.current_stream()):
                 self.h[:cap].zero_()
-        nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.h,
-                                out_dtype=NVFP4_OUT_BF16, epilogue=NVFP4_EPI_SWIGLU,
-                                dev_status=self.dev_status, stream=stream)
+        if self.train:  # keep the pre-activations for the backward
+            nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.gu,
+                                    out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
+            nvfp4_swiglu(self.gu, self.h, stream=stream)
+        else:
+            nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.h,
+                                    out_dtype=NVFP4_OUT_BF16, epilogue=NVFP4_EPI_SWIGLU,
+                                    dev_status=self.dev_status, stream=stream)
         h = self.h
         if self.sym:
             nvfp4_fake_quant(self.h[:cap].view(1, cap, self.I), self.h_hat[:cap].view(1, cap, self.I),
@@ -273,4 +301,44 @@ class QatMoE:
         out = self.out[:T]
         nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
         mark(6)
+        self._T = T
         return out
+
+    def backward(self, dout, stream=None):
+        """Gradients of the last forward (train=True) for the output gradient
+        dout [T, H] FP32, by the straight-through estimator of QUADS §3.2 Eq. 13
+        (the weight fake-quantizer is the identity in the backward):
+        returns (dx [T, H] FP32, dW13 [E, 2I, H] FP32, dW_down [E, H, I] FP32,
+        d_weights [T, topk] FP32, the combine weights' gradient) -- views of
+        reused buffers."""
+        assert self.train, "QatMoE(train=True) keeps what the backward needs"
+        T, E, H, I, R = self._T, self.E, self.H, self.I, self.rows_cap
+        assert dout.shape == (T, H) and dout.dtype == torch.float32
+        r = self.route
+        dst, w = r.dst_row[:T], r.weights[:T]
+        # routed output gradient, and the combine weights' gradient
+        nvfp4_moe_combine_backward(dout, self.y, dst, w, r.counts, r.offsets, E, self.dy,
+                                   dweights=self.dweights[:T], stream=stream)
+        # down projection: dh = dY W_hat_d (transposed weights), dW_d = dY^T h
+        nvfp4_transpose_bf16(self.wd_hat, self.wd_t, stream=stream)
+        nvfp4_bf16_grouped_gemm(self.dy, self.wd_t, r.offsets, E, I, H, self.dh, out_dtype=NVFP4_OUT_BF16,
+                                dev_status=self.dev_status, stream=stream)
+        dy_t, h_t = self.t_big[:H * R].view(H, R), self.t_small[:I * R].view(I, R)
+        nvfp4_transpose_bf16(self.dy, dy_t, stream=stream)
+        nvfp4_transpose_bf16(self.h, h_t, stream=stream)
+        nvfp4_bf16_grouped_gemm_wgrad(dy_t, h_t, r.offsets, E, self.dwd, dev_status=self.dev_status, stream=stream)
+        # SwiGLU
+        nvfp4_swiglu_backward(self.gu, self.dh, self.dgu, stream=stream)
+        # gate_up projection: dx_routed = d(gate|up) W_hat_13, dW_13 = d(gate|up)^T x_routed
+        nvfp4_transpose_bf16(self.w13_hat, self.w13_t, stream=stream)
+        nvfp4_bf16_grouped_gemm(self.dgu, self.w13_t, r.offsets, E, H, 2 * I, self.dxr, out_dtype=NVFP4_OUT_BF16,
+                                dev_status=self.dev_status, stream=stream)
+        dgu_t, xr_t = self.t_big[:2 * I * R].view(2 * I, R), self.t_small[:H * R].view(H, R)
+        nvfp4_transpose_bf16(self.dgu, dgu_t, stream=stream)
+        nvfp4_transpose_bf16(self.xr, xr_t, stream=stream)
+        nvfp4_bf16_grouped_gemm_wgrad(dgu_t, xr_t, r.offsets, E, self.dw13, dev_status=self.dev_status,
+                                      stream=stream)
+        # dx: each token's routed-row gradients summed
+        dx = self.dx[:T]
+        nvfp4_moe_combine(self.dxr, dst, self.ones[:T], self.topk, dx, stream=stream)
+        return dx, self.dw13, self.dwd, self.dweights[:T]

@@ -325,3 +325,51 @@ def combine(y, rows, weights):
     out = np.empty((T, H), np.float64)
     lib().orc_combine(y, H, rows, weights, T, topk, H, out)
     return out
+
+
+# ------------------------------------------------ trainer backward (Eq. 13) --
+# The asymmetric-QAT learner's backward with the straight-through estimator
+# (QUADS §3.2 Eq. 13): the weight fake-quantizer passes gradients unchanged,
+# so these are the plain derivatives of the layer's forward, in binary64.
+
+def swiglu_grad(gu, dh):
+    """Backward of h = silu(g) * u for gu = [g | u] ([M, 2I]): returns
+    [dg | du] with dg = dh * u * s * (1 + g * (1 - s)), du = dh * g * s,
+    s = 1 / (1 + exp(-g))."""
+    gu = _c(gu, np.float64)
+    dh = _c(dh, np.float64)
+    I = dh.shape[1]
+    g, u = gu[:, :I], gu[:, I:2 * I]
+    s = 1.0 / (1.0 + np.exp(-g))
+    return np.concatenate([dh * u * s * (1.0 + g * (1.0 - s)), dh * g * s], axis=1)
+
+
+def combine_grad(dout, y, rows, weights, R):
+    """Backward of combine(): for out[t] = sum_s w[t,s] y[rows[t,s]], returns
+    dy [R, H] (dy[rows[t,s]] = w[t,s] dout[t], other rows 0) and
+    dw[t,s] = <y[rows[t,s]], dout[t]>."""
+    dout = _c(dout, np.float64)
+    y = _c(y, np.float64)
+    rows = np.asarray(rows)
+    w = _c(weights, np.float64)
+    T, topk = rows.shape
+    dy = np.zeros((R, dout.shape[1]))
+    dw = np.zeros((T, topk))
+    for t in range(T):
+        for s in range(topk):
+            dy[rows[t, s]] = w[t, s] * dout[t]
+            dw[t, s] = y[rows[t, s]] @ dout[t]
+    return dy, dw
+
+
+def segment_wgrad(a, b, offsets):
+    """Per-expert weight gradient: dW[e] = a[seg e]^T . b[seg e] over the row
+    segments seg e = [offsets[e], offsets[e+1]) of a [R, M] and b [R, N]."""
+    a = _c(a, np.float64)
+    b = _c(b, np.float64)
+    E = len(offsets) - 1
+    out = np.zeros((E, a.shape[1], b.shape[1]))
+    for e in range(E):
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        out[e] = a[r0:r1].T @ b[r0:r1]
+    return out

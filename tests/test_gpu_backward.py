@@ -1,0 +1,170 @@
+"""GPU parity of the trainer backward (QUADS §3.2 Eq. 13, straight-through
+estimator) against the oracle's binary64 derivatives: the transposes
+bit-exact, the SwiGLU forward/backward within one BF16 rounding, the combine
+backward's routed gradient bit-exact, the grouped weight gradient (an empty
+expert included) within FP32 accumulation error, and QatMoE(train=True).backward
+stage by stage -- each stage against the oracle applied to the GPU's previous
+stage."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests import _gpu as G
+
+pytestmark = pytest.mark.gpu
+TOL_BF16 = 2.0 ** -8 + 1e-3
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_precision_moe_gb300 as m
+
+    m.load(build=True)
+    return m
+
+
+def f64(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def bf16_of(a):
+    return oracle.bf16_to_f32(oracle.bf16_round(np.asarray(a, np.float32))).astype(np.float64)
+
+
+def test_transpose_is_exact(nv):
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn((3, 37, 70), generator=g).to(torch.bfloat16).to(G.DEV)
+    y = torch.empty((3, 70, 37), dtype=torch.bfloat16, device=G.DEV)
+    nv.nvfp4_transpose_bf16(x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(y, x.transpose(1, 2))
+
+
+def test_swiglu_forward_and_backward(nv):
+    g = torch.Generator().manual_seed(5)
+    rows, I = 300, 192
+    gu = (torch.randn((rows, 2 * I), generator=g) * 3).to(torch.bfloat16)
+    dh = torch.randn((rows, I), generator=g).to(torch.bfloat16)
+    gud, dhd = gu.to(G.DEV), dh.to(G.DEV)
+    h = torch.empty((rows, I), dtype=torch.bfloat16, device=G.DEV)
+    dgu = torch.empty((rows, 2 * I), dtype=torch.bfloat16, device=G.DEV)
+    nv.nvfp4_swiglu(gud, h)
+    nv.nvfp4_swiglu_backward(gud, dhd, dgu)
+    torch.cuda.synchronize()
+    for got, ref in ((f64(h), oracle.swiglu(f64(gu), I)), (f64(dgu), oracle.swiglu_grad(f64(gu), f64(dh)))):
+        # one BF16 rounding of a binary32 evaluation: within 2^-8 relative (plus a tiny absolute floor)
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
+
+
+def _routing(nv, T, E, topk, seed, empty=None):
+    g = torch.Generator().manual_seed(seed)
+    logits = torch.randn((T, E), generator=g)
+    if empty is not None:
+        logits[:, empty] -= 100.0
+    ids, rw = oracle.route_topk(logits.numpy(), topk)
+    counts, offs, dst = oracle.route_layout(ids, E)
+    return logits, rw, counts, offs, dst
+
+
+def test_combine_backward(nv):
+    T, E, topk, H = 50, 4, 2, 256
+    logits, rw, counts, offs, dst = _routing(nv, T, E, topk, 7)
+    R = int(offs[-1]) + 128  # rows past offsets[E] too
+    g = torch.Generator().manual_seed(8)
+    y = torch.randn((R, H), generator=g).to(torch.bfloat16)
+    dout = torch.randn((T, H), generator=g)
+    dy = torch.full((R, H), 7.0, dtype=torch.bfloat16, device=G.DEV)  # stale values everywhere
+    dw = torch.empty((T, topk), dtype=torch.float32, device=G.DEV)
+    d = lambda a, dt=None: torch.as_tensor(a).to(G.DEV) if dt is None else torch.as_tensor(a, dtype=dt).to(G.DEV)
+    nv.nvfp4_moe_combine_backward(d(dout), d(y), d(dst, torch.int32), d(rw, torch.float32), d(counts, torch.int32),
+                                  d(offs, torch.int32), E, dy, dweights=dw)
+    torch.cuda.synchronize()
+    ref_dy, ref_dw = oracle.combine_grad(f64(dout), f64(y), dst, rw, R)
+    live = np.zeros(R, bool)
+    live[dst.reshape(-1)] = True
+    got = f64(dy)
+    rows = np.arange(int(offs[-1]))
+    # routed rows: bf16(fp32(w * dout)), exactly; padding rows inside the segments: zero
+    want = bf16_of(np.float32(rw)[:, :, None] * np.float32(f64(dout))[:, None, :]).reshape(-1, H)
+    assert np.array_equal(got[dst.reshape(-1)], want)
+    assert not got[rows[~live[rows]]].any()
+    assert np.allclose(f64(dw), ref_dw, rtol=1e-5, atol=1e-5)
+    assert np.allclose(got[dst.reshape(-1)], ref_dy[dst.reshape(-1)], rtol=2.0 ** -8, atol=0)
+
+
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_grouped_weight_gradient(nv, out_dtype):
+    T, E, topk, M, N = 200, 5, 2, 384, 512
+    _, _, counts, offs, dst = _routing(nv, T, E, topk, 11, empty=3)
+    assert counts[3] == 0
+    R = int(offs[-1]) + 128
+    g = torch.Generator().manual_seed(12)
+    a = torch.randn((R, M), generator=g).to(torch.bfloat16)
+    b = torch.randn((R, N), generator=g).to(torch.bfloat16)
+    a[int(offs[-1]):] = 1e4  # rows past offsets[E] must not be read
+    at, bt = a.t().contiguous().to(G.DEV), b.t().contiguous().to(G.DEV)
+    dw = torch.full((E, M, N), 5.0, dtype=torch.float32 if out_dtype == 0 else torch.bfloat16, device=G.DEV)
+    st = G.zeros(1, torch.int32)
+    nv.nvfp4_bf16_grouped_gemm_wgrad(at, bt, torch.as_tensor(offs, dtype=torch.int32).to(G.DEV), E, dw,
+                                     out_dtype=out_dtype, dev_status=st)
+    torch.cuda.synchronize()
+    G.status_ok(st)
+    ref = oracle.segment_wgrad(f64(a)[:int(offs[-1])], f64(b)[:int(offs[-1])], offs)
+    got = f64(dw)
+    assert not got[3].any()
+    tol = 1e-5 if out_dtype == 0 else TOL_BF16
+    assert G.rel_err(got, ref) <= tol
+
+
+def test_qat_layer_backward_stage_by_stage(nv):
+    from tests.test_oracle_mismatch import small_moe
+
+    x, logits, w13, wd = small_moe()
+    logits[:, 3] -= 100.0  # one expert without tokens: its weight gradients are zero
+    T, topk = x.shape[0], 2
+    E, N13, H = w13.shape
+    I = N13 // 2
+    dev = lambda a: torch.as_tensor(a).to(G.DEV)
+    layer = nv.QatMoE(dev(w13), dev(wd), topk, T, fake=True, train=True)
+    out = layer.forward(dev(x), dev(logits))
+    g = torch.Generator().manual_seed(13)
+    dout = torch.randn((T, H), generator=g)
+    dx, dw13, dwd, dweights = layer.backward(dout.to(G.DEV))
+    torch.cuda.synchronize()
+    G.status_ok(layer.dev_status)
+    r = layer.route
+    offs = r.offsets.cpu().numpy()
+    dst = r.dst_row.cpu().numpy()[:T]
+    rw = r.weights.cpu().numpy()[:T].astype(np.float64)
+    Rl = int(offs[-1])
+    W13, Wd = f64(layer.w13_hat), f64(layer.wd_hat)
+    xr, gu, h, y = f64(layer.xr)[:Rl], f64(layer.gu)[:Rl], f64(layer.h)[:Rl], f64(layer.y)[:Rl]
+
+    def per_expert(a, Wt):  # rows of expert e times Wt[e]
+        o = np.zeros((Rl, Wt.shape[1]))
+        for e in range(E):
+            o[offs[e]:offs[e + 1]] = a[offs[e]:offs[e + 1]] @ Wt[e].T
+        return o
+
+    # forward with saved pre-activations
+    assert G.rel_err(gu, per_expert(xr, W13)) <= TOL_BF16
+    assert np.all(np.abs(h - oracle.swiglu(gu, I)) <= 2.0 ** -8 * np.abs(oracle.swiglu(gu, I)) + 1e-5)
+    assert G.rel_err(f64(out), oracle.combine(y, dst.astype(np.int32), rw)) <= 1e-5
+    # backward
+    dy = f64(layer.dy)[:Rl]
+    ref_dy, ref_dw = oracle.combine_grad(f64(dout), y, dst, rw, Rl)
+    assert G.rel_err(dy, ref_dy) <= 2.0 ** -8
+    assert np.allclose(f64(dweights), ref_dw, rtol=1e-5, atol=1e-5)
+    dh = f64(layer.dh)[:Rl]
+    assert G.rel_err(dh, per_expert(dy, np.transpose(Wd, (0, 2, 1)))) <= TOL_BF16
+    assert G.rel_err(f64(dwd), oracle.segment_wgrad(dy, h, offs)) <= 1e-5
+    dgu = f64(layer.dgu)[:Rl]
+    ref_dgu = oracle.swiglu_grad(gu, dh)
+    assert np.all(np.abs(dgu - ref_dgu) <= 2.0 ** -8 * np.abs(ref_dgu) + 1e-5)
+    dxr = f64(layer.dxr)[:Rl]
+    assert G.rel_err(dxr, per_expert(dgu, np.transpose(W13, (0, 2, 1)))) <= TOL_BF16
+    assert G.rel_err(f64(dw13), oracle.segment_wgrad(dgu, xr, offs)) <= 1e-5
+    assert not f64(dw13)[3].any() and not f64(dwd)[3].any()
+    assert G.rel_err(f64(dx), oracle.combine(dxr, dst.astype(np.int32), np.ones(dst.shape))) <= 1e-5
