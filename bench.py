@@ -353,6 +353,43 @@ def qat_measure(dev, steps):
     assert int(layer.dev_status.item()) == 0
     st = lambda a, b: statistics.median([ev[i][a].elapsed_time(ev[i][b]) for i in range(steps)])
     fq_ms, g13_ms, gd_ms, fwd_ms = st(0, 1), st(3, 4), st(4, 5), st(0, 6)
+    del layer
+    # the training step's backward (QUADS §3.2 Eq. 13): forward with saved pre-activations, then backward
+    tl = nv.QatMoE(w13, wd, topk, T, train=True)
+    g2 = torch.Generator(device=dev)
+    g2.manual_seed(45)
+    dout = torch.randn((T, H), device=dev, generator=g2)
+    for _ in range(2):
+        tl.forward(x, logits)
+        tl.backward(dout)
+    torch.cuda.synchronize()
+    bev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        bev[i][0].record(stream)
+        tl.forward(x, logits)
+        bev[i][1].record(stream)
+        tl.backward(dout)
+        bev[i][2].record(stream)
+    torch.cuda.synchronize()
+    assert int(tl.dev_status.item()) == 0
+    tfwd = statistics.median([bev[i][0].elapsed_time(bev[i][1]) for i in range(steps)])
+    tbwd = statistics.median([bev[i][1].elapsed_time(bev[i][2]) for i in range(steps)])
+    # the wgrad launches alone: dW_down then dW_13, on the buffers the backward left
+    r = tl.route
+    Rc = tl.rows_cap
+    wev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    dy_t, h_t = tl.t_big[:H * Rc].view(H, Rc), tl.t_small[:I * Rc].view(I, Rc)
+    wev[0].record(stream)
+    for _ in range(5):
+        nv.nvfp4_bf16_grouped_gemm_wgrad(dy_t, h_t, r.offsets, E, tl.dwd, dev_status=tl.dev_status)
+    wev[1].record(stream)
+    dgu_t, xr_t = tl.t_big[:2 * I * Rc].view(2 * I, Rc), tl.t_small[:H * Rc].view(H, Rc)
+    for _ in range(5):
+        nv.nvfp4_bf16_grouped_gemm_wgrad(dgu_t, xr_t, r.offsets, E, tl.dw13, dev_status=tl.dev_status)
+    wev[2].record(stream)
+    torch.cuda.synchronize()
+    wd_ms, w13_ms = wev[0].elapsed_time(wev[1]) / 5, wev[1].elapsed_time(wev[2]) / 5
+    del tl
     n_w = E * (2 * I * H + H * I)
     fq_bytes = 4 * n_w  # read and write every BF16 weight once
     R = T * topk
@@ -364,7 +401,13 @@ def qat_measure(dev, steps):
             "bf16_gemm": {"gate_up_ms": round(g13_ms, 4), "down_ms": round(gd_ms, 4),
                           "tflops": round((fl13 + fld) / ((g13_ms + gd_ms) * 1e-3) / 1e12, 1),
                           "bf16_frac": round((fl13 + fld) / ((g13_ms + gd_ms) * 1e-3) / 1e12 / pk["bf16"], 4)},
-            "forward_ms": round(fwd_ms, 4)}
+            "forward_ms": round(fwd_ms, 4),
+            "train_step": {"forward_ms": round(tfwd, 4), "backward_ms": round(tbwd, 4),
+                           "wgrad_down_ms": round(wd_ms, 4), "wgrad_gate_up_ms": round(w13_ms, 4),
+                           "wgrad_tflops": round((fld + fl13) / ((wd_ms + w13_ms) * 1e-3) / 1e12, 1),
+                           "wgrad_bf16_frac": round((fld + fl13) / ((wd_ms + w13_ms) * 1e-3) / 1e12 / pk["bf16"], 4),
+                           "what": "QatMoE(train=True): forward keeping the gate/up pre-activations, then the "
+                                   "straight-through backward (dX, dW_13, dW_down, the combine weights' gradient)"}}
 
 
 def mismatch_measure(layer, x, logits, w13, wd):

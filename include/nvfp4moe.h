@@ -378,7 +378,8 @@ int nvfp4_swiglu_backward(const void *gu, const void *dh, int64_t rows, int64_t 
  * dweights[t,s] = sum_h y[dst_row[t,s], h] * dout[t, h] (binary32).
  *   dout      device float [T, H];  y  device BF16 [rows_cap, H] (the forward's rows)
  *   dy        device BF16 [rows_cap, H];  dweights  device float [T, topk] or NULL
- * Errors: INVALID_ARG, UNSUPPORTED (E > 65535). */
+ * Errors: INVALID_ARG, ALIGNMENT (16-byte pointers), UNSUPPORTED (E > 65535,
+ * H % 8, H > 8192). */
 int nvfp4_moe_combine_backward(const float *dout, const void *y, const int32_t *dst_row, const float *weights,
                                int32_t T, int32_t topk, int64_t H, const int32_t *counts, const int32_t *offsets,
                                int32_t E, int64_t rows_cap, void *dy, float *dweights, void *stream);

@@ -35,6 +35,81 @@ __global__ void __launch_bounds__(256) transpose_kernel(const uint16_t *x, int64
     }
 }
 
+// The same for even rows and cols: 64 x 64 tiles, 4-byte (two-element) reads
+// along c and 4-byte writes along r, so a warp moves 128 contiguous bytes on
+// both sides.
+__global__ void __launch_bounds__(256) transpose64_kernel(const uint16_t *x, int64_t rows, int64_t cols,
+                                                          uint16_t *y) {
+    __shared__ uint16_t t[64][66];
+    const int64_t off = (int64_t)blockIdx.z * rows * cols;
+    const uint16_t *xb = x + off;
+    uint16_t *yb = y + off;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8
+    const int64_t c0 = (int64_t)blockIdx.x * 64;
+    for (int64_t r0 = (int64_t)blockIdx.y * 64; r0 < rows; r0 += (int64_t)gridDim.y * 64) {
+#pragma unroll
+        for (int i = 0; i < 64; i += 8) {
+            const int64_t r = r0 + ty + i, c = c0 + 2 * tx;
+            uint32_t v = 0u;
+            if (r < rows && c < cols) v = *reinterpret_cast<const uint32_t *>(xb + r * cols + c);
+            t[ty + i][2 * tx] = (uint16_t)(v & 0xffffu);
+            t[ty + i][2 * tx + 1] = (uint16_t)(v >> 16);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 64; i += 8) {
+            const int64_t c = c0 + ty + i, r = r0 + 2 * tx;
+            if (c < cols && r < rows)
+                *reinterpret_cast<uint32_t *>(yb + c * rows + r) =
+                    (uint32_t)t[2 * tx][ty + i] | ((uint32_t)t[2 * tx + 1][ty + i] << 16);
+        }
+        __syncthreads();
+    }
+}
+
+// The same for rows and cols multiples of 8 and 16-byte aligned tensors:
+// 64 x 64 tiles moved with 16-byte global accesses on both sides -- a thread
+// reads 8 consecutive elements of a row and writes 8 consecutive elements of
+// a column (gathered from shared memory, whose 33-word row pitch keeps the
+// gathers at most 2-way bank-conflicted).
+__global__ void __launch_bounds__(256) transpose64v_kernel(const uint16_t *x, int64_t rows, int64_t cols,
+                                                           uint16_t *y) {
+    __shared__ uint32_t t[64][33];  // 64 rows x 64 BF16 (2 per word) + 1 word of pad
+    const int64_t off = (int64_t)blockIdx.z * rows * cols;
+    const uint16_t *xb = x + off;
+    uint16_t *yb = y + off;
+    const int q = threadIdx.x & 7, rr = threadIdx.x >> 3;  // 8-element chunk, row within 32
+    const int64_t c0 = (int64_t)blockIdx.x * 64;
+    for (int64_t r0 = (int64_t)blockIdx.y * 64; r0 < rows; r0 += (int64_t)gridDim.y * 64) {
+#pragma unroll
+        for (int h = 0; h < 64; h += 32) {
+            const int64_t r = r0 + rr + h, c = c0 + 8 * q;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < rows && c < cols) v = __ldg(reinterpret_cast<const uint4 *>(xb + r * cols + c));
+            t[rr + h][4 * q] = v.x;
+            t[rr + h][4 * q + 1] = v.y;
+            t[rr + h][4 * q + 2] = v.z;
+            t[rr + h][4 * q + 3] = v.w;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 64; h += 32) {
+            const int cc = rr + h;  // output row = input column c0 + cc
+            const int64_t c = c0 + cc, r = r0 + 8 * q;
+            uint32_t o[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t a = t[8 * q + 2 * u][cc >> 1], b = t[8 * q + 2 * u + 1][cc >> 1];
+                const uint32_t lo = (cc & 1) ? (a >> 16) : (a & 0xffffu);
+                const uint32_t hi = (cc & 1) ? (b >> 16) : (b & 0xffffu);
+                o[u] = lo | (hi << 16);
+            }
+            if (c < cols && r < rows) *reinterpret_cast<uint4 *>(yb + c * rows + r) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        __syncthreads();
+    }
+}
+
 __device__ __forceinline__ float bf(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 __device__ __forceinline__ uint16_t to_bf(float v) { return __bfloat16_as_ushort(__float2bfloat16_rn(v)); }
 
@@ -65,25 +140,82 @@ __global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint16_t *gu
     }
 }
 
+// The SwiGLU backward with 16-byte accesses (I % 8 == 0): 8 elements per thread
+__global__ void __launch_bounds__(256) swiglu_backward8_kernel(const uint16_t *gu, const uint16_t *dh, int64_t rows,
+                                                               int64_t I, uint16_t *dgu) {
+    const int64_t per_row = I >> 3, total = rows * per_row;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / per_row, c = (i - r * per_row) * 8;
+        const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * I + c));
+        const uint4 uv = __ldg(reinterpret_cast<const uint4 *>(gu + r * 2 * I + I + c));
+        const uint4 dv = __ldg(reinterpret_cast<const uint4 *>(dh + r * I + c));
+        const uint32_t G4[4] = {gv.x, gv.y, gv.z, gv.w}, U4[4] = {uv.x, uv.y, uv.z, uv.w},
+                       D4[4] = {dv.x, dv.y, dv.z, dv.w};
+        uint32_t og[4], ou[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t pg = 0, pu = 0;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const float g = __uint_as_float(hh ? (G4[k] & 0xffff0000u) : (G4[k] << 16));
+                const float u = __uint_as_float(hh ? (U4[k] & 0xffff0000u) : (U4[k] << 16));
+                const float d = __uint_as_float(hh ? (D4[k] & 0xffff0000u) : (D4[k] << 16));
+                const float sg = sigmoid(g);
+                const float ds = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sg))));
+                pg |= (uint32_t)to_bf(__fmul_rn(__fmul_rn(d, u), ds)) << (16 * hh);
+                pu |= (uint32_t)to_bf(__fmul_rn(d, __fmul_rn(g, sg))) << (16 * hh);
+            }
+            og[k] = pg;
+            ou[k] = pu;
+        }
+        *reinterpret_cast<uint4 *>(dgu + r * 2 * I + c) = make_uint4(og[0], og[1], og[2], og[3]);
+        *reinterpret_cast<uint4 *>(dgu + r * 2 * I + I + c) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+    }
+}
+
 // Backward of out[t] = sum_s w[t,s] y[dst[t,s]]: the routed gradient
 // dy[dst[t,s]] = bf16(w[t,s] dout[t]) and, when asked, the weights' gradient
 // dw[t,s] = <y[dst[t,s]], dout[t]> (binary32 lane sums, one block per token).
+// H % 8 == 0 and 16-byte aligned rows: 8 elements per thread and access
+// (dout read once per token into registers, reused for every slot).
+constexpr int kCombineBwdMaxVec = 4;  // 8-element vectors per thread: H <= 8 * 256 * 4
 __global__ void __launch_bounds__(256) combine_backward_kernel(const float *dout, const uint16_t *y,
                                                                const int32_t *dst, const float *w, int32_t topk,
                                                                int64_t H, int64_t rows_cap, uint16_t *dy, float *dw) {
     __shared__ float red[8];
     const int64_t t = blockIdx.x;
-    const float *g = dout + t * H;
+    const int nv = (int)(H >> 3);
+    float g[kCombineBwdMaxVec][8];
+#pragma unroll
+    for (int i = 0; i < kCombineBwdMaxVec; ++i) {
+        const int v = threadIdx.x + 256 * i;
+        if (v < nv) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(dout + t * H) + 2 * v);
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(dout + t * H) + 2 * v + 1);
+            g[i][0] = a.x, g[i][1] = a.y, g[i][2] = a.z, g[i][3] = a.w;
+            g[i][4] = b.x, g[i][5] = b.y, g[i][6] = b.z, g[i][7] = b.w;
+        }
+    }
     for (int s = 0; s < topk; ++s) {
         const int64_t r = dst[t * topk + s];
         const bool ok = r >= 0 && r < rows_cap;
         const float ws = w[t * topk + s];
         float acc = 0.0f;
-        for (int64_t h = threadIdx.x; h < H; h += blockDim.x) {
-            const float gv = g[h];
-            if (ok) {
-                dy[r * H + h] = to_bf(__fmul_rn(ws, gv));
-                acc = __fmaf_rn(bf(y[r * H + h]), gv, acc);
+#pragma unroll
+        for (int i = 0; i < kCombineBwdMaxVec; ++i) {
+            const int v = threadIdx.x + 256 * i;
+            if (ok && v < nv) {
+                const uint4 yv = __ldg(reinterpret_cast<const uint4 *>(y + r * H) + v);
+                const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    o[k] = (uint32_t)to_bf(__fmul_rn(ws, g[i][2 * k])) |
+                           ((uint32_t)to_bf(__fmul_rn(ws, g[i][2 * k + 1])) << 16);
+                    acc = __fmaf_rn(__uint_as_float(yw[k] << 16), g[i][2 * k], acc);
+                    acc = __fmaf_rn(__uint_as_float(yw[k] & 0xffff0000u), g[i][2 * k + 1], acc);
+                }
+                reinterpret_cast<uint4 *>(dy + r * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
         if (dw) {
@@ -127,6 +259,21 @@ extern "C" int nvfp4_transpose_bf16(const void *x, int32_t batch, int64_t rows, 
     if (batch > 65535 || (cols + 31) / 32 > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED;
     if (rows == 0 || cols == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
+    if (rows % 8 == 0 && cols % 8 == 0 && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(y) % 16 == 0) {
+        const int64_t gy = (rows + 63) / 64;
+        transpose64v_kernel<<<dim3((unsigned)((cols + 63) / 64), (unsigned)(gy < 65535 ? gy : 65535),
+                                   (unsigned)batch),
+                              256, 0, (cudaStream_t)stream>>>((const uint16_t *)x, rows, cols, (uint16_t *)y);
+        return launch_status("transpose64v_kernel");
+    }
+    if (rows % 2 == 0 && cols % 2 == 0 && reinterpret_cast<uintptr_t>(x) % 4 == 0 &&
+        reinterpret_cast<uintptr_t>(y) % 4 == 0) {
+        const int64_t gy = (rows + 63) / 64;
+        transpose64_kernel<<<dim3((unsigned)((cols + 63) / 64), (unsigned)(gy < 65535 ? gy : 65535), (unsigned)batch),
+                             256, 0, (cudaStream_t)stream>>>((const uint16_t *)x, rows, cols, (uint16_t *)y);
+        return launch_status("transpose64_kernel");
+    }
     const int64_t gy = (rows + 31) / 32;
     transpose_kernel<<<dim3((unsigned)((cols + 31) / 32), (unsigned)(gy < 65535 ? gy : 65535), (unsigned)batch), 256,
                        0, (cudaStream_t)stream>>>((const uint16_t *)x, rows, cols, (uint16_t *)y);
@@ -147,6 +294,12 @@ extern "C" int nvfp4_swiglu_backward(const void *gu, const void *dh, int64_t row
     if (!gu || !dh || !dgu || rows < 0 || I < 0) return NVFP4_ERR_INVALID_ARG;
     if (rows == 0 || I == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
+    if (I % 8 == 0 && reinterpret_cast<uintptr_t>(gu) % 16 == 0 && reinterpret_cast<uintptr_t>(dh) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(dgu) % 16 == 0) {
+        swiglu_backward8_kernel<<<grid_for(rows * I / 8, 256), 256, 0, (cudaStream_t)stream>>>(
+            (const uint16_t *)gu, (const uint16_t *)dh, rows, I, (uint16_t *)dgu);
+        return launch_status("swiglu_backward8_kernel");
+    }
     swiglu_backward_kernel<<<grid_for(rows * I, 256), 256, 0, (cudaStream_t)stream>>>(
         (const uint16_t *)gu, (const uint16_t *)dh, rows, I, (uint16_t *)dgu);
     return launch_status("swiglu_backward_kernel");
@@ -159,7 +312,8 @@ extern "C" int nvfp4_moe_combine_backward(const float *dout, const void *y, cons
     if (!dout || !y || !dst_row || !weights || !counts || !offsets || !dy || T < 0 || topk < 1 || H < 0 || E < 1 ||
         rows_cap < 0)
         return NVFP4_ERR_INVALID_ARG;
-    if (E > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (E > 65535 || H % 8 || H > 8 * 256 * kCombineBwdMaxVec) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(dout) || !aligned16(y) || !aligned16(dy)) return NVFP4_ERR_ALIGNMENT;
     if (H == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
     cudaStream_t st = (cudaStream_t)stream;

@@ -33,10 +33,11 @@ def bf16_of(a):
     return oracle.bf16_to_f32(oracle.bf16_round(np.asarray(a, np.float32))).astype(np.float64)
 
 
-def test_transpose_is_exact(nv):
+@pytest.mark.parametrize("shape", [(3, 37, 70), (2, 130, 200), (1, 64, 4096)])
+def test_transpose_is_exact(nv, shape):
     g = torch.Generator().manual_seed(3)
-    x = torch.randn((3, 37, 70), generator=g).to(torch.bfloat16).to(G.DEV)
-    y = torch.empty((3, 70, 37), dtype=torch.bfloat16, device=G.DEV)
+    x = torch.randn(shape, generator=g).to(torch.bfloat16).to(G.DEV)
+    y = torch.empty((shape[0], shape[2], shape[1]), dtype=torch.bfloat16, device=G.DEV)
     nv.nvfp4_transpose_bf16(x, y)
     torch.cuda.synchronize()
     assert torch.equal(y, x.transpose(1, 2))
