@@ -320,6 +320,25 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def build_qat_workload(dev):
+    """The QAT workload's inputs: 128 experts of random BF16 weights N(0, 0.02)
+    drawn on the device (seeded), the workload's seeded activations and logits."""
+    import torch
+
+    import synth
+
+    c = synth.CONFIGS[4]
+    E, H, I = c["E"], c["H"], c["I"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(44)
+    w13 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev)
+    wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
+    for e in range(E):
+        w13[e].copy_(torch.randn((2 * I, H), device=dev, generator=g) * 0.02)
+        wd[e].copy_(torch.randn((H, I), device=dev, generator=g) * 0.02)
+    return c, w13, wd, synth.activations(4).to(dev), synth.router_logits(4).to(dev)
+
+
 def qat_measure(dev, steps):
     """The trainer side at the QAT workload (128 experts, W13 3072x4096 and down
     4096x1536 fake-quantized every step, 4096 tokens top-8 through the BF16
@@ -330,17 +349,8 @@ def qat_measure(dev, steps):
     import nvfp4_precision_moe_gb300 as nv
     import synth
 
-    c = synth.CONFIGS[4]
+    c, w13, wd, x, logits = build_qat_workload(dev)
     E, H, I, T, topk = c["E"], c["H"], c["I"], c["T"], c["topk"]
-    g = torch.Generator(device=dev)
-    g.manual_seed(44)
-    w13 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev)
-    wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
-    for e in range(E):
-        w13[e].copy_(torch.randn((2 * I, H), device=dev, generator=g) * 0.02)
-        wd[e].copy_(torch.randn((H, I), device=dev, generator=g) * 0.02)
-    x = synth.activations(4).to(dev)
-    logits = synth.router_logits(4).to(dev)
     layer = nv.QatMoE(w13, wd, topk, T)
     stream = torch.cuda.current_stream()
     for _ in range(3):
