@@ -32,17 +32,38 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *logits, int32_t 
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
         // bitmask of experts already taken, E <= 1024 -> 32 words, word w owned by lane w
         uint32_t taken = 0u;
+        // up to 256 experts: this lane's logits (experts lane + 32i) stay in registers
+        constexpr int kRegE = 8;
+        float lr[kRegE];
+        const bool in_regs = E <= 32 * kRegE;
+#pragma unroll
+        for (int i = 0; i < kRegE; ++i) lr[i] = (in_regs && lane + 32 * i < E) ? l[lane + 32 * i] : -INFINITY;
         for (int s = 0; s < topk; ++s) {
             float bv = -INFINITY;
             int be = 0x7fffffff;
-            for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count for the shuffle
-                const int e = e0 + lane;
-                const uint32_t word = __shfl_sync(0xffffffffu, taken, e0 >> 5);
-                if (e < E && !((word >> lane) & 1u)) {
-                    float v = l[e];
-                    if (v > bv || (v == bv && e < be)) {
-                        bv = v;
-                        be = e;
+            if (in_regs) {
+#pragma unroll
+                for (int i = 0; i < kRegE; ++i) {
+                    const int e = lane + 32 * i;
+                    const uint32_t word = __shfl_sync(0xffffffffu, taken, i);
+                    if (e < E && !((word >> lane) & 1u)) {
+                        const float v = lr[i];
+                        if (v > bv || (v == bv && e < be)) {
+                            bv = v;
+                            be = e;
+                        }
+                    }
+                }
+            } else {
+                for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count for the shuffle
+                    const int e = e0 + lane;
+                    const uint32_t word = __shfl_sync(0xffffffffu, taken, e0 >> 5);
+                    if (e < E && !((word >> lane) & 1u)) {
+                        float v = l[e];
+                        if (v > bv || (v == bv && e < be)) {
+                            bv = v;
+                            be = e;
+                        }
                     }
                 }
             }
@@ -98,7 +119,15 @@ __global__ void __launch_bounds__(1024) dst_row_kernel(const int32_t *ids, int32
     if (vec) {
         const int4 *p = reinterpret_cast<const int4 *>(ids + t0 * topk);
         const int64_t n4 = (t1 - t0) * topk / 4;
-        for (int64_t i = 0; i < n4; ++i) {
+        int64_t i = 0;
+        for (; i + 4 <= n4; i += 4) {  // four 16-byte loads in flight
+            int4 q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) q[u] = __ldg(p + i + u);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) c += (q[u].x == e) + (q[u].y == e) + (q[u].z == e) + (q[u].w == e);
+        }
+        for (; i < n4; ++i) {
             const int4 q = __ldg(p + i);
             c += (q.x == e) + (q.y == e) + (q.z == e) + (q.w == e);
         }
@@ -132,7 +161,7 @@ __global__ void __launch_bounds__(1024) dst_row_kernel(const int32_t *ids, int32
         const int4 *p = reinterpret_cast<const int4 *>(ids + t0 * topk);
         const int64_t n4 = (t1 - t0) * topk / 4;
         for (int64_t i = 0; i < n4; ++i) {
-            const int4 q = __ldg(p + i);
+            const int4 q = __ldg(p + i);  // a second pass over the same run: L1 hits
             int32_t *d = dst_row + t0 * topk + 4 * i;
             if (q.x == e) d[0] = r++;
             if (q.y == e) d[1] = r++;
