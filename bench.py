@@ -561,7 +561,8 @@ def run_profile_case(args):
     launch shape: 128 experts, segments of the Zipf routing, about 2 GB),
     `quantize_x` (16384 x 4096 scatter-quantize, top-8), `quantize_h`
     (147456 x 1536, k=128), `combine` (16384 tokens x 8 x 4096), `bf16_gemm`
-    (QAT gate_up, BF16, same shape as gemm13).  Runs `--steps` launches."""
+    (QAT gate_up, BF16, same shape as gemm13), `wgrad` (the training step's dW_13 at the QAT
+    shapes for 16 experts x 256 rows, FP32 output).  Runs `--steps` launches."""
     import torch
 
     import nvfp4_precision_moe_gb300 as nv
@@ -616,6 +617,17 @@ def run_profile_case(args):
         fn = lambda: nv.nvfp4_bf16_grouped_gemm(x, w, offsets, E, N, K, y, out_dtype=nv.NVFP4_OUT_BF16,
                                                 epilogue=nv.NVFP4_EPI_SWIGLU)
         flops = 2 * rows * N * K
+    elif case == "wgrad":
+        # the training step's weight gradient dW_13 at the QAT shapes, 16 experts x 256 routed rows:
+        # a_t = d(gate|up)^T [3072, R], b_t = x_routed^T [4096, R], FP32 output [16, 3072, 4096]
+        E, per, M, N = 16, 256, 3072, 4096
+        R = E * per
+        offsets = torch.arange(0, R + 1, per, dtype=torch.int32, device=dev)
+        a_t = torch.randn((M, R), device=dev, generator=g).to(torch.bfloat16)
+        b_t = torch.randn((N, R), device=dev, generator=g).to(torch.bfloat16)
+        dw = torch.empty((E, M, N), dtype=torch.float32, device=dev)
+        fn = lambda: nv.nvfp4_bf16_grouped_gemm_wgrad(a_t, b_t, offsets, E, dw)
+        flops = 2 * R * M * N
     elif case == "quantize_x":
         T, H, topk, k = 16384, 4096, 8, 128
         x = torch.randn((T, H), device=dev, generator=g).to(torch.bfloat16)
