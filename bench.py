@@ -33,8 +33,8 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core ratio, nominal
 # one ncu capture (profiles/single_gemm_kernel_moe_prefill.md), valid only for the kernel
 # sources it was taken on (common.cuh, gemm_common.cuh, gemm_single.cu): reported as null
 # once they change.
-GATE_UP_TRAFFIC = {"bytes": 1362263000 + 415130624,
-                   "sources_sha256": "d07ad04fd73da3672c6c3f3025f5095194ddaf4f5d8b9a39ced2c303e0d54a82"}
+GATE_UP_TRAFFIC = {"bytes": 1362286000 + 415321088,
+                   "sources_sha256": "8dba006fff9f0106fc9337d001b5f8f1118b95edae3f7eef9bb7910f13f30f4c"}
 
 
 def gate_up_traffic():

@@ -58,6 +58,7 @@ struct GemmParams {
     // A [M, rows_cap] and B [N, rows_cap] K-major, seg e = [offsets[e], offsets[e+1])
     int32_t wgrad;
     int64_t M;
+    int32_t wgrad_tma;  // FP32 weight gradients stored through shared memory by TMA (the map in tmR)
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

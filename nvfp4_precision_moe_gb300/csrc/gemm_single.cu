@@ -38,14 +38,18 @@ constexpr uint32_t kIdescBF16 = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3)
 template <bool FP4>
 struct Cfg {
     static constexpr int kStageBytes = kATileBytes + kBTileBytes + (FP4 ? kSFABytes + kSFBBytes : 0);
-    static constexpr int kBarOffset = kStages * kStageBytes;
+    // BF16 only: one 2 KB store-staging box (16 rows x 128 bytes, 128-byte swizzle) per epilogue warp
+    static constexpr int kOutOffset = kStages * kStageBytes;
+    static constexpr int kOutBytes = FP4 ? 0 : kEpiWarps * 2048;
+    static constexpr int kBarOffset = kOutOffset + kOutBytes;
     // barriers: full/empty/sf_full/sf_ready per stage, acc_full, acc_empty, drain
     static constexpr int kNumBars = 4 * kStages + 3;
     static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
     static constexpr int kGswOffset = kOffOffset + (kMaxExperts + 1) * 4;
     static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
 };
-static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory budget");
+static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<false>::kSmemBytes <= 232448, "shared memory budget");
+static_assert(Cfg<false>::kOutOffset % 1024 == 0, "store staging boxes sit on 1024-byte swizzle atoms");
 
 // A tile of the weight-gradient mode: expert e, output tile (mt, nt), and the
 // expert's routed rows [k0, k0 + 64 nk) as the reduction range.
@@ -400,8 +404,38 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 128; ++i) v[i] = 0u;
                 }
-                const int64_t row = (int64_t)w.e * p.M + (int64_t)w.mt * kBM + row_in_tile;
                 const int64_t col = (int64_t)w.nt * kBN + 128 * half;
+                if (!FP4 && p.wgrad_tma) {
+                    // FP32 rows through this warp's staging box: rows 0-15 of the warp, then 16-31,
+                    // 32 columns at a time, written in the 128-byte swizzle (16-byte chunk c of
+                    // row r at chunk c ^ r%8) and stored by one TMA store each
+                    const uint32_t box = smem_u32(smem + C::kOutOffset + ew * 2048);
+                    const int32_t row0 = (int32_t)((int64_t)w.e * p.M + (int64_t)w.mt * kBM + q * 32);
+                    const int r = lane & 15;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            if ((lane >> 4) == hh) {
+#pragma unroll
+                                for (int c = 0; c < 8; ++c)
+                                    st_shared_v4(box + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)),
+                                                 v[32 * j + 4 * c], v[32 * j + 4 * c + 1], v[32 * j + 4 * c + 2],
+                                                 v[32 * j + 4 * c + 3]);
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_2d(&tmR, box, (int32_t)col + 32 * j, row0 + 16 * hh);
+                                bulk_commit();
+                                bulk_wait_read();  // the box may be rewritten
+                            }
+                            __syncwarp();
+                        }
+                    }
+                    continue;
+                }
+                const int64_t row = (int64_t)w.e * p.M + (int64_t)w.mt * kBM + row_in_tile;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) store16(p, row, col + 16 * j, 1.0f, v + 16 * j, amax_local);
                 continue;
@@ -419,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 8; ++j) store16(p, row, col + 16 * j, gmul, v + 16 * j, amax_local);
             }
         }
+        if (!FP4 && wgrad && p.wgrad_tma && lane == 0) bulk_wait_all();  // this warp's TMA stores are done
         if (p.amax_out) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, o));
