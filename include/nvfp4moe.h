@@ -133,6 +133,14 @@ int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float
 int nvfp4_fake_quant(const void *w, int32_t ntensors, int64_t rows, int64_t cols, void *w_hat,
                      float *gs_out, float *amax_ws, int32_t *dev_status, void *stream);
 
+/* nvfp4_fake_quant that also writes the transpose, for the learner's backward
+ * (QUADS §3.2 Eq. 13: dX = W_hat^T dY wants W_hat^T with the reduction axis
+ * contiguous): w_hat as nvfp4_fake_quant writes it, bit for bit, and
+ * w_hat_t[t] = w_hat[t]^T (device BF16 [ntensors, cols, rows]), from one read
+ * of w.  Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (rows % 64, cols % 64). */
+int nvfp4_fake_quant_transposed(const void *w, int32_t ntensors, int64_t rows, int64_t cols, void *w_hat,
+                                void *w_hat_t, float *gs_out, float *amax_ws, int32_t *dev_status, void *stream);
+
 /* nvfp4_fake_quant for callers that cannot allocate device memory.  The paper
  * has no counterpart; this is a convenience of the library.  A framework that
  * owns all device memory through its own pool, or a latency-critical loop

@@ -32,6 +32,7 @@ _SIGS = {
     "nvfp4_quantize": "pqqqpppipiqppppp",
     "nvfp4_fake_quant": "piqqppppp",
     "nvfp4_fake_quant_noalloc": "piqqpppp",
+    "nvfp4_fake_quant_transposed": "piqqpppppp",
     "nvfp4_prepare_weights": "piqqpiippppppp",
     "nvfp4_rac_select_channels": "pqqpippp",
     "nvfp4_rac_requant_residual": "pqipipppp",
@@ -139,6 +140,13 @@ def nvfp4_fake_quant(w, w_hat, amax_ws, gs_out=None, dev_status=None, stream=Non
     """A16: QDQ_W of each w[t] (w: [ntensors, rows, cols] BF16)."""
     nt, rows, cols = w.shape
     _call("nvfp4_fake_quant", _p(w), nt, rows, cols, _p(w_hat), _p(gs_out), _p(amax_ws),
+          _p(dev_status), _s(stream))
+
+
+def nvfp4_fake_quant_transposed(w, w_hat, w_hat_t, amax_ws, gs_out=None, dev_status=None, stream=None):
+    """QDQ_W of each w[t] and its transpose w_hat_t[t] = w_hat[t]^T, from one read of w."""
+    nt, rows, cols = w.shape
+    _call("nvfp4_fake_quant_transposed", _p(w), nt, rows, cols, _p(w_hat), _p(w_hat_t), _p(gs_out), _p(amax_ws),
           _p(dev_status), _s(stream))
 
 

@@ -815,6 +815,72 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_kernel(const ui
     }
 }
 
+// QDQ_W (QUADS §3.2 Eq. 12) that also writes the transpose, for the learner's
+// backward (dX = W_hat^T dY needs W_hat^T with the reduction axis contiguous):
+// a block owns a 64 x 64 tile of one tensor; each thread quantizes one
+// 16-element block exactly as quantize_kernel<fake> does (quant_block, the
+// tensor's gs), writes it to w_hat, and leaves it in shared memory; the tile
+// then leaves transposed, 16 bytes per thread.
+__global__ void __launch_bounds__(256) fake_quant_t_kernel(const uint16_t *w, int64_t rows, int64_t cols,
+                                                          const float *amax, float *gs_out, uint16_t *w_hat,
+                                                          uint16_t *w_hat_t, int32_t *dev_status) {
+    __shared__ QTables tb;
+    __shared__ uint32_t tile[64][33];  // 64 rows x 64 BF16 (two per word) + 1 word of pad
+    fill_tables(tb);
+    __syncthreads();
+    const int64_t tensor = blockIdx.z;
+    const float am = amax[tensor];
+    const float gs = tensor_scale(am);
+    const float p6 = __fmul_rn(gs, 6.0f);
+    const float inv_gs = __frcp_rn(gs);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        if (gs_out) gs_out[tensor] = gs;
+        if (!isfinite(am)) report(dev_status, NVFP4_ERR_NONFINITE);
+    }
+    const int64_t off = tensor * rows * cols;
+    const int64_t r0 = (int64_t)blockIdx.y * 64, c0 = (int64_t)blockIdx.x * 64;
+    {
+        const int r = threadIdx.x >> 2, b = threadIdx.x & 3;  // row in the tile, 16-element block
+        const int64_t gi = off + (r0 + r) * cols + c0 + 16 * b;
+        const uint4 *src = reinterpret_cast<const uint4 *>(w + gi);
+        float v[16];
+        unpack_block(__ldg(src), __ldg(src + 1), v);
+        BlockQ q;
+        quant_block(v, gs, p6, inv_gs, tb, q);
+        uint32_t o[8];
+#pragma unroll
+        for (int t = 0; t < 16; t += 2) {
+            const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
+            const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
+            o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
+                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(w_hat + gi);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tile[r][8 * b + i] = o[i];
+    }
+    __syncthreads();
+    // w_hat_t[tensor][c][r]: output row c0 + cc holds input rows r0 .. r0+63; a thread writes
+    // 8 consecutive of them (16 bytes), two such pieces per thread
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int idx = threadIdx.x + 256 * k;  // 64 output rows x 8 pieces
+        const int cc = idx >> 3, piece = idx & 7;
+        uint32_t o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int ra = 8 * piece + 2 * u;
+            const uint32_t a0 = tile[ra][cc >> 1], a1 = tile[ra + 1][cc >> 1];
+            const uint32_t lo = (cc & 1) ? (a0 >> 16) : (a0 & 0xffffu);
+            const uint32_t hi = (cc & 1) ? (a1 >> 16) : (a1 & 0xffffu);
+            o[u] = lo | (hi << 16);
+        }
+        *reinterpret_cast<uint4 *>(w_hat_t + off + (c0 + cc) * rows + r0 + 8 * piece) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 static int quant_grid(int64_t rows) {
     int64_t blocks = (rows + kQWarps - 1) / kQWarps;
     int64_t cap = (int64_t)sm_count() * 8;
@@ -909,6 +975,21 @@ extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t
     int g = quant_grid(rows) / (nt > 8 ? 8 : nt);
     quantize_kernel<kModeFake><<<dim3(g < 1 ? 1 : g, nt), kQThreads, 0, st>>>(a);
     return launch_status("quantize_kernel<fake>");
+}
+
+extern "C" int nvfp4_fake_quant_transposed(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat,
+                                           void *w_hat_t, float *gs_out, float *amax_ws, int32_t *dev_status,
+                                           void *stream) {
+    if (!w || !w_hat || !w_hat_t || !amax_ws || nt < 1 || rows < 0 || cols < 0) return NVFP4_ERR_INVALID_ARG;
+    if (rows % 64 || cols % 64 || nt > 65535 || rows / 64 > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(w) || !aligned16(w_hat) || !aligned16(w_hat_t)) return NVFP4_ERR_ALIGNMENT;
+    NVFP4_CHECK_INIT();
+    cudaStream_t st = (cudaStream_t)stream;
+    int s = amax_launch(w, rows, cols, cols, nt, rows * cols, amax_ws, st);
+    if (s != NVFP4_OK || rows == 0 || cols == 0) return s;
+    fake_quant_t_kernel<<<dim3((unsigned)(cols / 64), (unsigned)(rows / 64), (unsigned)nt), 256, 0, st>>>(
+        (const uint16_t *)w, rows, cols, amax_ws, gs_out, (uint16_t *)w_hat, (uint16_t *)w_hat_t, dev_status);
+    return launch_status("fake_quant_t_kernel");
 }
 
 extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_t K, const int32_t *S, int32_t k,

@@ -18,7 +18,8 @@ import torch
 from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16, NVFP4_OUT_F32,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
-               nvfp4_bf16_grouped_gemm_wgrad, nvfp4_gather_selected_weights, nvfp4_moe_combine_backward,
+               nvfp4_bf16_grouped_gemm_wgrad, nvfp4_fake_quant_transposed, nvfp4_gather_selected_weights,
+               nvfp4_moe_combine_backward,
                nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online, nvfp4_route_topk, nvfp4_swiglu,
                nvfp4_swiglu_backward, nvfp4_transpose_bf16, nvfp4_w4a4_rac_grouped_gemm)
 
@@ -248,6 +249,12 @@ class QatMoE:
     def fake_quant(self, stream=None):
         if not self.fake:
             return
+        if self.train:  # the transposes the backward needs come from the same read of W
+            nvfp4_fake_quant_transposed(self.w13, self.w13_hat, self.w13_t, self.amax_ws, gs_out=self.gs13,
+                                        dev_status=self.dev_status, stream=stream)
+            nvfp4_fake_quant_transposed(self.wd, self.wd_hat, self.wd_t, self.amax_ws, gs_out=self.gsd,
+                                        dev_status=self.dev_status, stream=stream)
+            return
         nvfp4_fake_quant(self.w13, self.w13_hat, self.amax_ws, gs_out=self.gs13,
                          dev_status=self.dev_status, stream=stream)
         nvfp4_fake_quant(self.wd, self.wd_hat, self.amax_ws, gs_out=self.gsd,
@@ -319,8 +326,10 @@ class QatMoE:
         # routed output gradient, and the combine weights' gradient
         nvfp4_moe_combine_backward(dout, self.y, dst, w, r.counts, r.offsets, E, self.dy,
                                    dweights=self.dweights[:T], stream=stream)
-        # down projection: dh = dY W_hat_d (transposed weights), dW_d = dY^T h
-        nvfp4_transpose_bf16(self.wd_hat, self.wd_t, stream=stream)
+        # down projection: dh = dY W_hat_d (the transposed weights: written by fake_quant for a
+        # fake-quantized trainer, transposed here for the BF16 one), dW_d = dY^T h
+        if not self.fake:
+            nvfp4_transpose_bf16(self.wd_hat, self.wd_t, stream=stream)
         nvfp4_bf16_grouped_gemm(self.dy, self.wd_t, r.offsets, E, I, H, self.dh, out_dtype=NVFP4_OUT_BF16,
                                 dev_status=self.dev_status, stream=stream)
         dy_t, h_t = self.t_big[:H * R].view(H, R), self.t_small[:I * R].view(I, R)
@@ -330,7 +339,8 @@ class QatMoE:
         # SwiGLU
         nvfp4_swiglu_backward(self.gu, self.dh, self.dgu, stream=stream)
         # gate_up projection: dx_routed = d(gate|up) W_hat_13, dW_13 = d(gate|up)^T x_routed
-        nvfp4_transpose_bf16(self.w13_hat, self.w13_t, stream=stream)
+        if not self.fake:
+            nvfp4_transpose_bf16(self.w13_hat, self.w13_t, stream=stream)
         nvfp4_bf16_grouped_gemm(self.dgu, self.w13_t, r.offsets, E, H, 2 * I, self.dxr, out_dtype=NVFP4_OUT_BF16,
                                 dev_status=self.dev_status, stream=stream)
         dgu_t, xr_t = self.t_big[:2 * I * R].view(2 * I, R), self.t_small[:H * R].view(H, R)

@@ -43,6 +43,21 @@ def test_transpose_is_exact(nv, shape):
     assert torch.equal(y, x.transpose(1, 2))
 
 
+def test_fake_quant_transposed(nv):
+    g = torch.Generator().manual_seed(17)
+    w = (torch.randn((3, 192, 320), generator=g) * 0.02).to(torch.bfloat16).to(G.DEV)
+    w[1, 5, 7] = 3.0  # an outlier block
+    ref = torch.empty_like(w)
+    got = torch.empty_like(w)
+    got_t = torch.empty((3, 320, 192), dtype=torch.bfloat16, device=G.DEV)
+    gs_ref, gs_got = G.zeros(3, torch.float32), G.zeros(3, torch.float32)
+    nv.nvfp4_fake_quant(w, ref, G.zeros(3, torch.float32), gs_out=gs_ref)
+    nv.nvfp4_fake_quant_transposed(w, got, got_t, G.zeros(3, torch.float32), gs_out=gs_got)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref) and torch.equal(gs_got, gs_ref)
+    assert torch.equal(got_t, ref.transpose(1, 2))
+
+
 def test_swiglu_forward_and_backward(nv):
     g = torch.Generator().manual_seed(5)
     rows, I = 300, 192

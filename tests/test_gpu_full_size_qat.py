@@ -65,6 +65,13 @@ def test_fake_quant_bit_exact(qat):
             assert np.array_equal(G.u16(w_hat[e]), ref), e
 
 
+def test_training_fake_quant_writes_the_transposes(qat):
+    P, L = qat["plain"], qat["train"]
+    assert torch.equal(L.w13_hat, P.w13_hat) and torch.equal(L.wd_hat, P.wd_hat)
+    for e in qat["experts"]:
+        assert torch.equal(L.w13_t[e], L.w13_hat[e].t()) and torch.equal(L.wd_t[e], L.wd_hat[e].t())
+
+
 def test_forward_sampled_rows(qat):
     L, I = qat["plain"], qat["c"]["I"]
     rng = np.random.default_rng(40)
