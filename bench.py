@@ -347,7 +347,6 @@ def qat_measure(dev, steps):
     import torch
 
     import nvfp4_precision_moe_gb300 as nv
-    import synth
 
     c, w13, wd, x, logits = build_qat_workload(dev)
     E, H, I, T, topk = c["E"], c["H"], c["I"], c["T"], c["topk"]

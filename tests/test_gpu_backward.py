@@ -10,7 +10,6 @@ import pytest
 import torch
 
 import oracle
-import synth
 from tests import _gpu as G
 
 pytestmark = pytest.mark.gpu
