@@ -158,7 +158,6 @@ __device__ __forceinline__ void unpack_block(const uint4 &a, const uint4 &b, flo
 constexpr int kQThreads = 256;
 constexpr int kQWarps = kQThreads / 32;
 constexpr int kMaxStagedK = 1024;  // residual row staged in shared memory up to this k
-constexpr int kResidBatch = 4;     // selected channels per lane whose inputs are fetched together
 
 // The RAC value of one selected element x (BF16 bits) of a block with scale
 // code sb: its E2M1 code is recomputed exactly as the block's quantization
@@ -171,6 +170,16 @@ __device__ __forceinline__ uint16_t resid_value(uint16_t xb, uint32_t sb, float 
     uint32_t c;
     if (__fmul_rn(sbf, gs) != 0.0f) c = e2m1x2_from_f32(__fmul_rn(v, __fmul_rn(tb.rcp[sb], inv_gs)), 0.0f) & 15u;
     else c = (__float_as_uint(v) >> 31) << 3;
+    const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
+    if (MODE == kModeWeight) return __bfloat16_as_ushort(__float2bfloat16_rn(cs));
+    const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
+}
+
+// The RAC value of element x of a block already quantized to code c with scale
+// value sbf (the same arithmetic as resid_value, without recomputing the code).
+template <int MODE>
+__device__ __forceinline__ uint16_t rac_value(float v, uint32_t c, float sbf, float gs, float inv_gs) {
     const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
     if (MODE == kModeWeight) return __bfloat16_as_ushort(__float2bfloat16_rn(cs));
     const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
@@ -192,6 +201,10 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
     __shared__ int64_t s_cbase[kQWarps][32];  // destination f: byte offset of its code row (-1: skipped)
     __shared__ int64_t s_sbase[kQWarps][32];  // destination f: row part of its swizzled scale offsets
     __shared__ int32_t s_S[kMaxStagedK];
+    // per 16-element block: which of its channels are in S (bit t = channel 16b + t), and the
+    // position in S of its first selected channel (S is strictly increasing)
+    __shared__ uint32_t s_selmask[kMaxBlocksPerRow];
+    __shared__ uint32_t s_selbase[kMaxBlocksPerRow];
     __shared__ QTables s_tab;
     const int tensor = blockIdx.y;
     fill_tables(s_tab);
@@ -199,8 +212,21 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
     const int64_t kslices = (nb + 15) >> 4;
     const bool has_sel = (MODE != kModeFake) && a.k > 0;
     const bool staged = a.k <= kMaxStagedK;
-    if (has_sel && staged)
-        for (int i = threadIdx.x; i < a.k; i += blockDim.x) s_S[i] = a.S[i];
+    if (has_sel && staged) {
+        for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+            s_selmask[i] = 0u;
+            s_selbase[i] = 0xffffffffu;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < a.k; i += blockDim.x) {
+            const int32_t j = a.S[i];
+            s_S[i] = j;
+            if (j >= 0 && j < a.K) {
+                atomicOr(&s_selmask[j >> 4], 1u << (j & 15));
+                atomicMin(&s_selbase[j >> 4], (uint32_t)i);
+            }
+        }
+    }
     __syncthreads();  // tables (and S) are ready
 
     const float amax_t = a.amax[tensor];
@@ -301,7 +327,24 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
                 continue;
             }
 
-            if (has_sel && valid) row_sb[b] = (uint8_t)q.sb;
+            if (has_sel && valid) {
+                if (staged) {
+                    // this block's selected channels: their RAC values go straight to the stage
+                    const uint32_t msk = s_selmask[b];
+                    if (msk) {
+                        const uint32_t base = s_selbase[b];
+                        uint32_t rem = msk;
+                        while (rem) {
+                            const int t = __ffs(rem) - 1;
+                            rem &= rem - 1u;
+                            stage[base + __popc(msk & ((1u << t) - 1u))] =
+                                rac_value<MODE>(sel16(v, t), q.code(t), q.sbf, gs, inv_gs);
+                        }
+                    }
+                } else {
+                    row_sb[b] = (uint8_t)q.sb;
+                }
+            }
             // four consecutive blocks' scales -> one 32-bit word (lane%4 == 0 stores)
             uint32_t sw = q.sb;
             const uint32_t s1 = __shfl_down_sync(0xffffffffu, sw, 1);
@@ -322,26 +365,8 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
             // residual (activation) or unscaled dequantized weight on S, one
             // selected channel per lane: the element's code is recomputed from
             // its block scale exactly as its block quantized it
-            __syncwarp();  // row_sb is complete
-            if (staged) {
-                // four selected channels per lane at a time: their inputs are
-                // fetched together, then each value is computed
-                for (int si0 = lane; si0 < a.k; si0 += 32 * kResidBatch) {
-                    int jj[kResidBatch];
-                    uint16_t xb[kResidBatch];
-#pragma unroll
-                    for (int u = 0; u < kResidBatch; ++u) {
-                        const int si = si0 + 32 * u;
-                        jj[u] = si < a.k ? s_S[si] : 0;
-                        xb[u] = si < a.k ? __ldg(xrow + jj[u]) : (uint16_t)0;
-                    }
-#pragma unroll
-                    for (int u = 0; u < kResidBatch; ++u) {
-                        const int si = si0 + 32 * u;
-                        if (si < a.k) stage[si] = resid_value<MODE>(xb[u], row_sb[jj[u] >> 4], gs, inv_gs, s_tab);
-                    }
-                }
-            } else {  // k beyond the stage: values go straight to every destination row
+            __syncwarp();  // the stage (or row_sb) is complete
+            if (!staged) {  // k beyond the stage: values go straight to every destination row
                 for (int si = lane; si < a.k; si += 32) {
                     const int j = __ldg(a.S + si);
                     const uint16_t val = resid_value<MODE>(__ldg(xrow + j), row_sb[j >> 4], gs, inv_gs, s_tab);
