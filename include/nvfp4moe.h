@@ -68,7 +68,8 @@ enum { NVFP4_PIPELINE_AUTO = 0, NVFP4_PIPELINE_SINGLE = 1, NVFP4_PIPELINE_PAIR =
 /* Name of a status code ("NVFP4_OK", ...); never NULL. */
 const char *nvfp4_status_str(int status);
 
-/* Checks that the current CUDA device is an sm_103 part and loads the driver
+/* Library set-up (no counterpart in QUADS).
+ * Checks that the current CUDA device is an sm_103 part and loads the driver
  * entry point used to build TMA descriptors.  Called implicitly by every
  * entry point; returns NVFP4_ERR_ARCH on any other device. */
 int nvfp4_init(void);
@@ -80,7 +81,8 @@ const char *nvfp4_last_error(void);
 /* Quantization (QUADS §2.2 "FP4."; §3.1 Eq. 9; §3.3 Eq. 20-21)              */
 /* ------------------------------------------------------------------------ */
 
-/* Per-tensor amax = max |x| for `ntensors` BF16 matrices of M x K (row
+/* The amax behind the per-tensor FP32 scale of QUADS §2.2 "FP4.".
+ * Per-tensor amax = max |x| for `ntensors` BF16 matrices of M x K (row
  * stride ldx elements) laid out `tensor_stride` elements apart.
  *   x          device, BF16
  *   amax_out   device float[ntensors]; overwritten (it is cleared first).
@@ -233,7 +235,9 @@ int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t k, const i
 int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K, const int32_t *offsets, int32_t E,
                                      const float *amax, int32_t k, int32_t *S_out, double *score_ws, void *stream);
 
-/* The selected weight columns of a rollout weight pack, for a new channel set:
+/* W_hat on S for the correction of QUADS §3.3 Eq. 21 when S changes (online
+ * selection, Eq. 23-24).
+ * The selected weight columns of a rollout weight pack, for a new channel set:
  * w_sel[e, n, s] = bf16(code * sb) of element (n, S[s]) of expert e -- what
  * nvfp4_prepare_weights writes for S -- read from its packed codes and tiled
  * scales (rows in the pack's own order, interleaved or not).
@@ -316,7 +320,8 @@ int nvfp4_gemm_pipeline(int32_t which, int32_t *previous);
 /* top-k softmax MoE)                                                         */
 /* ------------------------------------------------------------------------ */
 
-/* Top-k softmax router.  For each token t: p = softmax(logits[t]) in FP32;
+/* MoE glue (not described by QUADS).
+ * Top-k softmax router.  For each token t: p = softmax(logits[t]) in FP32;
  * ids[t] = the topk experts of largest logit (ties to the lower expert
  * index, in decreasing order), weights[t] = their p (no renormalization).
  * Routed rows are ordered by (expert, token); each expert segment starts at
@@ -329,21 +334,24 @@ int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32_t topk, in
                      float *weights, int32_t *counts, int32_t *offsets, int32_t *dst_row,
                      void *stream);
 
-/* Zero the padding rows [offsets[e]+counts[e], offsets[e+1]) of a routed
+/* MoE glue (not described by QUADS).
+ * Zero the padding rows [offsets[e]+counts[e], offsets[e+1]) of a routed
  * NVFP4 activation (codes [rows_cap, K/2], swizzled scales, resid [rows_cap,
  * k] BF16 or NULL when k = 0), so that padded rows contribute zeros. */
 int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *offsets, int32_t E,
                             int64_t rows_cap, int64_t K, int32_t k, uint8_t *codes,
                             uint8_t *scales, void *resid, void *stream);
 
-/* Copy BF16 token rows x [T, K] to their routed rows y [rows_cap, K]
+/* MoE glue (not described by QUADS).
+ * Copy BF16 token rows x [T, K] to their routed rows y [rows_cap, K]
  * (y[dst_row[t*topk+s]] = x[t]) and zero the padding rows (the QAT path's
  * dispatch).  counts/offsets/dst_row from nvfp4_route_topk. */
 int nvfp4_moe_scatter_rows(const void *x, int32_t T, int64_t K, int32_t topk,
                            const int32_t *dst_row, const int32_t *counts, const int32_t *offsets,
                            int32_t E, int64_t rows_cap, void *y, void *stream);
 
-/* Weighted combine: out[t, :] = sum_{s<topk} weights[t,s] * y[dst_row[t,s], :]
+/* MoE glue (not described by QUADS).
+ * Weighted combine: out[t, :] = sum_{s<topk} weights[t,s] * y[dst_row[t,s], :]
  * in FP32, slots in order.  y is F32 or BF16 (y_dtype) with row stride ldy.
  *   out  device float [T, H] (overwritten). */
 int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t *dst_row,
@@ -363,23 +371,28 @@ int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t
  * transposed weights (nvfp4_transpose_bf16), the weight gradients on
  * nvfp4_bf16_grouped_gemm_wgrad. */
 
-/* y[b] = x[b]^T for `batch` row-major BF16 matrices of rows x cols (y[b] is
+/* Data movement of the trainer backward (QUADS §3.2 Eq. 13).
+ * y[b] = x[b]^T for `batch` row-major BF16 matrices of rows x cols (y[b] is
  * cols x rows).  x and y may not overlap.  Errors: INVALID_ARG, UNSUPPORTED
  * (batch > 65535). */
 int nvfp4_transpose_bf16(const void *x, int32_t batch, int64_t rows, int64_t cols, void *y, void *stream);
 
-/* h = bf16(silu(g) * u) from saved BF16 pre-activations gu = [g | u]
+/* The SwiGLU of the MoE experts (glue, not described by QUADS), on saved
+ * pre-activations for the trainer backward of QUADS §3.2 Eq. 13.
+ * h = bf16(silu(g) * u) from saved BF16 pre-activations gu = [g | u]
  * (rows x 2I, the gate columns first), silu(g) = g / (1 + exp(-g)) in
  * binary32.  h: device BF16 [rows, I].  Errors: INVALID_ARG. */
 int nvfp4_swiglu(const void *gu, int64_t rows, int64_t I, void *h, void *stream);
 
-/* SwiGLU backward: from gu = [g | u] and dh (rows x I, BF16),
+/* Part of the trainer backward of QUADS §3.2 Eq. 13.
+ * SwiGLU backward: from gu = [g | u] and dh (rows x I, BF16),
  * d(gate) = bf16(dh * u * s (1 + g (1 - s))) and d(up) = bf16(dh * g * s),
  * s = 1 / (1 + exp(-g)), in binary32, written as dgu = [dg | du] (rows x 2I).
  * Errors: INVALID_ARG. */
 int nvfp4_swiglu_backward(const void *gu, const void *dh, int64_t rows, int64_t I, void *dgu, void *stream);
 
-/* Backward of nvfp4_moe_combine: dy[dst_row[t,s]] = bf16(weights[t,s] *
+/* Part of the trainer backward of QUADS §3.2 Eq. 13.
+ * Backward of nvfp4_moe_combine: dy[dst_row[t,s]] = bf16(weights[t,s] *
  * dout[t]) for every token t and slot s (rows outside [0, rows_cap) are
  * skipped), the padding rows [offsets[e] + counts[e], offsets[e+1]) of dy set
  * to zero, and, when dweights is not NULL, the combine weights' gradient
@@ -392,7 +405,8 @@ int nvfp4_moe_combine_backward(const float *dout, const void *y, const int32_t *
                                int32_t T, int32_t topk, int64_t H, const int32_t *counts, const int32_t *offsets,
                                int32_t E, int64_t rows_cap, void *dy, float *dweights, void *stream);
 
-/* Grouped weight gradient: dw[e] = a_t[:, seg e] . b_t[:, seg e]^T for every
+/* dW = dW_hat of the straight-through estimator, QUADS §3.2 Eq. 13.
+ * Grouped weight gradient: dw[e] = a_t[:, seg e] . b_t[:, seg e]^T for every
  * expert e, seg e = the routed rows [offsets[e], offsets[e+1]) (tcgen05 BF16
  * MMA, FP32 accumulation over the expert's rows; an expert without rows gets
  * zeros).  The operands are the transposed routed tensors, so the reduction
@@ -412,7 +426,8 @@ int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------ */
 
-/* Runs one CTA that waits, with the library's bounded-wait routine and a
+/* Failure handling (no counterpart in QUADS).
+ * Runs one CTA that waits, with the library's bounded-wait routine and a
  * limit of `limit_us` microseconds (1 .. 10^7), on a pipeline barrier that
  * nothing ever signals; when the limit runs out it writes NVFP4_ERR_TIMEOUT
  * to dev_status and returns normally.  Exercises the timeout path without a

@@ -120,3 +120,16 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(nv, "LIB", str(tmp_path / "absent.so"))
     with pytest.raises(RuntimeError):
         nv.load()
+
+
+def test_every_entry_point_cites_its_passage():
+    """Each declaration's own comment names the passage that defines it (QUADS
+    section / equation) or says that the paper has no counterpart."""
+    import re
+
+    h = open(HEADER).read()
+    for m in re.finditer(r"\n(?:int|const char \*)\s+(nvfp4_\w+)\(", h):
+        start, end = h.rfind("/*", 0, m.start()), h.rfind("*/", 0, m.start())
+        comment = h[start:end]
+        assert start >= 0 and end > start and (
+            "QUADS" in comment or "no counterpart" in comment or "not described" in comment), m.group(1)
