@@ -56,3 +56,20 @@ def test_single_process_needs_no_collective():
 
 
 PORT = _free_port()
+
+
+def test_gate_up_traffic_is_null_once_the_sources_change(monkeypatch):
+    """The recorded DRAM traffic of the gate_up GEMM belongs to the sources it was
+    captured on: bench.py reports it only while their hash matches."""
+    import bench
+
+    assert bench.gate_up_traffic() in (bench.GATE_UP_TRAFFIC["bytes"], None)
+    monkeypatch.setitem(bench.GATE_UP_TRAFFIC, "sources_sha256", "0" * 64)
+    assert bench.gate_up_traffic() is None
+
+
+def test_job_value_counts_all_ranks_units():
+    import bench
+
+    assert bench.job_value(1e12, 4, 2.0) == 4 * 1e12 / 2e-3
+    assert bench.job_time(3.0, 1) == 3.0
