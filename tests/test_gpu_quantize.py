@@ -104,6 +104,17 @@ def test_quantize_ragged_shapes(M, K):
     _check_against_oracle(synth.u16(x), S)
 
 
+def test_quantize_maximum_width_and_unstaged_residual():
+    """K = 16384 (the largest row the quantizer takes) with k = 1040 selected
+    channels: more than the per-warp stage holds, so the residual goes straight
+    to the destination rows from the row's block scales."""
+    rng = np.random.default_rng(77)
+    M, K, k = 40, 16384, 1040
+    x = torch.from_numpy(rng.standard_t(3, (M, K)).astype(np.float32)).to(torch.bfloat16)
+    S = np.sort(rng.choice(K, k, replace=False)).astype(np.int32)
+    _check_against_oracle(synth.u16(x), S)
+
+
 def test_element_encoder_all_bf16_values():
     # gs = 1 (amax 2688) and every block's first element 6 -> block scale 1.0,
     # so each element is rounded to E2M1 as is: this covers every BF16 value in
