@@ -30,7 +30,7 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core ratio, nominal
 
 
 # DRAM bytes (read + write) of one gate_up GEMM launch at this workload's launch shape, from
-# one ncu capture (profiles/single_gemm_kernel_moe_prefill.md), valid only for the kernel
+# one ncu capture of the gemm13_moe profile case, valid only for the kernel
 # sources it was taken on (common.cuh, gemm_common.cuh, gemm_single.cu): reported as null
 # once they change.
 GATE_UP_TRAFFIC = {"bytes": 1362286000 + 415321088,

@@ -116,8 +116,9 @@ int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensor
  * gives a signed zero code); dequant = (code*sb)*gs in binary32.
  * Output rows not named by dst_row are left untouched (see
  * nvfp4_moe_clear_padding).  dev_status gets NONFINITE if amax is not finite.
- * Errors: INVALID_ARG, ALIGNMENT (pointers; ldx % 8), UNSUPPORTED (K % 32,
- * k % 8, fanout < 1). */
+ * Errors: INVALID_ARG (null pointers, negative sizes, fanout < 1),
+ * ALIGNMENT (pointers; ldx % 8), UNSUPPORTED (K % 32, K > 16384, k % 8,
+ * fanout > 32). */
 int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float *amax,
                    float *gs_out, const int32_t *S, int32_t k, const int32_t *dst_row,
                    int32_t fanout, int64_t rows_out, uint8_t *codes, uint8_t *scales,
@@ -156,7 +157,10 @@ int nvfp4_fake_quant_transposed(const void *w, int32_t ntensors, int64_t rows, i
  *     (nvfp4_last_error() says why) and launch nothing.
  *   - The first call on a device, with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress); make that first call
- *     before any stream capture begins.
+ *     before any stream capture begins.  The address is kept per device and
+ *     CUDA context: after a cudaDeviceReset the next call looks it up again
+ *     (so, again, make that call outside any capture).
+ *   - Device ordinals above 63 return NVFP4_ERR_ARCH, as every entry point.
  *   - Every call shares the one array: the slots a call uses are cleared on
  *     `stream` before use, and keep that call's amax values afterwards.  Calls
  *     whose work can overlap on the GPU (different streams without ordering

@@ -26,7 +26,10 @@ int ensure_init() {
         set_last_error("cudaGetDevice", e);
         return NVFP4_ERR_ARCH;
     }
-    if (dev < 0 || dev >= 64) return NVFP4_ERR_ARCH;
+    if (dev < 0 || dev >= 64) {
+        set_last_error_text("the library supports device ordinals 0..63");
+        return NVFP4_ERR_ARCH;
+    }
     if (g_dev_ok[dev] == 0) {
         int major = 0, minor = 0, sms = 0;
         if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
@@ -50,6 +53,20 @@ int ensure_init() {
         g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     return NVFP4_OK;
+}
+
+void *current_context() {
+    static PFN_cuCtxGetCurrent_v4000 get = nullptr;
+    if (!get) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return nullptr;
+        get = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+    }
+    CUcontext c = nullptr;
+    return get(&c) == CUDA_SUCCESS ? (void *)c : nullptr;
 }
 
 int sm_count() {

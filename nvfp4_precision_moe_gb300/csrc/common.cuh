@@ -24,6 +24,9 @@ void set_last_error_text(const char *text);
 int ensure_init();
 // Number of SMs of the current device (cached).
 int sm_count();
+// The calling thread's current CUDA context (a driver handle; NULL if none or
+// if the driver call is unavailable).
+void *current_context();
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 int encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint64_t inner,
                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,

@@ -951,7 +951,8 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
         return NVFP4_ERR_INVALID_ARG;
     if (k > 0 && (!S || !resid)) return NVFP4_ERR_INVALID_ARG;
     if (!dst_row && (fanout != 1 || rows_out < M)) return NVFP4_ERR_INVALID_ARG;
-    if (K % 32 || k % 8 || K / 16 > kMaxBlocksPerRow) return NVFP4_ERR_UNSUPPORTED;
+    // a row's destinations are resolved into 32 per-warp slots
+    if (K % 32 || k % 8 || K / 16 > kMaxBlocksPerRow || fanout > 32) return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(x) || ldx % 8 || !aligned16(codes) || !aligned16(scales) || (resid && !aligned16(resid)))
         return NVFP4_ERR_ALIGNMENT;
     if (M == 0) return NVFP4_OK;
@@ -1192,20 +1193,30 @@ extern "C" int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, co
 namespace nvfp4 {
 constexpr int kNoAllocMaxTensors = 4096;  // 16 KB per GPU that loads the library
 static __device__ __align__(256) float g_noalloc_amax[kNoAllocMaxTensors];
-static float *g_noalloc_addr[64];  // device address of the array, per device
+// device address of the array per device ordinal, and the CUDA context it was looked up in
+static float *g_noalloc_addr[64];
+static void *g_noalloc_ctx[64];
 static std::mutex g_noalloc_mu;
 
 // The array's name in host code is not a device address: look the address up
-// once per device, with that device current, and pass it to the kernels.
+// with the device current, the first time a device is used, and pass it to
+// the kernels.  A device reset gives the device a new context in which the
+// array may sit elsewhere, so the cached address is keyed by the context too
+// and looked up again when that changes.
 static int noalloc_scratch(float **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    if (e != cudaSuccess) {
         set_last_error("cudaGetDevice", e);
         return NVFP4_ERR_CUDA;
     }
+    if (dev < 0 || dev >= 64) {
+        set_last_error_text("nvfp4_fake_quant_noalloc: the library supports device ordinals 0..63");
+        return NVFP4_ERR_ARCH;
+    }
+    void *ctx = current_context();
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
+    if (!g_noalloc_addr[dev] || g_noalloc_ctx[dev] != ctx) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_amax);
         if (e != cudaSuccess || !p) {
@@ -1213,6 +1224,7 @@ static int noalloc_scratch(float **out) {
             return NVFP4_ERR_CUDA;
         }
         g_noalloc_addr[dev] = static_cast<float *>(p);
+        g_noalloc_ctx[dev] = ctx;
     }
     *out = g_noalloc_addr[dev];
     return NVFP4_OK;

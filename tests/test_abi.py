@@ -81,6 +81,14 @@ def test_host_checks_without_gpu(lib):
     assert q(PM, 4, 64, 64, P, None, None, 0, None, 1, 4, P, P, None, None, None) == ALIGN
     assert q(P, 4, 64, 64, P, None, P, 8, None, 1, 4, P, P, None, None, None) == INVALID  # k>0, no resid
     assert q(P, 4, 64, 64, P, None, None, 0, None, 2, 4, P, P, None, None, None) == INVALID  # fanout w/o map
+    # a row's destinations live in 32 per-warp slots: more than 32 is refused before any launch
+    assert q(P, 4, 64, 64, P, None, None, 0, P, 33, 4 * 33, P, P, None, None, None) == UNSUP
+    fq = lib.nvfp4_fake_quant_noalloc
+    # w, ntensors, rows, cols, w_hat, gs_out, dev_status, stream
+    assert fq(P, 2, 16, 48, P, None, None, None) == UNSUP  # cols % 32
+    assert fq(P, 4097, 16, 64, P, None, None, None) == UNSUP  # beyond its 4096-slot array
+    assert b"4096" in lib.nvfp4_last_error()
+    assert fq(PM, 2, 16, 64, P, None, None, None) == ALIGN
     g = lib.nvfp4_w4a4_rac_grouped_gemm
     args = [P, P, None, P, P, P, P, None, 0, P, 1, 128, 256, 256, 0, 0, P, 256, None, None, None]
     bad_k = list(args)

@@ -46,6 +46,24 @@ def test_noalloc_fake_quant_matches_allocating_entry_point():
         assert torch.equal(gs_got, gs_ref)
 
 
+def test_noalloc_without_optional_outputs():
+    """gs_out and dev_status are optional: the same w_hat comes out without them."""
+    import nvfp4_precision_moe_gb300 as nv
+
+    L = nv.load(build=True)
+    stream = torch.cuda.current_stream().cuda_stream
+    nt, rows, cols = 2, 64, 256
+    w = _inputs(3, nt, rows, cols, 3.0)
+    ref = torch.empty_like(w)
+    got = torch.empty_like(w)
+    amax_ws = torch.zeros(nt, dtype=torch.float32, device="cuda:0")
+    assert L.nvfp4_fake_quant(w.data_ptr(), nt, rows, cols, ref.data_ptr(), None, amax_ws.data_ptr(), None,
+                              stream) == 0
+    assert L.nvfp4_fake_quant_noalloc(w.data_ptr(), nt, rows, cols, got.data_ptr(), None, None, stream) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
 def test_noalloc_rejects_more_tensors_than_its_array():
     import nvfp4_precision_moe_gb300 as nv
 
