@@ -1,7 +1,8 @@
-"""Parity at the benchmark's full size, in the launch configuration bench.py
-times: the prefill workload (16384 tokens, hidden 4096, 128 experts top-8 with
-Zipf routing, intermediate 1536, k = 128 on both projections) through
-RolloutMoE.forward, checked stage by stage on sampled rows.  Each stage's GPU
+"""Parity at full size, in the launch configuration bench.py times: the
+prefill workload (16384 tokens, hidden 4096, 128 experts top-8 with Zipf
+routing, intermediate 1536, k = 128 on both projections) and the decode
+workload (2048 tokens, hidden 2048, 64 experts top-8, intermediate 768,
+k = 64) through RolloutMoE.forward, checked stage by stage on sampled rows.  Each stage's GPU
 output is compared with the oracle applied to the previous stage's GPU output:
 
 * quantize x: gs exact; codes, block scales (read back through the tiled
@@ -28,34 +29,27 @@ TOL_BF16 = 2.0 ** -8 + 1e-3
 
 
 def _scale_rows(sw, rows, K):
-    """Canonical [len(rows), K/16] block scales of `rows` from the tiled layout
-    of the header: row m, block kb at ((m/128)*ceil(K/256) + kb/16)*2048 +
-    (m%128)*16 + kb%16."""
-    kt = (K // 16 + 15) // 16
-    kb = np.arange(K // 16)
-    out = np.empty((len(rows), K // 16), np.uint8)
-    for i, m in enumerate(rows):
-        idx = ((m // 128) * kt + kb // 16) * 2048 + (m % 128) * 16 + kb % 16
-        out[i] = sw[idx]
-    return out
+    """Canonical [len(rows), K/16] block scales of `rows` read back from the
+    scale layout of the header (through the oracle's layout)."""
+    return oracle.scale_rows(sw, rows, K)
 
 
-@pytest.fixture(scope="module")
-def layer_run():
+@pytest.fixture(scope="module", params=[5, 3], ids=["moe_prefill", "moe_decode"])
+def layer_run(request):
     import nvfp4_precision_moe_gb300 as nv
     import bench
 
     nv.load(build=True)
     dev = torch.device(G.DEV)
-    c, layer, x, logits, _ = bench.build_workload(dev)
+    c, layer, x, logits, _ = bench.build_workload(dev, request.param)
     out = layer.forward(x, logits)
     torch.cuda.synchronize()
     G.status_ok(layer.dev_status)
-    return c, layer, x, out
+    return request.param, c, layer, x, out
 
 
 def test_full_size_stage_parity(layer_run):
-    c, layer, x, out = layer_run
+    cfg, c, layer, x, out = layer_run
     T, H, E, I, topk, k = c["T"], c["H"], c["E"], c["I"], c["topk"], c["k"]
     r = layer.route
     ids = r.ids.cpu().numpy()
@@ -111,7 +105,7 @@ def test_full_size_stage_parity(layer_run):
         tk = tok_of_row[rr]
         assert (tk >= 0).all()
         ca, sa, ra, _ = oracle.quantize(xu[tk], gs=gs_x, S=S13)
-        cw, sw, _, gw = oracle.quantize(synth.u16(synth.expert_weight(5, e, "w13")))
+        cw, sw, _, gw = oracle.quantize(synth.u16(synth.expert_weight(cfg, e, "w13")))
         y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, gs_x), oracle.dequantize_exact(cw, sw, gw), ra, S13, gs_x)
         ref = oracle.swiglu(y, I)
         assert G.rel_err(oracle.bf16_to_f32(h_all[rr]), ref) <= TOL_BF16, e
@@ -131,7 +125,7 @@ def test_full_size_stage_parity(layer_run):
     y_all = layer.y
     for e, rr in samples:
         ch, sh, rh, _ = oracle.quantize(h_all[rr], gs=gs_h, S=Sd)
-        cw, sw, _, gw = oracle.quantize(synth.u16(synth.expert_weight(5, e, "down")))
+        cw, sw, _, gw = oracle.quantize(synth.u16(synth.expert_weight(cfg, e, "down")))
         ref = oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gs_h), oracle.dequantize_exact(cw, sw, gw), rh, Sd, gs_h)
         got = y_all[torch.from_numpy(rr).to(G.DEV)].float().cpu().numpy()
         assert G.rel_err(got, ref) <= TOL_BF16, e

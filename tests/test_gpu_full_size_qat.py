@@ -78,10 +78,9 @@ def test_forward_sampled_rows(qat):
     xr, h, y = L.xr, L.h, L.y
     for e in qat["experts"]:
         rr = torch.from_numpy(_rows(L, e, rng)).to(G.DEV)
-        W13, Wd = f64(L.w13_hat[e]), f64(L.wd_hat[e])
-        ref_h = oracle.swiglu(f64(xr[rr]) @ W13.T, I)
+        ref_h = oracle.swiglu(oracle.bf16_gemm(G.u16(xr[rr]), G.u16(L.w13_hat[e])), I)
         assert G.rel_err(f64(h[rr]), ref_h) <= TOL_BF16, e
-        assert G.rel_err(f64(y[rr]), f64(h[rr]) @ Wd.T) <= TOL_BF16, e
+        assert G.rel_err(f64(y[rr]), oracle.bf16_gemm(G.u16(h[rr]), G.u16(L.wd_hat[e]))) <= TOL_BF16, e
     T, topk = qat["c"]["T"], qat["c"]["topk"]
     toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
     dst = L.route.dst_row.cpu().numpy()[toks]
@@ -99,11 +98,13 @@ def test_training_step_gradients(qat):
         r0, r1 = int(offs[e]), int(offs[e + 1])  # the whole segment, padding rows included (zero)
         seg = torch.arange(r0, r1, device=G.DEV)
         dy, h, dgu, xr = f64(L.dy[seg]), f64(L.h[seg]), f64(L.dgu[seg]), f64(L.xr[seg])
-        assert G.rel_err(f64(qat["dwd"][e]), dy.T @ h) <= 1e-5, e
-        assert G.rel_err(f64(qat["dw13"][e]), dgu.T @ xr) <= 1e-5, e
+        one = np.array([0, r1 - r0])
+        assert G.rel_err(f64(qat["dwd"][e]), oracle.segment_wgrad(dy, h, one)[0]) <= 1e-5, e
+        assert G.rel_err(f64(qat["dw13"][e]), oracle.segment_wgrad(dgu, xr, one)[0]) <= 1e-5, e
         rr = torch.from_numpy(_rows(L, e, rng)).to(G.DEV)
-        assert G.rel_err(f64(L.dh[rr]), f64(L.dy[rr]) @ f64(L.wd_hat[e])) <= TOL_BF16, e
-        assert G.rel_err(f64(L.dxr[rr]), f64(L.dgu[rr]) @ f64(L.w13_hat[e])) <= TOL_BF16, e
+        # dh = dY . Wd_hat and dx = d(gate|up) . W13_hat: products with the transposed weights
+        assert G.rel_err(f64(L.dh[rr]), oracle.bf16_gemm(G.u16(L.dy[rr]), G.u16(L.wd_t[e]))) <= TOL_BF16, e
+        assert G.rel_err(f64(L.dxr[rr]), oracle.bf16_gemm(G.u16(L.dgu[rr]), G.u16(L.w13_t[e]))) <= TOL_BF16, e
     T, topk = qat["c"]["T"], qat["c"]["topk"]
     toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
     dst = L.route.dst_row.cpu().numpy()[toks]
