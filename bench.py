@@ -138,23 +138,27 @@ def job_value(units_per_rank, world, ms_job):
     return world * units_per_rank / (ms_job * 1e-3)
 
 
-def build_workload(dev):
+def build_workload(dev, cfg=WORKLOAD):
+    """A rollout MoE workload on `dev`: seeded activations, logits and expert
+    weights, RAC channel sets calibrated on an independent batch (x: the
+    calibration batch; h: the calibration batch's own h), and the layer with
+    its weights prepared."""
     import torch
 
     import nvfp4_precision_moe_gb300 as nv
     import synth
 
-    c = synth.CONFIGS[WORKLOAD]
+    c = synth.CONFIGS[cfg]
     E, H, I, T, topk, k = c["E"], c["H"], c["I"], c["T"], c["topk"], c["k"]
-    x = synth.activations(WORKLOAD).to(dev)
-    logits = synth.router_logits(WORKLOAD).to(dev)
+    x = synth.activations(cfg).to(dev)
+    logits = synth.router_logits(cfg).to(dev)
     w13 = torch.empty((E, 2 * I, H), dtype=torch.bfloat16, device=dev)
     wd = torch.empty((E, H, I), dtype=torch.bfloat16, device=dev)
     for e in range(E):
-        w13[e].copy_(synth.expert_weight(WORKLOAD, e, "w13"))
-        wd[e].copy_(synth.expert_weight(WORKLOAD, e, "down"))
+        w13[e].copy_(synth.expert_weight(cfg, e, "w13"))
+        wd[e].copy_(synth.expert_weight(cfg, e, "down"))
     # channel calibration (offline, Eq. 23-24) on an independent calibration batch
-    xc = synth.activations(WORKLOAD, batch=1).to(dev)
+    xc = synth.activations(cfg, batch=1).to(dev)
     amax = torch.zeros(1, dtype=torch.float32, device=dev)
     nv.nvfp4_amax(xc, amax)
     S13 = torch.empty(k, dtype=torch.int32, device=dev)
@@ -163,7 +167,7 @@ def build_workload(dev):
     g = torch.Generator().manual_seed(5)
     Sd0 = torch.sort(torch.randperm(I, generator=g)[:k]).values.to(torch.int32).to(dev)
     cal = nv.RolloutMoE(w13, wd, S13, Sd0, topk, T)
-    cal.forward(xc, synth.router_logits(WORKLOAD).roll(1, 0).to(dev))
+    cal.forward(xc, synth.router_logits(cfg).roll(1, 0).to(dev))
     hmax = torch.zeros(1, dtype=torch.float32, device=dev)
     nv.nvfp4_amax(cal.h, hmax)
     Sd = torch.empty(k, dtype=torch.int32, device=dev)
@@ -192,7 +196,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
 
     # per-stage events of one step (all launches are on `stream`)
-    nstage = 8
+    nstage = 9
 
     def step(ev=None):
         layer.forward(x, logits, mark=(lambda i: ev[i].record(stream)) if ev is not None else None)
@@ -221,10 +225,10 @@ def run_ours(args):
     ms = t0.elapsed_time(t1)
     ms = job_time(ms, world, dev)
     ms_step = ms / args.steps
-    names = ["route", "amax_x", "quantize_x", "gemm_gate_up", "quantize_h", "gemm_down", "combine"]
+    names = ["route", "amax_x", "quantize_x", "clear_padding", "gemm_gate_up", "quantize_h", "gemm_down", "combine"]
     stage = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)])
              for j, n in enumerate(names)}
-    gemm13_ms = statistics.mean([evs[i][3].elapsed_time(evs[i][4]) for i in range(args.steps)])
+    gemm13_ms = statistics.mean([evs[i][4].elapsed_time(evs[i][5]) for i in range(args.steps)])
 
     # ---- end to end through host buffers: each step's inputs H2D from pinned
     # memory and its FP32 result D2H, all inside the timed region.  Copies run
@@ -289,6 +293,9 @@ def run_ours(args):
     R = T * c["topk"]
     q_bytes = 2 * T * H + R * (H // 2 + H // 16 + 2 * k)  # read x, write routed codes/scales/residual
     q_gbs = q_bytes / (stage["quantize_x"] * 1e-3) / 1e9
+    rows_h = layer.rows_cap
+    qh_bytes = rows_h * (2 * I + I // 2 + I // 16 + 2 * k)  # read h (all rows_cap rows), write codes/scales/residual
+    qh_gbs = qh_bytes / (stage["quantize_h"] * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -298,6 +305,7 @@ def run_ours(args):
                    "l2": "no flush: every step streams ~3 GB, far more than the 129 MB L2"},
         "fp4_peak_frac_step": round(world * f4 / (ms_step * 1e-3) / 1e12 / fp4_peak, 4),
         "quantize_x": {"gbs": round(q_gbs, 1), "hbm_frac": round(q_gbs / pk["hbm"], 4), "bytes": q_bytes},
+        "quantize_h": {"gbs": round(qh_gbs, 1), "hbm_frac": round(qh_gbs / pk["hbm"], 4), "bytes": qh_bytes},
         "stages_ms": {n: round(v, 4) for n, v in stage.items()},
         "roofline": {"kernel": "single_gemm_kernel<fp4> (gate_up, SwiGLU)", "bound": "tensor",
                      "achieved": round(gemm13_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
@@ -311,6 +319,8 @@ def run_ours(args):
         "clocks": clk,
     }
     if rank == 0:
+        out["decode"] = decode_measure(dev, max(3, min(args.steps, 20)), pk)
+        out["quantize_dense"] = quantize_dense_measure(dev, pk)
         out["qat"] = qat_measure(dev, max(3, min(args.steps, 10)))
         out["mismatch"] = mismatch_measure(layer, x, logits, *w_bf16)
         out["cpu_baseline"] = cpu_baseline(seconds=args.cpu_seconds)
@@ -318,6 +328,105 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def decode_measure(dev, steps, pk):
+    """The rollout decode workload (2048 tokens top-8 over 64 experts, hidden
+    2048, intermediate 768, k = 64; QUADS §4.4.2 Fig. 9a measures rollout
+    decode): layer step time and per-stage CUDA events, inputs resident.  The
+    two GEMMs are bound by the bytes they move (the weights of all 64 experts
+    for about 256 routed rows each), so they are reported as GB/s of those
+    algorithmic bytes against the measured HBM bandwidth: weight codes and
+    scales, the selected weight columns, the routed A operands (codes, scales,
+    residual) and the outputs (h, y), each once."""
+    import torch
+
+    import synth
+
+    c, layer, x, logits, _ = build_workload(dev, 3)
+    T, H, E, I, k, topk = c["T"], c["H"], c["E"], c["I"], c["k"], c["topk"]
+    stream = torch.cuda.current_stream()
+    for _ in range(3):
+        layer.forward(x, logits)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        layer.forward(x, logits, mark=lambda j, i=i: evs[i][j].record(stream))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    ms = t0.elapsed_time(t1) / steps
+    names = ["route", "amax_x", "quantize_x", "clear_padding", "gemm_gate_up", "quantize_h", "gemm_down", "combine"]
+    stage = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)])
+             for j, n in enumerate(names)}
+    rows = int(layer.route.offsets[-1].item())  # routed rows incl. segment padding
+    w_bytes = E * (2 * I * (H // 2 + H // 16 + 2 * k) + H * (I // 2 + I // 16 + 2 * k))
+    a_bytes = rows * (H // 2 + H // 16 + 2 * k) + rows * (I // 2 + I // 16 + 2 * k)
+    o_bytes = rows * I * 2 + rows * H * 2
+    g_bytes = w_bytes + a_bytes + o_bytes
+    g_ms = stage["gemm_gate_up"] + stage["gemm_down"]
+    f4, fb = synth.flops_moe(3)
+    return {"workload": "moe_decode T=2048 H=2048 E=64 top8 I=768 k=64", "ms_per_step": round(ms, 4),
+            "tflops": round((f4 + fb) / (ms * 1e-3) / 1e12, 1),
+            "stages_ms": {n: round(v, 4) for n, v in stage.items()},
+            "gemm_bytes": g_bytes, "gemm_gbs": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
+            "gemm_hbm_frac": round(g_bytes / (g_ms * 1e-3) / 1e9 / pk["hbm"], 4),
+            "what": "both W4A4+RAC GEMMs: weights (codes, scales, selected columns) + routed A operands + "
+                    "outputs, once each, over the two GEMMs' CUDA-event time"}
+
+
+def quantize_dense_measure(dev, pk, reps=20):
+    """nvfp4_quantize alone on the dense decode workload's X (256 x 4096
+    Student-t with outliers, k = 128 RAC channels: a latency-class launch,
+    reported in microseconds) and W (4096 x 4096, no residual: GB/s of read
+    2NK + written NK/2 + NK/16 bytes against the measured HBM bandwidth).
+    Both fit in L2, so a 512 MB buffer is overwritten between timed launches
+    and each launch is timed on its own."""
+    import torch
+
+    import nvfp4_precision_moe_gb300 as nv
+    import synth
+
+    x = synth.activations(2).to(dev)
+    w = synth.dense_weight(2).to(dev)
+    M, K = x.shape
+    N = w.shape[0]
+    xc = synth.activations(2, batch=1).to(dev)
+    amax = torch.zeros(1, dtype=torch.float32, device=dev)
+    nv.nvfp4_amax(xc, amax)
+    S = torch.empty(128, dtype=torch.int32, device=dev)
+    nv.nvfp4_rac_select_channels(xc, amax, 128, S, torch.empty(K, dtype=torch.float64, device=dev))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    res = {}
+    for name, t, SS in (("x", x, S), ("w", w, None)):
+        rows, cols = t.shape
+        am = torch.zeros(1, dtype=torch.float32, device=dev)
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty(nv.scale_bytes(rows, cols), dtype=torch.uint8, device=dev)
+        resid = torch.empty((rows, 128), dtype=torch.bfloat16, device=dev) if SS is not None else None
+        nv.nvfp4_amax(t, am)
+        ts = {"quantize": [], "amax+quantize": []}
+        for r in range(reps + 3):
+            for key in ts:
+                flush.fill_(r & 255)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if key == "amax+quantize":
+                    nv.nvfp4_amax(t, am)
+                nv.nvfp4_quantize(t, am, codes, scales, resid=resid, S=SS)
+                e1.record()
+                torch.cuda.synchronize()
+                if r >= 3:
+                    ts[key].append(e0.elapsed_time(e1))
+        qb = 2 * rows * cols + rows * cols // 2 + rows * cols // 16 + (2 * rows * 128 if SS is not None else 0)
+        med = {kk: statistics.median(v) for kk, v in ts.items()}
+        res[name] = {"shape": [rows, cols], "k": 128 if SS is not None else 0,
+                     "us": round(med["quantize"] * 1e3, 2), "us_with_amax": round(med["amax+quantize"] * 1e3, 2),
+                     "bytes": qb, "gbs": round(qb / (med["quantize"] * 1e-3) / 1e9, 1),
+                     "hbm_frac": round(qb / (med["quantize"] * 1e-3) / 1e9 / pk["hbm"], 4)}
+    res["l2"] = "a 512 MB buffer is overwritten between timed launches (cold L2)"
+    return res
 
 
 def build_qat_workload(dev):
@@ -483,14 +592,11 @@ def mismatch_measure(layer, x, logits, w13, wd):
     return res
 
 
-_ORACLE_WEIGHTS = {}
-
-
-def cpu_baseline(seconds=10.0, rows=None):
-    """The oracle as it stands (plain C, one thread) on a bounded sample of the
-    workload: batches of routed rows of one expert through both W4A4+RAC
-    projections, repeated until `seconds` of oracle time have run (one batch
-    when 0).  Returns TFLOP/s of GEMM work."""
+def _oracle_worker(rows, barrier, in_q, out_q):
+    """One host core of the CPU baseline: prepares one expert's weights with the
+    plain C oracle (not timed), then for every request runs batches of `rows`
+    routed rows of that expert through both W4A4+RAC projections for the
+    requested seconds (one batch when 0), starting with the other workers."""
     import numpy as np
 
     import oracle
@@ -498,56 +604,112 @@ def cpu_baseline(seconds=10.0, rows=None):
 
     c = synth.CONFIGS[WORKLOAD]
     H, I, k = c["H"], c["I"], c["k"]
-    t_start = time.perf_counter()
-    n = rows or 64
-    x = synth.u16(synth.activations(WORKLOAD, rows=n))
+    x = synth.u16(synth.activations(WORKLOAD, rows=rows))
     S13 = np.arange(0, H, H // k, dtype=np.int32)
     Sd = np.arange(0, I, I // k, dtype=np.int32)
-    if "w" not in _ORACLE_WEIGHTS:  # the weight pack is per weight update: not timed
-        cw, sw, _, gw = oracle.quantize(synth.u16(synth.expert_weight(WORKLOAD, 0, "w13")))
-        cd, sd, _, gd = oracle.quantize(synth.u16(synth.expert_weight(WORKLOAD, 0, "down")))
-        _ORACLE_WEIGHTS["w"] = (oracle.dequantize_exact(cw, sw, gw), oracle.dequantize_exact(cd, sd, gd))
-    wq13, wqd = _ORACLE_WEIGHTS["w"]
-    dt, batches = 0.0, 0
-    while batches == 0 or dt < seconds:
-        t0 = time.perf_counter()
-        ca, sa, ra, ga = oracle.quantize(x, S=S13)
-        y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, ga), wq13, ra, S13, ga)
-        h = oracle.bf16_round(oracle.swiglu(y, I).astype(np.float32))
-        ch, sh, rh, gh = oracle.quantize(h, S=Sd)
-        oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gh), wqd, rh, Sd, gh)
-        dt += time.perf_counter() - t0
-        batches += 1
-    fl = batches * (2 * n * (2 * I) * (H + k) + 2 * n * H * (I + k))
-    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": "%d x %d routed rows of one expert: quantize x, W4A4+RAC gate_up, SwiGLU, quantize h, "
-                      "W4A4+RAC down; plain C oracle, 1 thread (%.1f s timed)" % (batches, n, dt),
-            "seconds": round(time.perf_counter() - t_start, 2)}
+    cw, sw, _, gw = oracle.quantize(synth.u16(synth.expert_weight(WORKLOAD, 0, "w13")))
+    cd, sd, _, gd = oracle.quantize(synth.u16(synth.expert_weight(WORKLOAD, 0, "down")))
+    wq13, wqd = oracle.dequantize_exact(cw, sw, gw), oracle.dequantize_exact(cd, sd, gd)
+    while True:
+        seconds = in_q.get()
+        if seconds is None:
+            return
+        barrier.wait()
+        t_start = time.perf_counter()
+        batches = 0
+        while batches == 0 or time.perf_counter() - t_start < seconds:
+            ca, sa, ra, ga = oracle.quantize(x, S=S13)
+            y = oracle.rac_gemm(oracle.dequantize_exact(ca, sa, ga), wq13, ra, S13, ga)
+            h = oracle.bf16_round(oracle.swiglu(y, I).astype(np.float32))
+            ch, sh, rh, gh = oracle.quantize(h, S=Sd)
+            oracle.rac_gemm(oracle.dequantize_exact(ch, sh, gh), wqd, rh, Sd, gh)
+            batches += 1
+        dt = time.perf_counter() - t_start
+        out_q.put((batches * (2 * rows * (2 * I) * (H + k) + 2 * rows * H * (I + k)), dt, batches))
+
+
+class OraclePool:
+    """The CPU baseline's processes: one per host core (the oracle is single-
+    threaded), spawned -- never forked from a process that holds a CUDA
+    context -- and kept for several runs."""
+
+    def __init__(self, rows, workers=None):
+        import multiprocessing as mp
+
+        from oracle.build import build_oracle
+
+        build_oracle()
+        self.rows = rows
+        self.cores = os.cpu_count() or 1
+        self.workers = workers or self.cores
+        ctx = mp.get_context("spawn")
+        self.barrier = ctx.Barrier(self.workers)
+        self.out_q = ctx.Queue()
+        self.in_q = [ctx.Queue() for _ in range(self.workers)]
+        self.procs = [ctx.Process(target=_oracle_worker, args=(rows, self.barrier, q, self.out_q), daemon=True)
+                      for q in self.in_q]
+        for p in self.procs:
+            p.start()
+
+    def run(self, seconds):
+        """TFLOP/s of GEMM work summed over the processes, all running at once."""
+        for q in self.in_q:
+            q.put(seconds)
+        res = [self.out_q.get() for _ in self.procs]
+        rate = sum(fl / dt for fl, dt, _ in res)
+        batches = sum(b for _, _, b in res)
+        dt = max(dt for _, dt, _ in res)
+        return {"value": round(rate / 1e12, 6), "unit": "TFLOP/s", "cores": self.workers,
+                "host_cores": self.cores, "kind": "oracle",
+                "sample": "%d processes x batches of %d routed rows of one expert (%d batches in all, %.2f s): "
+                          "quantize x, W4A4+RAC gate_up, SwiGLU, quantize h, W4A4+RAC down; plain C oracle, "
+                          "one thread per process" % (self.workers, self.rows, batches, dt)}
+
+    def close(self):
+        for q in self.in_q:
+            q.put(None)
+        for p in self.procs:
+            p.join()
+
+
+def cpu_baseline(seconds=10.0, rows=64):
+    """The oracle as it stands, timed on every host core at once on a bounded
+    sample of the workload (see OraclePool)."""
+    t_start = time.perf_counter()
+    pool = OraclePool(rows)
+    try:
+        out = pool.run(seconds)
+    finally:
+        pool.close()
+    out["seconds"] = round(time.perf_counter() - t_start, 2)
+    return out
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    from oracle.build import build_oracle
-
-    build_oracle()
     vals = []
-    for _ in range(args.warmup):
-        cpu_baseline(seconds=0, rows=32)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        vals.append(cpu_baseline(seconds=0, rows=32))
-    wall = time.perf_counter() - t0
+    pool = OraclePool(32)
+    try:
+        for _ in range(args.warmup):
+            pool.run(0)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            vals.append(pool.run(0))
+        wall = time.perf_counter() - t0
+    finally:
+        pool.close()
     v = statistics.median(x["value"] for x in vals)
     out = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / args.steps * 1e3, 2),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
            "data": "synthetic",
            "config": {"workload": "moe_prefill T=16384 H=4096 E=128 top8 zipf1.1 I=1536 k=128",
-                      "sample": "32 routed rows of one expert per step (the CPU oracle)"},
-           "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                            "sample": vals[0]["sample"]},
+                      "sample": "32 routed rows of one expert per process per step (the CPU oracle, one "
+                                "process per host core)"},
+           "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": vals[0]["cores"],
+                            "host_cores": vals[0]["host_cores"], "kind": "oracle", "sample": vals[0]["sample"]},
            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
@@ -567,6 +729,7 @@ def run_profile_case(args):
     import nvfp4_precision_moe_gb300 as nv
 
     nv.load(build=True)
+    nv.nvfp4_gemm_pipeline({"auto": 0, "single": 1, "pair": 2}[args.pipeline])
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev)
     g.manual_seed(7)
@@ -593,10 +756,11 @@ def run_profile_case(args):
         N, K = (3072, 4096) if case == "gemm13" else (4096, 1536)
         k = 128
         a = torch.randint(0, 256, (rows, K // 2), dtype=torch.uint8, device=dev, generator=g)
-        a_s = torch.randint(0x28, 0x40, (rows * K // 16,), dtype=torch.uint8, device=dev, generator=g)
+        a_s = torch.randint(0x28, 0x40, (nv.scale_bytes(rows, K),), dtype=torch.uint8, device=dev, generator=g)
         r = (torch.randn((rows, k), device=dev, generator=g) * 0.1).to(torch.bfloat16)
         w = torch.randint(0, 256, (E, N, K // 2), dtype=torch.uint8, device=dev, generator=g)
-        w_s = torch.randint(0x28, 0x40, (E * N * K // 16,), dtype=torch.uint8, device=dev, generator=g)
+        w_s = torch.randint(0x28, 0x40, (E * nv.scale_bytes(N, K),), dtype=torch.uint8, device=dev,
+                            generator=g)
         sel = torch.randn((E, N, k), device=dev, generator=g).to(torch.bfloat16)
         gs_a = torch.full((1,), 0.01, device=dev)
         gs_w = torch.full((E,), 0.001, device=dev)
@@ -627,31 +791,33 @@ def run_profile_case(args):
         dw = torch.empty((E, M, N), dtype=torch.float32, device=dev)
         fn = lambda: nv.nvfp4_bf16_grouped_gemm_wgrad(a_t, b_t, offsets, E, dw)
         flops = 2 * R * M * N
-    elif case == "quantize_x":
-        T, H, topk, k = 16384, 4096, 8, 128
-        x = torch.randn((T, H), device=dev, generator=g).to(torch.bfloat16)
-        cap = T * topk
-        dst = torch.randperm(cap, device=dev, generator=g).to(torch.int32).view(T, topk)
-        codes = torch.empty((cap, H // 2), dtype=torch.uint8, device=dev)
-        scales = torch.empty(nv.scale_bytes(cap, H), dtype=torch.uint8, device=dev)
-        resid = torch.empty((cap, k), dtype=torch.bfloat16, device=dev)
-        S = torch.arange(0, H, H // k, dtype=torch.int32, device=dev)
-        amax = torch.zeros(1, device=dev)
-        nv.nvfp4_amax(x, amax)
-        fn = lambda: nv.nvfp4_quantize(x, amax, codes, scales, resid=resid, S=S, dst_row=dst, fanout=topk,
-                                       rows_out=cap)
-        flops = 0
-    elif case == "quantize_h":
+    elif case == "quantize_h_syn":
+        # a synthetic stand-in for ncu (few launches before it): 147456 x 1536, the k = 128
+        # selected channels clustered in the first 512-element segment
         rows, I, k = 147456, 1536, 128
         x = (torch.randn((rows, I), device=dev, generator=g) * 0.1).to(torch.bfloat16)
         codes = torch.empty((rows, I // 2), dtype=torch.uint8, device=dev)
         scales = torch.empty(nv.scale_bytes(rows, I), dtype=torch.uint8, device=dev)
         resid = torch.empty((rows, k), dtype=torch.bfloat16, device=dev)
-        spread = os.environ.get("NVFP4_PROFILE_S", "spread") == "spread"
-        S = (torch.arange(0, I, I // k) if spread else torch.arange(k)).to(torch.int32).to(dev)
+        S = torch.arange(k, dtype=torch.int32, device=dev)
         amax = torch.zeros(1, device=dev)
         nv.nvfp4_amax(x, amax)
         fn = lambda: nv.nvfp4_quantize(x, amax, codes, scales, resid=resid, S=S)
+        flops = 0
+    elif case in ("quantize_x", "quantize_h"):
+        # the layer's own launches: the prefill workload's x dispatched to its routed rows with the
+        # calibrated S13, or the forward's h with the calibrated S_down
+        c, layer, x, logits, _ = build_workload(dev)
+        layer.forward(x, logits)
+        torch.cuda.synchronize()
+        r, xa, ha = layer.route, layer.xa, layer.ha
+        if case == "quantize_x":
+            fn = lambda: nv.nvfp4_quantize(x, xa.amax, xa.codes, xa.scales, resid=xa.resid, S=layer.S13,
+                                           gs_out=xa.gs, dst_row=r.dst_row, fanout=layer.topk,
+                                           rows_out=layer.rows_cap)
+        else:
+            fn = lambda: nv.nvfp4_quantize(layer.h, ha.amax, ha.codes, ha.scales, resid=ha.resid, S=layer.Sd,
+                                           gs_out=ha.gs)
         flops = 0
     elif case == "combine":
         T, topk, H = 16384, 8, 4096
@@ -687,6 +853,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--profile-case", default=None,
                     help="run one kernel on a reduced case for ncu: gemm13, gemm_down, quantize_x, bf16_gemm")
+    ap.add_argument("--pipeline", default="auto", choices=["auto", "single", "pair"],
+                    help="GEMM pipeline of the profile cases")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

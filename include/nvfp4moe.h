@@ -22,22 +22,32 @@
  *  - There is no CPU path: without an sm_103 device every call returns
  *    NVFP4_ERR_ARCH.
  *
- * NVFP4 tensor format produced by nvfp4_quantize (QUADS §2.2 "FP4."):
+ * NVFP4 tensor format (QUADS §2.2 "FP4."):
  *  - codes  [rows, K/2] uint8: E2M1 codes, two per byte, element 2i in the
  *           low nibble, element 2i+1 in the high nibble.
- *  - scales tiled E4M3 block scales, one per 16 consecutive elements along
- *           K, grouped in 2048-byte tiles of 128 rows x 16 blocks (one GEMM
- *           K-slice of 256 elements): tile (m/128, kb/16) starts at byte
- *           ((m/128)*(K/256) + kb/16)*2048 (with K/256 rounded up) and holds
- *           row m, block kb at byte (m%128)*16 + kb%16.  Size:
- *           ceil(rows/128)*128 * ceil(K/256)*16 bytes; unused bytes are 0.
- *           The GEMM copies a tile per K-slice and interleaves it into tensor
- *           memory as the block-scaled MMA reads it.
+ *  - scales E4M3 block scales, one per 16 consecutive elements along K, in
+ *           tiles of 128 rows x 16 blocks (one GEMM K-slice of 256 elements):
+ *           tile (m/128, kb/16) starts at byte ((m/128)*KS + kb/16)*2048, KS =
+ *           ceil(K/256).  A tile is four 512-byte groups, one per 4 consecutive
+ *           blocks (one MMA's 64 elements of K): block j = kb%16 of row
+ *           r = m%128 sits in group j/4, on line r%32 (16 bytes), at byte
+ *           4*(r/32) + j%4.  This is the 128-row x 4-block interleave the
+ *           block-scaled MMA reads from tensor memory: the GEMM copies a group
+ *           as is (one 32x128b.warpx4 tcgen05.cp).  The same layout serves
+ *           activations (nvfp4_quantize) and weights (nvfp4_prepare_weights).
+ *           Size ceil(rows/128) * KS * 2048 bytes (= rows * K/16 for
+ *           rows % 128 == 0 and K % 256 == 0); the bytes of rows past the
+ *           tensor's last row and of blocks past K/16 are not written.
  *  - gs     FP32 per-tensor scale: the smallest power of two not below
  *           fl(amax/2688) (amax = max|x| over the tensor; 2688 = 6*448), so
  *           every block-scale target amax16/(6*gs) is at most 448; gs = 1 for
  *           an all-zero tensor.
  *  - value  of element (m, j) = e2m1(code) * e4m3(scale) * gs.
+ *
+ * Scratch: no entry point allocates.  Where a kernel needs scratch in device
+ * memory (an amax, channel scores) the caller passes it with the call
+ * (`amax_ws`, `score_ws`, `amax_out` ...), sized as each call states;
+ * nvfp4_fake_quant_noalloc is the one variant that needs none from the caller.
  */
 #ifndef NVFP4MOE_H
 #define NVFP4MOE_H
@@ -105,7 +115,7 @@ int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensor
  *               dispatch: each token's codes go to its routed rows).
  *   rows_out    number of output rows (>= M when dst_row is NULL).
  *   codes       device uint8 [rows_out, K/2]
- *   scales      device uint8, swizzled layout for rows_out rows (see top)
+ *   scales      device uint8, the scale layout for rows_out rows (see top)
  *   resid       device BF16 [rows_out, k]: the residual r = bf16(x -
  *               dequant(q(x))) on S -- minus the quantization error Delta X_q
  *               of Eq. 20 -- in units of gs: bf16(r * (1/gs)), which is r/gs
@@ -174,7 +184,8 @@ int nvfp4_fake_quant_noalloc(const void *w, int32_t ntensors, int64_t rows, int6
  * NVFP4-quantize with the expert's own gs and gather the dequantized,
  * unscaled weight on the RAC channels:
  *   w_codes     device uint8 [E, N, K/2]
- *   w_scales    device uint8 [E][swizzled N x K] (E * N * K/16 bytes)
+ *   w_scales    device uint8, E tensors of N x K in the scale layout (see
+ *               top), E * ceil(N/128) * ceil(K/256) * 2048 bytes
  *   gs_w        device float[E]
  *   w_sel       device BF16 [E, N, k]: w_sel[e,n,s] = code*sb of W[e,n,S[s]]
  *               (exact in BF16; the GEMM multiplies by gs_w[e])
@@ -243,7 +254,7 @@ int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K,
  * selection, Eq. 23-24).
  * The selected weight columns of a rollout weight pack, for a new channel set:
  * w_sel[e, n, s] = bf16(code * sb) of element (n, S[s]) of expert e -- what
- * nvfp4_prepare_weights writes for S -- read from its packed codes and tiled
+ * nvfp4_prepare_weights writes for S -- read from its packed codes and block
  * scales (rows in the pack's own order, interleaved or not).
  *   w_codes, w_scales   from nvfp4_prepare_weights (E experts, N x K)
  *   S                   device int32[k], entries in [0, K) (others are clamped)
@@ -340,7 +351,7 @@ int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32_t topk, in
 
 /* MoE glue (not described by QUADS).
  * Zero the padding rows [offsets[e]+counts[e], offsets[e+1]) of a routed
- * NVFP4 activation (codes [rows_cap, K/2], swizzled scales, resid [rows_cap,
+ * NVFP4 activation (codes [rows_cap, K/2], block scales, resid [rows_cap,
  * k] BF16 or NULL when k = 0), so that padded rows contribute zeros. */
 int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *offsets, int32_t E,
                             int64_t rows_cap, int64_t K, int32_t k, uint8_t *codes,

@@ -126,7 +126,7 @@ def nvfp4_amax(x, amax_out, ntensors=1, stream=None):
 
 def nvfp4_quantize(x, amax, codes, scales, resid=None, S=None, gs_out=None, dst_row=None,
                    fanout=1, rows_out=None, dev_status=None, stream=None):
-    """A1-A5, A9: NVFP4 codes, swizzled scales and the RAC residual of x [M, K]."""
+    """A1-A5, A9: NVFP4 codes, block scales and the RAC residual of x [M, K]."""
     M, K = x.shape
     k = 0 if S is None else S.numel()
     if rows_out is None:

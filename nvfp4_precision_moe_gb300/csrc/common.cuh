@@ -292,11 +292,12 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_des
 // 32 rows x 16 bytes, no swizzle: the scale-factor source of tcgen05.cp.
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
 
-// Copy 32 rows x 128 bits of scale factors from shared memory into tensor
-// memory, replicated into all four 32-lane quarters.
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc)
-                 : "memory");
+// Scale-factor copies of a CTA pair, issued by the leader in its MMA stream
+// (executed in order with its MMAs): each CTA's shared memory at the
+// descriptor's address goes to its own tensor memory at `taddr`.
+// 32 rows x 128 bits -> lanes 0-31 and again 32-63, 64-95, 96-127, 4 columns.
+__device__ __forceinline__ void tc_cp_pair_32x128_x4(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
 }
 
 // D(tmem) (+)= A(smem) . B(smem)^T, E2M1 x E2M1 with UE4M3 scales per 16 K.
@@ -388,6 +389,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// 8 consecutive 32-bit columns of this warp's 32 TMEM lanes <- registers.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 // 16 consecutive 32-bit columns of this warp's 32 TMEM lanes <- registers.

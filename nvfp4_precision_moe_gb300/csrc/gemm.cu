@@ -62,7 +62,7 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
     const bool pair = use_pair(true);
     const uint32_t brows = pair ? 128 : 256;  // B rows per copy: this CTA's half, or the whole tile
 
-    CUtensorMap tA, tB, tR, tW;
+    CUtensorMap tA, tB, tR, tW, tSA, tSB;
     int s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a_codes, K / 2, rows_cap, K / 2, 128, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (s == NVFP4_OK)
@@ -78,9 +78,19 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
         tR = tA;
         tW = tB;
     }
+    // the scale tensors as rows of 256 bytes, a 2048-byte scale tile in 8 rows; the pair
+    // pipeline copies them with the operands
+    const int64_t kslices = K / 256;
+    if (s == NVFP4_OK && pair)
+        s = encode_tmap_2d(&tSA, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)a_scales, 256,
+                           (uint64_t)(rows_cap / 128) * kslices * 8, 256, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (s == NVFP4_OK && pair)
+        s = encode_tmap_2d(&tSB, CU_TENSOR_MAP_DATA_TYPE_UINT8, (void *)w_scales, 256,
+                           (uint64_t)E * (N / 128) * kslices * 8, 256, 256, 8, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (s != NVFP4_OK) return s;
 
     GemmParams p{};
+    p.a_codes_base = a_codes;
     p.a_scales = a_scales;
     p.w_scales = w_scales;
     p.gs_a = gs_a;
@@ -99,7 +109,7 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
               (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
     p.amax_out = amax_out;
     p.dev_status = dev_status;
-    return pair ? launch_pair_gemm<true>(tA, tB, tR, tW, p, rows_cap, N, (cudaStream_t)stream)
+    return pair ? launch_pair_gemm<true>(tA, tB, tR, tW, tSA, tSB, p, rows_cap, N, (cudaStream_t)stream)
                 : launch_single_gemm<true>(tA, tB, tR, tW, p, rows_cap, N, (cudaStream_t)stream);
 }
 
@@ -124,6 +134,7 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
                            CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != NVFP4_OK) return s;
     GemmParams p{};
+    p.a_codes_base = (const uint8_t *)x;
     p.epilogue = epilogue;
     p.offsets = offsets;
     p.rows_cap = (int32_t)rows_cap;
@@ -136,7 +147,7 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     p.vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) &&
               (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
     p.dev_status = dev_status;
-    return use_pair(false) ? launch_pair_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream)
+    return use_pair(false) ? launch_pair_gemm<false>(tA, tB, tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream)
                            : launch_single_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream);
 }
 

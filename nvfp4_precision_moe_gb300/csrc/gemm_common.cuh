@@ -10,20 +10,27 @@ namespace nvfp4 {
 constexpr int kBM = 128;             // output rows per CTA
 constexpr int kBN = 256;             // output columns per tile
 constexpr int kATileBytes = 16384;   // 128 rows x 128 bytes of K
-constexpr int kSFABytes = 2048;      // 4 MMA-K chunks x 512 bytes (128 rows x 4 scales)
-constexpr int kSFBBytes = 4096;      // the scales of all 256 B rows of a tile
+constexpr int kSFABytes = 2048;      // the A tile's scales: one 2048-byte tile of the scale layout
+constexpr int kSFBBytes = 4096;      // the scales of all 256 B rows of a tile: two tiles
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAcc = 0, kSFCol0 = 256, kSFSlotCols = 48;  // accumulator; per-stage scale slots
+// Tensor memory: the accumulator, then one scale slot per stage.  A scales in
+// its first 16 columns: MMA chunk c reads columns 4c..4c+3, in lane quarter q
+// column 4c + q at lane r%32 for row r = 32q + r%32 (every quarter gets the
+// same copy of group c).  B scales in the next 32: chunk c reads columns
+// 16 + 8c .. 16 + 8c + 7, column 16 + 8c + n/32 at lane n%32 of every quarter
+// for B row n.  (Scale addresses of the block-scaled MMA are 4-column aligned.)
+constexpr uint32_t kAcc = 0, kSFCol0 = 256, kSFSlotCols = 48, kSFBCol = 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxExperts = 1024;
 // Warp roles per CTA (512 threads, four warpgroups):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner + MMA issuer (one lane)
 //   warps 2-3   idle
-//   warps 4-7   scale warps (FP4): once a stage's block scales have landed,
-//               each writes them into its 32-lane quarter of tensor memory with
-//               tcgen05.st, replicated as the block-scaled MMA reads them
-//               (tcgen05.cp would occupy the tensor pipe between MMAs)
+//   warps 4-7   scale warps (FP4, single-CTA pipeline): once a stage's block
+//               scales have landed, each writes them into its 32-lane quarter
+//               of tensor memory with tcgen05.st, as the block-scaled MMA reads
+//               them.  (The pair pipeline copies them with tcgen05.cp in the
+//               MMA stream instead; there these warps idle.)
 //   warps 8-15  epilogue: warp w reads TMEM lane quarter w%4 and column half
 //               (w-8)/4 of the tile -- all 128 of a thread's columns at once --
 //               releases the accumulator, then scales, applies SwiGLU and
@@ -40,6 +47,7 @@ constexpr uint32_t kRegsCtl = 88, kRegsSF = 72, kRegsEpi = 176;
 static_assert(128 * kRegsCtl + 128 * kRegsSF + 256 * kRegsEpi <= 65536, "register split above the launch budget");
 
 struct GemmParams {
+    const uint8_t *a_codes_base;  // the A operand's base (at least 16 KB readable): the pair pipeline's abort drain
     const uint8_t *a_scales;
     const uint8_t *w_scales;
     const float *gs_a;
@@ -133,36 +141,35 @@ __device__ __forceinline__ void swiglu16(uint16_t *dst16, bool vec32, float gmul
 }
 
 // One stage's block scales, from shared memory to this warp's 32-lane quarter
-// of the stage's tensor-memory slot (every quarter holds the same copy, as the
-// block-scaled MMA reads it).  Shared memory holds the A tile [128 rows][16 B]
-// and then the B tile's rows 0-127 and 128-255, each [128][16 B]; MMA-K chunk
-// c of a row is its bytes 4c..4c+3.  Slot columns: A chunk c -> 4c..4c+3
-// (column 4c+j holds row 32j+lane); B chunk c -> 16+8c+j, rows 32j+lane for
-// j < 4 and 128+32(j-4)+lane for j >= 4.  The caller waits for the stores.
+// of the stage's tensor-memory slot -- the image the pair pipeline's
+// tcgen05.cp copies produce.  Shared memory holds the A tile's scale tile and
+// then those of B rows 0-127 and 128-255 (2048 bytes each: a 512-byte group
+// per MMA chunk c, row r on line r%32, 4 bytes per row at 4*(r/32)).  Line
+// `lane` of group c goes to columns 4c..4c+3 (A) or 16 + 8c + 4t .. +3 (B,
+// tile t).  The caller waits for the stores.
 __device__ __forceinline__ void sf_stage_to_tmem(const uint8_t *sfs, uint32_t base, int lane) {
-    {
-        uint32_t r[16];  // A: column 4c + j
+    uint32_t ra[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 a = *reinterpret_cast<const uint4 *>(sfs + 16 * (lane + 32 * j));
-            r[j] = a.x;
-            r[4 + j] = a.y;
-            r[8 + j] = a.z;
-            r[12 + j] = a.w;
+    for (int c = 0; c < 4; ++c) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(sfs + c * 512 + 16 * lane);
+        ra[4 * c] = w.x;
+        ra[4 * c + 1] = w.y;
+        ra[4 * c + 2] = w.z;
+        ra[4 * c + 3] = w.w;
+    }
+    tmem_st16(base, ra);
+    uint32_t rb[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(sfs + kSFABytes + t * 2048 + c * 512 + 16 * lane);
+            rb[8 * c + 4 * t] = w.x;
+            rb[8 * c + 4 * t + 1] = w.y;
+            rb[8 * c + 4 * t + 2] = w.z;
+            rb[8 * c + 4 * t + 3] = w.w;
         }
-        tmem_st16(base, r);
-    }
-    uint32_t rb[32];  // B: column 16 + 8c + j -> index 8c + j
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(sfs + kSFABytes + (j < 4 ? 0 : kSFBBytes / 2) +
-                                                         16 * (lane + 32 * (j & 3)));
-        rb[j] = w.x;
-        rb[8 + j] = w.y;
-        rb[16 + j] = w.z;
-        rb[24 + j] = w.w;
-    }
-    tmem_st32(base + 16, rb);
+    tmem_st32(base + kSFBCol, rb);
 }
 
 // Launchers of the two pipelines (FP4: W4A4 + RAC; !FP4: BF16).  Tensor maps:
@@ -172,8 +179,11 @@ __device__ __forceinline__ void sf_stage_to_tmem(const uint8_t *sfs, uint32_t ba
 template <bool FP4>
 int launch_single_gemm(const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tR, const CUtensorMap &tW,
                        const GemmParams &p, int64_t rows_cap, int64_t N, cudaStream_t stream);
+// The pair pipeline also takes the two scale tensors as maps (FP4; unused for
+// BF16): the activation's and the weights' scales, each as rows of 256 bytes.
 template <bool FP4>
 int launch_pair_gemm(const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tR, const CUtensorMap &tW,
-                     const GemmParams &p, int64_t rows_cap, int64_t N, cudaStream_t stream);
+                     const CUtensorMap &tSA, const CUtensorMap &tSB, const GemmParams &p, int64_t rows_cap, int64_t N,
+                     cudaStream_t stream);
 
 }  // namespace nvfp4

@@ -2,16 +2,22 @@
 //
 // Two CTAs of a cluster run one 2-SM MMA pipeline on 256-row x 256-column
 // tiles: each CTA holds its 128 A rows and half of the 256 B rows of every
-// K-slice, so a stage is half the B bytes of the single-CTA pipeline's.  The
-// leader (rank 0) issues M=256 MMAs that read A and B from both CTAs' shared
-// memory and write D rows 0-127 to its tensor memory and rows 128-255 to the
-// peer's; each SM reads the block scales of all 256 B rows from its own tensor
-// memory, so both CTAs load the whole scale set of the B tile.  Both CTAs'
-// operand copies complete on the leader's full barrier; the leader's MMA
-// commits free the stage in both CTAs (multicast); the scale and epilogue
-// warps of both CTAs signal the leader's barriers.
+// K-slice, so a stage is half the B bytes of the single-CTA pipeline's and each
+// SM's MMAs read half as much shared memory per FLOP.  The leader (rank 0)
+// issues M=256 MMAs that read A and B from both CTAs' shared memory and write D
+// rows 0-127 to its tensor memory and rows 128-255 to the peer's.  Every copy
+// of both CTAs completes on the leader's full barrier; the leader's MMA commits
+// free the stage in both CTAs (multicast); the epilogue warps of both CTAs
+// signal the leader's accumulator barrier.
 //  * FP4: the W4A4 + RAC GEMM of QUADS §3.3 Eq. 21 (kind::mxf4nvf4 block-scaled
-//    main product, BF16 RAC correction into the same accumulator).
+//    main product, BF16 RAC correction into the same accumulator).  The block
+//    scales come with the operands (each CTA: the scale tile of its A rows and
+//    those of all 256 B rows, since each SM reads the B scales of all N columns
+//    from its own tensor memory) and the leader copies them into both CTAs'
+//    tensor memory with tcgen05.cp in its MMA stream: per MMA chunk one
+//    32x128b.warpx4 copy for A and two for B, replicated into the four lane
+//    quarters.  No other warp touches the scales, so nothing couples the two
+//    CTAs per slice but the full barrier.
 //  * BF16: the GEMM of the asymmetric-QAT forward, QUADS §3.2 Eq. 12.
 // Each expert's 128-row tiles are paired in order; an odd last tile is paired
 // with a phantom half that the peer computes and never stores.  Stages: 5 for
@@ -23,7 +29,6 @@ namespace nvfp4 {
 namespace {
 
 constexpr int kBHalfBytes = 16384;                // this CTA's 128 of the tile's 256 B rows
-constexpr uint64_t kSettleNs = 200000ull;         // after an abort: 200 us for copies in flight
 
 // Instruction descriptors of the 2-SM MMA (M = 256, N = 256, both operands K-major).
 //  kind::mxf4nvf4: A, B = E2M1 (1) at bits 7-9 / 10-12, N>>3 at 17, scale
@@ -37,8 +42,8 @@ struct Cfg {
     static constexpr int kStages = FP4 ? 5 : 6;
     static constexpr int kStageBytes = kATileBytes + kBHalfBytes + (FP4 ? kSFABytes + kSFBBytes : 0);
     static constexpr int kBarOffset = kStages * kStageBytes;
-    // barriers: full/empty/sf_full/sf_ready per stage, acc_full, acc_empty, drain
-    static constexpr int kNumBars = 4 * kStages + 3;
+    // barriers: full/empty per stage, acc_full, acc_empty, drain, abort_sync
+    static constexpr int kNumBars = 2 * kStages + 4;
     static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
     static constexpr int kPairOffset = kOffOffset + (kMaxExperts + 1) * 4;
     static constexpr int kGswOffset = kPairOffset + (kMaxExperts + 1) * 4;
@@ -76,10 +81,17 @@ __device__ __forceinline__ PairTile decode_item(const int32_t *off, const int32_
     return t;
 }
 
+// Bytes one CTA copies for slice `it` of a tile (nkt main slices, then the RAC slices).
+template <bool FP4>
+__device__ __forceinline__ uint32_t slice_bytes(int it, int nkt) {
+    return kATileBytes + kBHalfBytes + ((FP4 && it < nkt) ? kSFABytes + kSFBBytes : 0);
+}
+
 template <bool FP4>
 __global__ void __launch_bounds__(kThreads, 1)
     pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmR, const __grid_constant__ CUtensorMap tmWs,
+                        const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                         GemmParams p) {
     using C = Cfg<FP4>;
     constexpr int kStages = C::kStages;
@@ -87,13 +99,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
     uint64_t *empty = full + kStages;
-    uint64_t *sf_full = empty + kStages;
-    uint64_t *sf_ready = sf_full + kStages;
-    uint64_t *acc_full = sf_ready + kStages;
+    uint64_t *acc_full = empty + kStages;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *drain = acc_empty + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    uint64_t *abort_sync = drain + 1;  // leader: the peer producer's report after an abort
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(abort_sync + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    volatile int *peer_issued = reinterpret_cast<volatile int *>(tmem_slot + 2);  // leader: the peer's slice count
     int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::kOffOffset);
     int32_t *s_pairs = reinterpret_cast<int32_t *>(smem + C::kPairOffset);
     float *s_gsw = reinterpret_cast<float *>(smem + C::kGswOffset);
@@ -109,20 +121,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = threadIdx.x; i < E; i += blockDim.x) s_gsw[i] = p.gs_w[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);                  // leader: its producer + both CTAs' operand bytes
-            mbar_init(&empty[s], 1);                 // the leader's MMA commit, sent to both CTAs
-            mbar_init(&sf_full[s], 1);               // this CTA's scale bytes
-            mbar_init(&sf_ready[s], 2 * kSFWarps);   // leader: the scale warps of both CTAs
+            mbar_init(&full[s], 1);   // leader: its producer's arrival + both CTAs' bytes
+            mbar_init(&empty[s], 1);  // the leader's MMA commit, sent to both CTAs
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 2 * kEpiWarps);  // leader: the epilogue warps of both CTAs
         mbar_init(drain, 1);
+        mbar_init(abort_sync, 1);
         *abort_flag = 0;
+        *peer_issued = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmA);
         prefetch_tmap(&tmB);
+        if (FP4) {
+            prefetch_tmap(&tmSA);
+            prefetch_tmap(&tmSB);
+        }
         if (FP4 && p.k > 0) {
             prefetch_tmap(&tmR);
             prefetch_tmap(&tmWs);
@@ -176,16 +192,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 0) {
             if (lane == 0) {
                 // ------------------------------------------------ TMA producer (both CTAs)
-                // A rows and this CTA's half of the B rows land in this CTA's
-                // shared memory; their bytes complete on the leader's full barrier.
+                // A rows, this CTA's half of the B rows and (FP4) the block scales land in
+                // this CTA's shared memory; their bytes complete on the leader's full barrier.
+                // Both CTAs issue the same sequence of slices; `issued` counts them.
                 int stage = 0;
                 uint32_t phase = 0;
-                uint32_t issued_phase[kStages];
-                bool issued[kStages];
-                for (int s = 0; s < kStages; ++s) issued[s] = false;
+                int issued = 0;
                 bool ok = true;
-                const int64_t kgroups = p.K / 64;
                 const uint32_t full_lead = cluster_addr(full, 0);
+                const int64_t nt128 = p.N / 128;  // weight-layout scale tiles per expert and K-slice column
                 for (int item = item0; ok && item < num_items; item += item_step) {
                     const PairTile t = decode_item(s_off, s_pairs, E, num_nt, item, rank);
                     const int64_t sfa_tile = (t.live ? t.m0 : t.lead_m0) / kBM;  // scales of a real tile
@@ -203,36 +218,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         uint8_t *sa = smem + stage * C::kStageBytes;
                         uint8_t *sb = sa + kATileBytes;
-                        if (FP4) {
-                            if (it < nkt) {
-                                // the scales first, on this CTA's own barrier: the scale
-                                // warps move them to tensor memory while A and B are in flight
-                                uint8_t *ssf = sb + kBHalfBytes;
-                                const uint8_t *wsc = p.w_scales + (int64_t)e * p.N * (p.K / 16);
-                                mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
-                                bulk_load(ssf, p.a_scales + (sfa_tile * kgroups + it * 4) * 512, kSFABytes, &sf_full[stage]);
-                                bulk_load(ssf + kSFABytes, wsc + ((int64_t)(2 * nt) * kgroups + it * 4) * 512, kSFBBytes / 2,
-                                          &sf_full[stage]);
-                                bulk_load(ssf + kSFABytes + kSFBBytes / 2,
-                                          wsc + ((int64_t)(2 * nt + 1) * kgroups + it * 4) * 512, kSFBBytes / 2,
-                                          &sf_full[stage]);
-                            } else {
-                                mbar_arrive(&sf_full[stage]);  // no scales: the scale warps only pass
-                            }
-                        }
-                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * (kATileBytes + kBHalfBytes));
+                        if (leader) mbar_arrive_expect_tx(&full[stage], 2 * slice_bytes<FP4>(it, nkt));
                         const uint32_t fb = full_lead + 8u * (uint32_t)stage;
                         if (it < nkt) {
                             const int32_t x = FP4 ? it * 128 : it * 64;
                             tma_load_2d_pair(sa, &tmA, x, t.m0, fb);
                             tma_load_2d_pair(sb, &tmB, x, brow_mine, fb);
+                            if (FP4) {
+                                // scales as rows of 256 bytes: the A tile's 2048-byte scale tile,
+                                // then the two of the 256 B rows
+                                uint8_t *ssf = sb + kBHalfBytes;
+                                tma_load_2d_pair(ssf, &tmSA, 0, (int32_t)((sfa_tile * nkt + it) * 8), fb);
+                                const int64_t wt = ((int64_t)e * nt128 + 2 * nt) * nkt + it;
+                                tma_load_2d_pair(ssf + kSFABytes, &tmSB, 0, (int32_t)(wt * 8), fb);
+                                tma_load_2d_pair(ssf + kSFABytes + 2048, &tmSB, 0, (int32_t)((wt + nkt) * 8), fb);
+                            }
                         } else {  // RAC slice: residual rows and the selected weight columns
                             const int r = it - nkt;
                             tma_load_2d_pair(sa, &tmR, r * 64, t.m0, fb);
                             tma_load_2d_pair(sb, &tmWs, r * 64, brow_mine, fb);
                         }
-                        issued[stage] = true;
-                        issued_phase[stage] = phase;
+                        ++issued;
                         if (++stage == kStages) {
                             stage = 0;
                             phase ^= 1u;
@@ -242,19 +248,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) {
                     report(p.dev_status, NVFP4_ERR_TIMEOUT);
                     *abort_flag = 1;
-                    // Every copy already issued must land before the CTAs can exit.  This
-                    // CTA's scale copies complete on its own barrier; the operand copies of
-                    // both CTAs complete on the leader's, which the peer cannot watch and
-                    // the leader may not have armed yet.  So wait for what can be watched,
-                    // then hold the CTA for a settle window far longer than a copy takes;
-                    // the cluster barrier at the end keeps the other CTA alive as long.
-                    for (int s = 0; s < kStages; ++s)
-                        if (issued[s]) {
-                            if (leader) (void)mbar_wait_bounded(&full[s], issued_phase[s], kWaitLimitNs);
-                            if (FP4) (void)mbar_wait_bounded(&sf_full[s], issued_phase[s], kWaitLimitNs);
+                    // Every copy already issued must land before the CTAs can exit.  All of
+                    // them complete on the leader's full barriers, so the leader settles
+                    // them: the peer reports how many slices it issued; for each of the last
+                    // kStages slices the leader arms the barrier for the bytes it has not
+                    // armed yet (the peer's slices it never reached) and, where it armed
+                    // bytes the peer never sent, sends as many dummy bytes into its own
+                    // stage (nothing reads it any more); then it waits for each of those
+                    // phases, with the same bound.  The cluster barrier at the end keeps
+                    // the peer alive until then.
+                    if (!leader) {
+                        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr((const void *)peer_issued, 0)),
+                                     "r"(issued)
+                                     : "memory");
+                        mbar_arrive_cluster(cluster_addr(abort_sync, 0));
+                    } else {
+                        const bool heard = mbar_wait_bounded(abort_sync, 0, 2 * kWaitLimitNs);
+                        asm volatile("fence.acq_rel.cluster;" ::: "memory");  // the peer's count before its arrival
+                        const int n_peer = heard ? *peer_issued : issued;
+                        const int n_max = max(issued, n_peer);
+                        const int per_item = nkt + nrt;
+                        for (int i = max(0, n_max - kStages); i < n_max; ++i) {
+                            const int st = i % kStages;
+                            const uint32_t par = (uint32_t)(i / kStages) & 1u;
+                            const uint32_t bytes = slice_bytes<FP4>(i % per_item, nkt);
+                            if (i >= issued) mbar_arrive_expect_tx(&full[st], bytes);  // only the peer's bytes come
+                            else if (i >= n_peer) {                                      // the peer's bytes never come
+                                for (uint32_t d = 0; d < bytes; d += 16384)
+                                    bulk_load(smem + st * C::kStageBytes + d, p.a_codes_base, min(16384u, bytes - d), &full[st]);
+                            }
+                            (void)mbar_wait_bounded(&full[st], par, kWaitLimitNs);
                         }
-                    const uint64_t t0 = global_ns();
-                    while (global_ns() - t0 < kSettleNs) {
                     }
                 }
             }
@@ -278,23 +302,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ok = false;
                             break;
                         }
-                        // the scale warps of both CTAs are done with this stage (they
-                        // pass RAC slices too): every phase of sf_ready is consumed here,
-                        // in order, so no arrival of a later use can land in this one
-                        if (FP4 && !mbar_wait_bounded(&sf_ready[stage], phase, kWaitLimitNs, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
                         tc_fence_after();
                         const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
                         const uint32_t b_addr = a_addr + kATileBytes;
                         if (it < nkt) {
                             if (FP4) {
+                                // the stage's scales into its tensor-memory slot of both CTAs (in
+                                // order with the MMAs below; the slot's previous MMAs finished
+                                // before the stage was refilled)
                                 const uint32_t sf = tmem + kSFCol0 + (uint32_t)stage * kSFSlotCols;
+                                const uint32_t ssf = b_addr + kBHalfBytes;
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) {
+                                    tc_cp_pair_32x128_x4(sf + 4 * c, desc_sf(ssf + 512 * c));
+#pragma unroll
+                                    for (int t = 0; t < 2; ++t)
+                                        tc_cp_pair_32x128_x4(sf + kSFBCol + 8 * c + 4 * t,
+                                                             desc_sf(ssf + kSFABytes + 2048 * t + 512 * c));
+                                }
 #pragma unroll
                                 for (int c = 0; c < 4; ++c)
                                     tc_mma_nvf4_pair(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                                     kIdescNVF4, sf + 4 * c, sf + 16 + 8 * c, (it | c) != 0);
+                                                     kIdescNVF4, sf + 4 * c, sf + kSFBCol + 8 * c, (it | c) != 0);
                             } else {
 #pragma unroll
                                 for (int c = 0; c < 4; ++c)
@@ -329,50 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }  // warps 2 and 3: idle
     } else if (warp < kEpiWarp0) {
-        regs_dec<kRegsSF>();
-        // ---------------------------------------------------- scale warps (both CTAs)
-        // Slice by slice in the producer's order: wait for the stage's scales
-        // (their own barrier, so this overlaps the A/B copies), then write them
-        // into this warp's lane quarter of the stage's tensor-memory slot
-        // (sf_stage_to_tmem: the tiled 128-row x 16-byte shared-memory layout
-        // interleaved as the block-scaled MMA reads it).
-        // Then one arrival per warp on the leader's sf_ready.
-        if (FP4) {
-            const uint32_t q = (uint32_t)(warp & 3);
-            const uint32_t ready_lead = cluster_addr(sf_ready, 0);
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int item = item0; item < num_items; item += item_step) {
-                bool ok = true;
-                for (int it = 0; it < nkt + nrt; ++it) {
-                    const bool got = mbar_wait_bounded(&sf_full[stage], phase, kWaitLimitNs, abort_flag);
-                    if (!__all_sync(0xffffffffu, got)) {
-                        ok = false;
-                        break;
-                    }
-                    if (it < nkt) {
-                        const uint8_t *sfs = smem + stage * C::kStageBytes + kATileBytes + kBHalfBytes;
-                        const uint32_t base = tmem + ((q * 32u) << 16) + kSFCol0 + (uint32_t)stage * kSFSlotCols;
-                        sf_stage_to_tmem(sfs, base, lane);
-                        tmem_st_wait();
-                    }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(ready_lead + 8u * (uint32_t)stage);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) {
-                    if (lane == 0) {
-                        report(p.dev_status, NVFP4_ERR_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-            }
-        }
+        regs_dec<kRegsSF>();  // warpgroup 1 idles: the leader copies the scales
     } else {
         regs_inc<kRegsEpi>();
         // ---------------------------------------------------- epilogue (both CTAs)
@@ -453,7 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // and as fit on the GPU at once.
 template <bool FP4>
 int launch_pair_gemm(const CUtensorMap &tA, const CUtensorMap &tB, const CUtensorMap &tR, const CUtensorMap &tW,
-                     const GemmParams &p, int64_t rows_cap, int64_t N, cudaStream_t stream) {
+                     const CUtensorMap &tSA, const CUtensorMap &tSB, const GemmParams &p, int64_t rows_cap, int64_t N,
+                     cudaStream_t stream) {
     static bool attr_done[2] = {false, false};
     if (!attr_done[FP4]) {
         const cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<FP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -492,7 +479,7 @@ int launch_pair_gemm(const CUtensorMap &tA, const CUtensorMap &tB, const CUtenso
     if (items < pairs) pairs = items;
     if (pairs < 1) pairs = 1;
     cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, pair_gemm_kernel<FP4>, tA, tB, tR, tW, p);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, pair_gemm_kernel<FP4>, tA, tB, tR, tW, tSA, tSB, p);
     if (e != cudaSuccess) {
         set_last_error("cudaLaunchKernelEx(pair_gemm_kernel)", e);
         return NVFP4_ERR_CUDA;
@@ -501,8 +488,10 @@ int launch_pair_gemm(const CUtensorMap &tA, const CUtensorMap &tB, const CUtenso
 }
 
 template int launch_pair_gemm<true>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                    const CUtensorMap &, const GemmParams &, int64_t, int64_t, cudaStream_t);
+                                    const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmParams &,
+                                    int64_t, int64_t, cudaStream_t);
 template int launch_pair_gemm<false>(const CUtensorMap &, const CUtensorMap &, const CUtensorMap &,
-                                     const CUtensorMap &, const GemmParams &, int64_t, int64_t, cudaStream_t);
+                                     const CUtensorMap &, const CUtensorMap &, const CUtensorMap &, const GemmParams &,
+                                     int64_t, int64_t, cudaStream_t);
 
 }  // namespace nvfp4

@@ -18,7 +18,8 @@
 // B: 32).  The accumulator is single-buffered; the epilogue releases it as
 // soon as it has read it.  Expert segments are contiguous 128-row groups of
 // the routed rows, so the tile list is (row tile, column tile) over all
-// routed rows; each tile's expert comes from a binary search of the offsets.
+// routed rows; each tile's expert comes from a binary search of the offsets
+// (read through the read-only cache: the stages leave no room for a copy).
 // Warp roles and the register split: gemm_common.cuh.
 #include "gemm_common.cuh"
 
@@ -44,9 +45,7 @@ struct Cfg {
     static constexpr int kBarOffset = kOutOffset + kOutBytes;
     // barriers: full/empty/sf_full/sf_ready per stage, acc_full, acc_empty, drain
     static constexpr int kNumBars = 4 * kStages + 3;
-    static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
-    static constexpr int kGswOffset = kOffOffset + (kMaxExperts + 1) * 4;
-    static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
+    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
 };
 static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<false>::kSmemBytes <= 232448, "shared memory budget");
 static_assert(Cfg<false>::kOutOffset % 1024 == 0, "store staging boxes sit on 1024-byte swizzle atoms");
@@ -66,7 +65,7 @@ __device__ __forceinline__ WTile wgrad_tile(const int32_t *off, int num_mt, int 
     const int rem = tile - w.e * per;
     w.mt = rem / num_nt;
     w.nt = rem - w.mt * num_nt;
-    const int32_t lo = min(max(off[w.e], 0), rows_cap), hi = min(max(off[w.e + 1], 0), rows_cap);
+    const int32_t lo = min(max(__ldg(off + w.e), 0), rows_cap), hi = min(max(__ldg(off + w.e + 1), 0), rows_cap);
     w.k0 = lo;
     w.nk = hi > lo ? (hi - lo) / 64 : 0;
     return w;
@@ -76,7 +75,7 @@ __device__ __forceinline__ int expert_of(const int32_t *off, int E, int32_t m0) 
     int lo = 0, hi = E - 1;  // first e with off[e+1] > m0
     while (lo < hi) {
         int mid = (lo + hi) >> 1;
-        if (off[mid + 1] <= m0) lo = mid + 1;
+        if (__ldg(off + mid + 1) <= m0) lo = mid + 1;
         else hi = mid;
     }
     return lo;
@@ -99,14 +98,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = acc_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::kOffOffset);
-    float *s_gsw = reinterpret_cast<float *>(smem + C::kGswOffset);
+    const int32_t *s_off = p.offsets;  // read-only for the kernel: read through __ldg
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
-    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = p.offsets[i];
-    if (FP4)
-        for (int i = threadIdx.x; i < E; i += blockDim.x) s_gsw[i] = p.gs_w[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -135,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     // rows beyond the caller's buffers are never touched, whatever offsets hold
-    const int32_t total_rows = min(s_off[E], p.rows_cap) & ~(kBM - 1);
+    const int32_t total_rows = min(__ldg(s_off + E), p.rows_cap) & ~(kBM - 1);
     const int num_nt = (int)(p.N / kBN);
     // weight-gradient mode (BF16): tiles (expert, M tile, N tile), each reducing over its expert's rows
     const bool wgrad = !FP4 && p.wgrad;
@@ -156,7 +151,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool issued[kStages];
                 for (int s = 0; s < kStages; ++s) issued[s] = false;
                 bool ok = true;
-                const int64_t kgroups = p.K / 64;
                 for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                     if (wgrad) {
                         // A rows [128 mt, +128) and B rows [256 nt, +256) over the expert's routed rows
@@ -200,14 +194,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (it < nkt) {
                             if (FP4) {
                                 // the scales first, on their own barrier: the scale warps
-                                // move them to tensor memory while A and B are in flight
+                                // move them to tensor memory while A and B are in flight.
+                                // A: the scale tile (row tile mt, slice it); B: the scale
+                                // tiles of rows 256nt.. and 256nt+128.. of expert e
                                 uint8_t *ssf = sb + kBTileBytes;
-                                const uint8_t *wsc = p.w_scales + (int64_t)e * p.N * (p.K / 16);
+                                const uint8_t *wsc = p.w_scales + (int64_t)e * (p.N / 128) * nkt * 2048;
                                 mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
-                                bulk_load(ssf, p.a_scales + ((int64_t)mt * kgroups + it * 4) * 512, kSFABytes, &sf_full[stage]);
-                                bulk_load(ssf + kSFABytes, wsc + ((int64_t)(2 * nt) * kgroups + it * 4) * 512, kSFBBytes / 2,
+                                bulk_load(ssf, p.a_scales + ((int64_t)mt * nkt + it) * 2048, kSFABytes, &sf_full[stage]);
+                                bulk_load(ssf + kSFABytes, wsc + ((int64_t)(2 * nt) * nkt + it) * 2048, kSFBBytes / 2,
                                           &sf_full[stage]);
-                                bulk_load(ssf + kSFABytes + kSFBBytes / 2, wsc + ((int64_t)(2 * nt + 1) * kgroups + it * 4) * 512,
+                                bulk_load(ssf + kSFABytes + kSFBBytes / 2, wsc + ((int64_t)(2 * nt + 1) * nkt + it) * 2048,
                                           kSFBBytes / 2, &sf_full[stage]);
                                 mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
                                 tma_load_2d(sa, &tmA, it * 128, m0, &full[stage]);
@@ -281,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int c = 0; c < 4; ++c)
                                     tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescNVF4,
-                                                sf + 4 * c, sf + 16 + 8 * c, (it | c) != 0);
+                                                sf + 4 * c, sf + kSFBCol + 8 * c, (it | c) != 0);
                             } else {
 #pragma unroll
                                 for (int c = 0; c < 4; ++c)
@@ -442,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int mt = tile / num_nt, nt = tile - mt * num_nt;
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
-            const float gmul = FP4 ? __fmul_rn(gsa, s_gsw[expert_of(s_off, E, mt * kBM)]) : 1.0f;
+            const float gmul = FP4 ? __fmul_rn(gsa, __ldg(p.gs_w + expert_of(s_off, E, mt * kBM))) : 1.0f;
             if (swiglu) {
                 uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 128 + 64 * half;
 #pragma unroll

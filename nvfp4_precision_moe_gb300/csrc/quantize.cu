@@ -43,31 +43,25 @@ struct QuantArgs {
     int32_t *dev_status;
 };
 
-// Byte offset of (row m, block kb) in the swizzled scale layout, for a
-// tensor whose rows hold K/16 blocks.
-// Tiles of 128 rows x 16 blocks (2048 bytes, one GEMM K-slice of a row tile):
-// tile (m/128, kb/16) at ((m/128)*kslices + kb/16)*2048, row m and block kb
-// inside it at (m%128)*16 + kb%16.
-__device__ __forceinline__ int64_t swz_offset(int64_t m, int64_t kb, int64_t kslices) {
-    return ((m >> 7) * kslices + (kb >> 4)) * 2048 + (m & 127) * 16 + (kb & 15);
+// Scale layout (activations and weights alike): tiles of 128 rows x 16 blocks
+// (one 256-element GEMM K-slice), tile (m/128, kb/16) number
+// (m/128)*kslices + kb/16, 2048 bytes each: four 512-byte groups, one per 4
+// consecutive blocks (one MMA's 64 elements of K); in a group row r of the
+// tile sits on line r%32 (16 bytes), its blocks at bytes 4*(r/32) + kb%4.  A
+// group is what the GEMM copies into tensor memory with one 32x128b.warpx4
+// tcgen05.cp (line l -> lane l of every lane quarter).  Four consecutive
+// blocks kb..kb+3 (kb % 4 == 0) are four consecutive bytes, stored as one word.
+__device__ __forceinline__ int64_t scale_row_offset(int64_t m, int64_t kslices) {
+    return (m >> 7) * kslices * 2048 + (m & 31) * 16 + ((m & 127) >> 5) * 4;
+}
+__device__ __forceinline__ int64_t scale_block_offset(int64_t b) {  // b % 4 == 0
+    return (b >> 4) * 2048 + ((b & 15) >> 2) * 512;
 }
 
 // E2M1 code -> value, from a packed table of 2*|value| (0,1,2,3,4,6,8,12).
 __device__ __forceinline__ float e2m1_val(uint32_t c) {
     const float mag = 0.5f * (float)((0xC8643210u >> (4u * (c & 7u))) & 15u);
     return (c & 8u) ? -mag : mag;
-}
-
-// v[t] for a run-time t, by a tree of selects (keeps v in registers)
-__device__ __forceinline__ float sel16(const float (&v)[16], int t) {
-    float a[8], b[4], c[2];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = (t & 1) ? v[2 * i + 1] : v[2 * i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) b[i] = (t & 2) ? a[2 * i + 1] : a[2 * i];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) c[i] = (t & 4) ? b[2 * i + 1] : b[2 * i];
-    return (t & 8) ? c[1] : c[0];
 }
 
 // One 16-element block: the E4M3 scale code, its value, and the 16 E2M1 codes
@@ -158,6 +152,10 @@ __device__ __forceinline__ void unpack_block(const uint4 &a, const uint4 &b, flo
 constexpr int kQThreads = 256;
 constexpr int kQWarps = kQThreads / 32;
 constexpr int kMaxStagedK = 1024;  // residual row staged in shared memory up to this k
+constexpr int kQSlots = 4;         // 1 KB segments in flight per warp
+constexpr int kQBlocksPerSM = 3;   // 24 warps, 96 KB of segments in flight per SM
+constexpr size_t kQRingBytes = (size_t)kQWarps * kQSlots * 1024;
+constexpr uint64_t kQWaitNs = 2000000000ull;  // 2 s per wait for a segment
 
 // The RAC value of one selected element x (BF16 bits) of a block with scale
 // code sb: its E2M1 code is recomputed exactly as the block's quantization
@@ -176,35 +174,30 @@ __device__ __forceinline__ uint16_t resid_value(uint16_t xb, uint32_t sb, float 
     return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
 }
 
-// The RAC value of element x of a block already quantized to code c with scale
-// value sbf (the same arithmetic as resid_value, without recomputing the code).
-template <int MODE>
-__device__ __forceinline__ uint16_t rac_value(float v, uint32_t c, float sbf, float gs, float inv_gs) {
-    const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
-    if (MODE == kModeWeight) return __bfloat16_as_ushort(__float2bfloat16_rn(cs));
-    const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
-    return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
-}
-
-// One warp per output row (grid-stride), looping over the row in segments of
-// 32 blocks (512 elements, one block per lane).  Each row's destination rows
-// are resolved once: their code-row offsets and the row part of their
-// swizzled scale offsets sit in shared memory, so a block's stores to every
-// destination cost an add each.  The RAC residual is computed after the row's
-// blocks, one selected channel per lane, from the row's block scales kept in
-// shared memory; it is staged there and written once per destination row as
+// One warp per output row (grid-stride), the row in segments of 32 blocks
+// (512 elements, one block per lane).  A warp's segments -- all of its rows',
+// in order -- stream through a ring of kQSlots 1 KB slots in shared memory:
+// lane 0 keeps kQSlots segments in flight with bulk copies (one mbarrier per
+// slot), so the bytes in flight do not cost registers.  Each row's destination
+// rows are resolved once: their code-row offsets and the row part of their
+// scale offsets sit in shared memory, so a block's stores to every destination
+// cost an add each.  The RAC values of a segment's selected channels are
+// computed right after its blocks, one selected channel per lane (the lane
+// reads the element from the slot and the block scale from the block's lane by
+// a shuffle, then recomputes the element's code exactly as the block did);
+// they are staged in shared memory and written once per destination row as
 // 16-byte chunks.
 template <int MODE>
-__global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(QuantArgs a) {
+    extern __shared__ __align__(128) uint8_t q_ring[];  // [kQWarps][kQSlots][1024]
+    __shared__ uint64_t s_qbar[kQWarps][kQSlots];
     __shared__ __align__(16) uint16_t s_res[kQWarps][kMaxStagedK];
     __shared__ uint8_t s_sb[kQWarps][kMaxBlocksPerRow];
     __shared__ int64_t s_cbase[kQWarps][32];  // destination f: byte offset of its code row (-1: skipped)
-    __shared__ int64_t s_sbase[kQWarps][32];  // destination f: row part of its swizzled scale offsets
+    __shared__ int64_t s_sbase[kQWarps][32];  // destination f: row part of its scale offsets
     __shared__ int32_t s_S[kMaxStagedK];
-    // per 16-element block: which of its channels are in S (bit t = channel 16b + t), and the
-    // position in S of its first selected channel (S is strictly increasing)
-    __shared__ uint32_t s_selmask[kMaxBlocksPerRow];
-    __shared__ uint32_t s_selbase[kMaxBlocksPerRow];
+    // per 512-element segment: the position in S of its first selected channel
+    __shared__ int32_t s_segfirst[kMaxBlocksPerRow / 32 + 1];
     __shared__ QTables s_tab;
     const int tensor = blockIdx.y;
     fill_tables(s_tab);
@@ -212,19 +205,19 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
     const int64_t kslices = (nb + 15) >> 4;
     const bool has_sel = (MODE != kModeFake) && a.k > 0;
     const bool staged = a.k <= kMaxStagedK;
+    const int segs = (nb + 31) >> 5;
     if (has_sel && staged) {
-        for (int i = threadIdx.x; i < nb; i += blockDim.x) {
-            s_selmask[i] = 0u;
-            s_selbase[i] = 0xffffffffu;
-        }
+        for (int i = threadIdx.x; i < a.k; i += blockDim.x) s_S[i] = min(max(a.S[i], 0), (int32_t)(a.K - 1));
         __syncthreads();
-        for (int i = threadIdx.x; i < a.k; i += blockDim.x) {
-            const int32_t j = a.S[i];
-            s_S[i] = j;
-            if (j >= 0 && j < a.K) {
-                atomicOr(&s_selmask[j >> 4], 1u << (j & 15));
-                atomicMin(&s_selbase[j >> 4], (uint32_t)i);
+        // S is increasing: the first position of segment s is the first i with S[i] >= 512 s
+        for (int sg = threadIdx.x; sg <= segs; sg += blockDim.x) {
+            int lo = 0, hi = a.k;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (s_S[mid] < 512 * sg) lo = mid + 1;
+                else hi = mid;
             }
+            s_segfirst[sg] = lo;
         }
     }
     __syncthreads();  // tables (and S) are ready
@@ -239,7 +232,6 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
     }
 
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    const int segs = (nb + 31) >> 5;
     const int64_t nwarps_total = (int64_t)gridDim.x * kQWarps;
     const uint16_t *xt = a.x + (int64_t)tensor * a.x_tstride;
     uint16_t *stage = s_res[wid];
@@ -256,92 +248,92 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
         }
         return m;
     };
-    // software pipeline across segments and rows: the next segment's 32
-    // bytes per lane are in flight while this one is quantized
-    uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
-    {
-        const int64_t m0 = (int64_t)blockIdx.x * kQWarps + wid;
-        if (m0 < a.M && lane < nb) {
-            const uint4 *p0 = reinterpret_cast<const uint4 *>(xt + source_row(m0) * a.ldx + lane * 16);
-            ra = __ldg(p0);
-            rb = __ldg(p0 + 1);
-        }
+    // This warp's rows m = first + i * nwarps_total (i < nrows) and their
+    // segments, flat index j -> row i = j / segs, segment j % segs; slot
+    // j % kQSlots of the warp's ring holds segment j.
+    uint8_t *ring = q_ring + (size_t)wid * kQSlots * 1024;
+    uint64_t *bars = s_qbar[wid];
+    const int64_t first = (int64_t)blockIdx.x * kQWarps + wid;
+    const int64_t nrows = first < a.M ? (a.M - 1 - first) / nwarps_total + 1 : 0;
+    const int64_t nseg = nrows * segs;
+    auto issue = [&](int64_t j) {  // lane 0: segment j into its slot
+        const int64_t m = first + (j / segs) * nwarps_total;
+        const int sg = (int)(j % segs);
+        const int slot = (int)(j % kQSlots);
+        const uint32_t bytes = (uint32_t)min(32, nb - 32 * sg) * 32u;
+        mbar_arrive_expect_tx(&bars[slot], bytes);
+        bulk_load(ring + slot * 1024, xt + source_row(m) * a.ldx + (int64_t)sg * 512, bytes, &bars[slot]);
+    };
+    if (lane == 0) {
+        for (int sl = 0; sl < kQSlots; ++sl) mbar_init(&bars[sl], 1);
+        fence_barrier_init();
+        for (int64_t j = 0; j < nseg && j < kQSlots; ++j) issue(j);
     }
-    for (int64_t m = (int64_t)blockIdx.x * kQWarps + wid; m < a.M; m += nwarps_total) {
-        const int64_t src_row = source_row(m);
-        if (MODE != kModeFake) {
+    __syncwarp();
+    int64_t j = 0;
+    bool ok = true;
+    for (; j < nseg; ++j) {
+        const int seg = (int)(j % segs);
+        const int64_t m = first + (j / segs) * nwarps_total;
+        if (MODE != kModeFake && seg == 0) {
             // destination rows of this source row: lane f resolves the f-th
             __syncwarp();  // the previous row's readers of s_cbase / s_sbase are done
             if (lane < fanout) {
                 int64_t dm = m;
                 if (MODE == kModeAct && a.dst_row) dm = (int64_t)a.dst_row[m * fanout + lane];
-                const bool ok = dm >= 0 && dm < ((MODE == kModeAct) ? a.rows_out : a.M);  // others are skipped
-                s_cbase[wid][lane] = ok ? dm * (a.K >> 1) : -1;
-                s_sbase[wid][lane] = ok ? ((dm >> 7) * kslices * 2048 + (dm & 127) * 16) : 0;
+                const bool okd = dm >= 0 && dm < ((MODE == kModeAct) ? a.rows_out : a.M);  // others are skipped
+                s_cbase[wid][lane] = okd ? dm * (a.K >> 1) : -1;
+                s_sbase[wid][lane] = okd ? scale_row_offset(dm, kslices) : 0;
             }
             __syncwarp();
         }
-        const uint16_t *xrow = xt + src_row * a.ldx;
-        const uint16_t *xnext = (m + nwarps_total < a.M) ? xt + source_row(m + nwarps_total) * a.ldx : nullptr;
+        const int slot = (int)(j % kQSlots);
+        const bool got = mbar_wait_bounded(&bars[slot], (uint32_t)(j / kQSlots) & 1u, kQWaitNs);
+        if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+        }
+        const uint16_t *xs = reinterpret_cast<const uint16_t *>(ring + slot * 1024);  // the segment
+        const int b = seg * 32 + lane;
+        const bool valid = b < nb;
+        float v[16];
+        BlockQ q;
+        if (valid) {
+            unpack_block(*reinterpret_cast<const uint4 *>(xs + lane * 16),
+                         *reinterpret_cast<const uint4 *>(xs + lane * 16 + 8), v);
+            quant_block(v, gs, p6, inv_gs, s_tab, q);
+        } else {
+            q.sb = 0u;
+            q.sbf = 0.0f;
+            q.w0 = q.w1 = 0u;
+        }
 
-        for (int seg = 0; seg < segs; ++seg) {
-            const int b = seg * 32 + lane;
-            const bool valid = b < nb;
-            const uint4 ca = ra, cb = rb;
-            if (seg + 1 < segs) {
-                if (b + 32 < nb) {
-                    const uint4 *pn = reinterpret_cast<const uint4 *>(xrow + (b + 32) * 16);
-                    ra = __ldg(pn);
-                    rb = __ldg(pn + 1);
-                }
-            } else if (xnext && lane < nb) {  // first segment of this warp's next row
-                const uint4 *pn = reinterpret_cast<const uint4 *>(xnext + lane * 16);
-                ra = __ldg(pn);
-                rb = __ldg(pn + 1);
-            }
-            float v[16];
-            BlockQ q;
+        if (MODE == kModeFake) {
             if (valid) {
-                unpack_block(ca, cb, v);
-                quant_block(v, gs, p6, inv_gs, s_tab, q);
-            } else {
-                q.sb = 0u;
-                q.sbf = 0.0f;
-                q.w0 = q.w1 = 0u;
-            }
-
-            if (MODE == kModeFake) {
-                if (valid) {
-                    uint32_t o[8];
+                uint32_t o[8];
 #pragma unroll
-                    for (int t = 0; t < 16; t += 2) {
-                        const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
-                        const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
-                        o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
-                                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(a.w_hat + (int64_t)tensor * a.what_tstride + m * a.K + b * 16);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                for (int t = 0; t < 16; t += 2) {
+                    const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
+                    const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
+                    o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
+                               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
                 }
-                continue;
+                uint4 *dst = reinterpret_cast<uint4 *>(a.w_hat + (int64_t)tensor * a.what_tstride + m * a.K + b * 16);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
             }
-
-            if (has_sel && valid) {
+        } else {
+            if (has_sel) {
                 if (staged) {
-                    // this block's selected channels: their RAC values go straight to the stage
-                    const uint32_t msk = s_selmask[b];
-                    if (msk) {
-                        const uint32_t base = s_selbase[b];
-                        uint32_t rem = msk;
-                        while (rem) {
-                            const int t = __ffs(rem) - 1;
-                            rem &= rem - 1u;
-                            stage[base + __popc(msk & ((1u << t) - 1u))] =
-                                rac_value<MODE>(sel16(v, t), q.code(t), q.sbf, gs, inv_gs);
-                        }
+                    // this segment's selected channels, one per lane: the RAC value goes to the stage
+                    const int i0 = s_segfirst[seg], i1 = s_segfirst[seg + 1];
+                    for (int base = i0; base < i1; base += 32) {  // the same trip count in every lane
+                        const int i = base + lane;
+                        const int jc = i < i1 ? s_S[i] : seg * 512;
+                        const uint32_t sbl = __shfl_sync(0xffffffffu, q.sb, (jc >> 4) & 31);
+                        if (i < i1) stage[i] = resid_value<MODE>(xs[jc - seg * 512], sbl, gs, inv_gs, s_tab);
                     }
-                } else {
+                } else if (valid) {
                     row_sb[b] = (uint8_t)q.sb;
                 }
             }
@@ -352,7 +344,7 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
             const uint32_t s3 = __shfl_down_sync(0xffffffffu, sw, 3);
             sw = sw | (s1 << 8) | (s2 << 16) | (s3 << 24);
             const bool group_lead = ((lane & 3) == 0) && (b < ((nb + 3) & ~3));
-            const int64_t boff = (int64_t)(b >> 4) * 2048 + (b & 15);  // block part of the scale offset
+            const int64_t boff = scale_block_offset(b);  // block part of the scale offsets
             for (int f = 0; f < fanout; ++f) {
                 const int64_t cbase = s_cbase[wid][f];
                 if (cbase < 0) continue;
@@ -360,16 +352,16 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
                 if (group_lead) *reinterpret_cast<uint32_t *>(scales + s_sbase[wid][f] + boff) = sw;
             }
         }
+        __syncwarp();  // every lane is done with the slot (and, at a row's end, the stage is complete)
+        if (lane == 0 && j + kQSlots < nseg) issue(j + kQSlots);
 
-        if (has_sel) {
-            // residual (activation) or unscaled dequantized weight on S, one
-            // selected channel per lane: the element's code is recomputed from
-            // its block scale exactly as its block quantized it
-            __syncwarp();  // the stage (or row_sb) is complete
-            if (!staged) {  // k beyond the stage: values go straight to every destination row
+        if (MODE != kModeFake && has_sel && seg == segs - 1) {
+            // the row's residual (activation) or unscaled dequantized weight on S
+            const uint16_t *xrow = xt + source_row(m) * a.ldx;
+            if (!staged) {  // k beyond the stage: one selected channel per lane, straight to every destination
                 for (int si = lane; si < a.k; si += 32) {
-                    const int j = __ldg(a.S + si);
-                    const uint16_t val = resid_value<MODE>(__ldg(xrow + j), row_sb[j >> 4], gs, inv_gs, s_tab);
+                    const int jc = __ldg(a.S + si);
+                    const uint16_t val = resid_value<MODE>(__ldg(xrow + jc), row_sb[jc >> 4], gs, inv_gs, s_tab);
                     for (int f = 0; f < fanout; ++f) {
                         const int64_t cbase = s_cbase[wid][f];
                         if (cbase < 0) continue;
@@ -378,9 +370,7 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
                         else a.resid[dm * a.k + si] = val;
                     }
                 }
-            }
-            if (staged) {  // the row's k values -> every destination row
-                __syncwarp();
+            } else {  // the row's k values -> every destination row
                 const int chunks = a.k >> 3;  // 16-byte chunks (k % 8 == 0)
                 const uint4 *src = reinterpret_cast<const uint4 *>(stage);
                 for (int f = 0; f < fanout; ++f) {
@@ -392,7 +382,14 @@ __global__ void __launch_bounds__(kQThreads, 4) quantize_kernel(QuantArgs a) {
                     for (int c = lane; c < chunks; c += 32) reinterpret_cast<uint4 *>(row)[c] = src[c];
                 }
             }
+            __syncwarp();  // the stage is read out before the next row writes it
         }
+    }
+    if (!ok && lane == 0) {
+        // a segment never arrived: report it, and let every copy still in flight land before the CTA exits
+        report(a.dev_status, NVFP4_ERR_TIMEOUT);
+        for (int64_t jj = j; jj < nseg && jj < j + kQSlots; ++jj)
+            (void)mbar_wait_bounded(&bars[jj % kQSlots], (uint32_t)(jj / kQSlots) & 1u, kQWaitNs);
     }
 }
 
@@ -456,8 +453,9 @@ __global__ void clear_padding_kernel(const int32_t *counts, const int32_t *offse
     const int64_t nb = K >> 4, kslices = (nb + 15) >> 4;
     uint32_t *c = reinterpret_cast<uint32_t *>(codes + row * (K >> 1));
     for (int64_t i = threadIdx.x; i < (K >> 3); i += blockDim.x) c[i] = 0u;
-    for (int64_t g = threadIdx.x; g < kslices * 4; g += blockDim.x)  // 4-byte words of the row's 16-byte runs
-        *reinterpret_cast<uint32_t *>(scales + swz_offset(row, g * 4, kslices)) = 0u;
+    const int64_t srow = scale_row_offset(row, kslices);
+    for (int64_t g = threadIdx.x; g < kslices * 4; g += blockDim.x)  // the row's 4-byte words, 4 per K-slice
+        *reinterpret_cast<uint32_t *>(scales + srow + scale_block_offset(g * 4)) = 0u;
     if (resid)
         for (int64_t i = threadIdx.x; i < k; i += blockDim.x) resid[row * k + i] = 0;
 }
@@ -815,15 +813,11 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_kernel(const ui
         const int64_t e = row / N, n = row - e * N;
         const uint4 *src = reinterpret_cast<const uint4 *>(codes + row * (K >> 1));
         for (int64_t i = lane; i < (K >> 5); i += 32) reinterpret_cast<uint4 *>(rowc)[i] = __ldg(src + i);
-        // the row's block scales: a 16-byte run per 256-element K-slice of the tiled layout
-        const uint8_t *sten = scales + e * N * nb;  // an expert's scales
-        for (int64_t t = lane; t < kslices; t += 32) {
-            const uint8_t *run = sten + ((n >> 7) * kslices + t) * 2048 + (n & 127) * 16;
-            const int64_t cnt = nb - 16 * t < 16 ? nb - 16 * t : 16;
-            if (cnt == 16) *reinterpret_cast<uint4 *>(rows_ + 16 * t) = __ldg(reinterpret_cast<const uint4 *>(run));
-            else
-                for (int64_t b = 0; b < cnt; ++b) rows_[16 * t + b] = run[b];
-        }
+        // the row's block scales: one 32-bit word per 4 blocks
+        const uint8_t *sten = scales + e * ((N + 127) >> 7) * kslices * 2048;  // an expert's scales
+        const int64_t srow = scale_row_offset(n, kslices);
+        for (int64_t g = lane; g < (nb >> 2); g += 32)
+            reinterpret_cast<uint32_t *>(rows_)[g] = __ldg(reinterpret_cast<const uint32_t *>(sten + srow + scale_block_offset(4 * g)));
         __syncwarp();
         uint32_t *dst = reinterpret_cast<uint32_t *>(wsel + row * k);
         for (int s2 = 2 * lane; s2 < k; s2 += 64) {
@@ -906,11 +900,29 @@ __global__ void __launch_bounds__(256) fake_quant_t_kernel(const uint16_t *w, in
     }
 }
 
+// Blocks for `rows` rows (one warp per row): as many as are resident at once.
 static int quant_grid(int64_t rows) {
     int64_t blocks = (rows + kQWarps - 1) / kQWarps;
-    int64_t cap = (int64_t)sm_count() * 8;
+    int64_t cap = (int64_t)sm_count() * kQBlocksPerSM;
     if (blocks > cap) blocks = cap;
     return (int)(blocks < 1 ? 1 : blocks);
+}
+
+// The segment ring is dynamic shared memory above the static arrays.
+template <int MODE>
+static int launch_quantize(dim3 grid, const QuantArgs &a, cudaStream_t st, const char *name) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(quantize_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kQRingBytes);
+        if (e != cudaSuccess) {
+            set_last_error("cudaFuncSetAttribute(quantize_kernel)", e);
+            return NVFP4_ERR_CUDA;
+        }
+        attr_done = true;
+    }
+    quantize_kernel<MODE><<<grid, kQThreads, kQRingBytes, st>>>(a);
+    return launch_status(name);
 }
 
 static int amax_launch(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t nt, int64_t tstride, float *out,
@@ -973,8 +985,7 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
     a.scales = scales;
     a.resid = (uint16_t *)resid;
     a.dev_status = dev_status;
-    quantize_kernel<kModeAct><<<quant_grid(M), kQThreads, 0, (cudaStream_t)stream>>>(a);
-    return launch_status("quantize_kernel");
+    return launch_quantize<kModeAct>(dim3(quant_grid(M)), a, (cudaStream_t)stream, "quantize_kernel");
 }
 
 extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat, float *gs_out,
@@ -999,8 +1010,7 @@ extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t
     a.what_tstride = rows * cols;
     a.dev_status = dev_status;
     int g = quant_grid(rows) / (nt > 8 ? 8 : nt);
-    quantize_kernel<kModeFake><<<dim3(g < 1 ? 1 : g, nt), kQThreads, 0, st>>>(a);
-    return launch_status("quantize_kernel<fake>");
+    return launch_quantize<kModeFake>(dim3(g < 1 ? 1 : g, nt), a, st, "quantize_kernel<fake>");
 }
 
 extern "C" int nvfp4_fake_quant_transposed(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat,
@@ -1046,14 +1056,13 @@ extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_
     a.codes = w_codes;
     a.codes_tstride = N * K / 2;
     a.scales = w_scales;
-    a.scales_tstride = N * K / 16;
+    a.scales_tstride = N * ((K / 16 + 15) / 16) * 16;  // an expert's scales
     a.wsel = (uint16_t *)w_sel;
     a.wsel_tstride = N * (int64_t)k;
     a.interleave = interleave;
     a.dev_status = dev_status;
     int g = quant_grid(N) / (E > 8 ? 8 : E);
-    quantize_kernel<kModeWeight><<<dim3(g < 1 ? 1 : g, E), kQThreads, 0, st>>>(a);
-    return launch_status("quantize_kernel<weight>");
+    return launch_quantize<kModeWeight>(dim3(g < 1 ? 1 : g, E), a, st, "quantize_kernel<weight>");
 }
 
 extern "C" int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t k, const int32_t *offsets, int32_t E,

@@ -25,8 +25,9 @@ from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16,
 
 
 def scale_bytes(rows, K):
-    """Bytes of the tiled block-scale layout of a rows x K NVFP4 tensor."""
-    return ((rows + 127) // 128) * 128 * ((K // 16 + 15) // 16) * 16
+    """Bytes of the block-scale layout of a rows x K NVFP4 tensor: 2048 per
+    tile of 128 rows x 256 elements of K."""
+    return ((rows + 127) // 128) * ((K // 16 + 15) // 16) * 2048
 
 
 def rows_capacity(T, topk, E):
@@ -44,7 +45,7 @@ class _Routing:
 
 
 class _Nvfp4Act:
-    """A routed NVFP4 activation: codes, swizzled scales, residual, gs."""
+    """A routed NVFP4 activation: codes, block scales, residual, gs."""
 
     def __init__(self, rows, K, k, dev):
         self.codes = torch.zeros((rows, K // 2), dtype=torch.uint8, device=dev)
@@ -63,7 +64,7 @@ class _Nvfp4Weights:
         k = 0 if S is None else S.numel()
         self.E, self.N, self.K, self.k = E, N, K, k
         self.codes = torch.empty((E, N, K // 2), dtype=torch.uint8, device=dev)
-        self.scales = torch.empty(E * N * K // 16, dtype=torch.uint8, device=dev)
+        self.scales = torch.empty(E * scale_bytes(N, K), dtype=torch.uint8, device=dev)
         self.gs = torch.empty(E, dtype=torch.float32, device=dev)
         self.sel = torch.empty((E, N, max(k, 1)), dtype=torch.bfloat16, device=dev)[:, :, :k].contiguous() \
             if k else None
@@ -129,9 +130,9 @@ class RolloutMoE:
         (e.g. to alternate output buffers while an earlier result is being
         copied out), else a view of a reused buffer.
 
-        `mark(i)`, if given, is called before stage i = 0..6 (route, amax,
-        quantize x, gate_up GEMM, quantize h, down GEMM, combine) and with
-        i = 7 at the end, e.g. to record CUDA events."""
+        `mark(i)`, if given, is called before stage i = 0..7 (route, amax,
+        quantize x, clear padding, gate_up GEMM, quantize h, down GEMM,
+        combine) and with i = 8 at the end, e.g. to record CUDA events."""
         mark = mark or (lambda i: None)
         T = x.shape[0]
         assert T <= self.max_tokens and logits.shape == (T, self.E)
@@ -151,18 +152,19 @@ class RolloutMoE:
                        S=self.S13 if self.k13 else None, gs_out=xa.gs, dst_row=dst,
                        fanout=self.topk, rows_out=self.rows_cap, dev_status=self.dev_status,
                        stream=stream)
+        mark(3)
         nvfp4_moe_clear_padding(r.counts, r.offsets, self.E, self.H, self.k13, xa.codes, xa.scales,
                                 xa.resid if self.k13 else None, stream=stream)
         if self.resid_fp4 and self.k13:
             nvfp4_rac_requant_residual(xa.resid, self.resid_amax[0:1], r.offsets, self.E, gs_out=self.resid_gs[0:1],
                                        dev_status=self.dev_status, stream=stream)
-        mark(3)
+        mark(4)
         W = self.w13
         nvfp4_w4a4_rac_grouped_gemm(xa.codes, xa.scales, xa.resid if W.k else None, xa.gs, W.codes,
                                     W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.h,
                                     epilogue=NVFP4_EPI_SWIGLU, out_dtype=NVFP4_OUT_BF16,
                                     amax_out=ha.amax, dev_status=self.dev_status, stream=stream)
-        mark(4)
+        mark(5)
         if self.online and self.kd:  # the routed rows of h only: rows past offsets[E] may be stale
             nvfp4_rac_select_channels_online(self.h, ha.amax, self.kd, self.Sd, self.score_ws, offsets=r.offsets,
                                              E=self.E, stream=stream)
@@ -174,18 +176,18 @@ class RolloutMoE:
         if self.resid_fp4 and self.kd:
             nvfp4_rac_requant_residual(ha.resid, self.resid_amax[1:2], r.offsets, self.E, gs_out=self.resid_gs[1:2],
                                        dev_status=self.dev_status, stream=stream)
-        mark(5)
+        mark(6)
         W = self.wd
         nvfp4_w4a4_rac_grouped_gemm(ha.codes, ha.scales, ha.resid if W.k else None, ha.gs, W.codes,
                                     W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.y,
                                     epilogue=NVFP4_EPI_NONE, out_dtype=NVFP4_OUT_BF16,
                                     dev_status=self.dev_status, stream=stream)
-        mark(6)
+        mark(7)
         if out is None:
             out = self.out[:T]
         assert out.shape == (T, self.H) and out.dtype == torch.float32
         nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
-        mark(7)
+        mark(8)
         return out
 
 

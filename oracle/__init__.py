@@ -11,8 +11,9 @@ via QUantization-error Alignment across Dual Sides".  BF16 tensors cross this
 interface as numpy ``uint16`` bit patterns.
 
 Parity status: every function is pinned by ``tests/test_oracle_*.py`` except
-the scale swizzle, whose layout is pinned only by the GPU exact-GEMM test
-(on the CPU it is checked to be a bijection with zero padding).
+the scale layout, which is pinned only by the GPU GEMM parity tests (a wrong
+layout gives errors far above their tolerance; on the CPU it is checked to be
+a bijection with zero padding).
 """
 import ctypes
 import numpy as np
@@ -50,7 +51,7 @@ def lib():
                                     ctypes.c_void_p, _i32, ctypes.c_void_p]),
             "orc_dequantize_exact": (None, [_u8p, _u8p, _i64, _i64, ctypes.c_float, _f64p]),
             "orc_dequantize_f32": (None, [_u8p, _u8p, _i64, _i64, ctypes.c_float, _f32p]),
-            "orc_swizzle_scales": (None, [_u8p, _i64, _i64, _u8p]),
+            "orc_scale_layout": (None, [_u8p, _i64, _i64, _u8p]),
             "orc_fake_quant": (None, [_u16p, _i64, _i64, _u16p, ctypes.POINTER(ctypes.c_float)]),
             "orc_rac_gemm": (None, [_f64p, ctypes.c_void_p, ctypes.c_void_p, _i32, ctypes.c_double,
                                     _f64p, _i64, _i64, _i64, _f64p]),
@@ -177,18 +178,41 @@ def dequantize_f32(codes, scales, gs):
     return out
 
 
-def swizzled_scale_bytes(M, K):
-    """Size of the tiled scale layout: ceil(M/128)*128 * ceil(K/256)*16."""
-    return ((M + 127) // 128) * 128 * ((K // 16 + 15) // 16) * 16
+def scale_bytes(M, K):
+    """Size of the scale layout: ceil(M/128) * ceil(K/256) * 2048 bytes."""
+    return ((M + 127) // 128) * ((K // 16 + 15) // 16) * 2048
 
 
-def swizzle_scales(scales, K):
-    """Canonical [M,K/16] scales -> the tiled layout of 128 rows x 16 blocks (1-D u8)."""
+def scale_layout(scales, K):
+    """Canonical [M,K/16] scales -> the scale layout shared by the quantizer
+    and the GEMM (1-D u8)."""
     scales = _c(scales, np.uint8)
     M = scales.shape[0]
-    out = np.empty(swizzled_scale_bytes(M, K), np.uint8)
-    lib().orc_swizzle_scales(scales, M, K, out)
+    out = np.empty(scale_bytes(M, K), np.uint8)
+    lib().orc_scale_layout(scales, M, K, out)
     return out
+
+
+def scale_offsets(K):
+    """Byte offsets [128, K/16] of every (row, block) of one 128-row tile in
+    the scale layout, found by laying out two index patterns (row ids,
+    block-in-slice ids) with the layout function itself."""
+    nb = K // 16
+    Lr = scale_layout(np.repeat(np.arange(1, 129, dtype=np.uint8)[:, None], nb, axis=1), K)
+    Lb = scale_layout(np.tile((np.arange(nb) % 16 + 1).astype(np.uint8), (128, 1)), K)
+    per_slice = Lr.size // ((nb + 15) // 16)
+    where = np.full((128, nb), -1, np.int64)
+    o = np.nonzero(Lr)[0]
+    where[Lr[o].astype(np.int64) - 1, (o // per_slice) * 16 + Lb[o].astype(np.int64) - 1] = o
+    assert (where >= 0).all()
+    return where
+
+
+def scale_rows(layout, rows, K):
+    """The canonical block scales [len(rows), K/16] of `rows`, read back from
+    a scale buffer in the scale layout."""
+    rows = np.asarray(rows, np.int64)
+    return np.asarray(layout)[(rows // 128)[:, None] * scale_bytes(128, K) + scale_offsets(K)[rows % 128]]
 
 
 def requant_residual(resid, gs_a):

@@ -25,7 +25,7 @@
  *   orc_bf16_round                      pinned: torch bfloat16 cast
  *   orc_quantize / orc_dequantize       pinned: grid, amax->6, idempotence,
  *                                       symmetry, zero tensor, scale brute force
- *   orc_swizzle_scales                  pinned on the GPU only (exact GEMM case);
+ *   orc_scale_layout                    pinned on the GPU only (GEMM parity);
  *                                       on the CPU: bijection + zero padding
  *   orc_rac_gemm / orc_bf16_gemm        pinned: numpy matmul, exact-integer case,
  *                                       k=0 and k=K special cases
@@ -285,20 +285,23 @@ void orc_dequantize_f32(const uint8_t *codes, const uint8_t *scales, int64_t M, 
         }
 }
 
-/* Scale layout shared by the quantizer and the block-scaled GEMM: the
- * canonical [M, K/16] scales regrouped into 2048-byte tiles of 128 rows x 16
- * blocks (one GEMM K-slice of 256 elements).  Tile (m/128, kb/16) sits at
- * ((m/128) * ceil(K/256) + kb/16) * 2048; inside it row m and block kb go to
- * (m%128)*16 + kb%16.  Rows beyond M and blocks beyond K/16 are zero.
- * (Layout choice of this build; the paper only says the quantizer's layout
- * must match the GEMM's, §3.2.) */
-void orc_swizzle_scales(const uint8_t *scales, int64_t M, int64_t K, uint8_t *out)
+/* Scale layout shared by the quantizer and the block-scaled GEMM, for
+ * activations and weights alike (a layout choice of this build: the paper
+ * only asks that the rollout quantizer's layout match its GEMM's, §3.2).  The
+ * canonical [M, K/16] block scales are grouped by tiles of 128 rows x 16
+ * blocks (one 256-element GEMM K-slice), tile (m/128, kb/16) the
+ * ((m/128) * ceil(K/256) + kb/16)-th, 2048 bytes each: four 512-byte groups,
+ * one per 4 consecutive blocks (one MMA's 64 elements of K); in group j/4
+ * (j = kb%16) row r = m%128 sits on line r%32 (16 bytes), block j at byte
+ * 4*(r/32) + j%4.  Rows beyond M and blocks beyond K/16 are zero. */
+void orc_scale_layout(const uint8_t *scales, int64_t M, int64_t K, uint8_t *out)
 {
     int64_t nb = K / 16, mt = (M + 127) / 128, kt = (nb + 15) / 16;
-    memset(out, 0, (size_t)(mt * 128 * kt * 16));
+    memset(out, 0, (size_t)(mt * kt * 2048));
     for (int64_t m = 0; m < M; m++)
         for (int64_t kb = 0; kb < nb; kb++) {
-            int64_t off = ((m / 128) * kt + kb / 16) * 2048 + (m % 128) * 16 + kb % 16;
+            int64_t r = m % 128, j = kb % 16;
+            int64_t off = ((m / 128) * kt + kb / 16) * 2048 + (j / 4) * 512 + (r % 32) * 16 + (r / 32) * 4 + j % 4;
             out[off] = scales[m * nb + kb];
         }
 }

@@ -61,7 +61,7 @@ def test_exact_integer_fp4_gemm():
     cw = rng.integers(0, 256, (E, N, K // 2), dtype=np.uint8)
     a_codes = torch.from_numpy(ca).to(G.DEV)
     w_codes = torch.from_numpy(cw).to(G.DEV)
-    a_scales = torch.full((oracle.swizzled_scale_bytes(rows, K),), 0x38, dtype=torch.uint8, device=G.DEV)
+    a_scales = torch.full((oracle.scale_bytes(rows, K),), 0x38, dtype=torch.uint8, device=G.DEV)
     w_scales = torch.full((E * N * K // 16,), 0x38, dtype=torch.uint8, device=G.DEV)
     one = torch.ones(1, dtype=torch.float32, device=G.DEV)
     gs_w = torch.ones(E, dtype=torch.float32, device=G.DEV)
@@ -99,7 +99,7 @@ class Dense:
         amax = G.zeros(1, torch.float32)
         nv.nvfp4_amax(x, amax)
         self.codes = G.zeros((Mp, K // 2), torch.uint8)
-        self.scales = G.zeros(oracle.swizzled_scale_bytes(Mp, K), torch.uint8)
+        self.scales = G.zeros(oracle.scale_bytes(Mp, K), torch.uint8)
         self.resid = G.zeros((Mp, k), torch.bfloat16) if k else None
         self.gs = G.zeros(1, torch.float32)
         nv.nvfp4_quantize(x, amax, self.codes, self.scales, resid=self.resid, S=Sd, gs_out=self.gs)
@@ -192,7 +192,7 @@ def test_grouped_ragged_segments():
     amax = G.zeros(1, torch.float32)
     nv.nvfp4_amax(x, amax)
     codes = G.zeros((rows, K // 2), torch.uint8)
-    scales = G.zeros(oracle.swizzled_scale_bytes(rows, K), torch.uint8)
+    scales = G.zeros(oracle.scale_bytes(rows, K), torch.uint8)
     resid = G.zeros((rows, k), torch.bfloat16)
     gs = G.zeros(1, torch.float32)
     Sd = torch.tensor(S, device=G.DEV)
@@ -243,7 +243,7 @@ def test_swiglu_epilogue_and_fused_amax():
     amax = G.zeros(1, torch.float32)
     nv.nvfp4_amax(x, amax)
     codes = G.zeros((rows, H // 2), torch.uint8)
-    scales = G.zeros(oracle.swizzled_scale_bytes(rows, H), torch.uint8)
+    scales = G.zeros(oracle.scale_bytes(rows, H), torch.uint8)
     resid = G.zeros((rows, k), torch.bfloat16)
     gs = G.zeros(1, torch.float32)
     Sd = torch.tensor(S, device=G.DEV)

@@ -1,6 +1,6 @@
 """GPU parity of the quantization kernels against the CPU oracle.
 
-Codes, swizzled scales, residuals, per-tensor scales, fake-quantized weights
+Codes, block scales (in the header's scale layout), residuals, per-tensor scales, fake-quantized weights
 and selected channels must be bit-exact (QUADS §2.2 "FP4.", Eq. 12, Eq. 20-21,
 Eq. 23-24).  Every input is a seeded synthetic tensor; the oracle computes
 its expected values from the same inputs on its own.
@@ -37,7 +37,7 @@ def _gpu_quantize(x_u16, S=None, rows_out=None, dst=None, fanout=1, amax_overrid
     else:
         amax.fill_(amax_override)
     codes = G.zeros((rows_out, K // 2), torch.uint8)
-    scales = G.zeros(oracle.swizzled_scale_bytes(rows_out, K), torch.uint8)
+    scales = G.zeros(oracle.scale_bytes(rows_out, K), torch.uint8)
     resid = G.zeros((rows_out, max(k, 1)), torch.bfloat16)[:, :k].contiguous() if k else None
     gs = G.zeros(1, torch.float32)
     st = G.zeros(1, torch.int32)
@@ -61,7 +61,7 @@ def _check_against_oracle(x_u16, S=None):
     bad = np.flatnonzero(got["codes"].reshape(-1) != codes.reshape(-1))
     assert bad.size == 0, "codes differ at %d bytes, first %s: gpu %02x oracle %02x" % (
         bad.size, bad[:4], got["codes"].reshape(-1)[bad[0]], codes.reshape(-1)[bad[0]])
-    sw = oracle.swizzle_scales(scales, K)
+    sw = oracle.scale_layout(scales, K)
     assert np.array_equal(got["scales"], sw)
     if S is not None and len(S):
         assert np.array_equal(got["resid"], resid)
@@ -188,7 +188,7 @@ def test_scatter_to_routed_rows():
             osc[dst[t, f]] = scales[t]
             ores[dst[t, f]] = resid[t]
     assert np.array_equal(got["codes"], oc)
-    assert np.array_equal(got["scales"], oracle.swizzle_scales(osc, 512))
+    assert np.array_equal(got["scales"], oracle.scale_layout(osc, 512))
     assert np.array_equal(got["resid"], ores)
 
 
@@ -265,7 +265,7 @@ def test_prepare_weights_parity(interleave):
         assert gs[e].item() == np.float32(g)
         assert np.array_equal(codes[e].cpu().numpy(), c)
         sc = scales.cpu().numpy()[e * N * K // 16:(e + 1) * N * K // 16]
-        assert np.array_equal(sc, oracle.swizzle_scales(s, K))
+        assert np.array_equal(sc, oracle.scale_layout(s, K))
         unscaled = oracle.dequantize_exact(c, s, 1.0)[:, S]
         assert np.array_equal(gsel[e], oracle.bf16_round(unscaled.astype(np.float32)))
 

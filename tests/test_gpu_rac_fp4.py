@@ -32,7 +32,7 @@ def _resid_of(nv, x_u16, S):
     nv.nvfp4_amax(x, amax)
     resid = G.zeros((M, len(S)), torch.bfloat16)
     nv.nvfp4_quantize(x, amax, G.zeros((M, K // 2), torch.uint8),
-                      G.zeros(oracle.swizzled_scale_bytes(M, K), torch.uint8), resid=resid,
+                      G.zeros(oracle.scale_bytes(M, K), torch.uint8), resid=resid,
                       S=torch.tensor(S, dtype=torch.int32, device=G.DEV), gs_out=gs)
     return resid, float(gs.item())
 

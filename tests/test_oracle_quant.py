@@ -190,17 +190,20 @@ def test_fake_quant_equals_dequant_of_quant():
     assert np.array_equal(oracle.bf16_to_f32(w_hat).astype(np.float64), oracle.dequantize_exact(codes, scales, gs))
 
 
-def test_swizzle_is_a_bijection_with_zero_padding():
+def test_scale_layout_is_a_bijection_with_zero_padding():
     M, K = 200, 320  # ragged in both dimensions: 2 row tiles, 2 slices of 16 blocks (the second 4/16 full)
     rng = np.random.default_rng(8)
     sc = rng.integers(1, 255, (M, K // 16), dtype=np.uint8)
-    out = oracle.swizzle_scales(sc, K)
-    assert out.size == 256 * 32
+    out = oracle.scale_layout(sc, K)
+    assert out.size == 2 * 2 * 2048
     assert np.count_nonzero(out) == sc.size
     assert sorted(out[out != 0].tolist()) == sorted(sc.reshape(-1).tolist())
-    # tile (row tile 0, slice 0) is the first 2048 bytes: row m, block kb at m*16 + kb
-    assert out[0] == sc[0, 0] and out[69 * 16 + 3] == sc[69, 3]
-    # tile (row tile 0, slice 1) starts at 2048: block 16 + j of row m at 2048 + m*16 + j
-    assert out[2048 + 5 * 16 + 2] == sc[5, 18] and out[2048 + 5 * 16 + 4] == 0
-    # tile (row tile 1, slice 1) starts at (1*2 + 1) * 2048
-    assert out[3 * 2048 + 3] == sc[128, 19]
+    # 512-byte groups of 4 blocks; row r on line r%32, bytes 4*(r/32) + kb%4
+    assert out[0] == sc[0, 0] and out[3] == sc[0, 3] and out[512] == sc[0, 4]
+    assert out[1 * 16 + 4 * 1 + 2] == sc[33, 2]
+    assert out[3 * 512 + 7 * 16 + 4 * 3 + 3] == sc[103, 15]
+    assert out[2048 + 5 * 16 + 2] == sc[5, 18]      # slice 1 of row tile 0
+    assert out[3 * 2048 + 3] == sc[128, 19]         # slice 1 of row tile 1
+    # reading rows back through the layout gives the canonical scales
+    rows = np.array([0, 5, 33, 127, 128, 199])
+    assert np.array_equal(oracle.scale_rows(out, rows, K), sc[rows])
