@@ -791,6 +791,15 @@ def run_profile_case(args):
         dw = torch.empty((E, M, N), dtype=torch.float32, device=dev)
         fn = lambda: nv.nvfp4_bf16_grouped_gemm_wgrad(a_t, b_t, offsets, E, dw)
         flops = 2 * R * M * N
+    elif case == "fake_quant":
+        # the QAT workload's W13 fake-quant: 128 experts x 3072 x 4096 BF16 (3.2 GB read, 3.2 GB written)
+        E, N, K = int(os.environ.get("NVFP4_PROFILE_E", "128")), 3072, 4096
+        w = (torch.randn((E, N, K), device=dev, generator=g) * 0.02).to(torch.bfloat16)
+        w_hat = torch.empty_like(w)
+        ws = torch.zeros(2 * E + 1, dtype=torch.float32, device=dev)
+        gsw = torch.empty(E, dtype=torch.float32, device=dev)
+        fn = lambda: nv.nvfp4_fake_quant(w, w_hat, ws, gs_out=gsw)
+        flops = 0
     elif case == "quantize_h_syn":
         # a synthetic stand-in for ncu (few launches before it): 147456 x 1536, the k = 128
         # selected channels clustered in the first 512-element segment

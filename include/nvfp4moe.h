@@ -141,8 +141,15 @@ int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float
  * dequantizes (Eq. 15-16).
  *   w, w_hat    device BF16 [ntensors, rows, cols] (may not alias)
  *   gs_out      device float[ntensors] or NULL
- *   amax_ws     device float[ntensors], caller-provided scratch (the amax).
- * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (cols % 32). */
+ *   amax_ws     device scratch of 2*ntensors + 1 32-bit words, cleared by the
+ *               call on `stream`: the amax of each tensor (as float), then
+ *               the work-scheduling counters.  One persistent launch reads
+ *               each tensor from HBM once: a tensor's amax items are taken
+ *               shortly before its quantize-dequantize items, which re-read
+ *               its rows from L2 (and wait, with a 2 s bound, for the amax;
+ *               dev_status gets TIMEOUT if it ran out).
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (cols % 32, cols > 16384,
+ * ntensors > 65535). */
 int nvfp4_fake_quant(const void *w, int32_t ntensors, int64_t rows, int64_t cols, void *w_hat,
                      float *gs_out, float *amax_ws, int32_t *dev_status, void *stream);
 
@@ -160,9 +167,10 @@ int nvfp4_fake_quant_transposed(const void *w, int32_t ntensors, int64_t rows, i
  * that must not call cudaMalloc/cudaFree (which can stall the whole device),
  * cannot provide the amax scratch that nvfp4_fake_quant asks for.  This
  * variant takes the same arguments minus `amax_ws` and computes the same
- * w_hat and gs_out (bit for bit), using a fixed array of 4096 floats that the
- * library declares in device memory (16 KB held on every GPU that loads the
- * library, until the process exits).  Nothing is allocated by the call.
+ * w_hat and gs_out (bit for bit), using a fixed array of 8193 32-bit words
+ * that the library declares in device memory (32 KB held on every GPU that
+ * loads the library, until the process exits) as nvfp4_fake_quant's scratch
+ * for up to 4096 tensors.  Nothing is allocated by the call.
  *   - ntensors must be <= 4096: larger calls return NVFP4_ERR_UNSUPPORTED
  *     (nvfp4_last_error() says why) and launch nothing.
  *   - The first call on a device, with that device current, looks up the

@@ -137,8 +137,11 @@ def nvfp4_quantize(x, amax, codes, scales, resid=None, S=None, gs_out=None, dst_
 
 
 def nvfp4_fake_quant(w, w_hat, amax_ws, gs_out=None, dev_status=None, stream=None):
-    """A16: QDQ_W of each w[t] (w: [ntensors, rows, cols] BF16)."""
+    """A16: QDQ_W of each w[t] (w: [ntensors, rows, cols] BF16); amax_ws holds
+    at least 2 * ntensors + 1 32-bit words of scratch."""
     nt, rows, cols = w.shape
+    if amax_ws.numel() * amax_ws.element_size() < 4 * (2 * nt + 1):
+        raise ValueError("nvfp4_fake_quant: amax_ws needs 2 * ntensors + 1 words")
     _call("nvfp4_fake_quant", _p(w), nt, rows, cols, _p(w_hat), _p(gs_out), _p(amax_ws),
           _p(dev_status), _s(stream))
 

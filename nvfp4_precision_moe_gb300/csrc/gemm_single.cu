@@ -19,7 +19,7 @@
 // soon as it has read it.  Expert segments are contiguous 128-row groups of
 // the routed rows, so the tile list is (row tile, column tile) over all
 // routed rows; each tile's expert comes from a binary search of the offsets
-// (read through the read-only cache: the stages leave no room for a copy).
+// (kept in shared memory with the experts' weight scales).
 // Warp roles and the register split: gemm_common.cuh.
 #include "gemm_common.cuh"
 
@@ -45,7 +45,9 @@ struct Cfg {
     static constexpr int kBarOffset = kOutOffset + kOutBytes;
     // barriers: full/empty/sf_full/sf_ready per stage, acc_full, acc_empty, drain
     static constexpr int kNumBars = 4 * kStages + 3;
-    static constexpr int kSmemBytes = 1024 + kBarOffset + kNumBars * 8 + 16;
+    static constexpr int kOffOffset = kBarOffset + kNumBars * 8 + 16;
+    static constexpr int kGswOffset = kOffOffset + (kMaxExperts + 1) * 4;
+    static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
 };
 static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<false>::kSmemBytes <= 232448, "shared memory budget");
 static_assert(Cfg<false>::kOutOffset % 1024 == 0, "store staging boxes sit on 1024-byte swizzle atoms");
@@ -65,7 +67,7 @@ __device__ __forceinline__ WTile wgrad_tile(const int32_t *off, int num_mt, int 
     const int rem = tile - w.e * per;
     w.mt = rem / num_nt;
     w.nt = rem - w.mt * num_nt;
-    const int32_t lo = min(max(__ldg(off + w.e), 0), rows_cap), hi = min(max(__ldg(off + w.e + 1), 0), rows_cap);
+    const int32_t lo = min(max(off[w.e], 0), rows_cap), hi = min(max(off[w.e + 1], 0), rows_cap);
     w.k0 = lo;
     w.nk = hi > lo ? (hi - lo) / 64 : 0;
     return w;
@@ -75,7 +77,7 @@ __device__ __forceinline__ int expert_of(const int32_t *off, int E, int32_t m0) 
     int lo = 0, hi = E - 1;  // first e with off[e+1] > m0
     while (lo < hi) {
         int mid = (lo + hi) >> 1;
-        if (__ldg(off + mid + 1) <= m0) lo = mid + 1;
+        if (off[mid + 1] <= m0) lo = mid + 1;
         else hi = mid;
     }
     return lo;
@@ -98,10 +100,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = acc_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    const int32_t *s_off = p.offsets;  // read-only for the kernel: read through __ldg
+    int32_t *s_off = reinterpret_cast<int32_t *>(smem + C::kOffOffset);
+    float *s_gsw = reinterpret_cast<float *>(smem + C::kGswOffset);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = p.offsets[i];
+    if (FP4)
+        for (int i = threadIdx.x; i < E; i += blockDim.x) s_gsw[i] = p.gs_w[i];
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
@@ -130,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     // rows beyond the caller's buffers are never touched, whatever offsets hold
-    const int32_t total_rows = min(__ldg(s_off + E), p.rows_cap) & ~(kBM - 1);
+    const int32_t total_rows = min(s_off[E], p.rows_cap) & ~(kBM - 1);
     const int num_nt = (int)(p.N / kBN);
     // weight-gradient mode (BF16): tiles (expert, M tile, N tile), each reducing over its expert's rows
     const bool wgrad = !FP4 && p.wgrad;
@@ -438,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int mt = tile / num_nt, nt = tile - mt * num_nt;
             const int64_t row = (int64_t)mt * kBM + row_in_tile;
-            const float gmul = FP4 ? __fmul_rn(gsa, __ldg(p.gs_w + expert_of(s_off, E, mt * kBM))) : 1.0f;
+            const float gmul = FP4 ? __fmul_rn(gsa, s_gsw[expert_of(s_off, E, mt * kBM)]) : 1.0f;
             if (swiglu) {
                 uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 128 + 64 * half;
 #pragma unroll

@@ -249,32 +249,38 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
         return m;
     };
     // This warp's rows m = first + i * nwarps_total (i < nrows) and their
-    // segments, flat index j -> row i = j / segs, segment j % segs; slot
-    // j % kQSlots of the warp's ring holds segment j.
+    // segments, in order, flat index j; slot j % kQSlots of the warp's ring
+    // holds segment j.  Lane 0 issues them ahead of the warp (position pm, pseg,
+    // count pj); the warp consumes them at (m, seg), j.
+    static_assert((kQSlots & (kQSlots - 1)) == 0, "slot index by mask");
     uint8_t *ring = q_ring + (size_t)wid * kQSlots * 1024;
     uint64_t *bars = s_qbar[wid];
     const int64_t first = (int64_t)blockIdx.x * kQWarps + wid;
     const int64_t nrows = first < a.M ? (a.M - 1 - first) / nwarps_total + 1 : 0;
     const int64_t nseg = nrows * segs;
-    auto issue = [&](int64_t j) {  // lane 0: segment j into its slot
-        const int64_t m = first + (j / segs) * nwarps_total;
-        const int sg = (int)(j % segs);
-        const int slot = (int)(j % kQSlots);
-        const uint32_t bytes = (uint32_t)min(32, nb - 32 * sg) * 32u;
+    int64_t pm = first, pj = 0;
+    int pseg = 0;
+    auto issue_next = [&]() {  // lane 0: segment pj into its slot
+        const int slot = (int)(pj & (kQSlots - 1));
+        const uint32_t bytes = (uint32_t)min(32, nb - 32 * pseg) * 32u;
         mbar_arrive_expect_tx(&bars[slot], bytes);
-        bulk_load(ring + slot * 1024, xt + source_row(m) * a.ldx + (int64_t)sg * 512, bytes, &bars[slot]);
+        bulk_load(ring + slot * 1024, xt + source_row(pm) * a.ldx + (int64_t)pseg * 512, bytes, &bars[slot]);
+        ++pj;
+        if (++pseg == segs) {
+            pseg = 0;
+            pm += nwarps_total;
+        }
     };
     if (lane == 0) {
         for (int sl = 0; sl < kQSlots; ++sl) mbar_init(&bars[sl], 1);
         fence_barrier_init();
-        for (int64_t j = 0; j < nseg && j < kQSlots; ++j) issue(j);
+        while (pj < nseg && pj < kQSlots) issue_next();
     }
     __syncwarp();
-    int64_t j = 0;
+    int64_t j = 0, m = first;
+    int seg = 0;
     bool ok = true;
     for (; j < nseg; ++j) {
-        const int seg = (int)(j % segs);
-        const int64_t m = first + (j / segs) * nwarps_total;
         if (MODE != kModeFake && seg == 0) {
             // destination rows of this source row: lane f resolves the f-th
             __syncwarp();  // the previous row's readers of s_cbase / s_sbase are done
@@ -287,7 +293,7 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
             }
             __syncwarp();
         }
-        const int slot = (int)(j % kQSlots);
+        const int slot = (int)(j & (kQSlots - 1));
         const bool got = mbar_wait_bounded(&bars[slot], (uint32_t)(j / kQSlots) & 1u, kQWaitNs);
         if (!__all_sync(0xffffffffu, got)) {
             ok = false;
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
             }
         }
         __syncwarp();  // every lane is done with the slot (and, at a row's end, the stage is complete)
-        if (lane == 0 && j + kQSlots < nseg) issue(j + kQSlots);
+        if (lane == 0 && pj < nseg) issue_next();
 
         if (MODE != kModeFake && has_sel && seg == segs - 1) {
             // the row's residual (activation) or unscaled dequantized weight on S
@@ -384,12 +390,16 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
             }
             __syncwarp();  // the stage is read out before the next row writes it
         }
+        if (++seg == segs) {
+            seg = 0;
+            m += nwarps_total;
+        }
     }
     if (!ok && lane == 0) {
         // a segment never arrived: report it, and let every copy still in flight land before the CTA exits
         report(a.dev_status, NVFP4_ERR_TIMEOUT);
-        for (int64_t jj = j; jj < nseg && jj < j + kQSlots; ++jj)
-            (void)mbar_wait_bounded(&bars[jj % kQSlots], (uint32_t)(jj / kQSlots) & 1u, kQWaitNs);
+        for (int64_t jj = j; jj < pj; ++jj)
+            (void)mbar_wait_bounded(&bars[jj & (kQSlots - 1)], (uint32_t)(jj / kQSlots) & 1u, kQWaitNs);
     }
 }
 
@@ -925,6 +935,148 @@ static int launch_quantize(dim3 grid, const QuantArgs &a, cudaStream_t st, const
     return launch_status(name);
 }
 
+// QDQ_W of many weight tensors (QUADS §3.2 Eq. 12) in one persistent launch
+// that reads every tensor from HBM once: its amax and its quantize-dequantize
+// are two kinds of work items of kFQRows rows, taken from one counter in the
+// order A(0), A(1), B(0), A(2), B(1), ..., B(nt-1) -- A(t) the amax of tensor
+// t, B(t) its QDQ -- so that B(t) re-reads rows that A(t) read shortly before
+// and that still sit in L2.  A B(t) item starts once every A(t) item has
+// added its maximum (a per-tensor count of finished A items, waited on with a
+// bound); no A item ever waits, and every A(t) item is taken before any B(t)
+// item, so the wait always ends.  Scratch (32-bit words, zeroed by the
+// caller's stream before the launch): amax[nt], done[nt], the work counter.
+constexpr int kFQRows = 64;
+constexpr uint64_t kFQWaitNs = 2000000000ull;
+
+struct FQArgs {
+    const uint16_t *w;
+    uint16_t *w_hat;
+    int64_t rows, cols;
+    int32_t nt, per;  // tensors, items per tensor and kind
+    uint32_t *ws;     // amax bits [nt], done [nt], counter
+    float *gs_out;
+    int32_t *dev_status;
+};
+
+__global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
+    __shared__ QTables tb;
+    __shared__ int64_t s_item;
+    __shared__ uint32_t s_red[8];
+    __shared__ int s_ok;
+    fill_tables(tb);
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const int64_t total = 2ll * a.nt * a.per;
+    const int nb = (int)(a.cols >> 4), segs = (nb + 31) >> 5;
+    uint32_t *amax_bits = a.ws, *done = a.ws + a.nt, *counter = a.ws + 2 * a.nt;
+    for (;;) {
+        __syncthreads();  // the previous item's readers of s_item, s_red and s_ok are done (and the tables ready)
+        if (threadIdx.x == 0) s_item = (int64_t)atomicAdd(counter, 1u);
+        __syncthreads();
+        const int64_t item = s_item;
+        if (item >= total) break;
+        // group gi: 0 -> A(0); 2nt-1 -> B(nt-1); odd -> A((gi+1)/2); even -> B(gi/2 - 1)
+        const int64_t gi = item / a.per;
+        const int chunk = (int)(item - gi * a.per);
+        const bool is_a = gi == 0 || (gi != 2ll * a.nt - 1 && (gi & 1));
+        const int t = gi == 0 ? 0 : (gi == 2ll * a.nt - 1 ? a.nt - 1 : (int)((gi & 1) ? (gi + 1) / 2 : gi / 2 - 1));
+        const int64_t r0 = (int64_t)chunk * kFQRows;
+        const int64_t r1 = min(a.rows, r0 + kFQRows);
+        const uint16_t *wt = a.w + (int64_t)t * a.rows * a.cols;
+        if (is_a) {
+            // max |w| of the rows: bit patterns of |bf16| order like the values (NaN above Inf)
+            const uint4 *p = reinterpret_cast<const uint4 *>(wt + r0 * a.cols);
+            const int64_t nvec = (r1 - r0) * (a.cols >> 3);
+            uint32_t mx = 0u;
+            int64_t i = threadIdx.x;
+            for (; i + 3 * 256 < nvec; i += 4 * 256) {
+                const uint4 v0 = __ldg(p + i), v1 = __ldg(p + i + 256), v2 = __ldg(p + i + 512), v3 = __ldg(p + i + 768);
+                const uint32_t w16[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
+                                          v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+                for (int u = 0; u < 16; ++u) mx = __vmaxu2(mx, w16[u] & 0x7fff7fffu);
+            }
+            for (; i < nvec; i += 256) {
+                const uint4 v = __ldg(p + i);
+                mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
+                mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
+                mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
+                mx = __vmaxu2(mx, v.w & 0x7fff7fffu);
+            }
+            uint32_t m16 = max(mx & 0xffffu, mx >> 16);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m16 = max(m16, __shfl_xor_sync(0xffffffffu, m16, o));
+            if (lane == 0) s_red[wid] = m16;
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                uint32_t r = 0u;
+                for (int q = 0; q < 8; ++q) r = max(r, s_red[q]);
+                atomicMax(amax_bits + t, r << 16);
+                __threadfence();  // the maximum is visible before the item counts as done
+                atomicAdd(done + t, 1u);
+            }
+            continue;
+        }
+        // B(t): wait for every A(t) item, then quantize-dequantize the rows
+        if (threadIdx.x == 0) {
+            const volatile uint32_t *d = done + t;
+            bool ok = *d >= (uint32_t)a.per;
+            const uint64_t t0 = global_ns();
+            while (!ok) {
+                __nanosleep(200);
+                ok = *d >= (uint32_t)a.per;
+                if (!ok && global_ns() - t0 > kFQWaitNs) break;
+            }
+            __threadfence();
+            s_ok = ok;
+            if (!ok) report(a.dev_status, NVFP4_ERR_TIMEOUT);
+        }
+        __syncthreads();
+        if (!s_ok) continue;
+        const float amax_t = __uint_as_float(*(const volatile uint32_t *)(amax_bits + t));
+        const float gs = tensor_scale(amax_t);
+        const float p6 = __fmul_rn(gs, 6.0f);
+        const float inv_gs = __frcp_rn(gs);
+        if (chunk == 0 && threadIdx.x == 0) {
+            if (a.gs_out) a.gs_out[t] = gs;
+            if (!isfinite(amax_t)) report(a.dev_status, NVFP4_ERR_NONFINITE);
+        }
+        uint16_t *ot = a.w_hat + (int64_t)t * a.rows * a.cols;
+        for (int64_t m = r0 + wid; m < r1; m += 8) {
+            const uint16_t *xr = wt + m * a.cols;
+            uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
+            if (lane < nb) {
+                ra = __ldg(reinterpret_cast<const uint4 *>(xr + lane * 16));
+                rb = __ldg(reinterpret_cast<const uint4 *>(xr + lane * 16) + 1);
+            }
+            for (int seg = 0; seg < segs; ++seg) {
+                const int b = seg * 32 + lane;
+                const uint4 ca = ra, cb = rb;
+                if (b + 32 < nb) {  // the next segment's loads in flight
+                    ra = __ldg(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16));
+                    rb = __ldg(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16) + 1);
+                }
+                if (b < nb) {
+                    float v[16];
+                    BlockQ q;
+                    unpack_block(ca, cb, v);
+                    quant_block(v, gs, p6, inv_gs, tb, q);
+                    uint32_t o[8];
+#pragma unroll
+                    for (int u = 0; u < 16; u += 2) {
+                        const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(u)), q.sbf), gs);
+                        const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(u + 1)), q.sbf), gs);
+                        o[u / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
+                                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(ot + m * a.cols + b * 16);
+                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                }
+            }
+        }
+    }
+}
+
 static int amax_launch(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t nt, int64_t tstride, float *out,
                        cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)nt, st);
@@ -991,26 +1143,34 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
 extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat, float *gs_out,
                                 float *amax_ws, int32_t *dev_status, void *stream) {
     if (!w || !w_hat || !amax_ws || nt < 1 || rows < 0 || cols < 0) return NVFP4_ERR_INVALID_ARG;
-    if (cols % 32 || cols / 16 > kMaxBlocksPerRow || nt > 65535) return NVFP4_ERR_UNSUPPORTED;
+    // items are counted in 32 bits
+    if (cols % 32 || cols / 16 > kMaxBlocksPerRow || nt > 65535 || 2 * (int64_t)nt * ((rows + kFQRows - 1) / kFQRows) > (1ll << 31))
+        return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(w) || !aligned16(w_hat)) return NVFP4_ERR_ALIGNMENT;
     NVFP4_CHECK_INIT();
     cudaStream_t st = (cudaStream_t)stream;
-    int s = amax_launch(w, rows, cols, cols, nt, rows * cols, amax_ws, st);
-    if (s != NVFP4_OK || rows == 0) return s;
-    QuantArgs a{};
-    a.x = (const uint16_t *)w;
-    a.M = rows;
-    a.K = cols;
-    a.ldx = cols;
-    a.x_tstride = rows * cols;
-    a.amax = amax_ws;
-    a.gs_out = gs_out;
-    a.fanout = 1;
+    // scratch: amax[nt], done[nt], the work counter -- all start at zero
+    const cudaError_t e = cudaMemsetAsync(amax_ws, 0, sizeof(float) * (2 * (size_t)nt + 1), st);
+    if (e != cudaSuccess) {
+        set_last_error("cudaMemsetAsync(fake-quant scratch)", e);
+        return NVFP4_ERR_CUDA;
+    }
+    if (rows == 0 || cols == 0) return NVFP4_OK;
+    FQArgs a{};
+    a.w = (const uint16_t *)w;
     a.w_hat = (uint16_t *)w_hat;
-    a.what_tstride = rows * cols;
+    a.rows = rows;
+    a.cols = cols;
+    a.nt = nt;
+    a.per = (int32_t)((rows + kFQRows - 1) / kFQRows);
+    a.ws = reinterpret_cast<uint32_t *>(amax_ws);
+    a.gs_out = gs_out;
     a.dev_status = dev_status;
-    int g = quant_grid(rows) / (nt > 8 ? 8 : nt);
-    return launch_quantize<kModeFake>(dim3(g < 1 ? 1 : g, nt), a, st, "quantize_kernel<fake>");
+    const int64_t items = 2ll * nt * a.per;
+    int64_t grid = (int64_t)sm_count() * 4;
+    if (grid > items) grid = items;
+    fake_quant_fused_kernel<<<(unsigned)grid, 256, 0, st>>>(a);
+    return launch_status("fake_quant_fused_kernel");
 }
 
 extern "C" int nvfp4_fake_quant_transposed(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat,
@@ -1200,8 +1360,9 @@ extern "C" int nvfp4_rac_select_channels(const void *x, int64_t M, int64_t K, co
 // for the per-tensor amax; this variant keeps them in a fixed array in device
 // memory that the library itself declares, so nothing is allocated at call time.
 namespace nvfp4 {
-constexpr int kNoAllocMaxTensors = 4096;  // 16 KB per GPU that loads the library
-static __device__ __align__(256) float g_noalloc_amax[kNoAllocMaxTensors];
+constexpr int kNoAllocMaxTensors = 4096;
+// nvfp4_fake_quant's scratch for that many tensors (amax, done counts, counter): 32 KB per GPU
+static __device__ __align__(256) float g_noalloc_amax[2 * kNoAllocMaxTensors + 1];
 // device address of the array per device ordinal, and the CUDA context it was looked up in
 static float *g_noalloc_addr[64];
 static void *g_noalloc_ctx[64];

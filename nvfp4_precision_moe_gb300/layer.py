@@ -214,7 +214,7 @@ class QatMoE:
         self.wd_hat = torch.empty_like(w_down) if fake else w_down
         self.gs13 = torch.empty(self.E, dtype=torch.float32, device=dev)
         self.gsd = torch.empty(self.E, dtype=torch.float32, device=dev)
-        self.amax_ws = torch.empty(self.E, dtype=torch.float32, device=dev)
+        self.amax_ws = torch.empty(2 * self.E + 1, dtype=torch.float32, device=dev)  # nvfp4_fake_quant scratch
         self.max_tokens = max_tokens
         self.rows_cap = rows_capacity(max_tokens, topk, self.E)
         self.route = _Routing(max_tokens, self.E, topk, dev)
@@ -245,7 +245,7 @@ class QatMoE:
         if sym:
             self.x_hat = torch.empty((max_tokens, self.H), dtype=torch.bfloat16, device=dev)
             self.h_hat = torch.zeros((self.rows_cap, self.I), dtype=torch.bfloat16, device=dev)
-            self.act_amax = torch.empty(2, dtype=torch.float32, device=dev)
+            self.act_amax = torch.empty(6, dtype=torch.float32, device=dev)  # two 3-word nvfp4_fake_quant scratches
             self.act_gs = torch.empty(2, dtype=torch.float32, device=dev)
 
     def fake_quant(self, stream=None):
@@ -278,7 +278,7 @@ class QatMoE:
         nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=stream)
         mark(2)
         if self.sym:  # QDQ_A of x over the batch's T tokens (the rollout's amax)
-            nvfp4_fake_quant(x.view(1, T, self.H), self.x_hat[:T].view(1, T, self.H), self.act_amax[0:1],
+            nvfp4_fake_quant(x.view(1, T, self.H), self.x_hat[:T].view(1, T, self.H), self.act_amax[0:3],
                              gs_out=self.act_gs[0:1], dev_status=self.dev_status, stream=stream)
             x = self.x_hat[:T]
         nvfp4_moe_scatter_rows(x, self.topk, dst, r.counts, r.offsets, self.E, self.xr, stream=stream)
@@ -300,7 +300,7 @@ class QatMoE:
         h = self.h
         if self.sym:
             nvfp4_fake_quant(self.h[:cap].view(1, cap, self.I), self.h_hat[:cap].view(1, cap, self.I),
-                             self.act_amax[1:2], gs_out=self.act_gs[1:2], dev_status=self.dev_status,
+                             self.act_amax[3:6], gs_out=self.act_gs[1:2], dev_status=self.dev_status,
                              stream=stream)
             h = self.h_hat
         mark(4)

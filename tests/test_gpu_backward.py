@@ -50,7 +50,7 @@ def test_fake_quant_transposed(nv):
     got = torch.empty_like(w)
     got_t = torch.empty((3, 320, 192), dtype=torch.bfloat16, device=G.DEV)
     gs_ref, gs_got = G.zeros(3, torch.float32), G.zeros(3, torch.float32)
-    nv.nvfp4_fake_quant(w, ref, G.zeros(3, torch.float32), gs_out=gs_ref)
+    nv.nvfp4_fake_quant(w, ref, G.zeros(7, torch.float32), gs_out=gs_ref)
     nv.nvfp4_fake_quant_transposed(w, got, got_t, G.zeros(3, torch.float32), gs_out=gs_got)
     torch.cuda.synchronize()
     assert torch.equal(got, ref) and torch.equal(gs_got, gs_ref)

@@ -204,7 +204,7 @@ def test_fake_quant_parity():
     wd = w.to(G.DEV)
     w_hat = torch.empty_like(wd)
     gs = G.zeros(3, torch.float32)
-    amax = G.zeros(3, torch.float32)
+    amax = G.zeros(7, torch.float32)  # 2 * 3 + 1 words of scratch
     st = G.zeros(1, torch.int32)
     nv.nvfp4_fake_quant(wd, w_hat, amax, gs_out=gs, dev_status=st)
     torch.cuda.synchronize()
@@ -223,7 +223,7 @@ def test_fake_quant_equals_rollout_dequant():
     w = synth.dense_weight(1)[:256]
     wd = w.to(G.DEV)[None]
     w_hat = torch.empty_like(wd)
-    nv.nvfp4_fake_quant(wd, w_hat, G.zeros(1, torch.float32))
+    nv.nvfp4_fake_quant(wd, w_hat, G.zeros(3, torch.float32))
     K = 512
     S = torch.arange(K, dtype=torch.int32, device=G.DEV)
     codes = G.zeros((1, 256, K // 2), torch.uint8)

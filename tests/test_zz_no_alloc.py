@@ -34,7 +34,7 @@ def test_noalloc_fake_quant_matches_allocating_entry_point():
         got = torch.empty_like(w)
         gs_ref = torch.zeros(nt, dtype=torch.float32, device="cuda:0")
         gs_got = torch.zeros(nt, dtype=torch.float32, device="cuda:0")
-        amax_ws = torch.zeros(nt, dtype=torch.float32, device="cuda:0")
+        amax_ws = torch.zeros(2 * nt + 1, dtype=torch.float32, device="cuda:0")
         status = torch.zeros(1, dtype=torch.int32, device="cuda:0")
         assert L.nvfp4_fake_quant(w.data_ptr(), nt, rows, cols, ref.data_ptr(), gs_ref.data_ptr(),
                                   amax_ws.data_ptr(), status.data_ptr(), stream) == 0
@@ -56,7 +56,7 @@ def test_noalloc_without_optional_outputs():
     w = _inputs(3, nt, rows, cols, 3.0)
     ref = torch.empty_like(w)
     got = torch.empty_like(w)
-    amax_ws = torch.zeros(nt, dtype=torch.float32, device="cuda:0")
+    amax_ws = torch.zeros(2 * nt + 1, dtype=torch.float32, device="cuda:0")
     assert L.nvfp4_fake_quant(w.data_ptr(), nt, rows, cols, ref.data_ptr(), None, amax_ws.data_ptr(), None,
                               stream) == 0
     assert L.nvfp4_fake_quant_noalloc(w.data_ptr(), nt, rows, cols, got.data_ptr(), None, None, stream) == 0
