@@ -33,8 +33,8 @@ NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense tensor-core ratio, nominal
 # one ncu capture of the gemm13_moe profile case, valid only for the kernel
 # sources it was taken on (common.cuh, gemm_common.cuh, gemm_single.cu): reported as null
 # once they change.
-GATE_UP_TRAFFIC = {"bytes": 1362286000 + 415321088,
-                   "sources_sha256": "8dba006fff9f0106fc9337d001b5f8f1118b95edae3f7eef9bb7910f13f30f4c"}
+GATE_UP_TRAFFIC = {"bytes": 1362302000 + 414904320,
+                   "sources_sha256": "d41b59e62bfa151d0332707bdcb1d38218ac2279311d9104ad1b6aeedd0e0a38"}
 
 
 def gate_up_traffic():
@@ -799,6 +799,22 @@ def run_profile_case(args):
         ws = torch.zeros(2 * E + 1, dtype=torch.float32, device=dev)
         gsw = torch.empty(E, dtype=torch.float32, device=dev)
         fn = lambda: nv.nvfp4_fake_quant(w, w_hat, ws, gs_out=gsw)
+        flops = 0
+    elif case == "quantize_x_syn":
+        # a synthetic stand-in for ncu: 16384 x 4096 dispatched to 8 routed rows each (a random
+        # permutation of the rows), k = 128 channels clustered in the first 512-element segment
+        T, H, topk, k = 16384, 4096, 8, 128
+        x = torch.randn((T, H), device=dev, generator=g).to(torch.bfloat16)
+        cap = T * topk
+        dst = torch.randperm(cap, device=dev, generator=g).to(torch.int32).view(T, topk)
+        codes = torch.empty((cap, H // 2), dtype=torch.uint8, device=dev)
+        scales = torch.empty(nv.scale_bytes(cap, H), dtype=torch.uint8, device=dev)
+        resid = torch.empty((cap, k), dtype=torch.bfloat16, device=dev)
+        S = torch.arange(k, dtype=torch.int32, device=dev)
+        amax = torch.zeros(1, device=dev)
+        nv.nvfp4_amax(x, amax)
+        fn = lambda: nv.nvfp4_quantize(x, amax, codes, scales, resid=resid, S=S, dst_row=dst, fanout=topk,
+                                       rows_out=cap)
         flops = 0
     elif case == "quantize_h_syn":
         # a synthetic stand-in for ncu (few launches before it): 147456 x 1536, the k = 128

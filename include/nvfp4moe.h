@@ -301,8 +301,11 @@ int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8_t *w_scale
  *                     on `stream` before the kernel runs.
  * Rows of a segment beyond the expert's real token count must hold zero
  * codes/scales/residual (nvfp4_moe_clear_padding); their outputs are zero.
+ * The correction runs ceil(k/64) BF16 slices after the K loop, so any k up to
+ * K works (the pages' k = 50% of the channels, QUADS §4.4.1, included; its
+ * cost grows with k).
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 256, N % 256, k % 16,
- * k > 256, E > 1024); dev_status gets TIMEOUT if a pipeline wait runs out. */
+ * k > K, E > 1024); dev_status gets TIMEOUT if a pipeline wait runs out. */
 int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
                                 const void *a_resid, const float *gs_a, const uint8_t *w_codes,
                                 const uint8_t *w_scales, const float *gs_w, const void *w_sel,

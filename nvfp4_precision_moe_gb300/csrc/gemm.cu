@@ -44,7 +44,7 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
     if (epilogue == NVFP4_EPI_SWIGLU && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
     const int64_t ncols = epilogue == NVFP4_EPI_SWIGLU ? N / 2 : N;
     if (ldy < ncols) return NVFP4_ERR_INVALID_ARG;
-    if (K % 256 || N % 256 || k % 16 || k > 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) ||
+    if (K % 256 || N % 256 || k % 16 || k > K || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) ||
         (int64_t)E * N > (1ll << 31))
         return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(a_codes) || !aligned16(a_scales) || !aligned16(w_codes) || !aligned16(w_scales) || !aligned16(y) ||

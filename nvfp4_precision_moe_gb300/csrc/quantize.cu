@@ -18,7 +18,7 @@ namespace nvfp4 {
 
 constexpr int kMaxBlocksPerRow = 1024;  // K <= 16384
 
-enum QuantMode { kModeAct = 0, kModeWeight = 1, kModeFake = 2 };
+enum QuantMode { kModeAct = 0, kModeWeight = 1 };
 
 struct QuantArgs {
     const uint16_t *x;
@@ -37,8 +37,6 @@ struct QuantArgs {
     uint16_t *resid;         // act mode: [rows_out, k]
     uint16_t *wsel;          // weight mode: [rows, k] per tensor
     int64_t wsel_tstride;
-    uint16_t *w_hat;  // fake mode: [M, K] per tensor
-    int64_t what_tstride;
     int32_t interleave;
     int32_t *dev_status;
 };
@@ -87,6 +85,14 @@ __device__ __forceinline__ uint32_t e2m1x8(const float *q) {
     return w;
 }
 
+// (a0, a1) * (b0, b1) as two IEEE binary32 products (round to nearest) in one
+// packed instruction.
+__device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1, float &r0, float &r1) {
+    asm("{ .reg .b64 x, y, z; mov.b64 x, {%2, %3}; mov.b64 y, {%4, %5}; mul.rn.f32x2 z, x, y; mov.b64 {%0, %1}, z; }"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Per-block tables, filled once per CTA (gs is a power of two, so scaling by
 // it commutes with rounding in the normal range):
 //   div6[m] = fl((1 + m/128) / 6): fl(a / (6 gs)) = div6[mant7(a)] * 2^exp(a) / gs
@@ -109,9 +115,12 @@ __device__ __forceinline__ float pow2f(int n) { return __uint_as_float((uint32_t
 
 __device__ __forceinline__ void quant_block(const float (&v)[16], float gs, float p6, float inv_gs,
                                             const QTables &tb, BlockQ &q) {
-    float amax_b = 0.0f;
+    float m8[8];  // the block amax as a tree of maxima (a short dependency chain)
 #pragma unroll
-    for (int t = 0; t < 16; ++t) amax_b = fmaxf(amax_b, fabsf(v[t]));
+    for (int t = 0; t < 8; ++t) m8[t] = fmaxf(fabsf(v[2 * t]), fabsf(v[2 * t + 1]));
+#pragma unroll
+    for (int t = 0; t < 4; ++t) m8[t] = fmaxf(m8[t], m8[t + 4]);
+    const float amax_b = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
     // block scale: E4M3 of fl(amax_b / (6*gs)), RNE with saturation
     const uint32_t ab = __float_as_uint(amax_b);
     const int ex = (int)(ab >> 23);  // biased exponent of the block amax
@@ -125,7 +134,7 @@ __device__ __forceinline__ void quant_block(const float (&v)[16], float gs, floa
         const float inv = __fmul_rn(tb.rcp[q.sb], inv_gs);  // = the correctly rounded 1/den
         float qv[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) qv[t] = __fmul_rn(v[t], inv);
+        for (int t = 0; t < 16; t += 2) fmul2_rn(v[t], v[t + 1], inv, inv, qv[t], qv[t + 1]);
         q.w0 = e2m1x8(qv);
         q.w1 = e2m1x8(qv + 8);
     } else {  // a zero block scale: signed zeros
@@ -174,6 +183,18 @@ __device__ __forceinline__ uint16_t resid_value(uint16_t xb, uint32_t sb, float 
     return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
 }
 
+// The RAC value of element x (BF16 bits) already quantized to code c in a
+// block of scale value sbf -- the value resid_value computes, from the code the
+// block stored rather than a recomputed one.
+template <int MODE>
+__device__ __forceinline__ uint16_t rac_from_code(uint16_t xb, uint32_t c, float sbf, float gs, float inv_gs) {
+    const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
+    if (MODE == kModeWeight) return __bfloat16_as_ushort(__float2bfloat16_rn(cs));
+    const float v = __uint_as_float((uint32_t)xb << 16);
+    const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
+    return __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(r, inv_gs)));
+}
+
 // One warp per output row (grid-stride), the row in segments of 32 blocks
 // (512 elements, one block per lane).  A warp's segments -- all of its rows',
 // in order -- stream through a ring of kQSlots 1 KB slots in shared memory:
@@ -203,7 +224,7 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
     fill_tables(s_tab);
     const int nb = (int)(a.K >> 4);
     const int64_t kslices = (nb + 15) >> 4;
-    const bool has_sel = (MODE != kModeFake) && a.k > 0;
+    const bool has_sel = a.k > 0;
     const bool staged = a.k <= kMaxStagedK;
     const int segs = (nb + 31) >> 5;
     if (has_sel && staged) {
@@ -281,7 +302,7 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
     int seg = 0;
     bool ok = true;
     for (; j < nseg; ++j) {
-        if (MODE != kModeFake && seg == 0) {
+        if (seg == 0) {
             // destination rows of this source row: lane f resolves the f-th
             __syncwarp();  // the previous row's readers of s_cbase / s_sbase are done
             if (lane < fanout) {
@@ -314,30 +335,37 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
             q.w0 = q.w1 = 0u;
         }
 
-        if (MODE == kModeFake) {
-            if (valid) {
-                uint32_t o[8];
-#pragma unroll
-                for (int t = 0; t < 16; t += 2) {
-                    const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
-                    const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
-                    o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
-                               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
-                }
-                uint4 *dst = reinterpret_cast<uint4 *>(a.w_hat + (int64_t)tensor * a.what_tstride + m * a.K + b * 16);
-                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            }
-        } else {
+        {
             if (has_sel) {
                 if (staged) {
-                    // this segment's selected channels, one per lane: the RAC value goes to the stage
+                    // this segment's selected channels, one or two per lane per pass: the
+                    // element from the slot, its code and block scale from the block's lane;
+                    // the RAC value goes to the stage
                     const int i0 = s_segfirst[seg], i1 = s_segfirst[seg + 1];
-                    for (int base = i0; base < i1; base += 32) {  // the same trip count in every lane
-                        const int i = base + lane;
-                        const int jc = i < i1 ? s_S[i] : seg * 512;
-                        const uint32_t sbl = __shfl_sync(0xffffffffu, q.sb, (jc >> 4) & 31);
-                        if (i < i1) stage[i] = resid_value<MODE>(xs[jc - seg * 512], sbl, gs, inv_gs, s_tab);
+                    for (int base = i0; base < i1; base += 64) {  // the same trip count in every lane
+                        const int ia = base + lane, ib = base + 32 + lane;
+                        const int ja = ia < i1 ? s_S[ia] : 0;
+                        const uint16_t xa = ia < i1 ? xs[ja - seg * 512] : 0;
+                        const int oa = (ja >> 4) & 31;
+                        const uint32_t a0 = __shfl_sync(0xffffffffu, q.w0, oa), a1 = __shfl_sync(0xffffffffu, q.w1, oa);
+                        const float fa = __shfl_sync(0xffffffffu, q.sbf, oa);
+                        if (base + 32 < i1) {  // uniform: a second channel for some lanes
+                            const int jb = ib < i1 ? s_S[ib] : 0;
+                            const uint16_t xb = ib < i1 ? xs[jb - seg * 512] : 0;
+                            const int ob = (jb >> 4) & 31;
+                            const uint32_t b0 = __shfl_sync(0xffffffffu, q.w0, ob), b1 = __shfl_sync(0xffffffffu, q.w1, ob);
+                            const float fb = __shfl_sync(0xffffffffu, q.sbf, ob);
+                            if (ib < i1) {
+                                const int tb = jb & 15;
+                                stage[ib] = rac_from_code<MODE>(xb, ((tb < 8 ? b0 : b1) >> (4 * (tb & 7))) & 15u, fb, gs,
+                                                                inv_gs);
+                            }
+                        }
+                        if (ia < i1) {
+                            const int ta = ja & 15;
+                            stage[ia] = rac_from_code<MODE>(xa, ((ta < 8 ? a0 : a1) >> (4 * (ta & 7))) & 15u, fa, gs,
+                                                            inv_gs);
+                        }
                     }
                 } else if (valid) {
                     row_sb[b] = (uint8_t)q.sb;
@@ -361,7 +389,7 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
         __syncwarp();  // every lane is done with the slot (and, at a row's end, the stage is complete)
         if (lane == 0 && pj < nseg) issue_next();
 
-        if (MODE != kModeFake && has_sel && seg == segs - 1) {
+        if (has_sel && seg == segs - 1) {
             // the row's residual (activation) or unscaled dequantized weight on S
             const uint16_t *xrow = xt + source_row(m) * a.ldx;
             if (!staged) {  // k beyond the stage: one selected channel per lane, straight to every destination
@@ -945,8 +973,37 @@ static int launch_quantize(dim3 grid, const QuantArgs &a, cudaStream_t st, const
 // bound); no A item ever waits, and every A(t) item is taken before any B(t)
 // item, so the wait always ends.  Scratch (32-bit words, zeroed by the
 // caller's stream before the launch): amax[nt], done[nt], the work counter.
-constexpr int kFQRows = 64;
+// Items are kept small (8 rows, one per warp) so that the items in flight at
+// once -- one per resident block -- span only about two tensors, whose rows
+// then fit in L2 between their two reads.
+constexpr int kFQRows = 8;
 constexpr uint64_t kFQWaitNs = 2000000000ull;
+
+// 16-byte global load / store with an L2 eviction-priority policy (createpolicy):
+// the amax pass keeps a tensor's lines in L2 for the second read, which then
+// lets them go, as does the output stream.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ld_hint(const uint4 *p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+__device__ __forceinline__ void st_hint(uint4 *p, const uint4 &v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w), "l"(pol)
+                 : "memory");
+}
 
 struct FQArgs {
     const uint16_t *w;
@@ -968,6 +1025,7 @@ __global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
     const int64_t total = 2ll * a.nt * a.per;
     const int nb = (int)(a.cols >> 4), segs = (nb + 31) >> 5;
     uint32_t *amax_bits = a.ws, *done = a.ws + a.nt, *counter = a.ws + 2 * a.nt;
+    const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
     for (;;) {
         __syncthreads();  // the previous item's readers of s_item, s_red and s_ok are done (and the tables ready)
         if (threadIdx.x == 0) s_item = (int64_t)atomicAdd(counter, 1u);
@@ -989,14 +1047,15 @@ __global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
             uint32_t mx = 0u;
             int64_t i = threadIdx.x;
             for (; i + 3 * 256 < nvec; i += 4 * 256) {
-                const uint4 v0 = __ldg(p + i), v1 = __ldg(p + i + 256), v2 = __ldg(p + i + 512), v3 = __ldg(p + i + 768);
+                const uint4 v0 = ld_hint(p + i, keep), v1 = ld_hint(p + i + 256, keep), v2 = ld_hint(p + i + 512, keep),
+                            v3 = ld_hint(p + i + 768, keep);
                 const uint32_t w16[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
                                           v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
 #pragma unroll
                 for (int u = 0; u < 16; ++u) mx = __vmaxu2(mx, w16[u] & 0x7fff7fffu);
             }
             for (; i < nvec; i += 256) {
-                const uint4 v = __ldg(p + i);
+                const uint4 v = ld_hint(p + i, keep);
                 mx = __vmaxu2(mx, v.x & 0x7fff7fffu);
                 mx = __vmaxu2(mx, v.y & 0x7fff7fffu);
                 mx = __vmaxu2(mx, v.z & 0x7fff7fffu);
@@ -1045,15 +1104,15 @@ __global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
             const uint16_t *xr = wt + m * a.cols;
             uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
             if (lane < nb) {
-                ra = __ldg(reinterpret_cast<const uint4 *>(xr + lane * 16));
-                rb = __ldg(reinterpret_cast<const uint4 *>(xr + lane * 16) + 1);
+                ra = ld_hint(reinterpret_cast<const uint4 *>(xr + lane * 16), drop);
+                rb = ld_hint(reinterpret_cast<const uint4 *>(xr + lane * 16) + 1, drop);
             }
             for (int seg = 0; seg < segs; ++seg) {
                 const int b = seg * 32 + lane;
                 const uint4 ca = ra, cb = rb;
                 if (b + 32 < nb) {  // the next segment's loads in flight
-                    ra = __ldg(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16));
-                    rb = __ldg(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16) + 1);
+                    ra = ld_hint(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16), drop);
+                    rb = ld_hint(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16) + 1, drop);
                 }
                 if (b < nb) {
                     float v[16];
@@ -1063,14 +1122,15 @@ __global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
                     uint32_t o[8];
 #pragma unroll
                     for (int u = 0; u < 16; u += 2) {
-                        const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(u)), q.sbf), gs);
-                        const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(u + 1)), q.sbf), gs);
+                        float c0, c1, d0, d1;
+                        fmul2_rn(e2m1_val(q.code(u)), e2m1_val(q.code(u + 1)), q.sbf, q.sbf, c0, c1);
+                        fmul2_rn(c0, c1, gs, gs, d0, d1);
                         o[u / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
                     }
                     uint4 *dst = reinterpret_cast<uint4 *>(ot + m * a.cols + b * 16);
-                    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                    st_hint(dst, make_uint4(o[0], o[1], o[2], o[3]), drop);
+                    st_hint(dst + 1, make_uint4(o[4], o[5], o[6], o[7]), drop);
                 }
             }
         }

@@ -176,6 +176,24 @@ def test_rac_k0_and_all_channels():
     assert G.rel_err(yk, w4a16) <= 2 * TOL
 
 
+def test_rac_half_and_all_channels_of_a_wide_layer():
+    """k beyond 256 (more RAC slices): half of the channels -- the pages' k = 50% setting
+    (QUADS §4.4.1) -- and all of them, where the RAC GEMM reproduces W4A16 within the BF16
+    rounding of the residual (the oracle's own pin, here on the GPU)."""
+    x = synth.u16(synth.activations(1))  # 64 x 512
+    w = synth.u16(synth.dense_weight(1))  # 512 x 512
+    sc = oracle.channel_scores_sq(x)
+    for k in (256, 512):
+        S = oracle.select_channels(sc, k)
+        d = Dense(x, w, S)
+        ref, _, wq = _oracle_dense(x, w, S)
+        y = d.run(0)[:64].cpu().numpy()
+        assert G.rel_err(y, ref) <= TOL, k
+        if k == 512:
+            w4a16 = oracle.bf16_to_f32(x).astype(np.float64) @ wq.T
+            assert G.rel_err(y, w4a16) <= 2 * TOL
+
+
 def test_grouped_ragged_segments():
     rng = np.random.default_rng(3)
     E, N, K, k = 5, 256, 512, 32
