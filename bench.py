@@ -494,22 +494,22 @@ def qat_measure(dev, steps):
     tbwd = statistics.median([bev[i][1].elapsed_time(bev[i][2]) for i in range(steps)])
     # the wgrad launches alone: dW_down then dW_13, on the buffers the backward left
     r = tl.route
-    Rc = tl.rows_cap
     wev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    dy_t, h_t = tl.t_big[:H * Rc].view(H, Rc), tl.t_small[:I * Rc].view(I, Rc)
     wev[0].record(stream)
     for _ in range(5):
-        nv.nvfp4_bf16_grouped_gemm_wgrad(dy_t, h_t, r.offsets, E, tl.dwd, dev_status=tl.dev_status)
+        nv.nvfp4_bf16_grouped_gemm_wgrad_rows(tl.dy, tl.h, r.offsets, E, tl.dwd, dev_status=tl.dev_status)
     wev[1].record(stream)
-    dgu_t, xr_t = tl.t_big[:2 * I * Rc].view(2 * I, Rc), tl.t_small[:H * Rc].view(H, Rc)
     for _ in range(5):
-        nv.nvfp4_bf16_grouped_gemm_wgrad(dgu_t, xr_t, r.offsets, E, tl.dw13, dev_status=tl.dev_status)
+        nv.nvfp4_bf16_grouped_gemm_wgrad_rows(tl.dgu, tl.xr, r.offsets, E, tl.dw13, dev_status=tl.dev_status)
     wev[2].record(stream)
     torch.cuda.synchronize()
     wd_ms, w13_ms = wev[0].elapsed_time(wev[1]) / 5, wev[1].elapsed_time(wev[2]) / 5
     del tl
     n_w = E * (2 * I * H + H * I)
     fq_bytes = 4 * n_w  # read and write every BF16 weight once
+    # the weight gradients write FP32 [E, 2I, H] and [E, H, I] and read the routed rows once
+    used = int(r.offsets[-1].item())
+    wg_bytes = 4 * n_w + 2 * used * (H + I + 2 * I + H)
     R = T * topk
     fl13, fld = 2 * R * 2 * I * H, 2 * R * H * I
     pk = peaks()
@@ -524,8 +524,12 @@ def qat_measure(dev, steps):
                            "wgrad_down_ms": round(wd_ms, 4), "wgrad_gate_up_ms": round(w13_ms, 4),
                            "wgrad_tflops": round((fld + fl13) / ((wd_ms + w13_ms) * 1e-3) / 1e12, 1),
                            "wgrad_bf16_frac": round((fld + fl13) / ((wd_ms + w13_ms) * 1e-3) / 1e12 / pk["bf16"], 4),
+                           "wgrad_gbs": round(wg_bytes / ((wd_ms + w13_ms) * 1e-3) / 1e9, 1),
+                           "wgrad_hbm_frac": round(wg_bytes / ((wd_ms + w13_ms) * 1e-3) / 1e9 / pk["hbm"], 4),
+                           "wgrad_bytes": wg_bytes,
                            "what": "QatMoE(train=True): forward keeping the gate/up pre-activations, then the "
-                                   "straight-through backward (dX, dW_13, dW_down, the combine weights' gradient)"}}
+                                   "straight-through backward (dX, dW_13, dW_down, the combine weights' gradient); "
+                                   "the weight gradients are bound by their FP32 writes (wgrad_hbm_frac)"}}
 
 
 def mismatch_measure(layer, x, logits, w13, wd):
@@ -723,7 +727,10 @@ def run_profile_case(args):
     `quantize_x` (16384 x 4096 scatter-quantize, top-8), `quantize_h`
     (147456 x 1536, k=128), `combine` (16384 tokens x 8 x 4096), `bf16_gemm`
     (QAT gate_up, BF16, same shape as gemm13), `wgrad` (the training step's dW_13 at the QAT
-    shapes for 16 experts x 256 rows, FP32 output).  Runs `--steps` launches."""
+    shapes for 16 experts x 256 rows, FP32 output, transposed operands), `wgrad_rows` (the same
+    from the routed rows as stored), `dgrad` (the input gradient with W13_hat as stored),
+    `fake_quant` / `fake_quant_down` (the QAT workload's W13 / down weights).  Runs `--steps`
+    launches."""
     import torch
 
     import nvfp4_precision_moe_gb300 as nv
@@ -791,9 +798,27 @@ def run_profile_case(args):
         dw = torch.empty((E, M, N), dtype=torch.float32, device=dev)
         fn = lambda: nv.nvfp4_bf16_grouped_gemm_wgrad(a_t, b_t, offsets, E, dw)
         flops = 2 * R * M * N
-    elif case == "fake_quant":
-        # the QAT workload's W13 fake-quant: 128 experts x 3072 x 4096 BF16 (3.2 GB read, 3.2 GB written)
-        E, N, K = int(os.environ.get("NVFP4_PROFILE_E", "128")), 3072, 4096
+    elif case in ("wgrad_rows", "dgrad"):
+        # the same dW_13 from the routed rows as stored (a = d(gate|up) [R, 3072], b = x_routed
+        # [R, 4096]); or the input gradient dx = d(gate|up) . W13_hat with W13_hat [16, 3072, 4096] as stored
+        E, per, M, N = 16, 256, 3072, 4096
+        R = E * per
+        offsets = torch.arange(0, R + 1, per, dtype=torch.int32, device=dev)
+        a = torch.randn((R, M), device=dev, generator=g).to(torch.bfloat16)
+        if case == "wgrad_rows":
+            b = torch.randn((R, N), device=dev, generator=g).to(torch.bfloat16)
+            dw = torch.empty((E, M, N), dtype=torch.float32, device=dev)
+            fn = lambda: nv.nvfp4_bf16_grouped_gemm_wgrad_rows(a, b, offsets, E, dw)
+        else:
+            w = (torch.randn((E, M, N), device=dev, generator=g) * 0.02).to(torch.bfloat16)
+            y = torch.empty((R, N), dtype=torch.bfloat16, device=dev)
+            fn = lambda: nv.nvfp4_bf16_grouped_gemm_dgrad(a, w, offsets, E, N, M, y, out_dtype=nv.NVFP4_OUT_BF16)
+        flops = 2 * R * M * N
+    elif case in ("fake_quant", "fake_quant_down"):
+        # the QAT workload's W13 fake-quant: 128 experts x 3072 x 4096 BF16 (3.2 GB read, 3.2 GB
+        # written), or its down projection's: 128 x 4096 x 1536
+        E = int(os.environ.get("NVFP4_PROFILE_E", "128"))
+        N, K = (3072, 4096) if case == "fake_quant" else (4096, 1536)
         w = (torch.randn((E, N, K), device=dev, generator=g) * 0.02).to(torch.bfloat16)
         w_hat = torch.empty_like(w)
         ws = torch.zeros(2 * E + 1, dtype=torch.float32, device=dev)

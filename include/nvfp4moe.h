@@ -267,7 +267,7 @@ int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K,
  *   w_codes, w_scales   from nvfp4_prepare_weights (E experts, N x K)
  *   S                   device int32[k], entries in [0, K) (others are clamped)
  *   w_sel               device BF16 [E, N, k]
- * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, k % 8). */
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, k % 8, E > 65535). */
 int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N, int64_t K,
                                   const int32_t *S, int32_t k, void *w_sel, void *stream);
 
@@ -393,9 +393,10 @@ int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t
  * combine backward -> dY routed; dh = dY Wd_hat; dWd = dY^T h; SwiGLU backward
  * -> d(gate|up); dx_routed = d(gate|up) W13_hat; dW13 = d(gate|up)^T x_routed;
  * dx = the sum of each token's routed rows (nvfp4_moe_combine with unit
- * weights).  The input-gradient products run on nvfp4_bf16_grouped_gemm with
- * transposed weights (nvfp4_transpose_bf16), the weight gradients on
- * nvfp4_bf16_grouped_gemm_wgrad. */
+ * weights).  The input-gradient products run on nvfp4_bf16_grouped_gemm_dgrad,
+ * which reads W_hat as stored (no transposed copy), the weight gradients on
+ * nvfp4_bf16_grouped_gemm_wgrad_rows, which reads the routed rows as stored
+ * (no transposes); nvfp4_bf16_grouped_gemm_wgrad takes transposed operands. */
 
 /* Data movement of the trainer backward (QUADS §3.2 Eq. 13).
  * y[b] = x[b]^T for `batch` row-major BF16 matrices of rows x cols (y[b] is
@@ -448,6 +449,35 @@ int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_
                                   int64_t M, int64_t N, int32_t out_dtype, void *dw, int32_t *dev_status,
                                   void *stream);
 
+/* dX = W_hat^T dY of the straight-through estimator, QUADS §3.2 Eq. 13.
+ * Grouped input gradient with the weights as stored:
+ * y[r, n] = sum_k dy[r, k] * w_hat[e, k, n] for the routed rows r of expert e
+ * (tcgen05 BF16 MMA, FP32 accumulate; the weights are read MN-major, so no
+ * transposed copy of W_hat is needed).
+ *   dy       device BF16 [rows_cap, K] (routed output gradient)
+ *   w_hat    device BF16 [E, K, N] (the forward weight: K outputs x N inputs,
+ *            e.g. nvfp4_fake_quant output)
+ *   offsets  as for nvfp4_bf16_grouped_gemm
+ *   y        device [rows_cap, N] (ldy), F32 or BF16 (out_dtype)
+ * Runs on the pipeline nvfp4_gemm_pipeline selects for BF16.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 256, E > 1024,
+ * E*K > 2^31); dev_status gets TIMEOUT if a pipeline wait runs out. */
+int nvfp4_bf16_grouped_gemm_dgrad(const void *dy, const void *w_hat, const int32_t *offsets, int32_t E,
+                                  int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, void *y,
+                                  int64_t ldy, int32_t *dev_status, void *stream);
+
+/* dW = dW_hat of the straight-through estimator, QUADS §3.2 Eq. 13, from the
+ * routed rows as stored: dw[e] = a[seg e, :]^T . b[seg e, :] for every expert
+ * e, seg e = the routed rows [offsets[e], offsets[e+1]) -- the same product
+ * as nvfp4_bf16_grouped_gemm_wgrad, with both operands read MN-major, so no
+ * transposes are needed.
+ *   a   device BF16 [R, M] (e.g. dY of a projection's output)
+ *   b   device BF16 [R, N] (e.g. its input)
+ *   offsets, dw, out_dtype, errors: as for nvfp4_bf16_grouped_gemm_wgrad. */
+int nvfp4_bf16_grouped_gemm_wgrad_rows(const void *a, const void *b, const int32_t *offsets, int32_t E,
+                                       int64_t R, int64_t M, int64_t N, int32_t out_dtype, void *dw,
+                                       int32_t *dev_status, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Diagnostics                                                                */
 /* ------------------------------------------------------------------------ */
@@ -459,6 +489,35 @@ int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_
  * to dev_status and returns normally.  Exercises the timeout path without a
  * real fault.  The GEMM pipelines use the same routine with a 2 s limit. */
 int nvfp4_selftest_wait_timeout(int32_t limit_us, int32_t *dev_status, void *stream);
+
+/* dX = W_hat^T dY of the straight-through estimator, QUADS §3.2 Eq. 13.
+ * Grouped input gradient with the weights as stored:
+ * y[r, n] = sum_k dy[r, k] * w_hat[e, k, n] for the routed rows r of expert e
+ * (tcgen05 BF16 MMA, FP32 accumulate; the weights are read MN-major, so no
+ * transposed copy of W_hat is needed).
+ *   dy       device BF16 [rows_cap, K] (routed output gradient)
+ *   w_hat    device BF16 [E, K, N] (the forward weight: K outputs x N inputs,
+ *            e.g. nvfp4_fake_quant output)
+ *   offsets  as for nvfp4_bf16_grouped_gemm
+ *   y        device [rows_cap, N] (ldy), F32 or BF16 (out_dtype)
+ * Runs on the pipeline nvfp4_gemm_pipeline selects for BF16.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 256, E > 1024,
+ * E*K > 2^31); dev_status gets TIMEOUT if a pipeline wait runs out. */
+int nvfp4_bf16_grouped_gemm_dgrad(const void *dy, const void *w_hat, const int32_t *offsets, int32_t E,
+                                  int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, void *y,
+                                  int64_t ldy, int32_t *dev_status, void *stream);
+
+/* dW = dW_hat of the straight-through estimator, QUADS §3.2 Eq. 13, from the
+ * routed rows as stored: dw[e] = a[seg e, :]^T . b[seg e, :] for every expert
+ * e, seg e = the routed rows [offsets[e], offsets[e+1]) -- the same product
+ * as nvfp4_bf16_grouped_gemm_wgrad, with both operands read MN-major, so no
+ * transposes are needed.
+ *   a   device BF16 [R, M] (e.g. dY of a projection's output)
+ *   b   device BF16 [R, N] (e.g. its input)
+ *   offsets, dw, out_dtype, errors: as for nvfp4_bf16_grouped_gemm_wgrad. */
+int nvfp4_bf16_grouped_gemm_wgrad_rows(const void *a, const void *b, const int32_t *offsets, int32_t E,
+                                       int64_t R, int64_t M, int64_t N, int32_t out_dtype, void *dw,
+                                       int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Diagnostics                                                                */

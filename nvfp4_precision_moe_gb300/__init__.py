@@ -43,6 +43,8 @@ _SIGS = {
     "nvfp4_swiglu_backward": "ppqqpp",
     "nvfp4_moe_combine_backward": "ppppiiqppiqppp",
     "nvfp4_bf16_grouped_gemm_wgrad": "pppiqqqippp",
+    "nvfp4_bf16_grouped_gemm_wgrad_rows": "pppiqqqippp",
+    "nvfp4_bf16_grouped_gemm_dgrad": "pppiqqqipqpp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
     "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
     "nvfp4_gemm_pipeline": "ip",
@@ -217,6 +219,14 @@ def nvfp4_bf16_grouped_gemm(x, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F
           epilogue, _p(y), y.stride(0), _p(dev_status), _s(stream))
 
 
+def nvfp4_bf16_grouped_gemm_dgrad(dy, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F32, dev_status=None,
+                                  stream=None):
+    """Eq. 13 dX: y = dy . w_hat[e] per expert segment, dy [rows_cap, K], w_hat [E, K, N] as stored."""
+    rows_cap = dy.shape[0]
+    _call("nvfp4_bf16_grouped_gemm_dgrad", _p(dy), _p(w_hat), _p(offsets), E, rows_cap, N, K, out_dtype, _p(y),
+          y.stride(0), _p(dev_status), _s(stream))
+
+
 def nvfp4_transpose_bf16(x, y, stream=None):
     """y[b] = x[b]^T for BF16 x [batch, rows, cols] (or [rows, cols])."""
     b, r, c = (1, *x.shape) if x.dim() == 2 else x.shape
@@ -247,6 +257,14 @@ def nvfp4_bf16_grouped_gemm_wgrad(a_t, b_t, offsets, E, dw, out_dtype=NVFP4_OUT_
     M, R = a_t.shape
     N = b_t.shape[0]
     _call("nvfp4_bf16_grouped_gemm_wgrad", _p(a_t), _p(b_t), _p(offsets), E, R, M, N, out_dtype, _p(dw),
+          _p(dev_status), _s(stream))
+
+
+def nvfp4_bf16_grouped_gemm_wgrad_rows(a, b, offsets, E, dw, out_dtype=NVFP4_OUT_F32, dev_status=None, stream=None):
+    """dw[e] = a[seg e, :]^T . b[seg e, :]; a [R, M], b [R, N] BF16 routed rows, dw [E, M, N]."""
+    R, M = a.shape
+    N = b.shape[1]
+    _call("nvfp4_bf16_grouped_gemm_wgrad_rows", _p(a), _p(b), _p(offsets), E, R, M, N, out_dtype, _p(dw),
           _p(dev_status), _s(stream))
 
 

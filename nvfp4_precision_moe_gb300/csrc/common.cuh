@@ -289,6 +289,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 // K-major operand tile in the 128-byte swizzle: 8-row groups 1024 bytes apart.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) { return smem_desc(saddr, 16, 1024, 2); }
+// MN-major BF16 operand tile in the 128-byte swizzle, as TMA leaves boxes of 64
+// MN-elements (128 bytes) x 64 K-rows: within a box the K-rows are 128 bytes
+// apart, so groups of 8 K-rows (one swizzle atom) are 1024 bytes apart (the
+// stride byte offset), and the boxes of consecutive 64-element MN ranges are
+// 8192 bytes apart (the leading byte offset).
+__device__ __forceinline__ uint64_t desc_sw128_mn(uint32_t saddr) { return smem_desc(saddr, 8192, 1024, 2); }
 // 32 rows x 16 bytes, no swizzle: the scale-factor source of tcgen05.cp.
 __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) { return smem_desc(saddr, 0, 128, 0); }
 

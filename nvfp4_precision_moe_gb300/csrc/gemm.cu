@@ -151,14 +151,54 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
                            : launch_single_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream);
 }
 
-extern "C" int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_t *offsets, int32_t E,
-                                             int64_t R, int64_t M, int64_t N, int32_t out_dtype, void *dw,
-                                             int32_t *dev_status, void *stream) {
-    if (!a_t || !b_t || !offsets || !dw || E < 1 || R < 0 || M < 0 || N < 0) return NVFP4_ERR_INVALID_ARG;
+extern "C" int nvfp4_bf16_grouped_gemm_dgrad(const void *dy, const void *w_hat, const int32_t *offsets, int32_t E,
+                                             int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, void *y,
+                                             int64_t ldy, int32_t *dev_status, void *stream) {
+    if (!dy || !w_hat || !offsets || !y || E < 1 || rows_cap < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+    if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (ldy < N) return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 || N % 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) || (int64_t)E * K > (1ll << 31))
+        return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(dy) || !aligned16(w_hat) || !aligned16(y) || ldy % 8) return NVFP4_ERR_ALIGNMENT;
+    if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    // A: dy rows, K-major; B: the experts' [K, N] blocks stacked, MN-major boxes of 64 columns x 64 K-rows
+    CUtensorMap tA, tB;
+    int s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)dy, K, rows_cap, 2 * K, 64, 128,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s == NVFP4_OK)
+        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)w_hat, N, (uint64_t)E * K, 2 * N, 64, 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != NVFP4_OK) return s;
+    GemmParams p{};
+    p.a_codes_base = (const uint8_t *)dy;
+    p.epilogue = NVFP4_EPI_NONE;
+    p.offsets = offsets;
+    p.rows_cap = (int32_t)rows_cap;
+    p.E = E;
+    p.N = N;
+    p.K = K;
+    p.b_mn = 1;
+    p.out_dtype = out_dtype;
+    p.y = y;
+    p.ldy = ldy;
+    p.vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) &&
+              (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
+    p.dev_status = dev_status;
+    return use_pair(false) ? launch_pair_gemm<false>(tA, tB, tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream)
+                           : launch_single_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream);
+}
+
+namespace {
+// The weight-gradient GEMM with its operands either transposed (K-major: a [M, R], b [N, R]) or
+// as the routed rows themselves (MN-major: a [R, M], b [R, N]).
+int wgrad_gemm(const void *a, const void *b, bool rows_major, const int32_t *offsets, int32_t E, int64_t R, int64_t M,
+               int64_t N, int32_t out_dtype, void *dw, int32_t *dev_status, void *stream) {
+    if (!a || !b || !offsets || !dw || E < 1 || R < 0 || M < 0 || N < 0) return NVFP4_ERR_INVALID_ARG;
     if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
     if (M % 128 || N % 256 || R % 128 || E > kMaxExperts || R > (1ll << 31) || (int64_t)E * M > (1ll << 31))
         return NVFP4_ERR_UNSUPPORTED;
-    if (!aligned16(a_t) || !aligned16(b_t) || !aligned16(dw)) return NVFP4_ERR_ALIGNMENT;
+    if (!aligned16(a) || !aligned16(b) || !aligned16(dw)) return NVFP4_ERR_ALIGNMENT;
     if (M == 0 || N == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
     if (R == 0) {  // no routed rows at all: every gradient is zero
@@ -171,11 +211,20 @@ extern "C" int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, c
         return NVFP4_OK;
     }
     CUtensorMap tA, tB, tY;
-    int s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a_t, R, M, 2 * R, 64, 128,
+    int s;
+    if (rows_major) {  // boxes of 64 columns x 64 rows
+        s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a, M, R, 2 * M, 64, 64,
                            CU_TENSOR_MAP_SWIZZLE_128B);
-    if (s == NVFP4_OK)
-        s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)b_t, R, N, 2 * R, 64, 128,
+        if (s == NVFP4_OK)
+            s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)b, N, R, 2 * N, 64, 64,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {  // boxes of 64 reduction elements x 128 rows
+        s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a, R, M, 2 * R, 64, 128,
                            CU_TENSOR_MAP_SWIZZLE_128B);
+        if (s == NVFP4_OK)
+            s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)b, R, N, 2 * R, 64, 128,
+                               CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     // FP32 gradients leave through TMA stores: boxes of 16 rows x 32 columns (128 bytes), 128-byte swizzle
     const bool tma_out = out_dtype == NVFP4_OUT_F32;
     if (s == NVFP4_OK && tma_out)
@@ -185,6 +234,8 @@ extern "C" int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, c
     GemmParams p{};
     p.wgrad = 1;
     p.wgrad_tma = tma_out ? 1 : 0;
+    p.a_mn = rows_major ? 1 : 0;
+    p.b_mn = rows_major ? 1 : 0;
     p.M = M;
     p.offsets = offsets;
     p.rows_cap = (int32_t)R;
@@ -199,4 +250,17 @@ extern "C" int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, c
     p.dev_status = dev_status;
     // the weight-gradient mode exists on the single-CTA pipeline only
     return launch_single_gemm<false>(tA, tB, tma_out ? tY : tA, tB, p, (int64_t)E * M, N, (cudaStream_t)stream);
+}
+}  // namespace
+
+extern "C" int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_t *offsets, int32_t E,
+                                             int64_t R, int64_t M, int64_t N, int32_t out_dtype, void *dw,
+                                             int32_t *dev_status, void *stream) {
+    return wgrad_gemm(a_t, b_t, false, offsets, E, R, M, N, out_dtype, dw, dev_status, stream);
+}
+
+extern "C" int nvfp4_bf16_grouped_gemm_wgrad_rows(const void *a, const void *b, const int32_t *offsets, int32_t E,
+                                                  int64_t R, int64_t M, int64_t N, int32_t out_dtype, void *dw,
+                                                  int32_t *dev_status, void *stream) {
+    return wgrad_gemm(a, b, true, offsets, E, R, M, N, out_dtype, dw, dev_status, stream);
 }

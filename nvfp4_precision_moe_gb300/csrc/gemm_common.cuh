@@ -20,6 +20,9 @@ constexpr uint32_t kTmemCols = 512;
 // 16 + 8c .. 16 + 8c + 7, column 16 + 8c + n/32 at lane n%32 of every quarter
 // for B row n.  (Scale addresses of the block-scaled MMA are 4-column aligned.)
 constexpr uint32_t kAcc = 0, kSFCol0 = 256, kSFSlotCols = 48, kSFBCol = 16;
+// Instruction-descriptor bits of kind::f16 MMAs: operand A / B is MN-major
+// (its M / N index contiguous in shared memory) rather than K-major.
+constexpr uint32_t kIdescTransA = 1u << 15, kIdescTransB = 1u << 16;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr int kMaxExperts = 1024;
 // Warp roles per CTA (512 threads, four warpgroups):
@@ -63,10 +66,14 @@ struct GemmParams {
     float *amax_out;
     int32_t *dev_status;
     // weight-gradient mode (BF16, single-CTA pipeline): y[e] (M x N) = A[:, seg e] . B[:, seg e]^T,
-    // A [M, rows_cap] and B [N, rows_cap] K-major, seg e = [offsets[e], offsets[e+1])
+    // A [M, rows_cap] and B [N, rows_cap] K-major (or [rows_cap, M] and [rows_cap, N] MN-major),
+    // seg e = [offsets[e], offsets[e+1])
     int32_t wgrad;
     int64_t M;
     int32_t wgrad_tma;  // FP32 weight gradients stored through shared memory by TMA (the map in tmR)
+    // BF16 operands stored MN-major (the M or N index contiguous): A (weight-gradient mode) and B
+    // (both modes) arrive as TMA boxes of 64 MN-elements x 64 K-rows, 8 KB apart (desc_sw128_mn)
+    int32_t a_mn, b_mn;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {

@@ -223,7 +223,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (it < nkt) {
                             const int32_t x = FP4 ? it * 128 : it * 64;
                             tma_load_2d_pair(sa, &tmA, x, t.m0, fb);
-                            tma_load_2d_pair(sb, &tmB, x, brow_mine, fb);
+                            if (!FP4 && p.b_mn) {
+                                // expert e's [K, N] block: this CTA's 128 columns as two boxes of
+                                // 64 columns x 64 K-rows
+                                const int32_t krow = (int32_t)(e * p.K + x);
+#pragma unroll
+                                for (int j = 0; j < 2; ++j)
+                                    tma_load_2d_pair(sb + 8192 * j, &tmB, nt * kBN + kBM * (int32_t)rank + 64 * j, krow,
+                                                     fb);
+                            } else {
+                                tma_load_2d_pair(sb, &tmB, x, brow_mine, fb);
+                            }
                             if (FP4) {
                                 // scales as rows of 256 bytes: the A tile's 2048-byte scale tile,
                                 // then the two of the 256 B rows
@@ -325,10 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tc_mma_nvf4_pair(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
                                                      kIdescNVF4, sf + 4 * c, sf + kSFBCol + 8 * c, (it | c) != 0);
                             } else {
+                                // B MN-major: chunk c is 16 K-rows (2048 bytes) into each box
 #pragma unroll
                                 for (int c = 0; c < 4; ++c)
-                                    tc_mma_bf16_pair(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c),
-                                                     kIdescBF16, (it | c) != 0);
+                                    tc_mma_bf16_pair(acc, desc_sw128(a_addr + 32 * c),
+                                                     p.b_mn ? desc_sw128_mn(b_addr + 2048 * c) : desc_sw128(b_addr + 32 * c),
+                                                     p.b_mn ? kIdescBF16 | kIdescTransB : kIdescBF16, (it | c) != 0);
                             }
                         } else {
                             // RAC: accumulate rg . W_sel^T into the same accumulator

@@ -170,9 +170,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             uint8_t *sb = sa + kATileBytes;
                             const int32_t x = w.k0 + it * 64;
                             mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
-                            tma_load_2d(sa, &tmA, x, w.mt * kBM, &full[stage]);
-                            tma_load_2d(sb, &tmB, x, w.nt * kBN, &full[stage]);
-                            tma_load_2d(sb + kBTileBytes / 2, &tmB, x, w.nt * kBN + 128, &full[stage]);
+                            if (p.a_mn) {  // [rows, M]: two boxes of 64 M-columns x 64 rows
+                                tma_load_2d(sa, &tmA, w.mt * kBM, x, &full[stage]);
+                                tma_load_2d(sa + 8192, &tmA, w.mt * kBM + 64, x, &full[stage]);
+                            } else {
+                                tma_load_2d(sa, &tmA, x, w.mt * kBM, &full[stage]);
+                            }
+                            if (p.b_mn) {  // [rows, N]: four boxes of 64 N-columns x 64 rows
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    tma_load_2d(sb + 8192 * j, &tmB, w.nt * kBN + 64 * j, x, &full[stage]);
+                            } else {
+                                tma_load_2d(sb, &tmB, x, w.nt * kBN, &full[stage]);
+                                tma_load_2d(sb + kBTileBytes / 2, &tmB, x, w.nt * kBN + 128, &full[stage]);
+                            }
                             issued[stage] = true;
                             issued_phase[stage] = phase;
                             if (++stage == kStages) {
@@ -217,8 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             } else {
                                 mbar_arrive_expect_tx(&full[stage], kATileBytes + kBTileBytes);
                                 tma_load_2d(sa, &tmA, it * 64, m0, &full[stage]);
-                                tma_load_2d(sb, &tmB, it * 64, brow_lo, &full[stage]);
-                                tma_load_2d(sb + kBTileBytes / 2, &tmB, it * 64, brow_hi, &full[stage]);
+                                if (p.b_mn) {  // expert e's [K, N] block: four boxes of 64 columns x 64 K-rows
+                                    const int32_t krow = (int32_t)(e * p.K + it * 64);
+#pragma unroll
+                                    for (int j = 0; j < 4; ++j)
+                                        tma_load_2d(sb + 8192 * j, &tmB, nt * kBN + 64 * j, krow, &full[stage]);
+                                } else {
+                                    tma_load_2d(sb, &tmB, it * 64, brow_lo, &full[stage]);
+                                    tma_load_2d(sb + kBTileBytes / 2, &tmB, it * 64, brow_hi, &full[stage]);
+                                }
                             }
                         } else {  // RAC slice: residual rows and the selected weight columns
                             const int r = it - nkt;
@@ -254,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool ok = true;
                 int local = 0;
                 const uint32_t acc = tmem + kAcc;
+                const uint32_t idesc_bf16 = kIdescBF16 | (p.a_mn ? kIdescTransA : 0u) | (p.b_mn ? kIdescTransB : 0u);
                 for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
                     // the epilogue has read the previous tile out of the accumulator
                     if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, kWaitLimitNs, abort_flag)) {
@@ -285,10 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tc_mma_nvf4(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescNVF4,
                                                 sf + 4 * c, sf + kSFBCol + 8 * c, (it | c) != 0);
                             } else {
+                                // K-major: chunk c starts 32 bytes into each row; MN-major: 16 K-rows
+                                // (2048 bytes) into each box
 #pragma unroll
                                 for (int c = 0; c < 4; ++c)
-                                    tc_mma_bf16(acc, desc_sw128(a_addr + 32 * c), desc_sw128(b_addr + 32 * c), kIdescBF16,
-                                                (it | c) != 0);
+                                    tc_mma_bf16(acc, p.a_mn ? desc_sw128_mn(a_addr + 2048 * c) : desc_sw128(a_addr + 32 * c),
+                                                p.b_mn ? desc_sw128_mn(b_addr + 2048 * c) : desc_sw128(b_addr + 32 * c),
+                                                idesc_bf16, (it | c) != 0);
                             }
                         } else {
                             // RAC: accumulate rg . W_sel^T into the same accumulator

@@ -85,6 +85,31 @@ __device__ __forceinline__ uint32_t e2m1x8(const float *q) {
     return w;
 }
 
+// Four code pairs (a word of packed E2M1 codes, element 2i in the low nibble)
+// -> their exact values as four f16x2 (element 2i in the low half).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t &h0, uint32_t &h1, uint32_t &h2, uint32_t &h3) {
+    asm("{ .reg .b8 b0, b1, b2, b3;\n"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+        "cvt.rn.f16x2.e2m1x2 %3, b3; }"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+}
+
+// f16x2 -> its two values in binary32 (exact), low half first.
+__device__ __forceinline__ void f16x2_to_f32(uint32_t h, float &lo, float &hi) {
+    asm("{ .reg .f16 l, u; mov.b32 {l, u}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, u; }" : "=f"(lo), "=f"(hi) : "r"(h));
+}
+
+// Two binary32 values -> BF16 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
 // (a0, a1) * (b0, b1) as two IEEE binary32 products (round to nearest) in one
 // packed instruction.
 __device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1, float &r0, float &r1) {
@@ -158,11 +183,41 @@ __device__ __forceinline__ void unpack_block(const uint4 &a, const uint4 &b, flo
     }
 }
 
+// The block's dequantized values (code * sb) * gs, both products in binary32,
+// the code's exact value from the hardware conversion.
+__device__ __forceinline__ void dequant_block_f32(const BlockQ &q, float gs, float (&d)[16]) {
+    uint32_t h[8];
+    e2m1x8_to_f16x2(q.w0, h[0], h[1], h[2], h[3]);
+    e2m1x8_to_f16x2(q.w1, h[4], h[5], h[6], h[7]);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        float c0, c1;
+        f16x2_to_f32(h[u], c0, c1);
+        fmul2_rn(c0, c1, q.sbf, q.sbf, c0, c1);
+        fmul2_rn(c0, c1, gs, gs, d[2 * u], d[2 * u + 1]);
+    }
+}
+
+// The block's QDQ as BF16, two elements per word (element 2i in the low half).
+__device__ __forceinline__ void dequant_block_bf16(const BlockQ &q, float gs, uint32_t (&o)[8]) {
+    float d[16];
+    dequant_block_f32(q, gs, d);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) o[u] = bf16x2_rn(d[2 * u], d[2 * u + 1]);
+}
+
 constexpr int kQThreads = 256;
 constexpr int kQWarps = kQThreads / 32;
 constexpr int kMaxStagedK = 1024;  // residual row staged in shared memory up to this k
 constexpr int kQSlots = 4;         // 1 KB segments in flight per warp
-constexpr int kQBlocksPerSM = 3;   // 24 warps, 96 KB of segments in flight per SM
+// Resident blocks per SM: 3 (24 warps, 96 KB of segments in flight per SM);
+// 4 blocks of activations measured no faster.
+template <int MODE>
+constexpr int q_blocks_per_sm() {
+    return 3;
+}
+// per warp: the staged RAC row (k <= kMaxStagedK) or, beyond it, the row's block scales
+constexpr int kQRowBuf = 2 * kMaxStagedK > kMaxBlocksPerRow ? 2 * kMaxStagedK : kMaxBlocksPerRow;
 constexpr size_t kQRingBytes = (size_t)kQWarps * kQSlots * 1024;
 constexpr uint64_t kQWaitNs = 2000000000ull;  // 2 s per wait for a segment
 
@@ -209,11 +264,10 @@ __device__ __forceinline__ uint16_t rac_from_code(uint16_t xb, uint32_t c, float
 // they are staged in shared memory and written once per destination row as
 // 16-byte chunks.
 template <int MODE>
-__global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(QuantArgs a) {
+__global__ void __launch_bounds__(kQThreads, q_blocks_per_sm<MODE>()) quantize_kernel(QuantArgs a) {
     extern __shared__ __align__(128) uint8_t q_ring[];  // [kQWarps][kQSlots][1024]
     __shared__ uint64_t s_qbar[kQWarps][kQSlots];
-    __shared__ __align__(16) uint16_t s_res[kQWarps][kMaxStagedK];
-    __shared__ uint8_t s_sb[kQWarps][kMaxBlocksPerRow];
+    __shared__ __align__(16) uint8_t s_row[kQWarps][kQRowBuf];
     __shared__ int64_t s_cbase[kQWarps][32];  // destination f: byte offset of its code row (-1: skipped)
     __shared__ int64_t s_sbase[kQWarps][32];  // destination f: row part of its scale offsets
     __shared__ int32_t s_S[kMaxStagedK];
@@ -255,8 +309,8 @@ __global__ void __launch_bounds__(kQThreads, kQBlocksPerSM) quantize_kernel(Quan
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     const int64_t nwarps_total = (int64_t)gridDim.x * kQWarps;
     const uint16_t *xt = a.x + (int64_t)tensor * a.x_tstride;
-    uint16_t *stage = s_res[wid];
-    uint8_t *row_sb = s_sb[wid];
+    uint16_t *stage = reinterpret_cast<uint16_t *>(s_row[wid]);  // staged: the RAC row
+    uint8_t *row_sb = s_row[wid];                                 // not staged: the block scales
     const int fanout = (MODE == kModeAct) ? a.fanout : 1;
     uint8_t *codes = a.codes + (int64_t)tensor * a.codes_tstride;
     uint8_t *scales = a.scales + (int64_t)tensor * a.scales_tstride;
@@ -720,13 +774,7 @@ __global__ void __launch_bounds__(256) resid_qdq_kernel(uint16_t *resid, int64_t
         BlockQ q;
         quant_block(v, gs, p6, inv_gs, tb, q);
         uint32_t o[8];
-#pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-            const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
-            const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
-            o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
-                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
-        }
+        dequant_block_bf16(q, gs, o);
         p[2 * b] = make_uint4(o[0], o[1], o[2], o[3]);
         p[2 * b + 1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
@@ -789,9 +837,11 @@ __global__ void __launch_bounds__(256) online_score_kernel(const uint16_t *x, in
                 unpack_block(raw[u][0], raw[u][1], v);
                 BlockQ q;
                 quant_block(v, gs, p6, inv_gs, tb, q);
+                float dq[16];
+                dequant_block_f32(q, gs, dq);
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
-                    const float d = __fsub_rn(__fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs), v[t]);
+                    const float d = __fsub_rn(dq[t], v[t]);
                     const float y = __fsub_rn(__fmul_rn(d, d), comp[t]);
                     const float s2 = __fadd_rn(sum[t], y);
                     comp[t] = __fsub_rn(__fsub_rn(s2, sum[t]), y);
@@ -828,54 +878,61 @@ __global__ void online_score_finish_kernel(const double *part, int64_t K, int nc
 
 // W_sel[e, n, s] = bf16(code * sb) of packed weight element (n, S[s]) of
 // expert e -- the unscaled dequantized value nvfp4_prepare_weights stores for
-// the channels S -- gathered for a new S.  One warp per weight row: the row's
-// packed codes and its block scales are read once, coalesced, into shared
-// memory; the lanes then emit the row's k outputs two at a time.
+// the channels S -- gathered for a new S.  A block covers 32 rows of one
+// expert (blockIdx.y), a warp 4 of them; lane l emits channels 4l + 128u ..
+// 4l + 128u + 3 of each row.  The code and scale bytes are loaded straight
+// from global memory, so only the sectors that hold selected channels are
+// read, and the 4 rows' loads are all issued before the first is used.
 constexpr int kGatherWarps = 8;
-
-__host__ __device__ constexpr int64_t gather_row_bytes(int64_t K) { return K / 2 + (((K / 16) + 15) / 16) * 16; }
-__host__ __device__ constexpr int64_t gather_s_bytes(int32_t k) { return (((int64_t)k * 4) + 15) / 16 * 16; }
+constexpr int kGatherRows = 4;  // rows per warp
 
 __global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_kernel(const uint8_t *codes, const uint8_t *scales,
-                                                                      int64_t E, int64_t N, int64_t K,
-                                                                      const int32_t *S, int32_t k, uint16_t *wsel) {
-    extern __shared__ __align__(16) uint8_t gsm[];
-    int32_t *sS = reinterpret_cast<int32_t *>(gsm);
+                                                                      int64_t N, int64_t K, const int32_t *S,
+                                                                      int32_t k, uint16_t *wsel) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    uint8_t *rowc = gsm + gather_s_bytes(k) + w * gather_row_bytes(K);  // codes, then scales
-    uint8_t *rows_ = rowc + K / 2;
-    for (int i = threadIdx.x; i < k; i += blockDim.x) sS[i] = min(max(S[i], 0), (int32_t)(K - 1));  // S within [0, K)
-    __syncthreads();
+    const int64_t e = blockIdx.y;
+    const int64_t n0 = ((int64_t)blockIdx.x * kGatherWarps + w) * kGatherRows;  // N % 128 == 0: all rows exist
     const int64_t nb = K >> 4, kslices = (nb + 15) >> 4;
-    for (int64_t row = (int64_t)blockIdx.x * kGatherWarps + w; row < E * N; row += (int64_t)gridDim.x * kGatherWarps) {
-        const int64_t e = row / N, n = row - e * N;
-        const uint4 *src = reinterpret_cast<const uint4 *>(codes + row * (K >> 1));
-        for (int64_t i = lane; i < (K >> 5); i += 32) reinterpret_cast<uint4 *>(rowc)[i] = __ldg(src + i);
-        // the row's block scales: one 32-bit word per 4 blocks
-        const uint8_t *sten = scales + e * ((N + 127) >> 7) * kslices * 2048;  // an expert's scales
-        const int64_t srow = scale_row_offset(n, kslices);
-        for (int64_t g = lane; g < (nb >> 2); g += 32)
-            reinterpret_cast<uint32_t *>(rows_)[g] = __ldg(reinterpret_cast<const uint32_t *>(sten + srow + scale_block_offset(4 * g)));
-        __syncwarp();
-        uint32_t *dst = reinterpret_cast<uint32_t *>(wsel + row * k);
-        for (int s2 = 2 * lane; s2 < k; s2 += 64) {
-            uint32_t h[2];
+    const uint8_t *sten = scales + e * (N >> 7) * kslices * 2048;  // the expert's scales
+    const uint8_t *cten = codes + e * N * (K >> 1);
+    for (int s0 = 4 * lane; s0 < k; s0 += 128) {  // k % 8 == 0: channels s0 .. s0 + 3 all exist
+        int32_t co[4];
+        uint32_t sh[4];
+        int64_t so[4];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int j = sS[s2 + u];
-                const uint32_t c = (rowc[j >> 1] >> (4 * (j & 1))) & 15u;
-                h[u] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(e2m1_val(c), e4m3_to_f32(rows_[j >> 4]))));
-            }
-            dst[s2 >> 1] = h[0] | (h[1] << 16);
+        for (int t = 0; t < 4; ++t) {
+            const int32_t j = min(max(__ldg(S + s0 + t), 0), (int32_t)(K - 1));
+            co[t] = j >> 1;
+            sh[t] = 4u * (uint32_t)(j & 1);
+            so[t] = scale_block_offset(j >> 4) + ((j >> 4) & 3);
         }
-        __syncwarp();
+        uint32_t cv[kGatherRows][4], sv[kGatherRows][4];
+#pragma unroll
+        for (int r = 0; r < kGatherRows; ++r) {
+            const uint8_t *crow = cten + (n0 + r) * (K >> 1);
+            const uint8_t *srow = sten + scale_row_offset(n0 + r, kslices);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                cv[r][t] = __ldg(crow + co[t]);
+                sv[r][t] = __ldg(srow + so[t]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kGatherRows; ++r) {
+            uint32_t h[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                h[t] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(__fmul_rn(e2m1_val((cv[r][t] >> sh[t]) & 15u), e4m3_to_f32(sv[r][t]))));
+            *reinterpret_cast<uint2 *>(wsel + (e * N + n0 + r) * k + s0) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        }
     }
 }
 
 // QDQ_W (QUADS §3.2 Eq. 12) that also writes the transpose, for the learner's
 // backward (dX = W_hat^T dY needs W_hat^T with the reduction axis contiguous):
 // a block owns a 64 x 64 tile of one tensor; each thread quantizes one
-// 16-element block exactly as quantize_kernel<fake> does (quant_block, the
+// 16-element block exactly as fake_quant_fused_kernel does (quant_block, the
 // tensor's gs), writes it to w_hat, and leaves it in shared memory; the tile
 // then leaves transposed, 16 bytes per thread.
 __global__ void __launch_bounds__(256) fake_quant_t_kernel(const uint16_t *w, int64_t rows, int64_t cols,
@@ -905,13 +962,7 @@ __global__ void __launch_bounds__(256) fake_quant_t_kernel(const uint16_t *w, in
         BlockQ q;
         quant_block(v, gs, p6, inv_gs, tb, q);
         uint32_t o[8];
-#pragma unroll
-        for (int t = 0; t < 16; t += 2) {
-            const float d0 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t)), q.sbf), gs);
-            const float d1 = __fmul_rn(__fmul_rn(e2m1_val(q.code(t + 1)), q.sbf), gs);
-            o[t / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
-                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
-        }
+        dequant_block_bf16(q, gs, o);
         uint4 *dst = reinterpret_cast<uint4 *>(w_hat + gi);
         dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
         dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -939,9 +990,10 @@ __global__ void __launch_bounds__(256) fake_quant_t_kernel(const uint16_t *w, in
 }
 
 // Blocks for `rows` rows (one warp per row): as many as are resident at once.
+template <int MODE>
 static int quant_grid(int64_t rows) {
     int64_t blocks = (rows + kQWarps - 1) / kQWarps;
-    int64_t cap = (int64_t)sm_count() * kQBlocksPerSM;
+    int64_t cap = (int64_t)sm_count() * q_blocks_per_sm<MODE>();
     if (blocks > cap) blocks = cap;
     return (int)(blocks < 1 ? 1 : blocks);
 }
@@ -965,7 +1017,7 @@ static int launch_quantize(dim3 grid, const QuantArgs &a, cudaStream_t st, const
 
 // QDQ_W of many weight tensors (QUADS §3.2 Eq. 12) in one persistent launch
 // that reads every tensor from HBM once: its amax and its quantize-dequantize
-// are two kinds of work items of kFQRows rows, taken from one counter in the
+// are two kinds of work items of `rpi` rows, taken from one counter in the
 // order A(0), A(1), B(0), A(2), B(1), ..., B(nt-1) -- A(t) the amax of tensor
 // t, B(t) its QDQ -- so that B(t) re-reads rows that A(t) read shortly before
 // and that still sit in L2.  A B(t) item starts once every A(t) item has
@@ -973,10 +1025,14 @@ static int launch_quantize(dim3 grid, const QuantArgs &a, cudaStream_t st, const
 // bound); no A item ever waits, and every A(t) item is taken before any B(t)
 // item, so the wait always ends.  Scratch (32-bit words, zeroed by the
 // caller's stream before the launch): amax[nt], done[nt], the work counter.
-// Items are kept small (8 rows, one per warp) so that the items in flight at
-// once -- one per resident block -- span only about two tensors, whose rows
-// then fit in L2 between their two reads.
-constexpr int kFQRows = 8;
+// Items are kept near 64 KB (rpi a multiple of 8 rows, at least 8) so that
+// the items in flight at once -- one per resident block -- span only about
+// two tensors, whose rows then fit in L2 between their two reads.
+constexpr int kFQItemBytes = 65536;
+__host__ __device__ constexpr int64_t fq_rows_per_item(int64_t cols) {
+    const int64_t r = (kFQItemBytes / 2 / (cols > 0 ? cols : 1) + 4) / 8 * 8;
+    return r < 8 ? 8 : r;
+}
 constexpr uint64_t kFQWaitNs = 2000000000ull;
 
 // 16-byte global load / store with an L2 eviction-priority policy (createpolicy):
@@ -1010,12 +1066,13 @@ struct FQArgs {
     uint16_t *w_hat;
     int64_t rows, cols;
     int32_t nt, per;  // tensors, items per tensor and kind
+    int32_t rpi;      // rows per item (a multiple of 8)
     uint32_t *ws;     // amax bits [nt], done [nt], counter
     float *gs_out;
     int32_t *dev_status;
 };
 
-__global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
+__global__ void __launch_bounds__(256, 4) fake_quant_fused_kernel(FQArgs a) {
     __shared__ QTables tb;
     __shared__ int64_t s_item;
     __shared__ uint32_t s_red[8];
@@ -1037,8 +1094,8 @@ __global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
         const int chunk = (int)(item - gi * a.per);
         const bool is_a = gi == 0 || (gi != 2ll * a.nt - 1 && (gi & 1));
         const int t = gi == 0 ? 0 : (gi == 2ll * a.nt - 1 ? a.nt - 1 : (int)((gi & 1) ? (gi + 1) / 2 : gi / 2 - 1));
-        const int64_t r0 = (int64_t)chunk * kFQRows;
-        const int64_t r1 = min(a.rows, r0 + kFQRows);
+        const int64_t r0 = (int64_t)chunk * a.rpi;
+        const int64_t r1 = min(a.rows, r0 + (int64_t)a.rpi);
         const uint16_t *wt = a.w + (int64_t)t * a.rows * a.cols;
         if (is_a) {
             // max |w| of the rows: bit patterns of |bf16| order like the values (NaN above Inf)
@@ -1100,38 +1157,46 @@ __global__ void __launch_bounds__(256) fake_quant_fused_kernel(FQArgs a) {
             if (!isfinite(amax_t)) report(a.dev_status, NVFP4_ERR_NONFINITE);
         }
         uint16_t *ot = a.w_hat + (int64_t)t * a.rows * a.cols;
-        for (int64_t m = r0 + wid; m < r1; m += 8) {
-            const uint16_t *xr = wt + m * a.cols;
-            uint4 ra = make_uint4(0, 0, 0, 0), rb = ra;
-            if (lane < nb) {
-                ra = ld_hint(reinterpret_cast<const uint4 *>(xr + lane * 16), drop);
-                rb = ld_hint(reinterpret_cast<const uint4 *>(xr + lane * 16) + 1, drop);
+        // this warp's rows r0 + wid + 8 i (i < nrw), their segments in order; the
+        // loads run two segments ahead, across row ends
+        const int nrw = r1 - r0 > wid ? (int)((r1 - r0 - wid + 7) >> 3) : 0;
+        auto load = [&](int i, int sg, uint4 &x0, uint4 &x1) {
+            const int b = sg * 32 + lane;
+            if (i < nrw && b < nb) {
+                const uint4 *p = reinterpret_cast<const uint4 *>(wt + (r0 + wid + 8 * i) * a.cols + b * 16);
+                x0 = ld_hint(p, drop);
+                x1 = ld_hint(p + 1, drop);
             }
-            for (int seg = 0; seg < segs; ++seg) {
-                const int b = seg * 32 + lane;
-                const uint4 ca = ra, cb = rb;
-                if (b + 32 < nb) {  // the next segment's loads in flight
-                    ra = ld_hint(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16), drop);
-                    rb = ld_hint(reinterpret_cast<const uint4 *>(xr + (b + 32) * 16) + 1, drop);
-                }
-                if (b < nb) {
-                    float v[16];
-                    BlockQ q;
-                    unpack_block(ca, cb, v);
-                    quant_block(v, gs, p6, inv_gs, tb, q);
-                    uint32_t o[8];
-#pragma unroll
-                    for (int u = 0; u < 16; u += 2) {
-                        float c0, c1, d0, d1;
-                        fmul2_rn(e2m1_val(q.code(u)), e2m1_val(q.code(u + 1)), q.sbf, q.sbf, c0, c1);
-                        fmul2_rn(c0, c1, gs, gs, d0, d1);
-                        o[u / 2] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d0)) |
-                                   ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(d1)) << 16);
-                    }
-                    uint4 *dst = reinterpret_cast<uint4 *>(ot + m * a.cols + b * 16);
-                    st_hint(dst, make_uint4(o[0], o[1], o[2], o[3]), drop);
-                    st_hint(dst + 1, make_uint4(o[4], o[5], o[6], o[7]), drop);
-                }
+        };
+        int li = 0, lsg = 0;  // the next segment to load
+        auto step = [&](int &i, int &sg) {
+            if (++sg == segs) {
+                sg = 0;
+                ++i;
+            }
+        };
+        uint4 n0a = make_uint4(0, 0, 0, 0), n0b = n0a, n1a = n0a, n1b = n0a;
+        load(li, lsg, n0a, n0b);
+        step(li, lsg);
+        load(li, lsg, n1a, n1b);
+        step(li, lsg);
+        for (int ci = 0, csg = 0; ci < nrw; step(ci, csg)) {
+            const uint4 ca = n0a, cb = n0b;
+            n0a = n1a;
+            n0b = n1b;
+            load(li, lsg, n1a, n1b);
+            step(li, lsg);
+            const int b = csg * 32 + lane;
+            if (b < nb) {
+                float v[16];
+                BlockQ q;
+                unpack_block(ca, cb, v);
+                quant_block(v, gs, p6, inv_gs, tb, q);
+                uint32_t o[8];
+                dequant_block_bf16(q, gs, o);
+                uint4 *dst = reinterpret_cast<uint4 *>(ot + (r0 + wid + 8 * ci) * a.cols + b * 16);
+                st_hint(dst, make_uint4(o[0], o[1], o[2], o[3]), drop);
+                st_hint(dst + 1, make_uint4(o[4], o[5], o[6], o[7]), drop);
             }
         }
     }
@@ -1197,14 +1262,15 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
     a.scales = scales;
     a.resid = (uint16_t *)resid;
     a.dev_status = dev_status;
-    return launch_quantize<kModeAct>(dim3(quant_grid(M)), a, (cudaStream_t)stream, "quantize_kernel");
+    return launch_quantize<kModeAct>(dim3(quant_grid<kModeAct>(M)), a, (cudaStream_t)stream, "quantize_kernel");
 }
 
 extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t cols, void *w_hat, float *gs_out,
                                 float *amax_ws, int32_t *dev_status, void *stream) {
     if (!w || !w_hat || !amax_ws || nt < 1 || rows < 0 || cols < 0) return NVFP4_ERR_INVALID_ARG;
     // items are counted in 32 bits
-    if (cols % 32 || cols / 16 > kMaxBlocksPerRow || nt > 65535 || 2 * (int64_t)nt * ((rows + kFQRows - 1) / kFQRows) > (1ll << 31))
+    const int64_t rpi = fq_rows_per_item(cols);
+    if (cols % 32 || cols / 16 > kMaxBlocksPerRow || nt > 65535 || 2 * (int64_t)nt * ((rows + rpi - 1) / rpi) > (1ll << 31))
         return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(w) || !aligned16(w_hat)) return NVFP4_ERR_ALIGNMENT;
     NVFP4_CHECK_INIT();
@@ -1222,7 +1288,8 @@ extern "C" int nvfp4_fake_quant(const void *w, int32_t nt, int64_t rows, int64_t
     a.rows = rows;
     a.cols = cols;
     a.nt = nt;
-    a.per = (int32_t)((rows + kFQRows - 1) / kFQRows);
+    a.per = (int32_t)((rows + rpi - 1) / rpi);
+    a.rpi = (int32_t)rpi;
     a.ws = reinterpret_cast<uint32_t *>(amax_ws);
     a.gs_out = gs_out;
     a.dev_status = dev_status;
@@ -1281,7 +1348,7 @@ extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_
     a.wsel_tstride = N * (int64_t)k;
     a.interleave = interleave;
     a.dev_status = dev_status;
-    int g = quant_grid(N) / (E > 8 ? 8 : E);
+    int g = quant_grid<kModeWeight>(N) / (E > 8 ? 8 : E);
     return launch_quantize<kModeWeight>(dim3(g < 1 ? 1 : g, E), a, st, "quantize_kernel<weight>");
 }
 
@@ -1340,24 +1407,12 @@ extern "C" int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8
                                              int64_t K, const int32_t *S, int32_t k, void *w_sel, void *stream) {
     if (!w_codes || !w_scales || !S || !w_sel || E < 1 || N < 0 || K < 0 || k < 1 || k > K)
         return NVFP4_ERR_INVALID_ARG;
-    if (K % 64 || N % 128 || k % 8 || K / 16 > kMaxBlocksPerRow) return NVFP4_ERR_UNSUPPORTED;
+    if (K % 64 || N % 128 || k % 8 || E > 65535 || N / 32 > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(w_sel) || !aligned16(w_codes) || !aligned16(w_scales)) return NVFP4_ERR_ALIGNMENT;
     if (N == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
-    const int64_t smem = gather_s_bytes(k) + kGatherWarps * gather_row_bytes(K);
-    if (smem > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(gather_wsel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)smem);
-        if (e != cudaSuccess) {
-            set_last_error("cudaFuncSetAttribute(gather_wsel_kernel)", e);
-            return NVFP4_ERR_CUDA;
-        }
-    }
-    int64_t blocks = ((int64_t)E * N + kGatherWarps - 1) / kGatherWarps;
-    const int64_t cap = (int64_t)sm_count() * 8;
-    if (blocks > cap) blocks = cap;
-    gather_wsel_kernel<<<(unsigned)blocks, 32 * kGatherWarps, (size_t)smem, (cudaStream_t)stream>>>(
-        w_codes, w_scales, E, N, K, S, k, (uint16_t *)w_sel);
+    gather_wsel_kernel<<<dim3((unsigned)(N / (kGatherWarps * kGatherRows)), (unsigned)E), 32 * kGatherWarps, 0,
+                         (cudaStream_t)stream>>>(w_codes, w_scales, N, K, S, k, (uint16_t *)w_sel);
     return launch_status("gather_wsel_kernel");
 }
 

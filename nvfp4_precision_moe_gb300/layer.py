@@ -18,10 +18,10 @@ import torch
 from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
-               nvfp4_bf16_grouped_gemm_wgrad, nvfp4_fake_quant_transposed, nvfp4_gather_selected_weights,
+               nvfp4_bf16_grouped_gemm_dgrad, nvfp4_bf16_grouped_gemm_wgrad_rows, nvfp4_gather_selected_weights,
                nvfp4_moe_combine_backward,
                nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online, nvfp4_route_topk, nvfp4_swiglu,
-               nvfp4_swiglu_backward, nvfp4_transpose_bf16, nvfp4_w4a4_rac_grouped_gemm)
+               nvfp4_swiglu_backward, nvfp4_w4a4_rac_grouped_gemm)
 
 
 def scale_bytes(rows, K):
@@ -232,10 +232,6 @@ class QatMoE:
             self.dh = torch.zeros((R, I), **bf)
             self.dgu = torch.zeros((R, 2 * I), **bf)
             self.dxr = torch.zeros((R, H), **bf)
-            self.t_big = torch.zeros(max(H, 2 * I) * R, **bf)   # a transposed routed tensor
-            self.t_small = torch.zeros(max(H, 2 * I) * R, **bf)  # the other operand of a weight gradient
-            self.w13_t = torch.empty((E, H, 2 * I), **bf)
-            self.wd_t = torch.empty((E, I, H), **bf)
             self.ones = torch.ones((max_tokens, topk), dtype=torch.float32, device=dev)
             self.dw13 = torch.empty((E, 2 * I, H), dtype=torch.float32, device=dev)
             self.dwd = torch.empty((E, H, I), dtype=torch.float32, device=dev)
@@ -250,12 +246,6 @@ class QatMoE:
 
     def fake_quant(self, stream=None):
         if not self.fake:
-            return
-        if self.train:  # the transposes the backward needs come from the same read of W
-            nvfp4_fake_quant_transposed(self.w13, self.w13_hat, self.w13_t, self.amax_ws, gs_out=self.gs13,
-                                        dev_status=self.dev_status, stream=stream)
-            nvfp4_fake_quant_transposed(self.wd, self.wd_hat, self.wd_t, self.amax_ws, gs_out=self.gsd,
-                                        dev_status=self.dev_status, stream=stream)
             return
         nvfp4_fake_quant(self.w13, self.w13_hat, self.amax_ws, gs_out=self.gs13,
                          dev_status=self.dev_status, stream=stream)
@@ -328,28 +318,19 @@ class QatMoE:
         # routed output gradient, and the combine weights' gradient
         nvfp4_moe_combine_backward(dout, self.y, dst, w, r.counts, r.offsets, E, self.dy,
                                    dweights=self.dweights[:T], stream=stream)
-        # down projection: dh = dY W_hat_d (the transposed weights: written by fake_quant for a
-        # fake-quantized trainer, transposed here for the BF16 one), dW_d = dY^T h
-        if not self.fake:
-            nvfp4_transpose_bf16(self.wd_hat, self.wd_t, stream=stream)
-        nvfp4_bf16_grouped_gemm(self.dy, self.wd_t, r.offsets, E, I, H, self.dh, out_dtype=NVFP4_OUT_BF16,
-                                dev_status=self.dev_status, stream=stream)
-        dy_t, h_t = self.t_big[:H * R].view(H, R), self.t_small[:I * R].view(I, R)
-        nvfp4_transpose_bf16(self.dy, dy_t, stream=stream)
-        nvfp4_transpose_bf16(self.h, h_t, stream=stream)
-        nvfp4_bf16_grouped_gemm_wgrad(dy_t, h_t, r.offsets, E, self.dwd, dev_status=self.dev_status, stream=stream)
+        # down projection: dh = dY W_hat_d (W_hat_d read as stored, [H, I] per expert), dW_d = dY^T h
+        # (the routed rows read as stored)
+        nvfp4_bf16_grouped_gemm_dgrad(self.dy, self.wd_hat, r.offsets, E, I, H, self.dh, out_dtype=NVFP4_OUT_BF16,
+                                      dev_status=self.dev_status, stream=stream)
+        nvfp4_bf16_grouped_gemm_wgrad_rows(self.dy, self.h, r.offsets, E, self.dwd, dev_status=self.dev_status,
+                                           stream=stream)
         # SwiGLU
         nvfp4_swiglu_backward(self.gu, self.dh, self.dgu, stream=stream)
         # gate_up projection: dx_routed = d(gate|up) W_hat_13, dW_13 = d(gate|up)^T x_routed
-        if not self.fake:
-            nvfp4_transpose_bf16(self.w13_hat, self.w13_t, stream=stream)
-        nvfp4_bf16_grouped_gemm(self.dgu, self.w13_t, r.offsets, E, H, 2 * I, self.dxr, out_dtype=NVFP4_OUT_BF16,
-                                dev_status=self.dev_status, stream=stream)
-        dgu_t, xr_t = self.t_big[:2 * I * R].view(2 * I, R), self.t_small[:H * R].view(H, R)
-        nvfp4_transpose_bf16(self.dgu, dgu_t, stream=stream)
-        nvfp4_transpose_bf16(self.xr, xr_t, stream=stream)
-        nvfp4_bf16_grouped_gemm_wgrad(dgu_t, xr_t, r.offsets, E, self.dw13, dev_status=self.dev_status,
-                                      stream=stream)
+        nvfp4_bf16_grouped_gemm_dgrad(self.dgu, self.w13_hat, r.offsets, E, H, 2 * I, self.dxr,
+                                      out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
+        nvfp4_bf16_grouped_gemm_wgrad_rows(self.dgu, self.xr, r.offsets, E, self.dw13, dev_status=self.dev_status,
+                                           stream=stream)
         # dx: each token's routed-row gradients summed
         dx = self.dx[:T]
         nvfp4_moe_combine(self.dxr, dst, self.ones[:T], self.topk, dx, stream=stream)

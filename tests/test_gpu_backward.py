@@ -2,9 +2,10 @@
 estimator) against the oracle's binary64 derivatives: the transposes
 bit-exact, the SwiGLU forward/backward within one BF16 rounding, the combine
 backward's routed gradient bit-exact, the grouped weight gradient (an empty
-expert included) within FP32 accumulation error, and QatMoE(train=True).backward
-stage by stage -- each stage against the oracle applied to the GPU's previous
-stage."""
+expert included) within FP32 accumulation error from transposed operands and
+from the routed rows as stored, the grouped input gradient from the weights as
+stored on both GEMM pipelines, and QatMoE(train=True).backward stage by stage
+-- each stage against the oracle applied to the GPU's previous stage."""
 import numpy as np
 import pytest
 import torch
@@ -13,6 +14,7 @@ import oracle
 from tests import _gpu as G
 
 pytestmark = pytest.mark.gpu
+TOL = 1e-3
 TOL_BF16 = 2.0 ** -8 + 1e-3
 
 
@@ -131,6 +133,68 @@ def test_grouped_weight_gradient(nv, out_dtype):
     assert not got[3].any()
     tol = 1e-5 if out_dtype == 0 else TOL_BF16
     assert G.rel_err(got, ref) <= tol
+
+
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_grouped_weight_gradient_from_rows(nv, out_dtype):
+    """The same weight gradient with both operands read as the routed rows
+    themselves (MN-major tiles: no transposes)."""
+    T, E, topk, M, N = 200, 5, 2, 384, 512
+    _, _, counts, offs, dst = _routing(nv, T, E, topk, 21, empty=1)
+    assert counts[1] == 0
+    R = int(offs[-1]) + 128
+    g = torch.Generator().manual_seed(22)
+    a = torch.randn((R, M), generator=g).to(torch.bfloat16)
+    b = torch.randn((R, N), generator=g).to(torch.bfloat16)
+    a[int(offs[-1]):] = 1e4  # rows past offsets[E] must not be read
+    dw = torch.full((E, M, N), 5.0, dtype=torch.float32 if out_dtype == 0 else torch.bfloat16, device=G.DEV)
+    st = G.zeros(1, torch.int32)
+    nv.nvfp4_bf16_grouped_gemm_wgrad_rows(a.to(G.DEV), b.to(G.DEV), torch.as_tensor(offs, dtype=torch.int32).to(G.DEV),
+                                          E, dw, out_dtype=out_dtype, dev_status=st)
+    torch.cuda.synchronize()
+    G.status_ok(st)
+    ref = oracle.segment_wgrad(f64(a)[:int(offs[-1])], f64(b)[:int(offs[-1])], offs)
+    got = f64(dw)
+    assert not got[1].any()
+    tol = 1e-5 if out_dtype == 0 else TOL_BF16
+    assert G.rel_err(got, ref) <= tol
+
+
+@pytest.mark.parametrize("pipe", ["single", "pair"])
+@pytest.mark.parametrize("out_dtype", [0, 1])
+def test_grouped_input_gradient(nv, pipe, out_dtype):
+    """dX = W_hat^T dY with W_hat read as stored ([E, K, N], MN-major tiles):
+    ragged experts, an empty one, three 256-column tiles and K over several
+    64-element slices; rows past each expert's tokens are zero and give zeros."""
+    E, K, N = 4, 320, 768
+    counts = np.array([70, 0, 300, 129])
+    offsets = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)]).astype(np.int32)
+    rows = int(offsets[-1])
+    rng = np.random.default_rng(23)
+    dy = np.zeros((rows, K), np.float32)
+    for e in range(E):
+        dy[offsets[e]:offsets[e] + counts[e]] = rng.standard_normal((counts[e], K))
+    dyu = oracle.bf16_round(dy)
+    wu = oracle.bf16_round((rng.standard_normal((E, K, N)) * 0.05).astype(np.float32))
+    y = G.zeros((rows, N), torch.float32 if out_dtype == 0 else torch.bfloat16)
+    y.fill_(7.0)
+    st = G.zeros(1, torch.int32)
+    prev = nv.nvfp4_gemm_pipeline({"single": 1, "pair": 2}[pipe])
+    try:
+        nv.nvfp4_bf16_grouped_gemm_dgrad(G.bf16_from_u16(dyu), G.bf16_from_u16(wu), torch.tensor(offsets, device=G.DEV),
+                                         E, N, K, y, out_dtype=out_dtype, dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        nv.nvfp4_gemm_pipeline(prev)
+    G.status_ok(st)
+    got = y.float().cpu().numpy()
+    tol = TOL if out_dtype == 0 else TOL_BF16
+    for e in range(E):
+        r0, n = int(offsets[e]), int(counts[e])
+        if n:
+            ref = oracle.bf16_gemm(dyu[r0:r0 + n], np.ascontiguousarray(wu[e].T))
+            assert G.rel_err(got[r0:r0 + n], ref) <= tol, e
+        assert not got[r0 + n:int(offsets[e + 1])].any(), e
 
 
 def test_qat_layer_backward_stage_by_stage(nv):

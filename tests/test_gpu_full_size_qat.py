@@ -65,11 +65,9 @@ def test_fake_quant_bit_exact(qat):
             assert np.array_equal(G.u16(w_hat[e]), ref), e
 
 
-def test_training_fake_quant_writes_the_transposes(qat):
+def test_training_fake_quant_matches_the_forward(qat):
     P, L = qat["plain"], qat["train"]
     assert torch.equal(L.w13_hat, P.w13_hat) and torch.equal(L.wd_hat, P.wd_hat)
-    for e in qat["experts"]:
-        assert torch.equal(L.w13_t[e], L.w13_hat[e].t()) and torch.equal(L.wd_t[e], L.wd_hat[e].t())
 
 
 def test_forward_sampled_rows(qat):
@@ -102,9 +100,9 @@ def test_training_step_gradients(qat):
         assert G.rel_err(f64(qat["dwd"][e]), oracle.segment_wgrad(dy, h, one)[0]) <= 1e-5, e
         assert G.rel_err(f64(qat["dw13"][e]), oracle.segment_wgrad(dgu, xr, one)[0]) <= 1e-5, e
         rr = torch.from_numpy(_rows(L, e, rng)).to(G.DEV)
-        # dh = dY . Wd_hat and dx = d(gate|up) . W13_hat: products with the transposed weights
-        assert G.rel_err(f64(L.dh[rr]), oracle.bf16_gemm(G.u16(L.dy[rr]), G.u16(L.wd_t[e]))) <= TOL_BF16, e
-        assert G.rel_err(f64(L.dxr[rr]), oracle.bf16_gemm(G.u16(L.dgu[rr]), G.u16(L.w13_t[e]))) <= TOL_BF16, e
+        # dh = dY . Wd_hat and dx = d(gate|up) . W13_hat (the oracle takes the transposed weights)
+        assert G.rel_err(f64(L.dh[rr]), oracle.bf16_gemm(G.u16(L.dy[rr]), G.u16(L.wd_hat[e].t().contiguous()))) <= TOL_BF16, e
+        assert G.rel_err(f64(L.dxr[rr]), oracle.bf16_gemm(G.u16(L.dgu[rr]), G.u16(L.w13_hat[e].t().contiguous()))) <= TOL_BF16, e
     T, topk = qat["c"]["T"], qat["c"]["topk"]
     toks = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
     dst = L.route.dst_row.cpu().numpy()[toks]
