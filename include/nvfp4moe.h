@@ -71,8 +71,9 @@ typedef enum {
 
 /* Output element type of the GEMMs. */
 enum { NVFP4_OUT_F32 = 0, NVFP4_OUT_BF16 = 1 };
-/* Epilogue of the W4A4 + RAC GEMM. */
-enum { NVFP4_EPI_NONE = 0, NVFP4_EPI_SWIGLU = 1 };
+/* Epilogue of the grouped GEMMs: none, SwiGLU of the gate/up product (forward),
+ * or the SwiGLU backward of the input-gradient GEMM (nvfp4_bf16_grouped_gemm_dgrad). */
+enum { NVFP4_EPI_NONE = 0, NVFP4_EPI_SWIGLU = 1, NVFP4_EPI_SWIGLU_BWD = 2 };
 enum { NVFP4_PIPELINE_AUTO = 0, NVFP4_PIPELINE_SINGLE = 1, NVFP4_PIPELINE_PAIR = 2 };
 
 /* Name of a status code ("NVFP4_OK", ...); never NULL. */
@@ -427,7 +428,7 @@ int nvfp4_swiglu_backward(const void *gu, const void *dh, int64_t rows, int64_t 
  *   dout      device float [T, H];  y  device BF16 [rows_cap, H] (the forward's rows)
  *   dy        device BF16 [rows_cap, H];  dweights  device float [T, topk] or NULL
  * Errors: INVALID_ARG, ALIGNMENT (16-byte pointers), UNSUPPORTED (E > 65535,
- * H % 8, H > 8192). */
+ * H % 8, H > 8192, topk > 32). */
 int nvfp4_moe_combine_backward(const float *dout, const void *y, const int32_t *dst_row, const float *weights,
                                int32_t T, int32_t topk, int64_t H, const int32_t *counts, const int32_t *offsets,
                                int32_t E, int64_t rows_cap, void *dy, float *dweights, void *stream);
@@ -458,13 +459,21 @@ int nvfp4_bf16_grouped_gemm_wgrad(const void *a_t, const void *b_t, const int32_
  *   w_hat    device BF16 [E, K, N] (the forward weight: K outputs x N inputs,
  *            e.g. nvfp4_fake_quant output)
  *   offsets  as for nvfp4_bf16_grouped_gemm
- *   y        device [rows_cap, N] (ldy), F32 or BF16 (out_dtype)
+ *   epilogue NVFP4_EPI_NONE: y [rows_cap, N] (ldy >= N), F32 or BF16 (out_dtype).
+ *            NVFP4_EPI_SWIGLU_BWD: the product is dh, the gradient of a SwiGLU
+ *            output h = silu(g) * u; with gu = the saved pre-activations
+ *            [g | u] (device BF16 [rows_cap, 2N]) the epilogue writes
+ *            y = [d(gate) | d(up)] (BF16 [rows_cap, 2N], ldy >= 2N), exactly
+ *            what nvfp4_swiglu_backward computes from dh rounded to BF16 -- so
+ *            dh itself never goes to memory.  out_dtype must be BF16.
+ *   gu       device BF16 [rows_cap, 2N] for NVFP4_EPI_SWIGLU_BWD, else NULL
  * Runs on the pipeline nvfp4_gemm_pipeline selects for BF16.
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 256, E > 1024,
  * E*K > 2^31); dev_status gets TIMEOUT if a pipeline wait runs out. */
 int nvfp4_bf16_grouped_gemm_dgrad(const void *dy, const void *w_hat, const int32_t *offsets, int32_t E,
-                                  int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, void *y,
-                                  int64_t ldy, int32_t *dev_status, void *stream);
+                                  int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype,
+                                  int32_t epilogue, const void *gu, void *y, int64_t ldy,
+                                  int32_t *dev_status, void *stream);
 
 /* dW = dW_hat of the straight-through estimator, QUADS §3.2 Eq. 13, from the
  * routed rows as stored: dw[e] = a[seg e, :]^T . b[seg e, :] for every expert
@@ -499,13 +508,21 @@ int nvfp4_selftest_wait_timeout(int32_t limit_us, int32_t *dev_status, void *str
  *   w_hat    device BF16 [E, K, N] (the forward weight: K outputs x N inputs,
  *            e.g. nvfp4_fake_quant output)
  *   offsets  as for nvfp4_bf16_grouped_gemm
- *   y        device [rows_cap, N] (ldy), F32 or BF16 (out_dtype)
+ *   epilogue NVFP4_EPI_NONE: y [rows_cap, N] (ldy >= N), F32 or BF16 (out_dtype).
+ *            NVFP4_EPI_SWIGLU_BWD: the product is dh, the gradient of a SwiGLU
+ *            output h = silu(g) * u; with gu = the saved pre-activations
+ *            [g | u] (device BF16 [rows_cap, 2N]) the epilogue writes
+ *            y = [d(gate) | d(up)] (BF16 [rows_cap, 2N], ldy >= 2N), exactly
+ *            what nvfp4_swiglu_backward computes from dh rounded to BF16 -- so
+ *            dh itself never goes to memory.  out_dtype must be BF16.
+ *   gu       device BF16 [rows_cap, 2N] for NVFP4_EPI_SWIGLU_BWD, else NULL
  * Runs on the pipeline nvfp4_gemm_pipeline selects for BF16.
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 256, E > 1024,
  * E*K > 2^31); dev_status gets TIMEOUT if a pipeline wait runs out. */
 int nvfp4_bf16_grouped_gemm_dgrad(const void *dy, const void *w_hat, const int32_t *offsets, int32_t E,
-                                  int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, void *y,
-                                  int64_t ldy, int32_t *dev_status, void *stream);
+                                  int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype,
+                                  int32_t epilogue, const void *gu, void *y, int64_t ldy,
+                                  int32_t *dev_status, void *stream);
 
 /* dW = dW_hat of the straight-through estimator, QUADS §3.2 Eq. 13, from the
  * routed rows as stored: dw[e] = a[seg e, :]^T . b[seg e, :] for every expert

@@ -19,7 +19,7 @@ import torch
 from .build import LIB, build_library
 
 NVFP4_OUT_F32, NVFP4_OUT_BF16 = 0, 1
-NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU = 0, 1
+NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_EPI_SWIGLU_BWD = 0, 1, 2
 NVFP4_PIPELINE_AUTO, NVFP4_PIPELINE_SINGLE, NVFP4_PIPELINE_PAIR = 0, 1, 2
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED",
           3: "NVFP4_ERR_ALIGNMENT", 4: "NVFP4_ERR_CUDA", 5: "NVFP4_ERR_TIMEOUT",
@@ -44,7 +44,7 @@ _SIGS = {
     "nvfp4_moe_combine_backward": "ppppiiqppiqppp",
     "nvfp4_bf16_grouped_gemm_wgrad": "pppiqqqippp",
     "nvfp4_bf16_grouped_gemm_wgrad_rows": "pppiqqqippp",
-    "nvfp4_bf16_grouped_gemm_dgrad": "pppiqqqipqpp",
+    "nvfp4_bf16_grouped_gemm_dgrad": "pppiqqqiippqpp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
     "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
     "nvfp4_gemm_pipeline": "ip",
@@ -219,12 +219,13 @@ def nvfp4_bf16_grouped_gemm(x, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F
           epilogue, _p(y), y.stride(0), _p(dev_status), _s(stream))
 
 
-def nvfp4_bf16_grouped_gemm_dgrad(dy, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F32, dev_status=None,
-                                  stream=None):
-    """Eq. 13 dX: y = dy . w_hat[e] per expert segment, dy [rows_cap, K], w_hat [E, K, N] as stored."""
+def nvfp4_bf16_grouped_gemm_dgrad(dy, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F32,
+                                  epilogue=NVFP4_EPI_NONE, gu=None, dev_status=None, stream=None):
+    """Eq. 13 dX: y = dy . w_hat[e] per expert segment, dy [rows_cap, K], w_hat [E, K, N] as stored;
+    with epilogue=NVFP4_EPI_SWIGLU_BWD and the saved pre-activations gu [rows_cap, 2N], y = [dg | du]."""
     rows_cap = dy.shape[0]
-    _call("nvfp4_bf16_grouped_gemm_dgrad", _p(dy), _p(w_hat), _p(offsets), E, rows_cap, N, K, out_dtype, _p(y),
-          y.stride(0), _p(dev_status), _s(stream))
+    _call("nvfp4_bf16_grouped_gemm_dgrad", _p(dy), _p(w_hat), _p(offsets), E, rows_cap, N, K, out_dtype, epilogue,
+          _p(gu), _p(y), y.stride(0), _p(dev_status), _s(stream))
 
 
 def nvfp4_transpose_bf16(x, y, stream=None):

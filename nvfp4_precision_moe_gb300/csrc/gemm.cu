@@ -152,14 +152,19 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
 }
 
 extern "C" int nvfp4_bf16_grouped_gemm_dgrad(const void *dy, const void *w_hat, const int32_t *offsets, int32_t E,
-                                             int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, void *y,
-                                             int64_t ldy, int32_t *dev_status, void *stream) {
+                                             int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype,
+                                             int32_t epilogue, const void *gu, void *y, int64_t ldy,
+                                             int32_t *dev_status, void *stream) {
     if (!dy || !w_hat || !offsets || !y || E < 1 || rows_cap < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
     if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
-    if (ldy < N) return NVFP4_ERR_INVALID_ARG;
+    if (epilogue != NVFP4_EPI_NONE && epilogue != NVFP4_EPI_SWIGLU_BWD) return NVFP4_ERR_INVALID_ARG;
+    const bool bwd = epilogue == NVFP4_EPI_SWIGLU_BWD;
+    if (bwd && (!gu || out_dtype != NVFP4_OUT_BF16)) return NVFP4_ERR_INVALID_ARG;
+    if (ldy < (bwd ? 2 * N : N)) return NVFP4_ERR_INVALID_ARG;
     if (K % 64 || N % 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) || (int64_t)E * K > (1ll << 31))
         return NVFP4_ERR_UNSUPPORTED;
-    if (!aligned16(dy) || !aligned16(w_hat) || !aligned16(y) || ldy % 8) return NVFP4_ERR_ALIGNMENT;
+    if (!aligned16(dy) || !aligned16(w_hat) || !aligned16(y) || ldy % 8 || (bwd && !aligned16(gu)))
+        return NVFP4_ERR_ALIGNMENT;
     if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
     // A: dy rows, K-major; B: the experts' [K, N] blocks stacked, MN-major boxes of 64 columns x 64 K-rows
@@ -172,7 +177,8 @@ extern "C" int nvfp4_bf16_grouped_gemm_dgrad(const void *dy, const void *w_hat, 
     if (s != NVFP4_OK) return s;
     GemmParams p{};
     p.a_codes_base = (const uint8_t *)dy;
-    p.epilogue = NVFP4_EPI_NONE;
+    p.epilogue = epilogue;
+    p.gu = bwd ? (const uint16_t *)gu : nullptr;
     p.offsets = offsets;
     p.rows_cap = (int32_t)rows_cap;
     p.E = E;

@@ -74,6 +74,8 @@ struct GemmParams {
     // BF16 operands stored MN-major (the M or N index contiguous): A (weight-gradient mode) and B
     // (both modes) arrive as TMA boxes of 64 MN-elements x 64 K-rows, 8 KB apart (desc_sw128_mn)
     int32_t a_mn, b_mn;
+    // NVFP4_EPI_SWIGLU_BWD (BF16): the saved pre-activations [g | u], [rows_cap, 2N]
+    const uint16_t *gu;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -145,6 +147,41 @@ __device__ __forceinline__ void swiglu16(uint16_t *dst16, bool vec32, float gmul
         amax_local = fmaxf(amax_local, fabsf(__uint_as_float(o[i / 2] & 0xffff0000u)));
     }
     store32B(dst16, vec32, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
+}
+
+// The SwiGLU backward of 16 columns col..col+15 of row `row` (BF16 pipelines,
+// NVFP4_EPI_SWIGLU_BWD): the accumulator holds dh = dY W_hat; rounded to BF16
+// (as a stored dh would be) and with the saved pre-activations g, u of those
+// columns it gives d(gate) = bf16(dh u s (1 + g (1 - s))) and d(up) =
+// bf16(dh g s), s = 1 / (1 + exp(-g)) in binary32, stored at columns col and
+// N + col of y -- the arithmetic of nvfp4_swiglu_backward.
+__device__ __forceinline__ void swiglu_bwd16(const GemmParams &p, int64_t row, int64_t col, const uint32_t *d) {
+    const uint16_t *gr = p.gu + row * 2 * p.N + col;
+    const uint4 g0 = __ldg(reinterpret_cast<const uint4 *>(gr)), g1 = __ldg(reinterpret_cast<const uint4 *>(gr) + 1);
+    const uint4 u0 = __ldg(reinterpret_cast<const uint4 *>(gr + p.N)),
+                u1 = __ldg(reinterpret_cast<const uint4 *>(gr + p.N) + 1);
+    const uint32_t G[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const uint32_t U[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    uint32_t og[8], ou[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float rg[2], ru[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const float g = __uint_as_float(hh ? (G[i] & 0xffff0000u) : (G[i] << 16));
+            const float u = __uint_as_float(hh ? (U[i] & 0xffff0000u) : (U[i] << 16));
+            const float dh = __bfloat162float(__float2bfloat16_rn(__uint_as_float(d[2 * i + hh])));
+            const float s = __frcp_rn(__fadd_rn(1.0f, expf(-g)));
+            const float ds = __fmul_rn(s, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, s))));
+            rg[hh] = __fmul_rn(__fmul_rn(dh, u), ds);
+            ru[hh] = __fmul_rn(dh, __fmul_rn(g, s));
+        }
+        og[i] = pack_bf16x2(rg[0], rg[1]);
+        ou[i] = pack_bf16x2(ru[0], ru[1]);
+    }
+    uint16_t *yr = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + col;
+    store32B(yr, p.vec32, og[0], og[1], og[2], og[3], og[4], og[5], og[6], og[7]);
+    store32B(yr + p.N, p.vec32, ou[0], ou[1], ou[2], ou[3], ou[4], ou[5], ou[6], ou[7]);
 }
 
 // One stage's block scales, from shared memory to this warp's 32-lane quarter

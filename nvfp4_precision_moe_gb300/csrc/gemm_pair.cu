@@ -421,6 +421,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)t.nt * 128 + 64 * half;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) swiglu16(yrow + 16 * j, p.vec32, gmul, v + 16 * j, v + 64 + 16 * j, amax_local);
+            } else if (!FP4 && p.epilogue == NVFP4_EPI_SWIGLU_BWD) {
+                const int64_t col = (int64_t)t.nt * kBN + 128 * half;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) swiglu_bwd16(p, row, col + 16 * j, v + 16 * j);
             } else {
                 const int64_t col = (int64_t)t.nt * kBN + 128 * half;
 #pragma unroll

@@ -1074,7 +1074,7 @@ struct FQArgs {
 
 __global__ void __launch_bounds__(256, 4) fake_quant_fused_kernel(FQArgs a) {
     __shared__ QTables tb;
-    __shared__ int64_t s_item;
+    __shared__ int64_t s_next[2];  // the item after the current one, by iteration parity
     __shared__ uint32_t s_red[8];
     __shared__ int s_ok;
     fill_tables(tb);
@@ -1083,12 +1083,10 @@ __global__ void __launch_bounds__(256, 4) fake_quant_fused_kernel(FQArgs a) {
     const int nb = (int)(a.cols >> 4), segs = (nb + 31) >> 5;
     uint32_t *amax_bits = a.ws, *done = a.ws + a.nt, *counter = a.ws + 2 * a.nt;
     const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
-    for (;;) {
-        __syncthreads();  // the previous item's readers of s_item, s_red and s_ok are done (and the tables ready)
-        if (threadIdx.x == 0) s_item = (int64_t)atomicAdd(counter, 1u);
-        __syncthreads();
-        const int64_t item = s_item;
-        if (item >= total) break;
+    if (threadIdx.x == 0) s_next[0] = (int64_t)atomicAdd(counter, 1u);
+    __syncthreads();  // the first item, and the tables, are ready
+    int64_t item = s_next[0];
+    for (int iter = 0; item < total; ++iter) {
         // group gi: 0 -> A(0); 2nt-1 -> B(nt-1); odd -> A((gi+1)/2); even -> B(gi/2 - 1)
         const int64_t gi = item / a.per;
         const int chunk = (int)(item - gi * a.per);
@@ -1130,75 +1128,83 @@ __global__ void __launch_bounds__(256, 4) fake_quant_fused_kernel(FQArgs a) {
                 __threadfence();  // the maximum is visible before the item counts as done
                 atomicAdd(done + t, 1u);
             }
-            continue;
-        }
-        // B(t): wait for every A(t) item, then quantize-dequantize the rows
-        if (threadIdx.x == 0) {
-            const volatile uint32_t *d = done + t;
-            bool ok = *d >= (uint32_t)a.per;
-            const uint64_t t0 = global_ns();
-            while (!ok) {
-                __nanosleep(200);
-                ok = *d >= (uint32_t)a.per;
-                if (!ok && global_ns() - t0 > kFQWaitNs) break;
-            }
-            __threadfence();
-            s_ok = ok;
-            if (!ok) report(a.dev_status, NVFP4_ERR_TIMEOUT);
-        }
-        __syncthreads();
-        if (!s_ok) continue;
-        const float amax_t = __uint_as_float(*(const volatile uint32_t *)(amax_bits + t));
-        const float gs = tensor_scale(amax_t);
-        const float p6 = __fmul_rn(gs, 6.0f);
-        const float inv_gs = __frcp_rn(gs);
-        if (chunk == 0 && threadIdx.x == 0) {
-            if (a.gs_out) a.gs_out[t] = gs;
-            if (!isfinite(amax_t)) report(a.dev_status, NVFP4_ERR_NONFINITE);
-        }
-        uint16_t *ot = a.w_hat + (int64_t)t * a.rows * a.cols;
-        // this warp's rows r0 + wid + 8 i (i < nrw), their segments in order; the
-        // loads run two segments ahead, across row ends
-        const int nrw = r1 - r0 > wid ? (int)((r1 - r0 - wid + 7) >> 3) : 0;
-        auto load = [&](int i, int sg, uint4 &x0, uint4 &x1) {
-            const int b = sg * 32 + lane;
-            if (i < nrw && b < nb) {
-                const uint4 *p = reinterpret_cast<const uint4 *>(wt + (r0 + wid + 8 * i) * a.cols + b * 16);
-                x0 = ld_hint(p, drop);
-                x1 = ld_hint(p + 1, drop);
-            }
-        };
-        int li = 0, lsg = 0;  // the next segment to load
-        auto step = [&](int &i, int &sg) {
-            if (++sg == segs) {
-                sg = 0;
-                ++i;
-            }
-        };
-        uint4 n0a = make_uint4(0, 0, 0, 0), n0b = n0a, n1a = n0a, n1b = n0a;
-        load(li, lsg, n0a, n0b);
-        step(li, lsg);
-        load(li, lsg, n1a, n1b);
-        step(li, lsg);
-        for (int ci = 0, csg = 0; ci < nrw; step(ci, csg)) {
-            const uint4 ca = n0a, cb = n0b;
-            n0a = n1a;
-            n0b = n1b;
+        } else {
+            // B(t): this warp's rows r0 + wid + 8 i (i < nrw), their segments in order; the
+            // loads run two segments ahead, across row ends.  The weights are inputs, so the
+            // first loads go out before the wait for the tensor's amax.
+            const int nrw = r1 - r0 > wid ? (int)((r1 - r0 - wid + 7) >> 3) : 0;
+            auto load = [&](int i, int sg, uint4 &x0, uint4 &x1) {
+                const int b = sg * 32 + lane;
+                if (i < nrw && b < nb) {
+                    const uint4 *p = reinterpret_cast<const uint4 *>(wt + (r0 + wid + 8 * i) * a.cols + b * 16);
+                    x0 = ld_hint(p, drop);
+                    x1 = ld_hint(p + 1, drop);
+                }
+            };
+            int li = 0, lsg = 0;  // the next segment to load
+            auto step = [&](int &i, int &sg) {
+                if (++sg == segs) {
+                    sg = 0;
+                    ++i;
+                }
+            };
+            uint4 n0a = make_uint4(0, 0, 0, 0), n0b = n0a, n1a = n0a, n1b = n0a;
+            load(li, lsg, n0a, n0b);
+            step(li, lsg);
             load(li, lsg, n1a, n1b);
             step(li, lsg);
-            const int b = csg * 32 + lane;
-            if (b < nb) {
-                float v[16];
-                BlockQ q;
-                unpack_block(ca, cb, v);
-                quant_block(v, gs, p6, inv_gs, tb, q);
-                uint32_t o[8];
-                dequant_block_bf16(q, gs, o);
-                uint4 *dst = reinterpret_cast<uint4 *>(ot + (r0 + wid + 8 * ci) * a.cols + b * 16);
-                st_hint(dst, make_uint4(o[0], o[1], o[2], o[3]), drop);
-                st_hint(dst + 1, make_uint4(o[4], o[5], o[6], o[7]), drop);
+            // wait for every A(t) item
+            if (threadIdx.x == 0) {
+                const volatile uint32_t *d = done + t;
+                bool ok = *d >= (uint32_t)a.per;
+                const uint64_t t0 = global_ns();
+                while (!ok) {
+                    __nanosleep(200);
+                    ok = *d >= (uint32_t)a.per;
+                    if (!ok && global_ns() - t0 > kFQWaitNs) break;
+                }
+                __threadfence();
+                s_ok = ok;
+                if (!ok) report(a.dev_status, NVFP4_ERR_TIMEOUT);
+            }
+            __syncthreads();
+            if (s_ok) {
+                const float amax_t = __uint_as_float(*(const volatile uint32_t *)(amax_bits + t));
+                const float gs = tensor_scale(amax_t);
+                const float p6 = __fmul_rn(gs, 6.0f);
+                const float inv_gs = __frcp_rn(gs);
+                if (chunk == 0 && threadIdx.x == 0) {
+                    if (a.gs_out) a.gs_out[t] = gs;
+                    if (!isfinite(amax_t)) report(a.dev_status, NVFP4_ERR_NONFINITE);
+                }
+                uint16_t *ot = a.w_hat + (int64_t)t * a.rows * a.cols;
+                for (int ci = 0, csg = 0; ci < nrw; step(ci, csg)) {
+                    const uint4 ca = n0a, cb = n0b;
+                    n0a = n1a;
+                    n0b = n1b;
+                    load(li, lsg, n1a, n1b);
+                    step(li, lsg);
+                    const int b = csg * 32 + lane;
+                    if (b < nb) {
+                        float v[16];
+                        BlockQ q;
+                        unpack_block(ca, cb, v);
+                        quant_block(v, gs, p6, inv_gs, tb, q);
+                        uint32_t o[8];
+                        dequant_block_bf16(q, gs, o);
+                        uint4 *dst = reinterpret_cast<uint4 *>(ot + (r0 + wid + 8 * ci) * a.cols + b * 16);
+                        st_hint(dst, make_uint4(o[0], o[1], o[2], o[3]), drop);
+                        st_hint(dst + 1, make_uint4(o[4], o[5], o[6], o[7]), drop);
+                    }
+                }
             }
         }
+        // thread 0 takes the next item once its own share is done, so the counter's round trip
+        // overlaps the other warps' tail (s_next by parity: every thread read the other slot
+        // before this iteration's barriers)
+        if (threadIdx.x == 0) s_next[(iter + 1) & 1] = (int64_t)atomicAdd(counter, 1u);
+        __syncthreads();  // the item is done: s_next is visible, s_red and s_ok may be rewritten
+        item = s_next[(iter + 1) & 1];
     }
 }
 

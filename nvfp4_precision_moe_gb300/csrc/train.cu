@@ -175,19 +175,25 @@ __global__ void __launch_bounds__(256) swiglu_backward8_kernel(const uint16_t *g
 
 // Backward of out[t] = sum_s w[t,s] y[dst[t,s]]: the routed gradient
 // dy[dst[t,s]] = bf16(w[t,s] dout[t]) and, when asked, the weights' gradient
-// dw[t,s] = <y[dst[t,s]], dout[t]> (binary32 lane sums, one block per token).
-// H % 8 == 0 and 16-byte aligned rows: 8 elements per thread and access
-// (dout read once per token into registers, reused for every slot).
+// dw[t,s] = <y[dst[t,s]], dout[t]> (binary32 lane sums in element order, a
+// warp's lanes by a butterfly, then the block's warps in order; one block per
+// token).  H % 8 == 0 and 16-byte aligned rows: NV 8-element vectors per
+// thread (dout read once per token into registers, reused for every slot);
+// the rows of kCombineBwdGroup slots are loaded together, and the weights'
+// gradients of all slots are summed across warps after one barrier.
 constexpr int kCombineBwdMaxVec = 4;  // 8-element vectors per thread: H <= 8 * 256 * 4
+constexpr int kCombineBwdGroup = 4;
+constexpr int kCombineBwdMaxTopk = 32;
+template <int NV>
 __global__ void __launch_bounds__(256) combine_backward_kernel(const float *dout, const uint16_t *y,
                                                                const int32_t *dst, const float *w, int32_t topk,
                                                                int64_t H, int64_t rows_cap, uint16_t *dy, float *dw) {
-    __shared__ float red[8];
+    __shared__ float red[kCombineBwdMaxTopk][8];
     const int64_t t = blockIdx.x;
     const int nv = (int)(H >> 3);
-    float g[kCombineBwdMaxVec][8];
+    float g[NV][8];
 #pragma unroll
-    for (int i = 0; i < kCombineBwdMaxVec; ++i) {
+    for (int i = 0; i < NV; ++i) {
         const int v = threadIdx.x + 256 * i;
         if (v < nv) {
             const float4 a = __ldg(reinterpret_cast<const float4 *>(dout + t * H) + 2 * v);
@@ -196,39 +202,57 @@ __global__ void __launch_bounds__(256) combine_backward_kernel(const float *dout
             g[i][4] = b.x, g[i][5] = b.y, g[i][6] = b.z, g[i][7] = b.w;
         }
     }
-    for (int s = 0; s < topk; ++s) {
-        const int64_t r = dst[t * topk + s];
-        const bool ok = r >= 0 && r < rows_cap;
-        const float ws = w[t * topk + s];
-        float acc = 0.0f;
+    for (int s0 = 0; s0 < topk; s0 += kCombineBwdGroup) {
+        int64_t r[kCombineBwdGroup];
+        bool ok[kCombineBwdGroup];
+        float ws[kCombineBwdGroup];
+        uint4 yv[kCombineBwdGroup][NV];
 #pragma unroll
-        for (int i = 0; i < kCombineBwdMaxVec; ++i) {
-            const int v = threadIdx.x + 256 * i;
-            if (ok && v < nv) {
-                const uint4 yv = __ldg(reinterpret_cast<const uint4 *>(y + r * H) + v);
-                const uint32_t yw[4] = {yv.x, yv.y, yv.z, yv.w};
-                uint32_t o[4];
+        for (int j = 0; j < kCombineBwdGroup; ++j) {
+            const bool in = s0 + j < topk;
+            r[j] = in ? (int64_t)dst[t * topk + s0 + j] : -1;
+            ok[j] = in && r[j] >= 0 && r[j] < rows_cap;
+            ws[j] = in ? w[t * topk + s0 + j] : 0.0f;
+        }
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    o[k] = (uint32_t)to_bf(__fmul_rn(ws, g[i][2 * k])) |
-                           ((uint32_t)to_bf(__fmul_rn(ws, g[i][2 * k + 1])) << 16);
-                    acc = __fmaf_rn(__uint_as_float(yw[k] << 16), g[i][2 * k], acc);
-                    acc = __fmaf_rn(__uint_as_float(yw[k] & 0xffff0000u), g[i][2 * k + 1], acc);
+        for (int j = 0; j < kCombineBwdGroup; ++j)
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int v = threadIdx.x + 256 * i;
+                if (ok[j] && v < nv) yv[j][i] = __ldg(reinterpret_cast<const uint4 *>(y + r[j] * H) + v);
+            }
+#pragma unroll
+        for (int j = 0; j < kCombineBwdGroup; ++j) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int v = threadIdx.x + 256 * i;
+                if (ok[j] && v < nv) {
+                    const uint32_t yw[4] = {yv[j][i].x, yv[j][i].y, yv[j][i].z, yv[j][i].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        o[k] = (uint32_t)to_bf(__fmul_rn(ws[j], g[i][2 * k])) |
+                               ((uint32_t)to_bf(__fmul_rn(ws[j], g[i][2 * k + 1])) << 16);
+                        acc = __fmaf_rn(__uint_as_float(yw[k] << 16), g[i][2 * k], acc);
+                        acc = __fmaf_rn(__uint_as_float(yw[k] & 0xffff0000u), g[i][2 * k + 1], acc);
+                    }
+                    reinterpret_cast<uint4 *>(dy + r[j] * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
                 }
-                reinterpret_cast<uint4 *>(dy + r * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (dw && s0 + j < topk) {
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if ((threadIdx.x & 31) == 0) red[s0 + j][threadIdx.x >> 5] = acc;
             }
         }
-        if (dw) {
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                float sum = 0.0f;
-                for (int i = 0; i < (int)(blockDim.x >> 5); ++i) sum += red[i];
-                dw[t * topk + s] = sum;
-            }
-            __syncthreads();
+    }
+    if (dw) {
+        __syncthreads();
+        if ((int)threadIdx.x < topk) {
+            float sum = 0.0f;
+            for (int i = 0; i < 8; ++i) sum += red[threadIdx.x][i];
+            dw[t * topk + threadIdx.x] = sum;
         }
     }
 }
@@ -312,7 +336,8 @@ extern "C" int nvfp4_moe_combine_backward(const float *dout, const void *y, cons
     if (!dout || !y || !dst_row || !weights || !counts || !offsets || !dy || T < 0 || topk < 1 || H < 0 || E < 1 ||
         rows_cap < 0)
         return NVFP4_ERR_INVALID_ARG;
-    if (E > 65535 || H % 8 || H > 8 * 256 * kCombineBwdMaxVec) return NVFP4_ERR_UNSUPPORTED;
+    if (E > 65535 || H % 8 || H > 8 * 256 * kCombineBwdMaxVec || topk > kCombineBwdMaxTopk)
+        return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(dout) || !aligned16(y) || !aligned16(dy)) return NVFP4_ERR_ALIGNMENT;
     if (H == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
@@ -320,7 +345,10 @@ extern "C" int nvfp4_moe_combine_backward(const float *dout, const void *y, cons
     zero_padding_bf16_kernel<<<dim3(127, E), 256, 0, st>>>(counts, offsets, rows_cap, H, (uint16_t *)dy);
     int s = launch_status("zero_padding_bf16_kernel");
     if (s != NVFP4_OK || T == 0) return s;
-    combine_backward_kernel<<<(unsigned)T, 256, 0, st>>>(dout, (const uint16_t *)y, dst_row, weights, topk, H,
-                                                         rows_cap, (uint16_t *)dy, dweights);
+    const int nv = (int)((H / 8 + 255) / 256);  // 8-element vectors per thread
+    auto kern = nv <= 1 ? combine_backward_kernel<1>
+                        : nv == 2 ? combine_backward_kernel<2> : nv == 3 ? combine_backward_kernel<3> : combine_backward_kernel<4>;
+    kern<<<(unsigned)T, 256, 0, st>>>(dout, (const uint16_t *)y, dst_row, weights, topk, H, rows_cap, (uint16_t *)dy,
+                                      dweights);
     return launch_status("combine_backward_kernel");
 }

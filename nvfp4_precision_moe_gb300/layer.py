@@ -15,13 +15,13 @@ combine.
 """
 import torch
 
-from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_OUT_BF16,
+from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_EPI_SWIGLU_BWD, NVFP4_OUT_BF16,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
                nvfp4_bf16_grouped_gemm_dgrad, nvfp4_bf16_grouped_gemm_wgrad_rows, nvfp4_gather_selected_weights,
                nvfp4_moe_combine_backward,
                nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online, nvfp4_route_topk, nvfp4_swiglu,
-               nvfp4_swiglu_backward, nvfp4_w4a4_rac_grouped_gemm)
+               nvfp4_w4a4_rac_grouped_gemm)
 
 
 def scale_bytes(rows, K):
@@ -229,7 +229,6 @@ class QatMoE:
             bf = dict(dtype=torch.bfloat16, device=dev)
             self.gu = torch.zeros((R, 2 * I), **bf)
             self.dy = torch.zeros((R, H), **bf)
-            self.dh = torch.zeros((R, I), **bf)
             self.dgu = torch.zeros((R, 2 * I), **bf)
             self.dxr = torch.zeros((R, H), **bf)
             self.ones = torch.ones((max_tokens, topk), dtype=torch.float32, device=dev)
@@ -318,14 +317,14 @@ class QatMoE:
         # routed output gradient, and the combine weights' gradient
         nvfp4_moe_combine_backward(dout, self.y, dst, w, r.counts, r.offsets, E, self.dy,
                                    dweights=self.dweights[:T], stream=stream)
-        # down projection: dh = dY W_hat_d (W_hat_d read as stored, [H, I] per expert), dW_d = dY^T h
-        # (the routed rows read as stored)
-        nvfp4_bf16_grouped_gemm_dgrad(self.dy, self.wd_hat, r.offsets, E, I, H, self.dh, out_dtype=NVFP4_OUT_BF16,
-                                      dev_status=self.dev_status, stream=stream)
+        # down projection: dh = dY W_hat_d (W_hat_d read as stored, [H, I] per expert) and, in the
+        # same GEMM's epilogue, the SwiGLU backward d(gate|up) from dh and the saved pre-activations;
+        # dW_d = dY^T h (the routed rows read as stored)
+        nvfp4_bf16_grouped_gemm_dgrad(self.dy, self.wd_hat, r.offsets, E, I, H, self.dgu, out_dtype=NVFP4_OUT_BF16,
+                                      epilogue=NVFP4_EPI_SWIGLU_BWD, gu=self.gu, dev_status=self.dev_status,
+                                      stream=stream)
         nvfp4_bf16_grouped_gemm_wgrad_rows(self.dy, self.h, r.offsets, E, self.dwd, dev_status=self.dev_status,
                                            stream=stream)
-        # SwiGLU
-        nvfp4_swiglu_backward(self.gu, self.dh, self.dgu, stream=stream)
         # gate_up projection: dx_routed = d(gate|up) W_hat_13, dW_13 = d(gate|up)^T x_routed
         nvfp4_bf16_grouped_gemm_dgrad(self.dgu, self.w13_hat, r.offsets, E, H, 2 * I, self.dxr,
                                       out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
