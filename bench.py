@@ -482,16 +482,39 @@ def qat_measure(dev, steps):
         tl.backward(dout)
     torch.cuda.synchronize()
     bev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    sev = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(steps)]
     for i in range(steps):
         bev[i][0].record(stream)
         tl.forward(x, logits)
         bev[i][1].record(stream)
-        tl.backward(dout)
+        tl.backward(dout, mark=lambda k, i=i: sev[i][k].record(stream))
         bev[i][2].record(stream)
     torch.cuda.synchronize()
     assert int(tl.dev_status.item()) == 0
     tfwd = statistics.median([bev[i][0].elapsed_time(bev[i][1]) for i in range(steps)])
     tbwd = statistics.median([bev[i][1].elapsed_time(bev[i][2]) for i in range(steps)])
+    bnames = ["combine_backward", "dgrad_down_swiglu_bwd", "wgrad_down", "dgrad_gate_up", "wgrad_gate_up", "dx_combine"]
+    bstages = {n: round(statistics.median(sev[i][k].elapsed_time(sev[i][k + 1]) for i in range(steps)), 4)
+               for k, n in enumerate(bnames)}
+    # the same step with every BF16 GEMM on each pipeline (the choice is process-wide)
+    by_pipe = {}
+    for pname, which in (("single", nv.NVFP4_PIPELINE_SINGLE), ("pair", nv.NVFP4_PIPELINE_PAIR)):
+        prev = nv.nvfp4_gemm_pipeline(which)
+        try:
+            pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+            tl.forward(x, logits)
+            tl.backward(dout)
+            for i in range(steps):
+                pev[i][0].record(stream)
+                tl.forward(x, logits)
+                pev[i][1].record(stream)
+                tl.backward(dout)
+                pev[i][2].record(stream)
+            torch.cuda.synchronize()
+        finally:
+            nv.nvfp4_gemm_pipeline(prev)
+        by_pipe[pname] = {"forward_ms": round(statistics.median(pev[i][0].elapsed_time(pev[i][1]) for i in range(steps)), 4),
+                          "backward_ms": round(statistics.median(pev[i][1].elapsed_time(pev[i][2]) for i in range(steps)), 4)}
     # the wgrad launches alone: dW_down then dW_13, on the buffers the backward left
     r = tl.route
     wev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -520,7 +543,8 @@ def qat_measure(dev, steps):
                           "tflops": round((fl13 + fld) / ((g13_ms + gd_ms) * 1e-3) / 1e12, 1),
                           "bf16_frac": round((fl13 + fld) / ((g13_ms + gd_ms) * 1e-3) / 1e12 / pk["bf16"], 4)},
             "forward_ms": round(fwd_ms, 4),
-            "train_step": {"forward_ms": round(tfwd, 4), "backward_ms": round(tbwd, 4),
+            "train_step": {"forward_ms": round(tfwd, 4), "backward_ms": round(tbwd, 4), "backward_stages_ms": bstages,
+                           "by_pipeline": by_pipe,
                            "wgrad_down_ms": round(wd_ms, 4), "wgrad_gate_up_ms": round(w13_ms, 4),
                            "wgrad_tflops": round((fld + fl13) / ((wd_ms + w13_ms) * 1e-3) / 1e12, 1),
                            "wgrad_bf16_frac": round((fld + fl13) / ((wd_ms + w13_ms) * 1e-3) / 1e12 / pk["bf16"], 4),
@@ -570,6 +594,16 @@ def mismatch_measure(layer, x, logits, w13, wd):
             ev[1].record()
             torch.cuda.synchronize()
             step_ms[name] = round(ev[0].elapsed_time(ev[1]) / 10, 4)
+            if name == "w4a4_rac_online":  # its stages: the selection passes sit in amax_x and quantize_h
+                sev = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(5)]
+                for i in range(5):
+                    lay.forward(x, logits, mark=lambda k, i=i: sev[i][k].record())
+                torch.cuda.synchronize()
+                names = ["route", "amax_x+select_x", "quantize_x", "clear_padding", "gemm_gate_up",
+                         "select_h+quantize_h", "gemm_down", "combine"]
+                step_ms["online_stages"] = {n: round(statistics.median(sev[i][k].elapsed_time(sev[i][k + 1])
+                                                                      for i in range(5)), 4)
+                                            for k, n in enumerate(names)}
         if drift:
             outs[name + "@eta"] = lay.forward(xe, logits).clone()
         torch.cuda.synchronize()
@@ -584,7 +618,8 @@ def mismatch_measure(layer, x, logits, w13, wd):
     res = {"no_qat": rel("w4a4", "w16a16"), "qat": rel("w4a4", "w4a16"), "qat_rac": rel("w4a4_rac", "w4a16"),
            "qat_rac_fp4": rel("w4a4_rac_fp4", "w4a16"), "qat_rac_online": rel("w4a4_rac_online", "w4a16"),
            "variant_ms_per_step": {"rac_fp4_residual": step_ms["w4a4_rac_fp4"],
-                                   "rac_online_selection": step_ms["w4a4_rac_online"]},
+                                   "rac_online_selection": step_ms["w4a4_rac_online"],
+                                   "rac_online_selection_stages": step_ms["online_stages"]},
            "sym_qat": rel("w4a4", "w4a4_sym"),
            "eta": {"rel": 2.0 ** -10, "bf16": rel("w16a16@eta", "w16a16"), "no_qat": rel("w4a4@eta", "w16a16"),
                    "qat": rel("w4a4@eta", "w4a16"), "qat_rac": rel("w4a4_rac@eta", "w4a16"),
@@ -868,6 +903,23 @@ def run_profile_case(args):
         else:
             fn = lambda: nv.nvfp4_quantize(layer.h, ha.amax, ha.codes, ha.scales, resid=ha.resid, S=layer.Sd,
                                            gs_out=ha.gs)
+        flops = 0
+    elif case in ("gather_w13", "gather_down"):
+        # the online mode's re-gather of the selected weight columns, k = 128, from packed weights of the
+        # prefill shapes: W13 128 x 3072 x 4096 or down 128 x 4096 x 1536
+        E, N, K, k = (128, 3072, 4096, 128) if case == "gather_w13" else (128, 4096, 1536, 128)
+        codes = torch.randint(0, 256, (E, N, K // 2), dtype=torch.uint8, device=dev, generator=g)
+        scales = torch.randint(0x28, 0x40, (E * nv.scale_bytes(N, K),), dtype=torch.uint8, device=dev, generator=g)
+        S = torch.sort(torch.randperm(K, device=dev, generator=g)[:k])[0].to(torch.int32)
+        wsel = torch.empty((E, N, k), dtype=torch.bfloat16, device=dev)
+        fn = lambda: nv.nvfp4_gather_selected_weights(codes, scales, E, N, K, S, wsel)
+        flops = 0
+    elif case == "online_step":
+        # the prefill layer forward with the channel sets chosen online (QUADS §3.3 Eq. 23-24)
+        c, layer, x, logits, w = build_workload(dev)
+        lay = nv.RolloutMoE(w[0], w[1], layer.S13, layer.Sd, layer.topk, c["T"], online=True)
+        del layer
+        fn = lambda: lay.forward(x, logits)
         flops = 0
     elif case == "combine":
         T, topk, H = 16384, 8, 4096

@@ -247,10 +247,10 @@ int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t k, const i
  * (Q_A(X)[i,j] - X[i,j])^2, S = the k largest, ties to the lower index, in
  * increasing order -- over the rows [0, offsets[E]) of a routed activation
  * (all rows_cap rows when offsets is NULL).  The sums are taken in a fixed
- * order built for speed (compensated binary32 per lane, binary64 across
- * lanes and row chunks): deterministic, within a few binary32 ulp of the
- * exact sums, so channels whose scores tie that closely may be chosen either
- * way.
+ * order built for speed (four-row binary32 partials into compensated binary32
+ * sums per lane, binary64 across lanes and row chunks): deterministic, within
+ * a few binary32 ulp of the exact sums, so channels whose scores tie that
+ * closely may be chosen either way.
  *   x          device BF16 [rows_cap, K]
  *   amax       device float: the activation's amax (nvfp4_amax, or a GEMM's amax_out)
  *   S_out      device int32[k]
@@ -268,9 +268,11 @@ int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K,
  *   w_codes, w_scales   from nvfp4_prepare_weights (E experts, N x K)
  *   S                   device int32[k], entries in [0, K) (others are clamped)
  *   w_sel               device BF16 [E, N, k]
- * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, k % 8, E > 65535). */
+ *   dev_status          device int32 or NULL: TIMEOUT if a copy wait ran out
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 128, k % 8,
+ * E > 65535, K > 16384, or K and k too large for one block's shared memory). */
 int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N, int64_t K,
-                                  const int32_t *S, int32_t k, void *w_sel, void *stream);
+                                  const int32_t *S, int32_t k, void *w_sel, int32_t *dev_status, void *stream);
 
 /* ------------------------------------------------------------------------ */
 /* Grouped GEMMs (QUADS §3.3 Eq. 21; §3.2 Eq. 12)                            */

@@ -37,7 +37,7 @@ _SIGS = {
     "nvfp4_rac_select_channels": "pqqpippp",
     "nvfp4_rac_requant_residual": "pqipipppp",
     "nvfp4_rac_select_channels_online": "pqqpipippp",
-    "nvfp4_gather_selected_weights": "ppiqqpipp",
+    "nvfp4_gather_selected_weights": "ppiqqpippp",
     "nvfp4_transpose_bf16": "piqqpp",
     "nvfp4_swiglu": "pqqpp",
     "nvfp4_swiglu_backward": "ppqqpp",
@@ -178,10 +178,10 @@ def nvfp4_rac_select_channels_online(x, amax, k, S_out, score_ws, offsets=None, 
           _p(score_ws), _s(stream))
 
 
-def nvfp4_gather_selected_weights(w_codes, w_scales, E, N, K, S, w_sel, stream=None):
+def nvfp4_gather_selected_weights(w_codes, w_scales, E, N, K, S, w_sel, dev_status=None, stream=None):
     """w_sel [E, N, k] of a weight pack for the channel set S."""
     _call("nvfp4_gather_selected_weights", _p(w_codes), _p(w_scales), E, N, K, _p(S), S.numel(), _p(w_sel),
-          _s(stream))
+          _p(dev_status), _s(stream))
 
 
 def nvfp4_prepare_weights(w, w_codes, w_scales, gs_w, amax_ws, S=None, w_sel=None, interleave=0,

@@ -98,6 +98,18 @@ __device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t &h0, uint32
         : "r"(w));
 }
 
+// One E2M1 code (the low nibble of c) -> its exact value in binary32.
+__device__ __forceinline__ float e2m1_to_f32_hw(uint32_t c) {
+    float lo;
+    asm("{ .reg .b8 b0, b1, b2, b3; .reg .b32 h; .reg .f16 l, u;\n"
+        "mov.b32 {b0, b1, b2, b3}, %1;\n"
+        "cvt.rn.f16x2.e2m1x2 h, b0;\n"
+        "mov.b32 {l, u}, h; cvt.f32.f16 %0, l; }"
+        : "=f"(lo)
+        : "r"(c & 15u));
+    return lo;
+}
+
 // f16x2 -> its two values in binary32 (exact), low half first.
 __device__ __forceinline__ void f16x2_to_f32(uint32_t h, float &lo, float &hi) {
     asm("{ .reg .f16 l, u; mov.b32 {l, u}, %2; cvt.f32.f16 %0, l; cvt.f32.f16 %1, u; }" : "=f"(lo), "=f"(hi) : "r"(h));
@@ -243,7 +255,7 @@ __device__ __forceinline__ uint16_t resid_value(uint16_t xb, uint32_t sb, float 
 // block stored rather than a recomputed one.
 template <int MODE>
 __device__ __forceinline__ uint16_t rac_from_code(uint16_t xb, uint32_t c, float sbf, float gs, float inv_gs) {
-    const float cs = __fmul_rn(e2m1_val(c), sbf);  // exact
+    const float cs = __fmul_rn(e2m1_to_f32_hw(c), sbf);  // exact
     if (MODE == kModeWeight) return __bfloat16_as_ushort(__float2bfloat16_rn(cs));
     const float v = __uint_as_float((uint32_t)xb << 16);
     const float r = __bfloat162float(__float2bfloat16_rn(__fsub_rn(v, __fmul_rn(cs, gs))));
@@ -433,11 +445,34 @@ __global__ void __launch_bounds__(kQThreads, q_blocks_per_sm<MODE>()) quantize_k
             sw = sw | (s1 << 8) | (s2 << 16) | (s3 << 24);
             const bool group_lead = ((lane & 3) == 0) && (b < ((nb + 3) & ~3));
             const int64_t boff = scale_block_offset(b);  // block part of the scale offsets
-            for (int f = 0; f < fanout; ++f) {
-                const int64_t cbase = s_cbase[wid][f];
-                if (cbase < 0) continue;
-                if (valid) *reinterpret_cast<uint2 *>(codes + cbase + b * 8) = make_uint2(q.w0, q.w1);
-                if (group_lead) *reinterpret_cast<uint32_t *>(scales + s_sbase[wid][f] + boff) = sw;
+            if (fanout == 1) {
+                const int64_t cbase = s_cbase[wid][0];
+                if (cbase >= 0) {
+                    if (valid) *reinterpret_cast<uint2 *>(codes + cbase + b * 8) = make_uint2(q.w0, q.w1);
+                    if (group_lead) *reinterpret_cast<uint32_t *>(scales + s_sbase[wid][0] + boff) = sw;
+                }
+            } else if (fanout <= 8) {
+                // up to 8 destinations: every base read first, so one shared-memory
+                // latency covers them all
+                int64_t cb[8], sbb[8];
+#pragma unroll
+                for (int f = 0; f < 8; ++f) {
+                    cb[f] = f < fanout ? s_cbase[wid][f] : -1;
+                    sbb[f] = f < fanout ? s_sbase[wid][f] : 0;
+                }
+#pragma unroll
+                for (int f = 0; f < 8; ++f) {
+                    if (cb[f] < 0) continue;
+                    if (valid) *reinterpret_cast<uint2 *>(codes + cb[f] + b * 8) = make_uint2(q.w0, q.w1);
+                    if (group_lead) *reinterpret_cast<uint32_t *>(scales + sbb[f] + boff) = sw;
+                }
+            } else {
+                for (int f = 0; f < fanout; ++f) {
+                    const int64_t cbase = s_cbase[wid][f];
+                    if (cbase < 0) continue;
+                    if (valid) *reinterpret_cast<uint2 *>(codes + cbase + b * 8) = make_uint2(q.w0, q.w1);
+                    if (group_lead) *reinterpret_cast<uint32_t *>(scales + s_sbase[wid][f] + boff) = sw;
+                }
             }
         }
         __syncwarp();  // every lane is done with the slot (and, at a row's end, the stage is complete)
@@ -625,12 +660,20 @@ __global__ void __launch_bounds__(32 * kScoreWarps) channel_score_kernel(const u
 // of the keys that share the bits found so far; then every channel with a key
 // above T, and the first (k - #above) channels with key T in channel order,
 // are written in channel order.
+constexpr int kTopkPerThread = 16;  // keys per thread: K <= 16 * 1024
 __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, int64_t K, int32_t k, int32_t *S) {
     __shared__ uint32_t hist[256];
     __shared__ int32_t warp_a[32], warp_b[32];
     __shared__ unsigned long long s_prefix;
     __shared__ int32_t s_need, carry_eq, carry_out;
     const unsigned long long *key = reinterpret_cast<const unsigned long long *>(ssq);
+    // the keys stay in registers for all passes: key j = threadIdx.x + i * blockDim.x
+    unsigned long long kv[kTopkPerThread];
+#pragma unroll
+    for (int i = 0; i < kTopkPerThread; ++i) {
+        const int64_t j = threadIdx.x + (int64_t)i * blockDim.x;
+        kv[i] = j < K ? key[j] : 0ull;
+    }
     if (threadIdx.x == 0) {
         s_prefix = 0ull;
         s_need = k;  // rank of T among the keys that share the prefix, counted from the top
@@ -644,9 +687,12 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, in
         const unsigned long long hi = shift == 56 ? 0ull : (~0ull << (shift + 8));
         const unsigned long long prefix = s_prefix;
         // warp-aggregated counts: the keys of a warp that fall in one bucket add once
-        for (int64_t j0 = 0; j0 < K; j0 += blockDim.x) {
+#pragma unroll
+        for (int i = 0; i < kTopkPerThread; ++i) {
+            const int64_t j0 = (int64_t)i * blockDim.x;
+            if (j0 >= K) break;  // the same in every thread
             const int64_t j = j0 + threadIdx.x;
-            const unsigned long long v = j < K ? key[j] : 0ull;
+            const unsigned long long v = kv[i];
             const bool act = j < K && (v & hi) == prefix;
             const uint32_t bucket = act ? (uint32_t)((v >> shift) & 255u) : 256u + (uint32_t)lane;
             const unsigned peers = __match_any_sync(0xffffffffu, bucket);
@@ -685,9 +731,12 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, in
     }
     const unsigned long long T = s_prefix;
     const int32_t need_eq = s_need;  // keys equal to T to keep, lowest channels first
-    for (int64_t j0 = 0; j0 < K; j0 += blockDim.x) {
+#pragma unroll
+    for (int i = 0; i < kTopkPerThread; ++i) {
+        const int64_t j0 = (int64_t)i * blockDim.x;
+        if (j0 >= K) break;  // the same in every thread
         const int64_t j = j0 + threadIdx.x;
-        const unsigned long long v = j < K ? key[j] : 0ull;
+        const unsigned long long v = kv[i];
         const int eq = j < K && v == T;
         // rank of this channel among the equal keys, in channel order
         const unsigned be = __ballot_sync(0xffffffffu, eq);
@@ -786,12 +835,12 @@ __global__ void __launch_bounds__(256) resid_qdq_kernel(uint16_t *resid, int64_t
 // block per lane as the quantizer sees it, 8 warps striding over the chunk's
 // rows.  The squared error of an element, (code*sb*gs - x)^2, is exact in
 // binary32 (both terms have few significant bits and lie within a factor of a
-// block scale of each other); a lane keeps compensated binary32 sums of its 16
-// channels, the warps' sums are added in binary64 in warp order, and the
+// block scale of each other); a lane adds four rows' squared errors of each of
+// its 16 channels in binary32 and the four-row partials into compensated
+// binary32 sums, the warps' sums are added in binary64 in warp order, and the
 // chunks' in chunk order -- deterministic, within a few ulp of binary32 of the
-// exact sums.
+// exact sums (all terms are nonnegative).
 constexpr int kOnlineChunks = 256;  // at most; about 512 rows of the buffer per chunk
-static_assert(kOnlineChunks % 16 == 0, "the finishing sum loads 16 chunks at a time");
 static int64_t online_chunks(int64_t rows_cap) {
     int64_t c = (rows_cap / 512 + 15) / 16 * 16;
     return c < 16 ? 16 : (c > kOnlineChunks ? kOnlineChunks : c);
@@ -831,6 +880,11 @@ __global__ void __launch_bounds__(256) online_score_kernel(const uint16_t *x, in
                     raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);  // adds exact zeros
                 }
             }
+            // the four rows' squared errors in binary32 (a sum of four nonnegative terms, within
+            // 3 ulp), then that partial into the compensated sum
+            float pz[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) pz[t] = 0.0f;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 float v[16];
@@ -842,11 +896,15 @@ __global__ void __launch_bounds__(256) online_score_kernel(const uint16_t *x, in
 #pragma unroll
                 for (int t = 0; t < 16; ++t) {
                     const float d = __fsub_rn(dq[t], v[t]);
-                    const float y = __fsub_rn(__fmul_rn(d, d), comp[t]);
-                    const float s2 = __fadd_rn(sum[t], y);
-                    comp[t] = __fsub_rn(__fsub_rn(s2, sum[t]), y);
-                    sum[t] = s2;
+                    pz[t] = __fmaf_rn(d, d, pz[t]);
                 }
+            }
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const float y = __fsub_rn(pz[t], comp[t]);
+                const float s2 = __fadd_rn(sum[t], y);
+                comp[t] = __fsub_rn(__fsub_rn(s2, sum[t]), y);
+                sum[t] = s2;
             }
         }
     }
@@ -862,70 +920,149 @@ __global__ void __launch_bounds__(256) online_score_kernel(const uint16_t *x, in
     }
 }
 
-__global__ void online_score_finish_kernel(const double *part, int64_t K, int nchunks, double *ssq) {
-    const int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (j >= K) return;
+// ssq[j] = the sum over chunks of part[c, j]: a block per 32 channels, warp w
+// adding chunks w, w + 8, ... in order (eight loads in flight), then the
+// warps' sums in warp order.
+__global__ void __launch_bounds__(256) online_score_finish_kernel(const double *part, int64_t K, int nchunks,
+                                                                  double *ssq) {
+    __shared__ double red[8][32];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t j = (int64_t)blockIdx.x * 32 + lane;
     double acc = 0.0;
-    for (int c0 = 0; c0 < nchunks; c0 += 16) {  // nchunks % 16 == 0  // 16 loads in flight, added in chunk order
-        double v[16];
+    if (j < K) {
+        for (int c0 = w; c0 < nchunks; c0 += 64) {
+            double v[8];
 #pragma unroll
-        for (int u = 0; u < 16; ++u) v[u] = __ldg(part + (int64_t)(c0 + u) * K + j);
+            for (int u = 0; u < 8; ++u) v[u] = c0 + 8 * u < nchunks ? __ldg(part + (int64_t)(c0 + 8 * u) * K + j) : 0.0;
 #pragma unroll
-        for (int u = 0; u < 16; ++u) acc = __dadd_rn(acc, v[u]);
+            for (int u = 0; u < 8; ++u) acc = __dadd_rn(acc, v[u]);
+        }
     }
-    ssq[j] = acc;
+    red[w][lane] = acc;
+    __syncthreads();
+    if (w == 0 && j < K) {
+        double sum = 0.0;
+        for (int i = 0; i < 8; ++i) sum = __dadd_rn(sum, red[i][lane]);
+        ssq[j] = sum;
+    }
 }
 
 // W_sel[e, n, s] = bf16(code * sb) of packed weight element (n, S[s]) of
 // expert e -- the unscaled dequantized value nvfp4_prepare_weights stores for
-// the channels S -- gathered for a new S.  A block covers 32 rows of one
-// expert (blockIdx.y), a warp 4 of them; lane l emits channels 4l + 128u ..
-// 4l + 128u + 3 of each row.  The code and scale bytes are loaded straight
-// from global memory, so only the sectors that hold selected channels are
-// read, and the 4 rows' loads are all issued before the first is used.
+// the channels S -- gathered for a new S.  A block covers one 128-row tile of
+// one expert (blockIdx.x, blockIdx.y); its block scales (the tile's 512-byte
+// scale groups) and its rows' packed codes arrive by bulk copies -- the scale
+// groups once, each 16 bytes further along the banks than the last, the rows
+// through a ring of kGatherSlots row slots per warp.  A warp takes 16 rows; a
+// lane emits channels 4l + 128u .. 4l + 128u + 3 of each.  A row's scale
+// words (4 blocks each) are all in one bank of a scale group, so lane g reads
+// word g of the row once (the skew spreads the groups over 8 banks) and the
+// lanes that need a block take its word by shuffle.
 constexpr int kGatherWarps = 8;
-constexpr int kGatherRows = 4;  // rows per warp
+constexpr int kGatherSlots = 4;                     // rows in flight per warp
+constexpr int kGatherRowsPerWarp = 128 / kGatherWarps;
+constexpr int kGatherGroupPitch = 512 + 16;         // a scale group's place in shared memory
+constexpr uint64_t kGatherWaitNs = 2000000000ull;  // 2 s per wait
+
+__host__ __device__ constexpr int64_t gather_groups(int64_t K) { return ((K / 16 + 15) / 16) * 4; }
+__host__ __device__ constexpr int64_t gather_smem_bytes(int64_t K, int32_t k) {
+    return gather_groups(K) * kGatherGroupPitch + (int64_t)kGatherWarps * kGatherSlots * (K / 2) +
+           (((int64_t)k * 4 + 15) / 16) * 16;
+}
 
 __global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_kernel(const uint8_t *codes, const uint8_t *scales,
                                                                       int64_t N, int64_t K, const int32_t *S,
-                                                                      int32_t k, uint16_t *wsel) {
+                                                                      int32_t k, uint16_t *wsel, int32_t *dev_status) {
+    extern __shared__ __align__(128) uint8_t gsm[];
+    __shared__ uint64_t s_bar[1 + kGatherWarps * kGatherSlots];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t e = blockIdx.y;
-    const int64_t n0 = ((int64_t)blockIdx.x * kGatherWarps + w) * kGatherRows;  // N % 128 == 0: all rows exist
-    const int64_t nb = K >> 4, kslices = (nb + 15) >> 4;
-    const uint8_t *sten = scales + e * (N >> 7) * kslices * 2048;  // the expert's scales
-    const uint8_t *cten = codes + e * N * (K >> 1);
-    for (int s0 = 4 * lane; s0 < k; s0 += 128) {  // k % 8 == 0: channels s0 .. s0 + 3 all exist
-        int32_t co[4];
-        uint32_t sh[4];
-        int64_t so[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int32_t j = min(max(__ldg(S + s0 + t), 0), (int32_t)(K - 1));
-            co[t] = j >> 1;
-            sh[t] = 4u * (uint32_t)(j & 1);
-            so[t] = scale_block_offset(j >> 4) + ((j >> 4) & 3);
+    const int64_t e = blockIdx.y, tile = blockIdx.x;
+    const int ngroups = (int)gather_groups(K);  // 512-byte scale groups of the tile: 4 per 256-element K-slice
+    const uint32_t rowb = (uint32_t)(K / 2);
+    uint8_t *s_sc = gsm;                                                 // the scale groups, skewed
+    uint8_t *ring = gsm + (size_t)ngroups * kGatherGroupPitch + (size_t)w * kGatherSlots * rowb;
+    int32_t *s_S = reinterpret_cast<int32_t *>(gsm + (size_t)ngroups * kGatherGroupPitch +
+                                               (size_t)kGatherWarps * kGatherSlots * rowb);
+    uint64_t *bars = s_bar + 1 + w * kGatherSlots;
+    for (int i = threadIdx.x; i < k; i += blockDim.x) s_S[i] = min(max(S[i], 0), (int32_t)(K - 1));
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 1 + kGatherWarps * kGatherSlots; ++i) mbar_init(&s_bar[i], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();  // S and the barriers are ready
+    const int64_t n0 = tile * 128 + (int64_t)w * kGatherRowsPerWarp;  // this warp's first row
+    const uint8_t *crow = codes + (e * N + n0) * rowb;
+    if (threadIdx.x == 0) {
+        const uint8_t *src = scales + (e * (N / 128) + tile) * (int64_t)ngroups * 512;
+        mbar_arrive_expect_tx(&s_bar[0], (uint32_t)ngroups * 512u);
+        for (int g = 0; g < ngroups; ++g) bulk_load(s_sc + g * kGatherGroupPitch, src + g * 512, 512u, &s_bar[0]);
+    }
+    if (lane == 0)
+        for (int i = 0; i < kGatherSlots; ++i) {
+            mbar_arrive_expect_tx(&bars[i], rowb);
+            bulk_load(ring + (size_t)i * rowb, crow + (size_t)i * rowb, rowb, &bars[i]);
         }
-        uint32_t cv[kGatherRows][4], sv[kGatherRows][4];
+    // channels 4 lane .. 4 lane + 3 (k <= 128 in one pass; more come from shared memory per row)
+    int cb[4], csh[4], wl[4], wb[4];
 #pragma unroll
-        for (int r = 0; r < kGatherRows; ++r) {
-            const uint8_t *crow = cten + (n0 + r) * (K >> 1);
-            const uint8_t *srow = sten + scale_row_offset(n0 + r, kslices);
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                cv[r][t] = __ldg(crow + co[t]);
-                sv[r][t] = __ldg(srow + so[t]);
-            }
+    for (int t = 0; t < 4; ++t) {
+        const int j = 4 * lane + t < k ? s_S[4 * lane + t] : 0;
+        cb[t] = j >> 1;             // the code byte
+        csh[t] = 4 * (j & 1);       // its nibble
+        wl[t] = j >> 6;             // the lane holding its block's scale word
+        wb[t] = 8 * ((j >> 4) & 3); // the scale byte in that word
+    }
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&s_bar[0], 0u, kGatherWaitNs));
+    int i = 0;
+    for (; ok && i < kGatherRowsPerWarp; ++i) {
+        const int slot = i % kGatherSlots;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&bars[slot], (uint32_t)(i / kGatherSlots) & 1u, kGatherWaitNs))) {
+            ok = false;
+            break;
         }
-#pragma unroll
-        for (int r = 0; r < kGatherRows; ++r) {
+        const uint8_t *rc = ring + (size_t)slot * rowb;
+        const int64_t n = n0 + i;
+        const int srow = (int)((n & 31) * 16 + ((n & 127) >> 5) * 4);  // the row's word in each scale group
+        uint16_t *out = wsel + (e * N + n) * k;
+        for (int s0 = 0; s0 < k; s0 += 128) {
+            uint32_t sw = 0u;  // lane g: the row's scale word of group g, then of group 32 + g, ...
             uint32_t h[4];
+            for (int g0 = 0; g0 < ngroups; g0 += 32) {
+                if (g0 + lane < ngroups)
+                    sw = *reinterpret_cast<const uint32_t *>(s_sc + (g0 + lane) * kGatherGroupPitch + srow);
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
-                h[t] = __bfloat16_as_ushort(
-                    __float2bfloat16_rn(__fmul_rn(e2m1_val((cv[r][t] >> sh[t]) & 15u), e4m3_to_f32(sv[r][t]))));
-            *reinterpret_cast<uint2 *>(wsel + (e * N + n0 + r) * k + s0) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+                for (int t = 0; t < 4; ++t) {
+                    int j = 0, cbt = cb[t], csht = csh[t], wlt = wl[t], wbt = wb[t];
+                    if (s0 > 0) {  // channels past the first 128: from shared memory
+                        j = s0 + 4 * lane + t < k ? s_S[s0 + 4 * lane + t] : 0;
+                        cbt = j >> 1;
+                        csht = 4 * (j & 1);
+                        wlt = j >> 6;
+                        wbt = 8 * ((j >> 4) & 3);
+                    }
+                    const uint32_t word = __shfl_sync(0xffffffffu, sw, wlt & 31);
+                    if ((wlt >> 5) == (g0 >> 5)) {
+                        const uint32_t c = (rc[cbt] >> csht) & 15u;
+                        const uint32_t sb = (word >> wbt) & 0xffu;
+                        h[t] = __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(e2m1_to_f32_hw(c), e4m3_to_f32(sb))));
+                    }
+                }
+            }
+            if (s0 + 4 * lane < k)
+                *reinterpret_cast<uint2 *>(out + s0 + 4 * lane) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
         }
+        __syncwarp();  // every lane is done with the slot
+        if (lane == 0 && i + kGatherSlots < kGatherRowsPerWarp) {
+            mbar_arrive_expect_tx(&bars[slot], rowb);
+            bulk_load(ring + (size_t)slot * rowb, crow + (size_t)(i + kGatherSlots) * rowb, rowb, &bars[slot]);
+        }
+    }
+    if (!ok && lane == 0) {
+        // a copy never arrived: report it, and let every copy still in flight land before the block exits
+        report(dev_status, NVFP4_ERR_TIMEOUT);
+        for (int ii = i; ii < kGatherRowsPerWarp && ii < i + kGatherSlots; ++ii)
+            (void)mbar_wait_bounded(&bars[ii % kGatherSlots], (uint32_t)(ii / kGatherSlots) & 1u, kGatherWaitNs);
+        if (w == 0) (void)mbar_wait_bounded(&s_bar[0], 0u, kGatherWaitNs);
     }
 }
 
@@ -1402,7 +1539,7 @@ extern "C" int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap,
         (const uint16_t *)x, rows_cap, K, offsets, E, amax, part);
     int s = launch_status("online_score_kernel");
     if (s != NVFP4_OK) return s;
-    online_score_finish_kernel<<<(unsigned)((K + 63) / 64), 64, 0, st>>>(part, K, nchunks, score_ws);
+    online_score_finish_kernel<<<(unsigned)((K + 31) / 32), 256, 0, st>>>(part, K, nchunks, score_ws);
     s = launch_status("online_score_finish_kernel");
     if (s != NVFP4_OK || k == 0) return s;
     select_topk_kernel<<<1, 1024, 0, st>>>(score_ws, K, k, S_out);
@@ -1410,15 +1547,26 @@ extern "C" int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap,
 }
 
 extern "C" int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N,
-                                             int64_t K, const int32_t *S, int32_t k, void *w_sel, void *stream) {
+                                             int64_t K, const int32_t *S, int32_t k, void *w_sel,
+                                             int32_t *dev_status, void *stream) {
     if (!w_codes || !w_scales || !S || !w_sel || E < 1 || N < 0 || K < 0 || k < 1 || k > K)
         return NVFP4_ERR_INVALID_ARG;
-    if (K % 64 || N % 128 || k % 8 || E > 65535 || N / 32 > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED;
+    if (K % 64 || N % 128 || k % 8 || E > 65535 || K > 16384 || N / 128 > 0x7fffffff) return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(w_sel) || !aligned16(w_codes) || !aligned16(w_scales)) return NVFP4_ERR_ALIGNMENT;
     if (N == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
-    gather_wsel_kernel<<<dim3((unsigned)(N / (kGatherWarps * kGatherRows)), (unsigned)E), 32 * kGatherWarps, 0,
-                         (cudaStream_t)stream>>>(w_codes, w_scales, N, K, S, k, (uint16_t *)w_sel);
+    const int64_t smem = gather_smem_bytes(K, k);
+    if (smem > 227 * 1024) return NVFP4_ERR_UNSUPPORTED;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(gather_wsel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)smem);
+        if (e != cudaSuccess) {
+            set_last_error("cudaFuncSetAttribute(gather_wsel_kernel)", e);
+            return NVFP4_ERR_CUDA;
+        }
+    }
+    gather_wsel_kernel<<<dim3((unsigned)(N / 128), (unsigned)E), 32 * kGatherWarps, (size_t)smem,
+                         (cudaStream_t)stream>>>(w_codes, w_scales, N, K, S, k, (uint16_t *)w_sel, dev_status);
     return launch_status("gather_wsel_kernel");
 }
 

@@ -146,7 +146,8 @@ class RolloutMoE:
         if self.online and self.k13:  # Eq. 23-24 on this batch, and the weight columns it picks
             nvfp4_rac_select_channels_online(x, xa.amax, self.k13, self.S13, self.score_ws, stream=stream)
             W = self.w13
-            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.S13, W.sel, stream=stream)
+            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.S13, W.sel,
+                                          dev_status=self.dev_status, stream=stream)
         mark(2)
         nvfp4_quantize(x, xa.amax, xa.codes, xa.scales, resid=xa.resid if self.k13 else None,
                        S=self.S13 if self.k13 else None, gs_out=xa.gs, dst_row=dst,
@@ -169,7 +170,8 @@ class RolloutMoE:
             nvfp4_rac_select_channels_online(self.h, ha.amax, self.kd, self.Sd, self.score_ws, offsets=r.offsets,
                                              E=self.E, stream=stream)
             W = self.wd
-            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.Sd, W.sel, stream=stream)
+            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.Sd, W.sel,
+                                          dev_status=self.dev_status, stream=stream)
         nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
                        S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
                        stream=stream)
@@ -302,35 +304,46 @@ class QatMoE:
         self._T = T
         return out
 
-    def backward(self, dout, stream=None):
+    def backward(self, dout, stream=None, mark=None):
         """Gradients of the last forward (train=True) for the output gradient
         dout [T, H] FP32, by the straight-through estimator of QUADS §3.2 Eq. 13
         (the weight fake-quantizer is the identity in the backward):
         returns (dx [T, H] FP32, dW13 [E, 2I, H] FP32, dW_down [E, H, I] FP32,
         d_weights [T, topk] FP32, the combine weights' gradient) -- views of
-        reused buffers."""
+        reused buffers.  `mark(i)`, if given, is called before stage i = 0..5
+        (combine backward, down input gradient with the SwiGLU backward, down
+        weight gradient, gate_up input gradient, gate_up weight gradient, dx)
+        and with i = 6 at the end."""
+        mark = mark or (lambda i: None)
         assert self.train, "QatMoE(train=True) keeps what the backward needs"
         T, E, H, I, R = self._T, self.E, self.H, self.I, self.rows_cap
         assert dout.shape == (T, H) and dout.dtype == torch.float32
         r = self.route
         dst, w = r.dst_row[:T], r.weights[:T]
         # routed output gradient, and the combine weights' gradient
+        mark(0)
         nvfp4_moe_combine_backward(dout, self.y, dst, w, r.counts, r.offsets, E, self.dy,
                                    dweights=self.dweights[:T], stream=stream)
+        mark(1)
         # down projection: dh = dY W_hat_d (W_hat_d read as stored, [H, I] per expert) and, in the
         # same GEMM's epilogue, the SwiGLU backward d(gate|up) from dh and the saved pre-activations;
         # dW_d = dY^T h (the routed rows read as stored)
         nvfp4_bf16_grouped_gemm_dgrad(self.dy, self.wd_hat, r.offsets, E, I, H, self.dgu, out_dtype=NVFP4_OUT_BF16,
                                       epilogue=NVFP4_EPI_SWIGLU_BWD, gu=self.gu, dev_status=self.dev_status,
                                       stream=stream)
+        mark(2)
         nvfp4_bf16_grouped_gemm_wgrad_rows(self.dy, self.h, r.offsets, E, self.dwd, dev_status=self.dev_status,
                                            stream=stream)
+        mark(3)
         # gate_up projection: dx_routed = d(gate|up) W_hat_13, dW_13 = d(gate|up)^T x_routed
         nvfp4_bf16_grouped_gemm_dgrad(self.dgu, self.w13_hat, r.offsets, E, H, 2 * I, self.dxr,
                                       out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
+        mark(4)
         nvfp4_bf16_grouped_gemm_wgrad_rows(self.dgu, self.xr, r.offsets, E, self.dw13, dev_status=self.dev_status,
                                            stream=stream)
+        mark(5)
         # dx: each token's routed-row gradients summed
         dx = self.dx[:T]
         nvfp4_moe_combine(self.dxr, dst, self.ones[:T], self.topk, dx, stream=stream)
+        mark(6)
         return dx, self.dw13, self.dwd, self.dweights[:T]

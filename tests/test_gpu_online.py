@@ -58,9 +58,8 @@ def test_online_selection_reads_routed_rows_only(nv):
     assert _chains.valid_topk(S, ref, k)
 
 
-@pytest.mark.parametrize("interleave", [0, 1])
-def test_gather_equals_the_weight_pack(nv, interleave):
-    E, N, K, k = 3, 512, 768, 48
+@pytest.mark.parametrize("interleave,E,N,K,k", [(0, 3, 512, 768, 48), (1, 3, 512, 768, 48), (0, 2, 384, 960, 160)])
+def test_gather_equals_the_weight_pack(nv, interleave, E, N, K, k):
     g = torch.Generator().manual_seed(21)
     w = (torch.randn((E, N, K), generator=g) * 0.02).to(torch.bfloat16)
     wd = w.to(G.DEV)
@@ -70,7 +69,7 @@ def test_gather_equals_the_weight_pack(nv, interleave):
 
     def pack(S):
         codes = G.zeros((E, N, K // 2), torch.uint8)
-        scales = G.zeros(E * N * K // 16, torch.uint8)
+        scales = G.zeros(E * nv.scale_bytes(N, K), torch.uint8)
         sel = G.zeros((E, N, k), torch.bfloat16)
         nv.nvfp4_prepare_weights(wd, codes, scales, G.zeros(E, torch.float32), G.zeros(E, torch.float32),
                                  S=torch.tensor(S, device=G.DEV), w_sel=sel, interleave=interleave)
@@ -79,8 +78,10 @@ def test_gather_equals_the_weight_pack(nv, interleave):
     codes, scales, _ = pack(Sa)
     _, _, want = pack(Sb)
     got = G.zeros((E, N, k), torch.bfloat16)
-    nv.nvfp4_gather_selected_weights(codes, scales, E, N, K, torch.tensor(Sb, device=G.DEV), got)
+    st = G.zeros(1, torch.int32)
+    nv.nvfp4_gather_selected_weights(codes, scales, E, N, K, torch.tensor(Sb, device=G.DEV), got, dev_status=st)
     torch.cuda.synchronize()
+    G.status_ok(st)
     assert torch.equal(got, want)
     if not interleave:  # rows in source order: the oracle's unscaled dequantized weights on Sb
         for e in range(E):
