@@ -129,7 +129,7 @@ int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensor
  * nvfp4_moe_clear_padding).  dev_status gets NONFINITE if amax is not finite.
  * Errors: INVALID_ARG (null pointers, negative sizes, fanout < 1),
  * ALIGNMENT (pointers; ldx % 8), UNSUPPORTED (K % 32, K > 16384, k % 8,
- * fanout > 32). */
+ * fanout > 32, M or rows_out above 2^31 - 1). */
 int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float *amax,
                    float *gs_out, const int32_t *S, int32_t k, const int32_t *dst_row,
                    int32_t fanout, int64_t rows_out, uint8_t *codes, uint8_t *scales,

@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(kQThreads, q_blocks_per_sm<MODE>()) quantize_k
     __shared__ __align__(16) uint8_t s_row[kQWarps][kQRowBuf];
     __shared__ int64_t s_cbase[kQWarps][32];  // destination f: byte offset of its code row (-1: skipped)
     __shared__ int64_t s_sbase[kQWarps][32];  // destination f: row part of its scale offsets
+    __shared__ int32_t s_dm[kQWarps][32];     // destination f: its row
     __shared__ int32_t s_S[kMaxStagedK];
     // per 512-element segment: the position in S of its first selected channel
     __shared__ int32_t s_segfirst[kMaxBlocksPerRow / 32 + 1];
@@ -377,6 +378,7 @@ __global__ void __launch_bounds__(kQThreads, q_blocks_per_sm<MODE>()) quantize_k
                 const bool okd = dm >= 0 && dm < ((MODE == kModeAct) ? a.rows_out : a.M);  // others are skipped
                 s_cbase[wid][lane] = okd ? dm * (a.K >> 1) : -1;
                 s_sbase[wid][lane] = okd ? scale_row_offset(dm, kslices) : 0;
+                s_dm[wid][lane] = okd ? (int32_t)dm : 0;
             }
             __syncwarp();
         }
@@ -486,9 +488,8 @@ __global__ void __launch_bounds__(kQThreads, q_blocks_per_sm<MODE>()) quantize_k
                     const int jc = __ldg(a.S + si);
                     const uint16_t val = resid_value<MODE>(__ldg(xrow + jc), row_sb[jc >> 4], gs, inv_gs, s_tab);
                     for (int f = 0; f < fanout; ++f) {
-                        const int64_t cbase = s_cbase[wid][f];
-                        if (cbase < 0) continue;
-                        const int64_t dm = cbase / (a.K >> 1);
+                        if (s_cbase[wid][f] < 0) continue;
+                        const int64_t dm = s_dm[wid][f];
                         if (MODE == kModeWeight) a.wsel[(int64_t)tensor * a.wsel_tstride + dm * a.k + si] = val;
                         else a.resid[dm * a.k + si] = val;
                     }
@@ -497,9 +498,8 @@ __global__ void __launch_bounds__(kQThreads, q_blocks_per_sm<MODE>()) quantize_k
                 const int chunks = a.k >> 3;  // 16-byte chunks (k % 8 == 0)
                 const uint4 *src = reinterpret_cast<const uint4 *>(stage);
                 for (int f = 0; f < fanout; ++f) {
-                    const int64_t cbase = s_cbase[wid][f];
-                    if (cbase < 0) continue;
-                    const int64_t dm = cbase / (a.K >> 1);
+                    if (s_cbase[wid][f] < 0) continue;
+                    const int64_t dm = s_dm[wid][f];
                     uint16_t *row = (MODE == kModeWeight) ? a.wsel + (int64_t)tensor * a.wsel_tstride + dm * a.k
                                                           : a.resid + dm * a.k;
                     for (int c = lane; c < chunks; c += 32) reinterpret_cast<uint4 *>(row)[c] = src[c];
@@ -984,24 +984,26 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_kernel(const ui
     int32_t *s_S = reinterpret_cast<int32_t *>(gsm + (size_t)ngroups * kGatherGroupPitch +
                                                (size_t)kGatherWarps * kGatherSlots * rowb);
     uint64_t *bars = s_bar + 1 + w * kGatherSlots;
-    for (int i = threadIdx.x; i < k; i += blockDim.x) s_S[i] = min(max(S[i], 0), (int32_t)(K - 1));
     if (threadIdx.x == 0) {
         for (int i = 0; i < 1 + kGatherWarps * kGatherSlots; ++i) mbar_init(&s_bar[i], 1);
         fence_barrier_init();
     }
-    __syncthreads();  // S and the barriers are ready
+    __syncthreads();  // the barriers are ready
     const int64_t n0 = tile * 128 + (int64_t)w * kGatherRowsPerWarp;  // this warp's first row
     const uint8_t *crow = codes + (e * N + n0) * rowb;
-    if (threadIdx.x == 0) {
+    if (w == 0) {  // the scale groups, issued by the 32 lanes of warp 0
         const uint8_t *src = scales + (e * (N / 128) + tile) * (int64_t)ngroups * 512;
-        mbar_arrive_expect_tx(&s_bar[0], (uint32_t)ngroups * 512u);
-        for (int g = 0; g < ngroups; ++g) bulk_load(s_sc + g * kGatherGroupPitch, src + g * 512, 512u, &s_bar[0]);
+        if (lane == 0) mbar_arrive_expect_tx(&s_bar[0], (uint32_t)ngroups * 512u);
+        __syncwarp();
+        for (int g = lane; g < ngroups; g += 32) bulk_load(s_sc + g * kGatherGroupPitch, src + g * 512, 512u, &s_bar[0]);
     }
     if (lane == 0)
         for (int i = 0; i < kGatherSlots; ++i) {
             mbar_arrive_expect_tx(&bars[i], rowb);
             bulk_load(ring + (size_t)i * rowb, crow + (size_t)i * rowb, rowb, &bars[i]);
         }
+    for (int i = threadIdx.x; i < k; i += blockDim.x) s_S[i] = min(max(S[i], 0), (int32_t)(K - 1));
+    __syncthreads();  // S is ready
     // channels 4 lane .. 4 lane + 3 (k <= 128 in one pass; more come from shared memory per row)
     int cb[4], csh[4], wl[4], wb[4];
 #pragma unroll
@@ -1063,6 +1065,57 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_kernel(const ui
         for (int ii = i; ii < kGatherRowsPerWarp && ii < i + kGatherSlots; ++ii)
             (void)mbar_wait_bounded(&bars[ii % kGatherSlots], (uint32_t)(ii / kGatherSlots) & 1u, kGatherWaitNs);
         if (w == 0) (void)mbar_wait_bounded(&s_bar[0], 0u, kGatherWaitNs);
+    }
+}
+
+// The same gather reading the code and scale bytes straight from global
+// memory (only the sectors that hold selected channels are read): a block
+// covers 32 rows of one expert (blockIdx.y), a warp 4 of them, the 4 rows'
+// loads all issued before the first is used.  For rows of 4096 channels and
+// more this beats the staged kernel (whose 128-row blocks wait for 32 KB of
+// scales before the first row); for shorter rows the staged one wins.
+constexpr int kGatherDirectRows = 4;  // rows per warp
+__global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_direct_kernel(const uint8_t *codes,
+                                                                             const uint8_t *scales, int64_t N,
+                                                                             int64_t K, const int32_t *S, int32_t k,
+                                                                             uint16_t *wsel) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t e = blockIdx.y;
+    const int64_t n0 = ((int64_t)blockIdx.x * kGatherWarps + w) * kGatherDirectRows;  // N % 128 == 0: all rows exist
+    const int64_t nb = K >> 4, kslices = (nb + 15) >> 4;
+    const uint8_t *sten = scales + e * (N >> 7) * kslices * 2048;  // the expert's scales
+    const uint8_t *cten = codes + e * N * (K >> 1);
+    for (int s0 = 4 * lane; s0 < k; s0 += 128) {  // k % 8 == 0: channels s0 .. s0 + 3 all exist
+        int32_t co[4];
+        uint32_t sh[4];
+        int64_t so[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int32_t j = min(max(__ldg(S + s0 + t), 0), (int32_t)(K - 1));
+            co[t] = j >> 1;
+            sh[t] = 4u * (uint32_t)(j & 1);
+            so[t] = scale_block_offset(j >> 4) + ((j >> 4) & 3);
+        }
+        uint32_t cv[kGatherDirectRows][4], sv[kGatherDirectRows][4];
+#pragma unroll
+        for (int r = 0; r < kGatherDirectRows; ++r) {
+            const uint8_t *crow = cten + (n0 + r) * (K >> 1);
+            const uint8_t *srow = sten + scale_row_offset(n0 + r, kslices);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                cv[r][t] = __ldg(crow + co[t]);
+                sv[r][t] = __ldg(srow + so[t]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kGatherDirectRows; ++r) {
+            uint32_t h[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                h[t] = __bfloat16_as_ushort(
+                    __float2bfloat16_rn(__fmul_rn(e2m1_to_f32_hw((cv[r][t] >> sh[t]) & 15u), e4m3_to_f32(sv[r][t]))));
+            *reinterpret_cast<uint2 *>(wsel + (e * N + n0 + r) * k + s0) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        }
     }
 }
 
@@ -1225,7 +1278,7 @@ __global__ void __launch_bounds__(256, 4) fake_quant_fused_kernel(FQArgs a) {
     int64_t item = s_next[0];
     for (int iter = 0; item < total; ++iter) {
         // group gi: 0 -> A(0); 2nt-1 -> B(nt-1); odd -> A((gi+1)/2); even -> B(gi/2 - 1)
-        const int64_t gi = item / a.per;
+        const int64_t gi = (int64_t)((uint32_t)item / (uint32_t)a.per);  // items fit in 32 bits
         const int chunk = (int)(item - gi * a.per);
         const bool is_a = gi == 0 || (gi != 2ll * a.nt - 1 && (gi & 1));
         const int t = gi == 0 ? 0 : (gi == 2ll * a.nt - 1 ? a.nt - 1 : (int)((gi & 1) ? (gi + 1) / 2 : gi / 2 - 1));
@@ -1384,7 +1437,8 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
     if (k > 0 && (!S || !resid)) return NVFP4_ERR_INVALID_ARG;
     if (!dst_row && (fanout != 1 || rows_out < M)) return NVFP4_ERR_INVALID_ARG;
     // a row's destinations are resolved into 32 per-warp slots
-    if (K % 32 || k % 8 || K / 16 > kMaxBlocksPerRow || fanout > 32) return NVFP4_ERR_UNSUPPORTED;
+    if (K % 32 || k % 8 || K / 16 > kMaxBlocksPerRow || fanout > 32 || M > INT32_MAX || rows_out > INT32_MAX)
+        return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(x) || ldx % 8 || !aligned16(codes) || !aligned16(scales) || (resid && !aligned16(resid)))
         return NVFP4_ERR_ALIGNMENT;
     if (M == 0) return NVFP4_OK;
@@ -1464,7 +1518,7 @@ extern "C" int nvfp4_prepare_weights(const void *w, int32_t E, int64_t N, int64_
     if (!w || !w_codes || !w_scales || !gs_w || !amax_ws || E < 1 || N < 0 || K < 0 || k < 0 || k > K)
         return NVFP4_ERR_INVALID_ARG;
     if (k > 0 && (!S || !w_sel)) return NVFP4_ERR_INVALID_ARG;
-    if (K % 64 || N % 128 || (interleave && N % 256) || k % 8 || K / 16 > kMaxBlocksPerRow || E > 65535)
+    if (K % 64 || N % 128 || (interleave && N % 256) || k % 8 || K / 16 > kMaxBlocksPerRow || E > 65535 || N > INT32_MAX)
         return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(w) || !aligned16(w_codes) || !aligned16(w_scales) || (w_sel && !aligned16(w_sel)))
         return NVFP4_ERR_ALIGNMENT;
@@ -1555,6 +1609,12 @@ extern "C" int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8
     if (!aligned16(w_sel) || !aligned16(w_codes) || !aligned16(w_scales)) return NVFP4_ERR_ALIGNMENT;
     if (N == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
+    if (K >= 4096) {  // long rows: straight from global memory (measured faster there)
+        gather_wsel_direct_kernel<<<dim3((unsigned)(N / (kGatherWarps * kGatherDirectRows)), (unsigned)E),
+                                    32 * kGatherWarps, 0, (cudaStream_t)stream>>>(w_codes, w_scales, N, K, S, k,
+                                                                                 (uint16_t *)w_sel);
+        return launch_status("gather_wsel_direct_kernel");
+    }
     const int64_t smem = gather_smem_bytes(K, k);
     if (smem > 227 * 1024) return NVFP4_ERR_UNSUPPORTED;
     if (smem > 48 * 1024) {

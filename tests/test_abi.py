@@ -114,6 +114,48 @@ def test_host_checks_without_gpu(lib):
     assert c(P, 3, 64, P, P, 4, 2, 64, P, None) == INVALID  # bad dtype
 
 
+def test_host_checks_of_the_trainer_and_online_entry_points(lib):
+    d = lib.nvfp4_bf16_grouped_gemm_dgrad
+    # dy, w_hat, offsets, E, rows_cap, N, K, out_dtype, epilogue, gu, y, ldy, dev_status, stream
+    args = [P, P, P, 2, 256, 256, 128, 1, 0, None, P, 256, None, None]
+    bad = list(args)
+    bad[6] = 96  # K % 64
+    assert d(*bad) == UNSUP
+    bad = list(args)
+    bad[5] = 128  # N % 256
+    assert d(*bad) == UNSUP
+    bad = list(args)
+    bad[8] = 2  # the SwiGLU backward needs the saved pre-activations
+    assert d(*bad) == INVALID
+    bad = list(args)
+    bad[8], bad[9], bad[7], bad[11] = 2, P, 0, 512  # ... and BF16 output
+    assert d(*bad) == INVALID
+    bad = list(args)
+    bad[8], bad[9], bad[11] = 2, P, 256  # ... and a row of 2N
+    assert d(*bad) == INVALID
+    bad = list(args)
+    bad[8] = 1  # the forward SwiGLU is not an input-gradient epilogue
+    assert d(*bad) == INVALID
+    bad = list(args)
+    bad[1] = PM
+    assert d(*bad) == ALIGN
+    w = lib.nvfp4_bf16_grouped_gemm_wgrad_rows
+    # a, b, offsets, E, R, M, N, out_dtype, dw, dev_status, stream
+    assert w(P, P, P, 2, 256, 96, 256, 0, P, None, None) == UNSUP  # M % 128
+    assert w(P, P, P, 2, 256, 128, 128, 0, P, None, None) == UNSUP  # N % 256
+    assert w(P, P, P, 2, 200, 128, 256, 0, P, None, None) == UNSUP  # R % 128
+    assert w(PM, P, P, 2, 256, 128, 256, 0, P, None, None) == ALIGN
+    gw = lib.nvfp4_gather_selected_weights
+    # w_codes, w_scales, E, N, K, S, k, w_sel, dev_status, stream
+    assert gw(P, P, 2, 256, 96, P, 8, P, None, None) == UNSUP  # K % 64
+    assert gw(P, P, 2, 200, 256, P, 8, P, None, None) == UNSUP  # N % 128
+    assert gw(P, P, 2, 256, 256, P, 12, P, None, None) == UNSUP  # k % 8
+    assert gw(P, P, 2, 256, 256, P, 300, P, None, None) == INVALID  # k > K
+    cb = lib.nvfp4_moe_combine_backward
+    # dout, y, dst_row, weights, T, topk, H, counts, offsets, E, rows_cap, dy, dweights, stream
+    assert cb(P, P, P, P, 4, 33, 64, P, P, 2, 256, P, None, None) == UNSUP  # topk > 32
+
+
 def test_gemm_pipeline_selector(lib):
     prev = ctypes.c_int32(-1)
     assert lib.nvfp4_gemm_pipeline(7, None) == INVALID

@@ -58,7 +58,8 @@ def test_online_selection_reads_routed_rows_only(nv):
     assert _chains.valid_topk(S, ref, k)
 
 
-@pytest.mark.parametrize("interleave,E,N,K,k", [(0, 3, 512, 768, 48), (1, 3, 512, 768, 48), (0, 2, 384, 960, 160)])
+@pytest.mark.parametrize("interleave,E,N,K,k", [(0, 3, 512, 768, 48), (1, 3, 512, 768, 48), (0, 2, 384, 960, 160),
+                                                (1, 2, 256, 4096, 136)])
 def test_gather_equals_the_weight_pack(nv, interleave, E, N, K, k):
     g = torch.Generator().manual_seed(21)
     w = (torch.randn((E, N, K), generator=g) * 0.02).to(torch.bfloat16)
