@@ -225,7 +225,8 @@ def run_ours(args):
     ms = t0.elapsed_time(t1)
     ms = job_time(ms, world, dev)
     ms_step = ms / args.steps
-    names = ["route", "amax_x", "quantize_x", "clear_padding", "gemm_gate_up", "quantize_h", "gemm_down", "combine"]
+    names = ["route", "amax_x_wait", "quantize_x", "clear_padding_wait", "gemm_gate_up", "quantize_h", "gemm_down",
+             "combine"]
     stage = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)])
              for j, n in enumerate(names)}
     gemm13_ms = statistics.mean([evs[i][4].elapsed_time(evs[i][5]) for i in range(args.steps)])
@@ -307,6 +308,9 @@ def run_ours(args):
         "quantize_x": {"gbs": round(q_gbs, 1), "hbm_frac": round(q_gbs / pk["hbm"], 4), "bytes": q_bytes},
         "quantize_h": {"gbs": round(qh_gbs, 1), "hbm_frac": round(qh_gbs / pk["hbm"], 4), "bytes": qh_bytes},
         "stages_ms": {n: round(v, 4) for n, v in stage.items()},
+        "stages_what": "each stage's share of the critical path on the layer's stream; the amax of x runs on a side "
+                       "stream beside the routing and the padding-row clear beside the quantization of x (the "
+                       "*_wait stages are what is left of them)",
         "roofline": {"kernel": "single_gemm_kernel<fp4> (gate_up, SwiGLU)", "bound": "tensor",
                      "achieved": round(gemm13_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                      "frac": round(gemm13_tflops / fp4_peak, 4), "traffic": gate_up_traffic(),
@@ -357,7 +361,8 @@ def decode_measure(dev, steps, pk):
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0
     ms = t0.elapsed_time(t1) / steps
-    names = ["route", "amax_x", "quantize_x", "clear_padding", "gemm_gate_up", "quantize_h", "gemm_down", "combine"]
+    names = ["route", "amax_x_wait", "quantize_x", "clear_padding_wait", "gemm_gate_up", "quantize_h", "gemm_down",
+             "combine"]
     stage = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps)])
              for j, n in enumerate(names)}
     rows = int(layer.route.offsets[-1].item())  # routed rows incl. segment padding
@@ -599,7 +604,7 @@ def mismatch_measure(layer, x, logits, w13, wd):
                 for i in range(5):
                     lay.forward(x, logits, mark=lambda k, i=i: sev[i][k].record())
                 torch.cuda.synchronize()
-                names = ["route", "amax_x+select_x", "quantize_x", "clear_padding", "gemm_gate_up",
+                names = ["route", "amax_x+select_x_wait", "quantize_x", "clear_padding_wait", "gemm_gate_up",
                          "select_h+quantize_h", "gemm_down", "combine"]
                 step_ms["online_stages"] = {n: round(statistics.median(sev[i][k].elapsed_time(sev[i][k + 1])
                                                                       for i in range(5)), 4)

@@ -122,6 +122,11 @@ class RolloutMoE:
             self.score_ws = torch.empty(257 * max(self.H, self.I), dtype=torch.float64, device=dev)
         self.LAUNCHES = 9 + (2 * (self.k13 > 0) + 2 * (self.kd > 0) if resid_fp4 else 0) + \
             (4 * (self.k13 > 0) + 4 * (self.kd > 0) if online else 0)
+        # work that does not depend on the routing (the amax of x, and its online channel
+        # selection) runs on a side stream beside it, and the padding rows are cleared there
+        # beside the quantization of x (they are rows the quantizer does not write)
+        self._side = torch.cuda.Stream(device=dev)
+        self._ev = [torch.cuda.Event() for _ in range(4)]
 
     LAUNCHES = 9
 
@@ -130,65 +135,78 @@ class RolloutMoE:
         (e.g. to alternate output buffers while an earlier result is being
         copied out), else a view of a reused buffer.
 
-        `mark(i)`, if given, is called before stage i = 0..7 (route, amax,
-        quantize x, clear padding, gate_up GEMM, quantize h, down GEMM,
-        combine) and with i = 8 at the end, e.g. to record CUDA events."""
+        `mark(i)`, if given, is called on the calling stream before stage i =
+        0..7 (routing, with the amax of x on a side stream beside it; the wait
+        for that amax; quantize x, with the padding rows cleared on the side
+        stream beside it; the wait for that clear; gate_up GEMM; quantize h;
+        down GEMM; combine) and with i = 8 at the end, e.g. to record CUDA
+        events: each stage's time is its share of the critical path."""
         mark = mark or (lambda i: None)
         T = x.shape[0]
         assert T <= self.max_tokens and logits.shape == (T, self.E)
         r = self.route
         ids, w, dst = r.ids[:T], r.weights[:T], r.dst_row[:T]
-        mark(0)
-        nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=stream)
+        main = stream or torch.cuda.current_stream(self.dev)
+        side, ev = self._side, self._ev
         xa, ha = self.xa, self.ha
-        mark(1)
-        nvfp4_amax(x, xa.amax, stream=stream)
+        mark(0)
+        ev[0].record(main)  # x and logits are ready
+        side.wait_event(ev[0])
+        nvfp4_amax(x, xa.amax, stream=side)
         if self.online and self.k13:  # Eq. 23-24 on this batch, and the weight columns it picks
-            nvfp4_rac_select_channels_online(x, xa.amax, self.k13, self.S13, self.score_ws, stream=stream)
+            nvfp4_rac_select_channels_online(x, xa.amax, self.k13, self.S13, self.score_ws, stream=side)
             W = self.w13
             nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.S13, W.sel,
-                                          dev_status=self.dev_status, stream=stream)
+                                          dev_status=self.dev_status, stream=side)
+        ev[1].record(side)
+        nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=main)
+        ev[2].record(main)
+        mark(1)
+        main.wait_event(ev[1])  # the amax of x (and its channel set)
         mark(2)
+        side.wait_event(ev[2])  # the routing's counts and offsets
+        nvfp4_moe_clear_padding(r.counts, r.offsets, self.E, self.H, self.k13, xa.codes, xa.scales,
+                                xa.resid if self.k13 else None, stream=side)
+        ev[3].record(side)
         nvfp4_quantize(x, xa.amax, xa.codes, xa.scales, resid=xa.resid if self.k13 else None,
                        S=self.S13 if self.k13 else None, gs_out=xa.gs, dst_row=dst,
                        fanout=self.topk, rows_out=self.rows_cap, dev_status=self.dev_status,
-                       stream=stream)
+                       stream=main)
         mark(3)
-        nvfp4_moe_clear_padding(r.counts, r.offsets, self.E, self.H, self.k13, xa.codes, xa.scales,
-                                xa.resid if self.k13 else None, stream=stream)
+        main.wait_event(ev[3])  # the padding rows are clear
         if self.resid_fp4 and self.k13:
             nvfp4_rac_requant_residual(xa.resid, self.resid_amax[0:1], r.offsets, self.E, gs_out=self.resid_gs[0:1],
-                                       dev_status=self.dev_status, stream=stream)
+                                       dev_status=self.dev_status, stream=main)
         mark(4)
         W = self.w13
         nvfp4_w4a4_rac_grouped_gemm(xa.codes, xa.scales, xa.resid if W.k else None, xa.gs, W.codes,
                                     W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.h,
                                     epilogue=NVFP4_EPI_SWIGLU, out_dtype=NVFP4_OUT_BF16,
-                                    amax_out=ha.amax, dev_status=self.dev_status, stream=stream)
+                                    amax_out=ha.amax, dev_status=self.dev_status, stream=main)
         mark(5)
         if self.online and self.kd:  # the routed rows of h only: rows past offsets[E] may be stale
             nvfp4_rac_select_channels_online(self.h, ha.amax, self.kd, self.Sd, self.score_ws, offsets=r.offsets,
-                                             E=self.E, stream=stream)
+                                             E=self.E, stream=main)
             W = self.wd
             nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.Sd, W.sel,
-                                          dev_status=self.dev_status, stream=stream)
+                                          dev_status=self.dev_status, stream=main)
         nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
                        S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
-                       stream=stream)
+                       stream=main)
         if self.resid_fp4 and self.kd:
             nvfp4_rac_requant_residual(ha.resid, self.resid_amax[1:2], r.offsets, self.E, gs_out=self.resid_gs[1:2],
-                                       dev_status=self.dev_status, stream=stream)
+                                       dev_status=self.dev_status, stream=main)
         mark(6)
         W = self.wd
         nvfp4_w4a4_rac_grouped_gemm(ha.codes, ha.scales, ha.resid if W.k else None, ha.gs, W.codes,
                                     W.scales, W.gs, W.sel, W.k, r.offsets, self.E, W.N, W.K, self.y,
                                     epilogue=NVFP4_EPI_NONE, out_dtype=NVFP4_OUT_BF16,
-                                    dev_status=self.dev_status, stream=stream)
+                                    dev_status=self.dev_status, stream=main)
         mark(7)
         if out is None:
             out = self.out[:T]
         assert out.shape == (T, self.H) and out.dtype == torch.float32
-        nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=stream)
+        nvfp4_moe_combine(self.y, dst, w, self.topk, out, stream=main)
         mark(8)
         return out
 
