@@ -840,10 +840,16 @@ __global__ void __launch_bounds__(256) resid_qdq_kernel(uint16_t *resid, int64_t
 // binary32 sums, the warps' sums are added in binary64 in warp order, and the
 // chunks' in chunk order -- deterministic, within a few ulp of binary32 of the
 // exact sums (all terms are nonnegative).
-constexpr int kOnlineChunks = 256;  // at most; about 512 rows of the buffer per chunk
-static int64_t online_chunks(int64_t rows_cap) {
-    int64_t c = (rows_cap / 512 + 15) / 16 * 16;
-    return c < 16 ? 16 : (c > kOnlineChunks ? kOnlineChunks : c);
+constexpr int kOnlineChunks = 256;  // row chunks of the score pass, at most
+// Row chunks of the score pass: one wave of blocks (two resident per SM) over the
+// (chunk, 512-column segment) grid, so that no partial last wave idles the GPU; at
+// least 512 rows per chunk when the rows are few.
+static int64_t online_chunks(int64_t rows_cap, int64_t K) {
+    const int64_t colblocks = (K + 511) / 512;
+    int64_t c = (int64_t)sm_count() * 2 / colblocks;
+    const int64_t by_rows = (rows_cap + 511) / 512;
+    if (c > by_rows) c = by_rows;
+    return c < 1 ? 1 : (c > kOnlineChunks ? kOnlineChunks : c);
 }
 
 __global__ void __launch_bounds__(256) online_score_kernel(const uint16_t *x, int64_t rows_cap, int64_t K,
@@ -1588,7 +1594,7 @@ extern "C" int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap,
     NVFP4_CHECK_INIT();
     cudaStream_t st = (cudaStream_t)stream;
     double *part = score_ws + K;  // [kOnlineChunks][K]
-    const int nchunks = (int)online_chunks(rows_cap);
+    const int nchunks = (int)online_chunks(rows_cap, K);
     online_score_kernel<<<dim3((unsigned)nchunks, (unsigned)((K + 511) / 512)), 256, 0, st>>>(
         (const uint16_t *)x, rows_cap, K, offsets, E, amax, part);
     int s = launch_status("online_score_kernel");
