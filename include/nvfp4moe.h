@@ -274,6 +274,26 @@ int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K,
 int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N, int64_t K,
                                   const int32_t *S, int32_t k, void *w_sel, int32_t *dev_status, void *stream);
 
+/* A channel-major copy of a weight pack for the online selection of QUADS
+ * §3.3 Eq. 23-24, made once per weight update, so that re-gathering W_hat on a
+ * new S reads only the selected channels (nvfp4_gather_selected_weights_t):
+ *   codes_t   device uint8 [E, K, N/2]: channel j of rows n, n+1 in one byte
+ *             (row n in the low nibble)
+ *   scales_t  device uint8 [E, K/16, N]: the block scale of row n, block kb
+ * from w_codes [E, N, K/2] and w_scales (the pack of nvfp4_prepare_weights).
+ * Errors: INVALID_ARG, ALIGNMENT (w_codes, codes_t), UNSUPPORTED (K % 64,
+ * N % 128, E > 65535). */
+int nvfp4_transpose_weight_pack(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N, int64_t K,
+                                uint8_t *codes_t, uint8_t *scales_t, void *stream);
+
+/* nvfp4_gather_selected_weights from the channel-major copy
+ * (nvfp4_transpose_weight_pack): the same w_sel [E, N, k], bit for bit,
+ * reading k/K of the codes (QUADS §3.3 Eq. 21's W_hat on the S of Eq. 23-24).
+ * Errors: INVALID_ARG, ALIGNMENT (codes_t, scales_t, w_sel), UNSUPPORTED
+ * (K % 64, N % 128, k % 8, E > 65535). */
+int nvfp4_gather_selected_weights_t(const uint8_t *codes_t, const uint8_t *scales_t, int32_t E, int64_t N, int64_t K,
+                                    const int32_t *S, int32_t k, void *w_sel, void *stream);
+
 /* ------------------------------------------------------------------------ */
 /* Grouped GEMMs (QUADS §3.3 Eq. 21; §3.2 Eq. 12)                            */
 /* ------------------------------------------------------------------------ */

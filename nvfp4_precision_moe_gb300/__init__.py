@@ -38,6 +38,8 @@ _SIGS = {
     "nvfp4_rac_requant_residual": "pqipipppp",
     "nvfp4_rac_select_channels_online": "pqqpipippp",
     "nvfp4_gather_selected_weights": "ppiqqpippp",
+    "nvfp4_transpose_weight_pack": "ppiqqppp",
+    "nvfp4_gather_selected_weights_t": "ppiqqpipp",
     "nvfp4_transpose_bf16": "piqqpp",
     "nvfp4_swiglu": "pqqpp",
     "nvfp4_swiglu_backward": "ppqqpp",
@@ -182,6 +184,17 @@ def nvfp4_gather_selected_weights(w_codes, w_scales, E, N, K, S, w_sel, dev_stat
     """w_sel [E, N, k] of a weight pack for the channel set S."""
     _call("nvfp4_gather_selected_weights", _p(w_codes), _p(w_scales), E, N, K, _p(S), S.numel(), _p(w_sel),
           _p(dev_status), _s(stream))
+
+
+def nvfp4_transpose_weight_pack(w_codes, w_scales, E, N, K, codes_t, scales_t, stream=None):
+    """Channel-major copy of a weight pack: codes_t [E, K, N/2], scales_t [E, K/16, N] (uint8)."""
+    _call("nvfp4_transpose_weight_pack", _p(w_codes), _p(w_scales), E, N, K, _p(codes_t), _p(scales_t), _s(stream))
+
+
+def nvfp4_gather_selected_weights_t(codes_t, scales_t, E, N, K, S, w_sel, stream=None):
+    """w_sel [E, N, k] for the channel set S from the channel-major copy of a weight pack."""
+    _call("nvfp4_gather_selected_weights_t", _p(codes_t), _p(scales_t), E, N, K, _p(S), S.numel(), _p(w_sel),
+          _s(stream))
 
 
 def nvfp4_prepare_weights(w, w_codes, w_scales, gs_w, amax_ws, S=None, w_sel=None, interleave=0,

@@ -1125,6 +1125,94 @@ __global__ void __launch_bounds__(32 * kGatherWarps) gather_wsel_direct_kernel(c
     }
 }
 
+// Channel-major copy of a weight pack, for the online gather: per expert e,
+// codes_t[e][j][n/2] holds channel j of rows n and n+1 (row n in the low
+// nibble) and scales_t[e][kb][n] the block scale of row n, block kb.  A block
+// transposes a 64-row x 64-channel tile of codes through shared memory (one
+// code per byte there) and the matching 64 x 4 block scales.
+__global__ void __launch_bounds__(256) pack_transpose_kernel(const uint8_t *codes, const uint8_t *scales, int64_t N,
+                                                             int64_t K, uint8_t *codes_t, uint8_t *scales_t) {
+    __shared__ uint8_t tile[64][64 + 4];  // [row][channel]
+    const int64_t e = blockIdx.z, n0 = (int64_t)blockIdx.y * 64, j0 = (int64_t)blockIdx.x * 64;
+    const int64_t nb = K >> 4, kslices = (nb + 15) >> 4;
+    const uint8_t *ce = codes + e * N * (K >> 1);
+    // read: 64 rows x 32 bytes (64 channels), 8 bytes per thread
+    {
+        const int r = threadIdx.x >> 2, q = threadIdx.x & 3;  // row, 8-byte quarter
+        const uint2 v = *reinterpret_cast<const uint2 *>(ce + (n0 + r) * (K >> 1) + (j0 >> 1) + 8 * q);
+        const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const uint32_t byte = (w[b >> 2] >> (8 * (b & 3))) & 0xffu;
+            tile[r][16 * q + 2 * b] = (uint8_t)(byte & 15u);
+            tile[r][16 * q + 2 * b + 1] = (uint8_t)(byte >> 4);
+        }
+    }
+    __syncthreads();
+    // write: 64 channels x 32 bytes (64 rows, two per byte), 8 bytes per thread
+    {
+        const int c = threadIdx.x >> 2, q = threadIdx.x & 3;  // channel, 8-byte quarter of the rows
+        uint32_t w[2] = {0u, 0u};
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            const int r = 16 * q + 2 * b;
+            w[b >> 2] |= ((uint32_t)tile[r][c] | ((uint32_t)tile[r + 1][c] << 4)) << (8 * (b & 3));
+        }
+        *reinterpret_cast<uint2 *>(codes_t + (e * K + j0 + c) * (N >> 1) + (n0 >> 1) + 8 * q) = make_uint2(w[0], w[1]);
+    }
+    // the tile's 4 blocks of scales: scales_t[e][kb][n0 .. n0 + 64)
+    if (threadIdx.x < 256) {
+        const int kb = (int)(j0 >> 4) + (threadIdx.x >> 6), r = threadIdx.x & 63;
+        if (kb < nb) {
+            const int64_t n = n0 + r;
+            const uint8_t *se = scales + e * (N >> 7) * kslices * 2048;
+            scales_t[(e * nb + kb) * N + n] =
+                se[scale_row_offset(n, kslices) + scale_block_offset(kb & ~3) + (kb & 3)];
+        }
+    }
+}
+
+// w_sel[e, n, s] from the channel-major pack: a block covers 128 rows x 64
+// selected channels of one expert; thread (s, quarter) reads the 32 rows'
+// codes of channel S[s] (16 bytes) and their 32 block scales, writes the 32
+// values into a shared tile, and the tile leaves as 128-byte row pieces.
+__global__ void __launch_bounds__(256) gather_wsel_t_kernel(const uint8_t *codes_t, const uint8_t *scales_t, int64_t N,
+                                                           int64_t K, const int32_t *S, int32_t k, uint16_t *wsel) {
+    __shared__ __align__(16) uint16_t tile[128][64 + 8];  // [row][selected channel]
+    const int64_t e = blockIdx.z, n0 = (int64_t)blockIdx.y * 128;
+    const int s0 = blockIdx.x * 64;
+    const int64_t nb = K >> 4;
+    {
+        const int sl = threadIdx.x >> 2, q = threadIdx.x & 3;  // channel in the tile, 32-row quarter
+        const int s = s0 + sl;
+        if (s < k) {
+            const int32_t j = min(max(__ldg(S + s), 0), (int32_t)(K - 1));
+            const uint4 c = __ldg(reinterpret_cast<const uint4 *>(codes_t + (e * K + j) * (N >> 1) + (n0 >> 1)) + q);
+            const uint8_t *sc = scales_t + (e * nb + (j >> 4)) * N + n0 + 32 * q;
+            const uint4 s_lo = __ldg(reinterpret_cast<const uint4 *>(sc)), s_hi = __ldg(reinterpret_cast<const uint4 *>(sc) + 1);
+            const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
+            const uint32_t sw[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const uint32_t code = (cw[i >> 3] >> (4 * (i & 7))) & 15u;
+                const uint32_t sb = (sw[i >> 2] >> (8 * (i & 3))) & 0xffu;
+                tile[32 * q + i][sl] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(e2m1_to_f32_hw(code), e4m3_to_f32(sb))));
+            }
+        }
+    }
+    __syncthreads();
+    // 128 rows x (up to) 64 channels = 128 bytes per row: 8 lanes x 16 bytes per row
+    const int nsel = min(64, k - s0);
+    for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
+        const int r = i >> 3, p = i & 7;
+        if (8 * p < nsel) {  // k % 8 == 0: whole 16-byte pieces
+            const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][8 * p]);
+            *reinterpret_cast<uint4 *>(wsel + (e * N + n0 + r) * k + s0 + 8 * p) = v;
+        }
+    }
+}
+
 // QDQ_W (QUADS §3.2 Eq. 12) that also writes the transpose, for the learner's
 // backward (dX = W_hat^T dY needs W_hat^T with the reduction axis contiguous):
 // a block owns a 64 x 64 tile of one tensor; each thread quantizes one
@@ -1634,6 +1722,31 @@ extern "C" int nvfp4_gather_selected_weights(const uint8_t *w_codes, const uint8
     gather_wsel_kernel<<<dim3((unsigned)(N / 128), (unsigned)E), 32 * kGatherWarps, (size_t)smem,
                          (cudaStream_t)stream>>>(w_codes, w_scales, N, K, S, k, (uint16_t *)w_sel, dev_status);
     return launch_status("gather_wsel_kernel");
+}
+
+extern "C" int nvfp4_transpose_weight_pack(const uint8_t *w_codes, const uint8_t *w_scales, int32_t E, int64_t N,
+                                           int64_t K, uint8_t *codes_t, uint8_t *scales_t, void *stream) {
+    if (!w_codes || !w_scales || !codes_t || !scales_t || E < 1 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 || N % 128 || E > 65535 || K / 64 > 0x7fffffff || N / 64 > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(w_codes) || !aligned16(codes_t)) return NVFP4_ERR_ALIGNMENT;
+    if (N == 0 || K == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    pack_transpose_kernel<<<dim3((unsigned)(K / 64), (unsigned)(N / 64), (unsigned)E), 256, 0,
+                            (cudaStream_t)stream>>>(w_codes, w_scales, N, K, codes_t, scales_t);
+    return launch_status("pack_transpose_kernel");
+}
+
+extern "C" int nvfp4_gather_selected_weights_t(const uint8_t *codes_t, const uint8_t *scales_t, int32_t E, int64_t N,
+                                               int64_t K, const int32_t *S, int32_t k, void *w_sel, void *stream) {
+    if (!codes_t || !scales_t || !S || !w_sel || E < 1 || N < 0 || K < 0 || k < 1 || k > K)
+        return NVFP4_ERR_INVALID_ARG;
+    if (K % 64 || N % 128 || k % 8 || E > 65535 || N / 128 > 65535) return NVFP4_ERR_UNSUPPORTED;
+    if (!aligned16(codes_t) || !aligned16(scales_t) || !aligned16(w_sel)) return NVFP4_ERR_ALIGNMENT;
+    if (N == 0) return NVFP4_OK;
+    NVFP4_CHECK_INIT();
+    gather_wsel_t_kernel<<<dim3((unsigned)((k + 63) / 64), (unsigned)(N / 128), (unsigned)E), 256, 0,
+                           (cudaStream_t)stream>>>(codes_t, scales_t, N, K, S, k, (uint16_t *)w_sel);
+    return launch_status("gather_wsel_t_kernel");
 }
 
 extern "C" int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,

@@ -18,7 +18,8 @@ import torch
 from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_EPI_SWIGLU_BWD, NVFP4_OUT_BF16,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
-               nvfp4_bf16_grouped_gemm_dgrad, nvfp4_bf16_grouped_gemm_wgrad_rows, nvfp4_gather_selected_weights,
+               nvfp4_bf16_grouped_gemm_dgrad, nvfp4_bf16_grouped_gemm_wgrad_rows, nvfp4_gather_selected_weights_t,
+               nvfp4_transpose_weight_pack,
                nvfp4_moe_combine_backward,
                nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online, nvfp4_route_topk, nvfp4_swiglu,
                nvfp4_w4a4_rac_grouped_gemm)
@@ -120,6 +121,12 @@ class RolloutMoE:
         self.online = online
         if online:
             self.score_ws = torch.empty(257 * max(self.H, self.I), dtype=torch.float64, device=dev)
+            # channel-major copies of the packs: a new S re-gathers only its own channels
+            for W in (self.w13, self.wd):
+                if W.k:
+                    W.codes_t = torch.empty((W.E, W.K, W.N // 2), dtype=torch.uint8, device=dev)
+                    W.scales_t = torch.empty((W.E, W.K // 16, W.N), dtype=torch.uint8, device=dev)
+                    nvfp4_transpose_weight_pack(W.codes, W.scales, W.E, W.N, W.K, W.codes_t, W.scales_t)
         self.LAUNCHES = 9 + (2 * (self.k13 > 0) + 2 * (self.kd > 0) if resid_fp4 else 0) + \
             (4 * (self.k13 > 0) + 4 * (self.kd > 0) if online else 0)
         # work that does not depend on the routing (the amax of x, and its online channel
@@ -156,8 +163,7 @@ class RolloutMoE:
         if self.online and self.k13:  # Eq. 23-24 on this batch, and the weight columns it picks
             nvfp4_rac_select_channels_online(x, xa.amax, self.k13, self.S13, self.score_ws, stream=side)
             W = self.w13
-            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.S13, W.sel,
-                                          dev_status=self.dev_status, stream=side)
+            nvfp4_gather_selected_weights_t(W.codes_t, W.scales_t, self.E, W.N, W.K, self.S13, W.sel, stream=side)
         ev[1].record(side)
         nvfp4_route_topk(logits, self.topk, ids, w, r.counts, r.offsets, dst, stream=main)
         ev[2].record(main)
@@ -188,8 +194,7 @@ class RolloutMoE:
             nvfp4_rac_select_channels_online(self.h, ha.amax, self.kd, self.Sd, self.score_ws, offsets=r.offsets,
                                              E=self.E, stream=main)
             W = self.wd
-            nvfp4_gather_selected_weights(W.codes, W.scales, self.E, W.N, W.K, self.Sd, W.sel,
-                                          dev_status=self.dev_status, stream=main)
+            nvfp4_gather_selected_weights_t(W.codes_t, W.scales_t, self.E, W.N, W.K, self.Sd, W.sel, stream=main)
         nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
                        S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
                        stream=main)

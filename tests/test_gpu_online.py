@@ -91,6 +91,43 @@ def test_gather_equals_the_weight_pack(nv, interleave, E, N, K, k):
             assert np.array_equal(G.u16(got[e]), ref)
 
 
+@pytest.mark.parametrize("interleave,E,N,K,k", [(0, 3, 512, 768, 48), (1, 2, 256, 4096, 136), (0, 2, 384, 960, 160)])
+def test_gather_from_the_channel_major_pack(nv, interleave, E, N, K, k):
+    """nvfp4_transpose_weight_pack + nvfp4_gather_selected_weights_t give the
+    same w_sel as the gather from the pack itself, bit for bit; the
+    channel-major copy holds every code and block scale of the pack."""
+    g = torch.Generator().manual_seed(31)
+    w = (torch.randn((E, N, K), generator=g) * 0.02).to(torch.bfloat16).to(G.DEV)
+    codes = G.zeros((E, N, K // 2), torch.uint8)
+    scales = G.zeros(E * nv.scale_bytes(N, K), torch.uint8)
+    nv.nvfp4_prepare_weights(w, codes, scales, G.zeros(E, torch.float32), G.zeros(E, torch.float32),
+                             interleave=interleave)
+    rng = np.random.default_rng(32)
+    S = torch.tensor(np.sort(rng.choice(K, k, replace=False)).astype(np.int32), device=G.DEV)
+    codes_t = G.zeros((E, K, N // 2), torch.uint8)
+    scales_t = G.zeros((E, K // 16, N), torch.uint8)
+    nv.nvfp4_transpose_weight_pack(codes, scales, E, N, K, codes_t, scales_t)
+    want = G.zeros((E, N, k), torch.bfloat16)
+    got = torch.full((E, N, k), 7.0, dtype=torch.bfloat16, device=G.DEV)
+    nv.nvfp4_gather_selected_weights(codes, scales, E, N, K, S, want)
+    nv.nvfp4_gather_selected_weights_t(codes_t, scales_t, E, N, K, S, got)
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    # the copy itself: every code and block scale, by the layouts' definitions
+    c = codes.cpu().numpy()
+    lo, hi = c & 15, c >> 4
+    full = np.empty((E, N, K), np.uint8)
+    full[:, :, 0::2], full[:, :, 1::2] = lo, hi
+    ct = codes_t.cpu().numpy()
+    tfull = np.empty((E, K, N), np.uint8)
+    tfull[:, :, 0::2], tfull[:, :, 1::2] = ct & 15, ct >> 4
+    assert np.array_equal(tfull, full.transpose(0, 2, 1))
+    sc = scales.cpu().numpy().reshape(E, -1)
+    st = scales_t.cpu().numpy()
+    for e in range(E):
+        assert np.array_equal(st[e].T, oracle.scale_rows(sc[e], np.arange(N), K))
+
+
 def test_rollout_layer_online(nv):
     from tests.test_oracle_mismatch import small_moe
 
