@@ -10,9 +10,23 @@
 
 namespace nvfp4 {
 
-// one warp per token; each block counts the experts its tokens chose
-// in shared memory and adds its counts into `counts` (zeroed on the stream
-// before the launch)
+// A logit as an unsigned key whose integer order is the float order (-0
+// counts as +0, so the two tie as floats do), and back.
+__device__ __forceinline__ uint32_t order_key(float f) {
+    uint32_t u = __float_as_uint(f);
+    if (u == 0x80000000u) u = 0u;
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k); }
+
+// One warp per token.  Lane l holds the keys of experts l + 32i (kPer of them,
+// E <= 32 kPer) in registers.  Each of the topk selections is two warp
+// reductions: the largest key among the lanes' best untaken ones, then the
+// lowest expert index holding it (ties go to the lower expert).  The softmax
+// sum adds a lane's experts in order, then across lanes by a butterfly.  Each
+// block counts the experts its tokens chose in shared memory and adds its
+// counts into `counts` (zeroed on the stream before the launch).
+template <int kPer>
 __global__ void __launch_bounds__(256) topk_kernel(const float *logits, int32_t T, int32_t E, int32_t topk,
                                                    int32_t *ids, float *weights, int32_t *counts) {
     __shared__ int32_t s_hist[1024];
@@ -22,66 +36,47 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *logits, int32_t 
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
         const float *l = logits + t * E;
-        float mx = -INFINITY;
-        for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
+        uint32_t key[kPer];
+        uint32_t lmax = 0u;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        for (int i = 0; i < kPer; ++i) {
+            const int e = lane + 32 * i;
+            key[i] = e < E ? order_key(__ldg(l + e)) : 0u;
+            lmax = max(lmax, key[i]);
+        }
+        const float mx = key_value(__reduce_max_sync(0xffffffffu, lmax));
         float sum = 0.0f;
-        for (int e = lane; e < E; e += 32) sum += expf(l[e] - mx);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            if (lane + 32 * i < E) sum += expf(key_value(key[i]) - mx);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        // bitmask of experts already taken, E <= 1024 -> 32 words, word w owned by lane w
-        uint32_t taken = 0u;
-        // up to 256 experts: this lane's logits (experts lane + 32i) stay in registers
-        constexpr int kRegE = 8;
-        float lr[kRegE];
-        const bool in_regs = E <= 32 * kRegE;
-#pragma unroll
-        for (int i = 0; i < kRegE; ++i) lr[i] = (in_regs && lane + 32 * i < E) ? l[lane + 32 * i] : -INFINITY;
+        uint32_t taken = 0u;  // bit i: expert lane + 32i is chosen
+        uint32_t my_id = 0u, my_key = 0u;
         for (int s = 0; s < topk; ++s) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-            if (in_regs) {
+            // this lane's best untaken expert (strict >: the lower index of equal keys); with
+            // topk <= E some lane always has one, so the chosen index is always < E
+            uint32_t bk = 0u;
+            int bi = -1;
 #pragma unroll
-                for (int i = 0; i < kRegE; ++i) {
-                    const int e = lane + 32 * i;
-                    const uint32_t word = __shfl_sync(0xffffffffu, taken, i);
-                    if (e < E && !((word >> lane) & 1u)) {
-                        const float v = lr[i];
-                        if (v > bv || (v == bv && e < be)) {
-                            bv = v;
-                            be = e;
-                        }
-                    }
+            for (int i = 0; i < kPer; ++i)
+                if (lane + 32 * i < E && !((taken >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+                    bk = key[i];
+                    bi = i;
                 }
-            } else {
-                for (int e0 = 0; e0 < E; e0 += 32) {  // uniform trip count for the shuffle
-                    const int e = e0 + lane;
-                    const uint32_t word = __shfl_sync(0xffffffffu, taken, e0 >> 5);
-                    if (e < E && !((word >> lane) & 1u)) {
-                        float v = l[e];
-                        if (v > bv || (v == bv && e < be)) {
-                            bv = v;
-                            be = e;
-                        }
-                    }
-                }
+            const uint32_t gk = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t ge =
+                __reduce_min_sync(0xffffffffu, bi >= 0 && bk == gk ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
+            if ((int)(ge & 31u) == lane) taken |= 1u << (ge >> 5);
+            if (lane == s) {
+                my_id = ge;
+                my_key = gk;
             }
-            // lanes with no candidate in this pass still take part in the shuffles
-            for (int o = 16; o > 0; o >>= 1) {
-                float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if (lane == (be >> 5)) taken |= 1u << (be & 31);
-            if (lane == 0) {
-                ids[t * topk + s] = be;
-                weights[t * topk + s] = expf(bv - mx) / sum;
-                atomicAdd(&s_hist[be], 1);
-            }
+        }
+        if (lane < topk) {
+            ids[t * topk + lane] = (int32_t)my_id;
+            weights[t * topk + lane] = expf(key_value(my_key) - mx) / sum;
+            if (my_id < (uint32_t)E) atomicAdd(&s_hist[my_id], 1);
         }
     }
     __syncthreads();
@@ -89,10 +84,14 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *logits, int32_t 
         if (s_hist[e]) atomicAdd(&counts[e], s_hist[e]);
 }
 
-// block per expert: the padded segment start (from all experts' counts),
-// then the ranks of its tokens in token order.  Thread i owns a contiguous
-// run of tokens: it counts its matches, a block-wide scan gives its first
-// rank, and a second pass over the same run writes the rows.
+// Block per expert: the padded segment start (from all experts' counts), then
+// the ranks of its tokens in token order.  Thread i owns a contiguous run of
+// tokens.  A run of at most 128 ids (read 16 bytes at a time, eight loads in
+// flight) keeps its matches as a 128-bit mask, so the ids are read once
+// however many of them match; a longer run counts its matches and reads the
+// run again to write them.  A block-wide scan gives each run its first rank.
+constexpr int kMaskIds = 128;
+
 __global__ void __launch_bounds__(1024) dst_row_kernel(const int32_t *ids, int32_t T, int32_t E, int32_t topk,
                                                        const int32_t *counts, int32_t *offsets, int32_t *dst_row) {
     const int e = blockIdx.x;
@@ -113,27 +112,47 @@ __global__ void __launch_bounds__(1024) dst_row_kernel(const int32_t *ids, int32
     const int64_t per = (T + (int64_t)blockDim.x - 1) / blockDim.x;
     const int64_t t0 = (int64_t)threadIdx.x * per;
     const int64_t t1 = min((int64_t)T, t0 + per);
+    const int64_t n = t1 > t0 ? (t1 - t0) * topk : 0;  // ids in the run
+    const int32_t *run = ids + t0 * topk;
     // the run's ids are contiguous: read them 16 bytes at a time when rows are whole int4s
     const bool vec = (topk & 3) == 0 && (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
+    const bool masked = vec && n <= kMaskIds;
+    const int4 *p = reinterpret_cast<const int4 *>(run);
+    uint32_t mk[kMaskIds / 32] = {0u, 0u, 0u, 0u};  // bit j: id j of the run is e
     int c = 0;
-    if (vec) {
-        const int4 *p = reinterpret_cast<const int4 *>(ids + t0 * topk);
-        const int64_t n4 = (t1 - t0) * topk / 4;
+    if (masked) {
+        const int n4 = (int)(n / 4);
+#pragma unroll
+        for (int i0 = 0; i0 < kMaskIds / 4; i0 += 8) {
+            int4 q[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) q[u] = i0 + u < n4 ? __ldg(p + i0 + u) : make_int4(-1, -1, -1, -1);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u;
+                const uint32_t b = (uint32_t)(q[u].x == e) | ((uint32_t)(q[u].y == e) << 1) |
+                                   ((uint32_t)(q[u].z == e) << 2) | ((uint32_t)(q[u].w == e) << 3);
+                mk[i >> 3] |= b << (4 * (i & 7));
+            }
+        }
+#pragma unroll
+        for (int w = 0; w < kMaskIds / 32; ++w) c += __popc(mk[w]);
+    } else if (vec) {
+        const int64_t n4 = n / 4;
         int64_t i = 0;
-        for (; i + 4 <= n4; i += 4) {  // four 16-byte loads in flight
-            int4 q[4];
+        for (; i + 8 <= n4; i += 8) {  // eight 16-byte loads in flight
+            int4 q[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) q[u] = __ldg(p + i + u);
+            for (int u = 0; u < 8; ++u) q[u] = __ldg(p + i + u);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) c += (q[u].x == e) + (q[u].y == e) + (q[u].z == e) + (q[u].w == e);
+            for (int u = 0; u < 8; ++u) c += (q[u].x == e) + (q[u].y == e) + (q[u].z == e) + (q[u].w == e);
         }
         for (; i < n4; ++i) {
             const int4 q = __ldg(p + i);
             c += (q.x == e) + (q.y == e) + (q.z == e) + (q.w == e);
         }
     } else {
-        for (int64_t t = t0; t < t1; ++t)
-            for (int s = 0; s < topk; ++s) c += ids[t * topk + s] == e;
+        for (int64_t i = 0; i < n; ++i) c += run[i] == e;
     }
     // block-wide exclusive scan of c (thread order = token order)
     int incl = c;
@@ -157,21 +176,23 @@ __global__ void __launch_bounds__(1024) dst_row_kernel(const int32_t *ids, int32
     __syncthreads();
     int r = s_base + s_part[wid] + incl - c;
     if (c == 0) return;  // nothing of this expert in the run
-    if (vec) {
-        const int4 *p = reinterpret_cast<const int4 *>(ids + t0 * topk);
-        const int64_t n4 = (t1 - t0) * topk / 4;
+    int32_t *d = dst_row + t0 * topk;
+    if (masked) {
+#pragma unroll
+        for (int w = 0; w < kMaskIds / 32; ++w)
+            for (uint32_t m = mk[w]; m; m &= m - 1u) d[32 * w + __ffs((int)m) - 1] = r++;
+    } else if (vec) {  // a second pass over the run, 16 bytes at a time
+        const int64_t n4 = n / 4;
         for (int64_t i = 0; i < n4; ++i) {
-            const int4 q = __ldg(p + i);  // a second pass over the same run: L1 hits
-            int32_t *d = dst_row + t0 * topk + 4 * i;
-            if (q.x == e) d[0] = r++;
-            if (q.y == e) d[1] = r++;
-            if (q.z == e) d[2] = r++;
-            if (q.w == e) d[3] = r++;
+            const int4 q = __ldg(p + i);
+            if (q.x == e) d[4 * i] = r++;
+            if (q.y == e) d[4 * i + 1] = r++;
+            if (q.z == e) d[4 * i + 2] = r++;
+            if (q.w == e) d[4 * i + 3] = r++;
         }
     } else {
-        for (int64_t t = t0; t < t1; ++t)
-            for (int s = 0; s < topk; ++s)
-                if (ids[t * topk + s] == e) dst_row[t * topk + s] = r++;
+        for (int64_t i = 0; i < n; ++i)
+            if (run[i] == e) d[i] = r++;
     }
 }
 
@@ -305,7 +326,10 @@ extern "C" int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32
     }
     if (T > 0) {
         // a warp per token: the selection passes are latency-bound, so every token gets its own warp
-        topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, st>>>(logits, T, E, topk, ids, weights, counts);
+        const unsigned blocks = (unsigned)((T + 7) / 8);
+        if (E <= 128) topk_kernel<4><<<blocks, 256, 0, st>>>(logits, T, E, topk, ids, weights, counts);
+        else if (E <= 256) topk_kernel<8><<<blocks, 256, 0, st>>>(logits, T, E, topk, ids, weights, counts);
+        else topk_kernel<32><<<blocks, 256, 0, st>>>(logits, T, E, topk, ids, weights, counts);
         int s = launch_status("topk_kernel");
         if (s != NVFP4_OK) return s;
     }

@@ -69,6 +69,25 @@ def test_routing_ties_and_small_shapes():
     assert np.array_equal(offs, ro) and np.array_equal(dst, rd)
 
 
+@pytest.mark.parametrize("T,E,topk,skew", [(300, 200, 8, 0.0), (257, 600, 5, 0.0), (12000, 64, 6, 8.0),
+                                             (16384, 128, 8, 8.0), (20000, 128, 8, 8.0)])
+def test_routing_wide_and_skewed(T, E, topk, skew):
+    """Expert counts that take the 8- and 32-key-per-lane selections, a slot
+    count that is not a multiple of 4, and routing so skewed that every id of
+    a thread's run of tokens matches (every token prefers the same topk
+    experts), with runs of 128 ids (kept as a match mask) and of 160 (counted,
+    then read again)."""
+    g = torch.Generator().manual_seed(T + E)
+    logits = torch.randn((T, E), generator=g)
+    logits[:, :topk] += skew
+    ids, w, counts, offs, dst = _route_gpu(logits, topk)
+    rid, rw = oracle.route_topk(logits.numpy(), topk)
+    assert np.array_equal(ids, rid)
+    assert np.allclose(w, rw, rtol=1e-5, atol=0)
+    rc, ro, rd = oracle.route_layout(rid, E)
+    assert np.array_equal(counts, rc) and np.array_equal(offs, ro) and np.array_equal(dst, rd)
+
+
 @pytest.mark.parametrize("ydt", [torch.float32, torch.bfloat16])
 def test_combine_parity(ydt):
     T, topk, E, H = 300, 8, 64, 512
