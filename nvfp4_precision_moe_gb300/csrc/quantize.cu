@@ -659,13 +659,17 @@ __global__ void __launch_bounds__(32 * kScoreWarps) channel_score_kernel(const u
 // k-th largest key T is found 8 bits at a time with shared-memory histograms
 // of the keys that share the bits found so far; then every channel with a key
 // above T, and the first (k - #above) channels with key T in channel order,
-// are written in channel order.
+// are written in channel order.  When the bucket that holds the k-th key holds
+// exactly the keys still needed, every key in it is kept whatever its lower
+// bits, so the search stops there (usually after two or three of the eight
+// passes) and the channels whose bits down to that digit are at least T's are
+// written -- the same set.
 constexpr int kTopkPerThread = 16;  // keys per thread: K <= 16 * 1024
 __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, int64_t K, int32_t k, int32_t *S) {
     __shared__ uint32_t hist[256];
     __shared__ int32_t warp_a[32], warp_b[32];
     __shared__ unsigned long long s_prefix;
-    __shared__ int32_t s_need, carry_eq, carry_out;
+    __shared__ int32_t s_need, carry_eq, carry_out, s_stop;
     const unsigned long long *key = reinterpret_cast<const unsigned long long *>(ssq);
     // the keys stay in registers for all passes: key j = threadIdx.x + i * blockDim.x
     unsigned long long kv[kTopkPerThread];
@@ -679,6 +683,7 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, in
         s_need = k;  // rank of T among the keys that share the prefix, counted from the top
         carry_eq = 0;
         carry_out = 0;
+        s_stop = -1;  // the digit's shift once the bucket of the k-th key is kept whole
     }
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (int)(blockDim.x >> 5);
     for (int shift = 56; shift >= 0; shift -= 8) {
@@ -721,6 +726,7 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, in
                     if (cum + (int32_t)h[i] >= need) {
                         s_prefix = prefix | ((unsigned long long)(255 - 8 * lane - i) << shift);
                         s_need = need - cum;
+                        if (cum + (int32_t)h[i] == need) s_stop = shift;
                         break;
                     }
                     cum += (int32_t)h[i];
@@ -728,23 +734,25 @@ __global__ void __launch_bounds__(1024) select_topk_kernel(const double *ssq, in
             }
         }
         __syncthreads();
+        if (s_stop >= 0) break;  // the same in every thread
     }
     const unsigned long long T = s_prefix;
     const int32_t need_eq = s_need;  // keys equal to T to keep, lowest channels first
+    const int stop = s_stop;
 #pragma unroll
     for (int i = 0; i < kTopkPerThread; ++i) {
         const int64_t j0 = (int64_t)i * blockDim.x;
         if (j0 >= K) break;  // the same in every thread
         const int64_t j = j0 + threadIdx.x;
         const unsigned long long v = kv[i];
-        const int eq = j < K && v == T;
+        const int eq = stop < 0 && j < K && v == T;
         // rank of this channel among the equal keys, in channel order
         const unsigned be = __ballot_sync(0xffffffffu, eq);
         if (lane == 0) warp_a[wid] = __popc(be);
         __syncthreads();
         int pre_eq = carry_eq + __popc(be & ((1u << lane) - 1u));
         for (int w = 0; w < wid; ++w) pre_eq += warp_a[w];
-        const int flag = j < K && (v > T || (eq && pre_eq < need_eq));
+        const int flag = j < K && (stop >= 0 ? (v >> stop) >= (T >> stop) : (v > T || (eq && pre_eq < need_eq)));
         const unsigned bf = __ballot_sync(0xffffffffu, flag);
         if (lane == 0) warp_b[wid] = __popc(bf);
         __syncthreads();

@@ -290,6 +290,32 @@ def test_channel_selection_parity(cfg):
     assert set(synth.outlier_channels(cfg).tolist()) <= set(S.cpu().tolist())
 
 
+@pytest.mark.parametrize("k", [3, 16, 40, 100])
+def test_channel_selection_ties_and_early_stop(k):
+    """Top-k on scores with exact ties: channels 32..63 copy channel 32 (two
+    whole blocks of equal columns, so equal binary64 scores) and a wider
+    outlier set; k values put the boundary inside the tied group (ties to the
+    lower channels) and inside distinct scores, where the radix search stops
+    once the k-th key's bucket is kept whole."""
+    g = torch.Generator().manual_seed(71 + k)
+    M, K = 96, 512
+    x = torch.randn((M, K), generator=g)
+    x[:, 32:64] = x[:, 32:33] * 3.0
+    x[:, 200:208] *= 5.0
+    xu = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    xd = x.to(torch.bfloat16).to(G.DEV)
+    amax = G.zeros(1, torch.float32)
+    nv.nvfp4_amax(xd, amax)
+    S = G.zeros(k, torch.int32)
+    ws = torch.zeros(K, dtype=torch.float64, device=G.DEV)
+    nv.nvfp4_rac_select_channels(xd, amax, k, S, ws)
+    torch.cuda.synchronize()
+    ssq = oracle.channel_scores_sq(xu)
+    assert np.array_equal(ws.cpu().numpy(), ssq)
+    assert len(set(ssq[32:64].tolist())) == 1  # the tied group
+    assert np.array_equal(S.cpu().numpy(), oracle.select_channels(ssq, k))
+
+
 def test_bounded_wait_times_out_cleanly():
     st = G.zeros(1, torch.int32)
     nv.nvfp4_selftest_wait_timeout(2000, st)  # 2 ms
