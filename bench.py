@@ -207,7 +207,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     assert int(layer.dev_status.item()) == 0, nv.STATUS.get(int(layer.dev_status.item()))
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage)] for _ in range(args.steps)]
+    # the timed step: the layer forward replayed as one CUDA graph (the same launches as
+    # an eager forward, issued at once), on inputs resident in HBM
+    graph, g_out = layer.capture(x, logits)
+    for _ in range(args.warmup):
+        graph.replay()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     if world > 1:
@@ -218,13 +222,24 @@ def run_ours(args):
     time.sleep(0.15)
     t0.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        graph.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     ms = t0.elapsed_time(t1)
     ms = job_time(ms, world, dev)
     ms_step = ms / args.steps
+    assert int(layer.dev_status.item()) == 0
+    g_res = g_out.clone()
+    assert torch.equal(g_res, layer.forward(x, logits))
+
+    # the stage breakdown: eager forwards with CUDA events between the stages
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nstage)] for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    eager_ms = job_time(evs[0][0].elapsed_time(evs[-1][nstage - 1]), world, dev) / args.steps
     names = ["route", "amax_x_wait", "quantize_x", "clear_padding_wait", "gemm_gate_up", "quantize_h", "gemm_down",
              "combine"]
     stage = {n: statistics.median([evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)])
@@ -243,6 +258,10 @@ def run_ours(args):
     ld = [torch.empty_like(logits) for _ in range(2)]
     od = [torch.empty((T, H), dtype=torch.float32, device=dev) for _ in range(2)]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    for i in range(2):
+        xd[i].copy_(x)
+        ld[i].copy_(logits)
+    graphs = [layer.capture(xd[i], ld[i], out=od[i])[0] for i in range(2)]  # one per buffer slot
 
     def e2e_run(n):
         h2d = [torch.cuda.Event() for _ in range(2)]
@@ -267,7 +286,7 @@ def run_ours(args):
             stream.wait_event(h2d[slot])
             if d2h[slot] is not None:  # step i-2's result has left this output buffer
                 stream.wait_event(d2h[slot])
-            layer.forward(xd[slot], ld[slot], out=od[slot])
+            graphs[slot].replay()
             comp[slot] = torch.cuda.Event()
             comp[slot].record(stream)
             s_out.wait_event(comp[slot])
@@ -303,12 +322,14 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "e2m1 (fp32 accum) + bf16 RAC", "data": "synthetic",
         "config": {"workload": "moe_prefill T=16384 H=4096 E=128 top8 zipf1.1 I=1536 k=128",
                    "T": T, "H": H, "E": E, "topk": c["topk"], "I": I, "k": k, "parallelism": "replicas",
-                   "l2": "no flush: every step streams ~3 GB, far more than the 129 MB L2"},
+                   "l2": "no flush: every step streams ~3 GB, far more than the 129 MB L2",
+                   "launch": "each step is one CUDA-graph replay of the layer forward (RolloutMoE.capture)"},
         "fp4_peak_frac_step": round(world * f4 / (ms_step * 1e-3) / 1e12 / fp4_peak, 4),
         "quantize_x": {"gbs": round(q_gbs, 1), "hbm_frac": round(q_gbs / pk["hbm"], 4), "bytes": q_bytes},
         "quantize_h": {"gbs": round(qh_gbs, 1), "hbm_frac": round(qh_gbs / pk["hbm"], 4), "bytes": qh_bytes},
         "stages_ms": {n: round(v, 4) for n, v in stage.items()},
-        "stages_what": "each stage's share of the critical path on the layer's stream; the amax of x runs on a side "
+        "stages_what": "eager forwards with CUDA events between the stages: each stage's share of the critical "
+                       "path on the layer's stream; the amax of x runs on a side "
                        "stream beside the routing and the padding-row clear beside the quantization of x (the "
                        "*_wait stages are what is left of them)",
         "roofline": {"kernel": "single_gemm_kernel<fp4> (gate_up, SwiGLU)", "bound": "tensor",
@@ -319,6 +340,9 @@ def run_ours(args):
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(x.numel() * 2 + logits.numel() * 4),
                 "d2h_bytes_per_step": int(T * H * 4),
                 "overlap": "double-buffered: step i+1 H2D and step i D2H on copy streams beside step i's compute"},
+        "eager": {"ms_per_step": round(eager_ms, 4), "value": round(job_value(f4 + fb, world, eager_ms) / 1e12, 2),
+                  "unit": "TFLOP/s", "what": "the same step launched eagerly with CUDA events between its stages "
+                                            "(where stages_ms comes from); the timed step replays it as one CUDA graph"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -332,6 +356,28 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def graph_step_ms(layer, x, logits, steps, stream):
+    """The layer step as a CUDA-graph replay (RolloutMoE.capture: the same
+    launches, issued at once, no per-stage events): ms per step over `steps`
+    replays after three, the replayed output checked against an eager forward."""
+    import torch
+
+    graph, out = layer.capture(x, logits)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    assert int(layer.dev_status.item()) == 0
+    got = out.clone()
+    assert torch.equal(got, layer.forward(x, logits))
+    return g0.elapsed_time(g1) / steps
 
 
 def decode_measure(dev, steps, pk):
@@ -372,8 +418,10 @@ def decode_measure(dev, steps, pk):
     g_bytes = w_bytes + a_bytes + o_bytes
     g_ms = stage["gemm_gate_up"] + stage["gemm_down"]
     f4, fb = synth.flops_moe(3)
+    graph_ms = graph_step_ms(layer, x, logits, steps, stream)
     return {"workload": "moe_decode T=2048 H=2048 E=64 top8 I=768 k=64", "ms_per_step": round(ms, 4),
             "tflops": round((f4 + fb) / (ms * 1e-3) / 1e12, 1),
+            "graph_ms_per_step": round(graph_ms, 4), "graph_tflops": round((f4 + fb) / (graph_ms * 1e-3) / 1e12, 1),
             "stages_ms": {n: round(v, 4) for n, v in stage.items()},
             "gemm_bytes": g_bytes, "gemm_gbs": round(g_bytes / (g_ms * 1e-3) / 1e9, 1),
             "gemm_hbm_frac": round(g_bytes / (g_ms * 1e-3) / 1e9 / pk["hbm"], 4),

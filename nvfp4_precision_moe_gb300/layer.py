@@ -215,6 +215,19 @@ class RolloutMoE:
         mark(8)
         return out
 
+    def capture(self, x, logits, out=None):
+        """Records one forward on the buffers x [T, H], logits [T, E] (and
+        `out`, as for forward) into a CUDA graph, after one eager forward that
+        does the library's one-time setup.  Returns (graph, out): graph.replay()
+        reruns the whole layer on whatever those buffers then hold, its
+        launches issued at once, and leaves the result in `out`."""
+        self.forward(x, logits, out=out)
+        torch.cuda.synchronize(self.dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            out = self.forward(x, logits, out=out)
+        return g, out
+
 
 class QatMoE:
     """Trainer-side asymmetric-QAT MoE forward (weights fake-quantized, BF16
