@@ -130,6 +130,26 @@ __device__ __forceinline__ void fmul2_rn(float a0, float a1, float b0, float b1,
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
+// (a0, a1) + (b0, b1), (a0, a1) - (b0, b1) and (a0, a1) * (b0, b1) + (c0, c1):
+// two IEEE binary32 operations each (round to nearest), one packed instruction.
+__device__ __forceinline__ void fadd2_rn(float a0, float a1, float b0, float b1, float &r0, float &r1) {
+    asm("{ .reg .b64 x, y, z; mov.b64 x, {%2, %3}; mov.b64 y, {%4, %5}; add.rn.f32x2 z, x, y; mov.b64 {%0, %1}, z; }"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fsub2_rn(float a0, float a1, float b0, float b1, float &r0, float &r1) {
+    asm("{ .reg .b64 x, y, z; mov.b64 x, {%2, %3}; mov.b64 y, {%4, %5}; sub.rn.f32x2 z, x, y; mov.b64 {%0, %1}, z; }"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void ffma2_rn(float a0, float a1, float b0, float b1, float c0, float c1, float &r0,
+                                         float &r1) {
+    asm("{ .reg .b64 x, y, w, z; mov.b64 x, {%2, %3}; mov.b64 y, {%4, %5}; mov.b64 w, {%6, %7};\n"
+        "fma.rn.f32x2 z, x, y, w; mov.b64 {%0, %1}, z; }"
+        : "=f"(r0), "=f"(r1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
 // Per-block tables, filled once per CTA (gs is a power of two, so scaling by
 // it commutes with rounding in the normal range):
 //   div6[m] = fl((1 + m/128) / 6): fl(a / (6 gs)) = div6[mant7(a)] * 2^exp(a) / gs
@@ -908,17 +928,21 @@ __global__ void __launch_bounds__(256) online_score_kernel(const uint16_t *x, in
                 float dq[16];
                 dequant_block_f32(q, gs, dq);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const float d = __fsub_rn(dq[t], v[t]);
-                    pz[t] = __fmaf_rn(d, d, pz[t]);
+                for (int t = 0; t < 16; t += 2) {  // d = dq - v, pz += d * d (pairs of channels)
+                    float d0, d1;
+                    fsub2_rn(dq[t], dq[t + 1], v[t], v[t + 1], d0, d1);
+                    ffma2_rn(d0, d1, d0, d1, pz[t], pz[t + 1], pz[t], pz[t + 1]);
                 }
             }
 #pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                const float y = __fsub_rn(pz[t], comp[t]);
-                const float s2 = __fadd_rn(sum[t], y);
-                comp[t] = __fsub_rn(__fsub_rn(s2, sum[t]), y);
-                sum[t] = s2;
+            for (int t = 0; t < 16; t += 2) {  // compensated sum += pz
+                float y0, y1, s0, s1, e0, e1;
+                fsub2_rn(pz[t], pz[t + 1], comp[t], comp[t + 1], y0, y1);
+                fadd2_rn(sum[t], sum[t + 1], y0, y1, s0, s1);
+                fsub2_rn(s0, s1, sum[t], sum[t + 1], e0, e1);
+                fsub2_rn(e0, e1, y0, y1, comp[t], comp[t + 1]);
+                sum[t] = s0;
+                sum[t + 1] = s1;
             }
         }
     }
@@ -1183,10 +1207,13 @@ __global__ void __launch_bounds__(256) pack_transpose_kernel(const uint8_t *code
 // w_sel[e, n, s] from the channel-major pack: a block covers 128 rows x 64
 // selected channels of one expert; thread (s, quarter) reads the 32 rows'
 // codes of channel S[s] (16 bytes) and their 32 block scales, writes the 32
-// values into a shared tile, and the tile leaves as 128-byte row pieces.
+// values into a shared tile, and the tile leaves as 128-byte row pieces.  The
+// tile's 16-byte column groups are swizzled by the row's quarter (group g of
+// row r sits at g ^ (r / 32)), so the four quarters' writes of one column fall
+// in different banks.
 __global__ void __launch_bounds__(256) gather_wsel_t_kernel(const uint8_t *codes_t, const uint8_t *scales_t, int64_t N,
                                                            int64_t K, const int32_t *S, int32_t k, uint16_t *wsel) {
-    __shared__ __align__(16) uint16_t tile[128][64 + 8];  // [row][selected channel]
+    __shared__ __align__(16) uint16_t tile[128][64];  // [row][selected channel, groups swizzled]
     const int64_t e = blockIdx.z, n0 = (int64_t)blockIdx.y * 128;
     const int s0 = blockIdx.x * 64;
     const int64_t nb = K >> 4;
@@ -1200,11 +1227,12 @@ __global__ void __launch_bounds__(256) gather_wsel_t_kernel(const uint8_t *codes
             const uint4 s_lo = __ldg(reinterpret_cast<const uint4 *>(sc)), s_hi = __ldg(reinterpret_cast<const uint4 *>(sc) + 1);
             const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
             const uint32_t sw[8] = {s_lo.x, s_lo.y, s_lo.z, s_lo.w, s_hi.x, s_hi.y, s_hi.z, s_hi.w};
+            const int col = sl ^ (8 * q);  // this channel's column in the swizzled rows of quarter q
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 const uint32_t code = (cw[i >> 3] >> (4 * (i & 7))) & 15u;
                 const uint32_t sb = (sw[i >> 2] >> (8 * (i & 3))) & 0xffu;
-                tile[32 * q + i][sl] =
+                tile[32 * q + i][col] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(__fmul_rn(e2m1_to_f32_hw(code), e4m3_to_f32(sb))));
             }
         }
@@ -1215,7 +1243,7 @@ __global__ void __launch_bounds__(256) gather_wsel_t_kernel(const uint8_t *codes
     for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
         const int r = i >> 3, p = i & 7;
         if (8 * p < nsel) {  // k % 8 == 0: whole 16-byte pieces
-            const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][8 * p]);
+            const uint4 v = *reinterpret_cast<const uint4 *>(&tile[r][8 * (p ^ (r >> 5))]);
             *reinterpret_cast<uint4 *>(wsel + (e * N + n0 + r) * k + s0 + 8 * p) = v;
         }
     }
