@@ -313,8 +313,8 @@ def run_ours(args):
     R = T * c["topk"]
     q_bytes = 2 * T * H + R * (H // 2 + H // 16 + 2 * k)  # read x, write routed codes/scales/residual
     q_gbs = q_bytes / (stage["quantize_x"] * 1e-3) / 1e9
-    rows_h = layer.rows_cap
-    qh_bytes = rows_h * (2 * I + I // 2 + I // 16 + 2 * k)  # read h (all rows_cap rows), write codes/scales/residual
+    rows_h = int(layer.route.offsets[-1].item())  # the routed rows up to the last segment's end
+    qh_bytes = rows_h * (2 * I + I // 2 + I // 16 + 2 * k)  # read h's routed rows, write codes/scales/residual
     qh_gbs = qh_bytes / (stage["quantize_h"] * 1e-3) / 1e9
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -122,6 +122,11 @@ int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensor
  *               of Eq. 20 -- in units of gs: bf16(r * (1/gs)), which is r/gs
  *               exactly (gs is a power of two) unless it falls below the BF16
  *               normal range.  The GEMM multiplies it by gs again.
+ *   row_limit   device int32 or NULL: only source rows m < *row_limit (read
+ *               when the kernel runs; clamped to [0, M]) are quantized, later
+ *               rows are neither read nor written.  The MoE layer passes
+ *               offsets + E for its routed h: rows past the last expert segment
+ *               are never read by the grouped GEMM.
  * Per element: block scale sb = e4m3_rn_sat(amax16 / (6*gs)); den = sb*gs;
  * code = e2m1_rn_sat(x * (1/den)) with 1/den correctly rounded (a zero den
  * gives a signed zero code); dequant = (code*sb)*gs in binary32.
@@ -133,7 +138,7 @@ int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensor
 int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float *amax,
                    float *gs_out, const int32_t *S, int32_t k, const int32_t *dst_row,
                    int32_t fanout, int64_t rows_out, uint8_t *codes, uint8_t *scales,
-                   void *resid, int32_t *dev_status, void *stream);
+                   void *resid, const int32_t *row_limit, int32_t *dev_status, void *stream);
 
 /* Trainer-side weight fake-quantization QDQ_W of QUADS §3.2 Eq. 12:
  * w_hat = bf16((code*sb)*gs) for `ntensors` BF16 weights of rows x cols,

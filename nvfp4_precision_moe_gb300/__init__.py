@@ -29,7 +29,7 @@ STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED",
 _SIGS = {
     "nvfp4_init": "",
     "nvfp4_amax": "pqqqiqpp",
-    "nvfp4_quantize": "pqqqpppipiqppppp",
+    "nvfp4_quantize": "pqqqpppipiqpppppp",
     "nvfp4_fake_quant": "piqqppppp",
     "nvfp4_fake_quant_noalloc": "piqqpppp",
     "nvfp4_fake_quant_transposed": "piqqpppppp",
@@ -129,15 +129,16 @@ def nvfp4_amax(x, amax_out, ntensors=1, stream=None):
 
 
 def nvfp4_quantize(x, amax, codes, scales, resid=None, S=None, gs_out=None, dst_row=None,
-                   fanout=1, rows_out=None, dev_status=None, stream=None):
-    """A1-A5, A9: NVFP4 codes, block scales and the RAC residual of x [M, K]."""
+                   fanout=1, rows_out=None, row_limit=None, dev_status=None, stream=None):
+    """A1-A5, A9: NVFP4 codes, block scales and the RAC residual of x [M, K]
+    (rows below the device int32 *row_limit only, if given)."""
     M, K = x.shape
     k = 0 if S is None else S.numel()
     if rows_out is None:
         rows_out = codes.shape[0]
     _call("nvfp4_quantize", _p(x), M, K, x.stride(0), _p(amax), _p(gs_out), _p(S), k,
-          _p(dst_row), fanout, rows_out, _p(codes), _p(scales), _p(resid), _p(dev_status),
-          _s(stream))
+          _p(dst_row), fanout, rows_out, _p(codes), _p(scales), _p(resid), _p(row_limit),
+          _p(dev_status), _s(stream))
 
 
 def nvfp4_fake_quant(w, w_hat, amax_ws, gs_out=None, dev_status=None, stream=None):

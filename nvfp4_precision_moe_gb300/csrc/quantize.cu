@@ -38,6 +38,7 @@ struct QuantArgs {
     uint16_t *wsel;          // weight mode: [rows, k] per tensor
     int64_t wsel_tstride;
     int32_t interleave;
+    const int32_t *row_limit;  // act mode, or null: source rows at or past *row_limit are skipped
     int32_t *dev_status;
 };
 
@@ -364,7 +365,9 @@ __global__ void __launch_bounds__(kQThreads, q_blocks_per_sm<MODE>()) quantize_k
     uint8_t *ring = q_ring + (size_t)wid * kQSlots * 1024;
     uint64_t *bars = s_qbar[wid];
     const int64_t first = (int64_t)blockIdx.x * kQWarps + wid;
-    const int64_t nrows = first < a.M ? (a.M - 1 - first) / nwarps_total + 1 : 0;
+    // source rows [0, Mq): all M, or those below the caller's device-side bound
+    const int64_t Mq = a.row_limit ? min(a.M, (int64_t)max(__ldg(a.row_limit), 0)) : a.M;
+    const int64_t nrows = first < Mq ? (Mq - 1 - first) / nwarps_total + 1 : 0;
     const int64_t nseg = nrows * segs;
     int64_t pm = first, pj = 0;
     int pseg = 0;
@@ -1561,7 +1564,8 @@ extern "C" int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int3
 
 extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, const float *amax, float *gs_out,
                               const int32_t *S, int32_t k, const int32_t *dst_row, int32_t fanout, int64_t rows_out,
-                              uint8_t *codes, uint8_t *scales, void *resid, int32_t *dev_status, void *stream) {
+                              uint8_t *codes, uint8_t *scales, void *resid, const int32_t *row_limit,
+                              int32_t *dev_status, void *stream) {
     if (!x || !amax || !codes || !scales || M < 0 || K < 0 || ldx < K || k < 0 || k > K || fanout < 1)
         return NVFP4_ERR_INVALID_ARG;
     if (k > 0 && (!S || !resid)) return NVFP4_ERR_INVALID_ARG;
@@ -1588,6 +1592,7 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
     a.codes = codes;
     a.scales = scales;
     a.resid = (uint16_t *)resid;
+    a.row_limit = row_limit;
     a.dev_status = dev_status;
     return launch_quantize<kModeAct>(dim3(quant_grid<kModeAct>(M)), a, (cudaStream_t)stream, "quantize_kernel");
 }

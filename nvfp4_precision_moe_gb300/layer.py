@@ -195,9 +195,10 @@ class RolloutMoE:
                                              E=self.E, stream=main)
             W = self.wd
             nvfp4_gather_selected_weights_t(W.codes_t, W.scales_t, self.E, W.N, W.K, self.Sd, W.sel, stream=main)
+        # the routed rows of h only: the down GEMM reads no row past the last expert segment
         nvfp4_quantize(self.h, ha.amax, ha.codes, ha.scales, resid=ha.resid if self.kd else None,
-                       S=self.Sd if self.kd else None, gs_out=ha.gs, dev_status=self.dev_status,
-                       stream=main)
+                       S=self.Sd if self.kd else None, gs_out=ha.gs, row_limit=r.offsets[self.E:],
+                       dev_status=self.dev_status, stream=main)
         if self.resid_fp4 and self.kd:
             nvfp4_rac_requant_residual(ha.resid, self.resid_amax[1:2], r.offsets, self.E, gs_out=self.resid_gs[1:2],
                                        dev_status=self.dev_status, stream=main)

@@ -75,14 +75,14 @@ PM = 0x10008  # misaligned
 
 def test_host_checks_without_gpu(lib):
     q = lib.nvfp4_quantize
-    # x, M, K, ldx, amax, gs, S, k, dst, fanout, rows_out, codes, scales, resid, status, stream
-    assert q(None, 4, 64, 64, P, None, None, 0, None, 1, 4, P, P, None, None, None) == INVALID
-    assert q(P, 4, 48, 48, P, None, None, 0, None, 1, 4, P, P, None, None, None) == UNSUP  # K % 32
-    assert q(PM, 4, 64, 64, P, None, None, 0, None, 1, 4, P, P, None, None, None) == ALIGN
-    assert q(P, 4, 64, 64, P, None, P, 8, None, 1, 4, P, P, None, None, None) == INVALID  # k>0, no resid
-    assert q(P, 4, 64, 64, P, None, None, 0, None, 2, 4, P, P, None, None, None) == INVALID  # fanout w/o map
+    # x, M, K, ldx, amax, gs, S, k, dst, fanout, rows_out, codes, scales, resid, row_limit, status, stream
+    assert q(None, 4, 64, 64, P, None, None, 0, None, 1, 4, P, P, None, None, None, None) == INVALID
+    assert q(P, 4, 48, 48, P, None, None, 0, None, 1, 4, P, P, None, None, None, None) == UNSUP  # K % 32
+    assert q(PM, 4, 64, 64, P, None, None, 0, None, 1, 4, P, P, None, None, None, None) == ALIGN
+    assert q(P, 4, 64, 64, P, None, P, 8, None, 1, 4, P, P, None, None, None, None) == INVALID  # k>0, no resid
+    assert q(P, 4, 64, 64, P, None, None, 0, None, 2, 4, P, P, None, None, None, None) == INVALID  # fanout w/o map
     # a row's destinations live in 32 per-warp slots: more than 32 is refused before any launch
-    assert q(P, 4, 64, 64, P, None, None, 0, P, 33, 4 * 33, P, P, None, None, None) == UNSUP
+    assert q(P, 4, 64, 64, P, None, None, 0, P, 33, 4 * 33, P, P, None, None, None, None) == UNSUP
     fq = lib.nvfp4_fake_quant_noalloc
     # w, ntensors, rows, cols, w_hat, gs_out, dev_status, stream
     assert fq(P, 2, 16, 48, P, None, None, None) == UNSUP  # cols % 32

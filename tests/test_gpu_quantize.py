@@ -12,6 +12,7 @@ import torch
 import oracle
 import synth
 from tests import _gpu as G
+from tests.test_oracle_quant import _rand_x
 
 pytestmark = pytest.mark.gpu
 
@@ -288,6 +289,37 @@ def test_channel_selection_parity(cfg):
     assert np.array_equal(S.cpu().numpy(), oracle.select_channels(ssq, k))
     # the seeded outlier channels are among the selected ones
     assert set(synth.outlier_channels(cfg).tolist()) <= set(S.cpu().tolist())
+
+
+@pytest.mark.parametrize("limit", [0, 1, 131, 300, 400, -5])
+def test_row_limit(limit):
+    """With a device-side row bound only the source rows below it are
+    quantized (bit-exact against the oracle, which quantizes those rows with
+    the whole tensor's amax); codes, scales and residuals of later rows are
+    never written (their sentinel bytes survive).  The bound is clamped to
+    [0, M]."""
+    M, K = 300, 512
+    x = _rand_x(M, K, seed=90)
+    S = np.array([3, 17, 200, 201, 300, 301, 302, 511], np.int32)
+    xd = G.bf16_from_u16(x)
+    amax = G.zeros(1, torch.float32)
+    nv.nvfp4_amax(xd, amax)
+    codes = torch.full((M, K // 2), 0xAB, dtype=torch.uint8, device=G.DEV)
+    scales = torch.full((oracle.scale_bytes(M, K),), 0xAB, dtype=torch.uint8, device=G.DEV)
+    resid = torch.full((M, len(S)), 7.0, dtype=torch.bfloat16, device=G.DEV)
+    lim = torch.tensor([limit], dtype=torch.int32, device=G.DEV)
+    Sd = torch.tensor(S, dtype=torch.int32, device=G.DEV)
+    nv.nvfp4_quantize(xd, amax, codes, scales, resid=resid, S=Sd, row_limit=lim)
+    torch.cuda.synchronize()
+    n = min(max(limit, 0), M)
+    c_ref, s_ref, r_ref, _ = oracle.quantize(x, S=S)
+    got_c, got_s, got_r = codes.cpu().numpy(), scales.cpu().numpy(), G.u16(resid)
+    assert np.array_equal(got_c[:n], c_ref[:n]) and (got_c[n:] == 0xAB).all()
+    assert np.array_equal(got_r[:n], r_ref[:n])
+    assert (resid[n:].float().cpu().numpy() == 7.0).all()
+    rows = np.arange(M)
+    sc = oracle.scale_rows(got_s, rows, K)
+    assert np.array_equal(sc[:n], s_ref[:n]) and (sc[n:] == 0xAB).all()
 
 
 @pytest.mark.parametrize("k", [3, 16, 40, 100])
