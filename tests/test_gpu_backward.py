@@ -259,17 +259,19 @@ def test_qat_layer_backward_stage_by_stage(nv):
     dst = r.dst_row.cpu().numpy()[:T]
     rw = r.weights.cpu().numpy()[:T].astype(np.float64)
     Rl = int(offs[-1])
-    W13, Wd = f64(layer.w13_hat), f64(layer.wd_hat)
     xr, gu, h, y = f64(layer.xr)[:Rl], f64(layer.gu)[:Rl], f64(layer.h)[:Rl], f64(layer.y)[:Rl]
 
-    def per_expert(a, Wt):  # rows of expert e times Wt[e]
-        o = np.zeros((Rl, Wt.shape[1]))
+    def per_expert(a, w_of):  # the BF16 rows of expert e times w_of(e) [N, K]^T: oracle.bf16_gemm
+        n = w_of(0).shape[0]
+        o = np.zeros((Rl, n))
         for e in range(E):
-            o[offs[e]:offs[e + 1]] = a[offs[e]:offs[e + 1]] @ Wt[e].T
+            r0, r1 = int(offs[e]), int(offs[e + 1])
+            if r1 > r0:
+                o[r0:r1] = oracle.bf16_gemm(G.u16(a[r0:r1]), G.u16(w_of(e)))
         return o
 
     # forward with saved pre-activations
-    assert G.rel_err(gu, per_expert(xr, W13)) <= TOL_BF16
+    assert G.rel_err(gu, per_expert(layer.xr, lambda e: layer.w13_hat[e])) <= TOL_BF16
     assert np.all(np.abs(h - oracle.swiglu(gu, I)) <= 2.0 ** -8 * np.abs(oracle.swiglu(gu, I)) + 1e-5)
     assert G.rel_err(f64(out), oracle.combine(y, dst.astype(np.int32), rw)) <= 1e-5
     # backward
@@ -281,10 +283,10 @@ def test_qat_layer_backward_stage_by_stage(nv):
     # d(gate|up): the SwiGLU gradient of dh = dY . Wd_hat, which the GEMM's epilogue rounds to BF16
     # (the oracle's product may round to the neighbouring BF16 value: one more 2^-8)
     dgu = f64(layer.dgu)[:Rl]
-    ref_dgu = oracle.swiglu_grad(gu, bf16_of(per_expert(dy, np.transpose(Wd, (0, 2, 1)))))
+    ref_dgu = oracle.swiglu_grad(gu, bf16_of(per_expert(layer.dy, lambda e: layer.wd_hat[e].t().contiguous())))
     assert G.rel_err(dgu, ref_dgu) <= 2.0 ** -7 + 1e-3
     dxr = f64(layer.dxr)[:Rl]
-    assert G.rel_err(dxr, per_expert(dgu, np.transpose(W13, (0, 2, 1)))) <= TOL_BF16
+    assert G.rel_err(dxr, per_expert(layer.dgu, lambda e: layer.w13_hat[e].t().contiguous())) <= TOL_BF16
     assert G.rel_err(f64(dw13), oracle.segment_wgrad(dgu, xr, offs)) <= 1e-5
     assert not f64(dw13)[3].any() and not f64(dwd)[3].any()
     assert G.rel_err(f64(dx), oracle.combine(dxr, dst.astype(np.int32), np.ones(dst.shape))) <= 1e-5
