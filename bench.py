@@ -305,6 +305,17 @@ def run_ours(args):
     e2e_ms = job_time(e0.elapsed_time(e1), world, dev) / args.steps
     assert int(layer.dev_status.item()) == 0
     assert torch.equal(oh[(args.steps - 1) % 2], layer.forward(x, logits).cpu())
+    # the host link's own copy rates on this machine (each copy alone, three times): the e2e step
+    # hides its copies only while the FP32 output's download is shorter than the step
+    link = {}
+    for name, dst, src in (("d2h", oh[0], od[0]), ("h2d", xd[0], xh)):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(3):
+            dst.copy_(src, non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        link[name + "_gbs"] = round(3 * src.numel() * src.element_size() / (c0.elapsed_time(c1) * 1e6), 1)
 
     pk = peaks()
     fp4_peak = pk["bf16"] * NOMINAL_FP4_OVER_BF16
@@ -339,7 +350,8 @@ def run_ours(args):
         "e2e": {"value": round(world * (f4 + fb) / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(x.numel() * 2 + logits.numel() * 4),
                 "d2h_bytes_per_step": int(T * H * 4),
-                "overlap": "double-buffered: step i+1 H2D and step i D2H on copy streams beside step i's compute"},
+                "overlap": "double-buffered: step i+1 H2D and step i D2H on copy streams beside step i's compute",
+                "link": link},
         "eager": {"ms_per_step": round(eager_ms, 4), "value": round(job_value(f4 + fb, world, eager_ms) / 1e12, 2),
                   "unit": "TFLOP/s", "what": "the same step launched eagerly with CUDA events between its stages "
                                             "(where stages_ms comes from); the timed step replays it as one CUDA graph"},
