@@ -19,6 +19,10 @@
  *    synchronizes.  Outputs are valid once the stream reaches them.
  *  - BF16 is passed as `void*` holding IEEE bfloat16 bit patterns.
  *  - Device pointers must be 16-byte aligned (NVFP4_ERR_ALIGNMENT otherwise).
+ *  - A batch of no tokens is valid: the token-sized buffers of nvfp4_amax,
+ *    nvfp4_quantize, nvfp4_route_topk, nvfp4_moe_scatter_rows,
+ *    nvfp4_moe_combine, nvfp4_moe_combine_backward and
+ *    nvfp4_rac_select_channels_online may be NULL when they hold no element.
  *  - There is no CPU path: without an sm_103 device every call returns
  *    NVFP4_ERR_ARCH.
  *

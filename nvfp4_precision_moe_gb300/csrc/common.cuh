@@ -33,6 +33,8 @@ int encode_tmap_2d(CUtensorMap *map, CUtensorMapDataType dtype, void *base, uint
                    CUtensorMapSwizzle swz);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+// A buffer of n elements that is needed but absent (a buffer of none may be null).
+inline bool missing(const void *p, int64_t n) { return p == nullptr && n > 0; }
 
 inline int launch_status(const char *what) {
     cudaError_t e = cudaGetLastError();

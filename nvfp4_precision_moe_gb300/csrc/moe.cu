@@ -314,7 +314,8 @@ extern "C" int nvfp4_mismatch_norm(const float *y_infer, const float *y_train, i
 
 extern "C" int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32_t topk, int32_t *ids, float *weights,
                                 int32_t *counts, int32_t *offsets, int32_t *dst_row, void *stream) {
-    if (!logits || !ids || !weights || !counts || !offsets || !dst_row || T < 0 || E < 1 || topk < 1)
+    if (missing(logits, T) || missing(ids, T) || missing(weights, T) || !counts || !offsets || missing(dst_row, T) ||
+        T < 0 || E < 1 || topk < 1)
         return NVFP4_ERR_INVALID_ARG;
     if (topk > 32 || topk > E || E > 1024) return NVFP4_ERR_UNSUPPORTED;
     NVFP4_CHECK_INIT();
@@ -339,7 +340,9 @@ extern "C" int nvfp4_route_topk(const float *logits, int32_t T, int32_t E, int32
 
 extern "C" int nvfp4_moe_combine(const void *y, int32_t y_dtype, int64_t ldy, const int32_t *dst_row,
                                  const float *weights, int32_t T, int32_t topk, int64_t H, float *out, void *stream) {
-    if (!y || !dst_row || !weights || !out || T < 0 || topk < 1 || H < 0 || ldy < H) return NVFP4_ERR_INVALID_ARG;
+    if (missing(y, (int64_t)T * H) || missing(dst_row, T) || missing(weights, T) || missing(out, (int64_t)T * H) || T < 0 ||
+        topk < 1 || H < 0 || ldy < H)
+        return NVFP4_ERR_INVALID_ARG;
     if (y_dtype != NVFP4_OUT_F32 && y_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
     if (H % 8 || ldy % 8) return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(y) || !aligned16(out)) return NVFP4_ERR_ALIGNMENT;

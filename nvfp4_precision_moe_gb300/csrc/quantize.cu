@@ -1554,7 +1554,8 @@ using namespace nvfp4;
 
 extern "C" int nvfp4_amax(const void *x, int64_t M, int64_t K, int64_t ldx, int32_t ntensors, int64_t tensor_stride,
                           float *amax_out, void *stream) {
-    if (!x || !amax_out || M < 0 || K < 0 || ldx < K || ntensors < 1 || tensor_stride < 0) return NVFP4_ERR_INVALID_ARG;
+    if (missing(x, M * K) || !amax_out || M < 0 || K < 0 || ldx < K || ntensors < 1 || tensor_stride < 0)
+        return NVFP4_ERR_INVALID_ARG;
     if (ntensors > 65535) return NVFP4_ERR_UNSUPPORTED;
     if (K % 8) return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(x) || ldx % 8 || tensor_stride % 8) return NVFP4_ERR_ALIGNMENT;
@@ -1566,10 +1567,11 @@ extern "C" int nvfp4_quantize(const void *x, int64_t M, int64_t K, int64_t ldx, 
                               const int32_t *S, int32_t k, const int32_t *dst_row, int32_t fanout, int64_t rows_out,
                               uint8_t *codes, uint8_t *scales, void *resid, const int32_t *row_limit,
                               int32_t *dev_status, void *stream) {
-    if (!x || !amax || !codes || !scales || M < 0 || K < 0 || ldx < K || k < 0 || k > K || fanout < 1)
+    if (missing(x, M * K) || !amax || missing(codes, rows_out * K) || missing(scales, rows_out * K) || M < 0 || K < 0 ||
+        ldx < K || k < 0 || k > K || fanout < 1)
         return NVFP4_ERR_INVALID_ARG;
-    if (k > 0 && (!S || !resid)) return NVFP4_ERR_INVALID_ARG;
-    if (!dst_row && (fanout != 1 || rows_out < M)) return NVFP4_ERR_INVALID_ARG;
+    if (k > 0 && (!S || missing(resid, rows_out))) return NVFP4_ERR_INVALID_ARG;
+    if (!dst_row && M > 0 && (fanout != 1 || rows_out < M)) return NVFP4_ERR_INVALID_ARG;
     // a row's destinations are resolved into 32 per-warp slots
     if (K % 32 || k % 8 || K / 16 > kMaxBlocksPerRow || fanout > 32 || M > INT32_MAX || rows_out > INT32_MAX)
         return NVFP4_ERR_UNSUPPORTED;
@@ -1714,7 +1716,7 @@ extern "C" int nvfp4_rac_requant_residual(void *resid, int64_t rows_cap, int32_t
 extern "C" int nvfp4_rac_select_channels_online(const void *x, int64_t rows_cap, int64_t K, const int32_t *offsets,
                                                 int32_t E, const float *amax, int32_t k, int32_t *S_out,
                                                 double *score_ws, void *stream) {
-    if (!x || !amax || !score_ws || rows_cap < 0 || K < 0 || k < 0 || (offsets && E < 1))
+    if (missing(x, rows_cap * K) || !amax || !score_ws || rows_cap < 0 || K < 0 || k < 0 || (offsets && E < 1))
         return NVFP4_ERR_INVALID_ARG;
     if (k > 0 && !S_out) return NVFP4_ERR_INVALID_ARG;
     if (K % 16 || K > 16384 || k > K) return NVFP4_ERR_UNSUPPORTED;
@@ -1806,7 +1808,8 @@ extern "C" int nvfp4_moe_clear_padding(const int32_t *counts, const int32_t *off
 extern "C" int nvfp4_moe_scatter_rows(const void *x, int32_t T, int64_t K, int32_t topk, const int32_t *dst_row,
                                       const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,
                                       void *y, void *stream) {
-    if (!x || !dst_row || !counts || !offsets || !y || T < 0 || K < 0 || topk < 1 || E < 1 || rows_cap < 0)
+    if (missing(x, (int64_t)T * K) || missing(dst_row, T) || !counts || !offsets || missing(y, rows_cap * K) || T < 0 ||
+        K < 0 || topk < 1 || E < 1 || rows_cap < 0)
         return NVFP4_ERR_INVALID_ARG;
     if (K % 8 || E > 65535) return NVFP4_ERR_UNSUPPORTED;
     if (!aligned16(x) || !aligned16(y)) return NVFP4_ERR_ALIGNMENT;

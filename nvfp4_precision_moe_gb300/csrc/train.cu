@@ -366,8 +366,8 @@ extern "C" int nvfp4_moe_combine_backward(const float *dout, const void *y, cons
                                           const float *weights, int32_t T, int32_t topk, int64_t H,
                                           const int32_t *counts, const int32_t *offsets, int32_t E, int64_t rows_cap,
                                           void *dy, float *dweights, void *stream) {
-    if (!dout || !y || !dst_row || !weights || !counts || !offsets || !dy || T < 0 || topk < 1 || H < 0 || E < 1 ||
-        rows_cap < 0)
+    if (missing(dout, (int64_t)T * H) || missing(y, rows_cap * H) || missing(dst_row, T) || missing(weights, T) || !counts ||
+        !offsets || missing(dy, rows_cap * H) || T < 0 || topk < 1 || H < 0 || E < 1 || rows_cap < 0)
         return NVFP4_ERR_INVALID_ARG;
     if (E > 65535 || H % 8 || H > 8 * 256 * kCombineBwdMaxVec || topk > kCombineBwdMaxTopk)
         return NVFP4_ERR_UNSUPPORTED;

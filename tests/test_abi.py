@@ -156,6 +156,24 @@ def test_host_checks_of_the_trainer_and_online_entry_points(lib):
     assert cb(P, P, P, P, 4, 33, 64, P, P, 2, 256, P, None, None) == UNSUP  # topk > 32
 
 
+def test_empty_batch_buffers_may_be_null(lib):
+    """A batch of no tokens passes the argument checks with NULL token-sized
+    buffers (on a machine without an sm_103 device the call then stops at the
+    architecture check; nothing is dereferenced)."""
+    ok = (OK, ARCH)
+    # x, M, K, ldx, ntensors, tensor_stride, amax_out, stream
+    assert lib.nvfp4_amax(None, 0, 64, 64, 1, 0, P, None) in ok
+    # x, M, K, ldx, amax, gs, S, k, dst, fanout, rows_out, codes, scales, resid, row_limit, status, stream
+    assert lib.nvfp4_quantize(None, 0, 64, 64, P, None, P, 8, None, 8, 128, P, P, P, None, None, None) in ok
+    # logits, T, E, topk, ids, weights, counts, offsets, dst_row, stream
+    assert lib.nvfp4_route_topk(None, 0, 16, 4, None, None, P, P, None, None) in ok
+    # y, y_dtype, ldy, dst_row, weights, T, topk, H, out, stream
+    assert lib.nvfp4_moe_combine(P, 1, 64, None, None, 0, 4, 64, None, None) in ok
+    # with tokens the same buffers are required
+    assert lib.nvfp4_route_topk(None, 3, 16, 4, None, None, P, P, None, None) == INVALID
+    assert lib.nvfp4_moe_combine(P, 1, 64, None, None, 3, 4, 64, None, None) == INVALID
+
+
 def test_gemm_pipeline_selector(lib):
     prev = ctypes.c_int32(-1)
     assert lib.nvfp4_gemm_pipeline(7, None) == INVALID

@@ -238,6 +238,23 @@ def test_input_gradient_with_fused_swiglu_backward(nv, pipe):
     assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-5)
 
 
+def test_qat_layer_empty_batch(nv):
+    """The training layer on a batch of no tokens: an empty output and input
+    gradient, and zero weight gradients for every expert."""
+    from tests.test_oracle_mismatch import small_moe
+
+    x, logits, w13, wd = small_moe()
+    dev = lambda a: torch.as_tensor(a).to(G.DEV)
+    E, N13, H = w13.shape
+    layer = nv.QatMoE(dev(w13), dev(wd), 2, x.shape[0], fake=True, train=True)
+    out = layer.forward(dev(x)[:0], dev(logits)[:0])
+    dx, dw13, dwd, dweights = layer.backward(torch.zeros((0, H), dtype=torch.float32, device=G.DEV))
+    torch.cuda.synchronize()
+    G.status_ok(layer.dev_status)
+    assert out.shape == (0, H) and dx.shape == (0, H) and dweights.shape == (0, 2)
+    assert not dw13.any().item() and not dwd.any().item()
+
+
 def test_qat_layer_backward_stage_by_stage(nv):
     from tests.test_oracle_mismatch import small_moe
 

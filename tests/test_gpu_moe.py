@@ -116,8 +116,30 @@ def _seeded_channels(K, k, seed):
     return torch.sort(torch.randperm(K, generator=g)[:k]).values.to(torch.int32).numpy()
 
 
-def test_rollout_layer_end_to_end_reduced():
+def test_rollout_layer_empty_batch():
+    """A batch of no tokens leaves nothing to route: the forward returns an
+    empty output without error, and the next batch is unaffected (its output
+    equals a fresh layer's)."""
     cfg, T = 3, 64
+    c, x, logits, w13, wd = _layer_inputs(cfg, T)
+    S13, Sd = _seeded_channels(c["H"], c["k"], 5), _seeded_channels(c["I"], c["k"], 6)
+    mk = lambda: nv.RolloutMoE(w13.to(G.DEV), wd.to(G.DEV), torch.from_numpy(S13).to(G.DEV),
+                               torch.from_numpy(Sd).to(G.DEV), c["topk"], T)
+    layer = mk()
+    xd, ld = x.to(G.DEV), logits.to(G.DEV)
+    out = layer.forward(xd[:0], ld[:0])
+    torch.cuda.synchronize()
+    G.status_ok(layer.dev_status)
+    assert out.shape == (0, c["H"])
+    got = layer.forward(xd, ld).clone()
+    ref = mk().forward(xd, ld)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("T", [1, 64])
+def test_rollout_layer_end_to_end_reduced(T):
+    cfg = 3
     c, x, logits, w13, wd = _layer_inputs(cfg, T)
     E, H, I, topk, k = c["E"], c["H"], c["I"], c["topk"], c["k"]
     S13 = oracle.select_channels(oracle.channel_scores_sq(synth.u16(synth.activations(cfg, batch=1)[:256])), k)
