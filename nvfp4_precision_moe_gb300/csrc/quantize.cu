@@ -1424,13 +1424,17 @@ __global__ void __launch_bounds__(256, 4) fake_quant_fused_kernel(FQArgs a) {
             const int64_t nvec = (r1 - r0) * (a.cols >> 3);
             uint32_t mx = 0u;
             int64_t i = threadIdx.x;
-            for (; i + 3 * 256 < nvec; i += 4 * 256) {
-                const uint4 v0 = ld_hint(p + i, keep), v1 = ld_hint(p + i + 256, keep), v2 = ld_hint(p + i + 512, keep),
-                            v3 = ld_hint(p + i + 768, keep);
-                const uint32_t w16[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
-                                          v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+            for (; i + 7 * 256 < nvec; i += 8 * 256) {  // eight 16-byte loads in flight per thread
+                uint4 v[8];
 #pragma unroll
-                for (int u = 0; u < 16; ++u) mx = __vmaxu2(mx, w16[u] & 0x7fff7fffu);
+                for (int u = 0; u < 8; ++u) v[u] = ld_hint(p + i + 256 * u, keep);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    mx = __vmaxu2(mx, v[u].x & 0x7fff7fffu);
+                    mx = __vmaxu2(mx, v[u].y & 0x7fff7fffu);
+                    mx = __vmaxu2(mx, v[u].z & 0x7fff7fffu);
+                    mx = __vmaxu2(mx, v[u].w & 0x7fff7fffu);
+                }
             }
             for (; i < nvec; i += 256) {
                 const uint4 v = ld_hint(p + i, keep);
