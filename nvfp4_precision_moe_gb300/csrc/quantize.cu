@@ -555,13 +555,17 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint16_t *x, int64_t M,
     int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (ldx == K) {
         const uint4 *p = reinterpret_cast<const uint4 *>(xt);
-        for (; i + 3 * stride < total; i += 4 * stride) {
-            uint4 v0 = __ldg(p + i), v1 = __ldg(p + i + stride), v2 = __ldg(p + i + 2 * stride),
-                  v3 = __ldg(p + i + 3 * stride);
-            uint32_t w[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
-                              v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+        for (; i + 7 * stride < total; i += 8 * stride) {  // eight 16-byte loads in flight per thread
+            uint4 v[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) mx = __vmaxu2(mx, w[j] & 0x7fff7fffu);
+            for (int u = 0; u < 8; ++u) v[u] = __ldg(p + i + u * stride);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                mx = __vmaxu2(mx, v[u].x & 0x7fff7fffu);
+                mx = __vmaxu2(mx, v[u].y & 0x7fff7fffu);
+                mx = __vmaxu2(mx, v[u].z & 0x7fff7fffu);
+                mx = __vmaxu2(mx, v[u].w & 0x7fff7fffu);
+            }
         }
         for (; i < total; i += stride) {
             uint4 v = __ldg(p + i);
