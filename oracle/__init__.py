@@ -308,7 +308,7 @@ def route_topk(logits, topk):
 
 
 def route_layout(ids, E, pad=128):
-    """Routed-row layout of the grouped GEMM (a layout choice of this build).
+    """Routed-row layout of the grouped GEMM (a layout choice of this library).
 
     Rows are ordered by (expert, token, slot); each expert's segment starts at
     a multiple of ``pad``.  Returns (counts [E], offsets [E+1] padded row

@@ -286,7 +286,7 @@ void orc_dequantize_f32(const uint8_t *codes, const uint8_t *scales, int64_t M, 
 }
 
 /* Scale layout shared by the quantizer and the block-scaled GEMM, for
- * activations and weights alike (a layout choice of this build: the paper
+ * activations and weights alike (a layout choice of this library: the paper
  * only asks that the rollout quantizer's layout match its GEMM's, §3.2).  The
  * canonical [M, K/16] block scales are grouped by tiles of 128 rows x 16
  * blocks (one 256-element GEMM K-slice), tile (m/128, kb/16) the
