@@ -1199,15 +1199,13 @@ __global__ void __launch_bounds__(256) pack_transpose_kernel(const uint8_t *code
         }
         *reinterpret_cast<uint2 *>(codes_t + (e * K + j0 + c) * (N >> 1) + (n0 >> 1) + 8 * q) = make_uint2(w[0], w[1]);
     }
-    // the tile's 4 blocks of scales: scales_t[e][kb][n0 .. n0 + 64)
-    if (threadIdx.x < 256) {
+    // the tile's 4 blocks of scales (K % 64 == 0: all of them exist): scales_t[e][kb][n0 .. n0 + 64),
+    // one byte per thread
+    {
         const int kb = (int)(j0 >> 4) + (threadIdx.x >> 6), r = threadIdx.x & 63;
-        if (kb < nb) {
-            const int64_t n = n0 + r;
-            const uint8_t *se = scales + e * (N >> 7) * kslices * 2048;
-            scales_t[(e * nb + kb) * N + n] =
-                se[scale_row_offset(n, kslices) + scale_block_offset(kb & ~3) + (kb & 3)];
-        }
+        const int64_t n = n0 + r;
+        const uint8_t *se = scales + e * (N >> 7) * kslices * 2048;
+        scales_t[(e * nb + kb) * N + n] = se[scale_row_offset(n, kslices) + scale_block_offset(kb & ~3) + (kb & 3)];
     }
 }
 
