@@ -77,7 +77,7 @@ typedef enum {
 enum { NVFP4_OUT_F32 = 0, NVFP4_OUT_BF16 = 1 };
 /* Epilogue of the grouped GEMMs: none, SwiGLU of the gate/up product (forward),
  * or the SwiGLU backward of the input-gradient GEMM (nvfp4_bf16_grouped_gemm_dgrad). */
-enum { NVFP4_EPI_NONE = 0, NVFP4_EPI_SWIGLU = 1, NVFP4_EPI_SWIGLU_BWD = 2 };
+enum { NVFP4_EPI_NONE = 0, NVFP4_EPI_SWIGLU = 1, NVFP4_EPI_SWIGLU_BWD = 2, NVFP4_EPI_SWIGLU_SAVE = 3 };
 enum { NVFP4_PIPELINE_AUTO = 0, NVFP4_PIPELINE_SINGLE = 1, NVFP4_PIPELINE_PAIR = 2 };
 
 /* Name of a status code ("NVFP4_OK", ...); never NULL. */
@@ -354,11 +354,16 @@ int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t *a_scales,
  *            order: for SwiGLU, gate rows [0, N/2) then up rows [N/2, N))
  *   offsets  as for nvfp4_w4a4_rac_grouped_gemm
  *   epilogue NVFP4_EPI_NONE: y [rows_cap, N]; NVFP4_EPI_SWIGLU: y =
- *            bf16(silu(gate) * up) [rows_cap, N/2] (out_dtype must be BF16).
+ *            bf16(silu(gate) * up) [rows_cap, N/2] (out_dtype must be BF16);
+ *            NVFP4_EPI_SWIGLU_SAVE: y as for NVFP4_EPI_SWIGLU, and the
+ *            pre-activations bf16(gate | up) -- the NVFP4_EPI_NONE output
+ *            with BF16 out_dtype, bit for bit -- to gu (the learner's
+ *            forward keeps them for the SwiGLU backward of Eq. 13).
+ *   gu       device BF16 [rows_cap, N] for NVFP4_EPI_SWIGLU_SAVE, else NULL
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (K % 64, N % 256, E > 1024). */
 int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const int32_t *offsets, int32_t E,
                             int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype,
-                            int32_t epilogue, void *y, int64_t ldy, int32_t *dev_status,
+                            int32_t epilogue, void *y, int64_t ldy, void *gu, int32_t *dev_status,
                             void *stream);
 
 /* Pipeline of the two grouped GEMMs above (no counterpart in the paper: an

@@ -19,7 +19,7 @@ import torch
 from .build import LIB, build_library
 
 NVFP4_OUT_F32, NVFP4_OUT_BF16 = 0, 1
-NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_EPI_SWIGLU_BWD = 0, 1, 2
+NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_EPI_SWIGLU_BWD, NVFP4_EPI_SWIGLU_SAVE = 0, 1, 2, 3
 NVFP4_PIPELINE_AUTO, NVFP4_PIPELINE_SINGLE, NVFP4_PIPELINE_PAIR = 0, 1, 2
 STATUS = {0: "NVFP4_OK", 1: "NVFP4_ERR_INVALID_ARG", 2: "NVFP4_ERR_UNSUPPORTED",
           3: "NVFP4_ERR_ALIGNMENT", 4: "NVFP4_ERR_CUDA", 5: "NVFP4_ERR_TIMEOUT",
@@ -48,7 +48,7 @@ _SIGS = {
     "nvfp4_bf16_grouped_gemm_wgrad_rows": "pppiqqqippp",
     "nvfp4_bf16_grouped_gemm_dgrad": "pppiqqqiippqpp",
     "nvfp4_w4a4_rac_grouped_gemm": "ppppppppipiqqqiipqppp",
-    "nvfp4_bf16_grouped_gemm": "pppiqqqiipqpp",
+    "nvfp4_bf16_grouped_gemm": "pppiqqqiipqppp",
     "nvfp4_gemm_pipeline": "ip",
     "nvfp4_route_topk": "piiipppppp",
     "nvfp4_moe_clear_padding": "ppiqqipppp",
@@ -226,11 +226,12 @@ def nvfp4_w4a4_rac_grouped_gemm(a_codes, a_scales, a_resid, gs_a, w_codes, w_sca
 
 
 def nvfp4_bf16_grouped_gemm(x, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F32,
-                            epilogue=NVFP4_EPI_NONE, dev_status=None, stream=None):
-    """A17: y = x . w_hat[e]^T per expert segment (BF16 in, FP32 accumulate)."""
+                            epilogue=NVFP4_EPI_NONE, gu=None, dev_status=None, stream=None):
+    """A17: y = x . w_hat[e]^T per expert segment (BF16 in, FP32 accumulate);
+    NVFP4_EPI_SWIGLU_SAVE also stores the BF16 pre-activations to gu."""
     rows_cap = x.shape[0]
     _call("nvfp4_bf16_grouped_gemm", _p(x), _p(w_hat), _p(offsets), E, rows_cap, N, K, out_dtype,
-          epilogue, _p(y), y.stride(0), _p(dev_status), _s(stream))
+          epilogue, _p(y), y.stride(0), _p(gu), _p(dev_status), _s(stream))
 
 
 def nvfp4_bf16_grouped_gemm_dgrad(dy, w_hat, offsets, E, N, K, y, out_dtype=NVFP4_OUT_F32,

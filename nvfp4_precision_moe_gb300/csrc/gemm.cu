@@ -115,15 +115,17 @@ extern "C" int nvfp4_w4a4_rac_grouped_gemm(const uint8_t *a_codes, const uint8_t
 
 extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const int32_t *offsets, int32_t E,
                                        int64_t rows_cap, int64_t N, int64_t K, int32_t out_dtype, int32_t epilogue,
-                                       void *y, int64_t ldy, int32_t *dev_status, void *stream) {
+                                       void *y, int64_t ldy, void *gu, int32_t *dev_status, void *stream) {
     if (!x || !w_hat || !offsets || !y || E < 1 || rows_cap < 0 || N < 0 || K < 0) return NVFP4_ERR_INVALID_ARG;
     if (out_dtype != NVFP4_OUT_F32 && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
-    if (epilogue != NVFP4_EPI_NONE && epilogue != NVFP4_EPI_SWIGLU) return NVFP4_ERR_INVALID_ARG;
-    if (epilogue == NVFP4_EPI_SWIGLU && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
-    if (ldy < (epilogue == NVFP4_EPI_SWIGLU ? N / 2 : N)) return NVFP4_ERR_INVALID_ARG;
+    const bool swiglu = epilogue == NVFP4_EPI_SWIGLU || epilogue == NVFP4_EPI_SWIGLU_SAVE;
+    if (epilogue != NVFP4_EPI_NONE && !swiglu) return NVFP4_ERR_INVALID_ARG;
+    if (swiglu && out_dtype != NVFP4_OUT_BF16) return NVFP4_ERR_INVALID_ARG;
+    if ((epilogue == NVFP4_EPI_SWIGLU_SAVE) != (gu != nullptr)) return NVFP4_ERR_INVALID_ARG;
+    if (ldy < (swiglu ? N / 2 : N)) return NVFP4_ERR_INVALID_ARG;
     if (K % 64 || N % 256 || E > kMaxExperts || rows_cap % 128 || rows_cap > (1ll << 31) || (int64_t)E * N > (1ll << 31))
         return NVFP4_ERR_UNSUPPORTED;
-    if (!aligned16(x) || !aligned16(w_hat) || !aligned16(y) || ldy % 8) return NVFP4_ERR_ALIGNMENT;
+    if (!aligned16(x) || !aligned16(w_hat) || !aligned16(y) || ldy % 8 || !aligned16(gu)) return NVFP4_ERR_ALIGNMENT;
     if (rows_cap == 0 || N == 0 || K == 0) return NVFP4_OK;
     NVFP4_CHECK_INIT();
     CUtensorMap tA, tB;
@@ -146,6 +148,8 @@ extern "C" int nvfp4_bf16_grouped_gemm(const void *x, const void *w_hat, const i
     p.ldy = ldy;
     p.vec32 = (reinterpret_cast<uintptr_t>(y) % 32 == 0) &&
               (ldy * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
+    p.gu_out = (uint16_t *)gu;
+    p.gu_vec32 = (reinterpret_cast<uintptr_t>(gu) % 32 == 0) && (N * 2) % 32 == 0;
     p.dev_status = dev_status;
     return use_pair(false) ? launch_pair_gemm<false>(tA, tB, tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream)
                            : launch_single_gemm<false>(tA, tB, tA, tB, p, rows_cap, N, (cudaStream_t)stream);

@@ -76,6 +76,9 @@ struct GemmParams {
     int32_t a_mn, b_mn;
     // NVFP4_EPI_SWIGLU_BWD (BF16): the saved pre-activations [g | u], [rows_cap, 2N]
     const uint16_t *gu;
+    // NVFP4_EPI_SWIGLU_SAVE (BF16): where the pre-activations go, [rows_cap, N]; gu_vec32: 32-byte aligned
+    uint16_t *gu_out;
+    int32_t gu_vec32;
 };
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -90,6 +93,10 @@ __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fdividef(g, 1.0f + e), u);
 }
 
+// 16 accumulator columns rounded to BF16 (bf16_rn, as the NVFP4_EPI_NONE BF16
+// output) and stored as 32 bytes.
+__device__ __forceinline__ void store_bf16x16(uint16_t *dst, bool vec32, const uint32_t *d);
+
 // 8 words to a 32-byte output segment: one whole-sector store when the
 // output allows it (stores are a large share of the kernel's L2 requests),
 // else two 16-byte stores.
@@ -102,6 +109,13 @@ __device__ __forceinline__ void store32B(void *dst, bool vec32, uint32_t a0, uin
         d[0] = make_uint4(a0, a1, a2, a3);
         d[1] = make_uint4(a4, a5, a6, a7);
     }
+}
+
+__device__ __forceinline__ void store_bf16x16(uint16_t *dst, bool vec32, const uint32_t *d) {
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(__uint_as_float(d[2 * i]), __uint_as_float(d[2 * i + 1]));
+    store32B(dst, vec32, o[0], o[1], o[2], o[3], o[4], o[5], o[6], o[7]);
 }
 
 // 16 columns of this warp's TMEM rows -> 16 BF16 stores (32 bytes), or 16

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int32_t brow = (int32_t)(e * p.N + (int64_t)nt * kBN);
                     // this CTA's B rows: [n0 + 128 rank, +128); for the BF16 SwiGLU the gate
                     // rows [128nt, +128) (leader) or the up rows N/2 + [128nt, +128) (peer)
-                    const bool swiglu_rows = !FP4 && p.epilogue == NVFP4_EPI_SWIGLU;
+                    const bool swiglu_rows = !FP4 && (p.epilogue == NVFP4_EPI_SWIGLU || p.epilogue == NVFP4_EPI_SWIGLU_SAVE);
                     const int32_t brow_mine =
                         swiglu_rows ? (int32_t)(e * p.N + (int64_t)rank * (p.N / 2) + nt * 128) : brow + kBM * (int32_t)rank;
                     for (int it = 0; it < nkt + nrt; ++it) {
@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int row_in_tile = q * 32 + lane;
         const float gsa = FP4 ? *p.gs_a : 1.0f;
-        const bool swiglu = p.epilogue == NVFP4_EPI_SWIGLU;
+        const bool swiglu = p.epilogue == NVFP4_EPI_SWIGLU || p.epilogue == NVFP4_EPI_SWIGLU_SAVE;
         const uint32_t empty_lead = cluster_addr(acc_empty, 0);
         float amax_local = 0.0f;
         int local = 0;
@@ -421,6 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)t.nt * 128 + 64 * half;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) swiglu16(yrow + 16 * j, p.vec32, gmul, v + 16 * j, v + 64 + 16 * j, amax_local);
+                if (!FP4 && p.epilogue == NVFP4_EPI_SWIGLU_SAVE) {
+                    // the pre-activations as well: gate columns 128 nt + 64 half + [0, 64), up N/2 + the same
+                    uint16_t *grow = p.gu_out + row * p.N + (int64_t)t.nt * 128 + 64 * half;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        store_bf16x16(grow + 16 * j, p.gu_vec32, v + 16 * j);
+                        store_bf16x16(grow + p.N / 2 + 16 * j, p.gu_vec32, v + 64 + 16 * j);
+                    }
+                }
             } else if (!FP4 && p.epilogue == NVFP4_EPI_SWIGLU_BWD) {
                 const int64_t col = (int64_t)t.nt * kBN + 128 * half;
 #pragma unroll

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int e = expert_of(s_off, E, m0);
                     const int32_t brow = (int32_t)(e * p.N + (int64_t)nt * kBN);
                     // BF16 SwiGLU: B rows are the gate rows [128nt, +128) and the up rows N/2 + [128nt, +128)
-                    const bool swiglu_rows = !FP4 && p.epilogue == NVFP4_EPI_SWIGLU;
+                    const bool swiglu_rows = !FP4 && (p.epilogue == NVFP4_EPI_SWIGLU || p.epilogue == NVFP4_EPI_SWIGLU_SAVE);
                     const int32_t brow_lo = swiglu_rows ? (int32_t)(e * p.N + nt * 128) : brow;
                     const int32_t brow_hi = swiglu_rows ? (int32_t)(e * p.N + p.N / 2 + nt * 128) : brow + 128;
                     for (int it = 0; it < nkt + nrt; ++it) {
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = (uint32_t)(q * 32) << 16;
         const int row_in_tile = q * 32 + lane;
         const float gsa = FP4 ? *p.gs_a : 1.0f;
-        const bool swiglu = p.epilogue == NVFP4_EPI_SWIGLU;
+        const bool swiglu = p.epilogue == NVFP4_EPI_SWIGLU || p.epilogue == NVFP4_EPI_SWIGLU_SAVE;
         float amax_local = 0.0f;
         int local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
@@ -471,6 +471,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint16_t *yrow = reinterpret_cast<uint16_t *>(p.y) + row * p.ldy + (int64_t)nt * 128 + 64 * half;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) swiglu16(yrow + 16 * j, p.vec32, gmul, v + 16 * j, v + 64 + 16 * j, amax_local);
+                if (!FP4 && p.epilogue == NVFP4_EPI_SWIGLU_SAVE) {
+                    // the pre-activations as well: gate columns 128 nt + 64 half + [0, 64), up N/2 + the same
+                    uint16_t *grow = p.gu_out + row * p.N + (int64_t)nt * 128 + 64 * half;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        store_bf16x16(grow + 16 * j, p.gu_vec32, v + 16 * j);
+                        store_bf16x16(grow + p.N / 2 + 16 * j, p.gu_vec32, v + 64 + 16 * j);
+                    }
+                }
             } else if (!FP4 && p.epilogue == NVFP4_EPI_SWIGLU_BWD) {
                 const int64_t col = (int64_t)nt * kBN + 128 * half;
 #pragma unroll

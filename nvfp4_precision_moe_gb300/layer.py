@@ -15,13 +15,13 @@ combine.
 """
 import torch
 
-from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_EPI_SWIGLU_BWD, NVFP4_OUT_BF16,
+from . import (NVFP4_EPI_NONE, NVFP4_EPI_SWIGLU, NVFP4_EPI_SWIGLU_BWD, NVFP4_EPI_SWIGLU_SAVE, NVFP4_OUT_BF16,
                nvfp4_amax, nvfp4_bf16_grouped_gemm, nvfp4_fake_quant, nvfp4_moe_clear_padding,
                nvfp4_moe_combine, nvfp4_moe_scatter_rows, nvfp4_prepare_weights, nvfp4_quantize,
                nvfp4_bf16_grouped_gemm_dgrad, nvfp4_bf16_grouped_gemm_wgrad_rows, nvfp4_gather_selected_weights_t,
                nvfp4_transpose_weight_pack,
                nvfp4_moe_combine_backward,
-               nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online, nvfp4_route_topk, nvfp4_swiglu,
+               nvfp4_rac_requant_residual, nvfp4_rac_select_channels_online, nvfp4_route_topk,
                nvfp4_w4a4_rac_grouped_gemm)
 
 
@@ -237,8 +237,8 @@ class QatMoE:
     symmetric W4A4 QAT ablation of QUADS §4.3.1 Fig. 7, which fake-quantizes
     the activations x and h as well (one tensor scale each, the rollout's
     NVFP4 recipe).  train=True keeps the gate/up pre-activations (the gate_up
-    GEMM stores them in BF16 and a separate SwiGLU pass makes h) so that
-    backward() can run (QUADS §3.2 Eq. 13)."""
+    GEMM's epilogue stores them in BF16 beside h) so that backward() can run
+    (QUADS §3.2 Eq. 13)."""
 
     def __init__(self, w13, w_down, topk, max_tokens, fake=True, sym=False, train=False):
         assert fake or not sym
@@ -317,10 +317,10 @@ class QatMoE:
             # first so that the amax of QDQ_A(h) sees the routed rows only
             with torch.cuda.stream(stream or torch.cuda.current_stream()):
                 self.h[:cap].zero_()
-        if self.train:  # keep the pre-activations for the backward
-            nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.gu,
-                                    out_dtype=NVFP4_OUT_BF16, dev_status=self.dev_status, stream=stream)
-            nvfp4_swiglu(self.gu, self.h, stream=stream)
+        if self.train:  # the same h, and the BF16 pre-activations kept for the backward
+            nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.h,
+                                    out_dtype=NVFP4_OUT_BF16, epilogue=NVFP4_EPI_SWIGLU_SAVE, gu=self.gu,
+                                    dev_status=self.dev_status, stream=stream)
         else:
             nvfp4_bf16_grouped_gemm(self.xr, self.w13_hat, r.offsets, self.E, 2 * self.I, self.H, self.h,
                                     out_dtype=NVFP4_OUT_BF16, epilogue=NVFP4_EPI_SWIGLU,

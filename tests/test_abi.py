@@ -174,6 +174,15 @@ def test_empty_batch_buffers_may_be_null(lib):
     assert lib.nvfp4_moe_combine(P, 1, 64, None, None, 3, 4, 64, None, None) == INVALID
 
 
+def test_bf16_gemm_pre_activation_buffer(lib):
+    b = lib.nvfp4_bf16_grouped_gemm
+    # x, w_hat, offsets, E, rows_cap, N, K, out_dtype, epilogue, y, ldy, gu, status, stream
+    assert b(P, P, P, 1, 128, 256, 64, 1, nv.NVFP4_EPI_SWIGLU_SAVE, P, 128, None, None, None) == INVALID  # no gu
+    assert b(P, P, P, 1, 128, 256, 64, 1, nv.NVFP4_EPI_SWIGLU, P, 128, P, None, None) == INVALID  # gu unused
+    assert b(P, P, P, 1, 128, 256, 64, 0, nv.NVFP4_EPI_SWIGLU_SAVE, P, 128, P, None, None) == INVALID  # F32 out
+    assert b(P, P, P, 1, 128, 256, 64, 1, nv.NVFP4_EPI_SWIGLU_SAVE, P, 128, PM, None, None) == ALIGN
+
+
 def test_gemm_pipeline_selector(lib):
     prev = ctypes.c_int32(-1)
     assert lib.nvfp4_gemm_pipeline(7, None) == INVALID

@@ -299,6 +299,40 @@ def test_swiglu_epilogue_and_fused_amax():
     assert hmax.item() == np.abs(got).max()
 
 
+@pytest.mark.parametrize("pipe", [1, 2])
+def test_bf16_swiglu_epilogue_that_keeps_the_pre_activations(pipe):
+    """NVFP4_EPI_SWIGLU_SAVE: its h equals the NVFP4_EPI_SWIGLU output and its
+    pre-activations the BF16 NVFP4_EPI_NONE output, bit for bit, on both GEMM
+    pipelines, over ragged and empty experts and two 256-column tiles."""
+    E, N, K = 3, 512, 192
+    counts = np.array([50, 0, 300])
+    offsets = np.concatenate([[0], np.cumsum((counts + 127) // 128 * 128)]).astype(np.int32)
+    rows = int(offsets[-1])
+    rng = np.random.default_rng(16)
+    xr = np.zeros((rows, K), np.float32)
+    for e in range(E):
+        xr[offsets[e]:offsets[e] + counts[e]] = rng.standard_normal((counts[e], K))
+    x = G.bf16_from_u16(oracle.bf16_round(xr))
+    w = G.bf16_from_u16(oracle.bf16_round((rng.standard_normal((E, N, K)) * 0.05).astype(np.float32)))
+    offs = torch.tensor(offsets, device=G.DEV)
+    st = G.zeros(1, torch.int32)
+    h_ref = G.zeros((rows, N // 2), torch.bfloat16)
+    gu_ref = G.zeros((rows, N), torch.bfloat16)
+    h = torch.full((rows, N // 2), 7.0, dtype=torch.bfloat16, device=G.DEV)
+    gu = torch.full((rows, N), 7.0, dtype=torch.bfloat16, device=G.DEV)
+    prev = nv.nvfp4_gemm_pipeline(pipe)
+    try:
+        nv.nvfp4_bf16_grouped_gemm(x, w, offs, E, N, K, h_ref, out_dtype=1, epilogue=nv.NVFP4_EPI_SWIGLU, dev_status=st)
+        nv.nvfp4_bf16_grouped_gemm(x, w, offs, E, N, K, gu_ref, out_dtype=1, dev_status=st)
+        nv.nvfp4_bf16_grouped_gemm(x, w, offs, E, N, K, h, out_dtype=1, epilogue=nv.NVFP4_EPI_SWIGLU_SAVE, gu=gu,
+                                   dev_status=st)
+        torch.cuda.synchronize()
+    finally:
+        nv.nvfp4_gemm_pipeline(prev)
+    G.status_ok(st)
+    assert torch.equal(h, h_ref) and torch.equal(gu, gu_ref)
+
+
 @pytest.mark.parametrize("swiglu", [False, True])
 def test_bf16_grouped_gemm_parity(swiglu):
     E, N, K = 3, 256, 192
