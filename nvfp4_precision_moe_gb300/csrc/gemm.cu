@@ -220,7 +220,7 @@ int wgrad_gemm(const void *a, const void *b, bool rows_major, const int32_t *off
         }
         return NVFP4_OK;
     }
-    CUtensorMap tA, tB, tY;
+    CUtensorMap tA, tB;
     int s;
     if (rows_major) {  // boxes of 64 columns x 64 rows
         s = encode_tmap_2d(&tA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)a, M, R, 2 * M, 64, 64,
@@ -235,15 +235,10 @@ int wgrad_gemm(const void *a, const void *b, bool rows_major, const int32_t *off
             s = encode_tmap_2d(&tB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (void *)b, R, N, 2 * R, 64, 128,
                                CU_TENSOR_MAP_SWIZZLE_128B);
     }
-    // FP32 gradients leave through TMA stores: boxes of 16 rows x 32 columns (128 bytes), 128-byte swizzle
-    const bool tma_out = out_dtype == NVFP4_OUT_F32;
-    if (s == NVFP4_OK && tma_out)
-        s = encode_tmap_2d(&tY, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, dw, N, (uint64_t)E * M, 4 * N, 32, 16,
-                           CU_TENSOR_MAP_SWIZZLE_128B);
     if (s != NVFP4_OK) return s;
     GemmParams p{};
     p.wgrad = 1;
-    p.wgrad_tma = tma_out ? 1 : 0;
+    p.wgrad_f32 = out_dtype == NVFP4_OUT_F32 ? 1 : 0;
     p.a_mn = rows_major ? 1 : 0;
     p.b_mn = rows_major ? 1 : 0;
     p.M = M;
@@ -259,7 +254,7 @@ int wgrad_gemm(const void *a, const void *b, bool rows_major, const int32_t *off
     p.vec32 = (reinterpret_cast<uintptr_t>(dw) % 32 == 0) && (N * (out_dtype == NVFP4_OUT_F32 ? 4 : 2)) % 32 == 0;
     p.dev_status = dev_status;
     // the weight-gradient mode exists on the single-CTA pipeline only
-    return launch_single_gemm<false>(tA, tB, tma_out ? tY : tA, tB, p, (int64_t)E * M, N, (cudaStream_t)stream);
+    return launch_single_gemm<false>(tA, tB, tA, tB, p, (int64_t)E * M, N, (cudaStream_t)stream);
 }
 }  // namespace
 

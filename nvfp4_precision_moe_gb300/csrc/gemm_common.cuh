@@ -70,7 +70,7 @@ struct GemmParams {
     // seg e = [offsets[e], offsets[e+1])
     int32_t wgrad;
     int64_t M;
-    int32_t wgrad_tma;  // FP32 weight gradients stored through shared memory by TMA (the map in tmR)
+    int32_t wgrad_f32;  // FP32 weight gradients: rows staged through shared memory, stored 128 bytes at a time
     // BF16 operands stored MN-major (the M or N index contiguous): A (weight-gradient mode) and B
     // (both modes) arrive as TMA boxes of 64 MN-elements x 64 K-rows, 8 KB apart (desc_sw128_mn)
     int32_t a_mn, b_mn;

@@ -39,7 +39,7 @@ constexpr uint32_t kIdescBF16 = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3)
 template <bool FP4>
 struct Cfg {
     static constexpr int kStageBytes = kATileBytes + kBTileBytes + (FP4 ? kSFABytes + kSFBBytes : 0);
-    // BF16 only: one 2 KB store-staging box (16 rows x 128 bytes, 128-byte swizzle) per epilogue warp
+    // BF16 only: one 2 KB store-staging box (16 rows x 128 bytes, chunks swizzled by row) per epilogue warp
     static constexpr int kOutOffset = kStages * kStageBytes;
     static constexpr int kOutBytes = FP4 ? 0 : kEpiWarps * 2048;
     static constexpr int kBarOffset = kOutOffset + kOutBytes;
@@ -50,7 +50,6 @@ struct Cfg {
     static constexpr int kSmemBytes = 1024 + kGswOffset + kMaxExperts * 4;
 };
 static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<false>::kSmemBytes <= 232448, "shared memory budget");
-static_assert(Cfg<false>::kOutOffset % 1024 == 0, "store staging boxes sit on 1024-byte swizzle atoms");
 
 // A tile of the weight-gradient mode: expert e, output tile (mt, nt), and the
 // expert's routed rows [k0, k0 + 64 nk) as the reduction range.
@@ -429,12 +428,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 128; ++i) v[i] = 0u;
                 }
                 const int64_t col = (int64_t)w.nt * kBN + 128 * half;
-                if (!FP4 && p.wgrad_tma) {
-                    // FP32 rows through this warp's staging box: rows 0-15 of the warp, then 16-31,
-                    // 32 columns at a time, written in the 128-byte swizzle (16-byte chunk c of
-                    // row r at chunk c ^ r%8) and stored by one TMA store each
+                if (!FP4 && p.wgrad_f32) {
+                    // FP32 rows through this warp's box (16 rows x 32 columns, 16-byte chunk c of
+                    // row r at chunk c ^ r%8), read back 8 lanes to a row and stored as whole
+                    // 128-byte row pieces by plain stores: nothing waits on the stores
                     const uint32_t box = smem_u32(smem + C::kOutOffset + ew * 2048);
-                    const int32_t row0 = (int32_t)((int64_t)w.e * p.M + (int64_t)w.mt * kBM + q * 32);
+                    float *ybase = reinterpret_cast<float *>(p.y) +
+                                   ((int64_t)w.e * p.M + (int64_t)w.mt * kBM + q * 32) * p.ldy + col;
                     const int r = lane & 15;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -443,18 +443,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if ((lane >> 4) == hh) {
 #pragma unroll
                                 for (int c = 0; c < 8; ++c)
-                                    st_shared_v4(box + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4)),
-                                                 v[32 * j + 4 * c], v[32 * j + 4 * c + 1], v[32 * j + 4 * c + 2],
-                                                 v[32 * j + 4 * c + 3]);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) {
-                                tma_store_2d(&tmR, box, (int32_t)col + 32 * j, row0 + 16 * hh);
-                                bulk_commit();
-                                bulk_wait_read();  // the box may be rewritten
+                                    st_shared_v4(box + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)), v[32 * j + 4 * c],
+                                                 v[32 * j + 4 * c + 1], v[32 * j + 4 * c + 2], v[32 * j + 4 * c + 3]);
                             }
                             __syncwarp();
+#pragma unroll
+                            for (int t = 0; t < 4; ++t) {
+                                const int rr = (32 * t + lane) >> 3, cc = lane & 7;
+                                const uint4 val = ld_shared_v4(box + (uint32_t)(rr * 128 + ((cc ^ (rr & 7)) << 4)));
+                                *reinterpret_cast<uint4 *>(ybase + (int64_t)(16 * hh + rr) * p.ldy + 32 * j + 4 * cc) =
+                                    val;
+                            }
+                            __syncwarp();  // the box is read out before it is rewritten
                         }
                     }
                     continue;
@@ -490,7 +490,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 8; ++j) store16(p, row, col + 16 * j, gmul, v + 16 * j, amax_local);
             }
         }
-        if (!FP4 && wgrad && p.wgrad_tma && lane == 0) bulk_wait_all();  // this warp's TMA stores are done
         if (p.amax_out) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) amax_local = fmaxf(amax_local, __shfl_xor_sync(0xffffffffu, amax_local, o));
