@@ -845,8 +845,9 @@ def run_profile_case(args):
     (QAT gate_up, BF16, same shape as gemm13), `wgrad` (the training step's dW_13 at the QAT
     shapes for 16 experts x 256 rows, FP32 output, transposed operands), `wgrad_rows` (the same
     from the routed rows as stored), `dgrad` (the input gradient with W13_hat as stored),
-    `fake_quant` / `fake_quant_down` (the QAT workload's W13 / down weights).  Runs `--steps`
-    launches."""
+    `fake_quant` / `fake_quant_down` (the QAT workload's W13 / down weights), `train_step` (the
+    QAT workload's training step: the forward keeping the pre-activations, then the backward; a
+    dozen launches, for a launch list).  Runs the case `--steps` times."""
     import torch
 
     import nvfp4_precision_moe_gb300 as nv
@@ -1002,6 +1003,19 @@ def run_profile_case(args):
         del layer
         fn = lambda: lay.forward(x, logits)
         flops = 0
+    elif case == "train_step":
+        c, w13, wd, x, logits = build_qat_workload(dev)
+        tl = nv.QatMoE(w13, wd, c["topk"], c["T"], train=True)
+        dout = torch.randn((c["T"], c["H"]), device=dev, generator=g)
+
+        def fn():
+            tl.forward(x, logits)
+            tl.backward(dout)
+
+        flops = 0
+        # launches from here on form the profiler range (ncu --profile-from-start off)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.start()
     elif case == "combine":
         T, topk, H = 16384, 8, 4096
         rows = T * topk
@@ -1023,6 +1037,8 @@ def run_profile_case(args):
     t1.record()
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / args.steps
+    if case == "train_step":
+        torch.cuda.profiler.stop()
     print(json.dumps({"profile_case": case, "ms": round(ms, 4),
                       "tflops": round(flops / ms / 1e9, 1) if flops else None}))
 
