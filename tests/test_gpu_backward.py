@@ -135,11 +135,13 @@ def test_grouped_weight_gradient(nv, out_dtype):
     assert G.rel_err(got, ref) <= tol
 
 
+@pytest.mark.parametrize("M,N", [(384, 512), (128, 256), (256, 768)])
 @pytest.mark.parametrize("out_dtype", [0, 1])
-def test_grouped_weight_gradient_from_rows(nv, out_dtype):
+def test_grouped_weight_gradient_from_rows(nv, out_dtype, M, N):
     """The same weight gradient with both operands read as the routed rows
-    themselves (MN-major tiles: no transposes)."""
-    T, E, topk, M, N = 200, 5, 2, 384, 512
+    themselves (MN-major tiles: no transposes); one output tile per expert
+    and an odd number of 256-column tiles included."""
+    T, E, topk = 200, 5, 2
     _, _, counts, offs, dst = _routing(nv, T, E, topk, 21, empty=1)
     assert counts[1] == 0
     R = int(offs[-1]) + 128
